@@ -1,0 +1,552 @@
+"""JoLT encode/decode written out plainly in float64 (the oracle).
+
+Test infrastructure only: imported by tests/, by __graft_entry__.smoke() and
+by bench.py's CPU-baseline leg.  The CUDA library never calls it.
+
+Sources (web pages on arXiv:2607.12550, cited by title and section):
+  [P1] "Joint Tucker-rank and residual-bit KV allocator" (synthcore idea 813):
+       Formulas; Mathematical statement; Implementation notes.
+  [P2] "A JoLT for the KV cache: Near-lossless KV cache compression via joint
+       Lagrangian allocation of Tucker ranks and a rotated residual" (abstract).
+  [P3] pith.science verdict on 2607.12550: key_machinery; referee report.
+  [P4] "Rotated Tucker residual for outlier-resistant KV quantization"
+       (synthcore idea 814): Mathematical statement; Key formulas;
+       Implementation notes.
+  [P5] "Technical Summary: A JOLT for the KV Cache" (gist.science):
+       Methodology 1-4.
+
+Notation: one unit is a group tensor X[H, T, D] (heads of the layer group,
+tokens, features) of one cache type.  Ranks r_T (token) and r_d (feature),
+residual bits b.  FULL (= -1) in a grid means "mode kept untruncated".
+
+Readings taken where the pages are silent (each is listed with its reason in
+the repository's design notes):
+  * ST-HOSVD mode order: feature mode first, then the token mode of the
+    feature-projected tensor.
+  * An untruncated mode has the identity as its factor.
+  * Factors U_T, U_d and the core G are stored in fp16; the reconstruction
+    that is scored is built from the stored (rounded) values.
+  * Q = H_D diag(sigma) / sqrt(D), H_D the Sylvester-order Hadamard matrix,
+    applied to each (h, t) row of the residual; one quantization block is one
+    such row (block = D).
+  * The block scale is stored as fp16 and quantization divides by the stored
+    scale; round() is round-half-to-even; a zero scale gives zero codes.
+  * Cost: the printed formula with alignment padding (see cost_table).
+  * Allocation: bisection on lambda as described in allocate().
+"""
+from __future__ import annotations
+
+import dataclasses
+import struct
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from .jacobi import jacobi_eigh
+
+FULL = -1
+BITS = (0, 2, 4, 8)
+HEADER_BYTES = 256
+MAGIC = 0x544C4F4A  # "JOLT" little-endian
+VERSION = 1
+
+
+# --------------------------------------------------------------------------
+# small helpers
+# --------------------------------------------------------------------------
+def f16(a: np.ndarray) -> np.ndarray:
+    """Round to fp16 (IEEE round-to-nearest-even) and return float64."""
+    return np.asarray(a, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def resolve(r: int, full: int) -> int:
+    return full if r == FULL or r >= full else r
+
+
+def align_up(x: int, a: int) -> int:
+    return (x + a - 1) // a * a
+
+
+# --------------------------------------------------------------------------
+# rotation  [P4 Mathematical statement, Implementation notes; P1 Formulas]
+# --------------------------------------------------------------------------
+def sylvester_hadamard(D: int) -> np.ndarray:
+    """H_1 = [1]; H_2n = [[H_n, H_n], [H_n, -H_n]]  (entries +-1)."""
+    if D < 1 or D & (D - 1):
+        raise ValueError("D must be a power of two")
+    Hm = np.ones((1, 1))
+    while Hm.shape[0] < D:
+        Hm = np.block([[Hm, Hm], [Hm, -Hm]])
+    return Hm
+
+
+def rotation_matrix(signs: np.ndarray) -> np.ndarray:
+    """Q = H_D diag(sigma) / sqrt(D): "a normalized Hadamard transform" with
+    random signs, orthogonal (Q^T Q = I) [P4 Implementation notes]."""
+    D = signs.shape[0]
+    return sylvester_hadamard(D) * np.asarray(signs, dtype=np.float64)[None, :] / np.sqrt(D)
+
+
+# --------------------------------------------------------------------------
+# Cholesky / CholeskyQR2 (Fukaya et al. 2014), for the randomized token mode
+# --------------------------------------------------------------------------
+def cholesky_lower(G: np.ndarray) -> np.ndarray:
+    """Cholesky–Banachiewicz: G = L L^T, L lower triangular."""
+    n = G.shape[0]
+    L = np.zeros_like(G, dtype=np.float64)
+    for j in range(n):
+        d = G[j, j] - np.dot(L[j, :j], L[j, :j])
+        if d <= 0.0:
+            raise np.linalg.LinAlgError("matrix not positive definite")
+        L[j, j] = np.sqrt(d)
+        L[j + 1:, j] = (G[j + 1:, j] - L[j + 1:, :j] @ L[j, :j]) / L[j, j]
+    return L
+
+
+def solve_upper_right(Z: np.ndarray, R: np.ndarray) -> np.ndarray:
+    """Z R^{-1} for upper-triangular R, by back substitution over columns."""
+    n = R.shape[0]
+    Qm = np.zeros_like(Z, dtype=np.float64)
+    for j in range(n):
+        Qm[:, j] = (Z[:, j] - Qm[:, :j] @ R[:j, j]) / R[j, j]
+    return Qm
+
+
+def cholesky_qr(Z: np.ndarray) -> np.ndarray:
+    R = cholesky_lower(Z.T @ Z).T
+    return solve_upper_right(Z, R)
+
+
+def cholesky_qr2(Z: np.ndarray) -> np.ndarray:
+    """CholeskyQR applied twice; returns the orthonormal factor."""
+    return cholesky_qr(cholesky_qr(Z))
+
+
+# --------------------------------------------------------------------------
+# partial Tucker by ST-HOSVD over the feature and token modes
+#   [P1 Mathematical statement, Implementation notes; P3 key_machinery;
+#    P5 Methodology 1 and 4]
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class Factors:
+    """Factors of one unit for every feature rank of the grid.
+
+    rd_list / rT_list hold resolved ranks (FULL replaced by D or T).
+    For each r_d (key = resolved r_d):
+      Ud[r_d]  : D x r_d  (identity when r_d == D)
+      UT[r_d]  : T x rT_max leading eigenvectors of the token Gram of the
+                 projected tensor (descending), rT_max = largest truncated r_T
+      G[r_d]   : H x rT_max x r_d core for the truncated r_T (nested slices)
+      Y[r_d]   : H x T x r_d projected tensor (the core when r_T == T)
+    *_16 are the fp16-rounded stored values.
+    """
+    H: int
+    T: int
+    D: int
+    rT_list: List[int]
+    rd_list: List[int]
+    rT_max: int
+    feat_eigvals: np.ndarray
+    Ud: Dict[int, np.ndarray]
+    UT: Dict[int, np.ndarray]
+    G: Dict[int, np.ndarray]
+    Y: Dict[int, np.ndarray]
+    tok_eigvals: Dict[int, np.ndarray]
+
+    def stored(self, rT: int, rd: int):
+        """fp16 (U_T, G, U_d) stored for candidate (rT, rd) (resolved
+        ranks); U_T or U_d is None when that mode is kept whole."""
+        H, T, D = self.H, self.T, self.D
+        Ud = None if rd == D else f16(self.Ud[rd])
+        if rT == T:
+            return None, f16(self.Y[rd]), Ud
+        return f16(self.UT[rd][:, :rT]), f16(self.G[rd][:, :rT, :]), Ud
+
+
+def feature_mode(X: np.ndarray):
+    """S_d = X_(d) X_(d)^T summed over all (h, t) rows; eigenvectors in
+    descending eigenvalue order."""
+    H, T, D = X.shape
+    rows = X.reshape(H * T, D)
+    S = rows.T @ rows
+    w, V, _ = jacobi_eigh(S)
+    return w, V
+
+
+def token_unfolding(Y: np.ndarray) -> np.ndarray:
+    """A = Y_(T): T x (H * r) with column index h * r + j."""
+    H, T, r = Y.shape
+    return Y.transpose(1, 0, 2).reshape(T, H * r)
+
+
+def token_mode_exact(Y: np.ndarray, k: int):
+    """Top-k eigenvectors of S_T = A A^T, A = Y_(T).
+
+    Jacobi runs on the smaller of S_T (T x T) and the dual A^T A, the latter
+    mapped back by U = A V diag(1/sqrt(w)); the dual is used only when it has
+    at least k columns, so that k eigenvectors come out of it."""
+    A = token_unfolding(Y)
+    T, K = A.shape
+    if K < T and K >= k:
+        w, V, _ = jacobi_eigh(A.T @ A)
+        w, V = w[:k], V[:, :k]
+        if np.all(w > 0.0):
+            return w, (A @ V) / np.sqrt(w)[None, :]
+    w, U, _ = jacobi_eigh(A @ A.T)
+    return w[:k], U[:, :k]
+
+
+def token_mode_randomized(Y: np.ndarray, omega: np.ndarray, k: int, q: int):
+    """FlashJoLT randomized token mode [P5 Methodology 4; P2]: range finder
+    with a Gaussian test matrix (k + oversampling columns), q power steps with
+    CholeskyQR2 re-orthonormalisation, then Rayleigh-Ritz.
+
+    omega: (H, r_d, ell) slice of the unit's sketch (ell = k + p)."""
+    A = token_unfolding(Y)
+    if not np.any(A):
+        # an all-zero unit: every orthonormal U_T reconstructs X~ = 0
+        return np.zeros(k), np.eye(A.shape[0])[:, :k]
+    Om = omega.reshape(-1, omega.shape[-1]).astype(np.float64)  # row h*r+j
+    Qm = cholesky_qr2(A @ Om)
+    for _ in range(q):
+        Qm = cholesky_qr2(A @ (A.T @ Qm))
+    B = Qm.T @ A
+    w, W, _ = jacobi_eigh(B @ B.T)
+    return w[:k], Qm @ W[:, :k]
+
+
+def factorize(X: np.ndarray, rT_grid: Sequence[int], rd_grid: Sequence[int],
+              token_mode: str = "exact", sketch: Optional[np.ndarray] = None,
+              power_iters: int = 2) -> Factors:
+    """ST-HOSVD over the feature then token mode, for every r_d of the grid."""
+    X = np.asarray(X, dtype=np.float64)
+    H, T, D = X.shape
+    rT_list = [resolve(r, T) for r in rT_grid]
+    rd_list = [resolve(r, D) for r in rd_grid]
+    trunc_T = [r for r in rT_list if r < T]
+    rT_max = max(trunc_T) if trunc_T else 0
+    fw, FV = feature_mode(X)
+    Ud, UT, G, Y, tw = {}, {}, {}, {}, {}
+    for rd in rd_list:
+        Ud[rd] = np.eye(D) if rd == D else FV[:, :rd]
+        Yr = X if rd == D else np.einsum("htd,dj->htj", X, Ud[rd])
+        Y[rd] = Yr
+        if rT_max == 0:
+            UT[rd] = np.zeros((T, 0))
+            G[rd] = np.zeros((H, 0, rd))
+            tw[rd] = np.zeros(0)
+            continue
+        if token_mode == "exact":
+            w, U = token_mode_exact(Yr, rT_max)
+        elif token_mode == "randomized":
+            if sketch is None:
+                raise ValueError("randomized token mode needs the sketch")
+            w, U = token_mode_randomized(Yr, sketch[:, :rd, :], rT_max, power_iters)
+        else:
+            raise ValueError(token_mode)
+        UT[rd] = U
+        tw[rd] = w
+        G[rd] = np.einsum("tr,htj->hrj", U, Yr)
+    return Factors(H, T, D, rT_list, rd_list, rT_max, fw, Ud, UT, G, Y, tw)
+
+
+def reconstruct(UT16: Optional[np.ndarray], G16: np.ndarray,
+                Ud16: Optional[np.ndarray]) -> np.ndarray:
+    """X~ = G x_2 U_T x_3 U_d [P1 Formulas]; None stands for the identity."""
+    Xt = G16 if UT16 is None else np.einsum("tr,hrj->htj", UT16, G16)
+    return Xt if Ud16 is None else np.einsum("htj,dj->htd", Xt, Ud16)
+
+
+# --------------------------------------------------------------------------
+# quantizer  [P4 Mathematical statement, Key formulas, Implementation notes]
+# --------------------------------------------------------------------------
+def quantize_blocks(Yrot: np.ndarray, b: int):
+    """Symmetric per-block absmax quantizer on rows of Yrot (one block per
+    row): s = max|y| / (2^(b-1) - 1) stored as fp16, codes
+    clip(round(y / s), -2^(b-1), 2^(b-1) - 1).  Returns (codes int64, s)."""
+    qmax = 2 ** (b - 1) - 1
+    m = np.max(np.abs(Yrot), axis=1)
+    s = f16(m / qmax)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(s[:, None] > 0.0, np.rint(Yrot / s[:, None]), 0.0)
+    q = np.clip(q, -(2 ** (b - 1)), 2 ** (b - 1) - 1)
+    return q.astype(np.int64), s
+
+
+def dequantize_blocks(codes: np.ndarray, s: np.ndarray) -> np.ndarray:
+    return codes.astype(np.float64) * s[:, None]
+
+
+# --------------------------------------------------------------------------
+# distortion of one candidate  [P1 Formulas; P4 Key formulas]
+# --------------------------------------------------------------------------
+def decode_residual(Q: np.ndarray, codes: np.ndarray, s: np.ndarray,
+                    shape) -> np.ndarray:
+    """Q^T Q_b(QR), row by row."""
+    return (dequantize_blocks(codes, s) @ Q).reshape(shape)
+
+
+def candidate_xhat(X: np.ndarray, Xt: np.ndarray, Q: np.ndarray, b: int):
+    """X^ = X~ + Q^T Q_b(Q R), R = X - X~; b = 0 gives X^ = X~."""
+    if b == 0:
+        return Xt
+    H, T, D = X.shape
+    R = (X - Xt).reshape(H * T, D)
+    Yrot = R @ Q.T                      # each row r -> Q r
+    codes, s = quantize_blocks(Yrot, b)
+    return Xt + decode_residual(Q, codes, s, X.shape)
+
+
+def distortion(X: np.ndarray, Xhat: np.ndarray) -> float:
+    """D = ||X - X^||_F^2 / ||X||_F^2, taken as 0 for an all-zero X."""
+    nx = float(np.sum(X * X))
+    if nx == 0.0:
+        return 0.0
+    return float(np.sum((X - Xhat) ** 2)) / nx
+
+
+def dist_table(X: np.ndarray, fac: Factors, signs: np.ndarray,
+               bits: Sequence[int] = BITS,
+               cells: Optional[Sequence[Tuple[int, int]]] = None) -> np.ndarray:
+    """dist[iT][id][ib] over the whole (r_T, r_d, b) grid, each entry computed
+    literally in the original domain with an explicit Q^T.  `cells` limits
+    the work to the listed (iT, id) pairs (others are NaN)."""
+    X = np.asarray(X, dtype=np.float64)
+    Q = rotation_matrix(signs)
+    nT, nd = len(fac.rT_list), len(fac.rd_list)
+    out = np.full((nT, nd, len(bits)), np.nan)
+    todo = cells if cells is not None else [(i, j) for i in range(nT) for j in range(nd)]
+    for iT, idd in todo:
+        rT, rd = fac.rT_list[iT], fac.rd_list[idd]
+        Xt = reconstruct(*fac.stored(rT, rd))
+        for ib, b in enumerate(bits):
+            out[iT, idd, ib] = distortion(X, candidate_xhat(X, Xt, Q, b))
+    return out
+
+
+# --------------------------------------------------------------------------
+# byte cost  [P1 Formulas; Implementation notes ("actual storage")]
+# --------------------------------------------------------------------------
+def blob_layout(H: int, T: int, D: int, rT: int, rd: int, b: int, block: int,
+                align: int = 256) -> Dict[str, int]:
+    """Byte offsets of the serialized candidate: 256-byte header, then U_T
+    (fp16 T x r_T, omitted when r_T = T), U_d (fp16 D x r_d, omitted when
+    r_d = D), G (fp16 H x r_T x r_d), scales (fp16, one per block) and
+    b-bit codes, each section starting on an `align` boundary."""
+    off = HEADER_BYTES
+    lay = {}
+    n = H * T * D
+
+    def sect(name, nbytes):
+        nonlocal off
+        off = align_up(off, align)
+        lay[name] = off if nbytes > 0 else 0
+        lay[name + "_bytes"] = nbytes
+        off += nbytes
+
+    sect("UT", 0 if rT == T else 2 * T * rT)
+    sect("Ud", 0 if rd == D else 2 * D * rd)
+    sect("G", 2 * H * rT * rd)
+    sect("scale", 0 if b == 0 else 2 * (n // block))
+    sect("codes", 0 if b == 0 else n * b // 8)
+    lay["bytes"] = align_up(off, align)
+    return lay
+
+
+def cost_formula(H: int, T: int, D: int, rT: int, rd: int, b: int, block: int,
+                 align: int = 256, s: int = 2) -> int:
+    """C = s H (r_T T + r_d r_T + r_d D) + (b/8) H T D + metadata, with each
+    term padded to `align` bytes; metadata = fp16 block scales plus a
+    256-byte header [P1 Formulas, Implementation notes]."""
+    n = H * T * D
+    c = align_up(s * H * (rT * T + rd * rT + rd * D), align)
+    if b > 0:
+        c += align_up(b * n // 8, align) + align_up(2 * n // block, align)
+    return c + HEADER_BYTES
+
+
+def cost_table(H: int, T: int, D: int, rT_list, rd_list, bits, block: int,
+               model: str = "formula", align: int = 256) -> np.ndarray:
+    out = np.zeros((len(rT_list), len(rd_list), len(bits)), dtype=np.int64)
+    for i, rT in enumerate(rT_list):
+        for j, rd in enumerate(rd_list):
+            for k, b in enumerate(bits):
+                if model == "formula":
+                    out[i, j, k] = cost_formula(H, T, D, rT, rd, b, block, align)
+                else:
+                    out[i, j, k] = blob_layout(H, T, D, rT, rd, b, block, align)["bytes"]
+    return out
+
+
+# --------------------------------------------------------------------------
+# Lagrangian allocation  [P1 Formulas, Mathematical statement,
+#                         Implementation notes; P5 Methodology 3]
+# --------------------------------------------------------------------------
+ALLOC_OK, ALLOC_INFEASIBLE = 0, 2
+
+
+def best_response(dist: np.ndarray, cost: np.ndarray, lam: float) -> np.ndarray:
+    """z*(lambda) per unit: argmin of dist + lambda * C (the product rounded
+    before the sum); ties to the smaller C, then the lower candidate index."""
+    U, Cn = dist.shape
+    val = dist + lam * cost.astype(np.float64)
+    choice = np.zeros(U, dtype=np.int64)
+    for u in range(U):
+        order = np.lexsort((np.arange(Cn), cost[u], val[u]))
+        choice[u] = order[0]
+    return choice
+
+
+def min_cost_choice(dist: np.ndarray, cost: np.ndarray) -> np.ndarray:
+    U, Cn = dist.shape
+    return np.array([np.lexsort((np.arange(Cn), dist[u], cost[u]))[0] for u in range(U)])
+
+
+def total_cost(cost: np.ndarray, choice: np.ndarray) -> int:
+    return int(sum(int(cost[u, c]) for u, c in enumerate(choice)))
+
+
+def allocate(dist: np.ndarray, cost: np.ndarray, budget: int, align: int = 256,
+             max_iter: int = 200):
+    """Bisection on the byte price lambda.
+
+    dist, cost: [units][candidates].  Returns (choice, lambda, status).
+      1. z(0) feasible -> return it with lambda = 0.
+      2. the min-cost allocation infeasible -> return it, status INFEASIBLE.
+      3. hi = 1, doubled until z(hi) is feasible; lo = 0; bisect on
+         mid = (lo + hi) / 2 for up to max_iter steps, keeping z(hi)
+         feasible; stop once sum C(z(hi)) lies within one alignment block
+         of the budget, or hi - lo <= 2^-52 hi.  Return z(hi), hi.
+    """
+    dist = np.asarray(dist, dtype=np.float64)
+    cost = np.asarray(cost, dtype=np.int64)
+    z = best_response(dist, cost, 0.0)
+    if total_cost(cost, z) <= budget:
+        return z, 0.0, ALLOC_OK
+    zmin = min_cost_choice(dist, cost)
+    if total_cost(cost, zmin) > budget:
+        return zmin, float("inf"), ALLOC_INFEASIBLE
+    lo, hi = 0.0, 1.0
+    zhi = best_response(dist, cost, hi)
+    while total_cost(cost, zhi) > budget:
+        lo = hi
+        hi = hi * 2.0
+        zhi = best_response(dist, cost, hi)
+    for _ in range(max_iter):
+        c_hi = total_cost(cost, zhi)
+        if budget - align < c_hi <= budget or hi - lo <= 2.0 ** -52 * hi:
+            break
+        mid = 0.5 * (lo + hi)
+        zmid = best_response(dist, cost, mid)
+        if total_cost(cost, zmid) <= budget:
+            hi, zhi = mid, zmid
+        else:
+            lo = mid
+    return zhi, hi, ALLOC_OK
+
+
+# --------------------------------------------------------------------------
+# encode / decode of the chosen candidate  [P4 Implementation notes]
+# --------------------------------------------------------------------------
+def pack_codes(codes: np.ndarray, b: int) -> bytes:
+    """Offset-binary u = q + 2^(b-1), element k in bits [k b, (k+1) b) of a
+    little-endian bit stream (bit j = bit j%8 of byte j//8)."""
+    u = (codes.reshape(-1) + 2 ** (b - 1)).astype(np.uint64)
+    per = 8 // b
+    if u.size % per:
+        raise ValueError("code count not a whole number of bytes")
+    u = u.reshape(-1, per)
+    byte = np.zeros(u.shape[0], dtype=np.uint64)
+    for i in range(per):
+        byte |= u[:, i] << np.uint64(i * b)
+    return byte.astype(np.uint8).tobytes()
+
+
+def unpack_codes(buf: bytes, n: int, b: int) -> np.ndarray:
+    byte = np.frombuffer(buf, dtype=np.uint8).astype(np.int64)
+    per = 8 // b
+    mask = (1 << b) - 1
+    u = np.stack([(byte >> (i * b)) & mask for i in range(per)], axis=1).reshape(-1)
+    return u[:n] - 2 ** (b - 1)
+
+
+def sign_bits(signs: np.ndarray) -> bytes:
+    """Bit i set <=> sigma_i = -1, packed LSB-first."""
+    D = signs.shape[0]
+    out = bytearray((D + 7) // 8)
+    for i in range(D):
+        if signs[i] < 0:
+            out[i // 8] |= 1 << (i % 8)
+    return bytes(out)
+
+
+def encode_unit(X: np.ndarray, fac: Factors, signs: np.ndarray, rT: int, rd: int,
+                b: int, block: int, align: int = 256) -> bytes:
+    """Serialize candidate (rT, rd, b) of one unit (resolved ranks)."""
+    X = np.asarray(X, dtype=np.float64)
+    H, T, D = X.shape
+    if block != D:
+        raise ValueError("one quantization block is one row of D values")
+    lay = blob_layout(H, T, D, rT, rd, b, block, align)
+    buf = bytearray(lay["bytes"])
+    UT16, G16, Ud16 = fac.stored(rT, rd)
+    flags = (1 if UT16 is None else 0) | (2 if Ud16 is None else 0)
+    struct.pack_into("<IIiiiiiiiI", buf, 0, MAGIC, VERSION, H, T, D, rT, rd, b, block, flags)
+    struct.pack_into("<QQQQQQ", buf, 40, lay["UT"], lay["Ud"], lay["G"], lay["scale"],
+                     lay["codes"], lay["bytes"])
+    sb = sign_bits(signs)
+    buf[88:88 + len(sb)] = sb
+    if UT16 is not None:
+        buf[lay["UT"]:lay["UT"] + lay["UT_bytes"]] = UT16.astype(np.float16).tobytes()
+    if Ud16 is not None:
+        buf[lay["Ud"]:lay["Ud"] + lay["Ud_bytes"]] = Ud16.astype(np.float16).tobytes()
+    buf[lay["G"]:lay["G"] + lay["G_bytes"]] = G16.astype(np.float16).tobytes()
+    if b > 0:
+        Xt = reconstruct(UT16, G16, Ud16)
+        Q = rotation_matrix(signs)
+        codes, s = quantize_blocks((X - Xt).reshape(H * T, D) @ Q.T, b)
+        buf[lay["scale"]:lay["scale"] + lay["scale_bytes"]] = s.astype(np.float16).tobytes()
+        buf[lay["codes"]:lay["codes"] + lay["codes_bytes"]] = pack_codes(codes, b)
+    return bytes(buf)
+
+
+def parse_header(blob: bytes) -> Dict[str, int]:
+    magic, ver, H, T, D, rT, rd, b, block, flags = struct.unpack_from("<IIiiiiiiiI", blob, 0)
+    if magic != MAGIC or ver != VERSION:
+        raise ValueError("not a JoLT blob")
+    offs = struct.unpack_from("<QQQQQQ", blob, 40)
+    hd = dict(H=H, T=T, D=D, rT=rT, rd=rd, b=b, block=block, flags=flags)
+    hd.update(zip(("UT", "Ud", "G", "scale", "codes", "bytes"), offs))
+    bits = blob[88:88 + (D + 7) // 8]
+    hd["signs"] = np.array([-1 if (bits[i // 8] >> (i % 8)) & 1 else 1 for i in range(D)],
+                           dtype=np.int8)
+    return hd
+
+
+def decode_unit(blob: bytes) -> np.ndarray:
+    """X^ = X~ + Q^T deq(codes), float64."""
+    hd = parse_header(blob)
+    H, T, D, rT, rd, b = hd["H"], hd["T"], hd["D"], hd["rT"], hd["rd"], hd["b"]
+
+    def arr(off, n, shape):
+        return np.frombuffer(blob, dtype=np.float16, count=n, offset=off).astype(np.float64).reshape(shape)
+
+    UT16 = None if hd["flags"] & 1 else arr(hd["UT"], T * rT, (T, rT))
+    Ud16 = None if hd["flags"] & 2 else arr(hd["Ud"], D * rd, (D, rd))
+    G16 = arr(hd["G"], H * rT * rd, (H, rT, rd))
+    Xt = reconstruct(UT16, G16, Ud16)
+    if b == 0:
+        return Xt
+    n = H * T * D
+    s = arr(hd["scale"], n // hd["block"], (n // hd["block"],))
+    codes = unpack_codes(blob[hd["codes"]:hd["codes"] + n * b // 8], n, b).reshape(H * T, D)
+    return Xt + decode_residual(rotation_matrix(hd["signs"]), codes, s, (H, T, D))
+
+
+# --------------------------------------------------------------------------
+# whole encode pass over a set of units
+# --------------------------------------------------------------------------
+def candidate_list(rT_list, rd_list, bits=BITS):
+    """Flat candidate index -> (iT, id, ib), iT-major then id then ib."""
+    return [(i, j, k) for i in range(len(rT_list)) for j in range(len(rd_list))
+            for k in range(len(bits))]

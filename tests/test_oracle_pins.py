@@ -1,0 +1,363 @@
+"""Pins of the float64 oracle against facts fixed outside the oracle itself:
+closed forms, library routines, textbook invariants, hand-worked values and
+brute force.  CPU only.
+
+What pins which oracle function:
+  jacobi_eigh            numpy.linalg.eigh on random symmetric matrices;
+                         2x2 closed form; diagonal input; residual/orthogonality
+  sylvester_hadamard     closed form H[i, j] = (-1)^popcount(i & j)
+  rotation_matrix        Q^T Q = I and ||Q R|| = ||R||  [P4 Key formulas]
+  quantize_blocks        hand-worked golden rows; brute-force nearest level;
+                         MSE ratio per +2 bits near 16  [P1 Stage 1]
+  feature/token modes,   truncation error = sum of discarded eigenvalues
+  cores (factorize)      (single mode) and = ||X||^2 - ||G||^2 (two modes)
+  dist_table             full ranks + b = 0 -> ~0; b = 0 monotone in r_T, r_d
+  token_mode_randomized  many power steps -> exact subspace
+  cholesky_qr2           numpy.linalg.qr up to column signs
+  cost_formula           hand arithmetic; fp16 footprint 268.4 MB [P5 Efficiency]
+  blob_layout/codec      decode(encode) reproduces the scored candidate
+  allocate               hand cases; brute force over all tiny allocations
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+
+import kvgen
+from oracle import jolt, run
+from oracle.jacobi import jacobi_eigh, round_robin_rounds
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- Jacobi
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 16, 33, 64])
+def test_jacobi_matches_library_eigh(n):
+    rng = np.random.default_rng(n)
+    A = rng.standard_normal((n, n))
+    S = A + A.T
+    w, V, _ = jacobi_eigh(S)
+    ref = np.linalg.eigh(S)[0][::-1]
+    scale = max(1.0, np.abs(ref).max())
+    assert np.max(np.abs(w - ref)) <= 1e-12 * scale
+    assert np.max(np.abs(V.T @ V - np.eye(n))) <= 1e-12
+    assert np.max(np.abs(S @ V - V * w[None, :])) <= 1e-12 * scale
+
+
+def test_jacobi_2x2_closed_form():
+    a, b, c = 3.0, 1.5, -2.0
+    S = np.array([[a, b], [b, c]])
+    w, V, _ = jacobi_eigh(S)
+    mid, rad = (a + c) / 2, np.hypot((a - c) / 2, b)
+    assert np.allclose(w, [mid + rad, mid - rad], rtol=0, atol=1e-14)
+
+
+def test_jacobi_diagonal_and_psd_gram():
+    d = np.array([1.0, 5.0, 3.0, 3.0])
+    w, V, sweeps = jacobi_eigh(np.diag(d))
+    assert sweeps == 0 and list(w) == [5.0, 3.0, 3.0, 1.0]
+    # ties broken by original index: the two 3.0 eigenvectors are e_2, e_3
+    assert np.array_equal(np.abs(V[:, 1]), [0, 0, 1, 0])
+    rng = np.random.default_rng(5)
+    Z = rng.standard_normal((200, 20))
+    w, V, _ = jacobi_eigh(Z.T @ Z)
+    s = np.linalg.svd(Z, compute_uv=False)
+    assert np.allclose(w, s ** 2, rtol=1e-12)
+
+
+def test_round_robin_covers_every_pair_once():
+    for n in (2, 5, 8, 13):
+        seen = []
+        for p, q in round_robin_rounds(n):
+            assert len(set(p) | set(q)) == 2 * len(p)  # disjoint in a round
+            seen += [tuple(sorted((int(a), int(b)))) for a, b in zip(p, q)]
+        assert sorted(seen) == sorted(itertools.combinations(range(n), 2))
+
+
+# ---------------------------------------------------------------- rotation
+@pytest.mark.parametrize("D", [1, 2, 8, 32, 128])
+def test_hadamard_closed_form(D):
+    Hm = jolt.sylvester_hadamard(D)
+    i = np.arange(D)
+    pop = np.vectorize(lambda v: bin(int(v)).count("1"))(i[:, None] & i[None, :])
+    assert np.array_equal(Hm, (-1.0) ** pop)
+
+
+def test_rotation_orthogonal_and_norm_preserving():
+    rng = np.random.default_rng(0)
+    sig = np.where(rng.random(128) < 0.5, -1, 1).astype(np.int8)
+    Q = jolt.rotation_matrix(sig)
+    assert np.max(np.abs(Q.T @ Q - np.eye(128))) <= 1e-14
+    R = rng.standard_normal((500, 128)) * np.linspace(0.1, 10, 128)
+    assert abs(np.linalg.norm(R @ Q.T) / np.linalg.norm(R) - 1) <= 1e-13
+
+
+def test_rotation_spreads_outlier():
+    # a single outlier coordinate is spread to equal magnitude on all D
+    # coordinates: the Hadamard outlier-spreading the pages describe
+    sig = kvgen.make_signs(kvgen.WORKLOADS["mistral_t1024"], 0)
+    Q = jolt.rotation_matrix(sig)
+    e = np.zeros(128)
+    e[17] = 8.0
+    assert np.allclose(np.abs(Q @ e), 8.0 / np.sqrt(128), atol=1e-14)
+
+
+# ---------------------------------------------------------------- quantizer
+def _golden_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "quantizer_worked_example.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            b, y, s, q, packed = [p.strip() for p in line.split("|")]
+            rows.append((int(b), np.array(y.split(), float), float(s),
+                         np.array(q.split(), int), bytes(int(v) for v in packed.split())))
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rows())
+def test_quantizer_golden(row):
+    b, y, s_ref, q_ref, packed_ref = row
+    q, s = jolt.quantize_blocks(y[None, :], b)
+    assert s[0] == s_ref
+    assert np.array_equal(q[0], q_ref)
+    assert jolt.pack_codes(q[0], b) == packed_ref
+    assert np.array_equal(jolt.unpack_codes(packed_ref, y.size, b), q_ref)
+
+
+@pytest.mark.parametrize("b", [2, 4, 8])
+def test_quantizer_nearest_level_brute_force(b):
+    rng = np.random.default_rng(b)
+    Y = rng.standard_normal((300, 16)) * rng.lognormal(0, 2, (300, 1))
+    Y[0] = 0.0
+    q, s = jolt.quantize_blocks(Y, b)
+    levels = np.arange(-(2 ** (b - 1)), 2 ** (b - 1))
+    for i in range(Y.shape[0]):
+        if s[i] == 0:
+            assert not q[i].any()
+            continue
+        err = np.abs(Y[i][:, None] - s[i] * levels[None, :])
+        best = err.min(axis=1)
+        mine = np.abs(Y[i] - s[i] * q[i])
+        assert np.all(mine <= best + 1e-15 * np.abs(Y[i]).max())
+        assert np.all(np.abs(q[i]) <= 2 ** (b - 1) - 1)  # clip never binds
+
+
+def test_quantizer_mse_ratio_per_two_bits():
+    # [P1 Stage 1]: MSE falls by 16.25-25.65x per two added bits against a
+    # high-rate prediction of 16x; the ratio shrinks toward 16 as b grows
+    rng = np.random.default_rng(11)
+    Y = rng.standard_normal((20000, 128))
+    mse = {}
+    for b in (2, 4, 6, 8):
+        q, s = jolt.quantize_blocks(Y, b)
+        mse[b] = np.mean((Y - q * s[:, None]) ** 2)
+    r = [mse[2] / mse[4], mse[4] / mse[6], mse[6] / mse[8]]
+    assert 12 <= r[1] <= 32 and 12 <= r[2] <= 32
+    assert r[0] > r[1] > r[2]
+
+
+# ---------------------------------------------------------------- Tucker
+def _small_tensor(H=3, T=40, D=16, seed=3):
+    w = kvgen.custom_workload("tiny", H=H, T=T, D=D, cp_rank=6, noise=0.05,
+                              outliers=(2,), seed=seed)
+    return kvgen.make_unit_f64(w, 0), kvgen.make_unit_f64(w, 1)
+
+
+@pytest.mark.parametrize("rd", [2, 5, 16])
+def test_feature_truncation_error_is_discarded_eigenvalues(rd):
+    for X in _small_tensor():
+        w, V = jolt.feature_mode(X)
+        P = V[:, :rd] @ V[:, :rd].T
+        err = np.sum((X - np.einsum("htd,de->hte", X, P)) ** 2)
+        assert abs(err - w[rd:].sum()) <= 1e-10 * np.sum(X * X)
+
+
+@pytest.mark.parametrize("rT,rd", [(3, 16), (7, 4), (20, 9), (40, 3)])
+def test_two_mode_st_hosvd_error(rT, rd):
+    for X in _small_tensor():
+        H, T, D = X.shape
+        fac = jolt.factorize(X, [rT, jolt.FULL], [rd, jolt.FULL])
+        rdr = jolt.resolve(rd, D)
+        if rT < T:
+            UT, G = fac.UT[rdr][:, :rT], fac.G[rdr][:, :rT, :]
+        else:
+            UT, G = None, fac.Y[rdr]
+        Ud = None if rdr == D else fac.Ud[rdr]
+        Xt = jolt.reconstruct(UT, G, Ud)
+        err = np.sum((X - Xt) ** 2)
+        nx = np.sum(X * X)
+        feat_tail = fac.feat_eigvals[rdr:].sum()
+        if rT < T:
+            S_T = jolt.token_unfolding(fac.Y[rdr]) @ jolt.token_unfolding(fac.Y[rdr]).T
+            tok_tail = np.linalg.eigvalsh(S_T)[::-1][rT:].sum()
+        else:
+            tok_tail = 0.0
+        assert abs(err - (feat_tail + tok_tail)) <= 1e-10 * nx
+        assert abs(err - (nx - np.sum(G * G))) <= 1e-10 * nx
+
+
+def test_dual_and_direct_token_modes_agree():
+    X, _ = _small_tensor(H=2, T=30, D=8)
+    Y = np.einsum("htd,dj->htj", X, jolt.feature_mode(X)[1][:, :4])  # K = 8 < T
+    w1, U1 = jolt.token_mode_exact(Y, 6)
+    A = jolt.token_unfolding(Y)
+    w2, U2, _ = jacobi_eigh(A @ A.T)
+    assert np.allclose(w1, w2[:6], rtol=1e-12)
+    assert np.max(np.abs(U1 @ U1.T - U2[:, :6] @ U2[:, :6].T)) <= 1e-10
+
+
+def _tiny_tables():
+    w = kvgen.WORKLOADS["tiny"]
+    Xs = [kvgen.unit_values_f64(w, kvgen.make_unit(w, u)) for u in range(w.n_units)]
+    S = [kvgen.make_signs(w, u) for u in range(w.n_units)]
+    return w, Xs, S, run.encode_units(Xs, S, w.rT, w.rd, w.bits, w.block, w.budget_bytes)
+
+
+_TINY = {}
+
+
+def tiny():
+    if not _TINY:
+        _TINY["v"] = _tiny_tables()
+    return _TINY["v"]
+
+
+def test_full_ranks_b0_reproduce_x():
+    w, Xs, S, r = tiny()
+    assert np.all(r.dist[:, -1, -1, 0] <= 1e-6)
+
+
+def test_b0_distortion_monotone_in_ranks():
+    w, Xs, S, r = tiny()
+    d0 = r.dist[..., 0]
+    assert np.all(np.diff(d0, axis=1) <= 1e-7)  # in r_T
+    assert np.all(np.diff(d0, axis=2) <= 1e-7)  # in r_d
+
+
+def test_residual_bits_lower_distortion():
+    w, Xs, S, r = tiny()
+    assert np.all(np.diff(r.dist, axis=3) < 0)
+
+
+def test_randomized_converges_to_exact():
+    w = kvgen.custom_workload("tiny", H=4, T=96, D=32, cp_rank=6, noise=0.001,
+                              rT=(2, 4, jolt.FULL), rd=(4, 8, jolt.FULL))
+    X = kvgen.make_unit_f64(w, 1)
+    sk = kvgen.make_sketch(w, 1).astype(np.float64)
+    ex = jolt.factorize(X, w.rT, w.rd, "exact")
+    rz = jolt.factorize(X, w.rT, w.rd, "randomized", sk, power_iters=30)
+    for rd in ex.rd_list:
+        for k in (2, 4):
+            Pe = ex.UT[rd][:, :k] @ ex.UT[rd][:, :k].T
+            Pr = rz.UT[rd][:, :k] @ rz.UT[rd][:, :k].T
+            assert np.max(np.abs(Pe - Pr)) <= 1e-8
+
+
+def test_cholesky_qr2_matches_library_qr():
+    rng = np.random.default_rng(2)
+    Z = rng.standard_normal((300, 12)) @ np.diag(np.logspace(0, 3, 12))
+    Q = jolt.cholesky_qr2(Z)
+    Qn, Rn = np.linalg.qr(Z)
+    Qn = Qn * np.sign(np.diag(Rn))[None, :]
+    assert np.max(np.abs(Q - Qn)) <= 1e-10
+    G = rng.standard_normal((9, 9))
+    G = G @ G.T + np.eye(9)
+    assert np.allclose(jolt.cholesky_lower(G), np.linalg.cholesky(G), atol=1e-13)
+
+
+# ---------------------------------------------------------------- cost / codec
+def test_cost_formula_hand_values():
+    # tiny unit H=4, T=64, D=32, block 32:
+    # (4,4,0): 2*4*(4*64 + 4*4 + 4*32) = 3200 -> 3328 aligned, + 256 header
+    assert jolt.cost_formula(4, 64, 32, 4, 4, 0, 32) == 3584
+    # (4,4,4): 3328 + 4*8192/8 = 4096 + 2*8192/32 = 512 + 256 = 8192
+    assert jolt.cost_formula(4, 64, 32, 4, 4, 4, 32) == 8192
+    # Mistral unit H=32, T=1024, D=128, (32,32,4):
+    # 2*32*(32768 + 1024 + 4096) = 2424832; codes 2097152; scales 65536
+    assert jolt.cost_formula(32, 1024, 128, 32, 32, 4, 128) == 2424832 + 2097152 + 65536 + 256
+
+
+def test_fp16_footprint_matches_pages():
+    # [P5 Efficiency]: Mistral KV at ctx 2048 is 268.4 MB in fp16
+    w = kvgen.WORKLOADS["mistral_t2048"]
+    assert w.fp16_bytes == 32 * 8 * 128 * 2048 * 2 * 2 == 268435456
+
+
+def test_blob_never_exceeds_formula_cost():
+    for w in kvgen.WORKLOADS.values():
+        rT = [jolt.resolve(r, w.T) for r in w.rT]
+        rd = [jolt.resolve(r, w.D) for r in w.rd]
+        f = jolt.cost_table(w.H, w.T, w.D, rT, rd, w.bits, w.block, "formula")
+        s = jolt.cost_table(w.H, w.T, w.D, rT, rd, w.bits, w.block, "serialized")
+        assert np.all(s <= f)
+
+
+def test_codec_round_trip_reproduces_scored_candidate():
+    w, Xs, S, r = tiny()
+    for u in range(w.n_units):
+        xh = jolt.decode_unit(r.blobs[u])
+        d = jolt.distortion(Xs[u], xh)
+        assert d == pytest.approx(r.dist[u].reshape(-1)[r.choice[u]], rel=1e-12, abs=1e-15)
+        hd = jolt.parse_header(r.blobs[u])
+        assert np.array_equal(hd["signs"], S[u])
+        assert hd["bytes"] == len(r.blobs[u]) <= r.cost[u].reshape(-1)[r.choice[u]]
+    # every candidate of one unit round-trips
+    X, fac = Xs[1], r.factors[1]
+    for iT, idd, ib in jolt.candidate_list(fac.rT_list, fac.rd_list, w.bits):
+        blob = jolt.encode_unit(X, fac, S[1], fac.rT_list[iT], fac.rd_list[idd], w.bits[ib], w.block)
+        assert jolt.distortion(X, jolt.decode_unit(blob)) == pytest.approx(
+            r.dist[1, iT, idd, ib], rel=1e-12, abs=1e-15)
+
+
+def test_zero_unit():
+    X = np.zeros((2, 16, 8))
+    fac = jolt.factorize(X, [4, jolt.FULL], [2, jolt.FULL])
+    d = jolt.dist_table(X, fac, np.ones(8, np.int8))
+    assert np.all(d == 0.0)
+
+
+# ---------------------------------------------------------------- allocation
+def test_allocate_hand_case():
+    dist = np.array([[1.0, 0.1], [0.5, 0.4]])
+    cost = np.array([[100, 300], [100, 200]])
+    # align = 1: stop only on an exact fit (the early stop within one
+    # alignment block would accept the first feasible point here)
+    z, lam, st = jolt.allocate(dist, cost, 400, align=1)
+    assert st == jolt.ALLOC_OK and list(z) == [1, 0]
+    assert 0.001 < lam < 0.0045
+    z, lam, st = jolt.allocate(dist, cost, 10 ** 6)
+    assert list(z) == [1, 1] and lam == 0.0
+    z, lam, st = jolt.allocate(dist, cost, 150)
+    assert st == jolt.ALLOC_INFEASIBLE and list(z) == [0, 0]
+
+
+def test_allocate_brute_force_tiny():
+    w, Xs, S, r = tiny()
+    U = w.n_units
+    dist = r.dist.reshape(U, -1)
+    cost = r.cost.reshape(U, -1)
+    z, lam, st = jolt.allocate(dist, cost, w.budget_bytes)
+    assert st == jolt.ALLOC_OK
+    Dz = sum(dist[u, z[u]] for u in range(U))
+    Cz = sum(int(cost[u, z[u]]) for u in range(U))
+    assert Cz <= w.budget_bytes
+    # all 80^4 allocations, as (units 0,1) x (units 2,3)
+    d01 = (dist[0][:, None] + dist[1][None, :]).reshape(-1)
+    c01 = (cost[0][:, None] + cost[1][None, :]).reshape(-1)
+    d23 = (dist[2][:, None] + dist[3][None, :]).reshape(-1)
+    c23 = (cost[2][:, None] + cost[3][None, :]).reshape(-1)
+    order = np.argsort(c23, kind="stable")
+    c23s, d23min = c23[order], np.minimum.accumulate(d23[order])
+
+    def best_at(limit):
+        k = np.searchsorted(c23s, limit - c01, side="right") - 1
+        ok = k >= 0
+        return np.min(np.where(ok, d01 + d23min[np.maximum(k, 0)], np.inf))
+
+    # on the lower convex hull: nothing at most as costly is better
+    assert best_at(Cz) >= Dz - 1e-12
+    # the duality gap to the true optimum at the budget is reported, not pinned
+    gap = Dz - best_at(w.budget_bytes)
+    assert gap >= -1e-12
