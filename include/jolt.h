@@ -1,0 +1,209 @@
+/*
+ * libjolt -- KV-cache encode and decode by partial Tucker + rotated residual
+ * + Lagrangian allocation (JoLT), for NVIDIA B300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "Joint Tucker-rank and residual-bit KV allocator": Formulas,
+ *        Mathematical statement, Implementation notes.
+ *   [P4] "Rotated Tucker residual for outlier-resistant KV quantization":
+ *        Mathematical statement, Key formulas, Implementation notes.
+ *   [P5] "Technical Summary: A JOLT for the KV Cache": Methodology 1-4.
+ *
+ * Vocabulary.  A *unit* is one group tensor X[H][T][D] of one cache type
+ * (K or V) of one layer group: H = layers-in-group x KV heads (kept whole),
+ * T tokens, D features (a power of two, 32..128).  A *candidate* is
+ * z = (r_T, r_d, b): token rank, feature rank, residual bits.  Candidates are
+ * numbered flat, iT-major, then id, then ib, over the grid of the config.
+ *
+ * Conventions shared by every call.
+ *   - All tensor arguments are DEVICE pointers unless the name ends in
+ *     `_host`.  The caller owns every buffer; the library never allocates
+ *     device memory.  Batches of units are contiguous: X is
+ *     [n_units][H][T][D], signs is [n_units][D], and so on.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and returns after its launches are queued.  Argument
+ *     errors are detected on the host before anything is launched and are
+ *     returned as JOLT_ERR_INVALID / JOLT_ERR_WORKSPACE.  Errors found on the
+ *     device (no convergence, non-finite input) are recorded in a status word
+ *     inside the workspace; jolt_read_status() synchronises and reports them.
+ *     No kernel traps or asserts.
+ *   - Random draws of the method (the rotation's sign vector and the
+ *     FlashJoLT Gaussian sketch) are inputs, never generated inside.
+ */
+#ifndef JOLT_H
+#define JOLT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  JOLT_OK = 0,
+  JOLT_ERR_INVALID = 1,     /* bad argument (shape, grid, pointer, dtype) */
+  JOLT_ERR_INFEASIBLE = 2,  /* budget below the cheapest allocation */
+  JOLT_ERR_NONFINITE = 3,   /* NaN/Inf met in X or in a scale */
+  JOLT_ERR_NOCONVERGE = 4,  /* an eigensolver hit its iteration cap */
+  JOLT_ERR_WORKSPACE = 5,   /* workspace missing or too small */
+  JOLT_ERR_CUDA = 6         /* a CUDA runtime call failed */
+} jolt_status;
+
+typedef enum { JOLT_F32 = 0, JOLT_BF16 = 1, JOLT_F16 = 2 } jolt_dtype;
+
+typedef enum {
+  JOLT_TOKEN_EXACT = 0,      /* token-mode eigenvectors solved to convergence */
+  JOLT_TOKEN_RANDOMIZED = 1  /* FlashJoLT randomized range finder [P5 Methodology 4] */
+} jolt_token_mode;
+
+typedef enum {
+  JOLT_COST_FORMULA = 0,     /* the printed cost expression [P1 Formulas] */
+  JOLT_COST_SERIALIZED = 1   /* bytes of the serialized blob [P1 Implementation notes] */
+} jolt_cost_model;
+
+/* Grid sentinel: keep a mode untruncated (r_T = T or r_d = D). */
+#define JOLT_FULL (-1)
+#define JOLT_MAX_GRID 8
+#define JOLT_HEADER_BYTES 256
+
+/*
+ * Shape, candidate grid and options of one batch of units.
+ *   rT[], rd[]   ascending; truncated ranks first, JOLT_FULL (at most once,
+ *                last) for the untruncated mode; truncated r_T <= 64,
+ *                truncated r_d <= 64 and < D, r_T < T.
+ *   b[]          ascending subset of {0, 2, 4, 8} [P1 Implementation notes].
+ *   quant_block  values per quantization block; must equal D (one block is
+ *                one (h, t) row of the rotated residual).
+ *   oversample, power_iters   FlashJoLT sketch width p and power steps q.
+ *   align        section alignment of the blob and of the cost model.
+ */
+typedef struct {
+  int H, T, D;
+  jolt_dtype dtype;                 /* X element type: JOLT_F32 or JOLT_BF16 */
+  int n_rT, rT[JOLT_MAX_GRID];
+  int n_rd, rd[JOLT_MAX_GRID];
+  int n_b, b[4];
+  int quant_block;
+  jolt_token_mode token_mode;
+  int oversample;
+  int power_iters;
+  jolt_cost_model cost_model;
+  int align;
+} jolt_config;
+
+/* Host-side description of one serialized unit (the blob's header fields). */
+typedef struct {
+  int H, T, D, rT, rd, b, block;
+  int flags;                        /* bit 0: U_T omitted (r_T = T); bit 1: U_d omitted (r_d = D) */
+  uint64_t off_UT, off_Ud, off_G, off_scale, off_codes, bytes;
+} jolt_blob_desc;
+
+/* Number of candidates n_rT * n_rd * n_b of a config (0 if invalid). */
+int jolt_num_candidates(const jolt_config* cfg);
+
+/* Bytes of workspace one unit needs; a batch of n units needs n times this,
+ * contiguous, 256-byte aligned.  0 if the config is invalid. */
+size_t jolt_workspace_size(const jolt_config* cfg);
+
+/*
+ * Partial Tucker factors of every unit, by ST-HOSVD over the feature mode and
+ * then the token mode, head axis kept [P1 Mathematical statement,
+ * Implementation notes; P5 Methodology 1]:
+ *   S_d = sum_{h,t} x_{h,t} x_{h,t}^T, U_d = its leading eigenvectors;
+ *   for every r_d of the grid: Y = X x_3 U_d(r_d)^T, S_T = Y_(T) Y_(T)^T,
+ *   U_T(r_d) = its leading eigenvectors (exact mode) or the FlashJoLT
+ *   randomized range finder's (randomized mode, [P5 Methodology 4]);
+ *   cores G = Y x_2 U_T^T.  Factors and cores are rounded to fp16, the
+ *   storage type, and kept in the workspace for the calls below.
+ *   X       [n_units][H][T][D], cfg->dtype
+ *   sketch  [n_units][H][D][max truncated r_T + oversample] fp32 Gaussian
+ *           test matrix (randomized mode only, else may be NULL); the sketch
+ *           for feature rank r_d is the leading r_d rows of each head's slab.
+ *   ws      n_units * jolt_workspace_size(cfg) bytes.
+ * Device errors: JOLT_ERR_NOCONVERGE (eigensolver cap) in the status word.
+ */
+jolt_status jolt_factor_group(const jolt_config* cfg, int n_units, const void* X,
+                              const float* sketch, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * Distortion and byte cost of every candidate of every unit [P1 Formulas]:
+ *   dist[u][iT][id][ib] = ||X - X^||_F^2 / ||X||_F^2 (0 for an all-zero X),
+ *   X^ = X~ + Q^T Q_b(Q R), R = X - X~, Q = H_D diag(sigma) / sqrt(D)
+ *   [P4 Key formulas, Implementation notes], Q_b the symmetric per-block
+ *   absmax quantizer with fp16 block scale, b = 0 meaning X^ = X~.
+ *   cost[u][iT][id][ib] in bytes, per cfg->cost_model.
+ *   signs  [n_units][D] int8, each +1 or -1 (diag(sigma) of the rotation).
+ *   dist   [n_units][n_cand] float64; cost [n_units][n_cand] int64.
+ * Requires jolt_factor_group on the same ws first.
+ * Device errors: JOLT_ERR_NONFINITE in the status word.
+ */
+jolt_status jolt_sweep_candidates(const jolt_config* cfg, int n_units, const void* X,
+                                  const int8_t* signs, void* ws, size_t ws_bytes,
+                                  double* dist, int64_t* cost, void* stream);
+
+/*
+ * One candidate per unit under a global byte budget by bisection on the
+ * Lagrange multiplier lambda [P1 Formulas, Mathematical statement,
+ * Implementation notes; P5 Methodology 3]: z(lambda) = argmin_z
+ * dist + lambda * cost per unit (product rounded before the sum; ties to the
+ * smaller cost, then the lower index).  If z(0) fits, it is returned with
+ * lambda = 0.  If the cheapest allocation does not fit, it is returned with
+ * status JOLT_ERR_INFEASIBLE.  Otherwise hi = 1 is doubled until z(hi) fits,
+ * then (lo, hi) is bisected (at most 200 steps) until the total cost lies
+ * within one `align` block below the budget or the interval is at the
+ * resolution of a double; z(hi) is returned.
+ *   dist [n_units][n_cand] f64, cost [n_units][n_cand] int64 (device).
+ *   choice [n_units] int32, lambda [1] f64, status [1] int32 (device,
+ *   JOLT_OK or JOLT_ERR_INFEASIBLE).
+ * Runs in one thread block.
+ */
+jolt_status jolt_allocate(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                          int64_t budget, int align, int32_t* choice, double* lambda,
+                          int32_t* status, void* stream);
+
+/* Size in bytes of the serialized blob of candidate `cand` (flat index). */
+size_t jolt_blob_bytes(const jolt_config* cfg, int cand);
+
+/*
+ * Serialize each unit's chosen candidate [P4 Implementation notes: store the
+ * block scale and the integer codes]: a 256-byte header, then U_T (fp16
+ * T x r_T, omitted when r_T = T), U_d (fp16 D x r_d, omitted when r_d = D),
+ * G (fp16 H x r_T x r_d), scales (fp16, one per row) and codes (b-bit
+ * offset-binary q + 2^(b-1), packed LSB-first), sections aligned to
+ * cfg->align.
+ *   choice_host [n_units] flat candidate indices (host memory).
+ *   blob        [n_units] slots of blob_stride bytes each (device).
+ *   desc_out    [n_units] filled on the host.
+ */
+jolt_status jolt_encode(const jolt_config* cfg, int n_units, const void* X,
+                        const int8_t* signs, const void* ws, size_t ws_bytes,
+                        const int32_t* choice_host, void* blob, size_t blob_stride,
+                        jolt_blob_desc* desc_out, void* stream);
+
+/*
+ * Rebuild X^ = G x_2 U_T x_3 U_d + Q^T (s * codes) of each unit from its blob
+ * [P1 Formulas; P4 Implementation notes: multiply codes by s, apply the
+ * inverse transform, add X~].  The kernel reads each blob's header on the
+ * device; desc gives the host the shapes for validation.
+ *   xhat  [n_units][H][T][D] in out_dtype (JOLT_F32 or JOLT_BF16, RNE).
+ */
+jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blob,
+                        size_t blob_stride, void* xhat, jolt_dtype out_dtype, void* stream);
+
+/* Synchronise `stream` and return the worst device status recorded in the
+ * workspace of the n_units units (then clear it). */
+jolt_status jolt_read_status(const jolt_config* cfg, int n_units, void* ws, void* stream);
+
+/* Human-readable name of a status code. */
+const char* jolt_status_string(jolt_status s);
+
+/* Number of kernel launches the library has queued since load (counter for
+ * benchmarks). */
+uint64_t jolt_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JOLT_H */

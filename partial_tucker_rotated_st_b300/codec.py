@@ -1,0 +1,100 @@
+"""Buffer management around the C entry points: one encoder for a batch of
+units of one shape.  Device memory comes from torch; every step of the method
+runs in libjolt's kernels (see jolt.py for the bindings).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import jolt as J
+
+_DT = {"f32": J.F32, "bf16": J.BF16}
+_TORCH_DT = {J.F32: torch.float32, J.BF16: torch.bfloat16}
+
+
+def config_for(w) -> J.JoltConfig:
+    """jolt_config of a workload description with fields H, T, D, dtype
+    ("f32"/"bf16"), rT, rd, bits, block, token_mode ("exact"/"randomized"),
+    oversample, power_iters."""
+    return J.make_config(w.H, w.T, w.D, _DT[w.dtype], list(w.rT), list(w.rd), list(w.bits),
+                         w.block,
+                         J.TOKEN_RANDOMIZED if w.token_mode == "randomized" else J.TOKEN_EXACT,
+                         getattr(w, "oversample", 8), getattr(w, "power_iters", 2))
+
+
+@dataclasses.dataclass
+class EncodeResult:
+    dist: torch.Tensor          # [U, n_cand] f64 (device)
+    cost: torch.Tensor          # [U, n_cand] int64 (device)
+    choice: List[int]           # host
+    lam: float
+    alloc_status: int
+    blob: torch.Tensor          # [U, stride] uint8 (device)
+    desc: List[J.JoltBlobDesc]
+
+
+class Encoder:
+    """Owns the workspace and tables for n_units units of config cfg."""
+
+    def __init__(self, cfg: J.JoltConfig, n_units: int, device="cuda"):
+        self.cfg = cfg
+        self.U = n_units
+        self.device = torch.device(device)
+        self.ncand = J.jolt_num_candidates(cfg)
+        if self.ncand == 0:
+            raise J.JoltError("jolt_num_candidates", J.ERR_INVALID)
+        self.ws_unit = J.jolt_workspace_size(cfg)
+        self.ws = torch.empty(n_units * self.ws_unit, dtype=torch.uint8, device=self.device)
+        self.dist = torch.empty(n_units, self.ncand, dtype=torch.float64, device=self.device)
+        self.cost = torch.empty(n_units, self.ncand, dtype=torch.int64, device=self.device)
+        self.choice = torch.empty(n_units, dtype=torch.int32, device=self.device)
+        self.lam = torch.empty(1, dtype=torch.float64, device=self.device)
+        self.astat = torch.empty(1, dtype=torch.int32, device=self.device)
+        self.stride = max(J.jolt_blob_bytes(cfg, c) for c in range(self.ncand))
+        self.stride = (self.stride + 255) // 256 * 256
+        self.blob = torch.empty(n_units, self.stride, dtype=torch.uint8, device=self.device)
+        self.choice_host = torch.empty(n_units, dtype=torch.int32, pin_memory=True)
+
+    def factor(self, X, sketch=None, stream=None):
+        J.jolt_factor_group(self.cfg, self.U, X, sketch, self.ws, stream=stream)
+
+    def sweep(self, X, signs, stream=None):
+        J.jolt_sweep_candidates(self.cfg, self.U, X, signs, self.ws, self.dist, self.cost,
+                                stream=stream)
+
+    def allocate(self, budget: int, stream=None):
+        J.jolt_allocate(self.U, self.ncand, self.dist, self.cost, budget, self.cfg.align,
+                        self.choice, self.lam, self.astat, stream=stream)
+
+    def serialize(self, X, signs, choice: Sequence[int], stream=None):
+        return J.jolt_encode(self.cfg, self.U, X, signs, self.ws, choice, self.blob, self.stride,
+                             stream=stream)
+
+    def encode(self, X, signs, budget: int, sketch=None, stream=None) -> EncodeResult:
+        """factor -> sweep -> allocate -> serialize; one small device-to-host
+        copy of the chosen candidates sits between allocate and serialize."""
+        self.factor(X, sketch, stream)
+        self.sweep(X, signs, stream)
+        self.allocate(budget, stream)
+        self.choice_host.copy_(self.choice, non_blocking=True)
+        s = torch.cuda.current_stream() if stream is None else stream
+        s.synchronize()
+        choice = self.choice_host.tolist()
+        desc = self.serialize(X, signs, choice, stream)
+        return EncodeResult(self.dist, self.cost, choice, float("nan"), -1, self.blob, desc)
+
+    def status(self) -> int:
+        return J.jolt_read_status(self.cfg, self.U, self.ws)
+
+
+def decode(desc: Sequence[J.JoltBlobDesc], blob: torch.Tensor, stride: int,
+           out_dtype: int = J.BF16, out: Optional[torch.Tensor] = None, stream=None):
+    d0 = desc[0]
+    if out is None:
+        out = torch.empty(len(desc), d0.H, d0.T, d0.D, dtype=_TORCH_DT[out_dtype],
+                          device=blob.device)
+    J.jolt_decode(desc, blob, stride, out, out_dtype, stream=stream)
+    return out

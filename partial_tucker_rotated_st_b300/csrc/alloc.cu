@@ -1,0 +1,148 @@
+// Global byte-budget allocation by bisection on the Lagrange multiplier.
+//
+// ["Joint Tucker-rank and residual-bit KV allocator", Formulas: L(z, lambda)
+//  = sum D(z) + lambda (sum C(z) - B), z*(lambda) = argmin_z D(z) + lambda C(z)
+//  per group and cache type; Implementation notes: binary-search lambda until
+//  total storage is within one alignment block of B; "Technical Summary: A
+//  JOLT for the KV Cache", Methodology 3.]
+//
+// One thread block.  Each best response is taken per unit by one warp: the
+// candidate with the least dist + lambda * cost (the product rounded before
+// the sum, no fused multiply-add), ties to the smaller cost, then the lower
+// candidate index.  The schedule of lambda values:
+//   z(0) fits            -> return it, lambda = 0
+//   cheapest misfits     -> return the cheapest allocation, INFEASIBLE
+//   otherwise hi = 1, doubled until z(hi) fits, lo = the last misfit (0 at
+//   first); then up to 200 bisection steps on mid = (lo + hi) / 2, keeping
+//   z(hi) feasible, stopping once sum C(z(hi)) is within one alignment block
+//   of the budget or hi - lo <= 2^-52 hi; return z(hi), hi.
+#include "jolt_internal.cuh"
+
+namespace jolt {
+
+namespace {
+
+constexpr int AL_THREADS = 512;
+constexpr int AL_MAX_ITER = 200;
+
+// Lexicographic key (k1, k2, index).
+struct Key {
+  double k1, k2;
+  int i;
+};
+
+__device__ __forceinline__ bool less_key(const Key& a, const Key& b) {
+  if (a.k1 != b.k1) return a.k1 < b.k1;
+  if (a.k2 != b.k2) return a.k2 < b.k2;
+  return a.i < b.i;
+}
+
+// mode 0: z(lambda), key (dist + lambda*cost, cost, index)
+// mode 1: cheapest allocation, key (cost, dist, index)
+// Writes out[u] and, through *tot, the total cost (all threads see it).
+__device__ void best_response(int U, int nc, const double* dist, const int64_t* cost, double lam,
+                              int mode, int* out, long long* tot) {
+  const int w = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+  __shared__ long long part[AL_THREADS / 32];
+  long long mine = 0;
+  for (int u = w; u < U; u += nw) {
+    Key b{INFINITY, INFINITY, INT_MAX};
+    for (int c = lane; c < nc; c += 32) {
+      const double d = dist[(long long)u * nc + c];
+      const double k = (double)cost[(long long)u * nc + c];
+      const Key x = (mode == 0) ? Key{__dadd_rn(d, __dmul_rn(lam, k)), k, c} : Key{k, d, c};
+      if (less_key(x, b)) b = x;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Key y;
+      y.k1 = __shfl_xor_sync(0xffffffffu, b.k1, o);
+      y.k2 = __shfl_xor_sync(0xffffffffu, b.k2, o);
+      y.i = __shfl_xor_sync(0xffffffffu, b.i, o);
+      if (less_key(y, b)) b = y;
+    }
+    if (lane == 0) {
+      out[u] = b.i;
+      mine += cost[(long long)u * nc + b.i];
+    }
+  }
+  if (lane == 0) part[w] = mine;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long s = 0;
+    for (int i = 0; i < nw; ++i) s += part[i];
+    *tot = s;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(AL_THREADS)
+alloc_kernel(int U, int nc, const double* __restrict__ dist, const int64_t* __restrict__ cost,
+             long long budget, int align, int32_t* choice, double* lambda, int32_t* status) {
+  extern __shared__ int zs[];
+  __shared__ long long tot;
+  int* zhi = zs;            // [U]
+  int* zmid = zs + U;       // [U]
+  best_response(U, nc, dist, cost, 0.0, 0, zhi, &tot);
+  if (tot <= budget) {
+    for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = zhi[u];
+    if (threadIdx.x == 0) { *lambda = 0.0; *status = JOLT_OK; }
+    return;
+  }
+  best_response(U, nc, dist, cost, 0.0, 1, zhi, &tot);
+  if (tot > budget) {
+    for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = zhi[u];
+    if (threadIdx.x == 0) { *lambda = INFINITY; *status = JOLT_ERR_INFEASIBLE; }
+    return;
+  }
+  double lo = 0.0, hi = 1.0;
+  best_response(U, nc, dist, cost, hi, 0, zhi, &tot);
+  long long chi = tot;
+  // z(lambda) reaches the cheapest allocation, which fits, as lambda grows;
+  // the cap only guards non-finite tables
+  while (chi > budget && hi < 1e300) {
+    lo = hi;
+    hi = hi * 2.0;
+    best_response(U, nc, dist, cost, hi, 0, zhi, &tot);
+    chi = tot;
+  }
+  for (int it = 0; it < AL_MAX_ITER; ++it) {
+    if ((budget - align < chi && chi <= budget) || hi - lo <= 0x1.0p-52 * hi) break;
+    const double mid = 0.5 * (lo + hi);
+    best_response(U, nc, dist, cost, mid, 0, zmid, &tot);
+    if (tot <= budget) {
+      hi = mid;
+      chi = tot;
+      for (int u = threadIdx.x; u < U; u += blockDim.x) zhi[u] = zmid[u];
+      __syncthreads();
+    } else {
+      lo = mid;
+    }
+  }
+  for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = zhi[u];
+  if (threadIdx.x == 0) {
+    *lambda = hi;
+    *status = (chi <= budget) ? JOLT_OK : JOLT_ERR_INFEASIBLE;
+  }
+}
+
+}  // namespace
+
+jolt_status alloc_run(int U, int nc, const double* dist, const int64_t* cost, int64_t budget,
+                      int align, int32_t* choice, double* lambda, int32_t* status,
+                      cudaStream_t st) {
+  const size_t smem = (size_t)2 * U * sizeof(int);
+  if (smem > 160 * 1024) return JOLT_ERR_INVALID;
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(alloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       160 * 1024));
+    attr = true;
+  }
+  alloc_kernel<<<1, AL_THREADS, smem, st>>>(U, nc, dist, cost, (long long)budget, align, choice,
+                                            lambda, status);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+}  // namespace jolt

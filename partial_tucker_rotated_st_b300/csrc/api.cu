@@ -1,0 +1,288 @@
+// C-ABI entry points of libjolt: argument validation, the per-unit workspace
+// layout, and dispatch to the kernels of factor.cu, sweep.cu, alloc.cu and
+// codec.cu.  Nothing here allocates device memory.
+#include "jolt_internal.cuh"
+
+#include <string.h>
+
+namespace jolt {
+
+unsigned long long g_launches = 0;
+
+jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
+  if (!cfg || !Lp) return JOLT_ERR_INVALID;
+  Layout L;
+  memset(&L, 0, sizeof(L));
+  L.H = cfg->H; L.T = cfg->T; L.D = cfg->D; L.dtype = cfg->dtype;
+  if (L.H <= 0 || L.T <= 0 || L.D <= 0) return JOLT_ERR_INVALID;
+  if (!(L.D == 32 || L.D == 64 || L.D == 128)) return JOLT_ERR_INVALID;
+  if (L.dtype != JOLT_F32 && L.dtype != JOLT_BF16) return JOLT_ERR_INVALID;
+  if (cfg->quant_block != L.D) return JOLT_ERR_INVALID;
+  if (cfg->n_rT < 1 || cfg->n_rT > JOLT_MAX_GRID || cfg->n_rd < 1 || cfg->n_rd > JOLT_MAX_GRID)
+    return JOLT_ERR_INVALID;
+  if (cfg->n_b < 1 || cfg->n_b > 4) return JOLT_ERR_INVALID;
+  L.nT = cfg->n_rT; L.nd = cfg->n_rd; L.nb = cfg->n_b;
+  // token ranks: ascending truncated ranks, then an optional FULL
+  for (int i = 0; i < L.nT; ++i) {
+    const int r = cfg->rT[i];
+    if (r == JOLT_FULL) {
+      if (i != L.nT - 1) return JOLT_ERR_INVALID;
+      L.rT[i] = L.T;
+      L.hasFullT = 1;
+    } else {
+      if (r < 1 || r > 64 || r >= L.T) return JOLT_ERR_INVALID;
+      if (i > 0 && r <= cfg->rT[i - 1]) return JOLT_ERR_INVALID;
+      L.rT[i] = r;
+      L.nTt = i + 1;
+      L.RT = r;
+    }
+  }
+  for (int i = 0; i < L.nd; ++i) {
+    const int r = cfg->rd[i];
+    if (r == JOLT_FULL) {
+      if (i != L.nd - 1) return JOLT_ERR_INVALID;
+      L.rd[i] = L.D;
+      L.hasFullD = 1;
+    } else {
+      if (r < 1 || r > 64 || r >= L.D) return JOLT_ERR_INVALID;
+      if (i > 0 && r <= cfg->rd[i - 1]) return JOLT_ERR_INVALID;
+      L.rd[i] = r;
+      L.ndt = i + 1;
+      L.RD = r;
+    }
+  }
+  for (int i = 0; i < L.nb; ++i) {
+    const int b = cfg->b[i];
+    if (!(b == 0 || b == 2 || b == 4 || b == 8)) return JOLT_ERR_INVALID;
+    if (i > 0 && b <= cfg->b[i - 1]) return JOLT_ERR_INVALID;
+    L.b[i] = b;
+  }
+  L.token_mode = cfg->token_mode;
+  if (L.token_mode != JOLT_TOKEN_EXACT && L.token_mode != JOLT_TOKEN_RANDOMIZED)
+    return JOLT_ERR_INVALID;
+  if (cfg->cost_model != JOLT_COST_FORMULA && cfg->cost_model != JOLT_COST_SERIALIZED)
+    return JOLT_ERR_INVALID;
+  if (cfg->align < 16 || cfg->align % 16) return JOLT_ERR_INVALID;
+  L.cost_model = cfg->cost_model;
+  L.align = cfg->align;
+  L.block = cfg->quant_block;
+  L.power_iters = cfg->power_iters;
+  L.ncand = L.nT * L.nd * L.nb;
+
+  const int RT = L.RT, RD = L.RD, H = L.H, T = L.T, D = L.D;
+  if (RT > 0 && L.token_mode == JOLT_TOKEN_RANDOMIZED) {
+    if (cfg->oversample < 0 || cfg->power_iters < 0 || cfg->power_iters > 16)
+      return JOLT_ERR_INVALID;
+    L.ell = RT + cfg->oversample;
+    if (L.ell > 64 || L.ell > T) return JOLT_ERR_INVALID;
+    // the sketch Z = A Omega needs at least ell independent columns of A
+    for (int i = 0; i < L.nd; ++i)
+      if ((long long)H * L.rd[i] < L.ell) return JOLT_ERR_INVALID;
+  }
+  if (RT > 0 && L.token_mode == JOLT_TOKEN_EXACT) {
+    if (T <= 128) {
+      L.L = T;
+    } else {
+      int w = RT + 8 > 2 * RT ? RT + 8 : 2 * RT;
+      w = (w + 7) / 8 * 8;
+      if (w > 128) w = 128;
+      if (w > T) w = T;
+      L.L = w;
+    }
+  }
+  // feature Gram split: groups of hg heads with hg * T <= 4096 rows
+  int hg = 1;
+  for (int d = 1; d <= H; ++d)
+    if (H % d == 0 && (long long)d * T <= 4096) hg = d;
+  L.nsplit = H / hg;
+  L.chunk = hg;
+  L.tile_rows = 64;
+  L.ntiles = H * ((T + 63) / 64);
+
+  const int Lw = (L.token_mode == JOLT_TOKEN_EXACT) ? L.L : L.ell;
+  const bool iter = RT > 0 && (L.token_mode == JOLT_TOKEN_RANDOMIZED || T > 128);
+  const int Dmax = L.hasFullD ? D : RD;
+  size_t off = 0;
+  auto sect = [&](size_t bytes) {
+    off = align_up(off, 256);
+    const size_t o = off;
+    off += bytes;
+    return o;
+  };
+  L.o_status = sect(256);
+  L.o_flag = sect(256);
+  L.o_Sd = sect((size_t)D * D * 4);
+  L.o_Sdp = sect((size_t)L.nsplit * D * D * 4);
+  L.o_evd = sect((size_t)D * 4);
+  L.o_Vd = sect((size_t)D * D * 4);
+  L.o_Ud16 = sect((size_t)D * RD * 2);
+  L.o_QUd = sect((size_t)RD * D * 4);
+  L.o_Y = sect((size_t)H * T * RD * 4);
+  L.o_Y16 = sect((size_t)H * T * RD * 2);
+  L.o_ST = sect((RT > 0 && L.token_mode == JOLT_TOKEN_EXACT) ? (size_t)T * T * 4 : 0);
+  const size_t blk = iter ? (size_t)T * Lw * 4 : 0;
+  L.o_V = sect(blk);
+  L.o_Z = sect(blk);
+  L.o_V2 = sect(blk);
+  L.o_Z2 = sect(blk);
+  const size_t sq = RT > 0 ? (size_t)Lw * Lw * 4 : 0;
+  L.o_Hm = sect(sq);
+  L.o_Wm = sect(sq);
+  L.o_Gram = sect(sq);
+  L.o_Rinv = sect(sq);
+  L.o_theta = sect((size_t)(Lw > T ? Lw : T) * 4);
+  L.o_UT32 = sect((size_t)L.nd * T * RT * 4);
+  L.o_UT16 = sect((size_t)L.nd * T * RT * 2);
+  L.o_tokev = sect((size_t)L.nd * RT * 4);
+  L.o_G32 = sect((size_t)L.nd * H * RT * D * 4);
+  L.o_G16 = sect((size_t)L.nd * H * RT * D * 2);
+  L.o_W = sect((size_t)L.nd * H * RT * D * 4);
+  L.o_part = sect((size_t)L.ntiles * (L.ncand + 1) * 4);
+  L.o_P = sect((RT > 0 && L.token_mode == JOLT_TOKEN_RANDOMIZED) ? (size_t)H * Dmax * L.ell * 4 : 0);
+  L.unit_bytes = align_up(off, 256);
+  *Lp = L;
+  return JOLT_OK;
+}
+
+int64_t cost_formula(int H, int T, int D, int rT, int rd, int b, int block, int align) {
+  const long long n = (long long)H * T * D;
+  long long c = (long long)align_up((size_t)(2LL * H * ((long long)rT * T + (long long)rd * rT + (long long)rd * D)), align);
+  if (b > 0) c += (long long)align_up((size_t)(b * n / 8), align) + (long long)align_up((size_t)(2 * n / block), align);
+  return c + JOLT_HEADER_BYTES;
+}
+
+}  // namespace jolt
+
+using namespace jolt;
+
+static cudaStream_t S(void* s) { return (cudaStream_t)s; }
+
+static bool ws_ok(const Layout& L, int n, const void* ws, size_t ws_bytes) {
+  return ws && ((uintptr_t)ws % 256 == 0) && ws_bytes >= (size_t)n * L.unit_bytes;
+}
+
+extern "C" {
+
+int jolt_num_candidates(const jolt_config* cfg) {
+  Layout L;
+  if (make_layout(cfg, &L) != JOLT_OK) return 0;
+  return L.ncand;
+}
+
+size_t jolt_workspace_size(const jolt_config* cfg) {
+  Layout L;
+  if (make_layout(cfg, &L) != JOLT_OK) return 0;
+  return L.unit_bytes;
+}
+
+jolt_status jolt_factor_group(const jolt_config* cfg, int n_units, const void* X,
+                              const float* sketch, void* ws, size_t ws_bytes, void* stream) {
+  Layout L;
+  jolt_status s = make_layout(cfg, &L);
+  if (s != JOLT_OK) return s;
+  if (n_units < 1 || n_units > 65535 || !X) return JOLT_ERR_INVALID;
+  if (L.token_mode == JOLT_TOKEN_RANDOMIZED && L.RT > 0 && !sketch) return JOLT_ERR_INVALID;
+  if (!ws_ok(L, n_units, ws, ws_bytes)) return JOLT_ERR_WORKSPACE;
+  return factor_run(L, n_units, X, sketch, (char*)ws, S(stream));
+}
+
+jolt_status jolt_sweep_candidates(const jolt_config* cfg, int n_units, const void* X,
+                                  const int8_t* signs, void* ws, size_t ws_bytes, double* dist,
+                                  int64_t* cost, void* stream) {
+  Layout L;
+  jolt_status s = make_layout(cfg, &L);
+  if (s != JOLT_OK) return s;
+  if (n_units < 1 || n_units > 65535 || !X || !signs || !dist || !cost) return JOLT_ERR_INVALID;
+  if (!ws_ok(L, n_units, ws, ws_bytes)) return JOLT_ERR_WORKSPACE;
+  return sweep_run(L, n_units, X, signs, (char*)ws, dist, cost, S(stream));
+}
+
+jolt_status jolt_allocate(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                          int64_t budget, int align, int32_t* choice, double* lambda,
+                          int32_t* status, void* stream) {
+  if (n_units < 1 || n_cand < 1 || !dist || !cost || !choice || !lambda || !status || align < 1)
+    return JOLT_ERR_INVALID;
+  return alloc_run(n_units, n_cand, dist, cost, budget, align, choice, lambda, status, S(stream));
+}
+
+size_t jolt_blob_bytes(const jolt_config* cfg, int cand) {
+  Layout L;
+  if (make_layout(cfg, &L) != JOLT_OK || cand < 0 || cand >= L.ncand) return 0;
+  int iT, id, ib;
+  cand_split(L, cand, &iT, &id, &ib);
+  jolt_blob_desc d;
+  blob_layout(L.H, L.T, L.D, L.rT[iT], L.rd[id], L.b[ib], L.block, L.align, &d);
+  return d.bytes;
+}
+
+jolt_status jolt_encode(const jolt_config* cfg, int n_units, const void* X, const int8_t* signs,
+                        const void* ws, size_t ws_bytes, const int32_t* choice_host, void* blob,
+                        size_t blob_stride, jolt_blob_desc* desc_out, void* stream) {
+  Layout L;
+  jolt_status s = make_layout(cfg, &L);
+  if (s != JOLT_OK) return s;
+  if (n_units < 1 || !X || !signs || !choice_host || !blob || !desc_out) return JOLT_ERR_INVALID;
+  if (((uintptr_t)blob % 256) || (blob_stride % 256)) return JOLT_ERR_INVALID;
+  if (!ws_ok(L, n_units, ws, ws_bytes)) return JOLT_ERR_WORKSPACE;
+  return encode_run(L, n_units, X, signs, (const char*)ws, choice_host, (char*)blob, blob_stride,
+                    desc_out, S(stream));
+}
+
+jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blob,
+                        size_t blob_stride, void* xhat, jolt_dtype out_dtype, void* stream) {
+  if (n_units < 1 || !desc || !blob || !xhat) return JOLT_ERR_INVALID;
+  if (out_dtype != JOLT_F32 && out_dtype != JOLT_BF16) return JOLT_ERR_INVALID;
+  if (((uintptr_t)blob % 256) || (blob_stride % 256)) return JOLT_ERR_INVALID;
+  const int H = desc[0].H, T = desc[0].T, D = desc[0].D;
+  if (H <= 0 || T <= 0 || !(D == 32 || D == 64 || D == 128)) return JOLT_ERR_INVALID;
+  for (int u = 0; u < n_units; ++u) {
+    const jolt_blob_desc& d = desc[u];
+    if (d.H != H || d.T != T || d.D != D || d.block != D) return JOLT_ERR_INVALID;
+    if (!(d.rT == T || (d.rT >= 1 && d.rT <= 64 && d.rT < T))) return JOLT_ERR_INVALID;
+    if (!(d.rd == D || (d.rd >= 1 && d.rd <= 64 && d.rd < D))) return JOLT_ERR_INVALID;
+    if (!(d.b == 0 || d.b == 2 || d.b == 4 || d.b == 8)) return JOLT_ERR_INVALID;
+    if (d.bytes > blob_stride) return JOLT_ERR_INVALID;
+    if (d.off_G + 2ull * H * d.rT * d.rd > d.bytes) return JOLT_ERR_INVALID;
+    if (d.b > 0 && d.off_codes + (unsigned long long)H * T * D * d.b / 8 > d.bytes)
+      return JOLT_ERR_INVALID;
+  }
+  return decode_run(n_units, desc, (const char*)blob, blob_stride, xhat, out_dtype, S(stream));
+}
+
+jolt_status jolt_read_status(const jolt_config* cfg, int n_units, void* ws, void* stream) {
+  Layout L;
+  jolt_status s = make_layout(cfg, &L);
+  if (s != JOLT_OK) return s;
+  if (n_units < 1 || !ws) return JOLT_ERR_INVALID;
+  cudaStream_t st = S(stream);
+  JOLT_CUDA_TRY(cudaStreamSynchronize(st));
+  int worst = 0;
+  for (int u = 0; u < n_units; ++u) {
+    int v = 0;
+    JOLT_CUDA_TRY(cudaMemcpy(&v, (char*)ws + (size_t)u * L.unit_bytes + L.o_status, sizeof(int),
+                             cudaMemcpyDeviceToHost));
+    worst |= v;
+  }
+  JOLT_CUDA_TRY(cudaMemset2DAsync((char*)ws + L.o_status, L.unit_bytes, 0, sizeof(int), n_units, st));
+  JOLT_CUDA_TRY(cudaStreamSynchronize(st));
+  if (worst & ST_NONFINITE) return JOLT_ERR_NONFINITE;
+  if (worst & (ST_NOCONVERGE | ST_NOTPD)) return JOLT_ERR_NOCONVERGE;
+  return JOLT_OK;
+}
+
+const char* jolt_status_string(jolt_status s) {
+  switch (s) {
+    case JOLT_OK: return "ok";
+    case JOLT_ERR_INVALID: return "invalid argument";
+    case JOLT_ERR_INFEASIBLE: return "budget below the cheapest allocation";
+    case JOLT_ERR_NONFINITE: return "non-finite value in the input";
+    case JOLT_ERR_NOCONVERGE: return "eigensolver did not converge";
+    case JOLT_ERR_WORKSPACE: return "workspace missing or too small";
+    case JOLT_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+uint64_t jolt_launch_count(void) { return (uint64_t)g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,471 @@
+// Serialization of the chosen candidate and the decoder.
+//
+// ["Rotated Tucker residual for outlier-resistant KV quantization",
+//  Implementation notes: store the block scale s and the integer codes
+//  clip(round(Y/s), ...); decode by multiplying codes by s, applying the
+//  inverse orthogonal transform and adding X~; for b = 0 return X~ only.
+//  "Joint Tucker-rank and residual-bit KV allocator", Implementation notes:
+//  actual storage includes factors, core, codes, scales, transform metadata
+//  and alignment padding.]
+//
+// Blob (little-endian): 256-byte header
+//   0: u32 magic "JOLT", u32 version, i32 H, T, D, r_T, r_d, b, block, u32 flags
+//  40: u64 offsets of U_T, U_d, G, scales, codes, and the total size
+//  88: sign bits of diag(sigma), bit i set when sigma_i = -1, LSB first
+// then the sections, each starting on an `align` boundary:
+//   U_T fp16 [T][r_T] (absent when r_T = T), U_d fp16 [D][r_d] (absent when
+//   r_d = D), G fp16 [H][r_T][r_d] (fp16(X) when both modes are whole),
+//   scales fp16 [H*T] (one per row block), codes b-bit offset-binary
+//   u = q + 2^(b-1), element k in bits [k b, (k+1) b) of the byte stream.
+#include "jolt_internal.cuh"
+
+#include <string.h>
+
+namespace jolt {
+
+namespace {
+
+constexpr uint32_t MAGIC = 0x544C4F4Au;  // "JOLT"
+constexpr uint32_t VERSION = 1;
+constexpr int CD_WARPS = 8, CD_ROWS = 8, CD_TILE = 64, CD_THREADS = 256;
+
+struct HeaderArgs {
+  unsigned char fixed[88];
+  int D;
+};
+
+__global__ void header_kernel(HeaderArgs a, const int8_t* signs, char* blob) {
+  const int t = threadIdx.x;
+  for (int i = t; i < 88; i += blockDim.x) blob[i] = (char)a.fixed[i];
+  for (int i = t; i < (a.D + 7) / 8; i += blockDim.x) {
+    unsigned char v = 0;
+    for (int k = 0; k < 8; ++k) {
+      const int d = i * 8 + k;
+      if (d < a.D && signs[d] < 0) v |= (unsigned char)(1u << k);
+    }
+    blob[88 + i] = (char)v;
+  }
+}
+
+// dst[a][b][c] = fp16(src[a*sa + b*sb + c]) for a < A, b < B, c < C.
+template <typename TS>
+__global__ void copy_f16_kernel(const TS* src, long long sa, long long sb, __half* dst, int A, int B,
+                                int C) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long n = (long long)A * B * C;
+  if (e >= n) return;
+  const int c = (int)(e % C);
+  const long long ab = e / C;
+  const int b = (int)(ab % B), aa = (int)(ab / B);
+  dst[e] = __float2half_rn(to_f32(src[aa * sa + b * sb + c]));
+}
+
+struct EncArgs {
+  const void* X;
+  const int8_t* signs;
+  const char* ws;
+  int H, T, D, dtype;
+  int b, mode, K;   // mode 0: U_T W chain; 1: Y16 (Q U_d)^T chain; 2: whole modes
+  const __half* Kg;  // chain coefficients, row t at Kg + h*k_hs + t*k_ld
+  long long k_hs, k_ld;
+  const float* Bg;   // rotated factor rows, K x D, at Bg + h*b_hs
+  long long b_hs;
+  char* blob;
+  unsigned long long off_scale, off_codes;
+};
+
+template <typename TX, int EPT>
+__global__ void __launch_bounds__(CD_THREADS) encode_codes_kernel(EncArgs a) {
+  constexpr int D = 32 * EPT;
+  extern __shared__ __align__(16) float dsm[];
+  float* Ks = dsm;                       // [64][CD_TILE]
+  float* Bs = Ks + 64 * CD_TILE;         // [64][D]
+  unsigned char (*codes)[D] = reinterpret_cast<unsigned char (*)[D]>(Bs + 64 * D);  // [warps][D]
+  const int h = blockIdx.y, t0 = blockIdx.x * CD_TILE;
+  const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const TX* Xh = (const TX*)a.X + (long long)h * a.T * D;
+  float sg[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) sg[e] = (float)a.signs[lane * EPT + e];
+  const float rs = rsqrtf((float)D);
+  float acc[CD_ROWS][EPT];
+#pragma unroll
+  for (int r = 0; r < CD_ROWS; ++r) {
+    const int t = t0 + w * CD_ROWS + r;
+    float x[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) x[e] = (t < a.T) ? to_f32(Xh[(long long)t * D + lane * EPT + e]) : 0.f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) acc[r][e] = (a.mode == 2 ? x[e] - round_f16(x[e]) : x[e]) * sg[e];
+    fwht_row<EPT>(acc[r], lane);
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) acc[r][e] *= rs;
+  }
+  if (a.mode != 2 && a.K > 0) {
+    for (int i = threadIdx.x; i < CD_TILE * a.K; i += CD_THREADS) {
+      const int row = i / a.K, k = i % a.K;
+      const int t = t0 + row;
+      Ks[k * CD_TILE + row] = (t < a.T) ? __half2float(a.Kg[h * a.k_hs + (long long)t * a.k_ld + k]) : 0.f;
+    }
+    const float* Bh = a.Bg + h * a.b_hs;
+    for (int i = threadIdx.x; i < a.K * D; i += CD_THREADS) Bs[i] = Bh[i];
+    __syncthreads();
+    for (int k = 0; k < a.K; ++k) {
+      const float* kk = Ks + k * CD_TILE + w * CD_ROWS;
+      float bv[EPT];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) bv[e] = Bs[k * D + lane * EPT + e];
+#pragma unroll
+      for (int r = 0; r < CD_ROWS; ++r)
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(-kk[r], bv[e], acc[r][e]);
+    }
+  }
+  const int b = a.b;
+  const float qmax = (float)((1 << (b - 1)) - 1);
+  const int qoff = 1 << (b - 1);
+  const int nbytes = D * b / 8;
+  for (int r = 0; r < CD_ROWS; ++r) {
+    const int t = t0 + w * CD_ROWS + r;
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) m = fmaxf(m, fabsf(acc[r][e]));
+    m = warp_max(m);
+    const float s = round_f16(__fdiv_rn(m, qmax));
+    const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      float q = rint_magic(acc[r][e] * inv);
+      q = fminf(fmaxf(q, -(float)qoff), (float)(qoff - 1));
+      codes[w][lane * EPT + e] = (unsigned char)((int)q + qoff);
+    }
+    __syncwarp();
+    if (t < a.T) {
+      const long long row = (long long)h * a.T + t;
+      unsigned char* cb = (unsigned char*)a.blob + a.off_codes + row * nbytes;
+      const int per = 8 / b;
+      for (int j = lane; j < nbytes; j += 32) {
+        unsigned v = 0;
+        for (int i = 0; i < per; ++i) v |= (unsigned)codes[w][j * per + i] << (i * b);
+        cb[j] = (unsigned char)v;
+      }
+      if (lane == 0) ((__half*)(a.blob + a.off_scale))[row] = __float2half_rn(s);
+    }
+    __syncwarp();
+  }
+}
+
+struct DecUnit {
+  int rT, rd, b, pad;
+  unsigned long long off_UT, off_Ud, off_G, off_scale, off_codes;
+};
+constexpr int DEC_MAX_UNITS = 32;
+struct DecArgs {
+  int H, T, D, out_dtype;
+  const char* blob;
+  unsigned long long stride;
+  void* xhat;
+  int u0;
+  DecUnit un[DEC_MAX_UNITS];
+};
+
+// X^ = X~ + Q^T (s * codes), one tile of 64 rows of one head per CTA.
+template <int EPT>
+__global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
+  constexpr int D = 32 * EPT;
+  extern __shared__ __align__(16) float dsm[];
+  float* Ks = dsm;                       // [64][CD_TILE]
+  float* Bs = Ks + 64 * CD_TILE;         // [64][D]
+  const int uz = blockIdx.z, h = blockIdx.y, t0 = blockIdx.x * CD_TILE;
+  const int u = a.u0 + uz;
+  const DecUnit du = a.un[uz];
+  const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const char* blob = a.blob + (unsigned long long)u * a.stride;
+  const int T = a.T, H = a.H;
+  const int rT = du.rT, rd = du.rd, b = du.b;
+  const bool fullT = (rT == T), fullD = (rd == D);
+  const __half* G = (const __half*)(blob + du.off_G);
+  float acc[CD_ROWS][EPT];
+  int K = 0;
+  if (fullT && fullD) {
+#pragma unroll
+    for (int r = 0; r < CD_ROWS; ++r) {
+      const int t = t0 + w * CD_ROWS + r;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e)
+        acc[r][e] = (t < T) ? __half2float(G[((long long)h * T + t) * D + lane * EPT + e]) : 0.f;
+    }
+  } else {
+    if (fullT) {
+      // X~[t] = G[h][t][:rd] U_d^T
+      K = rd;
+      const __half* Ud = (const __half*)(blob + du.off_Ud);
+      for (int i = threadIdx.x; i < CD_TILE * K; i += CD_THREADS) {
+        const int row = i / K, j = i % K, t = t0 + row;
+        Ks[j * CD_TILE + row] = (t < T) ? __half2float(G[((long long)h * T + t) * rd + j]) : 0.f;
+      }
+      for (int i = threadIdx.x; i < K * D; i += CD_THREADS) {
+        const int j = i / D, d = i % D;
+        Bs[i] = __half2float(Ud[(long long)d * rd + j]);
+      }
+    } else {
+      // X~[t] = U_T[t] P_h, P_h = G[h] U_d^T (rT x D)
+      K = rT;
+      const __half* UT = (const __half*)(blob + du.off_UT);
+      for (int i = threadIdx.x; i < CD_TILE * K; i += CD_THREADS) {
+        const int row = i / K, k = i % K, t = t0 + row;
+        Ks[k * CD_TILE + row] = (t < T) ? __half2float(UT[(long long)t * rT + k]) : 0.f;
+      }
+      const __half* Gh = G + (long long)h * rT * rd;
+      if (fullD) {
+        for (int i = threadIdx.x; i < K * D; i += CD_THREADS) Bs[i] = __half2float(Gh[i]);
+      } else {
+        const __half* Ud = (const __half*)(blob + du.off_Ud);
+        for (int i = threadIdx.x; i < K * D; i += CD_THREADS) {
+          const int k = i / D, d = i % D;
+          float v = 0.f;
+          for (int j = 0; j < rd; ++j)
+            v = fmaf(__half2float(Gh[k * rd + j]), __half2float(Ud[(long long)d * rd + j]), v);
+          Bs[i] = v;
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < CD_ROWS; ++r)
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) acc[r][e] = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const float* kk = Ks + k * CD_TILE + w * CD_ROWS;
+      float bv[EPT];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) bv[e] = Bs[k * D + lane * EPT + e];
+#pragma unroll
+      for (int r = 0; r < CD_ROWS; ++r)
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(kk[r], bv[e], acc[r][e]);
+    }
+  }
+  if (b > 0) {
+    const unsigned char* sbits = (const unsigned char*)blob + 88;
+    float sg[EPT];
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const int d = lane * EPT + e;
+      sg[e] = ((sbits[d >> 3] >> (d & 7)) & 1) ? -1.f : 1.f;
+    }
+    const float rs = rsqrtf((float)D);
+    const unsigned char* cb = (const unsigned char*)blob + du.off_codes;
+    const __half* sc = (const __half*)(blob + du.off_scale);
+    const int qoff = 1 << (b - 1), mask = (1 << b) - 1;
+#pragma unroll
+    for (int r = 0; r < CD_ROWS; ++r) {
+      const int t = t0 + w * CD_ROWS + r;
+      const bool ok = t < T;
+      const long long row = (long long)h * T + (ok ? t : 0);
+      float q[EPT];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const long long bit = (row * D + lane * EPT + e) * b;
+        const int uu = ok ? ((cb[bit >> 3] >> (bit & 7)) & mask) : qoff;
+        q[e] = (float)(uu - qoff);
+      }
+      fwht_row<EPT>(q, lane);
+      const float cs = ok ? __half2float(sc[row]) * rs : 0.f;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(sg[e] * cs, q[e], acc[r][e]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < CD_ROWS; ++r) {
+    const int t = t0 + w * CD_ROWS + r;
+    if (t >= T) continue;
+    const long long o = (((long long)u * H + h) * T + t) * D + lane * EPT;
+    if (a.out_dtype == JOLT_BF16) {
+      __nv_bfloat16* y = (__nv_bfloat16*)a.xhat + o;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) y[e] = __float2bfloat16_rn(acc[r][e]);
+    } else {
+      float* y = (float*)a.xhat + o;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) y[e] = acc[r][e];
+    }
+  }
+}
+
+unsigned nblk(long long n) { return (unsigned)((n + 255) / 256); }
+
+template <typename TX, int EPT>
+jolt_status launch_enc(dim3 grid, const EncArgs& ea, cudaStream_t st) {
+  constexpr int D = 32 * EPT;
+  const size_t smem = (64 * CD_TILE + 64 * D) * sizeof(float) + CD_WARPS * D;
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(encode_codes_kernel<TX, EPT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr = true;
+  }
+  encode_codes_kernel<TX, EPT><<<grid, CD_THREADS, smem, st>>>(ea);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+template <int EPT>
+jolt_status launch_dec(dim3 grid, const DecArgs& a, cudaStream_t st) {
+  constexpr int D = 32 * EPT;
+  const size_t smem = (64 * CD_TILE + 64 * D) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(decode_kernel<EPT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr = true;
+  }
+  decode_kernel<EPT><<<grid, CD_THREADS, smem, st>>>(a);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+template <typename TS>
+jolt_status copy_f16(const void* src, long long sa, long long sb, void* dst, int A, int B, int C,
+                     cudaStream_t st) {
+  const long long n = (long long)A * B * C;
+  if (n <= 0) return JOLT_OK;
+  copy_f16_kernel<TS><<<nblk(n), 256, 0, st>>>((const TS*)src, sa, sb, (__half*)dst, A, B, C);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+}  // namespace
+
+void blob_layout(int H, int T, int D, int rT, int rd, int b, int block, int align,
+                 jolt_blob_desc* d) {
+  const long long n = (long long)H * T * D;
+  long long off = JOLT_HEADER_BYTES;
+  uint64_t* offs[5] = {&d->off_UT, &d->off_Ud, &d->off_G, &d->off_scale, &d->off_codes};
+  const long long sz[5] = {rT == T ? 0 : 2LL * T * rT, rd == D ? 0 : 2LL * D * rd,
+                           2LL * H * rT * rd, b == 0 ? 0 : 2 * (n / block), b == 0 ? 0 : n * b / 8};
+  for (int s = 0; s < 5; ++s) {
+    off = (long long)align_up((size_t)off, (size_t)align);
+    *offs[s] = sz[s] > 0 ? (uint64_t)off : (uint64_t)0;
+    off += sz[s];
+  }
+  d->bytes = align_up((size_t)off, (size_t)align);
+  d->H = H; d->T = T; d->D = D; d->rT = rT; d->rd = rd; d->b = b; d->block = block;
+  d->flags = (rT == T ? 1 : 0) | (rd == D ? 2 : 0);
+}
+
+jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* signs, const char* ws,
+                       const int32_t* choice, char* blob, size_t stride, jolt_blob_desc* desc,
+                       cudaStream_t st) {
+  const int H = L.H, T = L.T, D = L.D, RT = L.RT, RD = L.RD;
+  const size_t xes = (L.dtype == JOLT_F32) ? 4 : 2;
+  const long long xu = (long long)H * T * D;
+  // validate and lay out every unit before launching anything
+  for (int u = 0; u < U; ++u) {
+    if (choice[u] < 0 || choice[u] >= L.ncand) return JOLT_ERR_INVALID;
+    int iT, id, ib;
+    cand_split(L, choice[u], &iT, &id, &ib);
+    blob_layout(H, T, D, L.rT[iT], L.rd[id], L.b[ib], L.block, L.align, &desc[u]);
+    if (desc[u].bytes > stride) return JOLT_ERR_INVALID;
+  }
+  jolt_status s0 = sweep_prep(L, U, signs, (char*)ws, st);
+  if (s0 != JOLT_OK) return s0;
+  for (int u = 0; u < U; ++u) {
+    int iT, id, ib;
+    cand_split(L, choice[u], &iT, &id, &ib);
+    const int rT = L.rT[iT], rd = L.rd[id], b = L.b[ib];
+    const jolt_blob_desc& dsc = desc[u];
+    char* bl = blob + (size_t)u * stride;
+    const char* wu = ws + (size_t)u * L.unit_bytes;
+    const void* Xu = (const char*)X + (size_t)u * xu * xes;
+    JOLT_CUDA_TRY(cudaMemsetAsync(bl, 0, dsc.bytes, st));
+    HeaderArgs ha;
+    memset(&ha, 0, sizeof(ha));
+    const uint32_t hd32[10] = {MAGIC, VERSION, (uint32_t)H, (uint32_t)T, (uint32_t)D, (uint32_t)rT,
+                               (uint32_t)rd, (uint32_t)b, (uint32_t)L.block, (uint32_t)dsc.flags};
+    memcpy(ha.fixed, hd32, 40);
+    const uint64_t hd64[6] = {dsc.off_UT, dsc.off_Ud, dsc.off_G, dsc.off_scale, dsc.off_codes,
+                              dsc.bytes};
+    memcpy(ha.fixed + 40, hd64, 48);
+    ha.D = D;
+    header_kernel<<<1, 128, 0, st>>>(ha, signs + (size_t)u * D, bl);
+    JOLT_LAUNCH_CHECK();
+    // factor sections
+    if (rT < T) {
+      jolt_status s = copy_f16<__half>(wu + L.o_UT16 + (size_t)id * T * RT * 2, 0, RT,
+                                       bl + dsc.off_UT, 1, T, rT, st);
+      if (s != JOLT_OK) return s;
+    }
+    if (rd < D) {
+      jolt_status s = copy_f16<__half>(wu + L.o_Ud16, 0, RD, bl + dsc.off_Ud, 1, D, rd, st);
+      if (s != JOLT_OK) return s;
+    }
+    jolt_status s;
+    if (rT < T) {
+      s = copy_f16<__half>(wu + L.o_G16 + (size_t)id * H * RT * D * 2, (long long)RT * rd, rd,
+                           bl + dsc.off_G, H, rT, rd, st);
+    } else if (rd < D) {
+      s = copy_f16<__half>(wu + L.o_Y16, (long long)T * RD, RD, bl + dsc.off_G, H, T, rd, st);
+    } else if (L.dtype == JOLT_BF16) {
+      s = copy_f16<__nv_bfloat16>(Xu, (long long)T * D, D, bl + dsc.off_G, H, T, D, st);
+    } else {
+      s = copy_f16<float>(Xu, (long long)T * D, D, bl + dsc.off_G, H, T, D, st);
+    }
+    if (s != JOLT_OK) return s;
+    if (b == 0) continue;
+    EncArgs ea;
+    ea.X = Xu; ea.signs = signs + (size_t)u * D; ea.ws = wu;
+    ea.H = H; ea.T = T; ea.D = D; ea.dtype = L.dtype; ea.b = b;
+    ea.blob = bl; ea.off_scale = dsc.off_scale; ea.off_codes = dsc.off_codes;
+    if (rT == T && rd == D) {
+      ea.mode = 2; ea.K = 0; ea.Kg = nullptr; ea.k_hs = 0; ea.k_ld = 0; ea.Bg = nullptr; ea.b_hs = 0;
+    } else if (rT == T) {
+      ea.mode = 1; ea.K = rd;
+      ea.Kg = (const __half*)(wu + L.o_Y16); ea.k_hs = (long long)T * RD; ea.k_ld = RD;
+      ea.Bg = (const float*)(wu + L.o_QUd); ea.b_hs = 0;
+    } else {
+      ea.mode = 0; ea.K = rT;
+      ea.Kg = (const __half*)(wu + L.o_UT16) + (size_t)id * T * RT; ea.k_hs = 0; ea.k_ld = RT;
+      ea.Bg = (const float*)(wu + L.o_W) + (size_t)id * H * RT * D; ea.b_hs = (long long)RT * D;
+    }
+    dim3 grid((T + CD_TILE - 1) / CD_TILE, H);
+    const bool bf = (L.dtype == JOLT_BF16);
+    jolt_status ls;
+    switch (D) {
+      case 128: ls = bf ? launch_enc<__nv_bfloat16, 4>(grid, ea, st) : launch_enc<float, 4>(grid, ea, st); break;
+      case 64: ls = bf ? launch_enc<__nv_bfloat16, 2>(grid, ea, st) : launch_enc<float, 2>(grid, ea, st); break;
+      default: ls = bf ? launch_enc<__nv_bfloat16, 1>(grid, ea, st) : launch_enc<float, 1>(grid, ea, st);
+    }
+    if (ls != JOLT_OK) return ls;
+  }
+  return JOLT_OK;
+}
+
+jolt_status decode_run(int U, const jolt_blob_desc* desc, const char* blob, size_t stride,
+                       void* xhat, int out_dtype, cudaStream_t st) {
+  const int H = desc[0].H, T = desc[0].T, D = desc[0].D;
+  for (int u0 = 0; u0 < U; u0 += DEC_MAX_UNITS) {
+    const int nu = (U - u0) < DEC_MAX_UNITS ? (U - u0) : DEC_MAX_UNITS;
+    DecArgs a;
+    memset(&a, 0, sizeof(a));
+    a.H = H; a.T = T; a.D = D; a.out_dtype = out_dtype; a.blob = blob; a.stride = stride;
+    a.xhat = xhat; a.u0 = u0;
+    for (int i = 0; i < nu; ++i) {
+      const jolt_blob_desc& d = desc[u0 + i];
+      a.un[i].rT = d.rT; a.un[i].rd = d.rd; a.un[i].b = d.b;
+      a.un[i].off_UT = d.off_UT; a.un[i].off_Ud = d.off_Ud; a.un[i].off_G = d.off_G;
+      a.un[i].off_scale = d.off_scale; a.un[i].off_codes = d.off_codes;
+    }
+    dim3 grid((T + CD_TILE - 1) / CD_TILE, H, nu);
+    jolt_status ls;
+    switch (D) {
+      case 128: ls = launch_dec<4>(grid, a, st); break;
+      case 64: ls = launch_dec<2>(grid, a, st); break;
+      default: ls = launch_dec<1>(grid, a, st);
+    }
+    if (ls != JOLT_OK) return ls;
+  }
+  return JOLT_OK;
+}
+
+}  // namespace jolt

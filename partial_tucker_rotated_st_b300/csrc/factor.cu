@@ -1,0 +1,415 @@
+// Partial Tucker factors of a batch of units by ST-HOSVD over the feature and
+// token modes, head axis kept.
+//
+// ["Joint Tucker-rank and residual-bit KV allocator", Mathematical statement
+//  and Implementation notes: partial Tucker approximation over the token and
+//  feature axes, sequential or randomized SVD of the unfoldings;
+//  "Technical Summary: A JOLT for the KV Cache", Methodology 1 (ST-HOSVD,
+//  head and layer axes kept) and 4 (FlashJoLT: randomized token-mode SVD).]
+//
+// Order (feature mode first, then the token mode of the projected tensor):
+//   S_d = sum_{h,t} x x^T            split over head groups, f64 reduction
+//   U_d = leading eigenvectors of S_d (Jacobi)
+//   Y   = X U_d[:, :RD]              all truncated feature ranks at once
+//   per feature rank r_d (ascending, untruncated last):
+//     exact:      S_T(r_d) = sum_h Y_h[:, :r_d] Y_h[:, :r_d]^T (prefix sums over
+//                 r_d; the untruncated mode uses X), then block subspace
+//                 iteration with Rayleigh-Ritz to the leading RT eigenvectors
+//                 (a direct Jacobi solve when T <= 128)
+//     randomized: range finder Z = A Omega, q power steps A (A^T Q) each
+//                 re-orthonormalised by CholeskyQR2, Rayleigh-Ritz on
+//                 (A^T Q)^T (A^T Q)
+//     cores G(r_d)[h] = U_T^T Y_h[:, :r_d]   (U_T^T X_h for r_d = D)
+//   factors and cores rounded to fp16 (the storage type).
+#include "jolt_internal.cuh"
+
+#include <vector>
+
+namespace jolt {
+
+namespace {
+
+constexpr int SUB_MAX_ITERS = 120;
+constexpr int SUB_CHECK_EVERY = 4;
+constexpr float RITZ_TOL_REL = 1e-4f;
+constexpr float RITZ_TOL_ABS = 1e-5f;
+
+// Sd[u] = sum_s Sdp[u][s], in f64.
+__global__ void reduce_splits_kernel(char* ws, size_t ub, size_t o_part, size_t o_out, int nsplit,
+                                     int n) {
+  const int u = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  const float* p = (const float*)(ws + u * ub + o_part);
+  double s = 0.0;
+  for (int k = 0; k < nsplit; ++k) s += (double)p[(size_t)k * n + e];
+  ((float*)(ws + u * ub + o_out))[e] = (float)s;
+}
+
+// out[u][r][c] = fp16(in[u][r][c]) for r < rows, c < cols (row strides given).
+__global__ void round_f16_kernel(char* ws, size_t ub, size_t o_in, int ld_in, size_t o_out,
+                                 int ld_out, int rows, int cols, long long in_bs2,
+                                 long long out_bs2, int nb2) {
+  const int u = blockIdx.z / nb2, b2 = blockIdx.z % nb2;
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)rows * cols) return;
+  const int r = (int)(e / cols), c = (int)(e % cols);
+  const float* in = (const float*)(ws + u * ub + o_in) + b2 * in_bs2;
+  __half* out = (__half*)(ws + u * ub + o_out) + b2 * out_bs2;
+  out[(long long)r * ld_out + c] = __float2half_rn(in[(long long)r * ld_in + c]);
+}
+
+// Deterministic start block for subspace iteration, uniform in [-1, 1).
+__global__ void init_block_kernel(char* ws, size_t ub, size_t o_V, int n) {
+  const int u = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  unsigned long long z = 0x9E3779B97F4A7C15ull * (unsigned long long)(e + 1) + 0x2545F4914F6CDD1Dull;
+  z ^= z >> 31; z *= 0xBF58476D1CE4E5B9ull; z ^= z >> 27; z *= 0x94D049BB133111EBull; z ^= z >> 31;
+  ((float*)(ws + u * ub + o_V))[e] = (float)((double)(z >> 11) * 0x1.0p-53 * 2.0 - 1.0);
+}
+
+// Rayleigh-Ritz convergence test and bookkeeping, one CTA per unit.
+//   V2 = V W (Ritz vectors), Z2 = S V2, theta (descending Ritz values).
+//   Converged when, for i < k, ||Z2_i - theta_i V2_i|| <= max(rel |theta_i|,
+//   abs |theta_0|).  On convergence (or at the last iteration) the leading k
+//   Ritz vectors go to U (T x k) and theta to ev.  Z2's columns are then
+//   scaled by 1/||Z2_i|| (equilibration before CholeskyQR; the span is kept).
+__global__ void ritz_check_kernel(char* ws, size_t ub, size_t o_V2, size_t o_Z2, size_t o_th,
+                                  size_t o_U, size_t o_ev, size_t o_flag, size_t o_status, int T,
+                                  int Lw, int k, int last) {
+  const int u = blockIdx.x;
+  char* base = ws + u * ub;
+  int* flag = (int*)(base + o_flag);
+  if (*flag) return;
+  const float* V2 = (const float*)(base + o_V2);
+  float* Z2 = (float*)(base + o_Z2);
+  const float* th = (const float*)(base + o_th);
+  __shared__ float res[128], nz[128];
+  __shared__ int ok;
+  const int t = threadIdx.x, w = t / 32, lane = t % 32, nw = blockDim.x / 32;
+  for (int i = w; i < Lw; i += nw) {
+    float r = 0.f, z = 0.f;
+    const float ti = th[i];
+    for (int row = lane; row < T; row += 32) {
+      const float zz = Z2[(long long)row * Lw + i];
+      const float d = zz - ti * V2[(long long)row * Lw + i];
+      r = fmaf(d, d, r);
+      z = fmaf(zz, zz, z);
+    }
+    r = warp_sum(r);
+    z = warp_sum(z);
+    if (lane == 0) { res[i] = sqrtf(r); nz[i] = sqrtf(z); }
+  }
+  __syncthreads();
+  __shared__ int nonfinite;
+  if (t == 0) {
+    int good = 1, nf = !isfinite(th[0]);
+    const float a = RITZ_TOL_ABS * fabsf(th[0]);
+    for (int i = 0; i < k; ++i) {
+      const float lim = fmaxf(RITZ_TOL_REL * fabsf(th[i]), a);
+      if (!(res[i] <= lim)) good = 0;
+      if (!isfinite(res[i])) nf = 1;
+    }
+    ok = good;
+    nonfinite = nf;
+  }
+  __syncthreads();
+  if (nonfinite) {
+    if (t == 0) {
+      *flag = 1;
+      atomicOr((int*)(base + o_status), ST_NONFINITE);
+    }
+    return;
+  }
+  if (ok || last) {
+    float* U = (float*)(base + o_U);
+    for (long long e = t; e < (long long)T * k; e += blockDim.x) {
+      const int row = (int)(e / k), c = (int)(e % k);
+      U[e] = V2[(long long)row * Lw + c];
+    }
+    float* ev = (float*)(base + o_ev);
+    for (int i = t; i < k; i += blockDim.x) ev[i] = th[i];
+    if (t == 0) {
+      *flag = 1;
+      if (!ok) atomicOr((int*)(base + o_status), ST_NOCONVERGE);
+    }
+    return;
+  }
+  for (long long e = t; e < (long long)T * Lw; e += blockDim.x) {
+    const int c = (int)(e % Lw);
+    const float s = nz[c] > 0.f ? 1.f / nz[c] : 0.f;
+    Z2[e] *= s;
+  }
+}
+
+// out[u] = first k columns of in[u] (rows x ld_in) into rows x k.
+__global__ void copy_cols_kernel(char* ws, size_t ub, size_t o_in, int ld_in, size_t o_out,
+                                 int rows, int k) {
+  const int u = blockIdx.y;
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= (long long)rows * k) return;
+  const int r = (int)(e / k), c = (int)(e % k);
+  ((float*)(ws + u * ub + o_out))[e] = ((const float*)(ws + u * ub + o_in))[(long long)r * ld_in + c];
+}
+
+__global__ void set_int_kernel(char* ws, size_t ub, size_t o, int v) {
+  if (threadIdx.x == 0) *(int*)(ws + blockIdx.x * ub + o) = v;
+}
+
+// Helpers building GemmDesc over the batch of units (b1 = unit).
+struct F {
+  const Layout& L;
+  char* ws;
+  int U;
+  cudaStream_t st;
+  float* f(size_t o) const { return (float*)(ws + o); }
+};
+
+Opnd opnd(const void* p, int dt, long long s0, long long s1, long long sseg = 0, long long sb1 = 0,
+          long long sb2 = 0) {
+  Opnd o;
+  o.p = p; o.dtype = dt; o.s0 = s0; o.s1 = s1; o.sseg = sseg; o.sb1 = sb1; o.sb2 = sb2;
+  return o;
+}
+
+GemmDesc gd(int M, int N, int K, int nseg, int nb1, int nb2, Opnd A, Opnd B, float* C, long long cm,
+            long long cn, long long cb1, long long cb2, float beta = 0.f, const int* skip = nullptr) {
+  GemmDesc g;
+  g.M = M; g.N = N; g.K = K; g.nseg = nseg; g.nb1 = nb1; g.nb2 = nb2;
+  g.A = A; g.B = B; g.C = C; g.cm = cm; g.cn = cn; g.cb1 = cb1; g.cb2 = cb2;
+  g.alpha = 1.f; g.beta = beta; g.skip = skip;
+  return g;
+}
+
+#define TRY(x)                       \
+  do {                               \
+    jolt_status s_ = (x);            \
+    if (s_ != JOLT_OK) return s_;    \
+  } while (0)
+
+
+// a <- orth(a) by CholeskyQR2 (Fukaya et al. 2014), b is scratch; T x Lw per unit.
+jolt_status cholqr2_inplace(const F& c, int T, int Lw, size_t o_a, size_t o_b, const int* skip,
+                            bool f64) {
+  const Layout& L = c.L;
+  const long long ub4 = (long long)L.unit_bytes / 4;
+  const long long sks = ub4;
+  size_t src = o_a, dst = o_b;
+  for (int pass = 0; pass < 2; ++pass) {
+    GemmDesc g = gd(Lw, Lw, T, 1, c.U, 1, opnd(c.ws + src, JOLT_F32, 1, Lw, 0, ub4),
+                    opnd(c.ws + src, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Gram), Lw, 1, ub4, 0, 0.f,
+                    skip);
+    g.skip_stride = sks;
+    TRY(launch_gemm(g, c.st));
+    TRY(launch_chol_inv(c.f(L.o_Gram), ub4, Lw, c.U, c.f(L.o_Rinv), ub4, (int*)(c.ws + L.o_status),
+                        ub4, skip, sks, f64, c.st));
+    g = gd(T, Lw, Lw, 1, c.U, 1, opnd(c.ws + src, JOLT_F32, Lw, 1, 0, ub4),
+           opnd(c.ws + L.o_Rinv, JOLT_F32, Lw, 1, 0, ub4), c.f(dst), Lw, 1, ub4, 0, 0.f, skip);
+    g.skip_stride = sks;
+    TRY(launch_gemm(g, c.st));
+    const size_t tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  return JOLT_OK;  // two passes: the result is back in o_a
+}
+
+jolt_status read_flags_all(const F& c, bool* all) {
+  std::vector<int> h(c.U);
+  JOLT_CUDA_TRY(cudaMemcpy2DAsync(h.data(), sizeof(int), c.ws + c.L.o_flag, c.L.unit_bytes,
+                                  sizeof(int), c.U, cudaMemcpyDeviceToHost, c.st));
+  JOLT_CUDA_TRY(cudaStreamSynchronize(c.st));
+  bool a = true;
+  for (int v : h) a = a && (v != 0);
+  *all = a;
+  return JOLT_OK;
+}
+
+unsigned blocks_for(long long n, int tpb = 256) { return (unsigned)((n + tpb - 1) / tpb); }
+
+}  // namespace
+
+jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketch, char* ws,
+                       cudaStream_t st) {
+  F c{L, ws, U, st};
+  const size_t ub = L.unit_bytes;
+  const long long ub4 = (long long)ub / 4;
+  const int H = L.H, T = L.T, D = L.D, RD = L.RD, RT = L.RT;
+  const int xdt = L.dtype;
+  const long long xu = (long long)H * T * D;
+  int* status = (int*)(ws + L.o_status);
+  int* flags = (int*)(ws + L.o_flag);
+
+  set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_status, 0);
+  JOLT_LAUNCH_CHECK();
+
+  // ---- feature mode: S_d, split over groups of hg heads, f64 reduction
+  {
+    const int hg = H / L.nsplit;
+    TRY(launch_gemm(gd(D, D, T, hg, U, L.nsplit,
+                       opnd(X, xdt, 1, D, (long long)T * D, xu, (long long)hg * T * D),
+                       opnd(X, xdt, D, 1, (long long)T * D, xu, (long long)hg * T * D),
+                       c.f(L.o_Sdp), D, 1, ub4, (long long)D * D),
+                    st));
+    reduce_splits_kernel<<<dim3(blocks_for(D * D), U), 256, 0, st>>>(ws, ub, L.o_Sdp, L.o_Sd,
+                                                                     L.nsplit, D * D);
+    JOLT_LAUNCH_CHECK();
+    TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
+                      status, ub4, nullptr, 0, st));
+  }
+  if (RD > 0) {
+    round_f16_kernel<<<dim3(blocks_for(D * RD), 1, U), 256, 0, st>>>(ws, ub, L.o_Vd, D, L.o_Ud16,
+                                                                     RD, D, RD, 0, 0, 1);
+    JOLT_LAUNCH_CHECK();
+    TRY(launch_gemm(gd(H * T, RD, D, 1, U, 1, opnd(X, xdt, D, 1, 0, xu),
+                       opnd(ws + L.o_Vd, JOLT_F32, D, 1, 0, ub4), c.f(L.o_Y), RD, 1, ub4, 0),
+                    st));
+    round_f16_kernel<<<dim3(blocks_for((long long)H * T * RD), 1, U), 256, 0, st>>>(
+        ws, ub, L.o_Y, RD, L.o_Y16, RD, H * T, RD, 0, 0, 1);
+    JOLT_LAUNCH_CHECK();
+  }
+  if (RT == 0) return JOLT_OK;
+
+  // ---- token mode, one feature rank at a time
+  const bool exact = (L.token_mode == JOLT_TOKEN_EXACT);
+  const int Lw = exact ? L.L : L.ell;
+  size_t oV = L.o_V, oZ = L.o_Z, oV2 = L.o_V2, oZ2 = L.o_Z2;
+  bool st_started = false, sub_started = false;
+  int prev = 0;
+  for (int id = 0; id < L.nd; ++id) {
+    const int rdv = L.rd[id];
+    const bool full = (rdv == D);
+    const void* Ab;
+    int adt;
+    long long as_t, aseg, aub;
+    if (full) { Ab = X; adt = xdt; as_t = D; aseg = (long long)T * D; aub = xu; }
+    else { Ab = ws + L.o_Y; adt = JOLT_F32; as_t = RD; aseg = (long long)T * RD; aub = ub4; }
+    const size_t oUT = L.o_UT32 + (size_t)id * T * RT * 4;
+    const size_t oEV = L.o_tokev + (size_t)id * RT * 4;
+
+    if (exact) {
+      if (full) {
+        TRY(launch_gemm(gd(T, T, D, H, U, 1, opnd(X, xdt, D, 1, (long long)T * D, xu),
+                           opnd(X, xdt, 1, D, (long long)T * D, xu), c.f(L.o_ST), T, 1, ub4, 0),
+                        st));
+      } else {
+        const float* Y0 = (const float*)(ws + L.o_Y) + prev;
+        TRY(launch_gemm(gd(T, T, rdv - prev, H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),
+                           opnd(Y0, JOLT_F32, 1, RD, aseg, ub4), c.f(L.o_ST), T, 1, ub4, 0,
+                           st_started ? 1.f : 0.f),
+                        st));
+        st_started = true;
+        prev = rdv;
+      }
+      if (T <= 128) {
+        // direct solve of the whole token Gram
+        TRY(launch_jacobi(c.f(L.o_ST), ub4, T, T, U, c.f(L.o_theta), ub4, c.f(oUT), ub4, RT, RT,
+                          status, ub4, nullptr, 0, st));
+        copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, T, oEV, 1,
+                                                                  RT);
+        JOLT_LAUNCH_CHECK();
+      } else {
+        if (!sub_started) {
+          init_block_kernel<<<dim3(blocks_for((long long)T * Lw), U), 256, 0, st>>>(ws, ub, oV,
+                                                                                   T * Lw);
+          JOLT_LAUNCH_CHECK();
+          set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_flag, 0);
+          JOLT_LAUNCH_CHECK();
+          TRY(cholqr2_inplace(c, T, Lw, oV, oZ, nullptr, false));
+          sub_started = true;
+        }
+        set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_flag, 0);
+        JOLT_LAUNCH_CHECK();
+        for (int it = 0; it < SUB_MAX_ITERS; ++it) {
+          GemmDesc g;
+          // Z = S V
+          g = gd(T, Lw, T, 1, U, 1, opnd(ws + L.o_ST, JOLT_F32, T, 1, 0, ub4),
+                 opnd(ws + oV, JOLT_F32, Lw, 1, 0, ub4), c.f(oZ), Lw, 1, ub4, 0, 0.f, flags);
+          g.skip_stride = ub4;
+          TRY(launch_gemm(g, st));
+          // H = V^T Z
+          g = gd(Lw, Lw, T, 1, U, 1, opnd(ws + oV, JOLT_F32, 1, Lw, 0, ub4),
+                 opnd(ws + oZ, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Hm), Lw, 1, ub4, 0, 0.f, flags);
+          g.skip_stride = ub4;
+          TRY(launch_gemm(g, st));
+          TRY(launch_jacobi(c.f(L.o_Hm), ub4, Lw, Lw, U, c.f(L.o_theta), ub4, c.f(L.o_Wm), ub4,
+                            Lw, Lw, status, ub4, flags, ub4, st));
+          // Ritz vectors V2 = V W and Z2 = Z W = S V2
+          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + oV, JOLT_F32, Lw, 1, 0, ub4),
+                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(oV2), Lw, 1, ub4, 0, 0.f, flags);
+          g.skip_stride = ub4;
+          TRY(launch_gemm(g, st));
+          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + oZ, JOLT_F32, Lw, 1, 0, ub4),
+                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(oZ2), Lw, 1, ub4, 0, 0.f, flags);
+          g.skip_stride = ub4;
+          TRY(launch_gemm(g, st));
+          const int last = (it == SUB_MAX_ITERS - 1);
+          ritz_check_kernel<<<U, 256, 0, st>>>(ws, ub, oV2, oZ2, L.o_theta, oUT, oEV, L.o_flag,
+                                               L.o_status, T, Lw, RT, last);
+          JOLT_LAUNCH_CHECK();
+          if (last) break;
+          TRY(cholqr2_inplace(c, T, Lw, oZ2, oV, flags, false));
+          std::swap(oV, oZ2);
+          if ((it + 1) % SUB_CHECK_EVERY == 0) {
+            bool all = false;
+            TRY(read_flags_all(c, &all));
+            if (all) break;
+          }
+        }
+      }
+    } else {
+      // FlashJoLT randomized range finder with q power steps
+      const int ell = L.ell;
+      const long long sk_h = (long long)D * ell, sk_u = (long long)H * D * ell;
+      size_t oQ = oZ, oS = oV;
+      TRY(launch_gemm(gd(T, ell, rdv, H, U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
+                         opnd(sketch, JOLT_F32, ell, 1, sk_h, sk_u), c.f(oQ), ell, 1, ub4, 0),
+                      st));
+      TRY(cholqr2_inplace(c, T, ell, oQ, oS, nullptr, true));
+      for (int q = 0; q <= L.power_iters; ++q) {
+        // P_h = A_h^T Q  (rdv x ell per head)
+        TRY(launch_gemm(gd(rdv, ell, T, 1, U, H, opnd(Ab, adt, 1, as_t, 0, aub, aseg),
+                           opnd(ws + oQ, JOLT_F32, ell, 1, 0, ub4, 0), c.f(L.o_P), ell, 1, ub4,
+                           (long long)rdv * ell),
+                        st));
+        if (q == L.power_iters) break;
+        // Z = sum_h A_h P_h, re-orthonormalised
+        TRY(launch_gemm(gd(T, ell, rdv, H, U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
+                           opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4),
+                           c.f(oS), ell, 1, ub4, 0),
+                        st));
+        TRY(cholqr2_inplace(c, T, ell, oS, oQ, nullptr, true));
+        std::swap(oQ, oS);
+      }
+      // Rayleigh-Ritz: B B^T with B = Q^T A, i.e. sum_h P_h^T P_h
+      TRY(launch_gemm(gd(ell, ell, rdv, H, U, 1,
+                         opnd(ws + L.o_P, JOLT_F32, 1, ell, (long long)rdv * ell, ub4),
+                         opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4),
+                         c.f(L.o_Hm), ell, 1, ub4, 0),
+                      st));
+      TRY(launch_jacobi(c.f(L.o_Hm), ub4, ell, ell, U, c.f(L.o_theta), ub4, c.f(L.o_Wm), ub4, ell,
+                        RT, status, ub4, nullptr, 0, st));
+      TRY(launch_gemm(gd(T, RT, ell, 1, U, 1, opnd(ws + oQ, JOLT_F32, ell, 1, 0, ub4),
+                         opnd(ws + L.o_Wm, JOLT_F32, ell, 1, 0, ub4), c.f(oUT), RT, 1, ub4, 0),
+                      st));
+      copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, ell, oEV, 1, RT);
+      JOLT_LAUNCH_CHECK();
+    }
+    // cores G(r_d)[h] = U_T^T A_h  (RT x rdv)
+    const size_t oG = L.o_G32 + (size_t)id * H * RT * D * 4;
+    TRY(launch_gemm(gd(RT, rdv, T, 1, U, H, opnd(ws + oUT, JOLT_F32, 1, RT, 0, ub4),
+                       opnd(Ab, adt, as_t, 1, 0, aub, aseg), c.f(oG), rdv, 1, ub4,
+                       (long long)RT * rdv),
+                    st));
+    round_f16_kernel<<<dim3(blocks_for((long long)H * RT * rdv), 1, U), 256, 0, st>>>(
+        ws, ub, oG, rdv, L.o_G16 + (size_t)id * H * RT * D * 2, rdv, H * RT, rdv, 0, 0, 1);
+    JOLT_LAUNCH_CHECK();
+  }
+  round_f16_kernel<<<dim3(blocks_for((long long)L.nd * T * RT), 1, U), 256, 0, st>>>(
+      ws, ub, L.o_UT32, RT, L.o_UT16, RT, L.nd * T, RT, 0, 0, 1);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+}  // namespace jolt

@@ -1,0 +1,188 @@
+// Internal declarations of libjolt: workspace layout, launch helpers and the
+// kernel launchers each .cu file provides.  Host + device.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+#include <climits>
+
+#include "../../include/jolt.h"
+
+namespace jolt {
+
+// ------------------------------------------------------------------ status
+// Device status word bits, OR-ed into the unit's status slot.
+enum : int {
+  ST_NOCONVERGE = 1,
+  ST_NONFINITE = 2,
+  ST_NOTPD = 4,  // Cholesky met a non-positive pivot (reported as NOCONVERGE)
+};
+
+extern unsigned long long g_launches;
+inline void count_launch(int n = 1) { g_launches += (unsigned long long)n; }
+
+#define JOLT_CUDA_TRY(expr)                                   \
+  do {                                                        \
+    cudaError_t e_ = (expr);                                  \
+    if (e_ != cudaSuccess) return JOLT_ERR_CUDA;              \
+  } while (0)
+
+#define JOLT_LAUNCH_CHECK()                                   \
+  do {                                                        \
+    ::jolt::count_launch();                                   \
+    cudaError_t e_ = cudaGetLastError();                      \
+    if (e_ != cudaSuccess) return JOLT_ERR_CUDA;              \
+  } while (0)
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ layout
+// Resolved grid + byte offsets of every per-unit workspace section.
+struct Layout {
+  int H, T, D, dtype;
+  int nT, nd, nb;
+  int rT[JOLT_MAX_GRID];   // resolved (FULL -> T)
+  int rd[JOLT_MAX_GRID];   // resolved (FULL -> D)
+  int b[4];
+  int nTt;        // truncated token ranks (all but a trailing FULL)
+  int RT;         // largest truncated token rank (0 if none)
+  int hasFullT;
+  int ndt;        // truncated feature ranks
+  int RD;         // largest truncated feature rank (0 if none)
+  int hasFullD;
+  int token_mode;
+  int L;          // subspace-iteration block width (exact mode)
+  int ell;        // sketch width RT + oversample (randomized mode)
+  int power_iters;
+  int nsplit, chunk;     // feature-Gram split over rows
+  int tile_rows;         // sweep rows per CTA
+  int ntiles;            // sweep CTAs per unit
+  int ncand;
+  int cost_model, align, block;
+  // section offsets, bytes from the unit's base
+  size_t o_status, o_Sd, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16, o_ST;
+  size_t o_V, o_Z, o_V2, o_Z2, o_Hm, o_Wm, o_theta, o_Gram, o_Rinv, o_flag;
+  size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
+  size_t unit_bytes;
+};
+
+jolt_status make_layout(const jolt_config* cfg, Layout* L);
+
+// ------------------------------------------------------------------ GEMM
+// C[b1,b2] = alpha * sum_s A[b1,b2,s] (M x K) * B[b1,b2,s] (K x N) + beta * C
+// with arbitrary element strides.  dtype codes: JOLT_F32, JOLT_BF16, JOLT_F16.
+struct Opnd {
+  const void* p;
+  int dtype;
+  long long s0, s1;        // strides of the two matrix indices (A: m,k; B: k,n)
+  long long sseg, sb1, sb2;
+};
+struct GemmDesc {
+  int M, N, K, nseg, nb1, nb2;
+  Opnd A, B;
+  float* C;
+  long long cm, cn, cb1, cb2;
+  float alpha, beta;
+  const int* skip;         // optional per-b1 flag skip[b1 * skip_stride]; nonzero -> skipped
+  long long skip_stride;
+};
+jolt_status launch_gemm(const GemmDesc& g, cudaStream_t st);
+
+// ------------------------------------------------------------------ eigen
+// Batched cyclic Jacobi (one CTA per symmetric n x n matrix, n <= 128).
+// in: A[b] at A + b*a_bstride, row stride lda.  out: evals[b][n] descending,
+// evecs[b] with column i the i-th eigenvector (row stride ldv).
+jolt_status launch_jacobi(const float* A, long long a_bstride, int lda, int n, int batch,
+                          float* evals, long long e_bstride, float* evecs,
+                          long long v_bstride, int ldv, int ncols_out, int* status,
+                          long long status_bstride, const int* skip, long long skip_stride,
+                          cudaStream_t st);
+// Batched inverse Cholesky factor: G = R^T R (n x n, n <= 128), writes R^{-1}
+// (upper triangular, f32).  Arithmetic in f64 (n <= 64) when f64 is set, for
+// poorly conditioned sketches; f32 for equilibrated, near-orthogonal blocks.
+jolt_status launch_chol_inv(const float* G, long long g_bstride, int n, int batch,
+                            float* Rinv, long long r_bstride, int* status,
+                            long long status_bstride, const int* skip, long long skip_stride,
+                            bool f64, cudaStream_t st);
+
+// ------------------------------------------------------------------ steps
+jolt_status factor_run(const Layout& L, int n_units, const void* X, const float* sketch,
+                       char* ws, cudaStream_t st);
+// Rotated factor rows for the sweep and the encoder: Q U_d and W = G (Q U_d)^T.
+jolt_status sweep_prep(const Layout& L, int n_units, const int8_t* signs, char* ws,
+                       cudaStream_t st);
+jolt_status sweep_run(const Layout& L, int n_units, const void* X, const int8_t* signs,
+                      char* ws, double* dist, int64_t* cost, cudaStream_t st);
+jolt_status alloc_run(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                      int64_t budget, int align, int32_t* choice, double* lambda,
+                      int32_t* status, cudaStream_t st);
+jolt_status encode_run(const Layout& L, int n_units, const void* X, const int8_t* signs,
+                       const char* ws, const int32_t* choice_host, char* blob,
+                       size_t blob_stride, jolt_blob_desc* desc, cudaStream_t st);
+jolt_status decode_run(int n_units, const jolt_blob_desc* desc, const char* blob,
+                       size_t blob_stride, void* xhat, int out_dtype, cudaStream_t st);
+
+// ------------------------------------------------------------------ cost/blob
+// Candidate (iT, id, ib) <-> flat index, iT-major.
+static inline void cand_split(const Layout& L, int c, int* iT, int* id, int* ib) {
+  *ib = c % L.nb;
+  *id = (c / L.nb) % L.nd;
+  *iT = c / (L.nb * L.nd);
+}
+int64_t cost_formula(int H, int T, int D, int rT, int rd, int b, int block, int align);
+void blob_layout(int H, int T, int D, int rT, int rd, int b, int block, int align,
+                 jolt_blob_desc* d);
+
+// ------------------------------------------------------------------ device helpers
+#ifdef __CUDACC__
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+// fp32 -> nearest fp16 value (round to nearest even), returned as fp32.
+__device__ __forceinline__ float round_f16(float x) { return __half2float(__float2half_rn(x)); }
+
+// Round to nearest integer, ties to even, for |z| < 2^22, in two adds.
+__device__ __forceinline__ float rint_magic(float z) {
+  const float M = 12582912.0f;  // 1.5 * 2^23
+  return __fsub_rn(__fadd_rn(z, M), M);
+}
+
+// Fast Walsh-Hadamard transform (Sylvester order) of a row spread over a warp:
+// element i = lane * EPT + e.
+template <int EPT>
+__device__ __forceinline__ void fwht_row(float (&v)[EPT], int lane) {
+#pragma unroll
+  for (int h = 1; h < EPT; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (!(e & h)) {
+        const float a = v[e], b = v[e + h];
+        v[e] = a + b;
+        v[e + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+      v[e] = (lane & m) ? (o - v[e]) : (v[e] + o);
+    }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+#endif
+
+}  // namespace jolt

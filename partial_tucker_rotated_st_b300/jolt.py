@@ -1,0 +1,209 @@
+"""ctypes binding of libjolt (include/jolt.h): argument marshalling only.
+
+Every function takes torch tensors (device memory, contiguous) or plain
+integers, passes their addresses and the current CUDA stream to the C entry
+point of the same name, and raises JoltError on a non-OK status.  No step of
+the method runs here: all of it runs in libjolt's CUDA kernels.  The library
+must have been built (python -m partial_tucker_rotated_st_b300.build); there
+is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+FULL = -1
+F32, BF16, F16 = 0, 1, 2
+TOKEN_EXACT, TOKEN_RANDOMIZED = 0, 1
+COST_FORMULA, COST_SERIALIZED = 0, 1
+HEADER_BYTES = 256
+
+STATUS = {0: "JOLT_OK", 1: "JOLT_ERR_INVALID", 2: "JOLT_ERR_INFEASIBLE", 3: "JOLT_ERR_NONFINITE",
+          4: "JOLT_ERR_NOCONVERGE", 5: "JOLT_ERR_WORKSPACE", 6: "JOLT_ERR_CUDA"}
+OK, ERR_INVALID, ERR_INFEASIBLE, ERR_NONFINITE, ERR_NOCONVERGE, ERR_WORKSPACE, ERR_CUDA = range(7)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libjolt.so")
+
+
+class JoltError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class JoltConfig(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("T", ctypes.c_int), ("D", ctypes.c_int),
+                ("dtype", ctypes.c_int),
+                ("n_rT", ctypes.c_int), ("rT", ctypes.c_int * 8),
+                ("n_rd", ctypes.c_int), ("rd", ctypes.c_int * 8),
+                ("n_b", ctypes.c_int), ("b", ctypes.c_int * 4),
+                ("quant_block", ctypes.c_int), ("token_mode", ctypes.c_int),
+                ("oversample", ctypes.c_int), ("power_iters", ctypes.c_int),
+                ("cost_model", ctypes.c_int), ("align", ctypes.c_int)]
+
+
+class JoltBlobDesc(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("T", ctypes.c_int), ("D", ctypes.c_int),
+                ("rT", ctypes.c_int), ("rd", ctypes.c_int), ("b", ctypes.c_int),
+                ("block", ctypes.c_int), ("flags", ctypes.c_int),
+                ("off_UT", ctypes.c_uint64), ("off_Ud", ctypes.c_uint64),
+                ("off_G", ctypes.c_uint64), ("off_scale", ctypes.c_uint64),
+                ("off_codes", ctypes.c_uint64), ("bytes", ctypes.c_uint64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+# C signatures: (name, restype, argtypes)
+_P = ctypes.c_void_p
+_SIG = {
+    "jolt_num_candidates": (ctypes.c_int, [ctypes.POINTER(JoltConfig)]),
+    "jolt_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(JoltConfig)]),
+    "jolt_factor_group": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P, _P,
+                                         ctypes.c_size_t, _P]),
+    "jolt_sweep_candidates": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P, _P,
+                                             ctypes.c_size_t, _P, _P, _P]),
+    "jolt_allocate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int64,
+                                     ctypes.c_int, _P, _P, _P, _P]),
+    "jolt_blob_bytes": (ctypes.c_size_t, [ctypes.POINTER(JoltConfig), ctypes.c_int]),
+    "jolt_encode": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P, _P,
+                                   ctypes.c_size_t, _P, _P, ctypes.c_size_t,
+                                   ctypes.POINTER(JoltBlobDesc), _P]),
+    "jolt_decode": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(JoltBlobDesc), _P,
+                                   ctypes.c_size_t, _P, ctypes.c_int, _P]),
+    "jolt_read_status": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P]),
+    "jolt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "jolt_launch_count": (ctypes.c_uint64, []),
+}
+EXPORTS = tuple(_SIG)
+
+_lib_handle = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libjolt.so; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m partial_tucker_rotated_st_b300.build`")
+        h = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIG.items():
+            fn = getattr(h, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib_handle = h
+    return _lib_handle
+
+
+def _check(fn: str, st: int):
+    if st != OK:
+        raise JoltError(fn, st)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def make_config(H: int, T: int, D: int, dtype: int, rT: Sequence[int], rd: Sequence[int],
+                bits: Sequence[int], block: int, token_mode: int = TOKEN_EXACT,
+                oversample: int = 8, power_iters: int = 2, cost_model: int = COST_FORMULA,
+                align: int = 256) -> JoltConfig:
+    c = JoltConfig()
+    c.H, c.T, c.D, c.dtype = H, T, D, dtype
+    c.n_rT = len(rT)
+    for i, r in enumerate(rT):
+        c.rT[i] = r
+    c.n_rd = len(rd)
+    for i, r in enumerate(rd):
+        c.rd[i] = r
+    c.n_b = len(bits)
+    for i, b in enumerate(bits):
+        c.b[i] = b
+    c.quant_block = block
+    c.token_mode = token_mode
+    c.oversample = oversample
+    c.power_iters = power_iters
+    c.cost_model = cost_model
+    c.align = align
+    return c
+
+
+def jolt_num_candidates(cfg: JoltConfig) -> int:
+    return lib().jolt_num_candidates(ctypes.byref(cfg))
+
+
+def jolt_workspace_size(cfg: JoltConfig) -> int:
+    return lib().jolt_workspace_size(ctypes.byref(cfg))
+
+
+def jolt_factor_group(cfg, n_units, X, sketch, ws, ws_bytes=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("jolt_factor_group", lib().jolt_factor_group(
+        ctypes.byref(cfg), n_units, _ptr(X), _ptr(sketch), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def jolt_sweep_candidates(cfg, n_units, X, signs, ws, dist, cost, ws_bytes=None, stream=None):
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("jolt_sweep_candidates", lib().jolt_sweep_candidates(
+        ctypes.byref(cfg), n_units, _ptr(X), _ptr(signs), _ptr(ws), ws_bytes, _ptr(dist),
+        _ptr(cost), _stream(stream)))
+
+
+def jolt_allocate(n_units, n_cand, dist, cost, budget, align, choice, lam, status, stream=None):
+    _check("jolt_allocate", lib().jolt_allocate(
+        n_units, n_cand, _ptr(dist), _ptr(cost), int(budget), int(align), _ptr(choice),
+        _ptr(lam), _ptr(status), _stream(stream)))
+
+
+def jolt_blob_bytes(cfg: JoltConfig, cand: int) -> int:
+    return lib().jolt_blob_bytes(ctypes.byref(cfg), cand)
+
+
+def jolt_encode(cfg, n_units, X, signs, ws, choice_host: Sequence[int], blob, blob_stride,
+                ws_bytes=None, stream=None):
+    """Returns the list of JoltBlobDesc (host) of the serialized units."""
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    ch = (ctypes.c_int32 * n_units)(*[int(c) for c in choice_host])
+    desc = (JoltBlobDesc * n_units)()
+    _check("jolt_encode", lib().jolt_encode(
+        ctypes.byref(cfg), n_units, _ptr(X), _ptr(signs), _ptr(ws), ws_bytes, ch, _ptr(blob),
+        blob_stride, desc, _stream(stream)))
+    return list(desc)
+
+
+def jolt_decode(desc: Sequence[JoltBlobDesc], blob, blob_stride, xhat, out_dtype, stream=None):
+    n = len(desc)
+    arr = (JoltBlobDesc * n)(*desc)
+    _check("jolt_decode", lib().jolt_decode(n, arr, _ptr(blob), blob_stride, _ptr(xhat),
+                                            out_dtype, _stream(stream)))
+
+
+def jolt_read_status(cfg, n_units, ws, stream=None) -> int:
+    """Synchronises and returns the device status code (not raised)."""
+    return lib().jolt_read_status(ctypes.byref(cfg), n_units, _ptr(ws), _stream(stream))
+
+
+def jolt_status_string(s: int) -> str:
+    return lib().jolt_status_string(s).decode()
+
+
+def jolt_launch_count() -> int:
+    return lib().jolt_launch_count()

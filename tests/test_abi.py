@@ -1,0 +1,118 @@
+"""Host-side checks of the C-ABI library, no GPU needed: the shared object
+loads and exports every function include/jolt.h declares; the host logic
+(grid validation, candidate count, blob layout, workspace sizing) agrees with
+the oracle's byte accounting; invalid arguments are rejected before any CUDA
+call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import kvgen
+from oracle import jolt as oj
+from partial_tucker_rotated_st_b300 import build as jbuild
+from partial_tucker_rotated_st_b300 import codec
+from partial_tucker_rotated_st_b300 import jolt as J
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    jbuild.build()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "jolt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(jolt_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = header_functions()
+    assert len(names) == 11
+    lib = ctypes.CDLL(J.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(J.EXPORTS)
+
+
+def test_struct_sizes_match_c_layout():
+    assert ctypes.sizeof(J.JoltConfig) == 4 * (4 + 1 + 8 + 1 + 8 + 1 + 4 + 6)
+    assert ctypes.sizeof(J.JoltBlobDesc) == 8 * 4 + 6 * 8
+
+
+@pytest.mark.parametrize("name", sorted(kvgen.WORKLOADS))
+def test_blob_bytes_match_oracle_layout(name):
+    w = kvgen.WORKLOADS[name]
+    cfg = codec.config_for(w)
+    rT = [oj.resolve(r, w.T) for r in w.rT]
+    rd = [oj.resolve(r, w.D) for r in w.rd]
+    cands = oj.candidate_list(rT, rd, w.bits)
+    assert J.jolt_num_candidates(cfg) == len(cands)
+    for c, (i, j, k) in enumerate(cands):
+        lay = oj.blob_layout(w.H, w.T, w.D, rT[i], rd[j], w.bits[k], w.block)
+        assert J.jolt_blob_bytes(cfg, c) == lay["bytes"]
+    assert J.jolt_workspace_size(cfg) % 256 == 0 and J.jolt_workspace_size(cfg) > 0
+
+
+def _cfg(**kw):
+    w = kvgen.custom_workload("mistral_t1024", **kw) if kw else kvgen.WORKLOADS["mistral_t1024"]
+    return codec.config_for(w)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(D=96), dict(D=256), dict(block=64), dict(bits=(0, 3)), dict(bits=(4, 2)),
+    dict(rT=(8, 4, kvgen.FULL)), dict(rT=(4, kvgen.FULL, 8)), dict(rT=(4, 2048)),
+    dict(rd=(4, 128)), dict(rd=(4, 96)), dict(rT=(4, 80)),
+    dict(token_mode="randomized", oversample=40),
+])
+def test_invalid_configs_rejected(bad):
+    cfg = _cfg(**bad)
+    assert J.jolt_num_candidates(cfg) == 0
+    assert J.jolt_workspace_size(cfg) == 0
+    st = J.lib().jolt_factor_group(ctypes.byref(cfg), 1, 1 << 20, None, 1 << 20, 1 << 40, None)
+    assert st == J.ERR_INVALID
+
+
+def test_null_and_workspace_errors_before_launch():
+    cfg = _cfg()
+    L = J.lib()
+    ws = J.jolt_workspace_size(cfg)
+    assert L.jolt_factor_group(ctypes.byref(cfg), 1, None, None, 1 << 20, ws, None) == J.ERR_INVALID
+    assert L.jolt_factor_group(ctypes.byref(cfg), 0, 1 << 20, None, 1 << 20, ws, None) == J.ERR_INVALID
+    assert L.jolt_factor_group(ctypes.byref(cfg), 2, 1 << 20, None, 1 << 20, ws, None) == J.ERR_WORKSPACE
+    assert L.jolt_factor_group(ctypes.byref(cfg), 1, 1 << 20, None, None, ws, None) == J.ERR_WORKSPACE
+    # misaligned workspace
+    assert L.jolt_factor_group(ctypes.byref(cfg), 1, 1 << 20, None, (1 << 20) + 8, ws, None) == J.ERR_WORKSPACE
+    # randomized mode needs the sketch
+    rc = _cfg(token_mode="randomized")
+    assert L.jolt_factor_group(ctypes.byref(rc), 1, 1 << 20, None, 1 << 20, 1 << 40, None) == J.ERR_INVALID
+    assert L.jolt_allocate(0, 10, 1, 1, 100, 256, 1, 1, 1, None) == J.ERR_INVALID
+    assert L.jolt_allocate(4, 10, None, 1, 100, 256, 1, 1, 1, None) == J.ERR_INVALID
+
+
+def test_decode_rejects_inconsistent_descriptors():
+    d = J.JoltBlobDesc()
+    d.H, d.T, d.D, d.rT, d.rd, d.b, d.block = 4, 64, 32, 4, 4, 4, 32
+    lay = oj.blob_layout(4, 64, 32, 4, 4, 4, 32)
+    d.off_UT, d.off_Ud, d.off_G = lay["UT"], lay["Ud"], lay["G"]
+    d.off_scale, d.off_codes, d.bytes = lay["scale"], lay["codes"], lay["bytes"]
+    arr = (J.JoltBlobDesc * 1)(d)
+    L = J.lib()
+    # stride smaller than the blob
+    assert L.jolt_decode(1, arr, 1 << 20, 256, 1 << 21, J.F32, None) == J.ERR_INVALID
+    # bad dtype, bad b, bad block
+    assert L.jolt_decode(1, arr, 1 << 20, 1 << 16, 1 << 21, J.F16, None) == J.ERR_INVALID
+    arr[0].b = 3
+    assert L.jolt_decode(1, arr, 1 << 20, 1 << 16, 1 << 21, J.F32, None) == J.ERR_INVALID
+    arr[0].b = 4
+    arr[0].block = 16
+    assert L.jolt_decode(1, arr, 1 << 20, 1 << 16, 1 << 21, J.F32, None) == J.ERR_INVALID
+
+
+def test_status_strings():
+    for s in range(7):
+        assert J.jolt_status_string(s) and "unknown" not in J.jolt_status_string(s)

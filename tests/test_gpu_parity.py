@@ -1,0 +1,218 @@
+"""GPU parity of the CUDA path (through the C-ABI) against the float64 oracle
+on the same seeded inputs.
+
+Tolerances (fixed by the benchmark spec of the path):
+  * distortion tables and reconstructions: relative error <= 1e-3 with an
+    absolute floor of 1e-6;
+  * byte costs, blob layout and the allocation (when the oracle allocator is
+    fed the GPU's own tables): bit-exact;
+  * quantized codes, recomputed by the oracle from the GPU's stored factors:
+    at most 1e-4 of them off, and only by +-1 (rounding ties and the
+    reciprocal-vs-divide step);
+  * decode of a blob: the oracle's decode of the same blob to 1e-5 relative
+    (identical stored factors), bf16 output within one bf16 step.
+"""
+import numpy as np
+import pytest
+
+import kvgen
+from oracle import jolt as oj
+from tests import gpu_harness as gh
+
+pytestmark = pytest.mark.gpu
+
+REL, ABS = 1e-3, 1e-6
+
+# Reduced workloads with the full-size generator: several tiles and a ragged
+# tail in T, the subspace-iteration path (T > 128) and the randomized path.
+SMALL = {
+    "tiny": kvgen.WORKLOADS["tiny"],
+    "mistral_small": kvgen.custom_workload("mistral_t1024", n_groups=2, H=8, T=160),
+    "flash_small": kvgen.custom_workload("flash_t4096", n_groups=2, H=16, T=320),
+}
+
+_RUNS = {}
+
+
+def gpu_run(name):
+    if name not in _RUNS:
+        _RUNS[name] = gh.run(SMALL[name])
+    return _RUNS[name]
+
+
+_ORACLE = {}
+
+
+def oracle_tables(name):
+    if name not in _ORACLE:
+        w = SMALL[name]
+        r = gpu_run(name)
+        dists, facs = [], []
+        for i, u in enumerate(r.units):
+            sk = None if r.sketch is None else r.sketch[i].astype(np.float64)
+            fac = oj.factorize(r.X64[i], w.rT, w.rd, w.token_mode, sk, w.power_iters)
+            facs.append(fac)
+            dists.append(oj.dist_table(r.X64[i], fac, r.signs[i], w.bits))
+        _ORACLE[name] = (np.stack(dists).reshape(len(r.units), -1), facs)
+    return _ORACLE[name]
+
+
+def close(a, b, rel=REL, ab=ABS):
+    a, b = np.asarray(a, float), np.asarray(b, float)
+    return np.abs(a - b) <= np.maximum(rel * np.abs(b), ab)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_status_ok(name):
+    assert gpu_run(name).status == 0
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_cost_table_bit_exact(name):
+    w, r = SMALL[name], gpu_run(name)
+    fac = oracle_tables(name)[1][0]
+    ref = oj.cost_table(w.H, w.T, w.D, fac.rT_list, fac.rd_list, w.bits, w.block).reshape(-1)
+    for u in range(len(r.units)):
+        assert np.array_equal(r.cost[u], ref)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_distortion_table_matches_oracle(name):
+    r = gpu_run(name)
+    ref = oracle_tables(name)[0]
+    ok = close(r.dist, ref)
+    bad = np.argwhere(~ok)
+    assert ok.all(), [(int(u), int(c), r.dist[u, c], ref[u, c]) for u, c in bad[:10]]
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_allocation_bit_exact_on_gpu_tables(name):
+    w, r = SMALL[name], gpu_run(name)
+    budget = int(w.budget_bytes * len(r.units) // w.n_units)
+    z, lam, st = oj.allocate(r.dist, r.cost, budget, 256)
+    assert list(z) == list(r.choice)
+    assert lam == r.lam
+    assert (st == oj.ALLOC_OK) == (r.alloc_status == 0)
+    assert sum(int(r.cost[u, z[u]]) for u in range(len(z))) <= budget
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_allocation_total_distortion_vs_oracle(name):
+    w, r = SMALL[name], gpu_run(name)
+    budget = int(w.budget_bytes * len(r.units) // w.n_units)
+    ref, _ = oracle_tables(name)
+    zo, _, _ = oj.allocate(ref, r.cost, budget, 256)
+    d_gpu = sum(r.dist[u, r.choice[u]] for u in range(len(r.units)))
+    d_ora = sum(ref[u, zo[u]] for u in range(len(r.units)))
+    assert abs(d_gpu - d_ora) <= 1e-3 * abs(d_ora) + 1e-9
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_blob_header_and_scored_distortion(name):
+    """The oracle decodes the GPU's blob; its distortion is the GPU's table
+    entry for the chosen candidate."""
+    w, r = SMALL[name], gpu_run(name)
+    for i in range(len(r.units)):
+        hd = oj.parse_header(r.blobs[i])
+        c = int(r.choice[i])
+        lay = oj.blob_layout(w.H, w.T, w.D, hd["rT"], hd["rd"], hd["b"], w.block)
+        assert hd["bytes"] == lay["bytes"] == len(r.blobs[i]) == r.desc[i].bytes
+        for k in ("UT", "Ud", "G", "scale", "codes"):
+            assert hd[k] == lay[k]
+        assert np.array_equal(hd["signs"], r.signs[i])
+        assert r.cost[i, c] >= hd["bytes"]
+        d = oj.distortion(r.X64[i], oj.decode_unit(r.blobs[i]))
+        assert close(r.dist[i, c], d, 1e-4, 1e-7), (i, c, r.dist[i, c], d)
+
+
+def oracle_codes_from_blob(blob):
+    """Codes and scales the oracle's quantizer gives for the blob's own
+    stored factors."""
+    hd = oj.parse_header(blob)
+    H, T, D, rT, rd, b = hd["H"], hd["T"], hd["D"], hd["rT"], hd["rd"], hd["b"]
+
+    def arr(off, n, shape):
+        return np.frombuffer(blob, np.float16, n, off).astype(np.float64).reshape(shape)
+
+    UT = None if hd["flags"] & 1 else arr(hd["UT"], T * rT, (T, rT))
+    Ud = None if hd["flags"] & 2 else arr(hd["Ud"], D * rd, (D, rd))
+    G = arr(hd["G"], H * rT * rd, (H, rT, rd))
+    return oj.reconstruct(UT, G, Ud), hd
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_codes_match_oracle_quantizer(name):
+    """Encode every b of one rank pair per unit and compare the codes with the
+    oracle's quantizer applied to the same stored factors."""
+    w = SMALL[name]
+    r0 = gpu_run(name)
+    nb, nd = len(w.bits), len(w.rd)
+    for iT in range(len(w.rT)):
+        # one rank pair per token rank, cycling through feature ranks
+        idd = iT % nd
+        choice = [((iT * nd + idd) * nb + nb - 1 - (u % 2)) for u in range(len(r0.units))]
+        r = gh.run(w, choice_override=choice, decode=False)
+        for i in range(len(r.units)):
+            Xt, hd = oracle_codes_from_blob(r.blobs[i])
+            b = hd["b"]
+            if b == 0:
+                continue
+            Q = oj.rotation_matrix(hd["signs"])
+            n = w.H * w.T * w.D
+            q_ref, s_ref = oj.quantize_blocks((r.X64[i] - Xt).reshape(-1, w.D) @ Q.T, b)
+            s_gpu = np.frombuffer(r.blobs[i], np.float16, n // w.D, hd["scale"]).astype(np.float64)
+            q_gpu = oj.unpack_codes(r.blobs[i][hd["codes"]:hd["codes"] + n * b // 8], n, b)
+            assert np.mean(s_gpu != s_ref) <= 1e-3
+            diff = np.abs(q_gpu - q_ref.reshape(-1))
+            assert diff.max() <= 1
+            assert np.mean(diff != 0) <= 1e-4
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_decode_matches_oracle_decode(name):
+    w, r = SMALL[name], gpu_run(name)
+    for i in range(len(r.units)):
+        ref = oj.decode_unit(r.blobs[i])
+        err = np.linalg.norm(r.xhat32[i] - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert err <= 1e-5
+        ref16 = kvgen.round_to_bf16(ref.astype(np.float32))
+        g16 = r.xhat16[i]
+        # one bf16 step at most, on values whose f32 reconstruction sits near
+        # a rounding boundary
+        d = np.abs(g16.astype(np.int32) - ref16.astype(np.int32))
+        assert d.max() <= 1
+        assert np.mean(d != 0) <= 1e-3
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_distortion_properties(name):
+    """Facts that hold whatever the factors: more bits never hurt, full
+    ranks without residual reproduce X to fp16 rounding, rank monotonicity of
+    the truncation error."""
+    w, r = SMALL[name], gpu_run(name)
+    nT, nd, nb = len(w.rT), len(w.rd), len(w.bits)
+    d = r.dist.reshape(-1, nT, nd, nb)
+    assert np.all(np.isfinite(d)) and np.all(d >= 0)
+    assert np.all(np.diff(d, axis=3) <= 1e-9)
+    assert np.all(d[:, -1, -1, 0] <= 1e-6)
+    assert np.all(np.diff(d[..., 0], axis=1) <= 1e-6)
+    assert np.all(np.diff(d[..., 0], axis=2) <= 1e-6)
+
+
+def test_zero_unit_and_nonfinite_input():
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    w = SMALL["mistral_small"]
+    cfg = codec.config_for(w)
+    enc = codec.Encoder(cfg, 2)
+    X = torch.zeros(2, w.H, w.T, w.D, dtype=torch.bfloat16, device="cuda")
+    S = torch.ones(2, w.D, dtype=torch.int8, device="cuda")
+    enc.factor(X)
+    enc.sweep(X, S)
+    assert enc.status() == J.OK
+    assert torch.all(enc.dist == 0)
+    X[1, 3, 7, 5] = float("nan")
+    enc.factor(X)
+    enc.sweep(X, S)
+    assert enc.status() == J.ERR_NONFINITE
