@@ -253,8 +253,9 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
         flush.fill_(1)
-    if enc.status() != J.OK:
-        raise SystemExit(f"device status {J.jolt_status_string(enc.status())}")
+    st0 = enc.status()
+    if st0 != J.OK:
+        raise SystemExit(f"device status {J.jolt_status_string(st0)}")
     timers = []
     torch.cuda.synchronize()
     barrier(ws)

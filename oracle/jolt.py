@@ -163,14 +163,27 @@ class Factors:
         return f16(self.UT[rd][:, :rT]), f16(self.G[rd][:, :rT, :]), Ud
 
 
+def fix_signs(V: np.ndarray) -> np.ndarray:
+    """Each column scaled by +-1 so that its entry of largest magnitude (the
+    lowest such index on a tie) is positive."""
+    idx = np.argmax(np.abs(V), axis=0)
+    s = np.where(V[idx, np.arange(V.shape[1])] < 0, -1.0, 1.0)
+    return V * s[None, :]
+
+
 def feature_mode(X: np.ndarray):
     """S_d = X_(d) X_(d)^T summed over all (h, t) rows; eigenvectors in
-    descending eigenvalue order."""
+    descending eigenvalue order, signs fixed by fix_signs.
+
+    Reading: the FlashJoLT Gaussian sketch is indexed by the feature
+    coordinates of the projected tensor Y = X x_3 U_d^T, so the sketch the
+    token mode sees depends on the sign of each column of U_d; the sign rule
+    makes it well defined.  Every other result is sign-invariant."""
     H, T, D = X.shape
     rows = X.reshape(H * T, D)
     S = rows.T @ rows
     w, V, _ = jacobi_eigh(S)
-    return w, V
+    return w, fix_signs(V)
 
 
 def token_unfolding(Y: np.ndarray) -> np.ndarray:

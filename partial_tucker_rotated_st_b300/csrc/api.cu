@@ -265,6 +265,7 @@ jolt_status jolt_read_status(const jolt_config* cfg, int n_units, void* ws, void
   }
   JOLT_CUDA_TRY(cudaMemset2DAsync((char*)ws + L.o_status, L.unit_bytes, 0, sizeof(int), n_units, st));
   JOLT_CUDA_TRY(cudaStreamSynchronize(st));
+  if (worst & ST_TIMEOUT) return JOLT_ERR_CUDA;
   if (worst & ST_NONFINITE) return JOLT_ERR_NONFINITE;
   if (worst & (ST_NOCONVERGE | ST_NOTPD)) return JOLT_ERR_NOCONVERGE;
   return JOLT_OK;

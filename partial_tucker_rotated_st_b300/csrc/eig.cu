@@ -123,7 +123,9 @@ jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n,
   }
   if (!converged && t == 0 && status) atomicOr(status + bidx * s_bs, ST_NOCONVERGE);
 
-  // descending order, ties to the lower index
+  // descending order, ties to the lower index; each eigenvector's sign is
+  // fixed so that its entry of largest magnitude (lowest index on a tie) is
+  // positive
   float* ev = evals + bidx * e_bs;
   float* vg = evecs + bidx * v_bs;
   for (int i = t; i < n; i += blockDim.x) {
@@ -134,8 +136,14 @@ jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n,
       rank += (lj > li) || (lj == li && j < i);
     }
     ev[rank] = li;
-    if (rank < ncols_out)
-      for (int row = 0; row < n; ++row) vg[(long long)row * ldv + rank] = V[row * ld + i];
+    if (rank < ncols_out) {
+      float big = -1.f, sgn = 1.f;
+      for (int row = 0; row < n; ++row) {
+        const float v = V[row * ld + i];
+        if (fabsf(v) > big) { big = fabsf(v); sgn = v < 0.f ? -1.f : 1.f; }
+      }
+      for (int row = 0; row < n; ++row) vg[(long long)row * ldv + rank] = sgn * V[row * ld + i];
+    }
   }
 }
 

@@ -128,6 +128,11 @@ __global__ void ritz_check_kernel(char* ws, size_t ub, size_t o_V2, size_t o_Z2,
       const int row = (int)(e / k), c = (int)(e % k);
       U[e] = V2[(long long)row * Lw + c];
     }
+    // the host swaps the roles of the V and Z2 buffers after every step, and
+    // a converged unit skips the re-orthonormalisation: leave the
+    // orthonormal Ritz basis in Z2 too, so that either buffer warm-starts
+    // the next feature rank with an orthonormal block
+    for (long long e = t; e < (long long)T * Lw; e += blockDim.x) Z2[e] = V2[e];
     float* ev = (float*)(base + o_ev);
     for (int i = t; i < k; i += blockDim.x) ev[i] = th[i];
     if (t == 0) {
@@ -244,14 +249,19 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_status, 0);
   JOLT_LAUNCH_CHECK();
 
+  const bool tc = gram_tc_supported(L);
   // ---- feature mode: S_d, split over groups of hg heads, f64 reduction
   {
     const int hg = H / L.nsplit;
-    TRY(launch_gemm(gd(D, D, T, hg, U, L.nsplit,
-                       opnd(X, xdt, 1, D, (long long)T * D, xu, (long long)hg * T * D),
-                       opnd(X, xdt, D, 1, (long long)T * D, xu, (long long)hg * T * D),
-                       c.f(L.o_Sdp), D, 1, ub4, (long long)D * D),
-                    st));
+    if (tc && (hg * T) % 64 == 0) {
+      TRY(gram_feat_tc(L, U, X, ws, st));
+    } else {
+      TRY(launch_gemm(gd(D, D, T, hg, U, L.nsplit,
+                         opnd(X, xdt, 1, D, (long long)T * D, xu, (long long)hg * T * D),
+                         opnd(X, xdt, D, 1, (long long)T * D, xu, (long long)hg * T * D),
+                         c.f(L.o_Sdp), D, 1, ub4, (long long)D * D),
+                      st));
+    }
     reduce_splits_kernel<<<dim3(blocks_for(D * D), U), 256, 0, st>>>(ws, ub, L.o_Sdp, L.o_Sd,
                                                                      L.nsplit, D * D);
     JOLT_LAUNCH_CHECK();
@@ -290,9 +300,13 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
 
     if (exact) {
       if (full) {
-        TRY(launch_gemm(gd(T, T, D, H, U, 1, opnd(X, xdt, D, 1, (long long)T * D, xu),
-                           opnd(X, xdt, 1, D, (long long)T * D, xu), c.f(L.o_ST), T, 1, ub4, 0),
-                        st));
+        if (tc) {
+          TRY(gram_tok_tc(L, U, X, ws, st));
+        } else {
+          TRY(launch_gemm(gd(T, T, D, H, U, 1, opnd(X, xdt, D, 1, (long long)T * D, xu),
+                             opnd(X, xdt, 1, D, (long long)T * D, xu), c.f(L.o_ST), T, 1, ub4, 0),
+                          st));
+        }
       } else {
         const float* Y0 = (const float*)(ws + L.o_Y) + prev;
         TRY(launch_gemm(gd(T, T, rdv - prev, H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),

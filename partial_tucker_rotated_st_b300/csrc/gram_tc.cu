@@ -1,0 +1,326 @@
+// Gram matrices of the factor step on the 5th-generation tensor cores:
+// tcgen05.mma (bf16 x bf16 -> fp32 in TMEM), operands staged by TMA with
+// 128-byte swizzle, one elected thread issuing MMAs, a 4-stage mbarrier
+// pipeline, fp32 epilogue through tcgen05.ld.  bf16 inputs multiply exactly,
+// so these Grams are the exact sums of products up to fp32 accumulation.
+//
+//   token Gram   S_T[u] = sum_h X_h X_h^T            (T x T, K = H*D)
+//     ["Technical Summary: A JOLT for the KV Cache", Methodology 1 and 4:
+//      the token-mode SVD of the unfolding, the expensive one on long
+//      contexts]  Tiles of 128 x 128 on and above the diagonal; the lower
+//      triangle is written as the mirror.  Operands are K-major (rows of X_h).
+//   feature Gram S_d[u] = sum_{h,t} x x^T             (D x D, K = H*T)
+//     ["Joint Tucker-rank and residual-bit KV allocator", Implementation
+//      notes: SVD of the feature unfolding]  Split over row ranges, each CTA
+//      writes one fp32 partial, summed afterwards in f64.  Operands are
+//      MN-major: X's rows are read as stored, no transpose.
+//
+// Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues
+// MMAs, warps 2-5 drain the accumulator.  All mbarrier waits are bounded; a
+// timeout sets the unit's status word and the CTA still frees its TMEM.
+#include "jolt_internal.cuh"
+#include "tc_common.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace jolt {
+
+namespace {
+
+constexpr int STAGES = 4;
+constexpr int TILE = 128;
+constexpr int KCH = 64;                       // bf16 elements per 128-byte row
+constexpr int TILE_BYTES = TILE * KCH * 2;    // 16 KB
+constexpr int TC_THREADS = 192;
+
+struct TcArgs {
+  int T, D, H;
+  int nt;             // token tiles per dim (T / 128 rounded up)
+  int rows_per;       // feature Gram: rows per split
+  int nsplit;
+  float* out;         // unit 0 base of the output (S_T or the partials)
+  long long out_us;   // output unit stride, floats
+  char* ws;
+  size_t ub, o_status;
+};
+
+struct Smem {
+  // operand stages come first (1024-byte aligned by the launch)
+  uint64_t full[STAGES], empty[STAGES], accum;
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ void set_err(const TcArgs& a, int u) {
+  atomicOr((int*)(a.ws + (size_t)u * a.ub + a.o_status), ST_TIMEOUT);
+}
+
+// Drain one 128 x 128 fp32 accumulator: warp q (of 4) owns TMEM lanes
+// 32q..32q+31 = tile rows; calls f(row_in_tile, col_in_tile, v[32]) per
+// 32-column slab.
+template <typename F>
+__device__ __forceinline__ void drain(uint32_t tmem, int q, F&& f) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (int c = 0; c < TILE / 32; ++c) {
+    float v[32];
+    tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c * 32), v);
+    f(32 * q + lane, c * 32, v);
+  }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gram_tok_tc_kernel(const __grid_constant__ CUtensorMap tm, TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  Smem* S = (Smem*)(base + STAGES * 2 * TILE_BYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int u = blockIdx.y;
+  // upper-triangular tile (mi <= ni)
+  int mi = 0, idx = blockIdx.x;
+  while (idx >= a.nt - mi) { idx -= a.nt - mi; ++mi; }
+  const int ni = mi + idx;
+  const bool diag = (mi == ni);
+  const int nk = a.H * (a.D / KCH);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&S->accum), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), TILE);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  bool ok = true;
+
+  if (warp == 0 && lane == 0) {
+    const uint32_t bytes = diag ? TILE_BYTES : 2 * TILE_BYTES;
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % STAGES, r = kk / STAGES;
+      if (r > 0 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), (r - 1) & 1)) { ok = false; break; }
+      const int h = kk / (a.D / KCH), k0 = (kk % (a.D / KCH)) * KCH;
+      const uint32_t fb = tc::smem_u32(&S->full[s]);
+      tc::mbar_expect_tx(fb, bytes);
+      const uint32_t sa = tc::smem_u32(base + s * 2 * TILE_BYTES);
+      tc::tma_load_3d(sa, &tm, k0, mi * TILE, u * a.H + h, fb);
+      if (!diag) tc::tma_load_3d(sa + TILE_BYTES, &tm, k0, ni * TILE, u * a.H + h, fb);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = tc::idesc_bf16(TILE, TILE, 0, 0);
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % STAGES, r = kk / STAGES;
+      if (!tc::mbar_wait(tc::smem_u32(&S->full[s]), r & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(base + s * 2 * TILE_BYTES);
+      const uint32_t sb = diag ? sa : sa + TILE_BYTES;
+#pragma unroll
+      for (int k4 = 0; k4 < KCH / 16; ++k4) {
+        const uint64_t ad = tc::sdesc_sw128(sa + 32 * k4, 16, 1024);
+        const uint64_t bd = tc::sdesc_sw128(sb + 32 * k4, 16, 1024);
+        tc::mma_f16(tmem, ad, bd, idesc, (kk | k4) != 0);
+      }
+      tc::mma_commit(tc::smem_u32(&S->empty[s]));
+    }
+    tc::mma_commit(tc::smem_u32(&S->accum));
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    if (!tc::mbar_wait(tc::smem_u32(&S->accum), 0)) {
+      ok = false;
+    } else {
+      tc::tc_fence_after();
+      float* C = a.out + (long long)u * a.out_us;
+      const int T = a.T;
+      drain(tmem, q, [&](int rt, int c0, const float (&v)[32]) {
+        const int row = mi * TILE + rt;
+        if (row < T) {
+          float* cr = C + (long long)row * T + ni * TILE + c0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (ni * TILE + c0 + j < T) cr[j] = v[j];
+        }
+        if (!diag) {
+          // mirror: lanes hold consecutive rows, so each column is one
+          // coalesced 128-byte store
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = ni * TILE + c0 + j;
+            if (col < T && row < T) C[(long long)col * T + row] = v[j];
+          }
+        }
+      });
+    }
+  }
+  if (!ok) set_err(a, u);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, TILE);
+}
+
+// Feature Gram partials, D = 128: rows [s*rows_per, (s+1)*rows_per) of unit u.
+// One stage = 64 rows x 128 features in two 64-feature swizzle atoms (8 KB
+// each); the A and B operands are the same tile (MN-major, LBO = 8 KB between
+// the feature atoms, SBO = 1 KB between 8-row groups).
+__global__ void __launch_bounds__(TC_THREADS, 1)
+gram_feat_tc_kernel(const __grid_constant__ CUtensorMap tm, TcArgs a) {
+  constexpr int SBYTES = 2 * 64 * 128;   // 16 KB per stage
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  Smem* S = (Smem*)(base + STAGES * SBYTES);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int u = blockIdx.y, sp = blockIdx.x;
+  const long long row0 = (long long)u * a.H * a.T + (long long)sp * a.rows_per;
+  const int nk = a.rows_per / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&S->accum), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), TILE);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  bool ok = true;
+
+  if (warp == 0 && lane == 0) {
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % STAGES, r = kk / STAGES;
+      if (r > 0 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), (r - 1) & 1)) { ok = false; break; }
+      const uint32_t fb = tc::smem_u32(&S->full[s]);
+      tc::mbar_expect_tx(fb, SBYTES);
+      const uint32_t sa = tc::smem_u32(base + s * SBYTES);
+      const int rr = (int)(row0 + (long long)kk * 64);
+      tc::tma_load_2d(sa, &tm, 0, rr, fb);
+      tc::tma_load_2d(sa + SBYTES / 2, &tm, 64, rr, fb);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = tc::idesc_bf16(TILE, TILE, 1, 1);
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % STAGES, r = kk / STAGES;
+      if (!tc::mbar_wait(tc::smem_u32(&S->full[s]), r & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(base + s * SBYTES);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const uint64_t d = tc::sdesc_sw128(sa + 2048 * k4, SBYTES / 2, 1024);
+        tc::mma_f16(tmem, d, d, idesc, (kk | k4) != 0);
+      }
+      tc::mma_commit(tc::smem_u32(&S->empty[s]));
+    }
+    tc::mma_commit(tc::smem_u32(&S->accum));
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    if (!tc::mbar_wait(tc::smem_u32(&S->accum), 0)) {
+      ok = false;
+    } else {
+      tc::tc_fence_after();
+      float* P = a.out + (long long)u * a.out_us + (long long)sp * 128 * 128;
+      drain(tmem, q, [&](int rt, int c0, const float (&v)[32]) {
+        float4* pr = reinterpret_cast<float4*>(P + rt * 128 + c0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pr[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      });
+    }
+  }
+  if (!ok) set_err(a, u);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, TILE);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t tc_smem(int stage_bytes) { return (size_t)STAGES * stage_bytes + 1024 + sizeof(Smem) + 64; }
+
+}  // namespace
+
+bool gram_tc_supported(const Layout& L) {
+  return L.dtype == JOLT_BF16 && L.D == 128 && encode_fn() != nullptr;
+}
+
+// S_T[u] = sum_h X_h X_h^T for every unit, T x T fp32 at ws + u*ub + o_ST.
+jolt_status gram_tok_tc(const Layout& L, int U, const void* X, char* ws, cudaStream_t st) {
+  CUtensorMap tm;
+  const cuuint64_t dims[3] = {(cuuint64_t)L.D, (cuuint64_t)L.T, (cuuint64_t)U * L.H};
+  const cuuint64_t strides[2] = {(cuuint64_t)L.D * 2, (cuuint64_t)L.T * L.D * 2};
+  const cuuint32_t box[3] = {KCH, TILE, 1};
+  if (!make_map(&tm, X, 3, dims, strides, box)) return JOLT_ERR_CUDA;
+  TcArgs a;
+  a.T = L.T; a.D = L.D; a.H = L.H;
+  a.nt = (L.T + TILE - 1) / TILE;
+  a.rows_per = 0; a.nsplit = 0;
+  a.out = (float*)(ws + L.o_ST);
+  a.out_us = (long long)L.unit_bytes / 4;
+  a.ws = ws; a.ub = L.unit_bytes; a.o_status = L.o_status;
+  const size_t smem = tc_smem(2 * TILE_BYTES);
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(gram_tok_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr = true;
+  }
+  dim3 grid(a.nt * (a.nt + 1) / 2, U);
+  gram_tok_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tm, a);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+// Feature-Gram partials Sdp[u][s] (128 x 128 fp32) over L.nsplit row ranges.
+jolt_status gram_feat_tc(const Layout& L, int U, const void* X, char* ws, cudaStream_t st) {
+  const long long rows = (long long)U * L.H * L.T;
+  const int rows_per = (L.H / L.nsplit) * L.T;
+  if (rows_per % 64) return JOLT_ERR_INVALID;
+  CUtensorMap tm;
+  const cuuint64_t dims[2] = {(cuuint64_t)L.D, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)L.D * 2};
+  const cuuint32_t box[2] = {64, 64};
+  if (!make_map(&tm, X, 2, dims, strides, box)) return JOLT_ERR_CUDA;
+  TcArgs a;
+  a.T = L.T; a.D = L.D; a.H = L.H; a.nt = 0;
+  a.rows_per = rows_per; a.nsplit = L.nsplit;
+  a.out = (float*)(ws + L.o_Sdp);
+  a.out_us = (long long)L.unit_bytes / 4;
+  a.ws = ws; a.ub = L.unit_bytes; a.o_status = L.o_status;
+  const size_t smem = tc_smem(2 * 64 * 128);
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(gram_feat_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr = true;
+  }
+  dim3 grid(L.nsplit, U);
+  gram_feat_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tm, a);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+}  // namespace jolt

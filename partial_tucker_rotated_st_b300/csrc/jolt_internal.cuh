@@ -18,7 +18,8 @@ namespace jolt {
 enum : int {
   ST_NOCONVERGE = 1,
   ST_NONFINITE = 2,
-  ST_NOTPD = 4,  // Cholesky met a non-positive pivot (reported as NOCONVERGE)
+  ST_NOTPD = 4,     // Cholesky met a non-positive pivot (reported as NOCONVERGE)
+  ST_TIMEOUT = 8,   // a bounded device wait gave up (reported as JOLT_ERR_CUDA)
 };
 
 extern unsigned long long g_launches;
@@ -107,6 +108,11 @@ jolt_status launch_chol_inv(const float* G, long long g_bstride, int n, int batc
                             float* Rinv, long long r_bstride, int* status,
                             long long status_bstride, const int* skip, long long skip_stride,
                             bool f64, cudaStream_t st);
+
+// ------------------------------------------------------------------ tensor cores
+bool gram_tc_supported(const Layout& L);
+jolt_status gram_tok_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
+jolt_status gram_feat_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
 
 // ------------------------------------------------------------------ steps
 jolt_status factor_run(const Layout& L, int n_units, const void* X, const float* sketch,

@@ -361,3 +361,13 @@ def test_allocate_brute_force_tiny():
     # the duality gap to the true optimum at the budget is reported, not pinned
     gap = Dz - best_at(w.budget_bytes)
     assert gap >= -1e-12
+
+
+def test_fix_signs_rule():
+    V = np.array([[0.6, -0.8, 0.0], [-0.8, -0.6, 0.5], [0.0, 0.0, -0.5]])
+    F = jolt.fix_signs(V)
+    # column 0: |-0.8| largest -> flipped; column 1: |-0.8| -> flipped;
+    # column 2: tie 0.5 / -0.5 -> the lower index (+0.5) decides, unchanged
+    assert np.array_equal(F, np.array([[-0.6, 0.8, 0.0], [0.8, 0.6, 0.5], [0.0, 0.0, -0.5]]))
+    w, V2 = jolt.feature_mode(_small_tensor()[0])
+    assert np.all(V2[np.argmax(np.abs(V2), 0), np.arange(V2.shape[1])] > 0)
