@@ -77,10 +77,27 @@ __device__ void best_response(int U, int nc, const double* dist, const int64_t* 
 }
 
 __global__ void __launch_bounds__(AL_THREADS)
-alloc_kernel(int U, int nc, const double* __restrict__ dist, const int64_t* __restrict__ cost,
-             long long budget, int align, int32_t* choice, double* lambda, int32_t* status) {
-  extern __shared__ int zs[];
+alloc_kernel(int U, int nc, const double* __restrict__ gdist, const int64_t* __restrict__ gcost,
+             long long budget, int align, int32_t* choice, double* lambda, int32_t* status,
+             int cached) {
+  extern __shared__ __align__(16) unsigned char asm_raw[];
   __shared__ long long tot;
+  // tables copied into shared memory once when they fit (the bisection
+  // evaluates best responses up to a few hundred times)
+  const double* dist = gdist;
+  const int64_t* cost = gcost;
+  int* zs;
+  if (cached) {
+    double* sd = (double*)asm_raw;
+    int64_t* sc = (int64_t*)(sd + (size_t)U * nc);
+    for (int i = threadIdx.x; i < U * nc; i += blockDim.x) { sd[i] = gdist[i]; sc[i] = gcost[i]; }
+    dist = sd;
+    cost = sc;
+    zs = (int*)(sc + (size_t)U * nc);
+  } else {
+    zs = (int*)asm_raw;
+  }
+  __syncthreads();
   int* zhi = zs;            // [U]
   int* zmid = zs + U;       // [U]
   best_response(U, nc, dist, cost, 0.0, 0, zhi, &tot);
@@ -131,7 +148,10 @@ alloc_kernel(int U, int nc, const double* __restrict__ dist, const int64_t* __re
 jolt_status alloc_run(int U, int nc, const double* dist, const int64_t* cost, int64_t budget,
                       int align, int32_t* choice, double* lambda, int32_t* status,
                       cudaStream_t st) {
-  const size_t smem = (size_t)2 * U * sizeof(int);
+  const size_t ztab = (size_t)2 * U * sizeof(int);
+  const size_t tabs = (size_t)U * nc * (sizeof(double) + sizeof(int64_t));
+  const int cached = (tabs + ztab <= 150 * 1024) ? 1 : 0;
+  const size_t smem = cached ? tabs + ztab : ztab;
   if (smem > 160 * 1024) return JOLT_ERR_INVALID;
   static bool attr = false;
   if (!attr) {
@@ -140,7 +160,7 @@ jolt_status alloc_run(int U, int nc, const double* dist, const int64_t* cost, in
     attr = true;
   }
   alloc_kernel<<<1, AL_THREADS, smem, st>>>(U, nc, dist, cost, (long long)budget, align, choice,
-                                            lambda, status);
+                                            lambda, status, cached);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

@@ -75,6 +75,7 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
       return JOLT_ERR_INVALID;
     L.ell = RT + cfg->oversample;
     if (L.ell > 64 || L.ell > T) return JOLT_ERR_INVALID;
+    if (!(L.ell == 32 || L.ell == 40 || L.ell == 48 || L.ell == 64)) return JOLT_ERR_INVALID;
     // the sketch Z = A Omega needs at least ell independent columns of A
     for (int i = 0; i < L.nd; ++i)
       if ((long long)H * L.rd[i] < L.ell) return JOLT_ERR_INVALID;
@@ -83,10 +84,11 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
     if (T <= 128) {
       L.L = T;
     } else {
-      int w = RT + 8 > 2 * RT ? RT + 8 : 2 * RT;
-      w = (w + 7) / 8 * 8;
-      if (w > 128) w = 128;
-      if (w > T) w = T;
+      // block width: twice the largest token rank, one of the widths the
+      // row-parallel triangular solve is built for
+      int w = 2 * RT < 32 ? 32 : (2 * RT <= 40 ? 40 : (2 * RT <= 48 ? 48 : 64));
+      if (w < RT + 8) w = 64;
+      if (w > T) return JOLT_ERR_INVALID;
       L.L = w;
     }
   }
@@ -96,8 +98,14 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
     if (H % d == 0 && (long long)d * T <= 4096) hg = d;
   L.nsplit = H / hg;
   L.chunk = hg;
-  L.tile_rows = 64;
-  L.ntiles = H * ((T + 63) / 64);
+  L.ks = 1;
+  for (int d = 1; d <= 4; ++d)
+    if (T % d == 0 && T / d >= 32) L.ks = d;
+  L.hs = 1;
+  for (int d = 1; d <= 16; ++d)
+    if (H % d == 0) L.hs = d;
+  L.tile_rows = 8192 / D;     // sweep CTA rows: 8 warps x (32 / (D/16)) row groups x 2 rows
+  L.ntiles = H * ((T + L.tile_rows - 1) / L.tile_rows);
 
   const int Lw = (L.token_mode == JOLT_TOKEN_EXACT) ? L.L : L.ell;
   const bool iter = RT > 0 && (L.token_mode == JOLT_TOKEN_RANDOMIZED || T > 128);
@@ -120,15 +128,19 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   L.o_Y = sect((size_t)H * T * RD * 4);
   L.o_Y16 = sect((size_t)H * T * RD * 2);
   L.o_ST = sect((RT > 0 && L.token_mode == JOLT_TOKEN_EXACT) ? (size_t)T * T * 4 : 0);
+  const bool svtc = RT > 0 && L.token_mode == JOLT_TOKEN_EXACT && T > 128 && L.L == 64;
+  L.o_STs = svtc ? sect((size_t)T * T * 4) : 0;
+  L.o_Vs = svtc ? sect((size_t)2 * T * 64 * 4) : 0;   // V^T and its tf32 low part
   const size_t blk = iter ? (size_t)T * Lw * 4 : 0;
   L.o_V = sect(blk);
   L.o_Z = sect(blk);
   L.o_V2 = sect(blk);
   L.o_Z2 = sect(blk);
   const size_t sq = RT > 0 ? (size_t)Lw * Lw * 4 : 0;
-  L.o_Hm = sect(sq);
+  const int nparts = L.ks > L.hs ? L.ks : L.hs;
+  L.o_Hm = sect(sq * nparts);
   L.o_Wm = sect(sq);
-  L.o_Gram = sect(sq);
+  L.o_Gram = sect(sq * L.ks);
   L.o_Rinv = sect(sq);
   L.o_theta = sect((size_t)(Lw > T ? Lw : T) * 4);
   L.o_UT32 = sect((size_t)L.nd * T * RT * 4);

@@ -29,8 +29,9 @@ namespace jolt {
 
 namespace {
 
-constexpr int SUB_MAX_ITERS = 120;
-constexpr int SUB_CHECK_EVERY = 4;
+constexpr int SUB_STEPS = 5;        // power steps between Rayleigh-Ritz checks
+constexpr float SUB_SHIFT = 1e-5f;  // shift of the equilibrated first CholeskyQR pass (f32)
+constexpr int SUB_MAX_BLOCKS = 25;
 constexpr float RITZ_TOL_REL = 1e-4f;
 constexpr float RITZ_TOL_ABS = 1e-5f;
 
@@ -76,8 +77,8 @@ __global__ void init_block_kernel(char* ws, size_t ub, size_t o_V, int n) {
 //   Ritz vectors go to U (T x k) and theta to ev.  Z2's columns are then
 //   scaled by 1/||Z2_i|| (equilibration before CholeskyQR; the span is kept).
 __global__ void ritz_check_kernel(char* ws, size_t ub, size_t o_V2, size_t o_Z2, size_t o_th,
-                                  size_t o_U, size_t o_ev, size_t o_flag, size_t o_status, int T,
-                                  int Lw, int k, int last) {
+                                  size_t o_U, size_t o_ev, size_t o_flag, size_t o_status,
+                                  size_t o_V, int T, int Lw, int k, int last) {
   const int u = blockIdx.x;
   char* base = ws + u * ub;
   int* flag = (int*)(base + o_flag);
@@ -85,24 +86,32 @@ __global__ void ritz_check_kernel(char* ws, size_t ub, size_t o_V2, size_t o_Z2,
   const float* V2 = (const float*)(base + o_V2);
   float* Z2 = (float*)(base + o_Z2);
   const float* th = (const float*)(base + o_th);
+  __shared__ float pr[512], pz[512];
   __shared__ float res[128], nz[128];
-  __shared__ int ok;
-  const int t = threadIdx.x, w = t / 32, lane = t % 32, nw = blockDim.x / 32;
-  for (int i = w; i < Lw; i += nw) {
-    float r = 0.f, z = 0.f;
-    const float ti = th[i];
-    for (int row = lane; row < T; row += 32) {
-      const float zz = Z2[(long long)row * Lw + i];
-      const float d = zz - ti * V2[(long long)row * Lw + i];
+  __shared__ int ok, nonfinite;
+  const int t = threadIdx.x;
+  const int G = blockDim.x / Lw;          // row groups
+  const int g = t / Lw, c = t % Lw;
+  float r = 0.f, z = 0.f;
+  if (g < G) {
+    const float ti = th[c];
+    for (int row = g; row < T; row += G) {
+      const float zz = Z2[(long long)row * Lw + c];
+      const float d = zz - ti * V2[(long long)row * Lw + c];
       r = fmaf(d, d, r);
       z = fmaf(zz, zz, z);
     }
-    r = warp_sum(r);
-    z = warp_sum(z);
-    if (lane == 0) { res[i] = sqrtf(r); nz[i] = sqrtf(z); }
+  }
+  pr[t] = r;
+  pz[t] = z;
+  __syncthreads();
+  if (t < Lw) {
+    float a = 0.f, b = 0.f;
+    for (int q = 0; q < G; ++q) { a += pr[q * Lw + t]; b += pz[q * Lw + t]; }
+    res[t] = sqrtf(a);
+    nz[t] = sqrtf(b);
   }
   __syncthreads();
-  __shared__ int nonfinite;
   if (t == 0) {
     int good = 1, nf = !isfinite(th[0]);
     const float a = RITZ_TOL_ABS * fabsf(th[0]);
@@ -125,14 +134,12 @@ __global__ void ritz_check_kernel(char* ws, size_t ub, size_t o_V2, size_t o_Z2,
   if (ok || last) {
     float* U = (float*)(base + o_U);
     for (long long e = t; e < (long long)T * k; e += blockDim.x) {
-      const int row = (int)(e / k), c = (int)(e % k);
-      U[e] = V2[(long long)row * Lw + c];
+      const int row = (int)(e / k), cc = (int)(e % k);
+      U[e] = V2[(long long)row * Lw + cc];
     }
-    // the host swaps the roles of the V and Z2 buffers after every step, and
-    // a converged unit skips the re-orthonormalisation: leave the
-    // orthonormal Ritz basis in Z2 too, so that either buffer warm-starts
-    // the next feature rank with an orthonormal block
-    for (long long e = t; e < (long long)T * Lw; e += blockDim.x) Z2[e] = V2[e];
+    // the orthonormal Ritz basis warm-starts the next feature rank
+    float* V = (float*)(base + o_V);
+    for (long long e = t; e < (long long)T * Lw; e += blockDim.x) V[e] = V2[e];
     float* ev = (float*)(base + o_ev);
     for (int i = t; i < k; i += blockDim.x) ev[i] = th[i];
     if (t == 0) {
@@ -141,10 +148,11 @@ __global__ void ritz_check_kernel(char* ws, size_t ub, size_t o_V2, size_t o_Z2,
     }
     return;
   }
+  // equilibrate the columns of Z2 before the next orthonormalisation
   for (long long e = t; e < (long long)T * Lw; e += blockDim.x) {
-    const int c = (int)(e % Lw);
-    const float s = nz[c] > 0.f ? 1.f / nz[c] : 0.f;
-    Z2[e] *= s;
+    const int cc = (int)(e % Lw);
+    const float sc = nz[cc] > 0.f ? 1.f / nz[cc] : 0.f;
+    Z2[e] *= sc;
   }
 }
 
@@ -194,30 +202,37 @@ GemmDesc gd(int M, int N, int K, int nseg, int nb1, int nb2, Opnd A, Opnd B, flo
   } while (0)
 
 
-// a <- orth(a) by CholeskyQR2 (Fukaya et al. 2014), b is scratch; T x Lw per unit.
-jolt_status cholqr2_inplace(const F& c, int T, int Lw, size_t o_a, size_t o_b, const int* skip,
-                            bool f64) {
+// dst <- orth(src) by CholeskyQR through mid; T x Lw per unit.  passes = 2
+// is CholeskyQR2 (Fukaya et al. 2014); `shift` > 0 shifts the first pass
+// (shifted CholeskyQR, Fukaya et al. 2020) for nearly dependent columns.
+// Each pass: Gram split over L.ks row chunks (the partials are summed inside
+// the Cholesky kernel), Cholesky R, then out = in R^{-1} row by row.  With
+// one pass the result goes straight to dst.  src and dst may be the same.
+jolt_status cholqr(const F& c, int T, int Lw, size_t src, size_t mid, size_t dst, const int* skip,
+                   bool f64, int passes, float shift) {
   const Layout& L = c.L;
   const long long ub4 = (long long)L.unit_bytes / 4;
-  const long long sks = ub4;
-  size_t src = o_a, dst = o_b;
-  for (int pass = 0; pass < 2; ++pass) {
-    GemmDesc g = gd(Lw, Lw, T, 1, c.U, 1, opnd(c.ws + src, JOLT_F32, 1, Lw, 0, ub4),
-                    opnd(c.ws + src, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Gram), Lw, 1, ub4, 0, 0.f,
-                    skip);
-    g.skip_stride = sks;
+  const int ks = L.ks, kc = T / L.ks;
+  const size_t ins[2] = {src, mid}, outs[2] = {passes == 1 ? dst : mid, dst};
+  for (int pass = 0; pass < passes; ++pass) {
+    GemmDesc g = gd(Lw, Lw, kc, 1, c.U, ks,
+                    opnd(c.ws + ins[pass], JOLT_F32, 1, Lw, 0, ub4, (long long)kc * Lw),
+                    opnd(c.ws + ins[pass], JOLT_F32, Lw, 1, 0, ub4, (long long)kc * Lw),
+                    c.f(L.o_Gram), Lw, 1, ub4, (long long)Lw * Lw, 0.f, skip);
+    g.skip_stride = ub4;
     TRY(launch_gemm(g, c.st));
-    TRY(launch_chol_inv(c.f(L.o_Gram), ub4, Lw, c.U, c.f(L.o_Rinv), ub4, (int*)(c.ws + L.o_status),
-                        ub4, skip, sks, f64, c.st));
-    g = gd(T, Lw, Lw, 1, c.U, 1, opnd(c.ws + src, JOLT_F32, Lw, 1, 0, ub4),
-           opnd(c.ws + L.o_Rinv, JOLT_F32, Lw, 1, 0, ub4), c.f(dst), Lw, 1, ub4, 0, 0.f, skip);
-    g.skip_stride = sks;
-    TRY(launch_gemm(g, c.st));
-    const size_t tmp = src;
-    src = dst;
-    dst = tmp;
+    TRY(launch_chol(c.f(L.o_Gram), ub4, Lw, ks, (long long)Lw * Lw, c.U, c.f(L.o_Rinv), ub4,
+                    (int*)(c.ws + L.o_status), ub4, skip, ub4, f64, pass == 0 ? shift : 0.f,
+                    c.st));
+    TRY(launch_trsm_rows(c.f(ins[pass]), c.f(outs[pass]), ub4, c.f(L.o_Rinv), ub4, T, Lw, c.U,
+                         skip, ub4, c.st));
   }
-  return JOLT_OK;  // two passes: the result is back in o_a
+  return JOLT_OK;
+}
+
+jolt_status cholqr2(const F& c, int T, int Lw, size_t src, size_t mid, size_t dst,
+                    const int* skip, bool f64) {
+  return cholqr(c, T, Lw, src, mid, dst, skip, f64, 2, f64 ? 0.f : SUB_SHIFT);
 }
 
 jolt_status read_flags_all(const F& c, bool* all) {
@@ -265,7 +280,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     reduce_splits_kernel<<<dim3(blocks_for(D * D), U), 256, 0, st>>>(ws, ub, L.o_Sdp, L.o_Sd,
                                                                      L.nsplit, D * D);
     JOLT_LAUNCH_CHECK();
-    TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
+    TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, 1, 0, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
                       status, ub4, nullptr, 0, st));
   }
   if (RD > 0) {
@@ -284,7 +299,6 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   // ---- token mode, one feature rank at a time
   const bool exact = (L.token_mode == JOLT_TOKEN_EXACT);
   const int Lw = exact ? L.L : L.ell;
-  size_t oV = L.o_V, oZ = L.o_Z, oV2 = L.o_V2, oZ2 = L.o_Z2;
   bool st_started = false, sub_started = false;
   int prev = 0;
   for (int id = 0; id < L.nd; ++id) {
@@ -318,93 +332,109 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       }
       if (T <= 128) {
         // direct solve of the whole token Gram
-        TRY(launch_jacobi(c.f(L.o_ST), ub4, T, T, U, c.f(L.o_theta), ub4, c.f(oUT), ub4, RT, RT,
-                          status, ub4, nullptr, 0, st));
+        TRY(launch_jacobi(c.f(L.o_ST), ub4, T, T, 1, 0, U, c.f(L.o_theta), ub4, c.f(oUT), ub4, RT,
+                          RT, status, ub4, nullptr, 0, st));
         copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, T, oEV, 1,
                                                                   RT);
         JOLT_LAUNCH_CHECK();
       } else {
         if (!sub_started) {
-          init_block_kernel<<<dim3(blocks_for((long long)T * Lw), U), 256, 0, st>>>(ws, ub, oV,
+          init_block_kernel<<<dim3(blocks_for((long long)T * Lw), U), 256, 0, st>>>(ws, ub, L.o_V,
                                                                                    T * Lw);
           JOLT_LAUNCH_CHECK();
-          set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_flag, 0);
-          JOLT_LAUNCH_CHECK();
-          TRY(cholqr2_inplace(c, T, Lw, oV, oZ, nullptr, false));
+          TRY(cholqr2(c, T, Lw, L.o_V, L.o_V2, L.o_V, nullptr, false));
           sub_started = true;
         }
         set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_flag, 0);
         JOLT_LAUNCH_CHECK();
-        for (int it = 0; it < SUB_MAX_ITERS; ++it) {
+        const bool svtc = sv_tc_supported(L);
+        if (svtc) TRY(split_tok_gram(L, U, ws, st));
+        // blocks of SUB_STEPS power steps V <- orth(S V), then Rayleigh-Ritz
+        // and the residual test; converged units are skipped from then on
+        for (int blk = 0; blk < SUB_MAX_BLOCKS; ++blk) {
           GemmDesc g;
-          // Z = S V
-          g = gd(T, Lw, T, 1, U, 1, opnd(ws + L.o_ST, JOLT_F32, T, 1, 0, ub4),
-                 opnd(ws + oV, JOLT_F32, Lw, 1, 0, ub4), c.f(oZ), Lw, 1, ub4, 0, 0.f, flags);
+          auto apply_S = [&]() -> jolt_status {  // Z = S V
+            if (svtc) return sv_tc(L, U, ws, flags, st);
+            GemmDesc gg = gd(T, Lw, T, 1, U, 1, opnd(ws + L.o_ST, JOLT_F32, T, 1, 0, ub4),
+                             opnd(ws + L.o_V, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Z), Lw, 1, ub4, 0,
+                             0.f, flags);
+            gg.skip_stride = ub4;
+            return launch_gemm(gg, st);
+          };
+          // one shifted CholeskyQR pass per power step; the last step of a
+          // block takes two so that Rayleigh-Ritz sees an orthonormal basis
+          for (int p = 0; p < SUB_STEPS; ++p) {
+            TRY(apply_S());
+            TRY(cholqr(c, T, Lw, L.o_Z, L.o_V2, L.o_V, flags, false, p == SUB_STEPS - 1 ? 2 : 1,
+                       SUB_SHIFT));
+          }
+          TRY(apply_S());
+          // H = V^T Z, split over row chunks; the Jacobi kernel sums the partials
+          const int kc = T / L.ks;
+          g = gd(Lw, Lw, kc, 1, U, L.ks, opnd(ws + L.o_V, JOLT_F32, 1, Lw, 0, ub4, (long long)kc * Lw),
+                 opnd(ws + L.o_Z, JOLT_F32, Lw, 1, 0, ub4, (long long)kc * Lw), c.f(L.o_Hm), Lw, 1,
+                 ub4, (long long)Lw * Lw, 0.f, flags);
           g.skip_stride = ub4;
           TRY(launch_gemm(g, st));
-          // H = V^T Z
-          g = gd(Lw, Lw, T, 1, U, 1, opnd(ws + oV, JOLT_F32, 1, Lw, 0, ub4),
-                 opnd(ws + oZ, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Hm), Lw, 1, ub4, 0, 0.f, flags);
-          g.skip_stride = ub4;
-          TRY(launch_gemm(g, st));
-          TRY(launch_jacobi(c.f(L.o_Hm), ub4, Lw, Lw, U, c.f(L.o_theta), ub4, c.f(L.o_Wm), ub4,
-                            Lw, Lw, status, ub4, flags, ub4, st));
+          TRY(launch_jacobi(c.f(L.o_Hm), ub4, Lw, Lw, L.ks, (long long)Lw * Lw, U, c.f(L.o_theta),
+                            ub4, c.f(L.o_Wm), ub4, Lw, Lw, status, ub4, flags, ub4, st));
           // Ritz vectors V2 = V W and Z2 = Z W = S V2
-          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + oV, JOLT_F32, Lw, 1, 0, ub4),
-                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(oV2), Lw, 1, ub4, 0, 0.f, flags);
+          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + L.o_V, JOLT_F32, Lw, 1, 0, ub4),
+                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_V2), Lw, 1, ub4, 0, 0.f, flags);
           g.skip_stride = ub4;
           TRY(launch_gemm(g, st));
-          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + oZ, JOLT_F32, Lw, 1, 0, ub4),
-                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(oZ2), Lw, 1, ub4, 0, 0.f, flags);
+          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + L.o_Z, JOLT_F32, Lw, 1, 0, ub4),
+                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Z2), Lw, 1, ub4, 0, 0.f, flags);
           g.skip_stride = ub4;
           TRY(launch_gemm(g, st));
-          const int last = (it == SUB_MAX_ITERS - 1);
-          ritz_check_kernel<<<U, 256, 0, st>>>(ws, ub, oV2, oZ2, L.o_theta, oUT, oEV, L.o_flag,
-                                               L.o_status, T, Lw, RT, last);
+          const int last = (blk == SUB_MAX_BLOCKS - 1);
+          ritz_check_kernel<<<U, 512, 0, st>>>(ws, ub, L.o_V2, L.o_Z2, L.o_theta, oUT, oEV,
+                                               L.o_flag, L.o_status, L.o_V, T, Lw, RT, last);
           JOLT_LAUNCH_CHECK();
           if (last) break;
-          TRY(cholqr2_inplace(c, T, Lw, oZ2, oV, flags, false));
-          std::swap(oV, oZ2);
-          if ((it + 1) % SUB_CHECK_EVERY == 0) {
-            bool all = false;
-            TRY(read_flags_all(c, &all));
-            if (all) break;
-          }
+          // next block starts from orth(Z2), Z2 equilibrated by the check
+          TRY(cholqr2(c, T, Lw, L.o_Z2, L.o_V2, L.o_V, flags, false));
+          bool all = false;
+          TRY(read_flags_all(c, &all));
+          if (all) break;
         }
       }
     } else {
       // FlashJoLT randomized range finder with q power steps
       const int ell = L.ell;
       const long long sk_h = (long long)D * ell, sk_u = (long long)H * D * ell;
-      size_t oQ = oZ, oS = oV;
+      // Q lives in V: Z = A Omega, Q = orth(Z); then q times Q = orth(A (A^T Q))
       TRY(launch_gemm(gd(T, ell, rdv, H, U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
-                         opnd(sketch, JOLT_F32, ell, 1, sk_h, sk_u), c.f(oQ), ell, 1, ub4, 0),
+                         opnd(sketch, JOLT_F32, ell, 1, sk_h, sk_u), c.f(L.o_Z), ell, 1, ub4, 0),
                       st));
-      TRY(cholqr2_inplace(c, T, ell, oQ, oS, nullptr, true));
+      TRY(cholqr2(c, T, ell, L.o_Z, L.o_V2, L.o_V, nullptr, true));
       for (int q = 0; q <= L.power_iters; ++q) {
         // P_h = A_h^T Q  (rdv x ell per head)
         TRY(launch_gemm(gd(rdv, ell, T, 1, U, H, opnd(Ab, adt, 1, as_t, 0, aub, aseg),
-                           opnd(ws + oQ, JOLT_F32, ell, 1, 0, ub4, 0), c.f(L.o_P), ell, 1, ub4,
+                           opnd(ws + L.o_V, JOLT_F32, ell, 1, 0, ub4, 0), c.f(L.o_P), ell, 1, ub4,
                            (long long)rdv * ell),
                         st));
         if (q == L.power_iters) break;
         // Z = sum_h A_h P_h, re-orthonormalised
         TRY(launch_gemm(gd(T, ell, rdv, H, U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
                            opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4),
-                           c.f(oS), ell, 1, ub4, 0),
+                           c.f(L.o_Z), ell, 1, ub4, 0),
                         st));
-        TRY(cholqr2_inplace(c, T, ell, oS, oQ, nullptr, true));
-        std::swap(oQ, oS);
+        TRY(cholqr2(c, T, ell, L.o_Z, L.o_V2, L.o_V, nullptr, true));
       }
-      // Rayleigh-Ritz: B B^T with B = Q^T A, i.e. sum_h P_h^T P_h
-      TRY(launch_gemm(gd(ell, ell, rdv, H, U, 1,
-                         opnd(ws + L.o_P, JOLT_F32, 1, ell, (long long)rdv * ell, ub4),
-                         opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4),
-                         c.f(L.o_Hm), ell, 1, ub4, 0),
+      // Rayleigh-Ritz: B B^T with B = Q^T A, i.e. sum_h P_h^T P_h, split over
+      // head groups; the Jacobi kernel sums the partials
+      const int hs = L.hs, hper = H / L.hs;
+      TRY(launch_gemm(gd(ell, ell, rdv, hper, U, hs,
+                         opnd(ws + L.o_P, JOLT_F32, 1, ell, (long long)rdv * ell, ub4,
+                              (long long)hper * rdv * ell),
+                         opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4,
+                              (long long)hper * rdv * ell),
+                         c.f(L.o_Hm), ell, 1, ub4, (long long)ell * ell),
                       st));
-      TRY(launch_jacobi(c.f(L.o_Hm), ub4, ell, ell, U, c.f(L.o_theta), ub4, c.f(L.o_Wm), ub4, ell,
-                        RT, status, ub4, nullptr, 0, st));
-      TRY(launch_gemm(gd(T, RT, ell, 1, U, 1, opnd(ws + oQ, JOLT_F32, ell, 1, 0, ub4),
+      TRY(launch_jacobi(c.f(L.o_Hm), ub4, ell, ell, hs, (long long)ell * ell, U, c.f(L.o_theta),
+                        ub4, c.f(L.o_Wm), ub4, ell, RT, status, ub4, nullptr, 0, st));
+      TRY(launch_gemm(gd(T, RT, ell, 1, U, 1, opnd(ws + L.o_V, JOLT_F32, ell, 1, 0, ub4),
                          opnd(ws + L.o_Wm, JOLT_F32, ell, 1, 0, ub4), c.f(oUT), RT, 1, ub4, 0),
                       st));
       copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, ell, oEV, 1, RT);

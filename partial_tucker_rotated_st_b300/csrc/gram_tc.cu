@@ -236,6 +236,155 @@ gram_feat_tc_kernel(const __grid_constant__ CUtensorMap tm, TcArgs a) {
   if (warp == 1) tc::tmem_dealloc(tmem, TILE);
 }
 
+// Z[u] (T x L) = S[u] (T x T) V[u] (T x L) on kind::tf32 with three
+// products: S V + S V_lo + S_lo V, where x_lo = x - trunc_tf32(x) is exact in
+// fp32; the dropped S_lo V_lo and the truncation of the lo parts leave about
+// 2^-21 relative error per product, the size of fp32 accumulation itself.
+// One CTA per 128-row tile of one unit.  Both operands are K-major: S rows,
+// and V^T (64 x T) written by split_v_kernel.
+constexpr int SV_STAGES = 3;
+constexpr int SV_A = TILE * 32 * 4;          // 16 KB: 128 rows x 32 k (fp32)
+constexpr int SV_B = 64 * 32 * 4;            // 8 KB: 64 rows (n) x 32 k
+constexpr int SV_STAGE = 2 * SV_A + 2 * SV_B;
+
+struct SvArgs {
+  int T, L;
+  float* Z;
+  long long z_us;      // floats
+  const int* flags;
+  long long f_us;      // ints
+  char* ws;
+  size_t ub, o_status;
+};
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+sv_tc_kernel(const __grid_constant__ CUtensorMap tS, const __grid_constant__ CUtensorMap tSl,
+             const __grid_constant__ CUtensorMap tV, const __grid_constant__ CUtensorMap tVl,
+             SvArgs a) {
+  const int u = blockIdx.y, mi = blockIdx.x;
+  if (a.flags && a.flags[u * a.f_us]) return;
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  struct Bars { uint64_t full[SV_STAGES], empty[SV_STAGES], accum; uint32_t tmem; };
+  Bars* S = (Bars*)(base + SV_STAGES * SV_STAGE);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int nk = (a.T + 31) / 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < SV_STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&S->accum), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), 64);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % SV_STAGES, r = kk / SV_STAGES;
+      if (r > 0 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), (r - 1) & 1)) { ok = false; break; }
+      const uint32_t fb = tc::smem_u32(&S->full[s]);
+      tc::mbar_expect_tx(fb, SV_STAGE);
+      const uint32_t sa = tc::smem_u32(base + s * SV_STAGE);
+      tc::tma_load_3d(sa, &tS, kk * 32, mi * TILE, u, fb);
+      tc::tma_load_3d(sa + SV_A, &tSl, kk * 32, mi * TILE, u, fb);
+      tc::tma_load_3d(sa + 2 * SV_A, &tV, kk * 32, 0, u, fb);
+      tc::tma_load_3d(sa + 2 * SV_A + SV_B, &tVl, kk * 32, 0, u, fb);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // kind::tf32, fp32 accumulate, A and B K-major, M = 128, N = 64
+    constexpr uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                               ((uint32_t)(64 >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % SV_STAGES, r = kk / SV_STAGES;
+      if (!tc::mbar_wait(tc::smem_u32(&S->full[s]), r & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(base + s * SV_STAGE);
+      const uint32_t sb = sa + 2 * SV_A;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const uint64_t ah = tc::sdesc_sw128(sa + 32 * k4, 16, 1024);
+        const uint64_t al = tc::sdesc_sw128(sa + SV_A + 32 * k4, 16, 1024);
+        const uint64_t bh = tc::sdesc_sw128(sb + 32 * k4, 16, 1024);
+        const uint64_t bl = tc::sdesc_sw128(sb + SV_B + 32 * k4, 16, 1024);
+        tc::mma_tf32(tmem, ah, bh, idesc, (kk | k4) != 0);
+        tc::mma_tf32(tmem, ah, bl, idesc, 1);
+        tc::mma_tf32(tmem, al, bh, idesc, 1);
+      }
+      tc::mma_commit(tc::smem_u32(&S->empty[s]));
+    }
+    tc::mma_commit(tc::smem_u32(&S->accum));
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    if (!tc::mbar_wait(tc::smem_u32(&S->accum), 0)) {
+      ok = false;
+    } else {
+      tc::tc_fence_after();
+      const int row = mi * TILE + 32 * q + lane;
+      float* zr = a.Z + (long long)u * a.z_us + (long long)row * 64;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        float v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(c * 32), v);
+        if (row < a.T) {
+          float4* z4 = reinterpret_cast<float4*>(zr + c * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) z4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+      }
+    }
+  }
+  if (!ok) atomicOr((int*)(a.ws + (size_t)u * a.ub + a.o_status), ST_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 64);
+}
+
+// lo[i] = x[i] - trunc_tf32(x[i]) over n floats per unit.
+__global__ void tf32_lo_kernel(const char* ws, size_t ub, size_t o_in, size_t o_out, long long n,
+                               const int* flags, long long f_us) {
+  const int u = blockIdx.y;
+  if (flags && flags[u * f_us]) return;
+  const float* x = (const float*)(ws + (size_t)u * ub + o_in);
+  float* y = (float*)((char*)ws + (size_t)u * ub + o_out);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float v = x[i];
+    y[i] = v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+  }
+}
+
+// V^T and its tf32 low part (64 x T each) from V (T x 64), via a 32 x 32
+// shared-memory transpose per block.
+__global__ void split_v_kernel(const char* ws, size_t ub, size_t o_V, size_t o_Vt, size_t o_Vtl,
+                               int T, const int* flags, long long f_us) {
+  const int u = blockIdx.z;
+  if (flags && flags[u * f_us]) return;
+  __shared__ float tile[32][33];
+  const float* V = (const float*)(ws + (size_t)u * ub + o_V);
+  float* Vt = (float*)((char*)ws + (size_t)u * ub + o_Vt);
+  float* Vtl = (float*)((char*)ws + (size_t)u * ub + o_Vtl);
+  const int t0 = blockIdx.x * 32, n0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8
+  for (int r = ty; r < 32; r += 8) {
+    const int t = t0 + r;
+    tile[r][tx] = t < T ? V[(long long)t * 64 + n0 + tx] : 0.f;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int n = n0 + r, t = t0 + tx;
+    if (t < T) {
+      const float v = tile[tx][r];
+      Vt[(long long)n * T + t] = v;
+      Vtl[(long long)n * T + t] = v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+    }
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -250,11 +399,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box,
+  return fn(m, dt, rank, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -319,6 +469,59 @@ jolt_status gram_feat_tc(const Layout& L, int U, const void* X, char* ws, cudaSt
   }
   dim3 grid(L.nsplit, U);
   gram_feat_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tm, a);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+bool sv_tc_supported(const Layout& L) {
+  return L.L == 64 && L.T % 4 == 0 && encode_fn() != nullptr && L.o_STs != 0;
+}
+
+// S_lo = S - trunc_tf32(S) for every unit (after S_T is final for an r_d).
+jolt_status split_tok_gram(const Layout& L, int U, char* ws, cudaStream_t st) {
+  dim3 grid(256, U);
+  tf32_lo_kernel<<<grid, 256, 0, st>>>(ws, L.unit_bytes, L.o_ST, L.o_STs, (long long)L.T * L.T,
+                                       nullptr, 0);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+// Z = S V for every unit not flagged (T x 64 blocks at o_V / o_Z).
+jolt_status sv_tc(const Layout& L, int U, char* ws, const int* flags, cudaStream_t st) {
+  const size_t ub = L.unit_bytes;
+  dim3 g2((L.T + 31) / 32, 2, U);
+  split_v_kernel<<<g2, dim3(32, 8), 0, st>>>(ws, ub, L.o_V, L.o_Vs, L.o_Vs + (size_t)L.T * 64 * 4,
+                                             L.T, flags, (long long)ub / 4);
+  JOLT_LAUNCH_CHECK();
+  CUtensorMap tS, tSl, tV, tVl;
+  const cuuint64_t dS[3] = {(cuuint64_t)L.T, (cuuint64_t)L.T, (cuuint64_t)U};
+  const cuuint64_t sS[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)ub};
+  const cuuint32_t bS[3] = {32, TILE, 1};
+  const cuuint64_t dV[3] = {(cuuint64_t)L.T, 64, (cuuint64_t)U};
+  const cuuint64_t sV[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)ub};
+  const cuuint32_t bV[3] = {32, 64, 1};
+  const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!make_map(&tS, ws + L.o_ST, 3, dS, sS, bS, f32) ||
+      !make_map(&tSl, ws + L.o_STs, 3, dS, sS, bS, f32) ||
+      !make_map(&tV, ws + L.o_Vs, 3, dV, sV, bV, f32) ||
+      !make_map(&tVl, ws + L.o_Vs + (size_t)L.T * 64 * 4, 3, dV, sV, bV, f32))
+    return JOLT_ERR_CUDA;
+  SvArgs a;
+  a.T = L.T; a.L = 64;
+  a.Z = (float*)(ws + L.o_Z);
+  a.z_us = (long long)ub / 4;
+  a.flags = flags;
+  a.f_us = (long long)ub / 4;
+  a.ws = ws; a.ub = ub; a.o_status = L.o_status;
+  const size_t smem = (size_t)SV_STAGES * SV_STAGE + 1024 + 256;
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(sv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem));
+    attr = true;
+  }
+  dim3 grid((L.T + TILE - 1) / TILE, U);
+  sv_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tS, tSl, tV, tVl, a);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

@@ -59,6 +59,8 @@ struct Layout {
   int ell;        // sketch width RT + oversample (randomized mode)
   int power_iters;
   int nsplit, chunk;     // feature-Gram split over rows
+  int ks;                // row chunks of the small Grams (divides T)
+  int hs;                // head groups of the randomized Rayleigh-Ritz Gram (divides H)
   int tile_rows;         // sweep rows per CTA
   int ntiles;            // sweep CTAs per unit
   int ncand;
@@ -67,6 +69,7 @@ struct Layout {
   size_t o_status, o_Sd, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16, o_ST;
   size_t o_V, o_Z, o_V2, o_Z2, o_Hm, o_Wm, o_theta, o_Gram, o_Rinv, o_flag;
   size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
+  size_t o_STs, o_Vs;    // tf32 low parts of S_T and V (tensor-core S V)
   size_t unit_bytes;
 };
 
@@ -94,25 +97,33 @@ jolt_status launch_gemm(const GemmDesc& g, cudaStream_t st);
 
 // ------------------------------------------------------------------ eigen
 // Batched cyclic Jacobi (one CTA per symmetric n x n matrix, n <= 128).
-// in: A[b] at A + b*a_bstride, row stride lda.  out: evals[b][n] descending,
-// evecs[b] with column i the i-th eigenvector (row stride ldv).
-jolt_status launch_jacobi(const float* A, long long a_bstride, int lda, int n, int batch,
-                          float* evals, long long e_bstride, float* evecs,
-                          long long v_bstride, int ldv, int ncols_out, int* status,
+// in: A[b] = sum over nparts partials at A + b*a_bstride + k*part_s, row
+// stride lda.  out: evals[b][n] descending, evecs[b] with column i the i-th
+// eigenvector (row stride ldv, first ncols_out columns written).
+jolt_status launch_jacobi(const float* A, long long a_bstride, int lda, int n, int nparts,
+                          long long part_s, int batch, float* evals, long long e_bstride,
+                          float* evecs, long long v_bstride, int ldv, int ncols_out, int* status,
                           long long status_bstride, const int* skip, long long skip_stride,
                           cudaStream_t st);
-// Batched inverse Cholesky factor: G = R^T R (n x n, n <= 128), writes R^{-1}
-// (upper triangular, f32).  Arithmetic in f64 (n <= 64) when f64 is set, for
-// poorly conditioned sketches; f32 for equilibrated, near-orthogonal blocks.
-jolt_status launch_chol_inv(const float* G, long long g_bstride, int n, int batch,
-                            float* Rinv, long long r_bstride, int* status,
-                            long long status_bstride, const int* skip, long long skip_stride,
-                            bool f64, cudaStream_t st);
+// Batched Cholesky G = R^T R of a sum of nparts partials (n x n, n <= 128;
+// n <= 64 in f64), writes the upper factor R in f32.  The Gram is
+// equilibrated to a unit diagonal first; `shift` is added to that diagonal.
+jolt_status launch_chol(const float* G, long long g_bstride, int n, int nparts, long long part_s,
+                        int batch, float* R, long long r_bstride, int* status,
+                        long long status_bstride, const int* skip, long long skip_stride,
+                        bool f64, float shift, cudaStream_t st);
+// Out[b] = In[b] R[b]^{-1} for a T x n block per batch entry, row-parallel.
+jolt_status launch_trsm_rows(const float* In, float* Out, long long blk_bstride, const float* R,
+                             long long r_bstride, int T, int n, int batch, const int* skip,
+                             long long skip_stride, cudaStream_t st);
 
 // ------------------------------------------------------------------ tensor cores
 bool gram_tc_supported(const Layout& L);
 jolt_status gram_tok_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
 jolt_status gram_feat_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
+bool sv_tc_supported(const Layout& L);
+jolt_status split_tok_gram(const Layout& L, int n_units, char* ws, cudaStream_t st);
+jolt_status sv_tc(const Layout& L, int n_units, char* ws, const int* flags, cudaStream_t st);
 
 // ------------------------------------------------------------------ steps
 jolt_status factor_run(const Layout& L, int n_units, const void* X, const float* sketch,

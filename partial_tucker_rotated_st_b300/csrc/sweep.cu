@@ -29,9 +29,9 @@ namespace jolt {
 namespace {
 
 constexpr int SW_WARPS = 8;
-constexpr int SW_ROWS = 8;                       // rows per warp
-constexpr int SW_TILE = SW_WARPS * SW_ROWS;      // 64 rows per CTA
 constexpr int SW_THREADS = SW_WARPS * 32;
+constexpr int SW_EPT = 16;   // features per lane
+constexpr int SW_RPT = 2;    // rows per thread
 
 struct SweepArgs {
   const void* X;
@@ -41,149 +41,207 @@ struct SweepArgs {
   int H, T, D, dtype;
   int nT, nd, nb, nTt, ndt, RT, RD, hasFullT, hasFullD;
   int rT[JOLT_MAX_GRID], rd[JOLT_MAX_GRID], b[4];
+  float rq[4];         // 1 / (2^(b-1) - 1) for b > 0
   int ncand, tiles_t;
   size_t o_UT16, o_W, o_Y16, o_QUd, o_part;
 };
 
-template <typename TX, int EPT>
-__device__ __forceinline__ void load_row(const TX* row, int lane, float (&v)[EPT]) {
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+// Fast Walsh-Hadamard transform (Sylvester order) of a row held by LPR lanes,
+// 16 consecutive features each: element index = (lane % LPR) * 16 + i.
+template <int LPR>
+__device__ __forceinline__ void fwht16(float (&v)[SW_EPT], int lane) {
 #pragma unroll
-  for (int e = 0; e < EPT; ++e) v[e] = to_f32(row[lane * EPT + e]);
+  for (int h = 1; h < SW_EPT; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < SW_EPT; ++e)
+      if (!(e & h)) {
+        const float a = v[e], b = v[e + h];
+        v[e] = a + b;
+        v[e + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < LPR; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < SW_EPT; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
+      v[e] = (lane & m) ? (o - v[e]) : (v[e] + o);
+    }
 }
 
-// Score one candidate: acc holds Q R for the warp's rows.
-template <int EPT>
-__device__ __forceinline__ void score(const float (&acc)[SW_ROWS][EPT], const SweepArgs& a,
-                                      float* cells, int cell0, int lane) {
-  float m[SW_ROWS];
-  float e0 = 0.f;
+// Sum v[0..3] over the 32 lanes of the warp (reduce-scatter butterfly);
+// lane 8*i (i < 4) ends with the total of v[i].
+__device__ __forceinline__ float reduce4(const float (&v)[4], int lane) {
+  const bool h16 = lane & 16;
+  float a0 = h16 ? v[2] : v[0], a1 = h16 ? v[3] : v[1];
+  const float s0 = h16 ? v[0] : v[2], s1 = h16 ? v[1] : v[3];
+  a0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  a1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  const bool h8 = lane & 8;
+  float c = h8 ? a1 : a0;
+  const float d = h8 ? a0 : a1;
+  c += __shfl_xor_sync(0xffffffffu, d, 8);
+  c += __shfl_xor_sync(0xffffffffu, c, 4);
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+
+// Score one candidate.  acc holds the rotated residual Q R of this thread's
+// two rows, 16 features each, as packed pairs.  Per row: m = max|y| over the
+// row's LPR lanes; per b > 0: s = fp16(m / qmax), z = y / s (a reciprocal
+// multiply), q = round-half-even(z), error y - s q; b = 0 scores y itself.
+template <int LPR>
+__device__ __forceinline__ void score(const float2 (&acc)[SW_RPT][SW_EPT / 2],
+                                      const SweepArgs& a, float* cells, int cell0, int lane) {
+  float m[SW_RPT];
+  float2 e02 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int r = 0; r < SW_ROWS; ++r) {
+  for (int r = 0; r < SW_RPT; ++r) {
     float mm = 0.f;
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      mm = fmaxf(mm, fabsf(acc[r][e]));
-      e0 = fmaf(acc[r][e], acc[r][e], e0);
+    for (int i = 0; i < SW_EPT / 2; ++i) {
+      mm = fmaxf(mm, fmaxf(fabsf(acc[r][i].x), fabsf(acc[r][i].y)));
+      e02 = __ffma2_rn(acc[r][i], acc[r][i], e02);
     }
+#pragma unroll
+    for (int o = 1; o < LPR; o <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
     m[r] = mm;
   }
+  const float2 M2 = f2(12582912.0f), nM2 = f2(-12582912.0f);  // round-half-even by 1.5*2^23
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int r = 0; r < SW_ROWS; ++r) m[r] = warp_max(m[r]);
-  for (int ib = 0; ib < a.nb; ++ib) {
-    const int b = a.b[ib];
-    float eb;
-    if (b == 0) {
-      eb = e0;
-    } else {
-      const float qmax = (float)((1 << (b - 1)) - 1);
-      eb = 0.f;
+  for (int ib = 0; ib < 4; ++ib) {
+    if (ib >= a.nb) break;
+    if (a.b[ib] == 0) { v[ib] = e02.x + e02.y; continue; }
+    float2 eb = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int r = 0; r < SW_ROWS; ++r) {
-        const float s = round_f16(__fdiv_rn(m[r], qmax));
-        const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+    for (int r = 0; r < SW_RPT; ++r) {
+      const float s = round_f16(m[r] * a.rq[ib]);
+      float inv;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(s));
+      if (!(s > 0.f)) inv = 0.f;
+      const float2 inv2 = f2(inv), ns2 = f2(-s);
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-          const float q = rint_magic(acc[r][e] * inv);
-          const float d = fmaf(-s, q, acc[r][e]);
-          eb = fmaf(d, d, eb);
-        }
+      for (int i = 0; i < SW_EPT / 2; ++i) {
+        const float2 z = __fmul2_rn(acc[r][i], inv2);
+        const float2 q = __fadd2_rn(__fadd2_rn(z, M2), nM2);
+        const float2 d = __ffma2_rn(ns2, q, acc[r][i]);
+        eb = __ffma2_rn(d, d, eb);
       }
     }
-    eb = warp_sum(eb);
-    if (lane == 0) atomicAdd(&cells[cell0 + ib], eb);
+    v[ib] = eb.x + eb.y;
+  }
+  const float t = reduce4(v, lane);
+  if ((lane & 7) == 0) {
+    const int ib = lane >> 3;
+    if (ib < a.nb) atomicAdd(&cells[cell0 + ib], t);
   }
 }
 
-template <typename TX, int EPT>
-__global__ void __launch_bounds__(SW_THREADS) sweep_kernel(SweepArgs a) {
-  constexpr int D = 32 * EPT;
+// acc -= K[k][rows] * B[k][:] for k in [k0, k1), then score at each nested rank.
+template <int LPR>
+__device__ __forceinline__ void chain_step(float2 (&acc)[SW_RPT][SW_EPT / 2], const float* Ks,
+                                           const float* Bs, int tile, int bld, int k, int row0,
+                                           int l) {
+  const float2 kr = *reinterpret_cast<const float2*>(Ks + k * tile + row0);
+  const float4* bp = reinterpret_cast<const float4*>(Bs + k * bld + l * 20);
+  float2 bv[SW_EPT / 2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 t4 = bp[q];
+    bv[2 * q] = make_float2(t4.x, t4.y);
+    bv[2 * q + 1] = make_float2(t4.z, t4.w);
+  }
+  const float2 n0 = f2(-kr.x), n1 = f2(-kr.y);
+#pragma unroll
+  for (int i = 0; i < SW_EPT / 2; ++i) {
+    acc[0][i] = __ffma2_rn(n0, bv[i], acc[0][i]);
+    acc[1][i] = __ffma2_rn(n1, bv[i], acc[1][i]);
+  }
+}
+
+template <typename TX, int LPR>
+__global__ void __launch_bounds__(SW_THREADS, 2) sweep_kernel(SweepArgs a) {
+  constexpr int D = SW_EPT * LPR;
+  constexpr int GPW = 32 / LPR;              // row groups per warp
+  constexpr int TILE = SW_WARPS * GPW * SW_RPT;
+  constexpr int BLD = LPR * 20;              // factor row, 16 floats + 4 pad per lane block
   extern __shared__ __align__(16) float smem[];
-  float* Ks = smem;                     // [64][SW_TILE]  chain coefficients, k-major
-  float* Bs = Ks + 64 * SW_TILE;        // [64][D]        rotated factor rows
-  float* cells = Bs + 64 * D;           // [ncand + 1]
+  float* Ks = smem;                          // [64][TILE] chain coefficients
+  float* Bs = Ks + 64 * TILE;                // [64][BLD]  rotated factor rows
+  float* cells = Bs + 64 * BLD;              // [ncand + 1]
 
   const int u = blockIdx.z, h = blockIdx.y, tt = blockIdx.x;
-  const int t0 = tt * SW_TILE;
-  const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t0 = tt * TILE;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l = lane % LPR, g = lane / LPR;
+  const int row0 = w * GPW * SW_RPT + g * SW_RPT;   // this thread's first tile row
   char* base = a.ws + u * a.ub;
   for (int i = threadIdx.x; i <= a.ncand; i += SW_THREADS) cells[i] = 0.f;
 
-  // ---- load X rows, rotate once: qx = H (sigma .* x) / sqrt(D)
+  // ---- X rows, rotated once: qx = H (sigma .* x) / sqrt(D)
   const TX* Xu = (const TX*)a.X + ((long long)u * a.H + h) * a.T * D;
-  float sg[EPT];
+  float sg[SW_EPT];
 #pragma unroll
-  for (int e = 0; e < EPT; ++e) sg[e] = (float)a.signs[(long long)u * D + lane * EPT + e];
+  for (int i = 0; i < SW_EPT; ++i) sg[i] = (float)a.signs[(long long)u * D + l * SW_EPT + i];
   const float rs = rsqrtf((float)D);
-  float x[SW_ROWS][EPT], qx[SW_ROWS][EPT];
+  float2 qx[SW_RPT][SW_EPT / 2], acc[SW_RPT][SW_EPT / 2];
   float xn = 0.f;
+  const bool fullTD = a.hasFullT && a.hasFullD;
 #pragma unroll
-  for (int r = 0; r < SW_ROWS; ++r) {
-    const int t = t0 + w * SW_ROWS + r;
-    if (t < a.T) {
-      load_row<TX, EPT>(Xu + (long long)t * D, lane, x[r]);
-    } else {
+  for (int r = 0; r < SW_RPT; ++r) {
+    const int t = t0 + row0 + r;
+    float x[SW_EPT], v[SW_EPT];
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) x[r][e] = 0.f;
+    for (int i = 0; i < SW_EPT; ++i)
+      x[i] = (t < a.T) ? to_f32(Xu[(long long)t * D + l * SW_EPT + i]) : 0.f;
+#pragma unroll
+    for (int i = 0; i < SW_EPT; ++i) {
+      xn = fmaf(x[i], x[i], xn);
+      v[i] = x[i] * sg[i];
     }
+    fwht16<LPR>(v, lane);
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) {
-      xn = fmaf(x[r][e], x[r][e], xn);
-      qx[r][e] = x[r][e] * sg[e];
+    for (int i = 0; i < SW_EPT / 2; ++i) qx[r][i] = make_float2(v[2 * i] * rs, v[2 * i + 1] * rs);
+    if (fullTD) {
+      // (r_T, r_d) = (T, D): the stored core is fp16(X) itself
+#pragma unroll
+      for (int i = 0; i < SW_EPT; ++i) v[i] = (x[i] - round_f16(x[i])) * sg[i];
+      fwht16<LPR>(v, lane);
+#pragma unroll
+      for (int i = 0; i < SW_EPT / 2; ++i) acc[r][i] = make_float2(v[2 * i] * rs, v[2 * i + 1] * rs);
     }
-    fwht_row<EPT>(qx[r], lane);
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) qx[r][e] *= rs;
   }
   __syncthreads();  // cells cleared
   xn = warp_sum(xn);
   if (lane == 0) atomicAdd(&cells[a.ncand], xn);
-
-  float acc[SW_ROWS][EPT];
   const int iTfull = a.nT - 1, idfull = a.nd - 1;
-
-  // ---- (r_T, r_d) = (T, D): the stored core is fp16(X) itself
-  if (a.hasFullT && a.hasFullD) {
-#pragma unroll
-    for (int r = 0; r < SW_ROWS; ++r) {
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) acc[r][e] = (x[r][e] - round_f16(x[r][e])) * sg[e];
-      fwht_row<EPT>(acc[r], lane);
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) acc[r][e] *= rs;
-    }
-    score<EPT>(acc, a, cells, (iTfull * a.nd + idfull) * a.nb, lane);
-  }
+  if (fullTD) score<LPR>(acc, a, cells, (iTfull * a.nd + idfull) * a.nb, lane);
 
   // ---- r_T = T, truncated r_d: X~ Q^T = Y16 (Q U_d)^T, prefix over r_d
   if (a.hasFullT && a.ndt > 0) {
     const __half* Yh = (const __half*)(base + a.o_Y16) + (long long)h * a.T * a.RD;
-    for (int i = threadIdx.x; i < SW_TILE * a.RD; i += SW_THREADS) {
-      const int row = i / a.RD, j = i % a.RD;
-      const int t = t0 + row;
-      Ks[j * SW_TILE + row] = (t < a.T) ? __half2float(Yh[(long long)t * a.RD + j]) : 0.f;
+    for (int i = threadIdx.x; i < TILE * a.RD; i += SW_THREADS) {
+      const int row = i / a.RD, j = i % a.RD, t = t0 + row;
+      Ks[j * TILE + row] = (t < a.T) ? __half2float(Yh[(long long)t * a.RD + j]) : 0.f;
     }
     const float* QU = (const float*)(base + a.o_QUd);
-    for (int i = threadIdx.x; i < a.RD * D; i += SW_THREADS) Bs[i] = QU[i];
+    for (int i = threadIdx.x; i < a.RD * D; i += SW_THREADS) {
+      const int j = i / D, e = i % D;
+      Bs[j * BLD + (e >> 4) * 20 + (e & 15)] = QU[i];
+    }
     __syncthreads();
 #pragma unroll
-    for (int r = 0; r < SW_ROWS; ++r)
+    for (int r = 0; r < SW_RPT; ++r)
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) acc[r][e] = qx[r][e];
+      for (int i = 0; i < SW_EPT / 2; ++i) acc[r][i] = qx[r][i];
     int next = 0;
     for (int j = 0; j < a.RD; ++j) {
-      const float* kk = Ks + j * SW_TILE + w * SW_ROWS;
-      const float* bb = Bs + j * D + lane * EPT;
-      float bv[EPT];
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) bv[e] = bb[e];
-#pragma unroll
-      for (int r = 0; r < SW_ROWS; ++r) {
-        const float kr = kk[r];
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(-kr, bv[e], acc[r][e]);
-      }
+      chain_step<LPR>(acc, Ks, Bs, TILE, BLD, j, row0, l);
       if (next < a.ndt && j + 1 == a.rd[next]) {
-        score<EPT>(acc, a, cells, (iTfull * a.nd + next) * a.nb, lane);
+        score<LPR>(acc, a, cells, (iTfull * a.nd + next) * a.nb, lane);
         ++next;
       }
     }
@@ -194,33 +252,25 @@ __global__ void __launch_bounds__(SW_THREADS) sweep_kernel(SweepArgs a) {
   if (a.nTt > 0) {
     for (int id = 0; id < a.nd; ++id) {
       const __half* Ug = (const __half*)(base + a.o_UT16) + (long long)id * a.T * a.RT;
-      for (int i = threadIdx.x; i < SW_TILE * a.RT; i += SW_THREADS) {
-        const int row = i / a.RT, k = i % a.RT;
-        const int t = t0 + row;
-        Ks[k * SW_TILE + row] = (t < a.T) ? __half2float(Ug[(long long)t * a.RT + k]) : 0.f;
+      for (int i = threadIdx.x; i < TILE * a.RT; i += SW_THREADS) {
+        const int row = i / a.RT, k = i % a.RT, t = t0 + row;
+        Ks[k * TILE + row] = (t < a.T) ? __half2float(Ug[(long long)t * a.RT + k]) : 0.f;
       }
       const float* Wg = (const float*)(base + a.o_W) + ((long long)id * a.H + h) * a.RT * D;
-      for (int i = threadIdx.x; i < a.RT * D; i += SW_THREADS) Bs[i] = Wg[i];
+      for (int i = threadIdx.x; i < a.RT * D; i += SW_THREADS) {
+        const int k = i / D, e = i % D;
+        Bs[k * BLD + (e >> 4) * 20 + (e & 15)] = Wg[i];
+      }
       __syncthreads();
 #pragma unroll
-      for (int r = 0; r < SW_ROWS; ++r)
+      for (int r = 0; r < SW_RPT; ++r)
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[r][e] = qx[r][e];
+        for (int i = 0; i < SW_EPT / 2; ++i) acc[r][i] = qx[r][i];
       int next = 0;
       for (int k = 0; k < a.RT; ++k) {
-        const float* kk = Ks + k * SW_TILE + w * SW_ROWS;
-        const float* bb = Bs + k * D + lane * EPT;
-        float bv[EPT];
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) bv[e] = bb[e];
-#pragma unroll
-        for (int r = 0; r < SW_ROWS; ++r) {
-          const float kr = kk[r];
-#pragma unroll
-          for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(-kr, bv[e], acc[r][e]);
-        }
+        chain_step<LPR>(acc, Ks, Bs, TILE, BLD, k, row0, l);
         if (next < a.nTt && k + 1 == a.rT[next]) {
-          score<EPT>(acc, a, cells, (next * a.nd + id) * a.nb, lane);
+          score<LPR>(acc, a, cells, (next * a.nd + id) * a.nb, lane);
           ++next;
         }
       }
@@ -349,25 +399,28 @@ __global__ void cost_kernel(CostArgs a, int n_units, int64_t* cost) {
   cost[i] = v;
 }
 
-template <int EPT>
-jolt_status launch_sweep_t(const SweepArgs& a, int U, size_t smem, cudaStream_t st) {
+template <int LPR>
+jolt_status launch_sweep_t(const SweepArgs& a, int U, cudaStream_t st) {
+  constexpr int D = SW_EPT * LPR, TILE = SW_WARPS * (32 / LPR) * SW_RPT, BLD = LPR * 20;
   dim3 grid(a.tiles_t, a.H, U);
+  const size_t smem = (size_t)(64 * TILE + 64 * BLD + a.ncand + 1) * sizeof(float);
+  (void)D;
   if (a.dtype == JOLT_BF16) {
     static bool s1 = false;
     if (!s1) {
-      JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_kernel<__nv_bfloat16, EPT>,
+      JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_kernel<__nv_bfloat16, LPR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
       s1 = true;
     }
-    sweep_kernel<__nv_bfloat16, EPT><<<grid, SW_THREADS, smem, st>>>(a);
+    sweep_kernel<__nv_bfloat16, LPR><<<grid, SW_THREADS, smem, st>>>(a);
   } else {
     static bool s2 = false;
     if (!s2) {
-      JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_kernel<float, EPT>,
+      JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_kernel<float, LPR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024));
       s2 = true;
     }
-    sweep_kernel<float, EPT><<<grid, SW_THREADS, smem, st>>>(a);
+    sweep_kernel<float, LPR><<<grid, SW_THREADS, smem, st>>>(a);
   }
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
@@ -401,7 +454,7 @@ jolt_status sweep_prep(const Layout& L, int U, const int8_t* signs, char* ws, cu
 jolt_status sweep_run(const Layout& L, int U, const void* X, const int8_t* signs, char* ws,
                       double* dist, int64_t* cost, cudaStream_t st) {
   const size_t ub = L.unit_bytes;
-  const int D = L.D, EPT = D / 32;
+  const int D = L.D;
   {
     jolt_status s0 = sweep_prep(L, U, signs, ws, st);
     if (s0 != JOLT_OK) return s0;
@@ -417,16 +470,15 @@ jolt_status sweep_run(const Layout& L, int U, const void* X, const int8_t* signs
   }
   for (int i = 0; i < 4; ++i) a.b[i] = L.b[i];
   a.ncand = L.ncand;
-  a.tiles_t = (L.T + SW_TILE - 1) / SW_TILE;
+  a.tiles_t = (L.T + L.tile_rows - 1) / L.tile_rows;
+  for (int i = 0; i < 4; ++i) a.rq[i] = L.b[i] > 0 ? 1.f / (float)((1 << (L.b[i] - 1)) - 1) : 0.f;
   a.o_UT16 = L.o_UT16; a.o_W = L.o_W; a.o_Y16 = L.o_Y16; a.o_QUd = L.o_QUd; a.o_part = L.o_part;
-  const size_t smem = (size_t)(64 * SW_TILE + 64 * D + L.ncand + 1) * sizeof(float);
   jolt_status s;
-  if (EPT == 4) s = launch_sweep_t<4>(a, U, smem, st);
-  else if (EPT == 2) s = launch_sweep_t<2>(a, U, smem, st);
-  else s = launch_sweep_t<1>(a, U, smem, st);
+  if (D == 128) s = launch_sweep_t<8>(a, U, st);
+  else if (D == 64) s = launch_sweep_t<4>(a, U, st);
+  else s = launch_sweep_t<2>(a, U, st);
   if (s != JOLT_OK) return s;
-  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, L.o_part, L.o_status, L.H * a.tiles_t, L.ncand,
-                                        dist);
+  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, L.o_part, L.o_status, L.ntiles, L.ncand, dist);
   JOLT_LAUNCH_CHECK();
   CostArgs ca;
   ca.H = L.H; ca.T = L.T; ca.D = D; ca.nT = L.nT; ca.nd = L.nd; ca.nb = L.nb;
