@@ -47,7 +47,8 @@ typedef enum {
   JOLT_ERR_NONFINITE = 3,   /* NaN/Inf met in X or in a scale */
   JOLT_ERR_NOCONVERGE = 4,  /* an eigensolver hit its iteration cap */
   JOLT_ERR_WORKSPACE = 5,   /* workspace missing or too small */
-  JOLT_ERR_CUDA = 6         /* a CUDA runtime call failed */
+  JOLT_ERR_CUDA = 6,        /* a CUDA runtime call failed */
+  JOLT_ERR_TOO_LARGE = 7    /* batch beyond the no-allocation entry point's static scratch */
 } jolt_status;
 
 typedef enum { JOLT_F32 = 0, JOLT_BF16 = 1, JOLT_F16 = 2 } jolt_dtype;
@@ -191,6 +192,34 @@ jolt_status jolt_encode(const jolt_config* cfg, int n_units, const void* X,
  */
 jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blob,
                         size_t blob_stride, void* xhat, jolt_dtype out_dtype, void* stream);
+
+/*
+ * The same sweep as jolt_sweep_candidates, for callers that cannot allocate
+ * device memory (code that runs where cudaMalloc is not allowed, or whose
+ * memory belongs to an allocator it may not call at this point).  The pages
+ * have no counterpart: this is a deployment variant of the call above, with
+ * the same arguments and the same results.
+ *   - Scratch: the per-tile partial sums go to one static device array of
+ *     jolt_noalloc_scratch_bytes() bytes (16 MiB) that the library holds on
+ *     every GPU it is loaded on until the process exits; nothing is
+ *     allocated.  A batch needs n_units * ceil(T / (8192 / D)) * H *
+ *     (n_cand + 1) * 4 bytes of it; a larger batch returns
+ *     JOLT_ERR_TOO_LARGE before any launch (split it into smaller batches).
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Sharing: every call on a device uses the same array.  Calls that
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it; order them on one stream or with events.  Every entry a call
+ *     reads is written by that call first, so nothing needs clearing.
+ *   - ws must hold the factors of jolt_factor_group as for the call above.
+ */
+jolt_status jolt_sweep_candidates_noalloc(const jolt_config* cfg, int n_units, const void* X,
+                                          const int8_t* signs, void* ws, size_t ws_bytes,
+                                          double* dist, int64_t* cost, void* stream);
+
+/* Size of the static scratch array of jolt_sweep_candidates_noalloc. */
+size_t jolt_noalloc_scratch_bytes(void);
 
 /* Synchronise `stream` and return the worst device status recorded in the
  * workspace of the n_units units (then clear it). */

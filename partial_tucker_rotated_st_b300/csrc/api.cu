@@ -292,6 +292,7 @@ const char* jolt_status_string(jolt_status s) {
     case JOLT_ERR_NOCONVERGE: return "eigensolver did not converge";
     case JOLT_ERR_WORKSPACE: return "workspace missing or too small";
     case JOLT_ERR_CUDA: return "CUDA runtime error";
+    case JOLT_ERR_TOO_LARGE: return "batch beyond the static scratch of the no-allocation call";
   }
   return "unknown status";
 }

@@ -131,8 +131,11 @@ jolt_status factor_run(const Layout& L, int n_units, const void* X, const float*
 // Rotated factor rows for the sweep and the encoder: Q U_d and W = G (Q U_d)^T.
 jolt_status sweep_prep(const Layout& L, int n_units, const int8_t* signs, char* ws,
                        cudaStream_t st);
+// part_override: where the per-tile partial sums go (n_units * ntiles *
+// (ncand + 1) floats); nullptr = the workspace section.
 jolt_status sweep_run(const Layout& L, int n_units, const void* X, const int8_t* signs,
-                      char* ws, double* dist, int64_t* cost, cudaStream_t st);
+                      char* ws, double* dist, int64_t* cost, cudaStream_t st,
+                      float* part_override = nullptr);
 jolt_status alloc_run(int n_units, int n_cand, const double* dist, const int64_t* cost,
                       int64_t budget, int align, int32_t* choice, double* lambda,
                       int32_t* status, cudaStream_t st);

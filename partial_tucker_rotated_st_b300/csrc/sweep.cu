@@ -43,7 +43,9 @@ struct SweepArgs {
   int rT[JOLT_MAX_GRID], rd[JOLT_MAX_GRID], b[4];
   float rq[4];         // 1 / (2^(b-1) - 1) for b > 0
   int ncand, tiles_t;
-  size_t o_UT16, o_W, o_Y16, o_QUd, o_part;
+  size_t o_UT16, o_W, o_Y16, o_QUd;
+  float* part;          // per-tile partial sums, unit u at part + u * part_us
+  long long part_us;
 };
 
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(SW_THREADS, 2) sweep_kernel(SweepArgs a) {
   }
 
   __syncthreads();
-  float* part = (float*)(base + a.o_part) + ((long long)h * a.tiles_t + tt) * (a.ncand + 1);
+  float* part = a.part + u * a.part_us + ((long long)h * a.tiles_t + tt) * (a.ncand + 1);
   for (int i = threadIdx.x; i <= a.ncand; i += SW_THREADS) part[i] = cells[i];
 }
 
@@ -346,10 +348,10 @@ __global__ void build_w_kernel(char* ws, size_t ub, const int8_t* signs, size_t 
 }
 
 // dist[u][c] = sum_tiles e / sum_tiles ||x||^2 (f64), 0 for an all-zero unit.
-__global__ void sweep_reduce_kernel(char* ws, size_t ub, size_t o_part, size_t o_status, int ntiles,
-                                    int ncand, double* dist) {
+__global__ void sweep_reduce_kernel(char* ws, size_t ub, const float* part_base, long long part_us,
+                                    size_t o_status, int ntiles, int ncand, double* dist) {
   const int u = blockIdx.x;
-  const float* part = (const float*)(ws + u * ub + o_part);
+  const float* part = part_base + u * part_us;
   __shared__ double xn;
   if (threadIdx.x < 32) {
     double s = 0.0;
@@ -452,7 +454,7 @@ jolt_status sweep_prep(const Layout& L, int U, const int8_t* signs, char* ws, cu
 }
 
 jolt_status sweep_run(const Layout& L, int U, const void* X, const int8_t* signs, char* ws,
-                      double* dist, int64_t* cost, cudaStream_t st) {
+                      double* dist, int64_t* cost, cudaStream_t st, float* part_override) {
   const size_t ub = L.unit_bytes;
   const int D = L.D;
   {
@@ -472,13 +474,21 @@ jolt_status sweep_run(const Layout& L, int U, const void* X, const int8_t* signs
   a.ncand = L.ncand;
   a.tiles_t = (L.T + L.tile_rows - 1) / L.tile_rows;
   for (int i = 0; i < 4; ++i) a.rq[i] = L.b[i] > 0 ? 1.f / (float)((1 << (L.b[i] - 1)) - 1) : 0.f;
-  a.o_UT16 = L.o_UT16; a.o_W = L.o_W; a.o_Y16 = L.o_Y16; a.o_QUd = L.o_QUd; a.o_part = L.o_part;
+  a.o_UT16 = L.o_UT16; a.o_W = L.o_W; a.o_Y16 = L.o_Y16; a.o_QUd = L.o_QUd;
+  if (part_override) {
+    a.part = part_override;
+    a.part_us = (long long)L.ntiles * (L.ncand + 1);
+  } else {
+    a.part = (float*)(ws + L.o_part);
+    a.part_us = (long long)ub / 4;
+  }
   jolt_status s;
   if (D == 128) s = launch_sweep_t<8>(a, U, st);
   else if (D == 64) s = launch_sweep_t<4>(a, U, st);
   else s = launch_sweep_t<2>(a, U, st);
   if (s != JOLT_OK) return s;
-  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, L.o_part, L.o_status, L.ntiles, L.ncand, dist);
+  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, a.part, a.part_us, L.o_status, L.ntiles, L.ncand,
+                                        dist);
   JOLT_LAUNCH_CHECK();
   CostArgs ca;
   ca.H = L.H; ca.T = L.T; ca.D = D; ca.nT = L.nT; ca.nd = L.nd; ca.nb = L.nb;

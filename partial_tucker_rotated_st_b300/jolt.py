@@ -20,8 +20,10 @@ COST_FORMULA, COST_SERIALIZED = 0, 1
 HEADER_BYTES = 256
 
 STATUS = {0: "JOLT_OK", 1: "JOLT_ERR_INVALID", 2: "JOLT_ERR_INFEASIBLE", 3: "JOLT_ERR_NONFINITE",
-          4: "JOLT_ERR_NOCONVERGE", 5: "JOLT_ERR_WORKSPACE", 6: "JOLT_ERR_CUDA"}
-OK, ERR_INVALID, ERR_INFEASIBLE, ERR_NONFINITE, ERR_NOCONVERGE, ERR_WORKSPACE, ERR_CUDA = range(7)
+          4: "JOLT_ERR_NOCONVERGE", 5: "JOLT_ERR_WORKSPACE", 6: "JOLT_ERR_CUDA",
+          7: "JOLT_ERR_TOO_LARGE"}
+(OK, ERR_INVALID, ERR_INFEASIBLE, ERR_NONFINITE, ERR_NOCONVERGE, ERR_WORKSPACE, ERR_CUDA,
+ ERR_TOO_LARGE) = range(8)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libjolt.so")
@@ -73,6 +75,9 @@ _SIG = {
                                    ctypes.POINTER(JoltBlobDesc), _P]),
     "jolt_decode": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(JoltBlobDesc), _P,
                                    ctypes.c_size_t, _P, ctypes.c_int, _P]),
+    "jolt_sweep_candidates_noalloc": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P,
+                                                     _P, _P, ctypes.c_size_t, _P, _P, _P]),
+    "jolt_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "jolt_read_status": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P]),
     "jolt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "jolt_launch_count": (ctypes.c_uint64, []),
@@ -165,6 +170,20 @@ def jolt_sweep_candidates(cfg, n_units, X, signs, ws, dist, cost, ws_bytes=None,
     _check("jolt_sweep_candidates", lib().jolt_sweep_candidates(
         ctypes.byref(cfg), n_units, _ptr(X), _ptr(signs), _ptr(ws), ws_bytes, _ptr(dist),
         _ptr(cost), _stream(stream)))
+
+
+def jolt_sweep_candidates_noalloc(cfg, n_units, X, signs, ws, dist, cost, ws_bytes=None,
+                                  stream=None):
+    """The sweep without any device allocation: its scratch is the library's
+    static array (see include/jolt.h)."""
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("jolt_sweep_candidates_noalloc", lib().jolt_sweep_candidates_noalloc(
+        ctypes.byref(cfg), n_units, _ptr(X), _ptr(signs), _ptr(ws), ws_bytes, _ptr(dist),
+        _ptr(cost), _stream(stream)))
+
+
+def jolt_noalloc_scratch_bytes() -> int:
+    return lib().jolt_noalloc_scratch_bytes()
 
 
 def jolt_allocate(n_units, n_cand, dist, cost, budget, align, choice, lam, status, stream=None):

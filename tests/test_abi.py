@@ -32,7 +32,7 @@ def header_functions():
 
 def test_library_exports_every_declared_symbol():
     names = header_functions()
-    assert len(names) == 11
+    assert len(names) == 13
     lib = ctypes.CDLL(J.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -114,5 +114,5 @@ def test_decode_rejects_inconsistent_descriptors():
 
 
 def test_status_strings():
-    for s in range(7):
+    for s in range(8):
         assert J.jolt_status_string(s) and "unknown" not in J.jolt_status_string(s)
