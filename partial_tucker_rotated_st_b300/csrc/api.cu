@@ -131,6 +131,7 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   const bool svtc = RT > 0 && L.token_mode == JOLT_TOKEN_EXACT && T > 128 && L.L == 64;
   L.o_STs = svtc ? sect((size_t)T * T * 4) : 0;
   L.o_Vs = svtc ? sect((size_t)2 * T * 64 * 4) : 0;   // V^T and its tf32 low part
+  L.o_Yt = (svtc && RD > 0) ? sect((size_t)2 * T * RD * H * 4) : 0;
   const size_t blk = iter ? (size_t)T * Lw * 4 : 0;
   L.o_V = sect(blk);
   L.o_Z = sect(blk);
@@ -148,7 +149,8 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   L.o_tokev = sect((size_t)L.nd * RT * 4);
   L.o_G32 = sect((size_t)L.nd * H * RT * D * 4);
   L.o_G16 = sect((size_t)L.nd * H * RT * D * 2);
-  L.o_W = sect((size_t)L.nd * H * RT * D * 4);
+  // rotated chain rows of the sweep; the encoder reuses the first two slots
+  L.o_W = sect((size_t)(L.nd > 2 ? L.nd : 2) * H * RT * D * 4);
   L.o_part = sect((size_t)L.ntiles * (L.ncand + 1) * 4);
   L.o_P = sect((RT > 0 && L.token_mode == JOLT_TOKEN_RANDOMIZED) ? (size_t)H * Dmax * L.ell * 4 : 0);
   L.unit_bytes = align_up(off, 256);

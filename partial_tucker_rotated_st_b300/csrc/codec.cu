@@ -63,43 +63,105 @@ __global__ void copy_f16_kernel(const TS* src, long long sa, long long sb, __hal
 struct EncArgs {
   const void* X;
   const int8_t* signs;
-  const char* ws;
   int H, T, D, dtype;
-  int b, mode, K;   // mode 0: U_T W chain; 1: Y16 (Q U_d)^T chain; 2: whole modes
-  const __half* Kg;  // chain coefficients, row t at Kg + h*k_hs + t*k_ld
+  int b, mode, K;     // mode 0/1: X~ = K B chain; 2: whole modes, X~ = fp16(X)
+  const __half* Kg;   // chain coefficients K[t][k] at Kg + h*k_hs + t*k_ld + k
   long long k_hs, k_ld;
-  const float* Bg;   // rotated factor rows, K x D, at Bg + h*b_hs
-  long long b_hs;
+  const __half* B16;  // fp16 chain rows B[k][d] at B16 + h*b_hs + k*b_ks + d*b_ds, or
+  long long b_hs, b_ks, b_ds;
+  const float* Bhi;   // double-float rows (Bhi + Blo)[h][k][d], row stride D
+  const float* Blo;
+  float rs_hi, rs_lo;  // 1/sqrt(D) as a double-float
   char* blob;
   unsigned long long off_scale, off_codes;
 };
 
+// Error-free transformations (Knuth TwoSum; TwoProduct through the fused
+// multiply-add).  Double-float values are unevaluated sums hi + lo.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// Walsh-Hadamard transform of a warp row of double-floats (element
+// lane * EPT + e), each butterfly a TwoSum with the low parts carried along.
+template <int EPT>
+__device__ __forceinline__ void fwht_row_df(float (&hi)[EPT], float (&lo)[EPT], int lane) {
+#pragma unroll
+  for (int h = 1; h < EPT; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPT; ++e)
+      if (!(e & h)) {
+        float s, es, d, ed;
+        two_sum(hi[e], hi[e + h], s, es);
+        two_sum(hi[e], -hi[e + h], d, ed);
+        const float l0 = lo[e], l1 = lo[e + h];
+        hi[e] = s; lo[e] = (l0 + l1) + es;
+        hi[e + h] = d; lo[e + h] = (l0 - l1) + ed;
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1)
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const float oh = __shfl_xor_sync(0xffffffffu, hi[e], m);
+      const float ol = __shfl_xor_sync(0xffffffffu, lo[e], m);
+      float s, es;
+      if (lane & m) {
+        two_sum(oh, -hi[e], s, es);
+        lo[e] = (ol - lo[e]) + es;
+      } else {
+        two_sum(hi[e], oh, s, es);
+        lo[e] = (lo[e] + ol) + es;
+      }
+      hi[e] = s;
+    }
+}
+
+// fp16 rounding (to nearest, ties to even) of the value zh + zl >= 0, where
+// zh is fp32-rounded: only when zh sits exactly on the midpoint of two fp16
+// neighbours does the low part decide.
+__device__ __forceinline__ float round_f16_df(float zh, float zl) {
+  const __half h = __float2half_rn(zh);
+  const float hf = __half2float(h);
+  const float d = zh - hf;
+  if (d == 0.f || zl == 0.f) return hf;
+  const unsigned short hb = __half_as_ushort(h);
+  const __half nb = __ushort_as_half((unsigned short)(d > 0.f ? hb + 1 : hb - 1));
+  const float nf = __half2float(nb);
+  if (zh == 0.5f * (hf + nf) && (d > 0.f) == (zl > 0.f)) return nf;
+  return hf;
+}
+
+// Codes of one residual row: R = X - K B in double-float (the chain
+// products are exact or TwoProduct-split), y = Q R by a double-float
+// Walsh-Hadamard transform, then the block scale and the codes decided on
+// the double-float y so that they agree with a correctly rounded evaluation
+// except where y sits within ~2^-44 |y| of a rounding boundary.
+// ["Rotated Tucker residual for outlier-resistant KV quantization",
+//  Formulas: Y = Q R, s = max|y| / (2^(b-1) - 1) in fp16, codes = round(y / s)
+//  clipped to the b-bit range.]
 template <typename TX, int EPT>
-__global__ void __launch_bounds__(CD_THREADS) encode_codes_kernel(EncArgs a) {
+__global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(EncArgs a) {
   constexpr int D = 32 * EPT;
   extern __shared__ __align__(16) float dsm[];
   float* Ks = dsm;                       // [64][CD_TILE]
-  float* Bs = Ks + 64 * CD_TILE;         // [64][D]
-  unsigned char (*codes)[D] = reinterpret_cast<unsigned char (*)[D]>(Bs + 64 * D);  // [warps][D]
+  float* Bsh = Ks + 64 * CD_TILE;        // [64][D]
+  float* Bsl = Bsh + 64 * D;             // [64][D]
+  unsigned char (*codes)[D] = reinterpret_cast<unsigned char (*)[D]>(Bsl + 64 * D);  // [warps][D]
   const int h = blockIdx.y, t0 = blockIdx.x * CD_TILE;
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
   const TX* Xh = (const TX*)a.X + (long long)h * a.T * D;
-  float sg[EPT];
-#pragma unroll
-  for (int e = 0; e < EPT; ++e) sg[e] = (float)a.signs[lane * EPT + e];
-  const float rs = rsqrtf((float)D);
-  float acc[CD_ROWS][EPT];
+  float ah[CD_ROWS][EPT], al[CD_ROWS][EPT];
 #pragma unroll
   for (int r = 0; r < CD_ROWS; ++r) {
     const int t = t0 + w * CD_ROWS + r;
-    float x[EPT];
 #pragma unroll
-    for (int e = 0; e < EPT; ++e) x[e] = (t < a.T) ? to_f32(Xh[(long long)t * D + lane * EPT + e]) : 0.f;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) acc[r][e] = (a.mode == 2 ? x[e] - round_f16(x[e]) : x[e]) * sg[e];
-    fwht_row<EPT>(acc[r], lane);
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) acc[r][e] *= rs;
+    for (int e = 0; e < EPT; ++e) {
+      const float x = (t < a.T) ? to_f32(Xh[(long long)t * D + lane * EPT + e]) : 0.f;
+      ah[r][e] = a.mode == 2 ? x - round_f16(x) : x;  // exact
+      al[r][e] = 0.f;
+    }
   }
   if (a.mode != 2 && a.K > 0) {
     for (int i = threadIdx.x; i < CD_TILE * a.K; i += CD_THREADS) {
@@ -107,35 +169,96 @@ __global__ void __launch_bounds__(CD_THREADS) encode_codes_kernel(EncArgs a) {
       const int t = t0 + row;
       Ks[k * CD_TILE + row] = (t < a.T) ? __half2float(a.Kg[h * a.k_hs + (long long)t * a.k_ld + k]) : 0.f;
     }
-    const float* Bh = a.Bg + h * a.b_hs;
-    for (int i = threadIdx.x; i < a.K * D; i += CD_THREADS) Bs[i] = Bh[i];
+    if (a.B16) {
+      const __half* Bh = a.B16 + h * a.b_hs;
+      for (int i = threadIdx.x; i < a.K * D; i += CD_THREADS) {
+        const int k = i / D, d = i % D;
+        Bsh[i] = __half2float(Bh[k * a.b_ks + d * a.b_ds]);
+        Bsl[i] = 0.f;
+      }
+    } else {
+      const float* Bh = a.Bhi + (long long)h * a.b_hs;
+      const float* Bl = a.Blo + (long long)h * a.b_hs;
+      for (int i = threadIdx.x; i < a.K * D; i += CD_THREADS) {
+        Bsh[i] = Bh[i];
+        Bsl[i] = Bl[i];
+      }
+    }
     __syncthreads();
     for (int k = 0; k < a.K; ++k) {
       const float* kk = Ks + k * CD_TILE + w * CD_ROWS;
-      float bv[EPT];
+      float bh[EPT], bl[EPT];
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) bv[e] = Bs[k * D + lane * EPT + e];
+      for (int e = 0; e < EPT; ++e) {
+        bh[e] = Bsh[k * D + lane * EPT + e];
+        bl[e] = Bsl[k * D + lane * EPT + e];
+      }
 #pragma unroll
-      for (int r = 0; r < CD_ROWS; ++r)
+      for (int r = 0; r < CD_ROWS; ++r) {
+        const float c = kk[r];
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(-kk[r], bv[e], acc[r][e]);
+        for (int e = 0; e < EPT; ++e) {
+          const float p = c * bh[e];
+          const float pe = fmaf(c, bh[e], -p);  // c bh = p + pe exactly
+          float s, es;
+          two_sum(ah[r][e], -p, s, es);
+          ah[r][e] = s;
+          al[r][e] = fmaf(-c, bl[e], al[r][e] + (es - pe));
+        }
+      }
     }
   }
+  float sg[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) sg[e] = (float)a.signs[lane * EPT + e];
   const int b = a.b;
   const float qmax = (float)((1 << (b - 1)) - 1);
   const int qoff = 1 << (b - 1);
   const int nbytes = D * b / 8;
+#pragma unroll
   for (int r = 0; r < CD_ROWS; ++r) {
     const int t = t0 + w * CD_ROWS + r;
-    float m = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPT; ++e) m = fmaxf(m, fabsf(acc[r][e]));
-    m = warp_max(m);
-    const float s = round_f16(__fdiv_rn(m, qmax));
-    const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+    float yh[EPT], yl[EPT];
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
-      float q = rint_magic(acc[r][e] * inv);
+      yh[e] = ah[r][e] * sg[e];
+      yl[e] = al[r][e] * sg[e];
+    }
+    fwht_row_df<EPT>(yh, yl, lane);
+    // times 1/sqrt(D), renormalised so that yh is the fp32 rounding of y
+    float mh = 0.f, ml = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const float p = yh[e] * a.rs_hi;
+      const float l = fmaf(yh[e], a.rs_hi, -p) + fmaf(yh[e], a.rs_lo, yl[e] * a.rs_hi);
+      yh[e] = p + l;
+      yl[e] = l - (yh[e] - p);
+      const float ay = fabsf(yh[e]), aly = yh[e] < 0.f ? -yl[e] : yl[e];
+      if (ay > mh || (ay == mh && aly > ml)) { mh = ay; ml = aly; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, mh, o);
+      const float ol = __shfl_xor_sync(0xffffffffu, ml, o);
+      if (oh > mh || (oh == mh && ol > ml)) { mh = oh; ml = ol; }
+    }
+    // s = fp16(max|y| / qmax) from the double-float max
+    const float z0 = __fdiv_rn(mh, qmax);
+    const float z1 = __fdiv_rn(fmaf(-z0, qmax, mh) + ml, qmax);
+    const float zh = z0 + z1;  // renormalised: zh is the fp32 rounding of the quotient
+    const float s = round_f16_df(zh, z1 - (zh - z0));
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      float q = 0.f;
+      if (s > 0.f) {
+        q = rintf(__fdiv_rn(yh[e], s));
+        // the boundaries (q +- 1/2) s are exact in fp32; their side is the
+        // sign of y - (q +- 1/2) s, taken on the double-float y
+        const float up = fmaf(-(q + 0.5f), s, yh[e]) + yl[e];
+        const float dn = fmaf(-(q - 0.5f), s, yh[e]) + yl[e];
+        if (up > 0.f || (up == 0.f && fmodf(q, 2.f) != 0.f)) q += 1.f;
+        else if (dn < 0.f || (dn == 0.f && fmodf(q, 2.f) != 0.f)) q -= 1.f;
+      }
       q = fminf(fmaxf(q, -(float)qoff), (float)(qoff - 1));
       codes[w][lane * EPT + e] = (unsigned char)((int)q + qoff);
     }
@@ -152,6 +275,28 @@ __global__ void __launch_bounds__(CD_THREADS) encode_codes_kernel(EncArgs a) {
       if (lane == 0) ((__half*)(a.blob + a.off_scale))[row] = __float2half_rn(s);
     }
     __syncwarp();
+  }
+}
+
+// Unrotated chain rows of a truncated core, B[h][k][:] = G16[h][k][:] U_d16^T,
+// accumulated in double-float (fp16 x fp16 products are exact in fp32).
+__global__ void enc_rows_kernel(const __half* G, long long g_hs, const __half* Ud, int ldu, int rT,
+                                int rd, int D, float* Bhi, float* Blo) {
+  const int h = blockIdx.y;
+  const __half* Gh = G + h * g_hs;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < rT * D; i += gridDim.x * blockDim.x) {
+    const int k = i / D, d = i % D;
+    float sh = 0.f, sl = 0.f;
+    for (int j = 0; j < rd; ++j) {
+      const float p = __half2float(Gh[k * rd + j]) * __half2float(Ud[(long long)d * ldu + j]);
+      float s, e;
+      two_sum(sh, p, s, e);
+      sh = s;
+      sl += e;
+    }
+    const float hi = sh + sl;
+    Bhi[(long long)h * rT * D + i] = hi;
+    Blo[(long long)h * rT * D + i] = sl - (hi - sh);
   }
 }
 
@@ -298,7 +443,7 @@ unsigned nblk(long long n) { return (unsigned)((n + 255) / 256); }
 template <typename TX, int EPT>
 jolt_status launch_enc(dim3 grid, const EncArgs& ea, cudaStream_t st) {
   constexpr int D = 32 * EPT;
-  const size_t smem = (64 * CD_TILE + 64 * D) * sizeof(float) + CD_WARPS * D;
+  const size_t smem = (64 * CD_TILE + 2 * 64 * D) * sizeof(float) + CD_WARPS * D;
   static bool attr = false;
   if (!attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(encode_codes_kernel<TX, EPT>,
@@ -368,8 +513,6 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
     blob_layout(H, T, D, L.rT[iT], L.rd[id], L.b[ib], L.block, L.align, &desc[u]);
     if (desc[u].bytes > stride) return JOLT_ERR_INVALID;
   }
-  jolt_status s0 = sweep_prep(L, U, signs, (char*)ws, st);
-  if (s0 != JOLT_OK) return s0;
   for (int u = 0; u < U; ++u) {
     int iT, id, ib;
     cand_split(L, choice[u], &iT, &id, &ib);
@@ -414,19 +557,38 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
     if (s != JOLT_OK) return s;
     if (b == 0) continue;
     EncArgs ea;
-    ea.X = Xu; ea.signs = signs + (size_t)u * D; ea.ws = wu;
+    memset(&ea, 0, sizeof(ea));
+    ea.X = Xu; ea.signs = signs + (size_t)u * D;
     ea.H = H; ea.T = T; ea.D = D; ea.dtype = L.dtype; ea.b = b;
     ea.blob = bl; ea.off_scale = dsc.off_scale; ea.off_codes = dsc.off_codes;
+    {
+      const double rs = 1.0 / sqrt((double)D);
+      ea.rs_hi = (float)rs;
+      ea.rs_lo = (float)(rs - (double)ea.rs_hi);
+    }
+    const __half* Ud16 = (const __half*)(wu + L.o_Ud16);
     if (rT == T && rd == D) {
-      ea.mode = 2; ea.K = 0; ea.Kg = nullptr; ea.k_hs = 0; ea.k_ld = 0; ea.Bg = nullptr; ea.b_hs = 0;
+      ea.mode = 2;
     } else if (rT == T) {
+      // X~_h = Y16_h U_d16^T
       ea.mode = 1; ea.K = rd;
       ea.Kg = (const __half*)(wu + L.o_Y16); ea.k_hs = (long long)T * RD; ea.k_ld = RD;
-      ea.Bg = (const float*)(wu + L.o_QUd); ea.b_hs = 0;
+      ea.B16 = Ud16; ea.b_hs = 0; ea.b_ks = 1; ea.b_ds = RD;
     } else {
+      // X~_h = U_T16 (G16_h U_d16^T)
       ea.mode = 0; ea.K = rT;
       ea.Kg = (const __half*)(wu + L.o_UT16) + (size_t)id * T * RT; ea.k_hs = 0; ea.k_ld = RT;
-      ea.Bg = (const float*)(wu + L.o_W) + (size_t)id * H * RT * D; ea.b_hs = (long long)RT * D;
+      const __half* G16 = (const __half*)(wu + L.o_G16) + (size_t)id * H * RT * D;
+      if (rd == D) {
+        ea.B16 = G16; ea.b_hs = (long long)RT * D; ea.b_ks = D; ea.b_ds = 1;
+      } else {
+        float* Bh = (float*)(ws + (size_t)u * L.unit_bytes + L.o_W);
+        float* Blo = Bh + (size_t)H * rT * D;
+        enc_rows_kernel<<<dim3((rT * D + 255) / 256, H), 256, 0, st>>>(
+            G16, (long long)RT * rd, Ud16, RD, rT, rd, D, Bh, Blo);
+        JOLT_LAUNCH_CHECK();
+        ea.Bhi = Bh; ea.Blo = Blo; ea.b_hs = (long long)rT * D;
+      }
     }
     dim3 grid((T + CD_TILE - 1) / CD_TILE, H);
     const bool bf = (L.dtype == JOLT_BF16);

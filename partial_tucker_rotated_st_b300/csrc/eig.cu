@@ -17,13 +17,15 @@ namespace {
 constexpr int JAC_THREADS = 1024;   // viewed as 32 x 32 (ty, tx)
 constexpr int JAC_MAX_SWEEPS = 40;
 constexpr float JAC_TOL = 1e-6f;    // relative: |a_pq| vs sqrt(|a_pp a_qq|)
-constexpr float JAC_ABS = 1e-10f;   // absolute floor vs ||A||_F: stops rotations on pure noise
+// absolute floors vs ||A||_F: JAC_ABS_EXACT for solves whose small
+// eigenvalues matter; JAC_ABS_RR for Rayleigh-Ritz blocks, whose trailing
+// Ritz vectors only seed the next block
 
 __global__ void __launch_bounds__(JAC_THREADS, 1)
 jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int nparts,
               long long part_s, float* __restrict__ evals, long long e_bs,
               float* __restrict__ evecs, long long v_bs, int ldv, int ncols_out, int* status,
-              long long s_bs, const int* skip, long long sk_s) {
+              long long s_bs, const int* skip, long long sk_s, float abs_tol) {
   const int bidx = blockIdx.x;
   if (skip && skip[bidx * sk_s]) return;
   extern __shared__ float sm[];
@@ -58,7 +60,7 @@ jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int
   __syncthreads();
   float abs_floor = 0.f;
   for (int i = 0; i < 32; ++i) abs_floor += fro_part[i];
-  abs_floor = JAC_ABS * sqrtf(abs_floor);
+  abs_floor = abs_tol * sqrtf(abs_floor);
 
   bool converged = false;
   int sweep = 0;
@@ -167,6 +169,214 @@ jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int
   }
 }
 
+// The same cyclic Jacobi method with the matrix and the accumulated
+// rotations held in registers, after Brent & Luk (1985): one thread per 2x2
+// block.  1024 threads form a 32 x 32 grid; thread (I, J) owns NB x NB blocks
+// at block coordinates (I + 32a, J + 32b).  Every round pairs positions
+// (2k, 2k+1); after the round the matrix indices move between positions by
+// the round-robin (circle) permutation, so that over m - 1 rounds every pair
+// of indices meets once and after a whole sweep every index is back in its
+// original position.  Per round: the diagonal-block threads compute their
+// rotation from their own registers, every thread applies J_i^T B J_j to its
+// A blocks and B J_j to its V blocks, then scatters them to the permuted
+// positions through shared memory (two barriers per round).
+template <int NB>
+__global__ void __launch_bounds__(1024, 1)
+jacobi_bl_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int nparts,
+                 long long part_s, float* __restrict__ evals, long long e_bs,
+                 float* __restrict__ evecs, long long v_bs, int ldv, int ncols_out, int* status,
+                 long long s_bs, const int* skip, long long sk_s, float abs_tol) {
+  const int bidx = blockIdx.x;
+  if (skip && skip[bidx * sk_s]) return;
+  const int m = n + (n & 1);      // even size; a padded index stays zero
+  const int nb = m / 2;           // blocks per dimension
+  const int pl = nb + 1;          // plane row stride
+  extern __shared__ float sm[];
+  float* PA = sm;                 // A as 4 planes [x][y][nb][pl]
+  float* PV = PA + 4 * nb * pl;   // V as 4 planes
+  float4* cs = (float4*)(PV + 4 * nb * pl);   // [nb] (c, s, t, -)
+  int* perm = (int*)(cs + nb);                // [m] position -> next position
+  const int t = threadIdx.x, J = t & 31, I = t >> 5;
+
+  // circle slots: slot 0 fixed, slots 1..m-1 advance by one per round; the
+  // pair (slot k, slot m-1-k) sits at positions (2k, 2k+1)
+  for (int sl = t; sl < m; sl += blockDim.x) {
+    auto pos = [&](int q) { return q < nb ? 2 * q : 2 * (m - 1 - q) + 1; };
+    const int nx = (sl == 0) ? 0 : (sl == m - 1 ? 1 : sl + 1);
+    perm[pos(sl)] = pos(nx);
+  }
+  const float* Ag = Ain + bidx * a_bs;
+  float a[NB][NB][4], v[NB][NB][4];
+  float fro = 0.f;
+#pragma unroll
+  for (int x = 0; x < NB; ++x)
+#pragma unroll
+    for (int y = 0; y < NB; ++y) {
+      const int BI = I + 32 * x, BJ = J + 32 * y;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = 2 * BI + (e >> 1), c = 2 * BJ + (e & 1);
+        float val = 0.f;
+        if (BI < nb && BJ < nb && r < n && c < n) {
+          for (int k = 0; k < nparts; ++k)
+            val += Ag[k * part_s + (long long)r * lda + c] + Ag[k * part_s + (long long)c * lda + r];
+          val *= 0.5f;
+        }
+        a[x][y][e] = val;
+        v[x][y][e] = (r == c && r < n) ? 1.f : 0.f;
+        fro = fmaf(val, val, fro);
+      }
+    }
+  __shared__ float fro_part[32];
+  fro = warp_sum(fro);
+  if (J == 0) fro_part[I] = fro;
+  __syncthreads();
+  float abs_floor = 0.f;
+  for (int i = 0; i < 32; ++i) abs_floor += fro_part[i];
+  abs_floor = abs_tol * sqrtf(abs_floor);
+  // destinations of this thread's elements under the fixed permutation, and
+  // its own (gather) offsets, in the 4-plane layout
+  int dstA[NB][NB][4], dstV[NB][NB][4], own[NB][NB][4];
+#pragma unroll
+  for (int x = 0; x < NB; ++x)
+#pragma unroll
+    for (int y = 0; y < NB; ++y) {
+      const int BI = I + 32 * x, BJ = J + 32 * y;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool in = BI < nb && BJ < nb;
+        const int P = in ? perm[2 * BI + (e >> 1)] : 0, Q = in ? perm[2 * BJ + (e & 1)] : 0;
+        const int Rw = 2 * BI + (e >> 1);
+        dstA[x][y][e] = (((P & 1) * 2 + (Q & 1)) * nb + (P >> 1)) * pl + (Q >> 1);
+        dstV[x][y][e] = (((Rw & 1) * 2 + (Q & 1)) * nb + (Rw >> 1)) * pl + (Q >> 1);
+        own[x][y][e] = (((e >> 1) * 2 + (e & 1)) * nb + BI) * pl + BJ;
+      }
+    }
+
+  bool converged = false;
+  int sweep = 0;
+  for (; sweep < JAC_MAX_SWEEPS; ++sweep) {
+    int rotated = 0;
+    for (int r = 0; r < m - 1; ++r) {
+      // 1. rotations of the pairs, from the diagonal blocks
+#pragma unroll
+      for (int x = 0; x < NB; ++x) {
+        const int BI = I + 32 * x;
+        if (x < NB && J + 32 * x == BI && BI < nb) {
+          // this thread owns diagonal block (BI, BI) when y == x
+          float* bl = a[x][x];
+          const float app = bl[0], aqq = bl[3], apq = bl[1];
+          float c = 1.f, sn = 0.f, tt = 0.f;
+          const float thr = JAC_TOL * sqrtf(fabsf(app) * fabsf(aqq));
+          if (fabsf(apq) > thr && fabsf(apq) > abs_floor && fabsf(apq) > 1e-30f) {
+            const float tau = (aqq - app) / (2.f * apq);
+            if (fabsf(tau) > 1e9f) tt = 0.5f / tau;
+            else tt = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+            c = rsqrtf(1.f + tt * tt);
+            sn = tt * c;
+            rotated = 1;
+          }
+          cs[BI] = make_float4(c, sn, tt, 0.f);
+        }
+      }
+      __syncthreads();
+      // 2. rotate own blocks, 3. scatter to the permuted positions
+#pragma unroll
+      for (int x = 0; x < NB; ++x)
+#pragma unroll
+        for (int y = 0; y < NB; ++y) {
+          const int BI = I + 32 * x, BJ = J + 32 * y;
+          if (BI >= nb || BJ >= nb) continue;
+          const float4 ri = cs[BI], rj = cs[BJ];
+          float* b = a[x][y];
+          if (BI == BJ) {
+            const float app = b[0], aqq = b[3], apq = b[1];
+            if (ri.y != 0.f) {
+              b[0] = app - ri.z * apq;
+              b[3] = aqq + ri.z * apq;
+              b[1] = 0.f;
+              b[2] = 0.f;
+            }
+          } else {
+            const float a1 = rj.x * b[0] - rj.y * b[1], b1 = rj.y * b[0] + rj.x * b[1];
+            const float c1 = rj.x * b[2] - rj.y * b[3], d1 = rj.y * b[2] + rj.x * b[3];
+            b[0] = ri.x * a1 - ri.y * c1;
+            b[2] = ri.y * a1 + ri.x * c1;
+            b[1] = ri.x * b1 - ri.y * d1;
+            b[3] = ri.y * b1 + ri.x * d1;
+          }
+          float* w = v[x][y];
+          const float w0 = rj.x * w[0] - rj.y * w[1], w1 = rj.y * w[0] + rj.x * w[1];
+          const float w2 = rj.x * w[2] - rj.y * w[3], w3 = rj.y * w[2] + rj.x * w[3];
+          w[0] = w0; w[1] = w1; w[2] = w2; w[3] = w3;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            PA[dstA[x][y][e]] = b[e];
+            PV[dstV[x][y][e]] = w[e];   // V rows do not move
+          }
+        }
+      __syncthreads();
+      // 4. gather own positions
+#pragma unroll
+      for (int x = 0; x < NB; ++x)
+#pragma unroll
+        for (int y = 0; y < NB; ++y) {
+          const int BI = I + 32 * x, BJ = J + 32 * y;
+          if (BI >= nb || BJ >= nb) continue;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            a[x][y][e] = PA[own[x][y][e]];
+            v[x][y][e] = PV[own[x][y][e]];
+          }
+        }
+    }
+    if (!__syncthreads_or(rotated)) { converged = true; break; }
+  }
+  if (t == 0 && status) {
+    if (!converged) atomicOr(status + bidx * s_bs, ST_NOCONVERGE);
+    atomicMax(status + bidx * s_bs + 1, sweep);
+  }
+  // positions are back to the identity: diagonal = eigenvalues, V columns =
+  // eigenvectors; write them to plain n x n layouts in shared memory
+  float* Dg = PA;                 // [m] eigenvalues
+  float* Vf = PA + m;             // [n][n+1]
+  __syncthreads();
+#pragma unroll
+  for (int x = 0; x < NB; ++x)
+#pragma unroll
+    for (int y = 0; y < NB; ++y) {
+      const int BI = I + 32 * x, BJ = J + 32 * y;
+      if (BI >= nb || BJ >= nb) continue;
+      if (BI == BJ) { Dg[2 * BI] = a[x][y][0]; Dg[2 * BI + 1] = a[x][y][3]; }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = 2 * BI + (e >> 1), c = 2 * BJ + (e & 1);
+        if (r < n && c < n) Vf[r * (n + 1) + c] = v[x][y][e];
+      }
+    }
+  __syncthreads();
+  // descending order, ties to the lower index; sign rule as in jacobi_kernel
+  float* ev = evals + bidx * e_bs;
+  float* vg = evecs + bidx * v_bs;
+  for (int i = t; i < n; i += blockDim.x) {
+    const float li = Dg[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) {
+      const float lj = Dg[j];
+      rank += (lj > li) || (lj == li && j < i);
+    }
+    ev[rank] = li;
+    if (rank < ncols_out) {
+      float big = -1.f, sgn = 1.f;
+      for (int row = 0; row < n; ++row) {
+        const float vv = Vf[row * (n + 1) + i];
+        if (fabsf(vv) > big) { big = fabsf(vv); sgn = vv < 0.f ? -1.f : 1.f; }
+      }
+      for (int row = 0; row < n; ++row) vg[(long long)row * ldv + rank] = sgn * Vf[row * (n + 1) + i];
+    }
+  }
+}
+
 // Cholesky G = R^T R of a sum of split-K partials, right-looking: after
 // column j is scaled by its pivot, the trailing block takes the rank-1 update
 // in parallel.  An exactly zero pivot (a zero column) is kept as a null
@@ -233,6 +443,124 @@ chol_kernel(const float* __restrict__ G, long long g_bs, int n, int nparts, long
   if (t == 0 && bad && status) atomicOr(status + bidx * s_bs, ST_NOTPD);
 }
 
+// The same factorisation for n = N <= 64 in fp32, returning R^{-1} instead
+// of R.  Four threads own each row of L' (thread (r, q) holds columns
+// q*N/4 .. (q+1)*N/4 - 1 in registers).  Step j of the outer-product form:
+// the owners publish column j (c_r = a_rj, r >= j) to shared memory, and
+// after one barrier every row r > j takes a_rk -= c_r c_k / c_j on its own
+// columns j < k <= r; L'[r][j] = c_r / sqrt(c_j) goes to shared memory.  The
+// published column is double-buffered, so one barrier per step suffices.
+// Then X = L'^{-1} (X L' = I, X lower) by substitution along the columns,
+// the four threads of a row summing their partial dot products by shuffle,
+// and R^{-1} = S^{-1} X^T with S the equilibration scales.
+template <int N>
+__global__ void __launch_bounds__(4 * N)
+chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long long part_s,
+                float* __restrict__ Rinv, long long r_bs, int* status, long long s_bs,
+                const int* skip, long long sk_s, float shift) {
+  constexpr int QW = N / 4;
+  constexpr int LD = N + 1;
+  const int u = blockIdx.x;
+  if (skip && skip[u * sk_s]) return;
+  __shared__ float S[N * LD];  // the Gram, then L'
+  __shared__ float rds[N], dsc[N];
+  __shared__ float col[2][N];
+  __shared__ int bad;
+  const int t = threadIdx.x, r = t >> 2, q = t & 3, k0 = q * QW;
+  const float* Gg = G + u * g_bs;
+  if (t == 0) bad = 0;
+  for (int e = t; e < N * N; e += 4 * N) {
+    float v = 0.f;
+    for (int p = 0; p < nparts; ++p) v += Gg[p * part_s + e];
+    S[(e / N) * LD + e % N] = v;
+  }
+  __syncthreads();
+  if (t < N) {
+    const float d = S[t * LD + t];
+    const float sd = d > 0.f ? sqrtf(d) : 0.f;
+    dsc[t] = sd;
+    rds[t] = sd > 0.f ? 1.f / sd : 0.f;
+  }
+  __syncthreads();
+  float a[QW];
+  {
+    const float rr = rds[r];
+#pragma unroll
+    for (int kk = 0; kk < QW; ++kk) {
+      const int k = k0 + kk;
+      float v = 0.f;
+      if (k <= r) {
+        v = 0.5f * (S[r * LD + k] + S[k * LD + r]) * rr * rds[k];
+        if (k == r && rr > 0.f) v += shift;
+      }
+      a[kk] = v;
+    }
+  }
+  __syncthreads();  // S is reused for L' below
+  for (int j = 0; j < N; ++j) {
+    float* cb = col[j & 1];
+    if (q == j / QW && r >= j) {
+      const int jj = j - k0;
+      float v = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < QW; ++kk) v = kk == jj ? a[kk] : v;
+      cb[r] = v;
+    }
+    __syncthreads();
+    if (r >= j) {
+      float d = cb[j];
+      if (!(d >= 0.f)) {
+        if (t == 4 * j) bad = 1;
+        d = 0.f;
+      }
+      const float cr = cb[r];
+      if (q == 0) {
+        const float piv = sqrtf(d);
+        S[r * LD + j] = r == j ? piv : (piv > 0.f ? cr / piv : 0.f);
+      }
+      if (r > j) {
+        const float f = d > 0.f ? cr / d : 0.f;
+#pragma unroll
+        for (int kk = 0; kk < QW; ++kk) {
+          const int k = k0 + kk;
+          if (k > j && k <= r) a[kk] = fmaf(-f, cb[k], a[kk]);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // row r of X = L'^{-1}: sum_{k=j..r} X[r][k] L'[k][j] = delta_rj, j descending
+  float x[QW];
+#pragma unroll
+  for (int kk = 0; kk < QW; ++kk) x[kk] = 0.f;
+  for (int j = N - 1; j >= 0; --j) {
+    float part = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < QW; ++kk) {
+      const int k = k0 + kk;
+      if (k > j && k <= r) part = fmaf(x[kk], S[k * LD + j], part);
+    }
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    if (j <= r && q == j / QW) {
+      const float ljj = S[j * LD + j];
+      const float v = ljj > 0.f ? ((j == r ? 1.f : 0.f) - part) / ljj : 0.f;
+      const int jj = j - k0;
+#pragma unroll
+      for (int kk = 0; kk < QW; ++kk)
+        if (kk == jj) x[kk] = v;
+    }
+  }
+  // R^{-1}[k][r] = X[r][k] / s_k
+  float* Rg = Rinv + u * r_bs;
+#pragma unroll
+  for (int kk = 0; kk < QW; ++kk) {
+    const int k = k0 + kk;
+    Rg[k * N + r] = k <= r ? x[kk] * rds[k] : 0.f;
+  }
+  if (t == 0 && bad && status) atomicOr(status + u * s_bs, ST_NOTPD);
+}
+
 // Out[row] = In[row] R^{-1} for every row of a T x n block, one row per
 // thread (forward substitution x R = z) with the row in registers; R upper
 // triangular in shared memory.  A zero diagonal gives a zero column.
@@ -273,8 +601,27 @@ trsm_rows_kernel(const float* __restrict__ In, float* __restrict__ Out, long lon
 jolt_status launch_jacobi(const float* A, long long a_bs, int lda, int n, int nparts,
                           long long part_s, int batch, float* evals, long long e_bs, float* evecs,
                           long long v_bs, int ldv, int ncols_out, int* status, long long s_bs,
-                          const int* skip, long long sk_s, cudaStream_t st) {
+                          const int* skip, long long sk_s, float abs_tol, cudaStream_t st) {
   if (n <= 0 || n > 128 || batch <= 0) return n <= 0 ? JOLT_OK : JOLT_ERR_INVALID;
+  const int m = n + (n & 1), nb = m / 2;
+  if (nb <= 32) {
+    // register-resident Brent-Luk variant
+    const size_t pl = (size_t)nb + 1;
+    size_t smem = (8 * nb * pl) * sizeof(float) + nb * sizeof(float4) + m * sizeof(int);
+    const size_t need_out = ((size_t)m + (size_t)n * (n + 1)) * sizeof(float);
+    if (smem < need_out) smem = need_out;
+    static bool attr_bl = false;
+    if (!attr_bl) {
+      JOLT_CUDA_TRY(cudaFuncSetAttribute(jacobi_bl_kernel<1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+      attr_bl = true;
+    }
+    jacobi_bl_kernel<1><<<batch, 1024, smem, st>>>(A, a_bs, lda, n, nparts < 1 ? 1 : nparts,
+                                                   part_s, evals, e_bs, evecs, v_bs, ldv,
+                                                   ncols_out, status, s_bs, skip, sk_s, abs_tol);
+    JOLT_LAUNCH_CHECK();
+    return JOLT_OK;
+  }
   const int half = (n + 1) / 2;
   const size_t smem = (size_t)2 * n * (n + 1) * sizeof(float) + 4 * half * sizeof(float) +
                       (2 * half + 4) * sizeof(int);
@@ -286,7 +633,7 @@ jolt_status launch_jacobi(const float* A, long long a_bs, int lda, int n, int np
   }
   jacobi_kernel<<<batch, JAC_THREADS, smem, st>>>(A, a_bs, lda, n, nparts < 1 ? 1 : nparts, part_s,
                                                   evals, e_bs, evecs, v_bs, ldv, ncols_out, status,
-                                                  s_bs, skip, sk_s);
+                                                  s_bs, skip, sk_s, abs_tol);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
@@ -295,6 +642,7 @@ template <typename R>
 static jolt_status chol_launch(const float* G, long long g_bs, int n, int nparts, long long part_s,
                                int batch, float* Rout, long long r_bs, int* status, long long s_bs,
                                const int* skip, long long sk_s, float shift, cudaStream_t st) {
+  nparts = nparts < 1 ? 1 : nparts;
   const size_t smem = (size_t)(n * (n + 1) + n) * sizeof(R);
   static bool attr_set = false;
   if (!attr_set) {
@@ -302,8 +650,8 @@ static jolt_status chol_launch(const float* G, long long g_bs, int n, int nparts
                                        200 * 1024));
     attr_set = true;
   }
-  chol_kernel<R><<<batch, 1024, smem, st>>>(G, g_bs, n, nparts < 1 ? 1 : nparts, part_s, Rout, r_bs,
-                                           status, s_bs, skip, sk_s, shift);
+  chol_kernel<R><<<batch, 1024, smem, st>>>(G, g_bs, n, nparts, part_s, Rout, r_bs, status, s_bs,
+                                           skip, sk_s, shift);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
@@ -318,6 +666,22 @@ jolt_status launch_chol(const float* G, long long g_bs, int n, int nparts, long 
                                sk_s, shift, st);
   return chol_launch<float>(G, g_bs, n, nparts, part_s, batch, Rout, r_bs, status, s_bs, skip,
                             sk_s, shift, st);
+}
+
+jolt_status launch_chol_inv(const float* G, long long g_bs, int n, int nparts, long long part_s,
+                            int batch, float* Rinv, long long r_bs, int* status, long long s_bs,
+                            const int* skip, long long sk_s, float shift, cudaStream_t st) {
+  if (n <= 0 || batch <= 0) return JOLT_OK;
+  nparts = nparts < 1 ? 1 : nparts;
+  switch (n) {
+    case 64: chol_inv_kernel<64><<<batch, 4 * 64, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 48: chol_inv_kernel<48><<<batch, 4 * 48, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 40: chol_inv_kernel<40><<<batch, 4 * 40, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 32: chol_inv_kernel<32><<<batch, 4 * 32, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    default: return JOLT_ERR_INVALID;
+  }
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
 }
 
 jolt_status launch_trsm_rows(const float* In, float* Out, long long blk_bs, const float* R,

@@ -23,6 +23,7 @@
 //   factors and cores rounded to fp16 (the storage type).
 #include "jolt_internal.cuh"
 
+#include <mutex>
 #include <vector>
 
 namespace jolt {
@@ -221,11 +222,22 @@ jolt_status cholqr(const F& c, int T, int Lw, size_t src, size_t mid, size_t dst
                     c.f(L.o_Gram), Lw, 1, ub4, (long long)Lw * Lw, 0.f, skip);
     g.skip_stride = ub4;
     TRY(launch_gemm(g, c.st));
-    TRY(launch_chol(c.f(L.o_Gram), ub4, Lw, ks, (long long)Lw * Lw, c.U, c.f(L.o_Rinv), ub4,
-                    (int*)(c.ws + L.o_status), ub4, skip, ub4, f64, pass == 0 ? shift : 0.f,
-                    c.st));
-    TRY(launch_trsm_rows(c.f(ins[pass]), c.f(outs[pass]), ub4, c.f(L.o_Rinv), ub4, T, Lw, c.U,
-                         skip, ub4, c.st));
+    const float sh = pass == 0 ? shift : 0.f;
+    if (!f64) {
+      // out = in R^{-1} as a plain product (R^{-1} from the Cholesky kernel)
+      TRY(launch_chol_inv(c.f(L.o_Gram), ub4, Lw, ks, (long long)Lw * Lw, c.U, c.f(L.o_Rinv),
+                          ub4, (int*)(c.ws + L.o_status), ub4, skip, ub4, sh, c.st));
+      GemmDesc m = gd(T, Lw, Lw, 1, c.U, 1, opnd(c.ws + ins[pass], JOLT_F32, Lw, 1, 0, ub4),
+                      opnd(c.ws + L.o_Rinv, JOLT_F32, Lw, 1, 0, ub4), c.f(outs[pass]), Lw, 1, ub4,
+                      0, 0.f, skip);
+      m.skip_stride = ub4;
+      TRY(launch_gemm(m, c.st));
+    } else {
+      TRY(launch_chol(c.f(L.o_Gram), ub4, Lw, ks, (long long)Lw * Lw, c.U, c.f(L.o_Rinv), ub4,
+                      (int*)(c.ws + L.o_status), ub4, skip, ub4, true, sh, c.st));
+      TRY(launch_trsm_rows(c.f(ins[pass]), c.f(outs[pass]), ub4, c.f(L.o_Rinv), ub4, T, Lw,
+                           c.U, skip, ub4, c.st));
+    }
   }
   return JOLT_OK;
 }
@@ -248,6 +260,40 @@ jolt_status read_flags_all(const F& c, bool* all) {
 
 unsigned blocks_for(long long n, int tpb = 256) { return (unsigned)((n + tpb - 1) / tpb); }
 
+// A non-blocking side stream per device for the feature stage, which runs
+// alongside the whole-feature token problem (it needs only X).  Callers that
+// share it serialise their feature stages on it; each joins through its own
+// events.
+jolt_status aux_stream(cudaStream_t* out) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  JOLT_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return JOLT_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!streams[dev]) JOLT_CUDA_TRY(cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking));
+  *out = streams[dev];
+  return JOLT_OK;
+}
+
+struct EventPair {
+  cudaEvent_t a = nullptr, b = nullptr;
+  ~EventPair() {
+    if (a) cudaEventDestroy(a);
+    if (b) cudaEventDestroy(b);
+  }
+};
+
+// On every exit (errors included) the caller's stream waits for all the
+// side-stream work, so that the workspace is never released under it.
+struct JoinGuard {
+  cudaStream_t st = nullptr, fs = nullptr;
+  cudaEvent_t ev = nullptr;
+  ~JoinGuard() {
+    if (ev && fs && fs != st && cudaEventRecord(ev, fs) == cudaSuccess) cudaStreamWaitEvent(st, ev, 0);
+  }
+};
+
 }  // namespace
 
 jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketch, char* ws,
@@ -265,45 +311,67 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   JOLT_LAUNCH_CHECK();
 
   const bool tc = gram_tc_supported(L);
+  // The whole-feature token problem (r_d = D) reads only X: the feature
+  // stage runs beside it on a side stream and the truncated ranks join it.
+  const bool overlap = RT > 0 && L.hasFullD && RD > 0;
+  cudaStream_t fs = st;
+  EventPair ev;
+  if (overlap) {
+    TRY(aux_stream(&fs));
+    JOLT_CUDA_TRY(cudaEventCreateWithFlags(&ev.a, cudaEventDisableTiming));
+    JOLT_CUDA_TRY(cudaEventCreateWithFlags(&ev.b, cudaEventDisableTiming));
+    JOLT_CUDA_TRY(cudaEventRecord(ev.a, st));
+    JOLT_CUDA_TRY(cudaStreamWaitEvent(fs, ev.a, 0));
+  }
+  JoinGuard join_guard;
+  if (overlap) { join_guard.st = st; join_guard.fs = fs; join_guard.ev = ev.a; }
   // ---- feature mode: S_d, split over groups of hg heads, f64 reduction
   {
     const int hg = H / L.nsplit;
     if (tc && (hg * T) % 64 == 0) {
-      TRY(gram_feat_tc(L, U, X, ws, st));
+      TRY(gram_feat_tc(L, U, X, ws, fs));
     } else {
       TRY(launch_gemm(gd(D, D, T, hg, U, L.nsplit,
                          opnd(X, xdt, 1, D, (long long)T * D, xu, (long long)hg * T * D),
                          opnd(X, xdt, D, 1, (long long)T * D, xu, (long long)hg * T * D),
                          c.f(L.o_Sdp), D, 1, ub4, (long long)D * D),
-                      st));
+                      fs));
     }
-    reduce_splits_kernel<<<dim3(blocks_for(D * D), U), 256, 0, st>>>(ws, ub, L.o_Sdp, L.o_Sd,
+    reduce_splits_kernel<<<dim3(blocks_for(D * D), U), 256, 0, fs>>>(ws, ub, L.o_Sdp, L.o_Sd,
                                                                      L.nsplit, D * D);
     JOLT_LAUNCH_CHECK();
     TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, 1, 0, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
-                      status, ub4, nullptr, 0, st));
+                      status, ub4, nullptr, 0, JAC_ABS_EXACT, fs));
   }
   if (RD > 0) {
-    round_f16_kernel<<<dim3(blocks_for(D * RD), 1, U), 256, 0, st>>>(ws, ub, L.o_Vd, D, L.o_Ud16,
+    round_f16_kernel<<<dim3(blocks_for(D * RD), 1, U), 256, 0, fs>>>(ws, ub, L.o_Vd, D, L.o_Ud16,
                                                                      RD, D, RD, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
     TRY(launch_gemm(gd(H * T, RD, D, 1, U, 1, opnd(X, xdt, D, 1, 0, xu),
                        opnd(ws + L.o_Vd, JOLT_F32, D, 1, 0, ub4), c.f(L.o_Y), RD, 1, ub4, 0),
-                    st));
-    round_f16_kernel<<<dim3(blocks_for((long long)H * T * RD), 1, U), 256, 0, st>>>(
+                    fs));
+    round_f16_kernel<<<dim3(blocks_for((long long)H * T * RD), 1, U), 256, 0, fs>>>(
         ws, ub, L.o_Y, RD, L.o_Y16, RD, H * T, RD, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
   }
+  if (overlap) JOLT_CUDA_TRY(cudaEventRecord(ev.b, fs));
   if (RT == 0) return JOLT_OK;
 
   // ---- token mode, one feature rank at a time
   const bool exact = (L.token_mode == JOLT_TOKEN_EXACT);
   const int Lw = exact ? L.L : L.ell;
-  bool st_started = false, sub_started = false;
-  int prev = 0;
-  for (int id = 0; id < L.nd; ++id) {
+  bool sub_started = false, yt_ready = false, joined = !overlap;
+  const bool ytc = exact && T > 128 && ygram_tc_supported(L);
+  // largest feature rank first (the whole-feature problem, when present,
+  // overlaps the feature stage); each next rank warm-starts from the last
+  for (int oi = L.nd - 1; oi >= 0; --oi) {
+    const int id = oi;
     const int rdv = L.rd[id];
     const bool full = (rdv == D);
+    if (!full && !joined) {
+      JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
+      joined = true;
+    }
     const void* Ab;
     int adt;
     long long as_t, aseg, aub;
@@ -321,19 +389,20 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
                              opnd(X, xdt, 1, D, (long long)T * D, xu), c.f(L.o_ST), T, 1, ub4, 0),
                           st));
         }
+      } else if (ytc) {
+        if (!yt_ready) TRY(ytrans(L, U, ws, st));
+        yt_ready = true;
+        TRY(ygram_tc(L, U, ws, 0, rdv, 0.f, st));
       } else {
-        const float* Y0 = (const float*)(ws + L.o_Y) + prev;
-        TRY(launch_gemm(gd(T, T, rdv - prev, H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),
-                           opnd(Y0, JOLT_F32, 1, RD, aseg, ub4), c.f(L.o_ST), T, 1, ub4, 0,
-                           st_started ? 1.f : 0.f),
+        const float* Y0 = (const float*)(ws + L.o_Y);
+        TRY(launch_gemm(gd(T, T, rdv, H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),
+                           opnd(Y0, JOLT_F32, 1, RD, aseg, ub4), c.f(L.o_ST), T, 1, ub4, 0),
                         st));
-        st_started = true;
-        prev = rdv;
       }
       if (T <= 128) {
         // direct solve of the whole token Gram
         TRY(launch_jacobi(c.f(L.o_ST), ub4, T, T, 1, 0, U, c.f(L.o_theta), ub4, c.f(oUT), ub4, RT,
-                          RT, status, ub4, nullptr, 0, st));
+                          RT, status, ub4, nullptr, 0, JAC_ABS_EXACT, st));
         copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, T, oEV, 1,
                                                                   RT);
         JOLT_LAUNCH_CHECK();
@@ -377,7 +446,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
           g.skip_stride = ub4;
           TRY(launch_gemm(g, st));
           TRY(launch_jacobi(c.f(L.o_Hm), ub4, Lw, Lw, L.ks, (long long)Lw * Lw, U, c.f(L.o_theta),
-                            ub4, c.f(L.o_Wm), ub4, Lw, Lw, status, ub4, flags, ub4, st));
+                            ub4, c.f(L.o_Wm), ub4, Lw, Lw, status, ub4, flags, ub4, JAC_ABS_RR, st));
           // Ritz vectors V2 = V W and Z2 = Z W = S V2
           g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + L.o_V, JOLT_F32, Lw, 1, 0, ub4),
                  opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_V2), Lw, 1, ub4, 0, 0.f, flags);
@@ -433,7 +502,8 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
                          c.f(L.o_Hm), ell, 1, ub4, (long long)ell * ell),
                       st));
       TRY(launch_jacobi(c.f(L.o_Hm), ub4, ell, ell, hs, (long long)ell * ell, U, c.f(L.o_theta),
-                        ub4, c.f(L.o_Wm), ub4, ell, RT, status, ub4, nullptr, 0, st));
+                        ub4, c.f(L.o_Wm), ub4, ell, RT, status, ub4, nullptr, 0, JAC_ABS_EXACT,
+                        st));
       TRY(launch_gemm(gd(T, RT, ell, 1, U, 1, opnd(ws + L.o_V, JOLT_F32, ell, 1, 0, ub4),
                          opnd(ws + L.o_Wm, JOLT_F32, ell, 1, 0, ub4), c.f(oUT), RT, 1, ub4, 0),
                       st));
@@ -450,6 +520,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
         ws, ub, oG, rdv, L.o_G16 + (size_t)id * H * RT * D * 2, rdv, H * RT, rdv, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
   }
+  if (!joined) JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
   round_f16_kernel<<<dim3(blocks_for((long long)L.nd * T * RT), 1, U), 256, 0, st>>>(
       ws, ub, L.o_UT32, RT, L.o_UT16, RT, L.nd * T, RT, 0, 0, 1);
   JOLT_LAUNCH_CHECK();

@@ -385,6 +385,146 @@ __global__ void split_v_kernel(const char* ws, size_t ub, size_t o_V, size_t o_V
   }
 }
 
+// Token Gram increments S[u] (+)= A A^T with A = Yt[u][:, k0:k1] (T x (k1-k0)),
+// on kind::tf32 with the three-product split (A_hi A_hi^T + A_hi A_lo^T +
+// A_lo A_hi^T).  Yt[u] is [T][RD*H] fp32 with column j*H + h = Y[u][h][:, j],
+// so that the feature ranks j0 <= j < j1 of an increment are one contiguous
+// column range.  Upper-triangular 128 x 128 tiles, mirrored; S = beta S + ...
+constexpr int YG_STAGES = 2;
+constexpr int YG_A = TILE * 32 * 4;          // 16 KB: 128 rows x 32 k
+constexpr int YG_STAGE = 4 * YG_A;           // A hi, A lo, B hi, B lo
+
+struct YgArgs {
+  int T, k0, k1, nt;
+  float beta;
+  float* S;
+  long long s_us;
+  char* ws;
+  size_t ub, o_status;
+};
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+ygram_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constant__ CUtensorMap tL,
+                YgArgs a) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  struct Bars { uint64_t full[YG_STAGES], empty[YG_STAGES], accum; uint32_t tmem; };
+  Bars* S = (Bars*)(base + YG_STAGES * YG_STAGE);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int u = blockIdx.y;
+  int mi = 0, idx = blockIdx.x;
+  while (idx >= a.nt - mi) { idx -= a.nt - mi; ++mi; }
+  const int ni = mi + idx;
+  const bool diag = (mi == ni);
+  const int klen = a.k1 - a.k0;
+  const int nk = (klen + 31) / 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < YG_STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&S->accum), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), TILE);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    const uint32_t bytes = diag ? 2 * YG_A : 4 * YG_A;
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % YG_STAGES, r = kk / YG_STAGES;
+      if (r > 0 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), (r - 1) & 1)) { ok = false; break; }
+      const uint32_t fb = tc::smem_u32(&S->full[s]);
+      tc::mbar_expect_tx(fb, bytes);
+      const uint32_t sa = tc::smem_u32(base + s * YG_STAGE);
+      const int kc = a.k0 + kk * 32;
+      tc::tma_load_3d(sa, &tH, kc, mi * TILE, u, fb);
+      tc::tma_load_3d(sa + YG_A, &tL, kc, mi * TILE, u, fb);
+      if (!diag) {
+        tc::tma_load_3d(sa + 2 * YG_A, &tH, kc, ni * TILE, u, fb);
+        tc::tma_load_3d(sa + 3 * YG_A, &tL, kc, ni * TILE, u, fb);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                               ((uint32_t)(TILE >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
+    bool first = true;
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % YG_STAGES, r = kk / YG_STAGES;
+      if (!tc::mbar_wait(tc::smem_u32(&S->full[s]), r & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(base + s * YG_STAGE);
+      const uint32_t sb = diag ? sa : sa + 2 * YG_A;
+      const int steps = min(4, (klen - kk * 32) / 8);   // K ranges are multiples of 8
+      for (int k4 = 0; k4 < steps; ++k4) {
+        const uint64_t ah = tc::sdesc_sw128(sa + 32 * k4, 16, 1024);
+        const uint64_t al = tc::sdesc_sw128(sa + YG_A + 32 * k4, 16, 1024);
+        const uint64_t bh = tc::sdesc_sw128(sb + 32 * k4, 16, 1024);
+        const uint64_t bl = tc::sdesc_sw128(sb + YG_A + 32 * k4, 16, 1024);
+        tc::mma_tf32(tmem, ah, bh, idesc, first ? 0u : 1u);
+        tc::mma_tf32(tmem, ah, bl, idesc, 1);
+        tc::mma_tf32(tmem, al, bh, idesc, 1);
+        first = false;
+      }
+      tc::mma_commit(tc::smem_u32(&S->empty[s]));
+    }
+    tc::mma_commit(tc::smem_u32(&S->accum));
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    if (!tc::mbar_wait(tc::smem_u32(&S->accum), 0)) {
+      ok = false;
+    } else {
+      tc::tc_fence_after();
+      float* C = a.S + (long long)u * a.s_us;
+      const int T = a.T;
+      const float beta = a.beta;
+      drain(tmem, q, [&](int rt, int c0, const float (&v)[32]) {
+        const int row = mi * TILE + rt;
+        if (row < T) {
+          float* cr = C + (long long)row * T + ni * TILE + c0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (ni * TILE + c0 + j < T) cr[j] = beta != 0.f ? cr[j] + v[j] : v[j];
+        }
+        if (!diag) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = ni * TILE + c0 + j;
+            if (col < T && row < T) {
+              float* c = C + (long long)col * T + row;
+              *c = beta != 0.f ? *c + v[j] : v[j];
+            }
+          }
+        }
+      });
+    }
+  }
+  if (!ok) atomicOr((int*)(a.ws + (size_t)u * a.ub + a.o_status), ST_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, TILE);
+}
+
+// Yt[u][t][j*H + h] = Y[u][h][t][j] and its tf32 low part.
+__global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt, int H, int T,
+                              int RD) {
+  const int u = blockIdx.y;
+  const float* Y = (const float*)(ws + (size_t)u * ub + o_Y);
+  float* Yt = (float*)((char*)ws + (size_t)u * ub + o_Yt);
+  float* Ytl = Yt + (size_t)T * RD * H;
+  const int K = RD * H;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)T * K;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / K), c = (int)(e % K), j = c / H, h = c % H;
+    const float v = Y[((long long)h * T + t) * RD + j];
+    Yt[e] = v;
+    Ytl[e] = v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -522,6 +662,54 @@ jolt_status sv_tc(const Layout& L, int U, char* ws, const int* flags, cudaStream
   }
   dim3 grid((L.T + TILE - 1) / TILE, U);
   sv_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tS, tSl, tV, tVl, a);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+bool ygram_tc_supported(const Layout& L) {
+  if (!(L.o_Yt != 0 && encode_fn() != nullptr)) return false;
+  for (int i = 0; i < L.ndt; ++i)
+    if ((L.rd[i] * L.H) % 8) return false;
+  return true;
+}
+
+// Yt = relayout of Y (once per factor call).
+jolt_status ytrans(const Layout& L, int U, char* ws, cudaStream_t st) {
+  dim3 grid(512, U);
+  ytrans_kernel<<<grid, 256, 0, st>>>(ws, L.unit_bytes, L.o_Y, L.o_Yt, L.H, L.T, L.RD);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+// S_T += (beta = 1) or = (beta = 0) the Gram of feature ranks [j0, j1).
+jolt_status ygram_tc(const Layout& L, int U, char* ws, int j0, int j1, float beta,
+                     cudaStream_t st) {
+  const size_t ub = L.unit_bytes;
+  const int K = L.RD * L.H;
+  CUtensorMap tH, tL;
+  const cuuint64_t d[3] = {(cuuint64_t)K, (cuuint64_t)L.T, (cuuint64_t)U};
+  const cuuint64_t sd[2] = {(cuuint64_t)K * 4, (cuuint64_t)ub};
+  const cuuint32_t box[3] = {32, TILE, 1};
+  const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!make_map(&tH, ws + L.o_Yt, 3, d, sd, box, f32) ||
+      !make_map(&tL, ws + L.o_Yt + (size_t)L.T * K * 4, 3, d, sd, box, f32))
+    return JOLT_ERR_CUDA;
+  YgArgs a;
+  a.T = L.T; a.k0 = j0 * L.H; a.k1 = j1 * L.H;
+  a.nt = (L.T + TILE - 1) / TILE;
+  a.beta = beta;
+  a.S = (float*)(ws + L.o_ST);
+  a.s_us = (long long)ub / 4;
+  a.ws = ws; a.ub = ub; a.o_status = L.o_status;
+  const size_t smem = (size_t)YG_STAGES * YG_STAGE + 1024 + 256;
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(ygram_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    attr = true;
+  }
+  dim3 grid(a.nt * (a.nt + 1) / 2, U);
+  ygram_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tH, tL, a);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

@@ -70,6 +70,7 @@ struct Layout {
   size_t o_V, o_Z, o_V2, o_Z2, o_Hm, o_Wm, o_theta, o_Gram, o_Rinv, o_flag;
   size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
   size_t o_STs, o_Vs;    // tf32 low parts of S_T and V (tensor-core S V)
+  size_t o_Yt;           // Y relaid [T][RD*H] and its tf32 low part (token Gram)
   size_t unit_bytes;
 };
 
@@ -100,11 +101,14 @@ jolt_status launch_gemm(const GemmDesc& g, cudaStream_t st);
 // in: A[b] = sum over nparts partials at A + b*a_bstride + k*part_s, row
 // stride lda.  out: evals[b][n] descending, evecs[b] with column i the i-th
 // eigenvector (row stride ldv, first ncols_out columns written).
+// abs_tol: rotations with |a_pq| below abs_tol * ||A||_F are not taken.
+constexpr float JAC_ABS_EXACT = 1e-10f;
+constexpr float JAC_ABS_RR = 1e-7f;
 jolt_status launch_jacobi(const float* A, long long a_bstride, int lda, int n, int nparts,
                           long long part_s, int batch, float* evals, long long e_bstride,
                           float* evecs, long long v_bstride, int ldv, int ncols_out, int* status,
                           long long status_bstride, const int* skip, long long skip_stride,
-                          cudaStream_t st);
+                          float abs_tol, cudaStream_t st);
 // Batched Cholesky G = R^T R of a sum of nparts partials (n x n, n <= 128;
 // n <= 64 in f64), writes the upper factor R in f32.  The Gram is
 // equilibrated to a unit diagonal first; `shift` is added to that diagonal.
@@ -112,6 +116,11 @@ jolt_status launch_chol(const float* G, long long g_bstride, int n, int nparts, 
                         int batch, float* R, long long r_bstride, int* status,
                         long long status_bstride, const int* skip, long long skip_stride,
                         bool f64, float shift, cudaStream_t st);
+// The same Cholesky (fp32, n in {32, 40, 48, 64}) writing R^{-1} instead of R.
+jolt_status launch_chol_inv(const float* G, long long g_bstride, int n, int nparts,
+                            long long part_s, int batch, float* Rinv, long long r_bstride,
+                            int* status, long long status_bstride, const int* skip,
+                            long long skip_stride, float shift, cudaStream_t st);
 // Out[b] = In[b] R[b]^{-1} for a T x n block per batch entry, row-parallel.
 jolt_status launch_trsm_rows(const float* In, float* Out, long long blk_bstride, const float* R,
                              long long r_bstride, int T, int n, int batch, const int* skip,
@@ -124,6 +133,10 @@ jolt_status gram_feat_tc(const Layout& L, int n_units, const void* X, char* ws, 
 bool sv_tc_supported(const Layout& L);
 jolt_status split_tok_gram(const Layout& L, int n_units, char* ws, cudaStream_t st);
 jolt_status sv_tc(const Layout& L, int n_units, char* ws, const int* flags, cudaStream_t st);
+bool ygram_tc_supported(const Layout& L);
+jolt_status ytrans(const Layout& L, int n_units, char* ws, cudaStream_t st);
+jolt_status ygram_tc(const Layout& L, int n_units, char* ws, int j0, int j1, float beta,
+                     cudaStream_t st);
 
 // ------------------------------------------------------------------ steps
 jolt_status factor_run(const Layout& L, int n_units, const void* X, const float* sketch,

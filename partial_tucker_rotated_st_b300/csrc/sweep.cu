@@ -225,8 +225,9 @@ __global__ void __launch_bounds__(SW_THREADS, 2) sweep_kernel(SweepArgs a) {
   // ---- r_T = T, truncated r_d: X~ Q^T = Y16 (Q U_d)^T, prefix over r_d
   if (a.hasFullT && a.ndt > 0) {
     const __half* Yh = (const __half*)(base + a.o_Y16) + (long long)h * a.T * a.RD;
+    // consecutive threads take consecutive rows: conflict-free stores
     for (int i = threadIdx.x; i < TILE * a.RD; i += SW_THREADS) {
-      const int row = i / a.RD, j = i % a.RD, t = t0 + row;
+      const int row = i % TILE, j = i / TILE, t = t0 + row;
       Ks[j * TILE + row] = (t < a.T) ? __half2float(Yh[(long long)t * a.RD + j]) : 0.f;
     }
     const float* QU = (const float*)(base + a.o_QUd);
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(SW_THREADS, 2) sweep_kernel(SweepArgs a) {
     for (int id = 0; id < a.nd; ++id) {
       const __half* Ug = (const __half*)(base + a.o_UT16) + (long long)id * a.T * a.RT;
       for (int i = threadIdx.x; i < TILE * a.RT; i += SW_THREADS) {
-        const int row = i / a.RT, k = i % a.RT, t = t0 + row;
+        const int row = i % TILE, k = i / TILE, t = t0 + row;
         Ks[k * TILE + row] = (t < a.T) ? __half2float(Ug[(long long)t * a.RT + k]) : 0.f;
       }
       const float* Wg = (const float*)(base + a.o_W) + ((long long)id * a.H + h) * a.RT * D;
