@@ -215,14 +215,20 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(EncArgs a) 
   const float qmax = (float)((1 << (b - 1)) - 1);
   const int qoff = 1 << (b - 1);
   const int nbytes = D * b / 8;
-#pragma unroll
+  // one row at a time, not unrolled (the row's values are picked out of the
+  // register arrays by static selects, which keeps the code small)
+#pragma unroll 1
   for (int r = 0; r < CD_ROWS; ++r) {
     const int t = t0 + w * CD_ROWS + r;
     float yh[EPT], yl[EPT];
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
-      yh[e] = ah[r][e] * sg[e];
-      yl[e] = al[r][e] * sg[e];
+      float vh = ah[0][e], vl = al[0][e];
+#pragma unroll
+      for (int rr = 1; rr < CD_ROWS; ++rr)
+        if (rr == r) { vh = ah[rr][e]; vl = al[rr][e]; }
+      yh[e] = vh * sg[e];
+      yl[e] = vl * sg[e];
     }
     fwht_row_df<EPT>(yh, yl, lane);
     // times 1/sqrt(D), renormalised so that yh is the fp32 rounding of y

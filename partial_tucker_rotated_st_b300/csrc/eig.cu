@@ -465,14 +465,22 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
   __shared__ float S[N * LD];  // the Gram, then L'
   __shared__ float rds[N], dsc[N];
   __shared__ float col[2][N];
+  __shared__ float rpiv[N];   // 1 / L'[j][j]
   __shared__ int bad;
   const int t = threadIdx.x, r = t >> 2, q = t & 3, k0 = q * QW;
   const float* Gg = G + u * g_bs;
   if (t == 0) bad = 0;
-  for (int e = t; e < N * N; e += 4 * N) {
-    float v = 0.f;
-    for (int p = 0; p < nparts; ++p) v += Gg[p * part_s + e];
-    S[(e / N) * LD + e % N] = v;
+  constexpr int PER = N / 4;   // N * N / (4 N) elements per thread
+  float gv[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) gv[i] = Gg[t + i * 4 * N];
+  for (int p = 1; p < nparts; ++p)
+#pragma unroll
+    for (int i = 0; i < PER; ++i) gv[i] += Gg[p * part_s + t + i * 4 * N];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = t + i * 4 * N;
+    S[(e / N) * LD + e % N] = gv[i];
   }
   __syncthreads();
   if (t < N) {
@@ -514,12 +522,13 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
         d = 0.f;
       }
       const float cr = cb[r];
+      const float rp = d > 0.f ? rsqrtf(d) : 0.f;  // 1 / sqrt(c_j)
       if (q == 0) {
-        const float piv = sqrtf(d);
-        S[r * LD + j] = r == j ? piv : (piv > 0.f ? cr / piv : 0.f);
+        S[r * LD + j] = r == j ? d * rp : cr * rp;
+        if (r == j) rpiv[j] = rp;
       }
       if (r > j) {
-        const float f = d > 0.f ? cr / d : 0.f;
+        const float f = cr * rp * rp;
 #pragma unroll
         for (int kk = 0; kk < QW; ++kk) {
           const int k = k0 + kk;
@@ -534,17 +543,18 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
 #pragma unroll
   for (int kk = 0; kk < QW; ++kk) x[kk] = 0.f;
   for (int j = N - 1; j >= 0; --j) {
-    float part = 0.f;
+    float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < QW; ++kk) {
+    for (int kk = 0; kk < QW; kk += 2) {
       const int k = k0 + kk;
-      if (k > j && k <= r) part = fmaf(x[kk], S[k * LD + j], part);
+      if (k > j && k <= r) p0 = fmaf(x[kk], S[k * LD + j], p0);
+      if (k + 1 > j && k + 1 <= r) p1 = fmaf(x[kk + 1], S[(k + 1) * LD + j], p1);
     }
+    float part = p0 + p1;
     part += __shfl_xor_sync(0xffffffffu, part, 1);
     part += __shfl_xor_sync(0xffffffffu, part, 2);
     if (j <= r && q == j / QW) {
-      const float ljj = S[j * LD + j];
-      const float v = ljj > 0.f ? ((j == r ? 1.f : 0.f) - part) / ljj : 0.f;
+      const float v = ((j == r ? 1.f : 0.f) - part) * rpiv[j];
       const int jj = j - k0;
 #pragma unroll
       for (int kk = 0; kk < QW; ++kk)
