@@ -118,7 +118,6 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
     return o;
   };
   L.o_status = sect(256);
-  L.o_flag = sect(256);
   L.o_Sd = sect((size_t)D * D * 4);
   L.o_Sdp = sect((size_t)L.nsplit * D * D * 4);
   L.o_evd = sect((size_t)D * 4);
@@ -127,23 +126,9 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   L.o_QUd = sect((size_t)RD * D * 4);
   L.o_Y = sect((size_t)H * T * RD * 4);
   L.o_Y16 = sect((size_t)H * T * RD * 2);
-  L.o_ST = sect((RT > 0 && L.token_mode == JOLT_TOKEN_EXACT) ? (size_t)T * T * 4 : 0);
-  const bool svtc = RT > 0 && L.token_mode == JOLT_TOKEN_EXACT && T > 128 && L.L == 64;
-  L.o_STs = svtc ? sect((size_t)T * T * 4) : 0;
-  L.o_Vs = svtc ? sect((size_t)2 * T * 64 * 4) : 0;   // V^T and its tf32 low part
+  const bool exact = RT > 0 && L.token_mode == JOLT_TOKEN_EXACT;
+  const bool svtc = exact && T > 128 && L.L == 64;
   L.o_Yt = (svtc && RD > 0) ? sect((size_t)2 * T * RD * H * 4) : 0;
-  const size_t blk = iter ? (size_t)T * Lw * 4 : 0;
-  L.o_V = sect(blk);
-  L.o_Z = sect(blk);
-  L.o_V2 = sect(blk);
-  L.o_Z2 = sect(blk);
-  const size_t sq = RT > 0 ? (size_t)Lw * Lw * 4 : 0;
-  const int nparts = L.ks > L.hs ? L.ks : L.hs;
-  L.o_Hm = sect(sq * nparts);
-  L.o_Wm = sect(sq);
-  L.o_Gram = sect(sq * L.ks);
-  L.o_Rinv = sect(sq);
-  L.o_theta = sect((size_t)(Lw > T ? Lw : T) * 4);
   L.o_UT32 = sect((size_t)L.nd * T * RT * 4);
   L.o_UT16 = sect((size_t)L.nd * T * RT * 2);
   L.o_tokev = sect((size_t)L.nd * RT * 4);
@@ -154,6 +139,31 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   L.o_part = sect((size_t)L.ntiles * (L.ncand + 1) * 4);
   L.o_P = sect((RT > 0 && L.token_mode == JOLT_TOKEN_RANDOMIZED) ? (size_t)H * Dmax * L.ell * 4 : 0);
   L.unit_bytes = align_up(off, 256);
+
+  // one token problem per feature rank
+  L.nprob = RT > 0 ? L.nd : 0;
+  off = 0;
+  L.p_status = sect(256);
+  L.p_flag = sect(256);
+  L.p_ST = exact ? sect((size_t)T * T * 4) : 0;
+  L.p_STs = svtc ? sect((size_t)T * T * 4) : 0;
+  L.p_Vs = svtc ? sect((size_t)2 * T * 64 * 4) : 0;   // V^T and its tf32 low part
+  const size_t blk = iter ? (size_t)T * Lw * 4 : 0;
+  L.p_V = sect(blk);
+  L.p_Z = sect(blk);
+  L.p_V2 = sect(blk);
+  L.p_Z2 = sect(blk);
+  const size_t sq = RT > 0 ? (size_t)Lw * Lw * 4 : 0;
+  const int nparts = L.ks > L.hs ? L.ks : L.hs;
+  L.p_Hm = sect(sq * nparts);
+  L.p_Wm = sect(sq);
+  L.p_Gram = sect(sq * L.ks);
+  L.p_Rinv = sect(sq);
+  L.p_theta = sect((size_t)(Lw > T ? Lw : T) * 4);
+  L.p_UT = sect((size_t)T * RT * 4);
+  L.p_ev = sect((size_t)RT * 4);
+  L.prob_bytes = L.nprob > 0 ? align_up(off, 256) : 0;
+  L.unit_total = L.unit_bytes + (size_t)L.nprob * L.prob_bytes;
   *Lp = L;
   return JOLT_OK;
 }
@@ -172,7 +182,7 @@ using namespace jolt;
 static cudaStream_t S(void* s) { return (cudaStream_t)s; }
 
 static bool ws_ok(const Layout& L, int n, const void* ws, size_t ws_bytes) {
-  return ws && ((uintptr_t)ws % 256 == 0) && ws_bytes >= (size_t)n * L.unit_bytes;
+  return ws && ((uintptr_t)ws % 256 == 0) && ws_bytes >= (size_t)n * L.unit_total;
 }
 
 extern "C" {
@@ -186,7 +196,7 @@ int jolt_num_candidates(const jolt_config* cfg) {
 size_t jolt_workspace_size(const jolt_config* cfg) {
   Layout L;
   if (make_layout(cfg, &L) != JOLT_OK) return 0;
-  return L.unit_bytes;
+  return L.unit_total;
 }
 
 jolt_status jolt_factor_group(const jolt_config* cfg, int n_units, const void* X,

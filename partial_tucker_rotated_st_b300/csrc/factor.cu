@@ -171,13 +171,62 @@ __global__ void set_int_kernel(char* ws, size_t ub, size_t o, int v) {
   if (threadIdx.x == 0) *(int*)(ws + blockIdx.x * ub + o) = v;
 }
 
-// Helpers building GemmDesc over the batch of units (b1 = unit).
+// Truncated problem p = u * ndt + id starts from the whole-feature problem's
+// converged Ritz basis of unit u: V[p] = V[full u].
+__global__ void warm_copy_kernel(char* pbase, size_t pb, size_t o_V, int ndt, const char* fbase,
+                                 long long n) {
+  const int p = blockIdx.y, u = p / ndt;
+  const float* src = (const float*)(fbase + (size_t)u * pb + o_V);
+  float* dst = (float*)(pbase + (size_t)p * pb + o_V);
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (long long)gridDim.x * blockDim.x)
+    dst[e] = src[e];
+}
+
+// Token factors and eigenvalues of every problem into its unit's sections
+// (U_T of rank id at o_UT + id * T * RT, eigenvalues at o_ev + id * RT), and
+// the problem's status bits OR-ed into the unit's status.
+__global__ void scatter_problems_kernel(char* ws, size_t ub, size_t o_UT, size_t o_ev,
+                                        size_t o_status, const char* pbase, size_t pb,
+                                        size_t p_UT, size_t p_ev, int ev_ld, size_t p_status,
+                                        int U, int ndt, int T, int RT) {
+  const int id = blockIdx.y, u = blockIdx.z;
+  const int p = id < ndt ? u * ndt + id : U * ndt + u;
+  const char* pr = pbase + (size_t)p * pb;
+  char* un = ws + (size_t)u * ub;
+  const float* src = (const float*)(pr + p_UT);
+  float* dst = (float*)(un + o_UT) + (size_t)id * T * RT;
+  const long long n = (long long)T * RT;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (long long)gridDim.x * blockDim.x)
+    dst[e] = src[e];
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < RT; i += blockDim.x)
+      ((float*)(un + o_ev))[id * RT + i] = ((const float*)(pr + p_ev))[i * ev_ld];
+    if (threadIdx.x == 0) {
+      const int sv = *(const int*)(pr + p_status);
+      if (sv) atomicOr((int*)(un + o_status), sv);
+    }
+  }
+}
+
+// The batch of units of one call (unit u at ws + u * unit_bytes).
 struct F {
   const Layout& L;
   char* ws;
   int U;
   cudaStream_t st;
   float* f(size_t o) const { return (float*)(ws + o); }
+};
+
+// A set of token problems: np problems at base + i * stride, offsets p_*.
+struct PS {
+  char* base;
+  size_t stride;
+  int np;
+  long long s4() const { return (long long)stride / 4; }
+  float* f(size_t o) const { return (float*)(base + o); }
+  char* c(size_t o) const { return base + o; }
 };
 
 Opnd opnd(const void* p, int dt, long long s0, long long s1, long long sseg = 0, long long sb1 = 0,
@@ -203,55 +252,57 @@ GemmDesc gd(int M, int N, int K, int nseg, int nb1, int nb2, Opnd A, Opnd B, flo
   } while (0)
 
 
-// dst <- orth(src) by CholeskyQR through mid; T x Lw per unit.  passes = 2
-// is CholeskyQR2 (Fukaya et al. 2014); `shift` > 0 shifts the first pass
+// dst <- orth(src) by CholeskyQR through mid; T x Lw per problem.  passes =
+// 2 is CholeskyQR2 (Fukaya et al. 2014); `shift` > 0 shifts the first pass
 // (shifted CholeskyQR, Fukaya et al. 2020) for nearly dependent columns.
 // Each pass: Gram split over L.ks row chunks (the partials are summed inside
-// the Cholesky kernel), Cholesky R, then out = in R^{-1} row by row.  With
-// one pass the result goes straight to dst.  src and dst may be the same.
-jolt_status cholqr(const F& c, int T, int Lw, size_t src, size_t mid, size_t dst, const int* skip,
-                   bool f64, int passes, float shift) {
-  const Layout& L = c.L;
-  const long long ub4 = (long long)L.unit_bytes / 4;
+// the Cholesky kernel), Cholesky R, then out = in R^{-1}.  With one pass the
+// result goes straight to dst.  Problems whose flag is set are skipped when
+// `use_flags`.
+jolt_status cholqr(const Layout& L, const PS& P, int T, int Lw, size_t src, size_t mid, size_t dst,
+                   bool use_flags, bool f64, int passes, float shift, cudaStream_t st) {
+  const long long s4 = P.s4();
   const int ks = L.ks, kc = T / L.ks;
+  const int* skip = use_flags ? (const int*)P.c(L.p_flag) : nullptr;
+  int* status = (int*)P.c(L.p_status);
   const size_t ins[2] = {src, mid}, outs[2] = {passes == 1 ? dst : mid, dst};
   for (int pass = 0; pass < passes; ++pass) {
-    GemmDesc g = gd(Lw, Lw, kc, 1, c.U, ks,
-                    opnd(c.ws + ins[pass], JOLT_F32, 1, Lw, 0, ub4, (long long)kc * Lw),
-                    opnd(c.ws + ins[pass], JOLT_F32, Lw, 1, 0, ub4, (long long)kc * Lw),
-                    c.f(L.o_Gram), Lw, 1, ub4, (long long)Lw * Lw, 0.f, skip);
-    g.skip_stride = ub4;
-    TRY(launch_gemm(g, c.st));
+    GemmDesc g = gd(Lw, Lw, kc, 1, P.np, ks,
+                    opnd(P.c(ins[pass]), JOLT_F32, 1, Lw, 0, s4, (long long)kc * Lw),
+                    opnd(P.c(ins[pass]), JOLT_F32, Lw, 1, 0, s4, (long long)kc * Lw),
+                    P.f(L.p_Gram), Lw, 1, s4, (long long)Lw * Lw, 0.f, skip);
+    g.skip_stride = s4;
+    TRY(launch_gemm(g, st));
     const float sh = pass == 0 ? shift : 0.f;
     if (!f64) {
       // out = in R^{-1} as a plain product (R^{-1} from the Cholesky kernel)
-      TRY(launch_chol_inv(c.f(L.o_Gram), ub4, Lw, ks, (long long)Lw * Lw, c.U, c.f(L.o_Rinv),
-                          ub4, (int*)(c.ws + L.o_status), ub4, skip, ub4, sh, c.st));
-      GemmDesc m = gd(T, Lw, Lw, 1, c.U, 1, opnd(c.ws + ins[pass], JOLT_F32, Lw, 1, 0, ub4),
-                      opnd(c.ws + L.o_Rinv, JOLT_F32, Lw, 1, 0, ub4), c.f(outs[pass]), Lw, 1, ub4,
-                      0, 0.f, skip);
-      m.skip_stride = ub4;
-      TRY(launch_gemm(m, c.st));
+      TRY(launch_chol_inv(P.f(L.p_Gram), s4, Lw, ks, (long long)Lw * Lw, P.np, P.f(L.p_Rinv), s4,
+                          status, s4, skip, s4, sh, st));
+      GemmDesc m = gd(T, Lw, Lw, 1, P.np, 1, opnd(P.c(ins[pass]), JOLT_F32, Lw, 1, 0, s4),
+                      opnd(P.c(L.p_Rinv), JOLT_F32, Lw, 1, 0, s4), P.f(outs[pass]), Lw, 1, s4, 0,
+                      0.f, skip);
+      m.skip_stride = s4;
+      TRY(launch_gemm(m, st));
     } else {
-      TRY(launch_chol(c.f(L.o_Gram), ub4, Lw, ks, (long long)Lw * Lw, c.U, c.f(L.o_Rinv), ub4,
-                      (int*)(c.ws + L.o_status), ub4, skip, ub4, true, sh, c.st));
-      TRY(launch_trsm_rows(c.f(ins[pass]), c.f(outs[pass]), ub4, c.f(L.o_Rinv), ub4, T, Lw,
-                           c.U, skip, ub4, c.st));
+      TRY(launch_chol(P.f(L.p_Gram), s4, Lw, ks, (long long)Lw * Lw, P.np, P.f(L.p_Rinv), s4,
+                      status, s4, skip, s4, true, sh, st));
+      TRY(launch_trsm_rows(P.f(ins[pass]), P.f(outs[pass]), s4, P.f(L.p_Rinv), s4, T, Lw, P.np,
+                           skip, s4, st));
     }
   }
   return JOLT_OK;
 }
 
-jolt_status cholqr2(const F& c, int T, int Lw, size_t src, size_t mid, size_t dst,
-                    const int* skip, bool f64) {
-  return cholqr(c, T, Lw, src, mid, dst, skip, f64, 2, f64 ? 0.f : SUB_SHIFT);
+jolt_status cholqr2(const Layout& L, const PS& P, int T, int Lw, size_t src, size_t mid,
+                    size_t dst, bool use_flags, bool f64, cudaStream_t st) {
+  return cholqr(L, P, T, Lw, src, mid, dst, use_flags, f64, 2, f64 ? 0.f : SUB_SHIFT, st);
 }
 
-jolt_status read_flags_all(const F& c, bool* all) {
-  std::vector<int> h(c.U);
-  JOLT_CUDA_TRY(cudaMemcpy2DAsync(h.data(), sizeof(int), c.ws + c.L.o_flag, c.L.unit_bytes,
-                                  sizeof(int), c.U, cudaMemcpyDeviceToHost, c.st));
-  JOLT_CUDA_TRY(cudaStreamSynchronize(c.st));
+jolt_status read_flags_all(const Layout& L, const PS& P, cudaStream_t st, bool* all) {
+  std::vector<int> h(P.np);
+  JOLT_CUDA_TRY(cudaMemcpy2DAsync(h.data(), sizeof(int), P.c(L.p_flag), P.stride, sizeof(int),
+                                  P.np, cudaMemcpyDeviceToHost, st));
+  JOLT_CUDA_TRY(cudaStreamSynchronize(st));
   bool a = true;
   for (int v : h) a = a && (v != 0);
   *all = a;
@@ -294,6 +345,136 @@ struct JoinGuard {
   }
 };
 
+// Exact token mode for a set of problems whose S_T (p_ST) is final: the
+// leading RT eigenvectors into p_UT, eigenvalues into p_ev (direct Jacobi when
+// T <= 128, else block subspace iteration with Rayleigh-Ritz).  `warm`: p_V
+// already holds an orthonormal start block.
+jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st) {
+  const int T = L.T, RT = L.RT, Lw = L.L;
+  const long long s4 = P.s4();
+  int* status = (int*)P.c(L.p_status);
+  if (T <= 128) {
+    TRY(launch_jacobi(P.f(L.p_ST), s4, T, T, 1, 0, P.np, P.f(L.p_theta), s4, P.f(L.p_UT), s4, RT,
+                      RT, status, s4, nullptr, 0, JAC_ABS_EXACT, st));
+    copy_cols_kernel<<<dim3(blocks_for(RT), P.np), 256, 0, st>>>(P.base, P.stride, L.p_theta, T,
+                                                                 L.p_ev, 1, RT);
+    JOLT_LAUNCH_CHECK();
+    return JOLT_OK;
+  }
+  if (!warm) {
+    init_block_kernel<<<dim3(blocks_for((long long)T * Lw), P.np), 256, 0, st>>>(
+        P.base, P.stride, L.p_V, T * Lw);
+    JOLT_LAUNCH_CHECK();
+    TRY(cholqr2(L, P, T, Lw, L.p_V, L.p_V2, L.p_V, false, false, st));
+  }
+  set_int_kernel<<<P.np, 32, 0, st>>>(P.base, P.stride, L.p_flag, 0);
+  JOLT_LAUNCH_CHECK();
+  const bool svtc = sv_tc_supported(L);
+  if (svtc) TRY(split_tok_gram(L, P.np, P.base, P.stride, st));
+  const int* flags = (const int*)P.c(L.p_flag);
+  auto apply_S = [&]() -> jolt_status {  // Z = S V
+    if (svtc) return sv_tc(L, P.np, P.base, P.stride, st);
+    GemmDesc gg = gd(T, Lw, T, 1, P.np, 1, opnd(P.c(L.p_ST), JOLT_F32, T, 1, 0, s4),
+                     opnd(P.c(L.p_V), JOLT_F32, Lw, 1, 0, s4), P.f(L.p_Z), Lw, 1, s4, 0, 0.f,
+                     flags);
+    gg.skip_stride = s4;
+    return launch_gemm(gg, st);
+  };
+  // blocks of SUB_STEPS power steps V <- orth(S V), then Rayleigh-Ritz and
+  // the residual test; converged problems are skipped from then on
+  for (int blk = 0; blk < SUB_MAX_BLOCKS; ++blk) {
+    // one shifted CholeskyQR pass per power step; the last step of a block
+    // takes two so that Rayleigh-Ritz sees an orthonormal basis
+    for (int q = 0; q < SUB_STEPS; ++q) {
+      TRY(apply_S());
+      TRY(cholqr(L, P, T, Lw, L.p_Z, L.p_V2, L.p_V, true, false, q == SUB_STEPS - 1 ? 2 : 1,
+                 SUB_SHIFT, st));
+    }
+    TRY(apply_S());
+    // H = V^T Z, split over row chunks; the Jacobi kernel sums the partials
+    const int kc = T / L.ks;
+    GemmDesc g = gd(Lw, Lw, kc, 1, P.np, L.ks,
+                    opnd(P.c(L.p_V), JOLT_F32, 1, Lw, 0, s4, (long long)kc * Lw),
+                    opnd(P.c(L.p_Z), JOLT_F32, Lw, 1, 0, s4, (long long)kc * Lw), P.f(L.p_Hm),
+                    Lw, 1, s4, (long long)Lw * Lw, 0.f, flags);
+    g.skip_stride = s4;
+    TRY(launch_gemm(g, st));
+    TRY(launch_jacobi(P.f(L.p_Hm), s4, Lw, Lw, L.ks, (long long)Lw * Lw, P.np, P.f(L.p_theta), s4,
+                      P.f(L.p_Wm), s4, Lw, Lw, status, s4, flags, s4, JAC_ABS_RR, st));
+    // Ritz vectors V2 = V W and Z2 = Z W = S V2
+    g = gd(T, Lw, Lw, 1, P.np, 1, opnd(P.c(L.p_V), JOLT_F32, Lw, 1, 0, s4),
+           opnd(P.c(L.p_Wm), JOLT_F32, Lw, 1, 0, s4), P.f(L.p_V2), Lw, 1, s4, 0, 0.f, flags);
+    g.skip_stride = s4;
+    TRY(launch_gemm(g, st));
+    g = gd(T, Lw, Lw, 1, P.np, 1, opnd(P.c(L.p_Z), JOLT_F32, Lw, 1, 0, s4),
+           opnd(P.c(L.p_Wm), JOLT_F32, Lw, 1, 0, s4), P.f(L.p_Z2), Lw, 1, s4, 0, 0.f, flags);
+    g.skip_stride = s4;
+    TRY(launch_gemm(g, st));
+    const int last = (blk == SUB_MAX_BLOCKS - 1);
+    ritz_check_kernel<<<P.np, 512, 0, st>>>(P.base, P.stride, L.p_V2, L.p_Z2, L.p_theta, L.p_UT,
+                                            L.p_ev, L.p_flag, L.p_status, L.p_V, T, Lw, RT, last);
+    JOLT_LAUNCH_CHECK();
+    if (last) break;
+    // next block starts from orth(Z2), Z2 equilibrated by the check
+    TRY(cholqr2(L, P, T, Lw, L.p_Z2, L.p_V2, L.p_V, true, false, st));
+    bool all = false;
+    TRY(read_flags_all(L, P, st, &all));
+    if (all) break;
+  }
+  return JOLT_OK;
+}
+
+// FlashJoLT randomized range finder for one feature rank over a set of U
+// problems (one per unit): A_h = Y_h[:, :rdv] (or X_h for rdv = D), leading
+// RT approximate eigenvectors of sum_h A_h A_h^T into p_UT, values into p_ev.
+jolt_status token_randomized(const F& c, const PS& P, const void* Ab, int adt, long long as_t,
+                             long long aseg, long long aub, int rdv, const float* sketch) {
+  const Layout& L = c.L;
+  const int T = L.T, H = L.H, D = L.D, RT = L.RT, ell = L.ell;
+  const long long s4 = P.s4(), ub4 = (long long)L.unit_bytes / 4;
+  cudaStream_t st = c.st;
+  int* status = (int*)P.c(L.p_status);
+  const long long sk_h = (long long)D * ell, sk_u = (long long)H * D * ell;
+  // Q lives in V: Z = A Omega, Q = orth(Z); then q times Q = orth(A (A^T Q))
+  TRY(launch_gemm(gd(T, ell, rdv, H, c.U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
+                     opnd(sketch, JOLT_F32, ell, 1, sk_h, sk_u), P.f(L.p_Z), ell, 1, s4, 0),
+                  st));
+  TRY(cholqr2(L, P, T, ell, L.p_Z, L.p_V2, L.p_V, false, true, st));
+  for (int q = 0; q <= L.power_iters; ++q) {
+    // P_h = A_h^T Q  (rdv x ell per head)
+    TRY(launch_gemm(gd(rdv, ell, T, 1, c.U, H, opnd(Ab, adt, 1, as_t, 0, aub, aseg),
+                       opnd(P.c(L.p_V), JOLT_F32, ell, 1, 0, s4, 0), c.f(L.o_P), ell, 1, ub4,
+                       (long long)rdv * ell),
+                    st));
+    if (q == L.power_iters) break;
+    // Z = sum_h A_h P_h, re-orthonormalised
+    TRY(launch_gemm(gd(T, ell, rdv, H, c.U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
+                       opnd(c.ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4),
+                       P.f(L.p_Z), ell, 1, s4, 0),
+                    st));
+    TRY(cholqr2(L, P, T, ell, L.p_Z, L.p_V2, L.p_V, false, true, st));
+  }
+  // Rayleigh-Ritz: B B^T with B = Q^T A, i.e. sum_h P_h^T P_h, split over
+  // head groups; the Jacobi kernel sums the partials
+  const int hs = L.hs, hper = H / L.hs;
+  TRY(launch_gemm(gd(ell, ell, rdv, hper, c.U, hs,
+                     opnd(c.ws + L.o_P, JOLT_F32, 1, ell, (long long)rdv * ell, ub4,
+                          (long long)hper * rdv * ell),
+                     opnd(c.ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4,
+                          (long long)hper * rdv * ell),
+                     P.f(L.p_Hm), ell, 1, s4, (long long)ell * ell),
+                  st));
+  TRY(launch_jacobi(P.f(L.p_Hm), s4, ell, ell, hs, (long long)ell * ell, c.U, P.f(L.p_theta), s4,
+                    P.f(L.p_Wm), s4, ell, RT, status, s4, nullptr, 0, JAC_ABS_EXACT, st));
+  TRY(launch_gemm(gd(T, RT, ell, 1, c.U, 1, opnd(P.c(L.p_V), JOLT_F32, ell, 1, 0, s4),
+                     opnd(P.c(L.p_Wm), JOLT_F32, ell, 1, 0, s4), P.f(L.p_UT), RT, 1, s4, 0),
+                  st));
+  copy_cols_kernel<<<dim3(blocks_for(RT), c.U), 256, 0, st>>>(P.base, P.stride, L.p_theta, ell,
+                                                              L.p_ev, 1, RT);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
 }  // namespace
 
 jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketch, char* ws,
@@ -305,7 +486,6 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   const int xdt = L.dtype;
   const long long xu = (long long)H * T * D;
   int* status = (int*)(ws + L.o_status);
-  int* flags = (int*)(ws + L.o_flag);
 
   set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_status, 0);
   JOLT_LAUNCH_CHECK();
@@ -357,160 +537,91 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   if (overlap) JOLT_CUDA_TRY(cudaEventRecord(ev.b, fs));
   if (RT == 0) return JOLT_OK;
 
-  // ---- token mode, one feature rank at a time
+  // ---- token mode: one problem per (unit, feature rank)
   const bool exact = (L.token_mode == JOLT_TOKEN_EXACT);
-  const int Lw = exact ? L.L : L.ell;
-  bool sub_started = false, yt_ready = false, joined = !overlap;
-  const bool ytc = exact && T > 128 && ygram_tc_supported(L);
-  // largest feature rank first (the whole-feature problem, when present,
-  // overlaps the feature stage); each next rank warm-starts from the last
-  for (int oi = L.nd - 1; oi >= 0; --oi) {
-    const int id = oi;
-    const int rdv = L.rd[id];
-    const bool full = (rdv == D);
-    if (!full && !joined) {
-      JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
-      joined = true;
+  const int ndt = L.ndt;
+  const size_t pb = L.prob_bytes;
+  char* preg = ws + (size_t)U * ub;
+  const PS all_tr{preg, pb, U * ndt};
+  const PS full_ps{preg + (size_t)U * ndt * pb, pb, U};
+  auto tr_id = [&](int id) { return PS{preg + (size_t)id * pb, (size_t)ndt * pb, U}; };
+  set_int_kernel<<<U * L.nprob, 32, 0, st>>>(preg, pb, L.p_status, 0);
+  JOLT_LAUNCH_CHECK();
+  bool joined = !overlap;
+  auto join = [&]() -> jolt_status {
+    if (!joined) JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
+    joined = true;
+    return JOLT_OK;
+  };
+  if (exact) {
+    // the whole-feature problem first: its Gram needs only X, so it runs
+    // beside the feature stage
+    if (L.hasFullD) {
+      if (tc) {
+        TRY(gram_tok_tc(L, U, X, full_ps.base, pb, st));
+      } else {
+        TRY(launch_gemm(gd(T, T, D, H, U, 1, opnd(X, xdt, D, 1, (long long)T * D, xu),
+                           opnd(X, xdt, 1, D, (long long)T * D, xu), full_ps.f(L.p_ST), T, 1,
+                           full_ps.s4(), 0),
+                        st));
+      }
+      TRY(token_exact(L, full_ps, false, st));
     }
-    const void* Ab;
-    int adt;
-    long long as_t, aseg, aub;
-    if (full) { Ab = X; adt = xdt; as_t = D; aseg = (long long)T * D; aub = xu; }
-    else { Ab = ws + L.o_Y; adt = JOLT_F32; as_t = RD; aseg = (long long)T * RD; aub = ub4; }
-    const size_t oUT = L.o_UT32 + (size_t)id * T * RT * 4;
-    const size_t oEV = L.o_tokev + (size_t)id * RT * 4;
-
-    if (exact) {
-      if (full) {
-        if (tc) {
-          TRY(gram_tok_tc(L, U, X, ws, st));
-        } else {
-          TRY(launch_gemm(gd(T, T, D, H, U, 1, opnd(X, xdt, D, 1, (long long)T * D, xu),
-                             opnd(X, xdt, 1, D, (long long)T * D, xu), c.f(L.o_ST), T, 1, ub4, 0),
+    TRY(join());
+    if (ndt > 0) {
+      // every truncated rank's Gram, then one batched solve for all of them
+      if (T > 128 && ygram_tc_supported(L)) {
+        TRY(ytrans(L, U, ws, st));
+        TRY(ygram_tc(L, U, ws, preg, pb, st));
+      } else {
+        for (int id = 0; id < ndt; ++id) {
+          const PS P = tr_id(id);
+          const float* Y0 = (const float*)(ws + L.o_Y);
+          const long long aseg = (long long)T * RD;
+          TRY(launch_gemm(gd(T, T, L.rd[id], H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),
+                             opnd(Y0, JOLT_F32, 1, RD, aseg, ub4), P.f(L.p_ST), T, 1, P.s4(), 0),
                           st));
         }
-      } else if (ytc) {
-        if (!yt_ready) TRY(ytrans(L, U, ws, st));
-        yt_ready = true;
-        TRY(ygram_tc(L, U, ws, 0, rdv, 0.f, st));
-      } else {
-        const float* Y0 = (const float*)(ws + L.o_Y);
-        TRY(launch_gemm(gd(T, T, rdv, H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),
-                           opnd(Y0, JOLT_F32, 1, RD, aseg, ub4), c.f(L.o_ST), T, 1, ub4, 0),
-                        st));
       }
-      if (T <= 128) {
-        // direct solve of the whole token Gram
-        TRY(launch_jacobi(c.f(L.o_ST), ub4, T, T, 1, 0, U, c.f(L.o_theta), ub4, c.f(oUT), ub4, RT,
-                          RT, status, ub4, nullptr, 0, JAC_ABS_EXACT, st));
-        copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, T, oEV, 1,
-                                                                  RT);
+      const bool warm = L.hasFullD && T > 128;
+      if (warm) {
+        warm_copy_kernel<<<dim3(64, U * ndt), 256, 0, st>>>(preg, pb, L.p_V, ndt, full_ps.base,
+                                                            (long long)T * L.L);
         JOLT_LAUNCH_CHECK();
-      } else {
-        if (!sub_started) {
-          init_block_kernel<<<dim3(blocks_for((long long)T * Lw), U), 256, 0, st>>>(ws, ub, L.o_V,
-                                                                                   T * Lw);
-          JOLT_LAUNCH_CHECK();
-          TRY(cholqr2(c, T, Lw, L.o_V, L.o_V2, L.o_V, nullptr, false));
-          sub_started = true;
-        }
-        set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_flag, 0);
-        JOLT_LAUNCH_CHECK();
-        const bool svtc = sv_tc_supported(L);
-        if (svtc) TRY(split_tok_gram(L, U, ws, st));
-        // blocks of SUB_STEPS power steps V <- orth(S V), then Rayleigh-Ritz
-        // and the residual test; converged units are skipped from then on
-        for (int blk = 0; blk < SUB_MAX_BLOCKS; ++blk) {
-          GemmDesc g;
-          auto apply_S = [&]() -> jolt_status {  // Z = S V
-            if (svtc) return sv_tc(L, U, ws, flags, st);
-            GemmDesc gg = gd(T, Lw, T, 1, U, 1, opnd(ws + L.o_ST, JOLT_F32, T, 1, 0, ub4),
-                             opnd(ws + L.o_V, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Z), Lw, 1, ub4, 0,
-                             0.f, flags);
-            gg.skip_stride = ub4;
-            return launch_gemm(gg, st);
-          };
-          // one shifted CholeskyQR pass per power step; the last step of a
-          // block takes two so that Rayleigh-Ritz sees an orthonormal basis
-          for (int p = 0; p < SUB_STEPS; ++p) {
-            TRY(apply_S());
-            TRY(cholqr(c, T, Lw, L.o_Z, L.o_V2, L.o_V, flags, false, p == SUB_STEPS - 1 ? 2 : 1,
-                       SUB_SHIFT));
-          }
-          TRY(apply_S());
-          // H = V^T Z, split over row chunks; the Jacobi kernel sums the partials
-          const int kc = T / L.ks;
-          g = gd(Lw, Lw, kc, 1, U, L.ks, opnd(ws + L.o_V, JOLT_F32, 1, Lw, 0, ub4, (long long)kc * Lw),
-                 opnd(ws + L.o_Z, JOLT_F32, Lw, 1, 0, ub4, (long long)kc * Lw), c.f(L.o_Hm), Lw, 1,
-                 ub4, (long long)Lw * Lw, 0.f, flags);
-          g.skip_stride = ub4;
-          TRY(launch_gemm(g, st));
-          TRY(launch_jacobi(c.f(L.o_Hm), ub4, Lw, Lw, L.ks, (long long)Lw * Lw, U, c.f(L.o_theta),
-                            ub4, c.f(L.o_Wm), ub4, Lw, Lw, status, ub4, flags, ub4, JAC_ABS_RR, st));
-          // Ritz vectors V2 = V W and Z2 = Z W = S V2
-          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + L.o_V, JOLT_F32, Lw, 1, 0, ub4),
-                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_V2), Lw, 1, ub4, 0, 0.f, flags);
-          g.skip_stride = ub4;
-          TRY(launch_gemm(g, st));
-          g = gd(T, Lw, Lw, 1, U, 1, opnd(ws + L.o_Z, JOLT_F32, Lw, 1, 0, ub4),
-                 opnd(ws + L.o_Wm, JOLT_F32, Lw, 1, 0, ub4), c.f(L.o_Z2), Lw, 1, ub4, 0, 0.f, flags);
-          g.skip_stride = ub4;
-          TRY(launch_gemm(g, st));
-          const int last = (blk == SUB_MAX_BLOCKS - 1);
-          ritz_check_kernel<<<U, 512, 0, st>>>(ws, ub, L.o_V2, L.o_Z2, L.o_theta, oUT, oEV,
-                                               L.o_flag, L.o_status, L.o_V, T, Lw, RT, last);
-          JOLT_LAUNCH_CHECK();
-          if (last) break;
-          // next block starts from orth(Z2), Z2 equilibrated by the check
-          TRY(cholqr2(c, T, Lw, L.o_Z2, L.o_V2, L.o_V, flags, false));
-          bool all = false;
-          TRY(read_flags_all(c, &all));
-          if (all) break;
-        }
       }
-    } else {
-      // FlashJoLT randomized range finder with q power steps
-      const int ell = L.ell;
-      const long long sk_h = (long long)D * ell, sk_u = (long long)H * D * ell;
-      // Q lives in V: Z = A Omega, Q = orth(Z); then q times Q = orth(A (A^T Q))
-      TRY(launch_gemm(gd(T, ell, rdv, H, U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
-                         opnd(sketch, JOLT_F32, ell, 1, sk_h, sk_u), c.f(L.o_Z), ell, 1, ub4, 0),
-                      st));
-      TRY(cholqr2(c, T, ell, L.o_Z, L.o_V2, L.o_V, nullptr, true));
-      for (int q = 0; q <= L.power_iters; ++q) {
-        // P_h = A_h^T Q  (rdv x ell per head)
-        TRY(launch_gemm(gd(rdv, ell, T, 1, U, H, opnd(Ab, adt, 1, as_t, 0, aub, aseg),
-                           opnd(ws + L.o_V, JOLT_F32, ell, 1, 0, ub4, 0), c.f(L.o_P), ell, 1, ub4,
-                           (long long)rdv * ell),
-                        st));
-        if (q == L.power_iters) break;
-        // Z = sum_h A_h P_h, re-orthonormalised
-        TRY(launch_gemm(gd(T, ell, rdv, H, U, 1, opnd(Ab, adt, as_t, 1, aseg, aub),
-                           opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4),
-                           c.f(L.o_Z), ell, 1, ub4, 0),
-                        st));
-        TRY(cholqr2(c, T, ell, L.o_Z, L.o_V2, L.o_V, nullptr, true));
-      }
-      // Rayleigh-Ritz: B B^T with B = Q^T A, i.e. sum_h P_h^T P_h, split over
-      // head groups; the Jacobi kernel sums the partials
-      const int hs = L.hs, hper = H / L.hs;
-      TRY(launch_gemm(gd(ell, ell, rdv, hper, U, hs,
-                         opnd(ws + L.o_P, JOLT_F32, 1, ell, (long long)rdv * ell, ub4,
-                              (long long)hper * rdv * ell),
-                         opnd(ws + L.o_P, JOLT_F32, ell, 1, (long long)rdv * ell, ub4,
-                              (long long)hper * rdv * ell),
-                         c.f(L.o_Hm), ell, 1, ub4, (long long)ell * ell),
-                      st));
-      TRY(launch_jacobi(c.f(L.o_Hm), ub4, ell, ell, hs, (long long)ell * ell, U, c.f(L.o_theta),
-                        ub4, c.f(L.o_Wm), ub4, ell, RT, status, ub4, nullptr, 0, JAC_ABS_EXACT,
-                        st));
-      TRY(launch_gemm(gd(T, RT, ell, 1, U, 1, opnd(ws + L.o_V, JOLT_F32, ell, 1, 0, ub4),
-                         opnd(ws + L.o_Wm, JOLT_F32, ell, 1, 0, ub4), c.f(oUT), RT, 1, ub4, 0),
-                      st));
-      copy_cols_kernel<<<dim3(blocks_for(RT), U), 256, 0, st>>>(ws, ub, L.o_theta, ell, oEV, 1, RT);
-      JOLT_LAUNCH_CHECK();
+      TRY(token_exact(L, all_tr, warm, st));
     }
-    // cores G(r_d)[h] = U_T^T A_h  (RT x rdv)
+  } else {
+    // randomized: the whole-feature rank first (beside the feature stage),
+    // then the truncated ranks one at a time (their sketches differ in size)
+    for (int oi = L.nd - 1; oi >= 0; --oi) {
+      const int id = oi;
+      const int rdv = L.rd[id];
+      const bool full = (rdv == D);
+      if (!full) TRY(join());
+      if (full) {
+        TRY(token_randomized(c, full_ps, X, xdt, D, (long long)T * D, xu, rdv, sketch));
+      } else {
+        TRY(token_randomized(c, tr_id(id), ws + L.o_Y, JOLT_F32, RD, (long long)T * RD, ub4, rdv,
+                             sketch));
+      }
+    }
+  }
+  TRY(join());
+  scatter_problems_kernel<<<dim3(64, L.nd, U), 256, 0, st>>>(
+      ws, ub, L.o_UT32, L.o_tokev, L.o_status, preg, pb, L.p_UT, L.p_ev, 1, L.p_status, U, ndt, T,
+      RT);
+  JOLT_LAUNCH_CHECK();
+  // cores G(r_d)[h] = U_T^T A_h  (RT x rdv)
+  for (int id = 0; id < L.nd; ++id) {
+    const int rdv = L.rd[id];
+    const bool full = (rdv == D);
+    const void* Ab = full ? X : (const void*)(ws + L.o_Y);
+    const int adt = full ? xdt : JOLT_F32;
+    const long long as_t = full ? D : RD;
+    const long long aseg = full ? (long long)T * D : (long long)T * RD;
+    const long long aub = full ? xu : ub4;
+    const size_t oUT = L.o_UT32 + (size_t)id * T * RT * 4;
     const size_t oG = L.o_G32 + (size_t)id * H * RT * D * 4;
     TRY(launch_gemm(gd(RT, rdv, T, 1, U, H, opnd(ws + oUT, JOLT_F32, 1, RT, 0, ub4),
                        opnd(Ab, adt, as_t, 1, 0, aub, aseg), c.f(oG), rdv, 1, ub4,
@@ -520,7 +631,6 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
         ws, ub, oG, rdv, L.o_G16 + (size_t)id * H * RT * D * 2, rdv, H * RT, rdv, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
   }
-  if (!joined) JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
   round_f16_kernel<<<dim3(blocks_for((long long)L.nd * T * RT), 1, U), 256, 0, st>>>(
       ws, ub, L.o_UT32, RT, L.o_UT16, RT, L.nd * T, RT, 0, 0, 1);
   JOLT_LAUNCH_CHECK();

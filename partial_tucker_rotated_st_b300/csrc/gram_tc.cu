@@ -21,6 +21,8 @@
 #include "jolt_internal.cuh"
 #include "tc_common.cuh"
 
+#include <string.h>
+
 #include <cudaTypedefs.h>
 
 namespace jolt {
@@ -385,18 +387,19 @@ __global__ void split_v_kernel(const char* ws, size_t ub, size_t o_V, size_t o_V
   }
 }
 
-// Token Gram increments S[u] (+)= A A^T with A = Yt[u][:, k0:k1] (T x (k1-k0)),
-// on kind::tf32 with the three-product split (A_hi A_hi^T + A_hi A_lo^T +
-// A_lo A_hi^T).  Yt[u] is [T][RD*H] fp32 with column j*H + h = Y[u][h][:, j],
-// so that the feature ranks j0 <= j < j1 of an increment are one contiguous
-// column range.  Upper-triangular 128 x 128 tiles, mirrored; S = beta S + ...
+// Token Grams of the truncated feature ranks: for problem p = u * ndt + id,
+// S[p] = A A^T with A = Yt[u][:, :H rd[id]] (T x H rd[id]), on kind::tf32
+// with the three-product split (A_hi A_hi^T + A_hi A_lo^T + A_lo A_hi^T).
+// Yt[u] is [T][RD*H] fp32 with column j*H + h = Y[u][h][:, j], so that the
+// feature ranks j < rd of one Gram are a leading column range.  Upper-
+// triangular 128 x 128 tiles, mirrored into the lower triangle.
 constexpr int YG_STAGES = 2;
 constexpr int YG_A = TILE * 32 * 4;          // 16 KB: 128 rows x 32 k
 constexpr int YG_STAGE = 4 * YG_A;           // A hi, A lo, B hi, B lo
 
 struct YgArgs {
-  int T, k0, k1, nt;
-  float beta;
+  int T, ndt, nt;
+  int k1s[JOLT_MAX_GRID];   // column count H * rd[id] of each truncated rank
   float* S;
   long long s_us;
   char* ws;
@@ -411,12 +414,12 @@ ygram_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constant__ 
   struct Bars { uint64_t full[YG_STAGES], empty[YG_STAGES], accum; uint32_t tmem; };
   Bars* S = (Bars*)(base + YG_STAGES * YG_STAGE);
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int u = blockIdx.y;
+  const int p = blockIdx.y, u = p / a.ndt;
   int mi = 0, idx = blockIdx.x;
   while (idx >= a.nt - mi) { idx -= a.nt - mi; ++mi; }
   const int ni = mi + idx;
   const bool diag = (mi == ni);
-  const int klen = a.k1 - a.k0;
+  const int klen = a.k1s[p % a.ndt];
   const int nk = (klen + 31) / 32;
   if (threadIdx.x == 0) {
     for (int s = 0; s < YG_STAGES; ++s) {
@@ -440,7 +443,7 @@ ygram_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constant__ 
       const uint32_t fb = tc::smem_u32(&S->full[s]);
       tc::mbar_expect_tx(fb, bytes);
       const uint32_t sa = tc::smem_u32(base + s * YG_STAGE);
-      const int kc = a.k0 + kk * 32;
+      const int kc = kk * 32;
       tc::tma_load_3d(sa, &tH, kc, mi * TILE, u, fb);
       tc::tma_load_3d(sa + YG_A, &tL, kc, mi * TILE, u, fb);
       if (!diag) {
@@ -478,31 +481,29 @@ ygram_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constant__ 
       ok = false;
     } else {
       tc::tc_fence_after();
-      float* C = a.S + (long long)u * a.s_us;
+      float* C = a.S + (long long)p * a.s_us;
       const int T = a.T;
-      const float beta = a.beta;
       drain(tmem, q, [&](int rt, int c0, const float (&v)[32]) {
         const int row = mi * TILE + rt;
         if (row < T) {
           float* cr = C + (long long)row * T + ni * TILE + c0;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (ni * TILE + c0 + j < T) cr[j] = beta != 0.f ? cr[j] + v[j] : v[j];
+            if (ni * TILE + c0 + j < T) cr[j] = v[j];
         }
         if (!diag) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int col = ni * TILE + c0 + j;
             if (col < T && row < T) {
-              float* c = C + (long long)col * T + row;
-              *c = beta != 0.f ? *c + v[j] : v[j];
+              C[(long long)col * T + row] = v[j];
             }
           }
         }
       });
     }
   }
-  if (!ok) atomicOr((int*)(a.ws + (size_t)u * a.ub + a.o_status), ST_TIMEOUT);
+  if (!ok) atomicOr((int*)(a.ws + (size_t)p * a.ub + a.o_status), ST_TIMEOUT);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) tc::tmem_dealloc(tmem, TILE);
@@ -557,8 +558,9 @@ bool gram_tc_supported(const Layout& L) {
   return L.dtype == JOLT_BF16 && L.D == 128 && encode_fn() != nullptr;
 }
 
-// S_T[u] = sum_h X_h X_h^T for every unit, T x T fp32 at ws + u*ub + o_ST.
-jolt_status gram_tok_tc(const Layout& L, int U, const void* X, char* ws, cudaStream_t st) {
+// S_T of problem u = sum_h X_h X_h^T of unit u, T x T fp32.
+jolt_status gram_tok_tc(const Layout& L, int U, const void* X, char* pbase, size_t pstride,
+                        cudaStream_t st) {
   CUtensorMap tm;
   const cuuint64_t dims[3] = {(cuuint64_t)L.D, (cuuint64_t)L.T, (cuuint64_t)U * L.H};
   const cuuint64_t strides[2] = {(cuuint64_t)L.D * 2, (cuuint64_t)L.T * L.D * 2};
@@ -568,9 +570,9 @@ jolt_status gram_tok_tc(const Layout& L, int U, const void* X, char* ws, cudaStr
   a.T = L.T; a.D = L.D; a.H = L.H;
   a.nt = (L.T + TILE - 1) / TILE;
   a.rows_per = 0; a.nsplit = 0;
-  a.out = (float*)(ws + L.o_ST);
-  a.out_us = (long long)L.unit_bytes / 4;
-  a.ws = ws; a.ub = L.unit_bytes; a.o_status = L.o_status;
+  a.out = (float*)(pbase + L.p_ST);
+  a.out_us = (long long)pstride / 4;
+  a.ws = pbase; a.ub = pstride; a.o_status = L.p_status;
   const size_t smem = tc_smem(2 * TILE_BYTES);
   static bool attr = false;
   if (!attr) {
@@ -614,45 +616,46 @@ jolt_status gram_feat_tc(const Layout& L, int U, const void* X, char* ws, cudaSt
 }
 
 bool sv_tc_supported(const Layout& L) {
-  return L.L == 64 && L.T % 4 == 0 && encode_fn() != nullptr && L.o_STs != 0;
+  return L.L == 64 && L.T % 4 == 0 && encode_fn() != nullptr && L.p_STs != 0;
 }
 
-// S_lo = S - trunc_tf32(S) for every unit (after S_T is final for an r_d).
-jolt_status split_tok_gram(const Layout& L, int U, char* ws, cudaStream_t st) {
-  dim3 grid(256, U);
-  tf32_lo_kernel<<<grid, 256, 0, st>>>(ws, L.unit_bytes, L.o_ST, L.o_STs, (long long)L.T * L.T,
+// S_lo = S - trunc_tf32(S) for every problem (after its S_T is final).
+jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st) {
+  dim3 grid(256, np);
+  tf32_lo_kernel<<<grid, 256, 0, st>>>(pbase, pstride, L.p_ST, L.p_STs, (long long)L.T * L.T,
                                        nullptr, 0);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
 
-// Z = S V for every unit not flagged (T x 64 blocks at o_V / o_Z).
-jolt_status sv_tc(const Layout& L, int U, char* ws, const int* flags, cudaStream_t st) {
-  const size_t ub = L.unit_bytes;
-  dim3 g2((L.T + 31) / 32, 2, U);
-  split_v_kernel<<<g2, dim3(32, 8), 0, st>>>(ws, ub, L.o_V, L.o_Vs, L.o_Vs + (size_t)L.T * 64 * 4,
-                                             L.T, flags, (long long)ub / 4);
+// Z = S V for every problem not flagged (T x 64 blocks at p_V / p_Z).
+jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st) {
+  const int* flags = (const int*)(pbase + L.p_flag);
+  const long long f_us = (long long)pstride / 4;
+  dim3 g2((L.T + 31) / 32, 2, np);
+  split_v_kernel<<<g2, dim3(32, 8), 0, st>>>(pbase, pstride, L.p_V, L.p_Vs,
+                                             L.p_Vs + (size_t)L.T * 64 * 4, L.T, flags, f_us);
   JOLT_LAUNCH_CHECK();
   CUtensorMap tS, tSl, tV, tVl;
-  const cuuint64_t dS[3] = {(cuuint64_t)L.T, (cuuint64_t)L.T, (cuuint64_t)U};
-  const cuuint64_t sS[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)ub};
+  const cuuint64_t dS[3] = {(cuuint64_t)L.T, (cuuint64_t)L.T, (cuuint64_t)np};
+  const cuuint64_t sS[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)pstride};
   const cuuint32_t bS[3] = {32, TILE, 1};
-  const cuuint64_t dV[3] = {(cuuint64_t)L.T, 64, (cuuint64_t)U};
-  const cuuint64_t sV[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)ub};
+  const cuuint64_t dV[3] = {(cuuint64_t)L.T, 64, (cuuint64_t)np};
+  const cuuint64_t sV[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)pstride};
   const cuuint32_t bV[3] = {32, 64, 1};
   const CUtensorMapDataType f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  if (!make_map(&tS, ws + L.o_ST, 3, dS, sS, bS, f32) ||
-      !make_map(&tSl, ws + L.o_STs, 3, dS, sS, bS, f32) ||
-      !make_map(&tV, ws + L.o_Vs, 3, dV, sV, bV, f32) ||
-      !make_map(&tVl, ws + L.o_Vs + (size_t)L.T * 64 * 4, 3, dV, sV, bV, f32))
+  if (!make_map(&tS, pbase + L.p_ST, 3, dS, sS, bS, f32) ||
+      !make_map(&tSl, pbase + L.p_STs, 3, dS, sS, bS, f32) ||
+      !make_map(&tV, pbase + L.p_Vs, 3, dV, sV, bV, f32) ||
+      !make_map(&tVl, pbase + L.p_Vs + (size_t)L.T * 64 * 4, 3, dV, sV, bV, f32))
     return JOLT_ERR_CUDA;
   SvArgs a;
   a.T = L.T; a.L = 64;
-  a.Z = (float*)(ws + L.o_Z);
-  a.z_us = (long long)ub / 4;
+  a.Z = (float*)(pbase + L.p_Z);
+  a.z_us = f_us;
   a.flags = flags;
-  a.f_us = (long long)ub / 4;
-  a.ws = ws; a.ub = ub; a.o_status = L.o_status;
+  a.f_us = f_us;
+  a.ws = pbase; a.ub = pstride; a.o_status = L.p_status;
   const size_t smem = (size_t)SV_STAGES * SV_STAGE + 1024 + 256;
   static bool attr = false;
   if (!attr) {
@@ -660,7 +663,7 @@ jolt_status sv_tc(const Layout& L, int U, char* ws, const int* flags, cudaStream
                                        (int)smem));
     attr = true;
   }
-  dim3 grid((L.T + TILE - 1) / TILE, U);
+  dim3 grid((L.T + TILE - 1) / TILE, np);
   sv_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tS, tSl, tV, tVl, a);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
@@ -681,11 +684,13 @@ jolt_status ytrans(const Layout& L, int U, char* ws, cudaStream_t st) {
   return JOLT_OK;
 }
 
-// S_T += (beta = 1) or = (beta = 0) the Gram of feature ranks [j0, j1).
-jolt_status ygram_tc(const Layout& L, int U, char* ws, int j0, int j1, float beta,
+// S_T of every truncated problem p = u * ndt + id: the Gram of feature ranks
+// [0, rd[id]) of unit u's Y, one launch for all.
+jolt_status ygram_tc(const Layout& L, int U, const char* ws, char* pbase, size_t pstride,
                      cudaStream_t st) {
   const size_t ub = L.unit_bytes;
   const int K = L.RD * L.H;
+  if (L.ndt < 1 || L.ndt > JOLT_MAX_GRID) return JOLT_ERR_INVALID;
   CUtensorMap tH, tL;
   const cuuint64_t d[3] = {(cuuint64_t)K, (cuuint64_t)L.T, (cuuint64_t)U};
   const cuuint64_t sd[2] = {(cuuint64_t)K * 4, (cuuint64_t)ub};
@@ -695,12 +700,14 @@ jolt_status ygram_tc(const Layout& L, int U, char* ws, int j0, int j1, float bet
       !make_map(&tL, ws + L.o_Yt + (size_t)L.T * K * 4, 3, d, sd, box, f32))
     return JOLT_ERR_CUDA;
   YgArgs a;
-  a.T = L.T; a.k0 = j0 * L.H; a.k1 = j1 * L.H;
+  memset(&a, 0, sizeof(a));
+  a.T = L.T;
+  a.ndt = L.ndt;
+  for (int i = 0; i < L.ndt; ++i) a.k1s[i] = L.rd[i] * L.H;
   a.nt = (L.T + TILE - 1) / TILE;
-  a.beta = beta;
-  a.S = (float*)(ws + L.o_ST);
-  a.s_us = (long long)ub / 4;
-  a.ws = ws; a.ub = ub; a.o_status = L.o_status;
+  a.S = (float*)(pbase + L.p_ST);
+  a.s_us = (long long)pstride / 4;
+  a.ws = pbase; a.ub = pstride; a.o_status = L.p_status;
   const size_t smem = (size_t)YG_STAGES * YG_STAGE + 1024 + 256;
   static bool attr = false;
   if (!attr) {
@@ -708,7 +715,7 @@ jolt_status ygram_tc(const Layout& L, int U, char* ws, int j0, int j1, float bet
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     attr = true;
   }
-  dim3 grid(a.nt * (a.nt + 1) / 2, U);
+  dim3 grid(a.nt * (a.nt + 1) / 2, U * L.ndt);
   ygram_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tH, tL, a);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;

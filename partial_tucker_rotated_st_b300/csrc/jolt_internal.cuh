@@ -65,13 +65,21 @@ struct Layout {
   int ntiles;            // sweep CTAs per unit
   int ncand;
   int cost_model, align, block;
-  // section offsets, bytes from the unit's base
-  size_t o_status, o_Sd, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16, o_ST;
-  size_t o_V, o_Z, o_V2, o_Z2, o_Hm, o_Wm, o_theta, o_Gram, o_Rinv, o_flag;
+  // section offsets, bytes from the unit's base (unit u at ws + u * unit_bytes)
+  size_t o_status, o_Sd, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16;
   size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
-  size_t o_STs, o_Vs;    // tf32 low parts of S_T and V (tensor-core S V)
   size_t o_Yt;           // Y relaid [T][RD*H] and its tf32 low part (token Gram)
   size_t unit_bytes;
+  // Token-mode problems, one per (unit, feature rank), in a region after the
+  // n unit regions of a call: truncated rank id of unit u is problem
+  // u * ndt + id, the whole-feature rank of unit u is problem n * ndt + u;
+  // problem p at ws + n * unit_bytes + p * prob_bytes.  Offsets from the
+  // problem's base:
+  int nprob;             // problems per unit (nd, or 0 without a token rank)
+  size_t prob_bytes;
+  size_t p_status, p_flag, p_ST, p_STs, p_Vs, p_V, p_Z, p_V2, p_Z2, p_Hm, p_Wm, p_Gram,
+      p_Rinv, p_theta, p_UT, p_ev;
+  size_t unit_total;     // workspace bytes per unit: unit_bytes + nprob * prob_bytes
 };
 
 jolt_status make_layout(const jolt_config* cfg, Layout* L);
@@ -128,14 +136,21 @@ jolt_status launch_trsm_rows(const float* In, float* Out, long long blk_bstride,
 
 // ------------------------------------------------------------------ tensor cores
 bool gram_tc_supported(const Layout& L);
-jolt_status gram_tok_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
+// S_T of problem p = sum_h X_h X_h^T of unit p (T x T fp32 at pbase + p * pstride + p_ST).
+jolt_status gram_tok_tc(const Layout& L, int n_units, const void* X, char* pbase, size_t pstride,
+                        cudaStream_t st);
 jolt_status gram_feat_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
 bool sv_tc_supported(const Layout& L);
-jolt_status split_tok_gram(const Layout& L, int n_units, char* ws, cudaStream_t st);
-jolt_status sv_tc(const Layout& L, int n_units, char* ws, const int* flags, cudaStream_t st);
+// p_STs = tf32 low part of p_ST for np problems.
+jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st);
+// p_Z = p_ST p_V for every problem whose p_flag is zero.
+jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st);
 bool ygram_tc_supported(const Layout& L);
+// Yt (unit region) = Y relaid [T][RD * H] and its tf32 low part.
 jolt_status ytrans(const Layout& L, int n_units, char* ws, cudaStream_t st);
-jolt_status ygram_tc(const Layout& L, int n_units, char* ws, int j0, int j1, float beta,
+// p_ST of truncated problem p = u * ndt + id: the Gram of feature ranks
+// [0, rd[id]) of unit u's Y.
+jolt_status ygram_tc(const Layout& L, int n_units, const char* ws, char* pbase, size_t pstride,
                      cudaStream_t st);
 
 // ------------------------------------------------------------------ steps

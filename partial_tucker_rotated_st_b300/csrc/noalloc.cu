@@ -50,7 +50,7 @@ extern "C" jolt_status jolt_sweep_candidates_noalloc(const jolt_config* cfg, int
   jolt_status s = make_layout(cfg, &L);
   if (s != JOLT_OK) return s;
   if (n_units < 1 || n_units > 65535 || !X || !signs || !dist || !cost) return JOLT_ERR_INVALID;
-  if (!ws || ((uintptr_t)ws % 256) || ws_bytes < (size_t)n_units * L.unit_bytes)
+  if (!ws || ((uintptr_t)ws % 256) || ws_bytes < (size_t)n_units * L.unit_total)
     return JOLT_ERR_WORKSPACE;
   const size_t need = (size_t)n_units * L.ntiles * (L.ncand + 1) * sizeof(float);
   if (need > NOALLOC_SCRATCH_BYTES) return JOLT_ERR_TOO_LARGE;
