@@ -119,6 +119,7 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   };
   L.o_status = sect(256);
   L.o_Sd = sect((size_t)D * D * 4);
+  L.o_Sd64 = sect((size_t)D * D * 8);
   L.o_Sdp = sect((size_t)L.nsplit * D * D * 4);
   L.o_evd = sect((size_t)D * 4);
   L.o_Vd = sect((size_t)D * D * 4);

@@ -17,6 +17,7 @@ namespace {
 constexpr int JAC_THREADS = 1024;   // viewed as 32 x 32 (ty, tx)
 constexpr int JAC_MAX_SWEEPS = 40;
 constexpr float JAC_TOL = 1e-6f;    // relative: |a_pq| vs sqrt(|a_pp a_qq|)
+constexpr float FEAT_TOL = 4e-6f;   // one-sided: |b_p . b_q| vs |b_p| |b_q| (fp32 dot products)
 // absolute floors vs ||A||_F: JAC_ABS_EXACT for solves whose small
 // eigenvalues matter; JAC_ABS_RR for Rayleigh-Ritz blocks, whose trailing
 // Ritz vectors only seed the next block
@@ -571,6 +572,205 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
   if (t == 0 && bad && status) atomicOr(status + u * s_bs, ST_NOTPD);
 }
 
+// RPT consecutive floats of shared memory (16-byte aligned when RPT % 4 == 0,
+// 8-byte aligned when RPT == 2) to registers and back.
+template <int RPT>
+__device__ __forceinline__ void ld_rows(const float* p, float (&v)[RPT]) {
+  if constexpr (RPT % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < RPT; i += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p + i);
+      v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+    }
+  } else if constexpr (RPT == 2) {
+    const float2 x = *reinterpret_cast<const float2*>(p);
+    v[0] = x.x; v[1] = x.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) v[i] = p[i];
+  }
+}
+template <int RPT>
+__device__ __forceinline__ void st_rows(float* p, const float (&v)[RPT]) {
+  if constexpr (RPT % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < RPT; i += 4)
+      *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+  } else if constexpr (RPT == 2) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) p[i] = v[i];
+  }
+}
+
+// Eigenpairs of the feature Gram by one-sided Jacobi (Hestenes 1958; its
+// relative accuracy: Demmel & Veselic 1992).  S = B B^T with B = diag(s) L',
+// L' the Cholesky factor (f64) of the equilibrated S' = diag(s)^-1 S
+// diag(s)^-1.  Plane rotations applied to the columns of B (fp32) drive them
+// to mutual orthogonality, B J = U Sigma; then S = U Sigma^2 U^T: the
+// eigenvectors are the normalised columns and the eigenvalues their squared
+// norms, so no rotation product has to be accumulated.  Columns live in
+// shared memory; each round of the round-robin (circle) ordering gives the
+// N/2 disjoint pairs to N/2 groups of 16 threads, each thread holding N/16
+// rows of its two columns in registers.  A pair is rotated while
+// |b_p . b_q| > tol sqrt(|b_p|^2 |b_q|^2) and above an absolute floor; a
+// sweep without rotations ends the solve.  A pivot that is not positive
+// (rank-deficient S) or a zero column leaves the unit's `done` flag clear,
+// and the caller solves that unit with the two-sided Jacobi instead.
+template <int N>
+__global__ void __launch_bounds__(8 * N, 1)
+feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restrict__ evals,
+                long long e_bs, float* __restrict__ evecs, long long v_bs, int ldv, int* status,
+                long long st_bs, int* done, long long d_bs, float tol, float abs_tol) {
+  constexpr int NT = 8 * N;
+  constexpr int RPT = N / 16;   // rows per thread
+  constexpr int LDA = N + 1;
+  constexpr int LDM = N + 4;    // column stride, 16-byte aligned
+  extern __shared__ __align__(16) unsigned char fe_sm[];
+  double* A = (double*)fe_sm;            // N x LDA: S', then L' (lower)
+  double* dsc = A + N * LDA;             // [N] sqrt(S_ii)
+  float* M = (float*)(dsc + N);          // N columns of LDM floats
+  float* lam = M + N * LDM;              // [N] squared column norms
+  __shared__ int fail;
+  __shared__ double fro_part[NT / 32];
+  const int u = blockIdx.x, t = threadIdx.x;
+  if (done) done[u * d_bs] = 0;
+  const double* Sg = S64 + u * s_bs;
+  if (t == 0) fail = 0;
+  double fro = 0.0;
+  for (int e = t; e < N * N; e += NT) {
+    const int i = e / N, j = e % N;
+    const double v = 0.5 * (Sg[i * N + j] + Sg[j * N + i]);
+    A[i * LDA + j] = v;
+    fro += v * v;
+  }
+  for (int o = 16; o > 0; o >>= 1) fro += __shfl_xor_sync(0xffffffffu, fro, o);
+  if ((t & 31) == 0) fro_part[t >> 5] = fro;
+  __syncthreads();
+  for (int i = t; i < N; i += NT) {
+    const double d = A[i * LDA + i];
+    dsc[i] = d > 0.0 ? sqrt(d) : 0.0;
+  }
+  double fro_s = 0.0;
+  for (int i = 0; i < NT / 32; ++i) fro_s += fro_part[i];
+  const float floor_abs = abs_tol * (float)sqrt(fro_s);
+  __syncthreads();
+  for (int e = t; e < N * N; e += NT) {
+    const int i = e / N, j = e % N;
+    if (j <= i) {
+      const double di = dsc[i], dj = dsc[j];
+      A[i * LDA + j] = (di > 0.0 && dj > 0.0) ? A[i * LDA + j] / (di * dj) : 0.0;
+    }
+  }
+  __syncthreads();
+  // right-looking Cholesky S' = L' L'^T (f64, lower triangle in place)
+  for (int j = 0; j < N; ++j) {
+    const double d = A[j * LDA + j];
+    if (!(d > 1e-300)) {
+      if (t == 0) fail = 1;
+      break;  // uniform: every thread read the same pivot
+    }
+    const double rp = 1.0 / sqrt(d);
+    for (int i = j + 1 + t; i < N; i += NT) A[i * LDA + j] *= rp;
+    __syncthreads();
+    if (t == 0) A[j * LDA + j] = d * rp;
+    const int w = N - j - 1;
+    for (int e = t; e < w * w; e += NT) {
+      const int i = j + 1 + e / w, k = j + 1 + e % w;
+      if (k <= i) A[i * LDA + k] -= A[i * LDA + j] * A[k * LDA + j];
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  if (fail) return;
+  // B = diag(s) L' as fp32 columns: M[c][r] = s_r L'[r][c] (r >= c)
+  for (int e = t; e < N * N; e += NT) {
+    const int c = e / N, r = e % N;
+    M[c * LDM + r] = r >= c ? (float)(dsc[r] * A[r * LDA + c]) : 0.f;
+  }
+  __syncthreads();
+  const int k = t >> 4, l16 = t & 15, r0 = l16 * RPT;
+  bool converged = false;
+  int sweep = 0;
+  for (; sweep < 40; ++sweep) {
+    int rot = 0;
+    for (int r = 0; r < N - 1; ++r) {
+      int p, q;
+      if (k == 0) { p = N - 1; q = r; }
+      else {
+        p = r + k; if (p >= N - 1) p -= N - 1;
+        q = r - k; if (q < 0) q += N - 1;
+      }
+      float cp[RPT], cq[RPT];
+      ld_rows<RPT>(M + p * LDM + r0, cp);
+      ld_rows<RPT>(M + q * LDM + r0, cq);
+      float a = 0.f, b = 0.f, g = 0.f;
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        a = fmaf(cp[i], cp[i], a);
+        b = fmaf(cq[i], cq[i], b);
+        g = fmaf(cp[i], cq[i], g);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+        g += __shfl_xor_sync(0xffffffffu, g, o);
+      }
+      if (fabsf(g) > tol * sqrtf(a * b) && fabsf(g) > floor_abs) {
+        const float zeta = (b - a) / (2.f * g);
+        const float tt = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
+        const float c = rsqrtf(1.f + tt * tt), s = tt * c;
+        float np_[RPT], nq_[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          np_[i] = c * cp[i] - s * cq[i];
+          nq_[i] = s * cp[i] + c * cq[i];
+        }
+        st_rows<RPT>(M + p * LDM + r0, np_);
+        st_rows<RPT>(M + q * LDM + r0, nq_);
+        rot = 1;
+      }
+      __syncthreads();
+    }
+    if (!__syncthreads_or(rot)) { converged = true; ++sweep; break; }
+  }
+  // eigenvalues = squared column norms; descending, ties to the lower index
+  for (int c = t; c < N; c += NT) {
+    float s = 0.f;
+    for (int r = 0; r < N; ++r) s = fmaf(M[c * LDM + r], M[c * LDM + r], s);
+    lam[c] = s;
+    if (!(s > 0.f)) fail = 1;
+  }
+  __syncthreads();
+  if (fail) return;
+  float* ev = evals + u * e_bs;
+  float* vg = evecs + u * v_bs;
+  for (int c = t; c < N; c += NT) {
+    const float lc = lam[c];
+    int rank = 0;
+    for (int j = 0; j < N; ++j) {
+      const float lj = lam[j];
+      rank += (lj > lc) || (lj == lc && j < c);
+    }
+    ev[rank] = lc;
+    // unit column, sign fixed so that its largest-magnitude entry (lowest
+    // index on a tie) is positive
+    const float inv = rsqrtf(lc);
+    float big = -1.f, sgn = 1.f;
+    for (int r = 0; r < N; ++r) {
+      const float v = M[c * LDM + r];
+      if (fabsf(v) > big) { big = fabsf(v); sgn = v < 0.f ? -1.f : 1.f; }
+    }
+    for (int r = 0; r < N; ++r) vg[(long long)r * ldv + rank] = sgn * inv * M[c * LDM + r];
+  }
+  if (t == 0) {
+    if (!converged && status) atomicOr(status + u * st_bs, ST_NOCONVERGE);
+    if (done) done[u * d_bs] = 1;
+  }
+}
+
 // Out[row] = In[row] R^{-1} for every row of a T x n block, one row per
 // thread (forward substitution x R = z) with the row in registers; R upper
 // triangular in shared memory.  A zero diagonal gives a zero column.
@@ -692,6 +892,26 @@ jolt_status launch_chol_inv(const float* G, long long g_bs, int n, int nparts, l
   }
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
+}
+
+jolt_status launch_feat_eig(const double* S64, long long s_bs, int n, int batch, float* evals,
+                            long long e_bs, float* evecs, long long v_bs, int ldv, int* status,
+                            long long st_bs, int* done, long long d_bs, cudaStream_t st) {
+  if (batch <= 0) return JOLT_OK;
+  auto go = [&](auto kern, int N) -> jolt_status {
+    const size_t smem = (size_t)N * (N + 1) * 8 + (size_t)N * 8 + (size_t)N * (N + 4) * 4 + N * 4;
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    kern<<<batch, 8 * N, smem, st>>>(S64, s_bs, evals, e_bs, evecs, v_bs, ldv, status, st_bs, done,
+                                     d_bs, FEAT_TOL, JAC_ABS_EXACT);
+    JOLT_LAUNCH_CHECK();
+    return JOLT_OK;
+  };
+  switch (n) {
+    case 128: return go(feat_eig_kernel<128>, 128);
+    case 64: return go(feat_eig_kernel<64>, 64);
+    case 32: return go(feat_eig_kernel<32>, 32);
+    default: return JOLT_ERR_INVALID;
+  }
 }
 
 jolt_status launch_trsm_rows(const float* In, float* Out, long long blk_bs, const float* R,

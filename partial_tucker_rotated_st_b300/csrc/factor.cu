@@ -36,9 +36,9 @@ constexpr int SUB_MAX_BLOCKS = 25;
 constexpr float RITZ_TOL_REL = 1e-4f;
 constexpr float RITZ_TOL_ABS = 1e-5f;
 
-// Sd[u] = sum_s Sdp[u][s], in f64.
-__global__ void reduce_splits_kernel(char* ws, size_t ub, size_t o_part, size_t o_out, int nsplit,
-                                     int n) {
+// Sd[u] = sum_s Sdp[u][s], in f64 (kept in f64 and rounded to fp32).
+__global__ void reduce_splits_kernel(char* ws, size_t ub, size_t o_part, size_t o_out,
+                                     size_t o_out64, int nsplit, int n) {
   const int u = blockIdx.y;
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
@@ -46,6 +46,7 @@ __global__ void reduce_splits_kernel(char* ws, size_t ub, size_t o_part, size_t 
   double s = 0.0;
   for (int k = 0; k < nsplit; ++k) s += (double)p[(size_t)k * n + e];
   ((float*)(ws + u * ub + o_out))[e] = (float)s;
+  ((double*)(ws + u * ub + o_out64))[e] = s;
 }
 
 // out[u][r][c] = fp16(in[u][r][c]) for r < rows, c < cols (row strides given).
@@ -518,10 +519,15 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
                       fs));
     }
     reduce_splits_kernel<<<dim3(blocks_for(D * D), U), 256, 0, fs>>>(ws, ub, L.o_Sdp, L.o_Sd,
-                                                                     L.nsplit, D * D);
+                                                                     L.o_Sd64, L.nsplit, D * D);
     JOLT_LAUNCH_CHECK();
+    // Cholesky + one-sided Jacobi; units whose S_d is not definite (done
+    // flag left clear) are solved by the two-sided Jacobi
+    int* done = status + 2;
+    TRY(launch_feat_eig((const double*)(ws + L.o_Sd64), ub4 / 2, D, U, c.f(L.o_evd), ub4,
+                        c.f(L.o_Vd), ub4, D, status, ub4, done, ub4, fs));
     TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, 1, 0, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
-                      status, ub4, nullptr, 0, JAC_ABS_EXACT, fs));
+                      status, ub4, done, ub4, JAC_ABS_EXACT, fs));
   }
   if (RD > 0) {
     round_f16_kernel<<<dim3(blocks_for(D * RD), 1, U), 256, 0, fs>>>(ws, ub, L.o_Vd, D, L.o_Ud16,

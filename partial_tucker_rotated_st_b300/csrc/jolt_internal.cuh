@@ -66,7 +66,7 @@ struct Layout {
   int ncand;
   int cost_model, align, block;
   // section offsets, bytes from the unit's base (unit u at ws + u * unit_bytes)
-  size_t o_status, o_Sd, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16;
+  size_t o_status, o_Sd, o_Sd64, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16;
   size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
   size_t o_Yt;           // Y relaid [T][RD*H] and its tf32 low part (token Gram)
   size_t unit_bytes;
@@ -124,6 +124,15 @@ jolt_status launch_chol(const float* G, long long g_bstride, int n, int nparts, 
                         int batch, float* R, long long r_bstride, int* status,
                         long long status_bstride, const int* skip, long long skip_stride,
                         bool f64, float shift, cudaStream_t st);
+// Eigenpairs of a batch of symmetric positive-definite n x n matrices (n in
+// {32, 64, 128}; f64 input, row-major) by Cholesky + one-sided Jacobi: evals
+// descending, evecs columns (row stride ldv), signs as launch_jacobi.  done[b]
+// is set to 1 on success and left 0 where the matrix is not definite (the
+// caller then re-solves those with launch_jacobi, skip = done).
+jolt_status launch_feat_eig(const double* S64, long long s_bstride, int n, int batch,
+                            float* evals, long long e_bstride, float* evecs, long long v_bstride,
+                            int ldv, int* status, long long status_bstride, int* done,
+                            long long done_bstride, cudaStream_t st);
 // The same Cholesky (fp32, n in {32, 40, 48, 64}) writing R^{-1} instead of R.
 jolt_status launch_chol_inv(const float* G, long long g_bstride, int n, int nparts,
                             long long part_s, int batch, float* Rinv, long long r_bstride,
