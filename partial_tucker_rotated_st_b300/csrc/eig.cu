@@ -572,113 +572,160 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
   if (t == 0 && bad && status) atomicOr(status + u * s_bs, ST_NOTPD);
 }
 
-// RPT consecutive floats of shared memory (16-byte aligned when RPT % 4 == 0,
-// 8-byte aligned when RPT == 2) to registers and back.
+// The RPT rows of lane l (of 16) in a shared-memory column: rows 4l..4l+3 of
+// every 64-row chunk (RPT % 4 == 0), else rows RPT l .. RPT l + RPT - 1; each
+// access of the 16 lanes is one contiguous stretch.
 template <int RPT>
-__device__ __forceinline__ void ld_rows(const float* p, float (&v)[RPT]) {
+__device__ __forceinline__ void ld_rows(const float* col, int l, float (&v)[RPT]) {
   if constexpr (RPT % 4 == 0) {
 #pragma unroll
-    for (int i = 0; i < RPT; i += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(p + i);
-      v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+    for (int c = 0; c < RPT / 4; ++c) {
+      const float4 x = *reinterpret_cast<const float4*>(col + 64 * c + 4 * l);
+      v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
     }
   } else if constexpr (RPT == 2) {
-    const float2 x = *reinterpret_cast<const float2*>(p);
+    const float2 x = *reinterpret_cast<const float2*>(col + 2 * l);
     v[0] = x.x; v[1] = x.y;
   } else {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) v[i] = p[i];
+    for (int i = 0; i < RPT; ++i) v[i] = col[RPT * l + i];
   }
 }
 template <int RPT>
-__device__ __forceinline__ void st_rows(float* p, const float (&v)[RPT]) {
+__device__ __forceinline__ void st_rows(float* col, int l, const float (&v)[RPT]) {
   if constexpr (RPT % 4 == 0) {
 #pragma unroll
-    for (int i = 0; i < RPT; i += 4)
-      *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    for (int c = 0; c < RPT / 4; ++c)
+      *reinterpret_cast<float4*>(col + 64 * c + 4 * l) =
+          make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
   } else if constexpr (RPT == 2) {
-    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+    *reinterpret_cast<float2*>(col + 2 * l) = make_float2(v[0], v[1]);
   } else {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) p[i] = v[i];
+    for (int i = 0; i < RPT; ++i) col[RPT * l + i] = v[i];
   }
+}
+
+// Double-float arithmetic (an unevaluated sum hi + lo of two floats, about
+// 48 significant bits; Dekker 1971), for the feature Cholesky: the fp64 pipe
+// of this part is far slower than fp32, and this factorisation needs more
+// than fp32 accuracy.
+struct df { float h, l; };
+__device__ __forceinline__ df df_norm(float s, float e) {
+  const float h = s + e;
+  return df{h, e - (h - s)};
+}
+__device__ __forceinline__ df df_mul(df a, df b) {
+  const float p = a.h * b.h;
+  float e = fmaf(a.h, b.h, -p);
+  e = fmaf(a.h, b.l, fmaf(a.l, b.h, e));
+  return df_norm(p, e);
+}
+// a - b c
+__device__ __forceinline__ df df_fnma(df a, df b, df c) {
+  const float p = b.h * c.h;
+  float pe = fmaf(b.h, c.h, -p);
+  pe = fmaf(b.h, c.l, fmaf(b.l, c.h, pe));
+  const float s = a.h - p;
+  const float bb = s - a.h;
+  float e = (a.h - (s - bb)) + (-p - bb);
+  e += a.l - pe;
+  return df_norm(s, e);
+}
+// 1 / sqrt(d) for d > 0: one Newton step y + y (1 - d y^2) / 2 from the fp32
+// estimate, the residual taken in double-float.
+__device__ __forceinline__ df df_rsqrt(df d) {
+  const float y = rsqrtf(d.h);
+  const df y2 = df_mul(df{y, 0.f}, df{y, 0.f});
+  const df r = df_fnma(df{1.f, 0.f}, d, y2);   // 1 - d y^2
+  return df_norm(y, 0.5f * y * r.h);
 }
 
 // Eigenpairs of the feature Gram by one-sided Jacobi (Hestenes 1958; its
 // relative accuracy: Demmel & Veselic 1992).  S = B B^T with B = diag(s) L',
-// L' the Cholesky factor (f64) of the equilibrated S' = diag(s)^-1 S
-// diag(s)^-1.  Plane rotations applied to the columns of B (fp32) drive them
-// to mutual orthogonality, B J = U Sigma; then S = U Sigma^2 U^T: the
+// L' the Cholesky factor (double-float) of the equilibrated S' = diag(s)^-1
+// S diag(s)^-1.  Plane rotations applied to the columns of B (fp32) drive
+// them to mutual orthogonality, B J = U Sigma; then S = U Sigma^2 U^T: the
 // eigenvectors are the normalised columns and the eigenvalues their squared
 // norms, so no rotation product has to be accumulated.  Columns live in
 // shared memory; each round of the round-robin (circle) ordering gives the
 // N/2 disjoint pairs to N/2 groups of 16 threads, each thread holding N/16
-// rows of its two columns in registers.  A pair is rotated while
-// |b_p . b_q| > tol sqrt(|b_p|^2 |b_q|^2) and above an absolute floor; a
-// sweep without rotations ends the solve.  A pivot that is not positive
-// (rank-deficient S) or a zero column leaves the unit's `done` flag clear,
-// and the caller solves that unit with the two-sided Jacobi instead.
+// rows of its two columns in registers (rows 4l..4l+3 of every 64-row chunk
+// for lane l, so that the 16-byte loads of a group are contiguous).  A pair
+// is rotated while |b_p . b_q| > tol sqrt(|b_p|^2 |b_q|^2) and above an
+// absolute floor; a sweep without rotations ends the solve.  A pivot that is
+// not positive (rank-deficient S) or a zero column leaves the unit's `done`
+// flag clear, and the caller solves that unit with the two-sided Jacobi.
 template <int N>
 __global__ void __launch_bounds__(8 * N, 1)
 feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restrict__ evals,
                 long long e_bs, float* __restrict__ evecs, long long v_bs, int ldv, int* status,
                 long long st_bs, int* done, long long d_bs, float tol, float abs_tol) {
   constexpr int NT = 8 * N;
-  constexpr int RPT = N / 16;   // rows per thread
+  constexpr int TY = NT / 32;   // thread rows of the Cholesky update
+  constexpr int RPT = N / 16;   // Jacobi rows per thread
   constexpr int LDA = N + 1;
   constexpr int LDM = N + 4;    // column stride, 16-byte aligned
   extern __shared__ __align__(16) unsigned char fe_sm[];
-  double* A = (double*)fe_sm;            // N x LDA: S', then L' (lower)
-  double* dsc = A + N * LDA;             // [N] sqrt(S_ii)
+  df* A = (df*)fe_sm;                    // N x LDA: S', then L' (lower)
+  df* dsc = A + N * LDA;                 // [N] sqrt(S_ii)
   float* M = (float*)(dsc + N);          // N columns of LDM floats
   float* lam = M + N * LDM;              // [N] squared column norms
   __shared__ int fail;
-  __shared__ double fro_part[NT / 32];
-  const int u = blockIdx.x, t = threadIdx.x;
-  if (done) done[u * d_bs] = 0;
+  __shared__ float fro_part[NT / 32];
+  const int u = blockIdx.x, t = threadIdx.x, tx = t & 31, ty = t >> 5;
+  if (done && t == 0) done[u * d_bs] = 0;
   const double* Sg = S64 + u * s_bs;
   if (t == 0) fail = 0;
-  double fro = 0.0;
+  // s_i = sqrt(S_ii) and 1 / s_i (f64, N values), Frobenius norm of S
+  if (t < N) {
+    const double d = Sg[t * N + t];
+    const double sd = d > 0.0 ? sqrt(d) : 0.0;
+    const double r = sd > 0.0 ? 1.0 / sd : 0.0;
+    const float sh = (float)sd, rh = (float)r;
+    dsc[t] = df{sh, (float)(sd - (double)sh)};
+    lam[t] = 0.f;
+    M[t] = rh;                                  // scratch: 1 / s_i (hi, lo)
+    M[N + t] = (float)(r - (double)rh);
+  }
+  float fro = 0.f;
   for (int e = t; e < N * N; e += NT) {
-    const int i = e / N, j = e % N;
-    const double v = 0.5 * (Sg[i * N + j] + Sg[j * N + i]);
-    A[i * LDA + j] = v;
-    fro += v * v;
+    const float v = (float)Sg[e];
+    fro = fmaf(v, v, fro);
   }
-  for (int o = 16; o > 0; o >>= 1) fro += __shfl_xor_sync(0xffffffffu, fro, o);
-  if ((t & 31) == 0) fro_part[t >> 5] = fro;
+  fro = warp_sum(fro);
+  if (tx == 0) fro_part[ty] = fro;
   __syncthreads();
-  for (int i = t; i < N; i += NT) {
-    const double d = A[i * LDA + i];
-    dsc[i] = d > 0.0 ? sqrt(d) : 0.0;
-  }
-  double fro_s = 0.0;
+  float fro_s = 0.f;
   for (int i = 0; i < NT / 32; ++i) fro_s += fro_part[i];
-  const float floor_abs = abs_tol * (float)sqrt(fro_s);
-  __syncthreads();
+  const float floor_abs = abs_tol * sqrtf(fro_s);
+  // S'_ij = S_ij / (s_i s_j), lower triangle, double-float
   for (int e = t; e < N * N; e += NT) {
     const int i = e / N, j = e % N;
     if (j <= i) {
-      const double di = dsc[i], dj = dsc[j];
-      A[i * LDA + j] = (di > 0.0 && dj > 0.0) ? A[i * LDA + j] / (di * dj) : 0.0;
+      const double x = 0.5 * (Sg[i * N + j] + Sg[j * N + i]);
+      const float xh = (float)x;
+      const df v{xh, (float)(x - (double)xh)};
+      A[i * LDA + j] = df_mul(df_mul(v, df{M[i], M[N + i]}), df{M[j], M[N + j]});
     }
   }
   __syncthreads();
-  // right-looking Cholesky S' = L' L'^T (f64, lower triangle in place)
+  // right-looking Cholesky S' = L' L'^T in double-float, lower triangle in
+  // place; thread (ty, tx) updates rows ty + TY a and columns tx + 32 b
   for (int j = 0; j < N; ++j) {
-    const double d = A[j * LDA + j];
-    if (!(d > 1e-300)) {
+    const df d = A[j * LDA + j];
+    if (!(d.h > 1e-30f)) {
       if (t == 0) fail = 1;
       break;  // uniform: every thread read the same pivot
     }
-    const double rp = 1.0 / sqrt(d);
-    for (int i = j + 1 + t; i < N; i += NT) A[i * LDA + j] *= rp;
+    const df rp = df_rsqrt(d);
+    for (int i = j + 1 + t; i < N; i += NT) A[i * LDA + j] = df_mul(A[i * LDA + j], rp);
     __syncthreads();
-    if (t == 0) A[j * LDA + j] = d * rp;
-    const int w = N - j - 1;
-    for (int e = t; e < w * w; e += NT) {
-      const int i = j + 1 + e / w, k = j + 1 + e % w;
-      if (k <= i) A[i * LDA + k] -= A[i * LDA + j] * A[k * LDA + j];
+    if (t == 0) A[j * LDA + j] = df_mul(d, rp);
+    for (int i = j + 1 + ty; i < N; i += TY) {
+      const df li = A[i * LDA + j];
+      for (int k = j + 1 + tx; k <= i; k += 32)
+        A[i * LDA + k] = df_fnma(A[i * LDA + k], li, A[k * LDA + j]);
     }
     __syncthreads();
   }
@@ -687,10 +734,10 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
   // B = diag(s) L' as fp32 columns: M[c][r] = s_r L'[r][c] (r >= c)
   for (int e = t; e < N * N; e += NT) {
     const int c = e / N, r = e % N;
-    M[c * LDM + r] = r >= c ? (float)(dsc[r] * A[r * LDA + c]) : 0.f;
+    M[c * LDM + r] = r >= c ? df_mul(dsc[r], A[r * LDA + c]).h : 0.f;
   }
   __syncthreads();
-  const int k = t >> 4, l16 = t & 15, r0 = l16 * RPT;
+  const int k = t >> 4, l16 = t & 15;
   bool converged = false;
   int sweep = 0;
   for (; sweep < 40; ++sweep) {
@@ -703,8 +750,8 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
         q = r - k; if (q < 0) q += N - 1;
       }
       float cp[RPT], cq[RPT];
-      ld_rows<RPT>(M + p * LDM + r0, cp);
-      ld_rows<RPT>(M + q * LDM + r0, cq);
+      ld_rows<RPT>(M + p * LDM, l16, cp);
+      ld_rows<RPT>(M + q * LDM, l16, cq);
       float a = 0.f, b = 0.f, g = 0.f;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) {
@@ -728,8 +775,8 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
           np_[i] = c * cp[i] - s * cq[i];
           nq_[i] = s * cp[i] + c * cq[i];
         }
-        st_rows<RPT>(M + p * LDM + r0, np_);
-        st_rows<RPT>(M + q * LDM + r0, nq_);
+        st_rows<RPT>(M + p * LDM, l16, np_);
+        st_rows<RPT>(M + q * LDM, l16, nq_);
         rot = 1;
       }
       __syncthreads();
@@ -900,6 +947,7 @@ jolt_status launch_feat_eig(const double* S64, long long s_bs, int n, int batch,
   if (batch <= 0) return JOLT_OK;
   auto go = [&](auto kern, int N) -> jolt_status {
     const size_t smem = (size_t)N * (N + 1) * 8 + (size_t)N * 8 + (size_t)N * (N + 4) * 4 + N * 4;
+    static_assert(sizeof(float2) == 8, "double-float element");
     JOLT_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     kern<<<batch, 8 * N, smem, st>>>(S64, s_bs, evals, e_bs, evecs, v_bs, ldv, status, st_bs, done,
                                      d_bs, FEAT_TOL, JAC_ABS_EXACT);

@@ -97,27 +97,41 @@ __device__ __forceinline__ float reduce4(const float (&v)[4], int lane) {
 template <int LPR>
 __device__ __forceinline__ void score(const float2 (&acc)[SW_RPT][SW_EPT / 2],
                                       const SweepArgs& a, float* cells, int cell0, int lane) {
+  // independent accumulators per row and per half of the row keep the
+  // dependency chains short
   float m[SW_RPT];
-  float2 e02 = make_float2(0.f, 0.f);
+  float2 e0[SW_RPT];
 #pragma unroll
   for (int r = 0; r < SW_RPT; ++r) {
-    float mm = 0.f;
+    float ma = 0.f, mb = 0.f;
+    float2 ea = make_float2(0.f, 0.f), eb = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < SW_EPT / 2; ++i) {
-      mm = fmaxf(mm, fmaxf(fabsf(acc[r][i].x), fabsf(acc[r][i].y)));
-      e02 = __ffma2_rn(acc[r][i], acc[r][i], e02);
+    for (int i = 0; i < SW_EPT / 2; i += 2) {
+      ma = fmaxf(ma, fmaxf(fabsf(acc[r][i].x), fabsf(acc[r][i].y)));
+      mb = fmaxf(mb, fmaxf(fabsf(acc[r][i + 1].x), fabsf(acc[r][i + 1].y)));
+      ea = __ffma2_rn(acc[r][i], acc[r][i], ea);
+      eb = __ffma2_rn(acc[r][i + 1], acc[r][i + 1], eb);
     }
+    float mm = fmaxf(ma, mb);
 #pragma unroll
     for (int o = 1; o < LPR; o <<= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
     m[r] = mm;
+    e0[r] = __fadd2_rn(ea, eb);
   }
-  const float2 M2 = f2(12582912.0f), nM2 = f2(-12582912.0f);  // round-half-even by 1.5*2^23
+  // round-half-even to an integer by adding and removing 1.5 * 2^23; the
+  // product y / s and the addition are fused, so q is the integer nearest
+  // to the exact y * (1/s)
+  const float2 M2 = f2(12582912.0f), nM2 = f2(-12582912.0f);
   float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ib = 0; ib < 4; ++ib) {
     if (ib >= a.nb) break;
-    if (a.b[ib] == 0) { v[ib] = e02.x + e02.y; continue; }
-    float2 eb = make_float2(0.f, 0.f);
+    if (a.b[ib] == 0) {
+      const float2 e = __fadd2_rn(e0[0], e0[1]);
+      v[ib] = e.x + e.y;
+      continue;
+    }
+    float2 ebr[SW_RPT];
 #pragma unroll
     for (int r = 0; r < SW_RPT; ++r) {
       const float s = round_f16(m[r] * a.rq[ib]);
@@ -125,15 +139,20 @@ __device__ __forceinline__ void score(const float2 (&acc)[SW_RPT][SW_EPT / 2],
       asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(inv) : "f"(s));
       if (!(s > 0.f)) inv = 0.f;
       const float2 inv2 = f2(inv), ns2 = f2(-s);
+      float2 ea = make_float2(0.f, 0.f), eb = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < SW_EPT / 2; ++i) {
-        const float2 z = __fmul2_rn(acc[r][i], inv2);
-        const float2 q = __fadd2_rn(__fadd2_rn(z, M2), nM2);
-        const float2 d = __ffma2_rn(ns2, q, acc[r][i]);
-        eb = __ffma2_rn(d, d, eb);
+      for (int i = 0; i < SW_EPT / 2; i += 2) {
+        const float2 qa = __fadd2_rn(__ffma2_rn(acc[r][i], inv2, M2), nM2);
+        const float2 qb = __fadd2_rn(__ffma2_rn(acc[r][i + 1], inv2, M2), nM2);
+        const float2 da = __ffma2_rn(ns2, qa, acc[r][i]);
+        const float2 db = __ffma2_rn(ns2, qb, acc[r][i + 1]);
+        ea = __ffma2_rn(da, da, ea);
+        eb = __ffma2_rn(db, db, eb);
       }
+      ebr[r] = __fadd2_rn(ea, eb);
     }
-    v[ib] = eb.x + eb.y;
+    const float2 e = __fadd2_rn(ebr[0], ebr[1]);
+    v[ib] = e.x + e.y;
   }
   const float t = reduce4(v, lane);
   if ((lane & 7) == 0) {
