@@ -25,9 +25,22 @@ namespace {
 constexpr int AL_THREADS = 512;
 constexpr int AL_MAX_ITER = 200;
 
-// Lexicographic key (k1, k2, index).
+// Lexicographic key (k1, k2, index) on unsigned integers that order like the
+// values they encode, so that no comparison needs the fp64 pipe: a double
+// maps to its bit pattern with the sign bit set (>= +0) or all bits inverted
+// (< 0), -0 first folded to +0; a signed cost to its value with the sign bit
+// flipped.
+__device__ __forceinline__ unsigned long long dkey(double x) {
+  long long b = __double_as_longlong(x);
+  if (b == (long long)0x8000000000000000ull) b = 0;
+  return (unsigned long long)(b ^ ((b >> 63) | (long long)0x8000000000000000ull));
+}
+__device__ __forceinline__ unsigned long long ikey(long long k) {
+  return (unsigned long long)k ^ 0x8000000000000000ull;
+}
+
 struct Key {
-  double k1, k2;
+  unsigned long long k1, k2;
   int i;
 };
 
@@ -46,11 +59,19 @@ __device__ void best_response(int U, int nc, const double* dist, const int64_t* 
   __shared__ long long part[AL_THREADS / 32];
   long long mine = 0;
   for (int u = w; u < U; u += nw) {
-    Key b{INFINITY, INFINITY, INT_MAX};
+    Key b{~0ull, ~0ull, INT_MAX};
     for (int c = lane; c < nc; c += 32) {
       const double d = dist[(long long)u * nc + c];
-      const double k = (double)cost[(long long)u * nc + c];
-      const Key x = (mode == 0) ? Key{__dadd_rn(d, __dmul_rn(lam, k)), k, c} : Key{k, d, c};
+      const long long k = cost[(long long)u * nc + c];
+      Key x;
+      if (mode == 0) {
+        x.k1 = dkey(__dadd_rn(d, __dmul_rn(lam, (double)k)));
+        x.k2 = ikey(k);
+      } else {
+        x.k1 = ikey(k);
+        x.k2 = dkey(d);
+      }
+      x.i = c;
       if (less_key(x, b)) b = x;
     }
 #pragma unroll

@@ -445,129 +445,162 @@ chol_kernel(const float* __restrict__ G, long long g_bs, int n, int nparts, long
 }
 
 // The same factorisation for n = N <= 64 in fp32, returning R^{-1} instead
-// of R.  Four threads own each row of L' (thread (r, q) holds columns
-// q*N/4 .. (q+1)*N/4 - 1 in registers).  Step j of the outer-product form:
-// the owners publish column j (c_r = a_rj, r >= j) to shared memory, and
-// after one barrier every row r > j takes a_rk -= c_r c_k / c_j on its own
-// columns j < k <= r; L'[r][j] = c_r / sqrt(c_j) goes to shared memory.  The
-// published column is double-buffered, so one barrier per step suffices.
-// Then X = L'^{-1} (X L' = I, X lower) by substitution along the columns,
-// the four threads of a row summing their partial dot products by shuffle,
-// and R^{-1} = S^{-1} X^T with S the equilibration scales.
+// of R, blocked by 8 columns so that the serial dependency chain is short:
+// per block column, warp 0 factors the 8 x 8 diagonal block in registers
+// (pivot and column entries broadcast by shuffle), one thread per row solves
+// its panel row against it, and all threads apply the rank-8 update to the
+// trailing lower triangle.  X = L'^{-1} follows blockwise: the diagonal
+// blocks by substitution (one thread per row), then X_ik = -X_ii sum_{m=k}^{i-1}
+// L_im X_mk, one block diagonal at a time.  R^{-1} = S^{-1} X^T with S the
+// equilibration scales.
 template <int N>
-__global__ void __launch_bounds__(4 * N)
+__global__ void __launch_bounds__(256)
 chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long long part_s,
                 float* __restrict__ Rinv, long long r_bs, int* status, long long s_bs,
                 const int* skip, long long sk_s, float shift) {
-  constexpr int QW = N / 4;
+  constexpr int NB = 8, NBLK = N / NB, NT = 256;
   constexpr int LD = N + 1;
+  static_assert(N % NB == 0 && N <= 64, "block size");
   const int u = blockIdx.x;
   if (skip && skip[u * sk_s]) return;
-  __shared__ float S[N * LD];  // the Gram, then L'
-  __shared__ float rds[N], dsc[N];
-  __shared__ float col[2][N];
-  __shared__ float rpiv[N];   // 1 / L'[j][j]
+  __shared__ float S[N * LD];    // the Gram, then L' (lower)
+  __shared__ float X[N * LD];    // L'^{-1} (lower); the gathered partial products
+  __shared__ float rds[N];
+  __shared__ float rpiv[N];      // 1 / L'_jj
   __shared__ int bad;
-  const int t = threadIdx.x, r = t >> 2, q = t & 3, k0 = q * QW;
+  const int t = threadIdx.x, lane = t & 31, tx = t & 31, ty = t >> 5;
   const float* Gg = G + u * g_bs;
   if (t == 0) bad = 0;
-  constexpr int PER = N / 4;   // N * N / (4 N) elements per thread
-  float gv[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) gv[i] = Gg[t + i * 4 * N];
-  for (int p = 1; p < nparts; ++p)
-#pragma unroll
-    for (int i = 0; i < PER; ++i) gv[i] += Gg[p * part_s + t + i * 4 * N];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = t + i * 4 * N;
-    S[(e / N) * LD + e % N] = gv[i];
+  for (int e = t; e < N * N; e += NT) {
+    float v = Gg[e];
+    for (int p = 1; p < nparts; ++p) v += Gg[p * part_s + e];
+    X[(e / N) * LD + e % N] = v;   // raw Gram, staged in X
   }
   __syncthreads();
   if (t < N) {
-    const float d = S[t * LD + t];
-    const float sd = d > 0.f ? sqrtf(d) : 0.f;
-    dsc[t] = sd;
-    rds[t] = sd > 0.f ? 1.f / sd : 0.f;
+    const float d = X[t * LD + t];
+    rds[t] = d > 0.f ? rsqrtf(d) : 0.f;
   }
   __syncthreads();
-  float a[QW];
-  {
-    const float rr = rds[r];
-#pragma unroll
-    for (int kk = 0; kk < QW; ++kk) {
-      const int k = k0 + kk;
-      float v = 0.f;
-      if (k <= r) {
-        v = 0.5f * (S[r * LD + k] + S[k * LD + r]) * rr * rds[k];
-        if (k == r && rr > 0.f) v += shift;
-      }
-      a[kk] = v;
+  // S' = D^-1 sym(G) D^-1 (+ shift on the diagonal), lower triangle
+  for (int e = t; e < N * N; e += NT) {
+    const int i = e / N, k = e % N;
+    if (k <= i) {
+      float v = 0.5f * (X[i * LD + k] + X[k * LD + i]) * rds[i] * rds[k];
+      if (k == i && rds[i] > 0.f) v += shift;
+      S[i * LD + k] = v;
     }
   }
-  __syncthreads();  // S is reused for L' below
-  for (int j = 0; j < N; ++j) {
-    float* cb = col[j & 1];
-    if (q == j / QW && r >= j) {
-      const int jj = j - k0;
-      float v = 0.f;
+  __syncthreads();
+  for (int kb = 0; kb < NBLK; ++kb) {
+    const int c0 = kb * NB, c1 = c0 + NB;
+    // (a) diagonal block, warp 0: lane r < 8 holds row c0 + r
+    if (t < 32) {
+      float a[NB];
 #pragma unroll
-      for (int kk = 0; kk < QW; ++kk) v = kk == jj ? a[kk] : v;
-      cb[r] = v;
-    }
-    __syncthreads();
-    if (r >= j) {
-      float d = cb[j];
-      if (!(d >= 0.f)) {
-        if (t == 4 * j) bad = 1;
-        d = 0.f;
-      }
-      const float cr = cb[r];
-      const float rp = d > 0.f ? rsqrtf(d) : 0.f;  // 1 / sqrt(c_j)
-      if (q == 0) {
-        S[r * LD + j] = r == j ? d * rp : cr * rp;
-        if (r == j) rpiv[j] = rp;
-      }
-      if (r > j) {
-        const float f = cr * rp * rp;
+      for (int m = 0; m < NB; ++m) a[m] = (lane < NB && m <= lane) ? S[(c0 + lane) * LD + c0 + m] : 0.f;
 #pragma unroll
-        for (int kk = 0; kk < QW; ++kk) {
-          const int k = k0 + kk;
-          if (k > j && k <= r) a[kk] = fmaf(-f, cb[k], a[kk]);
+      for (int j = 0; j < NB; ++j) {
+        float d = __shfl_sync(0xffffffffu, a[j], j);
+        if (!(d >= 0.f)) { if (lane == 0) bad = 1; d = 0.f; }
+        const float rp = d > 0.f ? rsqrtf(d) : 0.f;
+        if (lane == j) { a[j] = d * rp; rpiv[c0 + j] = rp; }
+        else if (lane > j) a[j] *= rp;
+#pragma unroll
+        for (int m = j + 1; m < NB; ++m) {
+          const float lm = __shfl_sync(0xffffffffu, a[j], m);
+          if (lane >= m && lane < NB) a[m] = fmaf(-a[j], lm, a[m]);
         }
       }
+      if (lane < NB)
+#pragma unroll
+        for (int m = 0; m < NB; ++m)
+          if (m <= lane) S[(c0 + lane) * LD + c0 + m] = a[m];
     }
+    __syncthreads();
+    if (c1 >= N) break;
+    // (b) panel: row i solves x L11^T = a, x_m = (a_m - sum_{q<m} x_q L11[m][q]) / L11[m][m]
+    for (int i = c1 + t; i < N; i += NT) {
+      float x[NB];
+#pragma unroll
+      for (int m = 0; m < NB; ++m) {
+        float v = S[i * LD + c0 + m];
+#pragma unroll
+        for (int q = 0; q < m; ++q) v = fmaf(-x[q], S[(c0 + m) * LD + c0 + q], v);
+        x[m] = v * rpiv[c0 + m];
+      }
+#pragma unroll
+      for (int m = 0; m < NB; ++m) S[i * LD + c0 + m] = x[m];
+    }
+    __syncthreads();
+    // (c) trailing update of the lower triangle: a_ik -= sum_m L[i][c0+m] L[k][c0+m]
+    for (int i = c1 + ty; i < N; i += NT / 32) {
+      float li[NB];
+#pragma unroll
+      for (int m = 0; m < NB; ++m) li[m] = S[i * LD + c0 + m];
+      for (int k = c1 + tx; k <= i; k += 32) {
+        float v = S[i * LD + k];
+#pragma unroll
+        for (int m = 0; m < NB; ++m) v = fmaf(-li[m], S[k * LD + c0 + m], v);
+        S[i * LD + k] = v;
+      }
+    }
+    __syncthreads();
+  }
+  // X = L'^{-1}: diagonal blocks first, row r of block kb by substitution
+  // (x L_kk = e_r: x_r = 1 / L_rr, x_j = -(sum_{m=j+1}^{r} x_m L_mj) / L_jj)
+  if (t < N) {
+    const int kb = t / NB, r = t % NB, c0 = kb * NB;
+    float x[NB];
+#pragma unroll
+    for (int j = NB - 1; j >= 0; --j) {
+      float v = 0.f;
+      if (j == r) v = rpiv[c0 + r];
+      else if (j < r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = j + 1; m < NB; ++m)
+          if (m <= r) acc = fmaf(x[m], S[(c0 + m) * LD + c0 + j], acc);
+        v = -acc * rpiv[c0 + j];
+      }
+      x[j] = v;
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) X[(c0 + r) * LD + c0 + j] = x[j];
   }
   __syncthreads();
-  // row r of X = L'^{-1}: sum_{k=j..r} X[r][k] L'[k][j] = delta_rj, j descending
-  float x[QW];
-#pragma unroll
-  for (int kk = 0; kk < QW; ++kk) x[kk] = 0.f;
-  for (int j = N - 1; j >= 0; --j) {
-    float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < QW; kk += 2) {
-      const int k = k0 + kk;
-      if (k > j && k <= r) p0 = fmaf(x[kk], S[k * LD + j], p0);
-      if (k + 1 > j && k + 1 <= r) p1 = fmaf(x[kk + 1], S[(k + 1) * LD + j], p1);
+  // off-diagonal blocks, one block diagonal d = i - k at a time:
+  // P_ik = sum_{m=k}^{i-1} L_im X_mk (into the upper triangle of X as scratch),
+  // then X_ik = -X_ii P_ik
+  for (int d = 1; d < NBLK; ++d) {
+    const int nblk = NBLK - d;
+    for (int e = t; e < nblk * NB * NB; e += NT) {
+      const int k = e / (NB * NB), rc = e % (NB * NB), r = rc / NB, c = rc % NB;
+      const int i = k + d;
+      const int row = i * NB + r, col = k * NB + c;
+      float acc = 0.f;
+      for (int m = k * NB + c; m < i * NB; ++m)   // X_mk is zero above its diagonal
+        acc = fmaf(S[row * LD + m], X[m * LD + col], acc);
+      X[col * LD + row] = acc;                     // P^T, upper triangle
     }
-    float part = p0 + p1;
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    if (j <= r && q == j / QW) {
-      const float v = ((j == r ? 1.f : 0.f) - part) * rpiv[j];
-      const int jj = j - k0;
+    __syncthreads();
+    for (int e = t; e < nblk * NB * NB; e += NT) {
+      const int k = e / (NB * NB), rc = e % (NB * NB), r = rc / NB, c = rc % NB;
+      const int i = k + d;
+      const int row = i * NB + r, col = k * NB + c;
+      float acc = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < QW; ++kk)
-        if (kk == jj) x[kk] = v;
+      for (int q = 0; q < NB; ++q)
+        if (q <= r) acc = fmaf(X[row * LD + i * NB + q], X[col * LD + i * NB + q], acc);
+      X[row * LD + col] = -acc;
     }
+    __syncthreads();
   }
   // R^{-1}[k][r] = X[r][k] / s_k
   float* Rg = Rinv + u * r_bs;
-#pragma unroll
-  for (int kk = 0; kk < QW; ++kk) {
-    const int k = k0 + kk;
-    Rg[k * N + r] = k <= r ? x[kk] * rds[k] : 0.f;
+  for (int e = t; e < N * N; e += NT) {
+    const int k = e / N, r = e % N;
+    Rg[e] = k <= r ? X[r * LD + k] * rds[k] : 0.f;
   }
   if (t == 0 && bad && status) atomicOr(status + u * s_bs, ST_NOTPD);
 }
@@ -656,11 +689,14 @@ __device__ __forceinline__ df df_rsqrt(df d) {
 // absolute floor; a sweep without rotations ends the solve.  A pivot that is
 // not positive (rank-deficient S) or a zero column leaves the unit's `done`
 // flag clear, and the caller solves that unit with the two-sided Jacobi.
-template <int N>
+// Input: the sum of nparts partials G + b*g_bs + p*part_s (row stride lda),
+// symmetrised; TIn is double or float.
+template <int N, typename TIn>
 __global__ void __launch_bounds__(8 * N, 1)
-feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restrict__ evals,
-                long long e_bs, float* __restrict__ evecs, long long v_bs, int ldv, int* status,
-                long long st_bs, int* done, long long d_bs, float tol, float abs_tol) {
+sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, long long part_s,
+               float* __restrict__ evals, long long e_bs, float* __restrict__ evecs,
+               long long v_bs, int ldv, int ncols_out, int* status, long long st_bs, int* done,
+               long long d_bs, const int* skip, long long sk_s, float tol, float abs_tol) {
   constexpr int NT = 8 * N;
   constexpr int TY = NT / 32;   // thread rows of the Cholesky update
   constexpr int RPT = N / 16;   // Jacobi rows per thread
@@ -674,12 +710,22 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
   __shared__ int fail;
   __shared__ float fro_part[NT / 32];
   const int u = blockIdx.x, t = threadIdx.x, tx = t & 31, ty = t >> 5;
-  if (done && t == 0) done[u * d_bs] = 0;
-  const double* Sg = S64 + u * s_bs;
+  if (skip && skip[u * sk_s]) {
+    if (t == 0) done[u * d_bs] = 1;   // nothing to solve
+    return;
+  }
+  if (t == 0) done[u * d_bs] = 0;
+  const TIn* Gg = G + u * g_bs;
+  auto sval = [&](int i, int j) -> double {  // symmetrised sum of the partials
+    double v = 0.0;
+    for (int p = 0; p < nparts; ++p)
+      v += (double)Gg[p * part_s + (long long)i * lda + j] + (double)Gg[p * part_s + (long long)j * lda + i];
+    return 0.5 * v;
+  };
   if (t == 0) fail = 0;
   // s_i = sqrt(S_ii) and 1 / s_i (f64, N values), Frobenius norm of S
   if (t < N) {
-    const double d = Sg[t * N + t];
+    const double d = sval(t, t);
     const double sd = d > 0.0 ? sqrt(d) : 0.0;
     const double r = sd > 0.0 ? 1.0 / sd : 0.0;
     const float sh = (float)sd, rh = (float)r;
@@ -690,7 +736,7 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
   }
   float fro = 0.f;
   for (int e = t; e < N * N; e += NT) {
-    const float v = (float)Sg[e];
+    const float v = (float)sval(e / N, e % N);
     fro = fmaf(v, v, fro);
   }
   fro = warp_sum(fro);
@@ -703,7 +749,7 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
   for (int e = t; e < N * N; e += NT) {
     const int i = e / N, j = e % N;
     if (j <= i) {
-      const double x = 0.5 * (Sg[i * N + j] + Sg[j * N + i]);
+      const double x = sval(i, j);
       const float xh = (float)x;
       const df v{xh, (float)(x - (double)xh)};
       A[i * LDA + j] = df_mul(df_mul(v, df{M[i], M[N + i]}), df{M[j], M[N + j]});
@@ -802,6 +848,7 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
       rank += (lj > lc) || (lj == lc && j < c);
     }
     ev[rank] = lc;
+    if (rank >= ncols_out) continue;
     // unit column, sign fixed so that its largest-magnitude entry (lowest
     // index on a tie) is positive
     const float inv = rsqrtf(lc);
@@ -814,7 +861,7 @@ feat_eig_kernel(const double* __restrict__ S64, long long s_bs, float* __restric
   }
   if (t == 0) {
     if (!converged && status) atomicOr(status + u * st_bs, ST_NOCONVERGE);
-    if (done) done[u * d_bs] = 1;
+    done[u * d_bs] = 1;
   }
 }
 
@@ -931,33 +978,39 @@ jolt_status launch_chol_inv(const float* G, long long g_bs, int n, int nparts, l
   if (n <= 0 || batch <= 0) return JOLT_OK;
   nparts = nparts < 1 ? 1 : nparts;
   switch (n) {
-    case 64: chol_inv_kernel<64><<<batch, 4 * 64, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
-    case 48: chol_inv_kernel<48><<<batch, 4 * 48, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
-    case 40: chol_inv_kernel<40><<<batch, 4 * 40, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
-    case 32: chol_inv_kernel<32><<<batch, 4 * 32, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 64: chol_inv_kernel<64><<<batch, 256, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 48: chol_inv_kernel<48><<<batch, 256, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 40: chol_inv_kernel<40><<<batch, 256, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
+    case 32: chol_inv_kernel<32><<<batch, 256, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
     default: return JOLT_ERR_INVALID;
   }
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
 
-jolt_status launch_feat_eig(const double* S64, long long s_bs, int n, int batch, float* evals,
-                            long long e_bs, float* evecs, long long v_bs, int ldv, int* status,
-                            long long st_bs, int* done, long long d_bs, cudaStream_t st) {
+jolt_status launch_sym_eig(const void* G, bool f64_in, long long g_bs, int lda, int n, int nparts,
+                           long long part_s, int batch, float* evals, long long e_bs,
+                           float* evecs, long long v_bs, int ldv, int ncols_out, int* status,
+                           long long st_bs, int* done, long long d_bs, const int* skip,
+                           long long sk_s, float abs_tol, cudaStream_t st) {
   if (batch <= 0) return JOLT_OK;
-  auto go = [&](auto kern, int N) -> jolt_status {
+  if (!done) return JOLT_ERR_INVALID;
+  nparts = nparts < 1 ? 1 : nparts;
+  auto go = [&](auto kern, int N, auto* gp) -> jolt_status {
     const size_t smem = (size_t)N * (N + 1) * 8 + (size_t)N * 8 + (size_t)N * (N + 4) * 4 + N * 4;
-    static_assert(sizeof(float2) == 8, "double-float element");
     JOLT_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    kern<<<batch, 8 * N, smem, st>>>(S64, s_bs, evals, e_bs, evecs, v_bs, ldv, status, st_bs, done,
-                                     d_bs, FEAT_TOL, JAC_ABS_EXACT);
+    kern<<<batch, 8 * N, smem, st>>>(gp, g_bs, lda, nparts, part_s, evals, e_bs, evecs, v_bs, ldv,
+                                     ncols_out, status, st_bs, done, d_bs, skip, sk_s, FEAT_TOL,
+                                     abs_tol);
     JOLT_LAUNCH_CHECK();
     return JOLT_OK;
   };
+  const double* gd = (const double*)G;
+  const float* gf = (const float*)G;
   switch (n) {
-    case 128: return go(feat_eig_kernel<128>, 128);
-    case 64: return go(feat_eig_kernel<64>, 64);
-    case 32: return go(feat_eig_kernel<32>, 32);
+    case 128: return f64_in ? go(sym_eig_kernel<128, double>, 128, gd) : go(sym_eig_kernel<128, float>, 128, gf);
+    case 64: return f64_in ? go(sym_eig_kernel<64, double>, 64, gd) : go(sym_eig_kernel<64, float>, 64, gf);
+    case 32: return f64_in ? go(sym_eig_kernel<32, double>, 32, gd) : go(sym_eig_kernel<32, float>, 32, gf);
     default: return JOLT_ERR_INVALID;
   }
 }

@@ -373,10 +373,14 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
   const bool svtc = sv_tc_supported(L);
   if (svtc) TRY(split_tok_gram(L, P.np, P.base, P.stride, st));
   const int* flags = (const int*)P.c(L.p_flag);
+  // Z lives in one of two buffers: Rayleigh-Ritz writes Z2 = S V2 into the
+  // other one, and the next block starts from it (its first power step is
+  // already done), so the roles swap every block
+  size_t zc = L.p_Z, zn = L.p_Z2;
   auto apply_S = [&]() -> jolt_status {  // Z = S V
-    if (svtc) return sv_tc(L, P.np, P.base, P.stride, st);
+    if (svtc) return sv_tc(L, P.np, P.base, P.stride, zc, st);
     GemmDesc gg = gd(T, Lw, T, 1, P.np, 1, opnd(P.c(L.p_ST), JOLT_F32, T, 1, 0, s4),
-                     opnd(P.c(L.p_V), JOLT_F32, Lw, 1, 0, s4), P.f(L.p_Z), Lw, 1, s4, 0, 0.f,
+                     opnd(P.c(L.p_V), JOLT_F32, Lw, 1, 0, s4), P.f(zc), Lw, 1, s4, 0, 0.f,
                      flags);
     gg.skip_stride = s4;
     return launch_gemm(gg, st);
@@ -387,37 +391,48 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
     // one shifted CholeskyQR pass per power step; the last step of a block
     // takes two so that Rayleigh-Ritz sees an orthonormal basis
     for (int q = 0; q < SUB_STEPS; ++q) {
-      TRY(apply_S());
-      TRY(cholqr(L, P, T, Lw, L.p_Z, L.p_V2, L.p_V, true, false, q == SUB_STEPS - 1 ? 2 : 1,
+      if (q > 0 || blk == 0) TRY(apply_S());
+      TRY(cholqr(L, P, T, Lw, zc, L.p_V2, L.p_V, true, false, q == SUB_STEPS - 1 ? 2 : 1,
                  SUB_SHIFT, st));
     }
     TRY(apply_S());
-    // H = V^T Z, split over row chunks; the Jacobi kernel sums the partials
+    // H = V^T Z, split over row chunks; the eigensolver sums the partials
     const int kc = T / L.ks;
     GemmDesc g = gd(Lw, Lw, kc, 1, P.np, L.ks,
                     opnd(P.c(L.p_V), JOLT_F32, 1, Lw, 0, s4, (long long)kc * Lw),
-                    opnd(P.c(L.p_Z), JOLT_F32, Lw, 1, 0, s4, (long long)kc * Lw), P.f(L.p_Hm),
+                    opnd(P.c(zc), JOLT_F32, Lw, 1, 0, s4, (long long)kc * Lw), P.f(L.p_Hm),
                     Lw, 1, s4, (long long)Lw * Lw, 0.f, flags);
     g.skip_stride = s4;
     TRY(launch_gemm(g, st));
-    TRY(launch_jacobi(P.f(L.p_Hm), s4, Lw, Lw, L.ks, (long long)Lw * Lw, P.np, P.f(L.p_theta), s4,
-                      P.f(L.p_Wm), s4, Lw, Lw, status, s4, flags, s4, JAC_ABS_RR, st));
+    {
+      // Cholesky + one-sided Jacobi where Lw allows it; problems it leaves
+      // unsolved (and every problem for another Lw) take the two-sided Jacobi
+      int* done = status + 2;
+      const jolt_status se = launch_sym_eig(P.c(L.p_Hm), false, s4, Lw, Lw, L.ks,
+                                            (long long)Lw * Lw, P.np, P.f(L.p_theta), s4,
+                                            P.f(L.p_Wm), s4, Lw, Lw, status, s4, done, s4, flags,
+                                            s4, JAC_ABS_RR, st);
+      if (se != JOLT_OK && se != JOLT_ERR_INVALID) return se;
+      TRY(launch_jacobi(P.f(L.p_Hm), s4, Lw, Lw, L.ks, (long long)Lw * Lw, P.np, P.f(L.p_theta),
+                        s4, P.f(L.p_Wm), s4, Lw, Lw, status, s4, se == JOLT_OK ? done : flags, s4,
+                        JAC_ABS_RR, st));
+    }
     // Ritz vectors V2 = V W and Z2 = Z W = S V2
     g = gd(T, Lw, Lw, 1, P.np, 1, opnd(P.c(L.p_V), JOLT_F32, Lw, 1, 0, s4),
            opnd(P.c(L.p_Wm), JOLT_F32, Lw, 1, 0, s4), P.f(L.p_V2), Lw, 1, s4, 0, 0.f, flags);
     g.skip_stride = s4;
     TRY(launch_gemm(g, st));
-    g = gd(T, Lw, Lw, 1, P.np, 1, opnd(P.c(L.p_Z), JOLT_F32, Lw, 1, 0, s4),
-           opnd(P.c(L.p_Wm), JOLT_F32, Lw, 1, 0, s4), P.f(L.p_Z2), Lw, 1, s4, 0, 0.f, flags);
+    g = gd(T, Lw, Lw, 1, P.np, 1, opnd(P.c(zc), JOLT_F32, Lw, 1, 0, s4),
+           opnd(P.c(L.p_Wm), JOLT_F32, Lw, 1, 0, s4), P.f(zn), Lw, 1, s4, 0, 0.f, flags);
     g.skip_stride = s4;
     TRY(launch_gemm(g, st));
     const int last = (blk == SUB_MAX_BLOCKS - 1);
-    ritz_check_kernel<<<P.np, 512, 0, st>>>(P.base, P.stride, L.p_V2, L.p_Z2, L.p_theta, L.p_UT,
+    ritz_check_kernel<<<P.np, 512, 0, st>>>(P.base, P.stride, L.p_V2, zn, L.p_theta, L.p_UT,
                                             L.p_ev, L.p_flag, L.p_status, L.p_V, T, Lw, RT, last);
     JOLT_LAUNCH_CHECK();
     if (last) break;
-    // next block starts from orth(Z2), Z2 equilibrated by the check
-    TRY(cholqr2(L, P, T, Lw, L.p_Z2, L.p_V2, L.p_V, true, false, st));
+    // the next block starts from Z2 (equilibrated by the check)
+    const size_t tmp = zc; zc = zn; zn = tmp;
     bool all = false;
     TRY(read_flags_all(L, P, st, &all));
     if (all) break;
@@ -524,8 +539,9 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     // Cholesky + one-sided Jacobi; units whose S_d is not definite (done
     // flag left clear) are solved by the two-sided Jacobi
     int* done = status + 2;
-    TRY(launch_feat_eig((const double*)(ws + L.o_Sd64), ub4 / 2, D, U, c.f(L.o_evd), ub4,
-                        c.f(L.o_Vd), ub4, D, status, ub4, done, ub4, fs));
+    TRY(launch_sym_eig(ws + L.o_Sd64, true, ub4 / 2, D, D, 1, 0, U, c.f(L.o_evd), ub4,
+                       c.f(L.o_Vd), ub4, D, D, status, ub4, done, ub4, nullptr, 0, JAC_ABS_EXACT,
+                       fs));
     TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, 1, 0, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
                       status, ub4, done, ub4, JAC_ABS_EXACT, fs));
   }

@@ -628,8 +628,9 @@ jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride,
   return JOLT_OK;
 }
 
-// Z = S V for every problem not flagged (T x 64 blocks at p_V / p_Z).
-jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st) {
+// Z = S V for every problem not flagged (T x 64 blocks at p_V / o_Z).
+jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, size_t o_Z,
+                  cudaStream_t st) {
   const int* flags = (const int*)(pbase + L.p_flag);
   const long long f_us = (long long)pstride / 4;
   dim3 g2((L.T + 31) / 32, 2, np);
@@ -651,7 +652,7 @@ jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, cudaStre
     return JOLT_ERR_CUDA;
   SvArgs a;
   a.T = L.T; a.L = 64;
-  a.Z = (float*)(pbase + L.p_Z);
+  a.Z = (float*)(pbase + o_Z);
   a.z_us = f_us;
   a.flags = flags;
   a.f_us = f_us;

@@ -125,14 +125,17 @@ jolt_status launch_chol(const float* G, long long g_bstride, int n, int nparts, 
                         long long status_bstride, const int* skip, long long skip_stride,
                         bool f64, float shift, cudaStream_t st);
 // Eigenpairs of a batch of symmetric positive-definite n x n matrices (n in
-// {32, 64, 128}; f64 input, row-major) by Cholesky + one-sided Jacobi: evals
-// descending, evecs columns (row stride ldv), signs as launch_jacobi.  done[b]
-// is set to 1 on success and left 0 where the matrix is not definite (the
-// caller then re-solves those with launch_jacobi, skip = done).
-jolt_status launch_feat_eig(const double* S64, long long s_bstride, int n, int batch,
-                            float* evals, long long e_bstride, float* evecs, long long v_bstride,
-                            int ldv, int* status, long long status_bstride, int* done,
-                            long long done_bstride, cudaStream_t st);
+// {32, 64, 128}) by Cholesky + one-sided Jacobi, same input (sum of nparts
+// partials, f64 or fp32) and outputs as launch_jacobi.  done[b] is set to 1
+// on success or when skip[b] is set, and left 0 where the matrix is not
+// definite: launch_jacobi with skip = done then solves exactly those.
+// Returns JOLT_ERR_INVALID for another n (nothing launched).
+jolt_status launch_sym_eig(const void* G, bool f64_in, long long g_bstride, int lda, int n,
+                           int nparts, long long part_s, int batch, float* evals,
+                           long long e_bstride, float* evecs, long long v_bstride, int ldv,
+                           int ncols_out, int* status, long long status_bstride, int* done,
+                           long long done_bstride, const int* skip, long long skip_stride,
+                           float abs_tol, cudaStream_t st);
 // The same Cholesky (fp32, n in {32, 40, 48, 64}) writing R^{-1} instead of R.
 jolt_status launch_chol_inv(const float* G, long long g_bstride, int n, int nparts,
                             long long part_s, int batch, float* Rinv, long long r_bstride,
@@ -152,8 +155,9 @@ jolt_status gram_feat_tc(const Layout& L, int n_units, const void* X, char* ws, 
 bool sv_tc_supported(const Layout& L);
 // p_STs = tf32 low part of p_ST for np problems.
 jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st);
-// p_Z = p_ST p_V for every problem whose p_flag is zero.
-jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st);
+// (o_Z) = p_ST p_V for every problem whose p_flag is zero.
+jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, size_t o_Z,
+                  cudaStream_t st);
 bool ygram_tc_supported(const Layout& L);
 // Yt (unit region) = Y relaid [T][RD * H] and its tf32 low part.
 jolt_status ytrans(const Layout& L, int n_units, char* ws, cudaStream_t st);
