@@ -471,10 +471,22 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
   const int t = threadIdx.x, lane = t & 31, tx = t & 31, ty = t >> 5;
   const float* Gg = G + u * g_bs;
   if (t == 0) bad = 0;
-  for (int e = t; e < N * N; e += NT) {
-    float v = Gg[e];
-    for (int p = 1; p < nparts; ++p) v += Gg[p * part_s + e];
-    X[(e / N) * LD + e % N] = v;   // raw Gram, staged in X
+  {
+    // every load of the (up to 4) partials in flight at once
+    constexpr int PER = (N * N + NT - 1) / NT;
+    float g[4][PER];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int e = t + i * NT;
+        g[p][i] = (p < nparts && e < N * N) ? Gg[p * part_s + e] : 0.f;
+      }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = t + i * NT;
+      if (e < N * N) X[(e / N) * LD + e % N] = (g[0][i] + g[1][i]) + (g[2][i] + g[3][i]);  // raw Gram, staged in X
+    }
   }
   __syncthreads();
   if (t < N) {
@@ -644,6 +656,11 @@ __device__ __forceinline__ void st_rows(float* col, int l, const float (&v)[RPT]
 // of this part is far slower than fp32, and this factorisation needs more
 // than fp32 accuracy.
 struct df { float h, l; };
+__device__ __forceinline__ void two_sum_f(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
 __device__ __forceinline__ df df_norm(float s, float e) {
   const float h = s + e;
   return df{h, e - (h - s)};
@@ -716,16 +733,42 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
   }
   if (t == 0) done[u * d_bs] = 0;
   const TIn* Gg = G + u * g_bs;
-  auto sval = [&](int i, int j) -> double {  // symmetrised sum of the partials
-    double v = 0.0;
-    for (int p = 0; p < nparts; ++p)
-      v += (double)Gg[p * part_s + (long long)i * lda + j] + (double)Gg[p * part_s + (long long)j * lda + i];
-    return 0.5 * v;
-  };
   if (t == 0) fail = 0;
+  // stage sum_p G_p (not yet symmetrised) in A as double-floats; each
+  // thread's loads of all partials are in flight together
+  constexpr int PER = (N * N + NT - 1) / NT;
+  constexpr int CH = PER < 8 ? PER : 8;     // elements per chunk
+#pragma unroll 1
+  for (int c0 = 0; c0 < PER; c0 += CH) {
+    double g[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) g[i] = 0.0;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      if (p >= nparts) break;
+      TIn v[CH];
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int e = t + (c0 + i) * NT;
+        v[i] = e < N * N ? Gg[p * part_s + (long long)(e / N) * lda + e % N] : (TIn)0;
+      }
+#pragma unroll
+      for (int i = 0; i < CH; ++i) g[i] += (double)v[i];
+    }
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int e = t + (c0 + i) * NT;
+      if (e < N * N) {
+        const float h = (float)g[i];
+        A[(e / N) * LDA + e % N] = df{h, (float)(g[i] - (double)h)};
+      }
+    }
+  }
+  __syncthreads();
   // s_i = sqrt(S_ii) and 1 / s_i (f64, N values), Frobenius norm of S
   if (t < N) {
-    const double d = sval(t, t);
+    const df a = A[t * LDA + t];
+    const double d = (double)a.h + (double)a.l;
     const double sd = d > 0.0 ? sqrt(d) : 0.0;
     const double r = sd > 0.0 ? 1.0 / sd : 0.0;
     const float sh = (float)sd, rh = (float)r;
@@ -736,7 +779,7 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
   }
   float fro = 0.f;
   for (int e = t; e < N * N; e += NT) {
-    const float v = (float)sval(e / N, e % N);
+    const float v = A[(e / N) * LDA + e % N].h;
     fro = fmaf(v, v, fro);
   }
   fro = warp_sum(fro);
@@ -745,13 +788,15 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
   float fro_s = 0.f;
   for (int i = 0; i < NT / 32; ++i) fro_s += fro_part[i];
   const float floor_abs = abs_tol * sqrtf(fro_s);
-  // S'_ij = S_ij / (s_i s_j), lower triangle, double-float
+  // S'_ij = (S_ij + S_ji) / (2 s_i s_j), lower triangle, double-float (the
+  // upper triangle is only read)
   for (int e = t; e < N * N; e += NT) {
     const int i = e / N, j = e % N;
     if (j <= i) {
-      const double x = sval(i, j);
-      const float xh = (float)x;
-      const df v{xh, (float)(x - (double)xh)};
+      const df x = A[i * LDA + j], y = A[j * LDA + i];
+      float sh, se;
+      two_sum_f(x.h, y.h, sh, se);
+      const df v = df_norm(0.5f * sh, 0.5f * (se + x.l + y.l));
       A[i * LDA + j] = df_mul(df_mul(v, df{M[i], M[N + i]}), df{M[j], M[N + j]});
     }
   }
@@ -812,9 +857,12 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
         g += __shfl_xor_sync(0xffffffffu, g, o);
       }
       if (fabsf(g) > tol * sqrtf(a * b) && fabsf(g) > floor_abs) {
-        const float zeta = (b - a) / (2.f * g);
-        const float tt = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
-        const float c = rsqrtf(1.f + tt * tt), s = tt * c;
+        // rotation parameters with the approximate (few-ulp) intrinsics: an
+        // angle off by an ulp only leaves a residue for the next sweep, and
+        // the column transform stays orthogonal to rounding
+        const float zeta = __fdividef(b - a, 2.f * g);
+        const float tt = __fdividef(copysignf(1.f, zeta), fabsf(zeta) + __fsqrt_rn(fmaf(zeta, zeta, 1.f)));
+        const float c = rsqrtf(fmaf(tt, tt, 1.f)), s = tt * c;
         float np_[RPT], nq_[RPT];
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
@@ -860,7 +908,10 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
     for (int r = 0; r < N; ++r) vg[(long long)r * ldv + rank] = sgn * inv * M[c * LDM + r];
   }
   if (t == 0) {
-    if (!converged && status) atomicOr(status + u * st_bs, ST_NOCONVERGE);
+    if (status) {
+      if (!converged) atomicOr(status + u * st_bs, ST_NOCONVERGE);
+      atomicMax(status + u * st_bs + 1, sweep);   // diagnostics: most sweeps used
+    }
     done[u * d_bs] = 1;
   }
 }
@@ -977,6 +1028,7 @@ jolt_status launch_chol_inv(const float* G, long long g_bs, int n, int nparts, l
                             const int* skip, long long sk_s, float shift, cudaStream_t st) {
   if (n <= 0 || batch <= 0) return JOLT_OK;
   nparts = nparts < 1 ? 1 : nparts;
+  if (nparts > 4) return JOLT_ERR_INVALID;
   switch (n) {
     case 64: chol_inv_kernel<64><<<batch, 256, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
     case 48: chol_inv_kernel<48><<<batch, 256, 0, st>>>(G, g_bs, nparts, part_s, Rinv, r_bs, status, s_bs, skip, sk_s, shift); break;
