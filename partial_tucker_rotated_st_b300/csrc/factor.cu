@@ -23,6 +23,8 @@
 //   factors and cores rounded to fp16 (the storage type).
 #include "jolt_internal.cuh"
 
+#include <string.h>
+
 #include <mutex>
 #include <vector>
 
@@ -208,6 +210,86 @@ __global__ void scatter_problems_kernel(char* ws, size_t ub, size_t o_UT, size_t
       const int sv = *(const int*)(pr + p_status);
       if (sv) atomicOr((int*)(un + o_status), sv);
     }
+  }
+}
+
+// Cores G(r_d)[h] = U_T(r_d)^T B_h[:, :n] for a set of feature ranks that
+// share the same B (Y for the truncated ranks, X for the whole-feature one),
+// one CTA per (head, unit).  B's rows and every rank's U_T rows are staged in
+// shared memory 32 tokens at a time and reused by all ranks of the set; each
+// thread owns one 4 x 4 tile of one core (r0..r0+3 x c0..c0+3), so the
+// products of all ranks cost one pass over B.
+constexpr int CO_THREADS = 256, CO_TK = 32;
+struct CoreArgs {
+  const void* B;            // unit u, head h at B + u * b_us + h * b_hs (elements), row stride ldb
+  long long b_us, b_hs;
+  int ldb, btype;           // 0 fp32, 1 bf16, 2 fp16 (btype must match TB)
+  int nset;                 // ranks in the set
+  int id[JOLT_MAX_GRID];    // their indices (U_T at o_UT + id * T * RT, core at o_G + id * H * RT * D)
+  int n[JOLT_MAX_GRID];     // their column counts (r_d)
+  int nmax;                 // max n, a multiple of 4
+  int T, RT, H, D;
+  char* ws;
+  size_t ub, o_UT, o_G;
+};
+
+template <typename TB>
+__global__ void __launch_bounds__(CO_THREADS) cores_kernel(CoreArgs a) {
+  extern __shared__ __align__(16) float co_sm[];
+  const int h = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
+  const int RT = a.RT;
+  float* Bs = co_sm;                             // [CO_TK][nmax]
+  float* Us = Bs + CO_TK * a.nmax;               // [nset][CO_TK][RT]
+  // this thread's tile: walk the ranks' tile counts (RT/4 x n/4 each)
+  int sel = -1, r0 = 0, c0 = 0, acc_t = t;
+  for (int s = 0; s < a.nset; ++s) {
+    const int tiles = (RT / 4) * (a.n[s] / 4);
+    if (sel < 0 && acc_t < tiles) { sel = s; r0 = (acc_t / (a.n[s] / 4)) * 4; c0 = (acc_t % (a.n[s] / 4)) * 4; }
+    else if (sel < 0) acc_t -= tiles;
+  }
+  char* base = a.ws + (size_t)u * a.ub;
+  const TB* Bh = (const TB*)a.B + u * a.b_us + h * a.b_hs;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = 0; k0 < a.T; k0 += CO_TK) {
+    const int kn = min(CO_TK, a.T - k0);
+    __syncthreads();
+    for (int e = t; e < CO_TK * a.nmax; e += CO_THREADS) {
+      const int k = e / a.nmax, c = e % a.nmax;
+      Bs[e] = k < kn ? to_f32(Bh[(long long)(k0 + k) * a.ldb + c]) : 0.f;
+    }
+    for (int s = 0; s < a.nset; ++s) {
+      const float* Ug = (const float*)(base + a.o_UT) + (size_t)a.id[s] * a.T * RT;
+      float* Ud = Us + s * CO_TK * RT;
+      for (int e = t; e < CO_TK * RT; e += CO_THREADS) {
+        const int k = e / RT;
+        Ud[e] = k < kn ? Ug[(long long)k0 * RT + e] : 0.f;
+      }
+    }
+    __syncthreads();
+    if (sel >= 0) {
+      const float* Ud = Us + sel * CO_TK * RT;
+#pragma unroll 8
+      for (int k = 0; k < CO_TK; ++k) {
+        const float4 uv = *reinterpret_cast<const float4*>(Ud + k * RT + r0);
+        const float4 bv = *reinterpret_cast<const float4*>(Bs + k * a.nmax + c0);
+        const float ur[4] = {uv.x, uv.y, uv.z, uv.w}, bc[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ur[i], bc[j], acc[i][j]);
+      }
+    }
+  }
+  if (sel >= 0) {
+    const int n = a.n[sel];
+    float* G = (float*)(base + a.o_G) + (size_t)a.id[sel] * a.H * RT * a.D + (size_t)h * RT * n;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      *reinterpret_cast<float4*>(G + (r0 + i) * n + c0) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
   }
 }
 
@@ -634,21 +716,61 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       ws, ub, L.o_UT32, L.o_tokev, L.o_status, preg, pb, L.p_UT, L.p_ev, 1, L.p_status, U, ndt, T,
       RT);
   JOLT_LAUNCH_CHECK();
-  // cores G(r_d)[h] = U_T^T A_h  (RT x rdv)
+  // cores G(r_d)[h] = U_T^T A_h  (RT x rdv): the truncated ranks share one
+  // pass over Y, the whole-feature rank reads X
+  for (int pass = 0; pass < 2; ++pass) {
+    CoreArgs ca;
+    memset(&ca, 0, sizeof(ca));
+    int tiles = 0;
+    bool fits = (RT % 4) == 0;
+    for (int id = 0; id < L.nd; ++id) {
+      const bool full = (L.rd[id] == D);
+      if (full != (pass == 1)) continue;
+      ca.id[ca.nset] = id;
+      ca.n[ca.nset] = L.rd[id];
+      ca.nmax = ca.nmax > L.rd[id] ? ca.nmax : L.rd[id];
+      fits = fits && (L.rd[id] % 4 == 0);
+      tiles += (RT / 4) * (L.rd[id] / 4);
+      ++ca.nset;
+    }
+    if (ca.nset == 0) continue;
+    fits = fits && tiles <= CO_THREADS;
+    if (fits) {
+      ca.T = T; ca.RT = RT; ca.H = H; ca.D = D;
+      ca.ws = ws; ca.ub = ub; ca.o_UT = L.o_UT32; ca.o_G = L.o_G32;
+      const size_t smem = ((size_t)CO_TK * ca.nmax + (size_t)ca.nset * CO_TK * RT) * 4;
+      const dim3 grid(H, U);
+      if (pass == 0) {
+        ca.B = ws + L.o_Y; ca.b_us = ub4; ca.b_hs = (long long)T * RD; ca.ldb = RD;
+        cores_kernel<float><<<grid, CO_THREADS, smem, st>>>(ca);
+      } else {
+        ca.B = X; ca.b_us = xu; ca.b_hs = (long long)T * D; ca.ldb = D;
+        if (xdt == JOLT_BF16) cores_kernel<__nv_bfloat16><<<grid, CO_THREADS, smem, st>>>(ca);
+        else if (xdt == JOLT_F16) cores_kernel<__half><<<grid, CO_THREADS, smem, st>>>(ca);
+        else cores_kernel<float><<<grid, CO_THREADS, smem, st>>>(ca);
+      }
+      JOLT_LAUNCH_CHECK();
+    } else {
+      for (int s = 0; s < ca.nset; ++s) {
+        const int id = ca.id[s], rdv = L.rd[id];
+        const bool full = (rdv == D);
+        const void* Ab = full ? X : (const void*)(ws + L.o_Y);
+        const int adt = full ? xdt : JOLT_F32;
+        const long long as_t = full ? D : RD;
+        const long long aseg = full ? (long long)T * D : (long long)T * RD;
+        const long long aub = full ? xu : ub4;
+        const size_t oUT = L.o_UT32 + (size_t)id * T * RT * 4;
+        const size_t oG = L.o_G32 + (size_t)id * H * RT * D * 4;
+        TRY(launch_gemm(gd(RT, rdv, T, 1, U, H, opnd(ws + oUT, JOLT_F32, 1, RT, 0, ub4),
+                           opnd(Ab, adt, as_t, 1, 0, aub, aseg), c.f(oG), rdv, 1, ub4,
+                           (long long)RT * rdv),
+                        st));
+      }
+    }
+  }
   for (int id = 0; id < L.nd; ++id) {
     const int rdv = L.rd[id];
-    const bool full = (rdv == D);
-    const void* Ab = full ? X : (const void*)(ws + L.o_Y);
-    const int adt = full ? xdt : JOLT_F32;
-    const long long as_t = full ? D : RD;
-    const long long aseg = full ? (long long)T * D : (long long)T * RD;
-    const long long aub = full ? xu : ub4;
-    const size_t oUT = L.o_UT32 + (size_t)id * T * RT * 4;
     const size_t oG = L.o_G32 + (size_t)id * H * RT * D * 4;
-    TRY(launch_gemm(gd(RT, rdv, T, 1, U, H, opnd(ws + oUT, JOLT_F32, 1, RT, 0, ub4),
-                       opnd(Ab, adt, as_t, 1, 0, aub, aseg), c.f(oG), rdv, 1, ub4,
-                       (long long)RT * rdv),
-                    st));
     round_f16_kernel<<<dim3(blocks_for((long long)H * RT * rdv), 1, U), 256, 0, st>>>(
         ws, ub, oG, rdv, L.o_G16 + (size_t)id * H * RT * D * 2, rdv, H * RT, rdv, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
