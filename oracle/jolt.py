@@ -458,6 +458,82 @@ def allocate(dist: np.ndarray, cost: np.ndarray, budget: int, align: int = 256,
     return zhi, hi, ALLOC_OK
 
 
+def refine_greedy(dist: np.ndarray, cost: np.ndarray, budget: int, choice: np.ndarray):
+    """Greedy improvement of a feasible allocation
+    ["Joint Tucker-rank and residual-bit KV allocator", Implementation notes:
+    after the bisection, optionally improve the result by swapping candidates
+    with the best distortion reduction per added byte].
+
+    Reading: a swap replaces one unit's candidate z by z' with
+    C(z') > C(z), D(z') < D(z) and C(z') - C(z) <= the remaining slack
+    B - sum C; its rate is (D(z) - D(z')) / (C(z') - C(z)) in f64.  Each
+    round applies the swap of highest rate over all units (ties: smaller
+    added bytes, then lower unit, then lower candidate index), until no swap
+    fits.  Returns (choice, number of swaps)."""
+    dist = np.asarray(dist, dtype=np.float64)
+    cost = np.asarray(cost, dtype=np.int64)
+    z = np.array(choice, dtype=np.int64).copy()
+    U, nc = dist.shape
+    slack = int(budget) - total_cost(cost, z)
+    swaps = 0
+    while True:
+        best = None  # (rate, dc, u, c)
+        for u in range(U):
+            d0, c0 = dist[u, z[u]], int(cost[u, z[u]])
+            for c in range(nc):
+                dc = int(cost[u, c]) - c0
+                dd = d0 - dist[u, c]
+                if dc <= 0 or dd <= 0.0 or dc > slack:
+                    continue
+                rate = dd / float(dc)
+                key = (-rate, dc, u, c)
+                if best is None or key < best:
+                    best = key
+        if best is None:
+            return z, swaps
+        _, dc, u, c = best
+        z[u] = c
+        slack -= dc
+        swaps += 1
+
+
+def allocate_uniform(dist: np.ndarray, cost: np.ndarray, budget: int, cand: Sequence[int]):
+    """The baseline allocators of the toy comparison ["Joint Tucker-rank and
+    residual-bit KV allocator", Verification, Stage 1: a fixed 4-bit
+    allocation, every group on the same (r_T, r_d, b)].  Every unit takes the
+    same candidate, chosen among `cand` (flat indices) as the one of least
+    total distortion whose total cost fits the budget (ties: lower index).
+    Returns (choice, status); with no candidate fitting, every unit takes the
+    cheapest of `cand` by total cost (ties: lower index) and the status is
+    INFEASIBLE."""
+    dist = np.asarray(dist, dtype=np.float64)
+    cost = np.asarray(cost, dtype=np.int64)
+    U = dist.shape[0]
+    best, cheapest = None, None
+    for c in cand:
+        tc = int(cost[:, c].sum())
+        td = 0.0
+        for u in range(U):
+            td += dist[u, c]
+        if cheapest is None or (tc, c) < cheapest:
+            cheapest = (tc, c)
+        if tc <= budget and (best is None or (td, c) < best):
+            best = (td, c)
+    if best is None:
+        return np.full(U, cheapest[1], dtype=np.int64), ALLOC_INFEASIBLE
+    return np.full(U, best[1], dtype=np.int64), ALLOC_OK
+
+
+def fixed_bit_candidates(nT: int, nd: int, nb: int, ib: int):
+    """Flat indices (iT * nd + id) * nb + ib of every rank pair at bit index ib."""
+    return [(iT * nd + id_) * nb + ib for iT in range(nT) for id_ in range(nd)]
+
+
+def fixed_rank_candidates(nT: int, nd: int, nb: int, iT: int, id_: int):
+    """Flat indices of every bit width at the rank pair (iT, id)."""
+    return [(iT * nd + id_) * nb + ib for ib in range(nb)]
+
+
 # --------------------------------------------------------------------------
 # encode / decode of the chosen candidate  [P4 Implementation notes]
 # --------------------------------------------------------------------------

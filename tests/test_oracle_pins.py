@@ -371,3 +371,53 @@ def test_fix_signs_rule():
     assert np.array_equal(F, np.array([[-0.6, 0.8, 0.0], [0.8, 0.6, 0.5], [0.0, 0.0, -0.5]]))
     w, V2 = jolt.feature_mode(_small_tensor()[0])
     assert np.all(V2[np.argmax(np.abs(V2), 0), np.arange(V2.shape[1])] > 0)
+
+
+def test_refine_greedy_hand_case():
+    # unit 0 can buy 0.5 of distortion for 100 bytes (rate 0.005), unit 1
+    # 0.3 for 50 bytes (rate 0.006): with 120 bytes of slack only unit 1's
+    # swap is taken first, and then unit 0's no longer fits
+    dist = np.array([[1.0, 0.5], [0.9, 0.6]])
+    cost = np.array([[100, 200], [100, 150]])
+    z, n = jolt.refine_greedy(dist, cost, 320, np.array([0, 0]))
+    assert list(z) == [0, 1] and n == 1
+    # with 150 bytes of slack both swaps fit, the higher rate first
+    z, n = jolt.refine_greedy(dist, cost, 350, np.array([0, 0]))
+    assert list(z) == [1, 1] and n == 2
+    # a swap that adds bytes but no distortion reduction is never taken
+    dist2 = np.array([[0.5, 0.5]])
+    cost2 = np.array([[100, 101]])
+    z, n = jolt.refine_greedy(dist2, cost2, 10 ** 6, np.array([0]))
+    assert list(z) == [0] and n == 0
+
+
+def test_refine_greedy_properties():
+    """Checked by enumeration: the result keeps the budget, never raises the
+    total distortion, and at the end no single swap that adds bytes and
+    lowers a unit's distortion still fits in the slack."""
+    rng = np.random.default_rng(7)
+    for trial in range(5):
+        dist = rng.random((5, 12))
+        cost = rng.integers(50, 400, (5, 12))
+        z0 = np.argmin(cost, axis=1)
+        budget = int(cost[np.arange(5), z0].sum()) + int(rng.integers(0, 900))
+        z, n = jolt.refine_greedy(dist, cost, budget, z0)
+        assert jolt.total_cost(cost, z) <= budget
+        assert dist[np.arange(5), z].sum() <= dist[np.arange(5), z0].sum()
+        slack = budget - jolt.total_cost(cost, z)
+        for u in range(5):
+            for c in range(12):
+                dc = cost[u, c] - cost[u, z[u]]
+                assert not (0 < dc <= slack and dist[u, c] < dist[u, z[u]])
+
+
+def test_allocate_uniform_hand_case():
+    # three candidates shared by two units: 1 is the best that fits
+    dist = np.array([[0.1, 0.3, 0.9], [0.2, 0.2, 0.8]])
+    cost = np.array([[500, 200, 50], [500, 250, 60]])
+    z, st = jolt.allocate_uniform(dist, cost, 460, [0, 1, 2])
+    assert st == jolt.ALLOC_OK and list(z) == [1, 1]
+    z, st = jolt.allocate_uniform(dist, cost, 100, [0, 1, 2])
+    assert st == jolt.ALLOC_INFEASIBLE and list(z) == [2, 2]
+    assert jolt.fixed_bit_candidates(2, 3, 4, 2) == [2, 6, 10, 14, 18, 22]
+    assert jolt.fixed_rank_candidates(2, 3, 4, 1, 2) == [20, 21, 22, 23]
