@@ -215,74 +215,114 @@ __global__ void scatter_problems_kernel(char* ws, size_t ub, size_t o_UT, size_t
 
 // Cores G(r_d)[h] = U_T(r_d)^T B_h[:, :n] for a set of feature ranks that
 // share the same B (Y for the truncated ranks, X for the whole-feature one),
-// one CTA per (head, unit).  B's rows and every rank's U_T rows are staged in
-// shared memory 32 tokens at a time and reused by all ranks of the set; each
-// thread owns one 4 x 4 tile of one core (r0..r0+3 x c0..c0+3), so the
-// products of all ranks cost one pass over B.
+// one CTA per (head, unit).  B's rows and every rank's U_T rows are copied
+// to shared memory 32 tokens at a time by cp.async, two stages deep, and
+// reused by all ranks of the set; each thread owns one 4 x 4 tile of one
+// core (r0..r0+3 x c0..c0+3), so the products of all ranks cost one pass
+// over B.  Global rows must be 16-byte aligned (checked by the caller).
 constexpr int CO_THREADS = 256, CO_TK = 32;
 struct CoreArgs {
   const void* B;            // unit u, head h at B + u * b_us + h * b_hs (elements), row stride ldb
   long long b_us, b_hs;
-  int ldb, btype;           // 0 fp32, 1 bf16, 2 fp16 (btype must match TB)
+  int ldb;
   int nset;                 // ranks in the set
   int id[JOLT_MAX_GRID];    // their indices (U_T at o_UT + id * T * RT, core at o_G + id * H * RT * D)
   int n[JOLT_MAX_GRID];     // their column counts (r_d)
-  int nmax;                 // max n, a multiple of 4
+  int nmax;                 // max n, a multiple of 8
   int T, RT, H, D;
   char* ws;
   size_t ub, o_UT, o_G;
 };
 
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc, bool valid) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(sdst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gsrc),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+template <typename T16>
+__device__ __forceinline__ void load4(const T16* p, float (&v)[4]) {
+  const uint2 x = *reinterpret_cast<const uint2*>(p);
+  const T16* h = reinterpret_cast<const T16*>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = to_f32(h[i]);
+}
+
 template <typename TB>
 __global__ void __launch_bounds__(CO_THREADS) cores_kernel(CoreArgs a) {
-  extern __shared__ __align__(16) float co_sm[];
+  extern __shared__ __align__(16) unsigned char co_sm[];
   const int h = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
   const int RT = a.RT;
-  float* Bs = co_sm;                             // [CO_TK][nmax]
-  float* Us = Bs + CO_TK * a.nmax;               // [nset][CO_TK][RT]
+  const size_t b_bytes = (size_t)CO_TK * a.nmax * sizeof(TB);
+  const size_t stage_bytes = b_bytes + (size_t)a.nset * CO_TK * RT * 4;
   // this thread's tile: walk the ranks' tile counts (RT/4 x n/4 each)
-  int sel = -1, r0 = 0, c0 = 0, acc_t = t;
+  int sel = -1, r0 = 0, c0 = 0, rem = t;
   for (int s = 0; s < a.nset; ++s) {
     const int tiles = (RT / 4) * (a.n[s] / 4);
-    if (sel < 0 && acc_t < tiles) { sel = s; r0 = (acc_t / (a.n[s] / 4)) * 4; c0 = (acc_t % (a.n[s] / 4)) * 4; }
-    else if (sel < 0) acc_t -= tiles;
+    if (sel < 0 && rem < tiles) { sel = s; r0 = (rem / (a.n[s] / 4)) * 4; c0 = (rem % (a.n[s] / 4)) * 4; }
+    else if (sel < 0) rem -= tiles;
   }
   char* base = a.ws + (size_t)u * a.ub;
   const TB* Bh = (const TB*)a.B + u * a.b_us + h * a.b_hs;
+  auto issue = [&](int k0, int stg) {
+    unsigned char* sb = co_sm + stg * stage_bytes;
+    const int segs = (int)(a.nmax * sizeof(TB) / 16);   // 16-byte pieces per B row
+    for (int e = t; e < CO_TK * segs; e += CO_THREADS) {
+      const int k = e / segs, sg = e % segs;
+      const bool ok = k0 + k < a.T;
+      const TB* src = Bh + (long long)(ok ? k0 + k : 0) * a.ldb;
+      cp_async16(sb + (size_t)k * a.nmax * sizeof(TB) + sg * 16,
+                 reinterpret_cast<const unsigned char*>(src) + sg * 16, ok);
+    }
+    for (int s = 0; s < a.nset; ++s) {
+      const float* Ug = (const float*)(base + a.o_UT) + (size_t)a.id[s] * a.T * RT;
+      unsigned char* su = sb + b_bytes + (size_t)s * CO_TK * RT * 4;
+      for (int e = t; e < CO_TK * RT / 4; e += CO_THREADS) {
+        const int k = (4 * e) / RT;
+        const bool ok = k0 + k < a.T;
+        cp_async16(su + (size_t)e * 16, Ug + (ok ? (long long)k0 * RT + 4 * e : 0), ok);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
   float acc[4][4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  issue(0, 0);
+  int stg = 0;
   for (int k0 = 0; k0 < a.T; k0 += CO_TK) {
-    const int kn = min(CO_TK, a.T - k0);
-    __syncthreads();
-    for (int e = t; e < CO_TK * a.nmax; e += CO_THREADS) {
-      const int k = e / a.nmax, c = e % a.nmax;
-      Bs[e] = k < kn ? to_f32(Bh[(long long)(k0 + k) * a.ldb + c]) : 0.f;
-    }
-    for (int s = 0; s < a.nset; ++s) {
-      const float* Ug = (const float*)(base + a.o_UT) + (size_t)a.id[s] * a.T * RT;
-      float* Ud = Us + s * CO_TK * RT;
-      for (int e = t; e < CO_TK * RT; e += CO_THREADS) {
-        const int k = e / RT;
-        Ud[e] = k < kn ? Ug[(long long)k0 * RT + e] : 0.f;
-      }
+    const bool more = k0 + CO_TK < a.T;
+    if (more) {
+      issue(k0 + CO_TK, stg ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
     }
     __syncthreads();
     if (sel >= 0) {
-      const float* Ud = Us + sel * CO_TK * RT;
+      const unsigned char* sb = co_sm + stg * stage_bytes;
+      const TB* bs = reinterpret_cast<const TB*>(sb);
+      const float* us = reinterpret_cast<const float*>(sb + b_bytes) + sel * CO_TK * RT;
 #pragma unroll 8
       for (int k = 0; k < CO_TK; ++k) {
-        const float4 uv = *reinterpret_cast<const float4*>(Ud + k * RT + r0);
-        const float4 bv = *reinterpret_cast<const float4*>(Bs + k * a.nmax + c0);
-        const float ur[4] = {uv.x, uv.y, uv.z, uv.w}, bc[4] = {bv.x, bv.y, bv.z, bv.w};
+        float ur[4], bc[4];
+        load4(us + k * RT + r0, ur);
+        load4(bs + k * a.nmax + c0, bc);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ur[i], bc[j], acc[i][j]);
       }
     }
+    __syncthreads();   // this stage is refilled next
+    stg ^= 1;
   }
   if (sel >= 0) {
     const int n = a.n[sel];
@@ -734,11 +774,17 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       ++ca.nset;
     }
     if (ca.nset == 0) continue;
-    fits = fits && tiles <= CO_THREADS;
+    const size_t xel = pass == 1 ? (xdt == JOLT_F32 ? 4 : 2) : 4;
+    fits = fits && tiles <= CO_THREADS && ca.nmax % 8 == 0 && RT % 4 == 0 &&
+           (pass == 0 || ((uintptr_t)X % 16 == 0 && (D * xel) % 16 == 0));
     if (fits) {
       ca.T = T; ca.RT = RT; ca.H = H; ca.D = D;
       ca.ws = ws; ca.ub = ub; ca.o_UT = L.o_UT32; ca.o_G = L.o_G32;
-      const size_t smem = ((size_t)CO_TK * ca.nmax + (size_t)ca.nset * CO_TK * RT) * 4;
+      const size_t smem = 2 * ((size_t)CO_TK * ca.nmax * xel + (size_t)ca.nset * CO_TK * RT * 4);
+      if (smem > 48 * 1024) fits = false;
+    }
+    if (fits) {
+      const size_t smem = 2 * ((size_t)CO_TK * ca.nmax * xel + (size_t)ca.nset * CO_TK * RT * 4);
       const dim3 grid(H, U);
       if (pass == 0) {
         ca.B = ws + L.o_Y; ca.b_us = ub4; ca.b_hs = (long long)T * RD; ca.ldb = RD;

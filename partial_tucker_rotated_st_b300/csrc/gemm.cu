@@ -20,8 +20,10 @@ __global__ void __launch_bounds__(NT) gemm_kernel(GemmDesc g) {
   const TA* A = (const TA*)g.A.p + b1 * g.A.sb1 + b2 * g.A.sb2;
   const TB* B = (const TB*)g.B.p + b1 * g.B.sb1 + b2 * g.B.sb2;
 
-  __shared__ __align__(16) float As[BK][BM + 4];
-  __shared__ __align__(16) float Bs[BK][BN + 4];
+  // two stages: the next tile's global loads are in flight (in registers)
+  // while the current tile is multiplied
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
 
   const int t = threadIdx.x;
   const int tx = t % 16, ty = t / 16;
@@ -36,7 +38,8 @@ __global__ void __launch_bounds__(NT) gemm_kernel(GemmDesc g) {
 
   const int ktiles = (g.K + BK - 1) / BK;
   const int total = ktiles * g.nseg;
-  for (int it = 0; it < total; ++it) {
+  float ra[4], rb[4];
+  auto load = [&](int it) {
     const int s = it / ktiles;
     const int k0 = (it % ktiles) * BK;
     const TA* As_g = A + s * g.A.sseg;
@@ -47,9 +50,7 @@ __global__ void __launch_bounds__(NT) gemm_kernel(GemmDesc g) {
       int m, k;
       if (a_kfast) { m = e / BK; k = e % BK; } else { m = e % BM; k = e / BM; }
       const int gm = m0 + m, gk = k0 + k;
-      float v = 0.f;
-      if (gm < g.M && gk < g.K) v = to_f32(As_g[gm * g.A.s0 + gk * g.A.s1]);
-      As[k][m] = v;
+      ra[i] = (gm < g.M && gk < g.K) ? to_f32(As_g[gm * g.A.s0 + gk * g.A.s1]) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -57,15 +58,35 @@ __global__ void __launch_bounds__(NT) gemm_kernel(GemmDesc g) {
       int k, n;
       if (b_nfast) { k = e / BN; n = e % BN; } else { n = e / BK; k = e % BK; }
       const int gk = k0 + k, gn = n0 + n;
-      float v = 0.f;
-      if (gk < g.K && gn < g.N) v = to_f32(Bs_g[gk * g.B.s0 + gn * g.B.s1]);
-      Bs[k][n] = v;
+      rb[i] = (gk < g.K && gn < g.N) ? to_f32(Bs_g[gk * g.B.s0 + gn * g.B.s1]) : 0.f;
     }
-    __syncthreads();
+  };
+  auto store = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = t + i * NT;
+      int m, k;
+      if (a_kfast) { m = e / BK; k = e % BK; } else { m = e % BM; k = e / BM; }
+      As[buf][k][m] = ra[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = t + i * NT;
+      int k, n;
+      if (b_nfast) { k = e / BN; n = e % BN; } else { n = e / BK; k = e % BK; }
+      Bs[buf][k][n] = rb[i];
+    }
+  };
+  load(0);
+  store(0);
+  __syncthreads();
+  for (int it = 0; it < total; ++it) {
+    const int buf = it & 1;
+    if (it + 1 < total) load(it + 1);
 #pragma unroll
     for (int k = 0; k < BK; ++k) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[k][ty * 4]);
-      const float4 bb = *reinterpret_cast<const float4*>(&Bs[k][tx * 4]);
+      const float4 a = *reinterpret_cast<const float4*>(&As[buf][k][ty * 4]);
+      const float4 bb = *reinterpret_cast<const float4*>(&Bs[buf][k][tx * 4]);
       const float av[4] = {a.x, a.y, a.z, a.w};
       const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
 #pragma unroll
@@ -73,6 +94,7 @@ __global__ void __launch_bounds__(NT) gemm_kernel(GemmDesc g) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
+    if (it + 1 < total) store(buf ^ 1);
     __syncthreads();
   }
 
