@@ -66,6 +66,7 @@ typedef enum {
 /* Grid sentinel: keep a mode untruncated (r_T = T or r_d = D). */
 #define JOLT_FULL (-1)
 #define JOLT_MAX_GRID 8
+#define JOLT_MAX_CAND (JOLT_MAX_GRID * JOLT_MAX_GRID * 4)   /* largest candidate grid */
 #define JOLT_HEADER_BYTES 256
 
 /*
@@ -163,6 +164,51 @@ jolt_status jolt_sweep_candidates(const jolt_config* cfg, int n_units, const voi
 jolt_status jolt_allocate(int n_units, int n_cand, const double* dist, const int64_t* cost,
                           int64_t budget, int align, int32_t* choice, double* lambda,
                           int32_t* status, void* stream);
+
+/*
+ * Greedy improvement of a feasible allocation, run after jolt_allocate
+ * [P1 Implementation notes: after the bisection, optionally improve the
+ * result by swapping candidates with the best distortion reduction per added
+ * byte].  A swap replaces unit u's candidate z by c when it adds
+ * dc = cost[u][c] - cost[u][z] bytes with 0 < dc <= the slack
+ * (budget - total cost) and lowers the unit's distortion by
+ * dd = dist[u][z] - dist[u][c] > 0; its rate is dd / dc (f64, correctly
+ * rounded).  Each round applies the swap of highest rate (ties: smaller dc,
+ * then lower unit, then lower candidate index) until none fits.
+ *   dist, cost as for jolt_allocate; choice [n_units] int32 (device), read
+ *   and rewritten in place (it must fit the budget); n_swaps [1] int32
+ *   (device, may be NULL) receives the number of swaps applied.
+ * Runs in one thread block.
+ */
+jolt_status jolt_refine(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                        int64_t budget, int32_t* choice, int32_t* n_swaps, void* stream);
+
+/*
+ * Uniform baseline allocation [P1 Verification, Stage 1: the comparison
+ * against every group on the same candidate, fixed at 4 bits]: every unit
+ * takes the same candidate, chosen among `cand_host` (n_list flat indices,
+ * host memory, 1 <= n_list <= JOLT_MAX_CAND) as the one of least total
+ * distortion (the units' dists summed in unit order, f64) whose total cost
+ * fits the budget, ties to the lower index.  If none fits, every unit takes
+ * the list's candidate of least total cost (ties: lower index) and *status
+ * is JOLT_ERR_INFEASIBLE.  Fixed-bit: the list of every rank pair at one bit
+ * width; fixed-rank: every bit width at one rank pair.
+ *   choice [n_units] int32, status [1] int32 (device).
+ */
+jolt_status jolt_allocate_uniform(int n_units, int n_cand, const double* dist,
+                                  const int64_t* cost, int64_t budget, const int32_t* cand_host,
+                                  int n_list, int32_t* choice, int32_t* status, void* stream);
+
+/*
+ * Measurement hook: when both are non-NULL, the two CUDA events (cudaEvent_t
+ * created with timing enabled, owned by the caller) are recorded on the call's
+ * stream immediately before and after the fused sweep kernel of every later
+ * jolt_sweep_candidates / jolt_sweep_candidates_noalloc call, so that the
+ * kernel's own duration can be read with cudaEventElapsedTime.  NULL, NULL
+ * turns it off.  Process-wide setting, not thread-safe; JOLT_ERR_INVALID if
+ * only one is NULL.
+ */
+jolt_status jolt_set_sweep_events(void* start, void* stop);
 
 /* Size in bytes of the serialized blob of candidate `cand` (flat index). */
 size_t jolt_blob_bytes(const jolt_config* cfg, int cand);

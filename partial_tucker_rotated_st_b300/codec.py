@@ -53,6 +53,7 @@ class Encoder:
         self.choice = torch.empty(n_units, dtype=torch.int32, device=self.device)
         self.lam = torch.empty(1, dtype=torch.float64, device=self.device)
         self.astat = torch.empty(1, dtype=torch.int32, device=self.device)
+        self.nswap = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.stride = max(J.jolt_blob_bytes(cfg, c) for c in range(self.ncand))
         self.stride = (self.stride + 255) // 256 * 256
         self.blob = torch.empty(n_units, self.stride, dtype=torch.uint8, device=self.device)
@@ -65,20 +66,26 @@ class Encoder:
         J.jolt_sweep_candidates(self.cfg, self.U, X, signs, self.ws, self.dist, self.cost,
                                 stream=stream)
 
-    def allocate(self, budget: int, stream=None):
+    def allocate(self, budget: int, stream=None, refine: bool = False):
+        """Bisection on lambda; with `refine`, then the greedy swaps."""
         J.jolt_allocate(self.U, self.ncand, self.dist, self.cost, budget, self.cfg.align,
                         self.choice, self.lam, self.astat, stream=stream)
+        if refine:
+            J.jolt_refine(self.U, self.ncand, self.dist, self.cost, budget, self.choice,
+                          self.nswap, stream=stream)
 
     def serialize(self, X, signs, choice: Sequence[int], stream=None):
         return J.jolt_encode(self.cfg, self.U, X, signs, self.ws, choice, self.blob, self.stride,
                              stream=stream)
 
-    def encode(self, X, signs, budget: int, sketch=None, stream=None) -> EncodeResult:
-        """factor -> sweep -> allocate -> serialize; one small device-to-host
-        copy of the chosen candidates sits between allocate and serialize."""
+    def encode(self, X, signs, budget: int, sketch=None, stream=None,
+               refine: bool = True) -> EncodeResult:
+        """factor -> sweep -> allocate (bisection, then the greedy swaps unless
+        `refine` is False) -> serialize; one small device-to-host copy of the
+        chosen candidates sits between allocate and serialize."""
         self.factor(X, sketch, stream)
         self.sweep(X, signs, stream)
-        self.allocate(budget, stream)
+        self.allocate(budget, stream, refine=refine)
         self.choice_host.copy_(self.choice, non_blocking=True)
         s = torch.cuda.current_stream() if stream is None else stream
         s.synchronize()

@@ -164,6 +164,133 @@ alloc_kernel(int U, int nc, const double* __restrict__ gdist, const int64_t* __r
   }
 }
 
+// Greedy improvement of a feasible allocation ["Joint Tucker-rank and
+// residual-bit KV allocator", Implementation notes: swap candidates with the
+// best distortion reduction per added byte].  A swap replaces unit u's
+// candidate z by c with added bytes dc = C(c) - C(z) in (0, slack] and
+// reduction dd = D(z) - D(c) > 0; its rate is dd / dc (f64, correctly
+// rounded).  Every round applies the swap of highest rate (ties: smaller dc,
+// then lower unit, then lower candidate), until none fits.  One thread block;
+// each warp scans whole units, the block reduces the warps' bests.
+struct SwapKey {
+  unsigned long long k1, k2;   // ~rate key (higher rate first), dc
+  int uc;                      // u * nc + c
+};
+__device__ __forceinline__ bool less_swap(const SwapKey& a, const SwapKey& b) {
+  if (a.k1 != b.k1) return a.k1 < b.k1;
+  if (a.k2 != b.k2) return a.k2 < b.k2;
+  return a.uc < b.uc;
+}
+
+__global__ void __launch_bounds__(AL_THREADS)
+refine_kernel(int U, int nc, const double* __restrict__ dist, const int64_t* __restrict__ cost,
+              long long budget, int32_t* choice, int32_t* n_swaps) {
+  extern __shared__ __align__(16) unsigned char rf_raw[];
+  int* z = (int*)rf_raw;   // [U]
+  __shared__ SwapKey wbest[AL_THREADS / 32];
+  __shared__ long long slack;
+  __shared__ int done;
+  const int w = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
+  for (int u = threadIdx.x; u < U; u += blockDim.x) z[u] = choice[u];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    for (int u = 0; u < U; ++u) c += cost[(long long)u * nc + z[u]];
+    slack = budget - c;
+  }
+  __syncthreads();
+  const SwapKey none{~0ull, ~0ull, INT_MAX};
+  int swaps = 0;
+  for (int round = 0; round < U * nc; ++round) {
+    SwapKey b = none;
+    for (int u = w; u < U; u += nw) {
+      const double d0 = dist[(long long)u * nc + z[u]];
+      const long long c0 = cost[(long long)u * nc + z[u]];
+      for (int c = lane; c < nc; c += 32) {
+        const long long dc = cost[(long long)u * nc + c] - c0;
+        const double dd = __dsub_rn(d0, dist[(long long)u * nc + c]);
+        if (dc <= 0 || dc > slack || !(dd > 0.0)) continue;
+        const double rate = __ddiv_rn(dd, (double)dc);
+        const SwapKey k{~dkey(rate), ikey(dc), u * nc + c};
+        if (less_swap(k, b)) b = k;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      SwapKey y;
+      y.k1 = __shfl_xor_sync(0xffffffffu, b.k1, o);
+      y.k2 = __shfl_xor_sync(0xffffffffu, b.k2, o);
+      y.uc = __shfl_xor_sync(0xffffffffu, b.uc, o);
+      if (less_swap(y, b)) b = y;
+    }
+    if (lane == 0) wbest[w] = b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      SwapKey best = none;
+      for (int i = 0; i < nw; ++i)
+        if (less_swap(wbest[i], best)) best = wbest[i];
+      done = (best.uc == INT_MAX);
+      if (!done) {
+        const int u = best.uc / nc, c = best.uc % nc;
+        slack -= cost[(long long)u * nc + c] - cost[(long long)u * nc + z[u]];
+        z[u] = c;
+      }
+    }
+    __syncthreads();
+    if (done) break;
+    ++swaps;
+  }
+  for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = z[u];
+  if (threadIdx.x == 0 && n_swaps) *n_swaps = swaps;
+}
+
+struct UniformArgs {
+  int n;                      // candidates in the list
+  int cand[JOLT_MAX_CAND];    // flat indices
+};
+
+// The uniform baseline allocators ["Joint Tucker-rank and residual-bit KV
+// allocator", Verification, Stage 1: every group on the same (r_T, r_d, b),
+// fixed 4-bit]: every unit takes the same candidate of the list, the one of
+// least total distortion (summed over units in order, f64) whose total cost
+// fits (ties: lower index); with none fitting, the cheapest by total cost
+// (ties: lower index) and JOLT_ERR_INFEASIBLE.  One thread per candidate,
+// then one thread picks.
+__global__ void __launch_bounds__(256)
+uniform_kernel(int U, int nc, const double* __restrict__ dist, const int64_t* __restrict__ cost,
+               long long budget, UniformArgs a, int32_t* choice, int32_t* status) {
+  __shared__ double td[JOLT_MAX_CAND];
+  __shared__ long long tc[JOLT_MAX_CAND];
+  __shared__ int pick, st;
+  for (int i = threadIdx.x; i < a.n; i += blockDim.x) {
+    const int c = a.cand[i];
+    double d = 0.0;
+    long long k = 0;
+    for (int u = 0; u < U; ++u) {
+      d = __dadd_rn(d, dist[(long long)u * nc + c]);
+      k += cost[(long long)u * nc + c];
+    }
+    td[i] = d;
+    tc[i] = k;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = -1, cheap = -1;
+    for (int i = 0; i < a.n; ++i) {
+      const int c = a.cand[i];
+      if (cheap < 0 || tc[i] < tc[cheap] || (tc[i] == tc[cheap] && c < a.cand[cheap])) cheap = i;
+      if (tc[i] <= budget &&
+          (best < 0 || td[i] < td[best] || (td[i] == td[best] && c < a.cand[best])))
+        best = i;
+    }
+    pick = best >= 0 ? a.cand[best] : a.cand[cheap];
+    st = best >= 0 ? JOLT_OK : JOLT_ERR_INFEASIBLE;
+    *status = st;
+  }
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = pick;
+}
+
 }  // namespace
 
 jolt_status alloc_run(int U, int nc, const double* dist, const int64_t* cost, int64_t budget,
@@ -182,6 +309,37 @@ jolt_status alloc_run(int U, int nc, const double* dist, const int64_t* cost, in
   }
   alloc_kernel<<<1, AL_THREADS, smem, st>>>(U, nc, dist, cost, (long long)budget, align, choice,
                                             lambda, status, cached);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+}  // namespace jolt
+
+namespace jolt {
+
+jolt_status refine_run(int U, int nc, const double* dist, const int64_t* cost, int64_t budget,
+                       int32_t* choice, int32_t* n_swaps, cudaStream_t st) {
+  const size_t smem = (size_t)U * sizeof(int);
+  if (smem > 160 * 1024) return JOLT_ERR_INVALID;
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(refine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       160 * 1024));
+    attr = true;
+  }
+  refine_kernel<<<1, AL_THREADS, smem, st>>>(U, nc, dist, cost, (long long)budget, choice,
+                                             n_swaps);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+jolt_status uniform_run(int U, int nc, const double* dist, const int64_t* cost, int64_t budget,
+                        const int32_t* cand_host, int n_list, int32_t* choice, int32_t* status,
+                        cudaStream_t st) {
+  UniformArgs a;
+  a.n = n_list;
+  for (int i = 0; i < n_list; ++i) a.cand[i] = cand_host[i];
+  uniform_kernel<<<1, 256, 0, st>>>(U, nc, dist, cost, (long long)budget, a, choice, status);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

@@ -230,6 +230,33 @@ jolt_status jolt_allocate(int n_units, int n_cand, const double* dist, const int
   return alloc_run(n_units, n_cand, dist, cost, budget, align, choice, lambda, status, S(stream));
 }
 
+jolt_status jolt_set_sweep_events(void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr)) return JOLT_ERR_INVALID;
+  g_sweep_ev[0] = start;
+  g_sweep_ev[1] = stop;
+  return JOLT_OK;
+}
+
+jolt_status jolt_refine(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                        int64_t budget, int32_t* choice, int32_t* n_swaps, void* stream) {
+  if (n_units < 1 || n_cand < 1 || n_cand > JOLT_MAX_CAND || !dist || !cost || !choice)
+    return JOLT_ERR_INVALID;
+  if ((long long)n_units * n_cand > (1LL << 30)) return JOLT_ERR_INVALID;
+  return refine_run(n_units, n_cand, dist, cost, budget, choice, n_swaps, S(stream));
+}
+
+jolt_status jolt_allocate_uniform(int n_units, int n_cand, const double* dist,
+                                  const int64_t* cost, int64_t budget, const int32_t* cand_host,
+                                  int n_list, int32_t* choice, int32_t* status, void* stream) {
+  if (n_units < 1 || n_cand < 1 || n_cand > JOLT_MAX_CAND || !dist || !cost || !choice ||
+      !status || !cand_host || n_list < 1 || n_list > JOLT_MAX_CAND)
+    return JOLT_ERR_INVALID;
+  for (int i = 0; i < n_list; ++i)
+    if (cand_host[i] < 0 || cand_host[i] >= n_cand) return JOLT_ERR_INVALID;
+  return uniform_run(n_units, n_cand, dist, cost, budget, cand_host, n_list, choice, status,
+                     S(stream));
+}
+
 size_t jolt_blob_bytes(const jolt_config* cfg, int cand) {
   Layout L;
   if (make_layout(cfg, &L) != JOLT_OK || cand < 0 || cand >= L.ncand) return 0;

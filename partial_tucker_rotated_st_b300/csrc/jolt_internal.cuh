@@ -23,6 +23,7 @@ enum : int {
 };
 
 extern unsigned long long g_launches;
+extern void* g_sweep_ev[2];   // cudaEvent_t pair recorded around the fused sweep kernel, or null
 inline void count_launch(int n = 1) { g_launches += (unsigned long long)n; }
 
 #define JOLT_CUDA_TRY(expr)                                   \
@@ -177,6 +178,11 @@ jolt_status sweep_prep(const Layout& L, int n_units, const int8_t* signs, char* 
 jolt_status sweep_run(const Layout& L, int n_units, const void* X, const int8_t* signs,
                       char* ws, double* dist, int64_t* cost, cudaStream_t st,
                       float* part_override = nullptr);
+jolt_status refine_run(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                       int64_t budget, int32_t* choice, int32_t* n_swaps, cudaStream_t st);
+jolt_status uniform_run(int n_units, int n_cand, const double* dist, const int64_t* cost,
+                        int64_t budget, const int32_t* cand_host, int n_list, int32_t* choice,
+                        int32_t* status, cudaStream_t st);
 jolt_status alloc_run(int n_units, int n_cand, const double* dist, const int64_t* cost,
                       int64_t budget, int align, int32_t* choice, double* lambda,
                       int32_t* status, cudaStream_t st);

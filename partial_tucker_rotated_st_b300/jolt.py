@@ -69,6 +69,12 @@ _SIG = {
                                              ctypes.c_size_t, _P, _P, _P]),
     "jolt_allocate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int64,
                                      ctypes.c_int, _P, _P, _P, _P]),
+    "jolt_refine": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int64, _P, _P,
+                                   _P]),
+    "jolt_allocate_uniform": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_int64,
+                                             ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _P,
+                                             _P, _P]),
+    "jolt_set_sweep_events": (ctypes.c_int, [_P, _P]),
     "jolt_blob_bytes": (ctypes.c_size_t, [ctypes.POINTER(JoltConfig), ctypes.c_int]),
     "jolt_encode": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P, _P,
                                    ctypes.c_size_t, _P, _P, ctypes.c_size_t,
@@ -190,6 +196,38 @@ def jolt_allocate(n_units, n_cand, dist, cost, budget, align, choice, lam, statu
     _check("jolt_allocate", lib().jolt_allocate(
         n_units, n_cand, _ptr(dist), _ptr(cost), int(budget), int(align), _ptr(choice),
         _ptr(lam), _ptr(status), _stream(stream)))
+
+
+def jolt_refine(n_units, n_cand, dist, cost, budget, choice, n_swaps=None, stream=None):
+    _check("jolt_refine", lib().jolt_refine(
+        n_units, n_cand, _ptr(dist), _ptr(cost), int(budget), _ptr(choice), _ptr(n_swaps),
+        _stream(stream)))
+
+
+def jolt_allocate_uniform(n_units, n_cand, dist, cost, budget, cand_host: Sequence[int], choice,
+                          status, stream=None):
+    arr = (ctypes.c_int32 * len(cand_host))(*[int(c) for c in cand_host])
+    _check("jolt_allocate_uniform", lib().jolt_allocate_uniform(
+        n_units, n_cand, _ptr(dist), _ptr(cost), int(budget), arr, len(cand_host), _ptr(choice),
+        _ptr(status), _stream(stream)))
+
+
+def fixed_bit_candidates(cfg: JoltConfig, ib: int):
+    """Flat indices of every rank pair at bit index ib of the config's grid."""
+    return [(iT * cfg.n_rd + i_d) * cfg.n_b + ib for iT in range(cfg.n_rT) for i_d in range(cfg.n_rd)]
+
+
+def fixed_rank_candidates(cfg: JoltConfig, iT: int, i_d: int):
+    """Flat indices of every bit width at rank pair (iT, id) of the config's grid."""
+    return [(iT * cfg.n_rd + i_d) * cfg.n_b + ib for ib in range(cfg.n_b)]
+
+
+def jolt_set_sweep_events(start=None, stop=None):
+    """Record two torch.cuda.Event (timing enabled) around the fused sweep
+    kernel of later sweep calls; no arguments turns it off."""
+    a = None if start is None else start.cuda_event
+    b = None if stop is None else stop.cuda_event
+    _check("jolt_set_sweep_events", lib().jolt_set_sweep_events(a, b))
 
 
 def jolt_blob_bytes(cfg: JoltConfig, cand: int) -> int:

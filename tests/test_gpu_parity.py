@@ -247,3 +247,74 @@ def test_zero_unit_and_nonfinite_input():
     enc.factor(X)
     enc.sweep(X, S)
     assert enc.status() == J.ERR_NONFINITE
+
+
+def test_rank_deficient_feature_gram_matches_oracle():
+    """A feature that is identically zero makes S_d singular: the Cholesky of
+    the one-sided eigensolver meets a zero pivot, and that unit is solved by
+    the two-sided Jacobi instead.  Its tables still match the oracle, and the
+    unit next to it (definite S_d) is unaffected."""
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    w = SMALL["mistral_small"]
+    xs, signs, sk = gh.host_inputs(w, [0, 1])
+    xs[0] = xs[0].copy()
+    xs[0][:, :, 5] = 0
+    X, S, K = gh.to_device(w, xs, signs, sk)
+    enc = codec.Encoder(codec.config_for(w), 2)
+    enc.factor(X, K)
+    enc.sweep(X, S)
+    assert enc.status() == J.OK
+    dist = enc.dist.cpu().numpy()
+    for i in range(2):
+        x64 = kvgen.unit_values_f64(w, xs[i])
+        fac = oj.factorize(x64, w.rT, w.rd, w.token_mode, None, w.power_iters)
+        ref = oj.dist_table(x64, fac, signs[i], w.bits).reshape(-1)
+        assert np.all(close(dist[i], ref)), i
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_refine_and_uniform_allocators_bit_exact_on_gpu_tables(name):
+    """The greedy swap refinement and the uniform fixed-bit / fixed-rank
+    allocators on the GPU, against the oracle's own on the same (GPU) tables:
+    bit-exact choices and status."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    w, r = SMALL[name], gpu_run(name)
+    U = len(r.units)
+    nc = r.dist.shape[1]
+    dist = torch.from_numpy(r.dist).cuda()
+    cost = torch.from_numpy(r.cost).cuda()
+    budget = int(w.budget_bytes * U // w.n_units)
+    # refinement after the bisection, from the GPU's own bisection result
+    z0, _, st0 = oj.allocate(r.dist, r.cost, budget)
+    ch = torch.from_numpy(np.asarray(r.choice, dtype=np.int32)).cuda()
+    assert list(r.choice) == list(z0)
+    ns = torch.zeros(1, dtype=torch.int32, device="cuda")
+    J.jolt_refine(U, nc, dist, cost, budget, ch, ns)
+    torch.cuda.synchronize()
+    zref, nref = oj.refine_greedy(r.dist, r.cost, budget, z0)
+    assert list(ch.cpu().numpy()) == list(zref) and int(ns.item()) == nref
+    # a looser budget so that swaps actually happen
+    zl, _, _ = oj.allocate(r.dist, r.cost, budget)
+    loose = int(oj.total_cost(r.cost, zl)) + 3 * int(r.cost.max())
+    ch = torch.from_numpy(np.asarray(zl, dtype=np.int32)).cuda()
+    J.jolt_refine(U, nc, dist, cost, loose, ch, ns)
+    torch.cuda.synchronize()
+    zref, nref = oj.refine_greedy(r.dist, r.cost, loose, zl)
+    assert list(ch.cpu().numpy()) == list(zref) and int(ns.item()) == nref
+    # uniform baselines: fixed bits (every b of the grid) and fixed ranks
+    cfg = codec.config_for(w)
+    out = torch.zeros(U, dtype=torch.int32, device="cuda")
+    stt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lists = [J.fixed_bit_candidates(cfg, ib) for ib in range(cfg.n_b)]
+    lists += [J.fixed_rank_candidates(cfg, iT, i_d) for iT in range(cfg.n_rT)
+              for i_d in range(cfg.n_rd)]
+    for cand in lists:
+        for bud in (budget, budget // 4):
+            J.jolt_allocate_uniform(U, nc, dist, cost, bud, cand, out, stt)
+            torch.cuda.synchronize()
+            zref, sref = oj.allocate_uniform(r.dist, r.cost, bud, cand)
+            assert list(out.cpu().numpy()) == list(zref)
+            assert int(stt.item()) == (J.OK if sref == oj.ALLOC_OK else J.ERR_INFEASIBLE)
