@@ -236,6 +236,8 @@ def run_ours(args):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         # the fused sweep kernel alone, between two events the library records
         kev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for e in kev:
+            e.record(st)   # creates the CUDA event; the library records it again
         ev[0].record(st)
         enc.factor(X, K)
         ev[1].record(st)

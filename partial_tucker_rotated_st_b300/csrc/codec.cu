@@ -141,8 +141,14 @@ __device__ __forceinline__ float round_f16_df(float zh, float zl) {
 // ["Rotated Tucker residual for outlier-resistant KV quantization",
 //  Formulas: Y = Q R, s = max|y| / (2^(b-1) - 1) in fp16, codes = round(y / s)
 //  clipped to the b-bit range.]
+constexpr int ENC_MAX_UNITS = 16;
+struct EncBatch {
+  EncArgs u[ENC_MAX_UNITS];
+};
+
 template <typename TX, int EPT>
-__global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(EncArgs a) {
+__global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __grid_constant__ EncBatch eb) {
+  const EncArgs& a = eb.u[blockIdx.z];
   constexpr int D = 32 * EPT;
   extern __shared__ __align__(16) float dsm[];
   float* Ks = dsm;                       // [64][CD_TILE]
@@ -324,7 +330,7 @@ struct DecArgs {
 // head: the head's factor rows B (rT x D: W = G_h U_d^T, or U_d^T when
 // r_T = T) are formed once in shared memory from the fp16 blob sections
 // (staged in shared memory first) and serve every tile of the CTA.
-constexpr int DEC_TPC = 4;
+constexpr int DEC_TPC = 1;
 template <int EPT>
 __global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
   constexpr int D = 32 * EPT;
@@ -433,11 +439,30 @@ __global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
         const bool ok = t < T;
         const long long row = (long long)h * T + (ok ? t : 0);
         float q[EPT];
+        const long long bit0 = (row * D + lane * EPT) * b;
+        if (((EPT * b) & 7) == 0) {
+          // this lane's EPT codes are EPT * b (8, 16 or 32) contiguous bits
+          // starting on a byte boundary: one load
+          unsigned word = 0;
+          if (ok) {
+            const unsigned char* p0 = cb + (bit0 >> 3);
+            const int nbytes = (EPT * b) >> 3;
+            if (nbytes == 4) word = *reinterpret_cast<const unsigned*>(p0);
+            else if (nbytes == 2) word = *reinterpret_cast<const unsigned short*>(p0);
+            else word = *p0;
+          }
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) {
-          const long long bit = (row * D + lane * EPT + e) * b;
-          const int uu = ok ? ((cb[bit >> 3] >> (bit & 7)) & mask) : qoff;
-          q[e] = (float)(uu - qoff);
+          for (int e = 0; e < EPT; ++e) {
+            const int uu = ok ? (int)((word >> (e * b)) & mask) : qoff;
+            q[e] = (float)(uu - qoff);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            const long long bit = bit0 + (long long)e * b;
+            const int uu = ok ? ((cb[bit >> 3] >> (bit & 7)) & mask) : qoff;
+            q[e] = (float)(uu - qoff);
+          }
         }
         fwht_row<EPT>(q, lane);
         const float cs = ok ? __half2float(sc[row]) * rs : 0.f;
@@ -475,7 +500,7 @@ __global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
 unsigned nblk(long long n) { return (unsigned)((n + 255) / 256); }
 
 template <typename TX, int EPT>
-jolt_status launch_enc(dim3 grid, const EncArgs& ea, cudaStream_t st) {
+jolt_status launch_enc(dim3 grid, const EncBatch& ea, cudaStream_t st) {
   constexpr int D = 32 * EPT;
   const size_t smem = (64 * CD_TILE + 2 * 64 * D) * sizeof(float) + CD_WARPS * D;
   static bool attr = false;
@@ -547,6 +572,21 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
     blob_layout(H, T, D, L.rT[iT], L.rd[id], L.b[ib], L.block, L.align, &desc[u]);
     if (desc[u].bytes > stride) return JOLT_ERR_INVALID;
   }
+  // the codes of up to ENC_MAX_UNITS units per launch (grid z = unit)
+  EncBatch batch;
+  int nbatch = 0;
+  auto flush = [&]() -> jolt_status {
+    dim3 grid((T + CD_TILE - 1) / CD_TILE, H, nbatch);
+    const bool bf = (L.dtype == JOLT_BF16);
+    jolt_status ls;
+    switch (D) {
+      case 128: ls = bf ? launch_enc<__nv_bfloat16, 4>(grid, batch, st) : launch_enc<float, 4>(grid, batch, st); break;
+      case 64: ls = bf ? launch_enc<__nv_bfloat16, 2>(grid, batch, st) : launch_enc<float, 2>(grid, batch, st); break;
+      default: ls = bf ? launch_enc<__nv_bfloat16, 1>(grid, batch, st) : launch_enc<float, 1>(grid, batch, st);
+    }
+    nbatch = 0;
+    return ls;
+  };
   for (int u = 0; u < U; ++u) {
     int iT, id, ib;
     cand_split(L, choice[u], &iT, &id, &ib);
@@ -624,14 +664,14 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
         ea.Bhi = Bh; ea.Blo = Blo; ea.b_hs = (long long)rT * D;
       }
     }
-    dim3 grid((T + CD_TILE - 1) / CD_TILE, H);
-    const bool bf = (L.dtype == JOLT_BF16);
-    jolt_status ls;
-    switch (D) {
-      case 128: ls = bf ? launch_enc<__nv_bfloat16, 4>(grid, ea, st) : launch_enc<float, 4>(grid, ea, st); break;
-      case 64: ls = bf ? launch_enc<__nv_bfloat16, 2>(grid, ea, st) : launch_enc<float, 2>(grid, ea, st); break;
-      default: ls = bf ? launch_enc<__nv_bfloat16, 1>(grid, ea, st) : launch_enc<float, 1>(grid, ea, st);
+    batch.u[nbatch++] = ea;
+    if (nbatch == ENC_MAX_UNITS) {
+      jolt_status ls = flush();
+      if (ls != JOLT_OK) return ls;
     }
+  }
+  if (nbatch > 0) {
+    jolt_status ls = flush();
     if (ls != JOLT_OK) return ls;
   }
   return JOLT_OK;

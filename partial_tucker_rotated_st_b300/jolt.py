@@ -223,10 +223,13 @@ def fixed_rank_candidates(cfg: JoltConfig, iT: int, i_d: int):
 
 
 def jolt_set_sweep_events(start=None, stop=None):
-    """Record two torch.cuda.Event (timing enabled) around the fused sweep
-    kernel of later sweep calls; no arguments turns it off."""
+    """Record two torch.cuda.Event (timing enabled, already created, i.e.
+    recorded once) around the fused sweep kernel of later sweep calls; no
+    arguments turns it off."""
     a = None if start is None else start.cuda_event
     b = None if stop is None else stop.cuda_event
+    if (start is not None and not a) or (stop is not None and not b):
+        raise ValueError("record the events once before passing them")
     _check("jolt_set_sweep_events", lib().jolt_set_sweep_events(a, b))
 
 
