@@ -326,19 +326,14 @@ struct DecArgs {
   DecUnit un[DEC_MAX_UNITS];
 };
 
-// X^ = X~ + Q^T (s * codes).  One CTA per DEC_TPC tiles of 64 rows of one
-// head: the head's factor rows B (rT x D: W = G_h U_d^T, or U_d^T when
-// r_T = T) are formed once in shared memory from the fp16 blob sections
-// (staged in shared memory first) and serve every tile of the CTA.
-constexpr int DEC_TPC = 1;
+// X^ = X~ + Q^T (s * codes), one tile of 64 rows of one head per CTA.
 template <int EPT>
 __global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
   constexpr int D = 32 * EPT;
   extern __shared__ __align__(16) float dsm[];
-  float* Ks = dsm;                       // [64][CD_TILE] chain coefficients (also G_h staging)
-  float* Bs = Ks + 64 * CD_TILE;         // [64][D] factor rows
-  __half* Us = (__half*)(Bs + 64 * D);   // [D][64] U_d staging
-  const int uz = blockIdx.z, h = blockIdx.y;
+  float* Ks = dsm;                       // [64][CD_TILE]
+  float* Bs = Ks + 64 * CD_TILE;         // [64][D]
+  const int uz = blockIdx.z, h = blockIdx.y, t0 = blockIdx.x * CD_TILE;
   const int u = a.u0 + uz;
   const DecUnit du = a.un[uz];
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -347,152 +342,138 @@ __global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
   const int rT = du.rT, rd = du.rd, b = du.b;
   const bool fullT = (rT == T), fullD = (rd == D);
   const __half* G = (const __half*)(blob + du.off_G);
+  float acc[CD_ROWS][EPT];
   int K = 0;
-  if (!(fullT && fullD)) {
+  if (fullT && fullD) {
+#pragma unroll
+    for (int r = 0; r < CD_ROWS; ++r) {
+      const int t = t0 + w * CD_ROWS + r;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e)
+        acc[r][e] = (t < T) ? __half2float(G[((long long)h * T + t) * D + lane * EPT + e]) : 0.f;
+    }
+  } else {
     if (fullT) {
-      // X~[t] = G[h][t][:rd] U_d^T: B = U_d^T
+      // X~[t] = G[h][t][:rd] U_d^T
       K = rd;
       const __half* Ud = (const __half*)(blob + du.off_Ud);
+      for (int i = threadIdx.x; i < CD_TILE * K; i += CD_THREADS) {
+        const int row = i / K, j = i % K, t = t0 + row;
+        Ks[j * CD_TILE + row] = (t < T) ? __half2float(G[((long long)h * T + t) * rd + j]) : 0.f;
+      }
       for (int i = threadIdx.x; i < K * D; i += CD_THREADS) {
         const int j = i / D, d = i % D;
         Bs[i] = __half2float(Ud[(long long)d * rd + j]);
       }
     } else {
-      // X~[t] = U_T[t] W_h, W_h = G[h] U_d^T (rT x D)
+      // X~[t] = U_T[t] P_h, P_h = G[h] U_d^T (rT x D)
       K = rT;
+      const __half* UT = (const __half*)(blob + du.off_UT);
+      for (int i = threadIdx.x; i < CD_TILE * K; i += CD_THREADS) {
+        const int row = i / K, k = i % K, t = t0 + row;
+        Ks[k * CD_TILE + row] = (t < T) ? __half2float(UT[(long long)t * rT + k]) : 0.f;
+      }
       const __half* Gh = G + (long long)h * rT * rd;
       if (fullD) {
         for (int i = threadIdx.x; i < K * D; i += CD_THREADS) Bs[i] = __half2float(Gh[i]);
       } else {
         const __half* Ud = (const __half*)(blob + du.off_Ud);
-        for (int i = threadIdx.x; i < K * rd; i += CD_THREADS) Ks[i] = __half2float(Gh[i]);
-        for (int i = threadIdx.x; i < D * rd; i += CD_THREADS) Us[i] = Ud[i];
-        __syncthreads();
         for (int i = threadIdx.x; i < K * D; i += CD_THREADS) {
           const int k = i / D, d = i % D;
           float v = 0.f;
-          for (int j = 0; j < rd; ++j) v = fmaf(Ks[k * rd + j], __half2float(Us[d * rd + j]), v);
+          for (int j = 0; j < rd; ++j)
+            v = fmaf(__half2float(Gh[k * rd + j]), __half2float(Ud[(long long)d * rd + j]), v);
           Bs[i] = v;
         }
       }
     }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < CD_ROWS; ++r)
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) acc[r][e] = 0.f;
+    for (int k = 0; k < K; ++k) {
+      const float* kk = Ks + k * CD_TILE + w * CD_ROWS;
+      float bv[EPT];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) bv[e] = Bs[k * D + lane * EPT + e];
+#pragma unroll
+      for (int r = 0; r < CD_ROWS; ++r)
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(kk[r], bv[e], acc[r][e]);
+    }
   }
-  float sg[EPT];
-  {
+  if (b > 0) {
     const unsigned char* sbits = (const unsigned char*)blob + 88;
+    float sg[EPT];
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
       const int d = lane * EPT + e;
       sg[e] = ((sbits[d >> 3] >> (d & 7)) & 1) ? -1.f : 1.f;
     }
-  }
-  const float rs = rsqrtf((float)D);
-  const unsigned char* cb = (const unsigned char*)blob + du.off_codes;
-  const __half* sc = (const __half*)(blob + du.off_scale);
-  const int qoff = b > 0 ? 1 << (b - 1) : 0, mask = (1 << b) - 1;
-  for (int tile = 0; tile < DEC_TPC; ++tile) {
-    const int t0 = (blockIdx.x * DEC_TPC + tile) * CD_TILE;
-    if (t0 >= T) break;
-    float acc[CD_ROWS][EPT];
-    __syncthreads();   // Ks of the previous tile (or the G_h staging) is free
-    if (fullT && fullD) {
-#pragma unroll
-      for (int r = 0; r < CD_ROWS; ++r) {
-        const int t = t0 + w * CD_ROWS + r;
-#pragma unroll
-        for (int e = 0; e < EPT; ++e)
-          acc[r][e] = (t < T) ? __half2float(G[((long long)h * T + t) * D + lane * EPT + e]) : 0.f;
-      }
-    } else {
-      if (fullT) {
-        for (int i = threadIdx.x; i < CD_TILE * K; i += CD_THREADS) {
-          const int row = i / K, j = i % K, t = t0 + row;
-          Ks[j * CD_TILE + row] = (t < T) ? __half2float(G[((long long)h * T + t) * rd + j]) : 0.f;
-        }
-      } else {
-        const __half* UT = (const __half*)(blob + du.off_UT);
-        for (int i = threadIdx.x; i < CD_TILE * K; i += CD_THREADS) {
-          const int row = i / K, k = i % K, t = t0 + row;
-          Ks[k * CD_TILE + row] = (t < T) ? __half2float(UT[(long long)t * rT + k]) : 0.f;
-        }
-      }
-      __syncthreads();
-#pragma unroll
-      for (int r = 0; r < CD_ROWS; ++r)
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[r][e] = 0.f;
-      for (int k = 0; k < K; ++k) {
-        const float* kk = Ks + k * CD_TILE + w * CD_ROWS;
-        float bv[EPT];
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) bv[e] = Bs[k * D + lane * EPT + e];
-#pragma unroll
-        for (int r = 0; r < CD_ROWS; ++r)
-#pragma unroll
-          for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(kk[r], bv[e], acc[r][e]);
-      }
-    }
-    if (b > 0) {
-#pragma unroll
-      for (int r = 0; r < CD_ROWS; ++r) {
-        const int t = t0 + w * CD_ROWS + r;
-        const bool ok = t < T;
-        const long long row = (long long)h * T + (ok ? t : 0);
-        float q[EPT];
-        const long long bit0 = (row * D + lane * EPT) * b;
-        if (((EPT * b) & 7) == 0) {
-          // this lane's EPT codes are EPT * b (8, 16 or 32) contiguous bits
-          // starting on a byte boundary: one load
-          unsigned word = 0;
-          if (ok) {
-            const unsigned char* p0 = cb + (bit0 >> 3);
-            const int nbytes = (EPT * b) >> 3;
-            if (nbytes == 4) word = *reinterpret_cast<const unsigned*>(p0);
-            else if (nbytes == 2) word = *reinterpret_cast<const unsigned short*>(p0);
-            else word = *p0;
-          }
-#pragma unroll
-          for (int e = 0; e < EPT; ++e) {
-            const int uu = ok ? (int)((word >> (e * b)) & mask) : qoff;
-            q[e] = (float)(uu - qoff);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < EPT; ++e) {
-            const long long bit = bit0 + (long long)e * b;
-            const int uu = ok ? ((cb[bit >> 3] >> (bit & 7)) & mask) : qoff;
-            q[e] = (float)(uu - qoff);
-          }
-        }
-        fwht_row<EPT>(q, lane);
-        const float cs = ok ? __half2float(sc[row]) * rs : 0.f;
-#pragma unroll
-        for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(sg[e] * cs, q[e], acc[r][e]);
-      }
-    }
+    const float rs = rsqrtf((float)D);
+    const unsigned char* cb = (const unsigned char*)blob + du.off_codes;
+    const __half* sc = (const __half*)(blob + du.off_scale);
+    const int qoff = 1 << (b - 1), mask = (1 << b) - 1;
 #pragma unroll
     for (int r = 0; r < CD_ROWS; ++r) {
       const int t = t0 + w * CD_ROWS + r;
-      if (t >= T) continue;
-      const long long o = (((long long)u * H + h) * T + t) * D + lane * EPT;
-      if (a.out_dtype == JOLT_BF16) {
-        __nv_bfloat16* y = (__nv_bfloat16*)a.xhat + o;
-        if constexpr (EPT == 4) {
-          __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[r][0], acc[r][1]);
-          __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[r][2], acc[r][3]);
-          uint2 pk;
-          pk.x = *reinterpret_cast<unsigned*>(&p0);
-          pk.y = *reinterpret_cast<unsigned*>(&p1);
-          *reinterpret_cast<uint2*>(y) = pk;
-        } else {
+      const bool ok = t < T;
+      const long long row = (long long)h * T + (ok ? t : 0);
+      float q[EPT];
+      const long long bit0 = (row * D + lane * EPT) * b;
+      if (((EPT * b) & 7) == 0) {
+        // this lane's EPT codes are EPT * b (8, 16 or 32) contiguous bits
+        // starting on a byte boundary: one load
+        unsigned word = 0;
+        if (ok) {
+          const unsigned char* p0 = cb + (bit0 >> 3);
+          const int nbytes = (EPT * b) >> 3;
+          if (nbytes == 4) word = *reinterpret_cast<const unsigned*>(p0);
+          else if (nbytes == 2) word = *reinterpret_cast<const unsigned short*>(p0);
+          else word = *p0;
+        }
 #pragma unroll
-          for (int e = 0; e < EPT; ++e) y[e] = __float2bfloat16_rn(acc[r][e]);
+        for (int e = 0; e < EPT; ++e) {
+          const int uu = ok ? (int)((word >> (e * b)) & mask) : qoff;
+          q[e] = (float)(uu - qoff);
         }
       } else {
-        float* y = (float*)a.xhat + o;
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) y[e] = acc[r][e];
+        for (int e = 0; e < EPT; ++e) {
+          const long long bit = bit0 + (long long)e * b;
+          const int uu = ok ? ((cb[bit >> 3] >> (bit & 7)) & mask) : qoff;
+          q[e] = (float)(uu - qoff);
+        }
       }
+      fwht_row<EPT>(q, lane);
+      const float cs = ok ? __half2float(sc[row]) * rs : 0.f;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) acc[r][e] = fmaf(sg[e] * cs, q[e], acc[r][e]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < CD_ROWS; ++r) {
+    const int t = t0 + w * CD_ROWS + r;
+    if (t >= T) continue;
+    const long long o = (((long long)u * H + h) * T + t) * D + lane * EPT;
+    if (a.out_dtype == JOLT_BF16) {
+      __nv_bfloat16* y = (__nv_bfloat16*)a.xhat + o;
+      if constexpr (EPT == 4) {
+        __nv_bfloat162 p0 = __floats2bfloat162_rn(acc[r][0], acc[r][1]);
+        __nv_bfloat162 p1 = __floats2bfloat162_rn(acc[r][2], acc[r][3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<unsigned*>(&p0);
+        pk.y = *reinterpret_cast<unsigned*>(&p1);
+        *reinterpret_cast<uint2*>(y) = pk;
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) y[e] = __float2bfloat16_rn(acc[r][e]);
+      }
+    } else {
+      float* y = (float*)a.xhat + o;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) y[e] = acc[r][e];
     }
   }
 }
@@ -517,7 +498,7 @@ jolt_status launch_enc(dim3 grid, const EncBatch& ea, cudaStream_t st) {
 template <int EPT>
 jolt_status launch_dec(dim3 grid, const DecArgs& a, cudaStream_t st) {
   constexpr int D = 32 * EPT;
-  const size_t smem = (64 * CD_TILE + 64 * D) * sizeof(float) + (size_t)D * 64 * sizeof(__half);
+  const size_t smem = (64 * CD_TILE + 64 * D) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(decode_kernel<EPT>,
@@ -692,7 +673,7 @@ jolt_status decode_run(int U, const jolt_blob_desc* desc, const char* blob, size
       a.un[i].off_UT = d.off_UT; a.un[i].off_Ud = d.off_Ud; a.un[i].off_G = d.off_G;
       a.un[i].off_scale = d.off_scale; a.un[i].off_codes = d.off_codes;
     }
-    dim3 grid((T + CD_TILE * DEC_TPC - 1) / (CD_TILE * DEC_TPC), H, nu);
+    dim3 grid((T + CD_TILE - 1) / CD_TILE, H, nu);
     jolt_status ls;
     switch (D) {
       case 128: ls = launch_dec<4>(grid, a, st); break;

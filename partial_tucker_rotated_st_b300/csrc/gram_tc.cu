@@ -526,6 +526,330 @@ __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt
   }
 }
 
+// ---------------------------------------------------------------- sweep (TC)
+// The candidate sweep with the dense products on the tensor cores, for bf16
+// X with D = 128 and truncated ranks <= 32.  One CTA scores 128 tokens of one
+// head, one thread per token row:
+//   * QX = X (diag(sigma) H) by kind::f16 MMAs (bf16 X and the +-1 matrix are
+//     exact; fp32 accumulate) into TMEM columns [0, 128);
+//   * every reconstruction in the rotated domain, U_T W or Y16 (Q U_d)^T at a
+//     rank checkpoint r, as K[:, :r] B[:r, :] by kind::tf32 MMAs (K, fp16
+//     values, is exact in tf32; B split hi + lo) into TMEM columns [128, 256),
+//     recomputed from k = 0 for each checkpoint (columns r..8*ceil(r/8) of K
+//     zeroed meanwhile);
+//   * each thread then reads its row y = QX / sqrt(D) - P back in 32-column
+//     chunks and scores every b exactly as the SIMT sweep does (row max,
+//     fp16 scale, round-half-even by the magic constant, squared error).
+// The K and B operands are written by the threads in the 128-byte swizzled
+// K-major layout (16-byte unit u of row r at u ^ (r % 8)), X and the sign
+// matrix arrive by TMA in the same layout.
+constexpr int STC_ROWS = 128, STC_THREADS = 128;
+constexpr int STC_XBYTES = STC_ROWS * 256;       // 128 rows x 128 bf16
+constexpr int STC_KBYTES = STC_ROWS * 128;       // 128 rows x 32 fp32
+
+struct SweepTcArgs {
+  int H, T, nT, nd, nb, nTt, ndt, RT, RD, hasFullT, hasFullD;
+  int rT[JOLT_MAX_GRID], rd[JOLT_MAX_GRID], b[4];
+  float rq[4];
+  int ncand, tiles_t;
+  char* ws;
+  size_t ub, o_UT16, o_W, o_Y16, o_QUd, o_status;
+  float* part;
+  long long part_us;
+};
+
+__device__ __forceinline__ uint32_t sw128(int r, int byte) {
+  return (uint32_t)(r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
+}
+
+__device__ __forceinline__ void tmem_ld32_pair(uint32_t a0, float (&v0)[32], uint32_t a1,
+                                               float (&v1)[32], bool two) {
+  uint32_t r0[32], r1[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]),
+        "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]),
+        "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]),
+        "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]),
+        "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31])
+      : "r"(a0));
+  if (two) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]),
+          "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]),
+          "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]),
+          "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]),
+          "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
+        : "r"(a1));
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
+  if (two) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v1[i] = __uint_as_float(r1[i]);
+  }
+}
+
+// Score one candidate from TMEM: row `trow` (this thread's lane address);
+// y = QX rs - P (with_qx) or y = P rs (the whole-modes residual).
+__device__ __forceinline__ void stc_score(uint32_t trow, bool with_qx, float rs,
+                                          const SweepTcArgs& a, float* cells, int cell0) {
+  const float2 rs2 = make_float2(rs, rs);
+  float m = 0.f;
+  float2 e0 = make_float2(0.f, 0.f);
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    float q[32], p[32];
+    tmem_ld32_pair(trow + 128 + c, p, trow + c, q, with_qx);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float2 pp = make_float2(p[j], p[j + 1]);
+      const float2 y = with_qx ? __ffma2_rn(make_float2(q[j], q[j + 1]), rs2, make_float2(-pp.x, -pp.y))
+                               : __fmul2_rn(pp, rs2);
+      m = fmaxf(m, fmaxf(fabsf(y.x), fabsf(y.y)));
+      e0 = __ffma2_rn(y, y, e0);
+    }
+  }
+  float s[4], inv[4];
+#pragma unroll
+  for (int ib = 0; ib < 4; ++ib) {
+    s[ib] = 0.f; inv[ib] = 0.f;
+    if (ib < a.nb && a.b[ib] > 0) {
+      s[ib] = round_f16(m * a.rq[ib]);
+      float r;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s[ib]));
+      inv[ib] = s[ib] > 0.f ? r : 0.f;
+    }
+  }
+  const float2 M2 = make_float2(12582912.0f, 12582912.0f), nM2 = make_float2(-12582912.0f, -12582912.0f);
+  float2 eb[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+  for (int c = 0; c < 128; c += 32) {
+    float q[32], p[32];
+    tmem_ld32_pair(trow + 128 + c, p, trow + c, q, with_qx);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float2 pp = make_float2(p[j], p[j + 1]);
+      const float2 y = with_qx ? __ffma2_rn(make_float2(q[j], q[j + 1]), rs2, make_float2(-pp.x, -pp.y))
+                               : __fmul2_rn(pp, rs2);
+#pragma unroll
+      for (int ib = 0; ib < 4; ++ib) {
+        if (ib >= a.nb || a.b[ib] == 0) continue;
+        const float2 i2 = make_float2(inv[ib], inv[ib]), ns2 = make_float2(-s[ib], -s[ib]);
+        const float2 qq = __fadd2_rn(__ffma2_rn(y, i2, M2), nM2);
+        const float2 d = __ffma2_rn(ns2, qq, y);
+        eb[ib] = __ffma2_rn(d, d, eb[ib]);
+      }
+    }
+  }
+  float v[4];
+#pragma unroll
+  for (int ib = 0; ib < 4; ++ib) v[ib] = (ib < a.nb && a.b[ib] == 0) ? e0.x + e0.y : eb[ib].x + eb[ib].y;
+#pragma unroll
+  for (int ib = 0; ib < 4; ++ib)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v[ib] += __shfl_xor_sync(0xffffffffu, v[ib], o);
+  if ((threadIdx.x & 31) == 0)
+#pragma unroll
+    for (int ib = 0; ib < 4; ++ib)
+      if (ib < a.nb) atomicAdd(&cells[cell0 + ib], v[ib]);
+}
+
+__global__ void __launch_bounds__(STC_THREADS, 2)
+sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tHs,
+                SweepTcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  unsigned char* sX = base;                       // X tile (2 chunks), later K operand
+  unsigned char* sH = base + STC_XBYTES;          // sign matrix (2 chunks), later B hi / lo
+  float* cells = (float*)(base + 2 * STC_XBYTES); // [ncand + 1]
+  struct Bars { uint64_t tma, mma; uint32_t tmem; int nz; };
+  Bars* S = (Bars*)(cells + 260);
+  const int t = threadIdx.x, warp = t >> 5;
+  const int tt = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
+  const int t0 = tt * STC_ROWS, row = t0 + t;
+  const bool in = row < a.T;
+  char* ub = a.ws + (size_t)u * a.ub;
+  for (int i = t; i <= a.ncand; i += STC_THREADS) cells[i] = 0.f;
+  if (t == 0) {
+    tc::mbar_init(tc::smem_u32(&S->tma), 1);
+    tc::mbar_init(tc::smem_u32(&S->mma), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&S->tmem), 256);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  bool ok = true;
+  uint32_t mma_phase = 0;
+  auto mma_wait = [&]() {
+    if (!tc::mbar_wait(tc::smem_u32(&S->mma), mma_phase & 1)) ok = false;
+    ++mma_phase;
+    tc::tc_fence_after();
+  };
+  // ---- X and the sign matrix by TMA; QX = X Hs into TMEM [0, 128)
+  if (t == 0) {
+    const uint32_t fb = tc::smem_u32(&S->tma);
+    tc::mbar_expect_tx(fb, 2 * STC_XBYTES);
+    const int xr = u * a.H + h;
+    tc::tma_load_3d(tc::smem_u32(sX), &tX, 0, t0, xr, fb);
+    tc::tma_load_3d(tc::smem_u32(sX + STC_XBYTES / 2), &tX, 64, t0, xr, fb);
+    tc::tma_load_3d(tc::smem_u32(sH), &tHs, 0, 0, u, fb);
+    tc::tma_load_3d(tc::smem_u32(sH + STC_XBYTES / 2), &tHs, 64, 0, u, fb);
+  }
+  if (!tc::mbar_wait(tc::smem_u32(&S->tma), 0)) ok = false;
+  constexpr uint32_t idesc16 = tc::idesc_bf16(128, 128, 0, 0);
+  constexpr uint32_t idesc32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                               ((uint32_t)(128 >> 4) << 24);
+  auto mma_x = [&](uint32_t dcol) {   // D[dcol..] = sX sH^T over K = 128 (bf16)
+    if (t == 0) {
+      tc::tc_fence_after();
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sX + kc * (STC_XBYTES / 2)) + 32 * k, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sH + kc * (STC_XBYTES / 2)) + 32 * k, 16, 1024);
+          tc::mma_f16(tmem + dcol, ad, bd, idesc16, (kc | k) != 0);
+        }
+      tc::mma_commit(tc::smem_u32(&S->mma));
+    }
+  };
+  mma_x(0);
+  mma_wait();
+  // ---- ||x||^2 and the whole-modes residual x - fp16(x) (in place, bf16-exact)
+  const float rs = rsqrtf(128.f);
+  {
+    float xn = 0.f;
+    int nz = 0;
+#pragma unroll 4
+    for (int c = 0; c < 128; c += 8) {
+      unsigned char* p = sX + (c >> 6) * (STC_XBYTES / 2) + sw128(t, (c & 63) * 2);
+      uint4 v = *reinterpret_cast<uint4*>(p);
+      __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float x = __bfloat162float(e[i]);
+        xn = fmaf(x, x, xn);
+        const float r = x - round_f16(x);
+        nz |= (r != 0.f);
+        e[i] = __float2bfloat16_rn(r);
+      }
+      *reinterpret_cast<uint4*>(p) = v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) xn += __shfl_xor_sync(0xffffffffu, xn, o);
+    if ((t & 31) == 0) atomicAdd(&cells[a.ncand], xn);
+    nz = __syncthreads_or(nz);
+    if (a.hasFullT && a.hasFullD && nz) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+      mma_x(128);
+      mma_wait();
+      stc_score(trow, false, rs, a, cells, ((a.nT - 1) * a.nd + (a.nd - 1)) * a.nb);
+    }
+  }
+  // ---- rank chains: P = K[:, :r] B[:r, :] for each checkpoint r
+  unsigned char* sK = sX;                 // 128 x 32 fp32
+  unsigned char* sBh = sH;                // 128 (n) x 32 fp32
+  unsigned char* sBl = sH + STC_KBYTES;
+  auto run_chain = [&](const __half* Kg, long long k_ld, int kn, const float* Bg, int nck,
+                       const int* ranks, int cellbase, int cellstride) {
+    tc::tc_fence_before();
+    __syncthreads();   // previous MMAs and TMEM reads done, operands free
+    // K rows (this thread's token row), fp16 -> fp32, zero past kn / T
+    for (int k = 0; k < 32; k += 4) {
+      float4 v;
+      float* pv = reinterpret_cast<float*>(&v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        pv[i] = (in && k + i < kn) ? __half2float(Kg[(long long)row * k_ld + k + i]) : 0.f;
+      *reinterpret_cast<float4*>(sK + sw128(t, k * 4)) = v;
+    }
+    // B^T rows: n = t, B^T[n][k] = B[k][n], split hi + lo
+    for (int k = 0; k < 32; k += 4) {
+      float4 hi, lo;
+      float* ph = reinterpret_cast<float*>(&hi);
+      float* pl = reinterpret_cast<float*>(&lo);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float b = (k + i < kn) ? Bg[(long long)(k + i) * 128 + t] : 0.f;
+        const float bh = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
+        ph[i] = bh;
+        pl[i] = b - bh;
+      }
+      *reinterpret_cast<float4*>(sBh + sw128(t, k * 4)) = hi;
+      *reinterpret_cast<float4*>(sBl + sw128(t, k * 4)) = lo;
+    }
+    for (int ci = 0; ci < nck; ++ci) {
+      const int r = ranks[ci];
+      const int ks = (r + 7) >> 3;
+      // zero K columns r .. 8 ks - 1 of this row for this checkpoint
+      float saved[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = r + i;
+        saved[i] = 0.f;
+        if (k < 8 * ks) {
+          float* p = reinterpret_cast<float*>(sK + sw128(t, k * 4));
+          saved[i] = *p;
+          *p = 0.f;
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tc::tc_fence_before();
+      __syncthreads();
+      if (t == 0) {
+        tc::tc_fence_after();
+        for (int k = 0; k < ks; ++k) {
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sK) + 32 * k, 16, 1024);
+          const uint64_t bh = tc::sdesc_sw128(tc::smem_u32(sBh) + 32 * k, 16, 1024);
+          const uint64_t bl = tc::sdesc_sw128(tc::smem_u32(sBl) + 32 * k, 16, 1024);
+          tc::mma_tf32(tmem + 128, ad, bh, idesc32, k != 0);
+          tc::mma_tf32(tmem + 128, ad, bl, idesc32, 1);
+        }
+        tc::mma_commit(tc::smem_u32(&S->mma));
+      }
+      mma_wait();
+      stc_score(trow, true, rs, a, cells, cellbase + ci * cellstride);
+      // restore the zeroed columns for the next checkpoint
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int k = r + i;
+        if (k < 8 * ks) *reinterpret_cast<float*>(sK + sw128(t, k * 4)) = saved[i];
+      }
+      tc::tc_fence_before();
+      __syncthreads();
+    }
+  };
+  if (a.hasFullT && a.ndt > 0) {
+    const __half* Yh = (const __half*)(ub + a.o_Y16) + (long long)h * a.T * a.RD;
+    run_chain(Yh, a.RD, a.RD, (const float*)(ub + a.o_QUd), a.ndt, a.rd,
+              ((a.nT - 1) * a.nd) * a.nb, a.nb);
+  }
+  if (a.nTt > 0) {
+    for (int id = 0; id < a.nd; ++id) {
+      const __half* Ug = (const __half*)(ub + a.o_UT16) + (long long)id * a.T * a.RT;
+      const float* Wg = (const float*)(ub + a.o_W) + ((long long)id * a.H + h) * a.RT * 128;
+      run_chain(Ug, a.RT, a.RT, Wg, a.nTt, a.rT, id * a.nb, a.nd * a.nb);
+    }
+  }
+  if (!ok) atomicOr((int*)(ub + a.o_status), ST_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  float* part = a.part + u * a.part_us + ((long long)h * a.tiles_t + tt) * (a.ncand + 1);
+  for (int i = t; i <= a.ncand; i += STC_THREADS) part[i] = cells[i];
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -719,6 +1043,58 @@ jolt_status ygram_tc(const Layout& L, int U, const char* ws, char* pbase, size_t
   dim3 grid(a.nt * (a.nt + 1) / 2, U * L.ndt);
   ygram_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tH, tL, a);
   JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+// ---- tensor-core sweep
+bool sweep_tc_supported(const Layout& L) {
+  if (!(L.dtype == JOLT_BF16 && L.D == 128 && L.RT <= 32 && L.RD <= 32 && L.o_Hs != 0 &&
+        encode_fn() != nullptr && L.ncand + 1 <= 260 && L.nb <= 4))
+    return false;
+  return true;
+}
+
+jolt_status sweep_tc_run(const Layout& L, int U, const void* X, char* ws, float* part,
+                         long long part_us, int* tiles_t_out, cudaStream_t st) {
+  CUtensorMap tX;
+  const cuuint64_t dX[3] = {128, (cuuint64_t)L.T, (cuuint64_t)U * L.H};
+  const cuuint64_t sX[2] = {256, (cuuint64_t)L.T * 256};
+  const cuuint32_t bX[3] = {64, 128, 1};
+  if (!make_map(&tX, X, 3, dX, sX, bX)) return JOLT_ERR_CUDA;
+  // the sign matrices sit one per unit region: a 3-D map (128 cols, 128 rows, unit)
+  CUtensorMap tH3;
+  const cuuint64_t dH3[3] = {128, 128, (cuuint64_t)U};
+  const cuuint64_t sH3[2] = {256, (cuuint64_t)L.unit_bytes};
+  const cuuint32_t bH3[3] = {64, 128, 1};
+  if (!make_map(&tH3, ws + L.o_Hs, 3, dH3, sH3, bH3)) return JOLT_ERR_CUDA;
+  SweepTcArgs a;
+  memset(&a, 0, sizeof(a));
+  a.H = L.H; a.T = L.T; a.nT = L.nT; a.nd = L.nd; a.nb = L.nb; a.nTt = L.nTt; a.ndt = L.ndt;
+  a.RT = L.RT; a.RD = L.RD; a.hasFullT = L.hasFullT; a.hasFullD = L.hasFullD;
+  for (int i = 0; i < JOLT_MAX_GRID; ++i) {
+    a.rT[i] = i < L.nTt ? L.rT[i] : -1;
+    a.rd[i] = i < L.ndt ? L.rd[i] : -1;
+  }
+  for (int i = 0; i < 4; ++i) {
+    a.b[i] = L.b[i];
+    a.rq[i] = L.b[i] > 0 ? 1.f / (float)((1 << (L.b[i] - 1)) - 1) : 0.f;
+  }
+  a.ncand = L.ncand;
+  a.tiles_t = (L.T + STC_ROWS - 1) / STC_ROWS;
+  a.ws = ws; a.ub = L.unit_bytes;
+  a.o_UT16 = L.o_UT16; a.o_W = L.o_W; a.o_Y16 = L.o_Y16; a.o_QUd = L.o_QUd; a.o_status = L.o_status;
+  a.part = part; a.part_us = part_us;
+  const size_t smem = 2 * STC_XBYTES + 260 * 4 + 64 + 1024;
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem));
+    attr = true;
+  }
+  dim3 grid(a.tiles_t, L.H, U);
+  sweep_tc_kernel<<<grid, STC_THREADS, smem, st>>>(tX, tH3, a);
+  JOLT_LAUNCH_CHECK();
+  *tiles_t_out = a.tiles_t;
   return JOLT_OK;
 }
 

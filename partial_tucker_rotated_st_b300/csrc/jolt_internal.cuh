@@ -70,6 +70,7 @@ struct Layout {
   size_t o_status, o_Sd, o_Sd64, o_Sdp, o_evd, o_Vd, o_Ud16, o_QUd, o_Y, o_Y16;
   size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
   size_t o_Yt;           // Y relaid [T][RD*H] and its tf32 low part (token Gram)
+  size_t o_Hs;           // diag(sigma) H_D as bf16 [D][D] (tensor-core sweep), or 0
   size_t unit_bytes;
   // Token-mode problems, one per (unit, feature rank), in a region after the
   // n unit regions of a call: truncated rank id of unit u is problem
@@ -171,6 +172,11 @@ jolt_status ygram_tc(const Layout& L, int n_units, const char* ws, char* pbase, 
 jolt_status factor_run(const Layout& L, int n_units, const void* X, const float* sketch,
                        char* ws, cudaStream_t st);
 // Rotated factor rows for the sweep and the encoder: Q U_d and W = G (Q U_d)^T.
+bool sweep_tc_supported(const Layout& L);
+// The tensor-core sweep over all units: per-tile partial sums at part (unit
+// stride part_us floats); *tiles_t_out = row tiles per head.
+jolt_status sweep_tc_run(const Layout& L, int n_units, const void* X, char* ws, float* part,
+                         long long part_us, int* tiles_t_out, cudaStream_t st);
 jolt_status sweep_prep(const Layout& L, int n_units, const int8_t* signs, char* ws,
                        cudaStream_t st);
 // part_override: where the per-tile partial sums go (n_units * ntiles *

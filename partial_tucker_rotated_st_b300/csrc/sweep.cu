@@ -330,6 +330,18 @@ __global__ void rotate_ud_kernel(char* ws, size_t ub, const int8_t* signs, size_
   for (int e = 0; e < EPT; ++e) out[lane * EPT + e] = v[e] * rs;
 }
 
+// Hs[u][j][d] = sigma_d (-1)^popcount(d & j): B^T of the rotation X diag(sigma) H
+// (Sylvester order, unnormalised) for the tensor-core sweep, bf16 (exact).
+__global__ void sign_hadamard_kernel(char* ws, size_t ub, const int8_t* signs, size_t o_Hs, int D) {
+  const int u = blockIdx.y;
+  __nv_bfloat16* Hs = (__nv_bfloat16*)(ws + u * ub + o_Hs);
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < D * D; e += gridDim.x * blockDim.x) {
+    const int j = e / D, d = e % D;
+    const int sgn = (__popc(d & j) & 1) ? -1 : 1;
+    Hs[e] = __float2bfloat16_rn((float)(sgn * (int)signs[(long long)u * D + d]));
+  }
+}
+
 // W[id][h][k][:] = sum_j G16[id][h][k][j] QUd[j][:]  (r_d < D), or
 //                = Q G16[id][h][k][:]                  (r_d = D).
 template <int EPT>
@@ -463,6 +475,10 @@ jolt_status sweep_prep(const Layout& L, int U, const int8_t* signs, char* ws, cu
     else rotate_ud_kernel<1><<<g, 256, 0, st>>>(ws, ub, signs, L.o_Ud16, L.RD, L.o_QUd);
     JOLT_LAUNCH_CHECK();
   }
+  if (L.o_Hs != 0) {
+    sign_hadamard_kernel<<<dim3(16, U), 256, 0, st>>>(ws, ub, signs, L.o_Hs, L.D);
+    JOLT_LAUNCH_CHECK();
+  }
   if (L.RT > 0) {
     for (int id = 0; id < L.nd; ++id) {
       dim3 g(1, L.H, U);
@@ -505,14 +521,23 @@ jolt_status sweep_run(const Layout& L, int U, const void* X, const int8_t* signs
     a.part_us = (long long)ub / 4;
   }
   jolt_status s;
+  int ntiles = L.ntiles;
   // optional timing events around the fused kernel alone (measurement hook)
   if (g_sweep_ev[0]) JOLT_CUDA_TRY(cudaEventRecord((cudaEvent_t)g_sweep_ev[0], st));
-  if (D == 128) s = launch_sweep_t<8>(a, U, st);
-  else if (D == 64) s = launch_sweep_t<4>(a, U, st);
-  else s = launch_sweep_t<2>(a, U, st);
+  if (sweep_tc_supported(L)) {
+    int tiles_t = 0;
+    s = sweep_tc_run(L, U, X, ws, a.part, a.part_us, &tiles_t, st);
+    ntiles = L.H * tiles_t;
+  } else if (D == 128) {
+    s = launch_sweep_t<8>(a, U, st);
+  } else if (D == 64) {
+    s = launch_sweep_t<4>(a, U, st);
+  } else {
+    s = launch_sweep_t<2>(a, U, st);
+  }
   if (g_sweep_ev[1]) JOLT_CUDA_TRY(cudaEventRecord((cudaEvent_t)g_sweep_ev[1], st));
   if (s != JOLT_OK) return s;
-  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, a.part, a.part_us, L.o_status, L.ntiles, L.ncand,
+  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, a.part, a.part_us, L.o_status, ntiles, L.ncand,
                                         dist);
   JOLT_LAUNCH_CHECK();
   CostArgs ca;
