@@ -342,9 +342,9 @@ def run_ours(args):
 
 
 SWEEP_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tucker_rotated_st_b300",
-                         "csrc", "sweep.cu")
+                         "csrc", "gram_tc.cu")
 SWEEP_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
-                             "sweep_kernel_mistral_t1024.md")
+                             "sweep_tc_kernel_mistral_t1024.md")
 
 
 def sweep_traffic(workload):
@@ -366,26 +366,32 @@ def sweep_traffic(workload):
 
 
 def roofline(w, kernel_s, hbm, kind, pk):
-    """Roofline of the fused sweep kernel (the dominant kernel of the step):
-    FP32-ALU bound by construction; the algorithmic operation count per
-    element is spelled out in the design notes.  `kernel_s` is the kernel's
-    own average duration (CUDA events around its launch)."""
+    """Roofline of the fused sweep kernel (the dominant kernel of the step).
+    Its dense products (the rotation of X and every rank checkpoint's
+    reconstruction) run on the tensor cores; what bounds it is the FP32
+    scoring of every candidate, counted per element and rank pair as: the
+    residual y (1 FMA), |y| max (1), y^2 for b = 0 (1 FMA), and per b > 0 the
+    scaled rounding (1 FMA + 1 add), the residual (1 FMA) and its square
+    (1 FMA), FMA = 2 flops: 26 flops per pair per element.  `kernel_s` is the
+    kernel's own average duration (CUDA events around its launch)."""
     U, N = w.n_units, w.elems_per_unit
     RT = max(r for r in w.rT if r != kvgen.FULL)
     RD = max(r for r in w.rd if r != kvgen.FULL)
     nd, nT, nb = len(w.rd), len(w.rT), len(w.bits)
     nbq = sum(1 for b in w.bits if b > 0)
     pairs = nT * nd
-    flops_el = 2 * (nd * RT + RD) + pairs * (6 * nbq + 2 * (nb - nbq) + 1) + 2 * 8
+    flops_el = pairs * (2 + 1 + 2 * (nb - nbq) + 7 * nbq)
+    tensor_el = 2 * w.D + 2 * 2 * (nd * RT + RD)   # rotation; chains with the hi/lo split
     flops = flops_el * N * U
     sm_max = pk.get("sm_max_mhz", 2032.0)
     peak = 148 * 128 * 2 * sm_max * 1e6 / 1e12
     ach = flops / kernel_s / 1e12
-    return {"kernel": "sweep_kernel", "bound": "alu", "achieved": ach, "peak": peak,
+    return {"kernel": "sweep_tc_kernel", "bound": "alu", "achieved": ach, "peak": peak,
             "unit": "TFLOP/s", "frac": ach / peak, "traffic": sweep_traffic(w.name),
             "kernel_ms": 1e3 * kernel_s,
             "peak_source": "derived: FP32 pipe, 148 SMs x 128 lanes x 2 flop x max SM clock",
-            "flops_per_element": flops_el, "bytes_per_element_algorithmic": 2,
+            "flops_per_element": flops_el, "tensor_flops_per_element": tensor_el,
+            "bytes_per_element_algorithmic": 2,
             "hbm_peak_gbs": hbm, "hbm_peak_kind": kind}
 
 

@@ -562,37 +562,75 @@ __device__ __forceinline__ uint32_t sw128(int r, int byte) {
   return (uint32_t)(r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
 }
 
-__device__ __forceinline__ void tmem_ld32_pair(uint32_t a0, float (&v0)[32], uint32_t a1,
-                                               float (&v1)[32], bool two) {
-  uint32_t r0[32], r1[32];
+// 16 columns of this thread's TMEM lane into registers, without waiting.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t addr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];"
-      : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]),
-        "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]),
-        "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]),
-        "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]),
-        "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31])
-      : "r"(a0));
-  if (two) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-        "%30, %31}, [%32];"
-        : "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]),
-          "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]),
-          "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]),
-          "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]),
-          "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
-        : "r"(a1));
-  }
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(addr));
+}
+// Wait for this thread's TMEM loads, tied to the registers it makes valid
+// (so that no use of them can be scheduled before it).
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16], uint32_t (&q)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(q[0]), "+r"(q[1]),
+                 "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7]),
+                 "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]), "+r"(q[12]), "+r"(q[13]),
+                 "+r"(q[14]), "+r"(q[15])
+               :
+               : "memory");
+}
+
+// One pass over this thread's row, 16 columns at a time, with the loads of
+// the next 16 columns in flight while the current ones are used:
+// f(y0, y1) is called on consecutive pairs of y = QX rs - P (with_qx) or
+// y = P rs.
+template <typename F>
+__device__ __forceinline__ void stc_pass(uint32_t trow, bool with_qx, float rs, F&& f) {
+  const float2 rs2 = make_float2(rs, rs);
+  uint32_t pa[16], qa[16], pb[16], qb[16];
+  tmem_ld16_issue(trow + 128, pa);
+  if (with_qx) tmem_ld16_issue(trow, qa);
+  if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);
+  auto use = [&](const uint32_t (&p)[16], const uint32_t (&q)[16]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v0[i] = __uint_as_float(r0[i]);
-  if (two) {
+    for (int j = 0; j < 16; j += 2) {
+      const float2 pp = make_float2(__uint_as_float(p[j]), __uint_as_float(p[j + 1]));
+      const float2 y = with_qx
+                           ? __ffma2_rn(make_float2(__uint_as_float(q[j]), __uint_as_float(q[j + 1])),
+                                        rs2, make_float2(-pp.x, -pp.y))
+                           : __fmul2_rn(pp, rs2);
+      f(y);
+    }
+  };
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v1[i] = __uint_as_float(r1[i]);
+  for (int c = 0; c < 128; c += 32) {
+    // columns c..c+15 are in (pa, qa); fetch c+16..c+31 into (pb, qb)
+    tmem_ld16_issue(trow + 128 + c + 16, pb);
+    if (with_qx) tmem_ld16_issue(trow + c + 16, qb);
+    use(pa, qa);
+    if (with_qx) tmem_ld_wait(pb, qb); else tmem_ld_wait(pb);
+    if (c + 32 < 128) {
+      tmem_ld16_issue(trow + 128 + c + 32, pa);
+      if (with_qx) tmem_ld16_issue(trow + c + 32, qa);
+    }
+    use(pb, qb);
+    if (c + 32 < 128) {
+      if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);
+    }
   }
 }
 
@@ -600,22 +638,14 @@ __device__ __forceinline__ void tmem_ld32_pair(uint32_t a0, float (&v0)[32], uin
 // y = QX rs - P (with_qx) or y = P rs (the whole-modes residual).
 __device__ __forceinline__ void stc_score(uint32_t trow, bool with_qx, float rs,
                                           const SweepTcArgs& a, float* cells, int cell0) {
-  const float2 rs2 = make_float2(rs, rs);
-  float m = 0.f;
+  float m0 = 0.f, m1 = 0.f;
   float2 e0 = make_float2(0.f, 0.f);
-#pragma unroll 1
-  for (int c = 0; c < 128; c += 32) {
-    float q[32], p[32];
-    tmem_ld32_pair(trow + 128 + c, p, trow + c, q, with_qx);
-#pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float2 pp = make_float2(p[j], p[j + 1]);
-      const float2 y = with_qx ? __ffma2_rn(make_float2(q[j], q[j + 1]), rs2, make_float2(-pp.x, -pp.y))
-                               : __fmul2_rn(pp, rs2);
-      m = fmaxf(m, fmaxf(fabsf(y.x), fabsf(y.y)));
-      e0 = __ffma2_rn(y, y, e0);
-    }
-  }
+  stc_pass(trow, with_qx, rs, [&](float2 y) {
+    m0 = fmaxf(m0, fabsf(y.x));
+    m1 = fmaxf(m1, fabsf(y.y));
+    e0 = __ffma2_rn(y, y, e0);
+  });
+  const float m = fmaxf(m0, m1);
   float s[4], inv[4];
 #pragma unroll
   for (int ib = 0; ib < 4; ++ib) {
@@ -629,25 +659,16 @@ __device__ __forceinline__ void stc_score(uint32_t trow, bool with_qx, float rs,
   }
   const float2 M2 = make_float2(12582912.0f, 12582912.0f), nM2 = make_float2(-12582912.0f, -12582912.0f);
   float2 eb[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
-  for (int c = 0; c < 128; c += 32) {
-    float q[32], p[32];
-    tmem_ld32_pair(trow + 128 + c, p, trow + c, q, with_qx);
+  stc_pass(trow, with_qx, rs, [&](float2 y) {
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float2 pp = make_float2(p[j], p[j + 1]);
-      const float2 y = with_qx ? __ffma2_rn(make_float2(q[j], q[j + 1]), rs2, make_float2(-pp.x, -pp.y))
-                               : __fmul2_rn(pp, rs2);
-#pragma unroll
-      for (int ib = 0; ib < 4; ++ib) {
-        if (ib >= a.nb || a.b[ib] == 0) continue;
-        const float2 i2 = make_float2(inv[ib], inv[ib]), ns2 = make_float2(-s[ib], -s[ib]);
-        const float2 qq = __fadd2_rn(__ffma2_rn(y, i2, M2), nM2);
-        const float2 d = __ffma2_rn(ns2, qq, y);
-        eb[ib] = __ffma2_rn(d, d, eb[ib]);
-      }
+    for (int ib = 0; ib < 4; ++ib) {
+      if (ib >= a.nb || a.b[ib] == 0) continue;
+      const float2 i2 = make_float2(inv[ib], inv[ib]), ns2 = make_float2(-s[ib], -s[ib]);
+      const float2 qq = __fadd2_rn(__ffma2_rn(y, i2, M2), nM2);
+      const float2 d = __ffma2_rn(ns2, qq, y);
+      eb[ib] = __ffma2_rn(d, d, eb[ib]);
     }
-  }
+  });
   float v[4];
 #pragma unroll
   for (int ib = 0; ib < 4; ++ib) v[ib] = (ib < a.nb && a.b[ib] == 0) ? e0.x + e0.y : eb[ib].x + eb[ib].y;
@@ -766,13 +787,29 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
     tc::tc_fence_before();
     __syncthreads();   // previous MMAs and TMEM reads done, operands free
     // K rows (this thread's token row), fp16 -> fp32, zero past kn / T
-    for (int k = 0; k < 32; k += 4) {
-      float4 v;
-      float* pv = reinterpret_cast<float*>(&v);
+    if (kn == 32 && (k_ld & 7) == 0) {
+      uint4 raw[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
-        pv[i] = (in && k + i < kn) ? __half2float(Kg[(long long)row * k_ld + k + i]) : 0.f;
-      *reinterpret_cast<float4*>(sK + sw128(t, k * 4)) = v;
+        raw[i] = in ? reinterpret_cast<const uint4*>(Kg + (long long)row * k_ld)[i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half* hv = reinterpret_cast<const __half*>(&raw[i]);
+        float4 v0, v1;
+        v0.x = __half2float(hv[0]); v0.y = __half2float(hv[1]); v0.z = __half2float(hv[2]); v0.w = __half2float(hv[3]);
+        v1.x = __half2float(hv[4]); v1.y = __half2float(hv[5]); v1.z = __half2float(hv[6]); v1.w = __half2float(hv[7]);
+        *reinterpret_cast<float4*>(sK + sw128(t, (8 * i) * 4)) = v0;
+        *reinterpret_cast<float4*>(sK + sw128(t, (8 * i + 4) * 4)) = v1;
+      }
+    } else {
+      for (int k = 0; k < 32; k += 4) {
+        float4 v;
+        float* pv = reinterpret_cast<float*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          pv[i] = (in && k + i < kn) ? __half2float(Kg[(long long)row * k_ld + k + i]) : 0.f;
+        *reinterpret_cast<float4*>(sK + sw128(t, k * 4)) = v;
+      }
     }
     // B^T rows: n = t, B^T[n][k] = B[k][n], split hi + lo
     for (int k = 0; k < 32; k += 4) {
