@@ -472,7 +472,8 @@ struct JoinGuard {
 // leading RT eigenvectors into p_UT, eigenvalues into p_ev (direct Jacobi when
 // T <= 128, else block subspace iteration with Rayleigh-Ritz).  `warm`: p_V
 // already holds an orthonormal start block.
-jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st) {
+jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st,
+                        bool split_done = false) {
   const int T = L.T, RT = L.RT, Lw = L.L;
   const long long s4 = P.s4();
   int* status = (int*)P.c(L.p_status);
@@ -493,7 +494,7 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
   set_int_kernel<<<P.np, 32, 0, st>>>(P.base, P.stride, L.p_flag, 0);
   JOLT_LAUNCH_CHECK();
   const bool svtc = sv_tc_supported(L);
-  if (svtc) TRY(split_tok_gram(L, P.np, P.base, P.stride, st));
+  if (svtc && !split_done) TRY(split_tok_gram(L, P.np, P.base, P.stride, st));
   const int* flags = (const int*)P.c(L.p_flag);
   // Z lives in one of two buffers: Rayleigh-Ritz writes Z2 = S V2 into the
   // other one, and the next block starts from it (its first power step is
@@ -678,6 +679,28 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
         ws, ub, L.o_Y, RD, L.o_Y16, RD, H * T, RD, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
   }
+  // The truncated ranks' token Grams need only Y: they follow the feature
+  // stage on its stream, still beside the whole-feature token solve.
+  const bool early_tr = RT > 0 && L.token_mode == JOLT_TOKEN_EXACT && L.ndt > 0 && L.T > 128;
+  if (early_tr) {
+    char* preg0 = ws + (size_t)U * ub;
+    const size_t pb0 = L.prob_bytes;
+    if (ygram_tc_supported(L)) {
+      TRY(ytrans(L, U, ws, fs));
+      TRY(ygram_tc(L, U, ws, preg0, pb0, fs));
+    } else {
+      for (int id = 0; id < L.ndt; ++id) {
+        const long long ps4 = (long long)((size_t)L.ndt * pb0) / 4;
+        const float* Y0 = (const float*)(ws + L.o_Y);
+        const long long aseg = (long long)T * RD;
+        TRY(launch_gemm(gd(T, T, L.rd[id], H, U, 1, opnd(Y0, JOLT_F32, RD, 1, aseg, ub4),
+                           opnd(Y0, JOLT_F32, 1, RD, aseg, ub4),
+                           (float*)(preg0 + (size_t)id * pb0 + L.p_ST), T, 1, ps4, 0),
+                        fs));
+      }
+    }
+    if (sv_tc_supported(L)) TRY(split_tok_gram(L, U * L.ndt, preg0, pb0, fs));
+  }
   if (overlap) JOLT_CUDA_TRY(cudaEventRecord(ev.b, fs));
   if (RT == 0) return JOLT_OK;
 
@@ -713,8 +736,10 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     }
     TRY(join());
     if (ndt > 0) {
-      // every truncated rank's Gram, then one batched solve for all of them
-      if (T > 128 && ygram_tc_supported(L)) {
+      // every truncated rank's Gram (already queued after the feature stage
+      // when T > 128), then one batched solve for all of them
+      if (early_tr) {
+      } else if (T > 128 && ygram_tc_supported(L)) {
         TRY(ytrans(L, U, ws, st));
         TRY(ygram_tc(L, U, ws, preg, pb, st));
       } else {
@@ -733,7 +758,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
                                                             (long long)T * L.L);
         JOLT_LAUNCH_CHECK();
       }
-      TRY(token_exact(L, all_tr, warm, st));
+      TRY(token_exact(L, all_tr, warm, st, early_tr));
     }
   } else {
     // randomized: the whole-feature rank first (beside the feature stage),
