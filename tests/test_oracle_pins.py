@@ -421,3 +421,51 @@ def test_allocate_uniform_hand_case():
     assert st == jolt.ALLOC_INFEASIBLE and list(z) == [2, 2]
     assert jolt.fixed_bit_candidates(2, 3, 4, 2) == [2, 6, 10, 14, 18, 22]
     assert jolt.fixed_rank_candidates(2, 3, 4, 1, 2) == [20, 21, 22, 23]
+
+
+# ---------------------------------------------------------------- modeled error
+@pytest.mark.parametrize("rT,rd", [(3, 16), (7, 4), (20, 9), (40, 3), (40, 16)])
+def test_tail_energy_is_the_unrounded_truncation_error(rT, rd):
+    """tau from the spectra equals ||X - X~||^2 reconstructed from the
+    unrounded factors (measured directly, not through the spectra)."""
+    for X in _small_tensor():
+        H, T, D = X.shape
+        fac = jolt.factorize(X, [rT, jolt.FULL], [rd, jolt.FULL])
+        rdr, rTr = jolt.resolve(rd, D), jolt.resolve(rT, T)
+        if rTr < T:
+            UT, G = fac.UT[rdr][:, :rTr], fac.G[rdr][:, :rTr, :]
+        else:
+            UT, G = None, fac.Y[rdr]
+        Ud = None if rdr == D else fac.Ud[rdr]
+        err = np.sum((X - jolt.reconstruct(UT, G, Ud)) ** 2)
+        nx = float(np.sum(X * X))
+        assert abs(jolt.tail_energy(fac, rTr, rdr, nx) - err) <= 1e-9 * nx
+
+
+def test_eps2_uniform_noise_approximation():
+    """For fine steps the rounding error of a row is uniform on [-s/2, s/2]:
+    eps^2(b) ~ E[s^2] / 12 / E[y^2] with s = max|y| / (2^(b-1) - 1).  Checked at
+    b = 8 against that closed form, within the fp16 rounding of s and the
+    Monte Carlo spread; eps^2(0) = 1 and eps^2 falls with b."""
+    rng = np.random.default_rng(11)
+    rows = rng.standard_normal((4000, 128))
+    e = jolt.eps2_calibrate(rows, [0, 2, 4, 8])
+    assert e[0] == 1.0 and e[0] > e[1] > e[2] > e[3] > 0
+    m2 = np.mean(np.max(np.abs(rows), axis=1) ** 2)
+    approx = m2 / 127.0 ** 2 / 12.0 / np.mean(rows * rows)
+    assert abs(e[3] / approx - 1.0) < 0.05
+
+
+def test_model_dist_table_layout_and_scaling():
+    X, _ = _small_tensor()
+    H, T, D = X.shape
+    fac = jolt.factorize(X, [4, jolt.FULL], [4, jolt.FULL])
+    nx = float(np.sum(X * X))
+    eps2 = np.array([1.0, 0.5, 0.01, 1e-4])
+    t = jolt.model_dist_table(fac, nx, [0, 2, 4, 8], eps2).reshape(2, 2, 4)
+    # (T, D) reproduces X exactly; b = 0 is the bare tail; b > 0 scales it
+    assert np.all(t[1, 1] == 0.0)
+    assert abs(t[0, 0, 0] - jolt.tail_energy(fac, 4, 4, nx) / nx) <= 1e-15
+    assert np.allclose(t[0, 0, 1:], eps2[1:] * t[0, 0, 0], rtol=1e-15)
+    assert abs(t[1, 0, 0] - fac.feat_eigvals[4:].sum() / nx) <= 1e-12
+    assert np.all(jolt.model_dist_table(fac, 0.0, [0, 2, 4, 8], eps2) == 0.0)
