@@ -34,32 +34,6 @@ struct HeaderArgs {
   int D;
 };
 
-__global__ void header_kernel(HeaderArgs a, const int8_t* signs, char* blob) {
-  const int t = threadIdx.x;
-  for (int i = t; i < 88; i += blockDim.x) blob[i] = (char)a.fixed[i];
-  for (int i = t; i < (a.D + 7) / 8; i += blockDim.x) {
-    unsigned char v = 0;
-    for (int k = 0; k < 8; ++k) {
-      const int d = i * 8 + k;
-      if (d < a.D && signs[d] < 0) v |= (unsigned char)(1u << k);
-    }
-    blob[88 + i] = (char)v;
-  }
-}
-
-// dst[a][b][c] = fp16(src[a*sa + b*sb + c]) for a < A, b < B, c < C.
-template <typename TS>
-__global__ void copy_f16_kernel(const TS* src, long long sa, long long sb, __half* dst, int A, int B,
-                                int C) {
-  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long n = (long long)A * B * C;
-  if (e >= n) return;
-  const int c = (int)(e % C);
-  const long long ab = e / C;
-  const int b = (int)(ab % B), aa = (int)(ab / B);
-  dst[e] = __float2half_rn(to_f32(src[aa * sa + b * sb + c]));
-}
-
 struct EncArgs {
   const void* X;
   const int8_t* signs;
@@ -290,25 +264,92 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
   }
 }
 
-// Unrotated chain rows of a truncated core, B[h][k][:] = G16[h][k][:] U_d16^T,
+// Serialization of the header and the factor sections of a batch of units in
+// one launch (grid y = unit): each unit lists up to three copies
+// dst[a][b][c] = fp16(src[a*sa + b*sb + c]) (a < A, b < B, c < C) of a source
+// in fp16, bf16 or fp32, and its 256-byte header.
+struct CopyJob {
+  const void* src;
+  __half* dst;
+  long long sa, sb;
+  int A, B, C, type;   // type: 0 fp16, 1 bf16, 2 fp32
+};
+struct SecUnit {
+  CopyJob job[3];
+  int njobs;
+  HeaderArgs ha;
+  const int8_t* signs;
+  char* blob;
+};
+struct SecBatch {
+  SecUnit u[ENC_MAX_UNITS];
+};
+
+__global__ void sections_kernel(const __grid_constant__ SecBatch sb) {
+  const SecUnit& su = sb.u[blockIdx.y];
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < 88; i += blockDim.x) su.blob[i] = (char)su.ha.fixed[i];
+    for (int i = threadIdx.x; i < (su.ha.D + 7) / 8; i += blockDim.x) {
+      unsigned char v = 0;
+      for (int k = 0; k < 8; ++k) {
+        const int d = i * 8 + k;
+        if (d < su.ha.D && su.signs[d] < 0) v |= (unsigned char)(1u << k);
+      }
+      su.blob[88 + i] = (char)v;
+    }
+  }
+  for (int j = 0; j < su.njobs; ++j) {
+    const CopyJob& cj = su.job[j];
+    const long long n = (long long)cj.A * cj.B * cj.C;
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (long long)gridDim.x * blockDim.x) {
+      const int c = (int)(e % cj.C);
+      const long long ab = e / cj.C;
+      const int b = (int)(ab % cj.B), aa = (int)(ab / cj.B);
+      const long long si = aa * cj.sa + b * cj.sb + c;
+      float v;
+      if (cj.type == 0) v = __half2float(((const __half*)cj.src)[si]);
+      else if (cj.type == 1) v = __bfloat162float(((const __nv_bfloat16*)cj.src)[si]);
+      else v = ((const float*)cj.src)[si];
+      cj.dst[e] = __float2half_rn(v);
+    }
+  }
+}
+
+// Unrotated chain rows of a truncated core for a batch of units (grid z =
+// unit; an entry with rT = 0 is skipped): B[h][k][:] = G16[h][k][:] U_d16^T,
 // accumulated in double-float (fp16 x fp16 products are exact in fp32).
-__global__ void enc_rows_kernel(const __half* G, long long g_hs, const __half* Ud, int ldu, int rT,
-                                int rd, int D, float* Bhi, float* Blo) {
+struct RowsUnit {
+  const __half* G;
+  long long g_hs;
+  const __half* Ud;
+  int ldu, rT, rd;
+  float* Bhi;
+  float* Blo;
+};
+struct RowsBatch {
+  RowsUnit u[ENC_MAX_UNITS];
+  int D;
+};
+__global__ void enc_rows_batch_kernel(const __grid_constant__ RowsBatch rb) {
+  const RowsUnit& r = rb.u[blockIdx.z];
+  const int D = rb.D;
+  if (r.rT == 0) return;
   const int h = blockIdx.y;
-  const __half* Gh = G + h * g_hs;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < rT * D; i += gridDim.x * blockDim.x) {
+  const __half* Gh = r.G + h * r.g_hs;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < r.rT * D; i += gridDim.x * blockDim.x) {
     const int k = i / D, d = i % D;
     float sh = 0.f, sl = 0.f;
-    for (int j = 0; j < rd; ++j) {
-      const float p = __half2float(Gh[k * rd + j]) * __half2float(Ud[(long long)d * ldu + j]);
-      float s, e;
-      two_sum(sh, p, s, e);
-      sh = s;
+    for (int j = 0; j < r.rd; ++j) {
+      const float p = __half2float(Gh[k * r.rd + j]) * __half2float(r.Ud[(long long)d * r.ldu + j]);
+      float s2, e;
+      two_sum(sh, p, s2, e);
+      sh = s2;
       sl += e;
     }
     const float hi = sh + sl;
-    Bhi[(long long)h * rT * D + i] = hi;
-    Blo[(long long)h * rT * D + i] = sl - (hi - sh);
+    r.Bhi[(long long)h * r.rT * D + i] = hi;
+    r.Blo[(long long)h * r.rT * D + i] = sl - (hi - sh);
   }
 }
 
@@ -478,8 +519,6 @@ __global__ void __launch_bounds__(CD_THREADS) decode_kernel(DecArgs a) {
   }
 }
 
-unsigned nblk(long long n) { return (unsigned)((n + 255) / 256); }
-
 template <typename TX, int EPT>
 jolt_status launch_enc(dim3 grid, const EncBatch& ea, cudaStream_t st) {
   constexpr int D = 32 * EPT;
@@ -510,15 +549,6 @@ jolt_status launch_dec(dim3 grid, const DecArgs& a, cudaStream_t st) {
   return JOLT_OK;
 }
 
-template <typename TS>
-jolt_status copy_f16(const void* src, long long sa, long long sb, void* dst, int A, int B, int C,
-                     cudaStream_t st) {
-  const long long n = (long long)A * B * C;
-  if (n <= 0) return JOLT_OK;
-  copy_f16_kernel<TS><<<nblk(n), 256, 0, st>>>((const TS*)src, sa, sb, (__half*)dst, A, B, C);
-  JOLT_LAUNCH_CHECK();
-  return JOLT_OK;
-}
 
 }  // namespace
 
@@ -553,19 +583,35 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
     blob_layout(H, T, D, L.rT[iT], L.rd[id], L.b[ib], L.block, L.align, &desc[u]);
     if (desc[u].bytes > stride) return JOLT_ERR_INVALID;
   }
-  // the codes of up to ENC_MAX_UNITS units per launch (grid z = unit)
+  // one zero fill for every blob slot (padding bytes are deterministic)
+  JOLT_CUDA_TRY(cudaMemsetAsync(blob, 0, (size_t)U * stride, st));
+  // per batch of up to ENC_MAX_UNITS units: one launch for the headers and
+  // factor sections, one for the chain rows, one for the codes
+  SecBatch secs;
+  RowsBatch rows;
   EncBatch batch;
-  int nbatch = 0;
+  int nsec = 0, nrows = 0, nbatch = 0;
+  const bool bf = (L.dtype == JOLT_BF16);
   auto flush = [&]() -> jolt_status {
-    dim3 grid((T + CD_TILE - 1) / CD_TILE, H, nbatch);
-    const bool bf = (L.dtype == JOLT_BF16);
-    jolt_status ls;
-    switch (D) {
-      case 128: ls = bf ? launch_enc<__nv_bfloat16, 4>(grid, batch, st) : launch_enc<float, 4>(grid, batch, st); break;
-      case 64: ls = bf ? launch_enc<__nv_bfloat16, 2>(grid, batch, st) : launch_enc<float, 2>(grid, batch, st); break;
-      default: ls = bf ? launch_enc<__nv_bfloat16, 1>(grid, batch, st) : launch_enc<float, 1>(grid, batch, st);
+    if (nsec > 0) {
+      sections_kernel<<<dim3(64, nsec), 256, 0, st>>>(secs);
+      JOLT_LAUNCH_CHECK();
     }
-    nbatch = 0;
+    if (nrows > 0) {
+      rows.D = D;
+      enc_rows_batch_kernel<<<dim3((RT * D + 255) / 256, H, nrows), 256, 0, st>>>(rows);
+      JOLT_LAUNCH_CHECK();
+    }
+    jolt_status ls = JOLT_OK;
+    if (nbatch > 0) {
+      dim3 grid((T + CD_TILE - 1) / CD_TILE, H, nbatch);
+      switch (D) {
+        case 128: ls = bf ? launch_enc<__nv_bfloat16, 4>(grid, batch, st) : launch_enc<float, 4>(grid, batch, st); break;
+        case 64: ls = bf ? launch_enc<__nv_bfloat16, 2>(grid, batch, st) : launch_enc<float, 2>(grid, batch, st); break;
+        default: ls = bf ? launch_enc<__nv_bfloat16, 1>(grid, batch, st) : launch_enc<float, 1>(grid, batch, st);
+      }
+    }
+    nsec = nrows = nbatch = 0;
     return ls;
   };
   for (int u = 0; u < U; ++u) {
@@ -576,82 +622,77 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
     char* bl = blob + (size_t)u * stride;
     const char* wu = ws + (size_t)u * L.unit_bytes;
     const void* Xu = (const char*)X + (size_t)u * xu * xes;
-    JOLT_CUDA_TRY(cudaMemsetAsync(bl, 0, dsc.bytes, st));
-    HeaderArgs ha;
-    memset(&ha, 0, sizeof(ha));
+    SecUnit& su = secs.u[nsec++];
+    memset(&su, 0, sizeof(su));
     const uint32_t hd32[10] = {MAGIC, VERSION, (uint32_t)H, (uint32_t)T, (uint32_t)D, (uint32_t)rT,
                                (uint32_t)rd, (uint32_t)b, (uint32_t)L.block, (uint32_t)dsc.flags};
-    memcpy(ha.fixed, hd32, 40);
+    memcpy(su.ha.fixed, hd32, 40);
     const uint64_t hd64[6] = {dsc.off_UT, dsc.off_Ud, dsc.off_G, dsc.off_scale, dsc.off_codes,
                               dsc.bytes};
-    memcpy(ha.fixed + 40, hd64, 48);
-    ha.D = D;
-    header_kernel<<<1, 128, 0, st>>>(ha, signs + (size_t)u * D, bl);
-    JOLT_LAUNCH_CHECK();
+    memcpy(su.ha.fixed + 40, hd64, 48);
+    su.ha.D = D;
+    su.signs = signs + (size_t)u * D;
+    su.blob = bl;
+    auto job = [&](const void* src, int type, long long sa, long long sbv, size_t off, int A, int B,
+                   int C) {
+      CopyJob& j = su.job[su.njobs++];
+      j.src = src; j.type = type; j.sa = sa; j.sb = sbv;
+      j.dst = (__half*)(bl + off); j.A = A; j.B = B; j.C = C;
+    };
     // factor sections
+    if (rT < T) job(wu + L.o_UT16 + (size_t)id * T * RT * 2, 0, 0, RT, dsc.off_UT, 1, T, rT);
+    if (rd < D) job(wu + L.o_Ud16, 0, 0, RD, dsc.off_Ud, 1, D, rd);
     if (rT < T) {
-      jolt_status s = copy_f16<__half>(wu + L.o_UT16 + (size_t)id * T * RT * 2, 0, RT,
-                                       bl + dsc.off_UT, 1, T, rT, st);
-      if (s != JOLT_OK) return s;
-    }
-    if (rd < D) {
-      jolt_status s = copy_f16<__half>(wu + L.o_Ud16, 0, RD, bl + dsc.off_Ud, 1, D, rd, st);
-      if (s != JOLT_OK) return s;
-    }
-    jolt_status s;
-    if (rT < T) {
-      s = copy_f16<__half>(wu + L.o_G16 + (size_t)id * H * RT * D * 2, (long long)RT * rd, rd,
-                           bl + dsc.off_G, H, rT, rd, st);
+      job(wu + L.o_G16 + (size_t)id * H * RT * D * 2, 0, (long long)RT * rd, rd, dsc.off_G, H, rT, rd);
     } else if (rd < D) {
-      s = copy_f16<__half>(wu + L.o_Y16, (long long)T * RD, RD, bl + dsc.off_G, H, T, rd, st);
-    } else if (L.dtype == JOLT_BF16) {
-      s = copy_f16<__nv_bfloat16>(Xu, (long long)T * D, D, bl + dsc.off_G, H, T, D, st);
+      job(wu + L.o_Y16, 0, (long long)T * RD, RD, dsc.off_G, H, T, rd);
     } else {
-      s = copy_f16<float>(Xu, (long long)T * D, D, bl + dsc.off_G, H, T, D, st);
+      job(Xu, L.dtype == JOLT_BF16 ? 1 : (L.dtype == JOLT_F16 ? 0 : 2), (long long)T * D, D,
+          dsc.off_G, H, T, D);
     }
-    if (s != JOLT_OK) return s;
-    if (b == 0) continue;
-    EncArgs ea;
-    memset(&ea, 0, sizeof(ea));
-    ea.X = Xu; ea.signs = signs + (size_t)u * D;
-    ea.H = H; ea.T = T; ea.D = D; ea.dtype = L.dtype; ea.b = b;
-    ea.blob = bl; ea.off_scale = dsc.off_scale; ea.off_codes = dsc.off_codes;
-    {
-      const double rs = 1.0 / sqrt((double)D);
-      ea.rs_hi = (float)rs;
-      ea.rs_lo = (float)(rs - (double)ea.rs_hi);
-    }
-    const __half* Ud16 = (const __half*)(wu + L.o_Ud16);
-    if (rT == T && rd == D) {
-      ea.mode = 2;
-    } else if (rT == T) {
-      // X~_h = Y16_h U_d16^T
-      ea.mode = 1; ea.K = rd;
-      ea.Kg = (const __half*)(wu + L.o_Y16); ea.k_hs = (long long)T * RD; ea.k_ld = RD;
-      ea.B16 = Ud16; ea.b_hs = 0; ea.b_ks = 1; ea.b_ds = RD;
-    } else {
-      // X~_h = U_T16 (G16_h U_d16^T)
-      ea.mode = 0; ea.K = rT;
-      ea.Kg = (const __half*)(wu + L.o_UT16) + (size_t)id * T * RT; ea.k_hs = 0; ea.k_ld = RT;
-      const __half* G16 = (const __half*)(wu + L.o_G16) + (size_t)id * H * RT * D;
-      if (rd == D) {
-        ea.B16 = G16; ea.b_hs = (long long)RT * D; ea.b_ks = D; ea.b_ds = 1;
-      } else {
-        float* Bh = (float*)(ws + (size_t)u * L.unit_bytes + L.o_W);
-        float* Blo = Bh + (size_t)H * rT * D;
-        enc_rows_kernel<<<dim3((rT * D + 255) / 256, H), 256, 0, st>>>(
-            G16, (long long)RT * rd, Ud16, RD, rT, rd, D, Bh, Blo);
-        JOLT_LAUNCH_CHECK();
-        ea.Bhi = Bh; ea.Blo = Blo; ea.b_hs = (long long)rT * D;
+    if (b > 0) {
+      EncArgs ea;
+      memset(&ea, 0, sizeof(ea));
+      ea.X = Xu; ea.signs = signs + (size_t)u * D;
+      ea.H = H; ea.T = T; ea.D = D; ea.dtype = L.dtype; ea.b = b;
+      ea.blob = bl; ea.off_scale = dsc.off_scale; ea.off_codes = dsc.off_codes;
+      {
+        const double rs = 1.0 / sqrt((double)D);
+        ea.rs_hi = (float)rs;
+        ea.rs_lo = (float)(rs - (double)ea.rs_hi);
       }
+      const __half* Ud16 = (const __half*)(wu + L.o_Ud16);
+      if (rT == T && rd == D) {
+        ea.mode = 2;
+      } else if (rT == T) {
+        // X~_h = Y16_h U_d16^T
+        ea.mode = 1; ea.K = rd;
+        ea.Kg = (const __half*)(wu + L.o_Y16); ea.k_hs = (long long)T * RD; ea.k_ld = RD;
+        ea.B16 = Ud16; ea.b_hs = 0; ea.b_ks = 1; ea.b_ds = RD;
+      } else {
+        // X~_h = U_T16 (G16_h U_d16^T)
+        ea.mode = 0; ea.K = rT;
+        ea.Kg = (const __half*)(wu + L.o_UT16) + (size_t)id * T * RT; ea.k_hs = 0; ea.k_ld = RT;
+        const __half* G16 = (const __half*)(wu + L.o_G16) + (size_t)id * H * RT * D;
+        if (rd == D) {
+          ea.B16 = G16; ea.b_hs = (long long)RT * D; ea.b_ks = D; ea.b_ds = 1;
+        } else {
+          float* Bh = (float*)(ws + (size_t)u * L.unit_bytes + L.o_W);
+          float* Blo = Bh + (size_t)H * rT * D;
+          RowsUnit& ru = rows.u[nrows++];
+          ru.G = G16; ru.g_hs = (long long)RT * rd; ru.Ud = Ud16; ru.ldu = RD;
+          ru.rT = rT; ru.rd = rd; ru.Bhi = Bh; ru.Blo = Blo;
+          ea.Bhi = Bh; ea.Blo = Blo; ea.b_hs = (long long)rT * D;
+        }
+      }
+      batch.u[nbatch++] = ea;
     }
-    batch.u[nbatch++] = ea;
-    if (nbatch == ENC_MAX_UNITS) {
+    if (nsec == ENC_MAX_UNITS) {
       jolt_status ls = flush();
       if (ls != JOLT_OK) return ls;
     }
   }
-  if (nbatch > 0) {
+  {
     jolt_status ls = flush();
     if (ls != JOLT_OK) return ls;
   }
