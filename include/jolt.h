@@ -210,6 +210,34 @@ jolt_status jolt_allocate_uniform(int n_units, int n_cand, const double* dist,
  */
 jolt_status jolt_set_sweep_events(void* start, void* stop);
 
+/*
+ * Modeled-error distortion table, an alternative to jolt_sweep_candidates
+ * that needs no pass over X ["A JoLT for the KV cache" verdict page, referee
+ * report on Section 4, Eq. (2): e ~ eps^2(b) tau; P5 Methodology 4: tail-mass
+ * accounting].  From the spectra of jolt_factor_group on the same ws:
+ *   tau(r_T, r_d) = sum_{i >= r_d} lambda_i              (r_T = T)
+ *                 = ||X||^2 - sum_{j < r_T} mu_j(r_d)    (r_T < T),
+ * lambda the feature eigenvalues (||X||^2 = their sum), mu the token
+ * eigenvalues of feature rank r_d; dist[u][cand] = eps2[ib] tau / ||X||^2
+ * (eps2 of b = 0 taken as 1; 0 for an all-zero unit).
+ *   eps2_host [cfg->n_b] f64 (host), e.g. from jolt_calibrate_eps2;
+ *   dist [n_units][n_cand] f64 (device).
+ */
+jolt_status jolt_model_candidates(const jolt_config* cfg, int n_units, const void* ws,
+                                  size_t ws_bytes, const double* eps2_host, double* dist,
+                                  void* stream);
+
+/*
+ * Calibration of eps^2(b) on a Gaussian round trip [same passage]: rows
+ * (device, n_rows x D fp32, D in {32, 64, 128}) are the caller's standard
+ * normal draws; each row goes through the per-row absmax quantizer with fp16
+ * scale of the codec, and eps2[ib] = sum ||y - Q_b(y)||^2 / sum ||y||^2
+ * (1 for b = 0).  bits_host [n_b] (host, each 0, 2, 4 or 8); scratch [8] f64
+ * and eps2 [n_b] f64 (device).
+ */
+jolt_status jolt_calibrate_eps2(const float* rows, int n_rows, int D, const int32_t* bits_host,
+                                int n_b, double* scratch, double* eps2, void* stream);
+
 /* Size in bytes of the serialized blob of candidate `cand` (flat index). */
 size_t jolt_blob_bytes(const jolt_config* cfg, int cand);
 

@@ -238,6 +238,30 @@ jolt_status jolt_set_sweep_events(void* start, void* stop) {
   return JOLT_OK;
 }
 
+jolt_status jolt_model_candidates(const jolt_config* cfg, int n_units, const void* ws,
+                                  size_t ws_bytes, const double* eps2_host, double* dist,
+                                  void* stream) {
+  Layout L;
+  jolt_status s = make_layout(cfg, &L);
+  if (s != JOLT_OK) return s;
+  if (n_units < 1 || n_units > 65535 || !eps2_host || !dist) return JOLT_ERR_INVALID;
+  if (!ws_ok(L, n_units, ws, ws_bytes)) return JOLT_ERR_WORKSPACE;
+  for (int i = 0; i < L.nb; ++i)
+    if (L.b[i] > 0 && !(eps2_host[i] >= 0.0)) return JOLT_ERR_INVALID;
+  return model_table_run(L, n_units, (const char*)ws, eps2_host, dist, S(stream));
+}
+
+jolt_status jolt_calibrate_eps2(const float* rows, int n_rows, int D, const int32_t* bits_host,
+                                int n_b, double* scratch, double* eps2, void* stream) {
+  if (!rows || n_rows < 1 || !(D == 32 || D == 64 || D == 128) || !bits_host || n_b < 1 ||
+      n_b > 4 || !scratch || !eps2)
+    return JOLT_ERR_INVALID;
+  for (int i = 0; i < n_b; ++i)
+    if (!(bits_host[i] == 0 || bits_host[i] == 2 || bits_host[i] == 4 || bits_host[i] == 8))
+      return JOLT_ERR_INVALID;
+  return eps2_run(rows, n_rows, D, bits_host, n_b, scratch, eps2, S(stream));
+}
+
 jolt_status jolt_refine(int n_units, int n_cand, const double* dist, const int64_t* cost,
                         int64_t budget, int32_t* choice, int32_t* n_swaps, void* stream) {
   if (n_units < 1 || n_cand < 1 || n_cand > JOLT_MAX_CAND || !dist || !cost || !choice)

@@ -184,6 +184,10 @@ jolt_status sweep_prep(const Layout& L, int n_units, const int8_t* signs, char* 
 jolt_status sweep_run(const Layout& L, int n_units, const void* X, const int8_t* signs,
                       char* ws, double* dist, int64_t* cost, cudaStream_t st,
                       float* part_override = nullptr);
+jolt_status model_table_run(const Layout& L, int n_units, const char* ws, const double* eps2_host,
+                            double* dist, cudaStream_t st);
+jolt_status eps2_run(const float* rows, int n, int D, const int* bits_host, int nb, double* scratch,
+                     double* eps2, cudaStream_t st);
 jolt_status refine_run(int n_units, int n_cand, const double* dist, const int64_t* cost,
                        int64_t budget, int32_t* choice, int32_t* n_swaps, cudaStream_t st);
 jolt_status uniform_run(int n_units, int n_cand, const double* dist, const int64_t* cost,

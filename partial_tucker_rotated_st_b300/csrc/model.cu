@@ -1,0 +1,144 @@
+// The modeled-error distortion table and its calibration.
+//
+// ["A JoLT for the KV cache" verdict page, referee report on Section 4,
+//  Eq. (2): the separable error model e ~ eps^2(b) tau that drives the
+//  allocation, with eps^2(b) calibrated on a Gaussian round-trip;
+//  "Technical Summary: A JOLT for the KV Cache", Methodology 4: tail-mass
+//  accounting, the omitted spectral tail counted as residual energy.]
+//
+// tau(r_T, r_d) = ||X - X~||^2 of the unrounded ST-HOSVD factors follows
+// from the spectra of the factor step alone:
+//   r_T = T:  sum_{i >= r_d} lambda_i            (feature tail)
+//   r_T < T:  ||X||^2 - sum_{j < r_T} mu_j(r_d)   (all energy minus the token
+//             energy captured), ||X||^2 = sum_i lambda_i = trace S_d,
+// so the table needs no pass over X.  D_model = eps^2(b) tau / ||X||^2 with
+// eps^2(0) = 1; 0 for an all-zero unit.
+#include "jolt_internal.cuh"
+
+namespace jolt {
+
+namespace {
+
+struct ModelArgs {
+  int nT, nd, nb, T, D, RT;
+  int rT[JOLT_MAX_GRID], rd[JOLT_MAX_GRID];
+  double eps2[4];
+  char* ws;
+  size_t ub, o_evd, o_tokev;
+  int ncand;
+};
+
+__global__ void model_table_kernel(ModelArgs a, double* dist) {
+  const int u = blockIdx.x;
+  const char* base = a.ws + (size_t)u * a.ub;
+  const float* lam = (const float*)(base + a.o_evd);
+  const float* mu = (const float*)(base + a.o_tokev);
+  __shared__ double xn;
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int i = 0; i < a.D; ++i) s += (double)lam[i];
+    xn = s;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < a.ncand; c += blockDim.x) {
+    const int ib = c % a.nb, id = (c / a.nb) % a.nd, iT = c / (a.nb * a.nd);
+    const int rT = a.rT[iT], rd = a.rd[id];
+    double tau = 0.0;
+    if (rT == a.T) {
+      for (int i = rd; i < a.D; ++i) tau += (double)lam[i];
+    } else {
+      double cap = 0.0;
+      for (int j = 0; j < rT; ++j) cap += (double)mu[id * a.RT + j];
+      tau = xn - cap;
+    }
+    if (tau < 0.0) tau = 0.0;   // the captured energy may round above the total
+    dist[(long long)u * a.ncand + c] = (xn > 0.0) ? a.eps2[ib] * tau / xn : 0.0;
+  }
+}
+
+// Per-row absmax round trip of Gaussian rows: numerator and denominator of
+// eps^2(b) accumulated in f64 (one warp per row, D = 32 * EPT).
+struct Rq {
+  float v[4];   // 1 / (2^(b-1) - 1), 0 for b = 0
+};
+
+template <int EPT>
+__global__ void eps2_kernel(const float* __restrict__ rows, int n, Rq rq, int nb, double* acc) {
+  constexpr int D = 32 * EPT;
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  double num[4] = {0.0, 0.0, 0.0, 0.0}, den = 0.0;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < n; r += warps) {
+    float y[EPT];
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      y[e] = rows[(long long)r * D + lane * EPT + e];
+      m = fmaxf(m, fabsf(y[e]));
+      den += (double)y[e] * y[e];
+    }
+    m = warp_max(m);
+    for (int ib = 0; ib < nb; ++ib) {
+      if (rq.v[ib] == 0.f) continue;
+      const float s = round_f16(m * rq.v[ib]);
+      const float inv = s > 0.f ? 1.f / s : 0.f;
+      double e2 = 0.0;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const float q = rintf(y[e] * inv);
+        const double d = (double)y[e] - (double)s * (double)q;
+        e2 += d * d;
+      }
+      num[ib] += e2;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    den += __shfl_xor_sync(0xffffffffu, den, o);
+    for (int ib = 0; ib < 4; ++ib) num[ib] += __shfl_xor_sync(0xffffffffu, num[ib], o);
+  }
+  if (lane == 0) {
+    atomicAdd(&acc[4], den);
+    for (int ib = 0; ib < nb; ++ib) atomicAdd(&acc[ib], num[ib]);
+  }
+}
+
+__global__ void eps2_finish_kernel(const double* acc, Rq rq, int nb, double* eps2) {
+  const int ib = threadIdx.x;
+  if (ib < nb) eps2[ib] = rq.v[ib] == 0.f ? 1.0 : (acc[4] > 0.0 ? acc[ib] / acc[4] : 0.0);
+}
+
+}  // namespace
+
+jolt_status model_table_run(const Layout& L, int U, const char* ws, const double* eps2_host,
+                            double* dist, cudaStream_t st) {
+  ModelArgs a;
+  a.nT = L.nT; a.nd = L.nd; a.nb = L.nb; a.T = L.T; a.D = L.D; a.RT = L.RT;
+  for (int i = 0; i < JOLT_MAX_GRID; ++i) { a.rT[i] = L.rT[i]; a.rd[i] = L.rd[i]; }
+  for (int i = 0; i < 4; ++i) a.eps2[i] = i < L.nb ? (L.b[i] == 0 ? 1.0 : eps2_host[i]) : 0.0;
+  a.ws = (char*)ws; a.ub = L.unit_bytes; a.o_evd = L.o_evd; a.o_tokev = L.o_tokev;
+  a.ncand = L.ncand;
+  model_table_kernel<<<U, 128, 0, st>>>(a, dist);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+jolt_status eps2_run(const float* rows, int n, int D, const int* bits_host, int nb, double* scratch,
+                     double* eps2, cudaStream_t st) {
+  Rq rq;
+  for (int i = 0; i < 4; ++i)
+    rq.v[i] = (i < nb && bits_host[i] > 0) ? 1.f / (float)((1 << (bits_host[i] - 1)) - 1) : 0.f;
+  JOLT_CUDA_TRY(cudaMemsetAsync(scratch, 0, 5 * sizeof(double), st));
+  const int blocks = (n + 7) / 8 < 1184 ? (n + 7) / 8 : 1184;
+  switch (D) {
+    case 128: eps2_kernel<4><<<blocks, 256, 0, st>>>(rows, n, rq, nb, scratch); break;
+    case 64: eps2_kernel<2><<<blocks, 256, 0, st>>>(rows, n, rq, nb, scratch); break;
+    case 32: eps2_kernel<1><<<blocks, 256, 0, st>>>(rows, n, rq, nb, scratch); break;
+    default: return JOLT_ERR_INVALID;
+  }
+  JOLT_LAUNCH_CHECK();
+  eps2_finish_kernel<<<1, 32, 0, st>>>(scratch, rq, nb, eps2);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+}  // namespace jolt

@@ -75,6 +75,12 @@ _SIG = {
                                              ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _P,
                                              _P, _P]),
     "jolt_set_sweep_events": (ctypes.c_int, [_P, _P]),
+    "jolt_model_candidates": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P,
+                                             ctypes.c_size_t, ctypes.POINTER(ctypes.c_double),
+                                             _P, _P]),
+    "jolt_calibrate_eps2": (ctypes.c_int, [_P, ctypes.c_int, ctypes.c_int,
+                                           ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _P, _P,
+                                           _P]),
     "jolt_blob_bytes": (ctypes.c_size_t, [ctypes.POINTER(JoltConfig), ctypes.c_int]),
     "jolt_encode": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P, _P,
                                    ctypes.c_size_t, _P, _P, ctypes.c_size_t,
@@ -231,6 +237,23 @@ def jolt_set_sweep_events(start=None, stop=None):
     if (start is not None and not a) or (stop is not None and not b):
         raise ValueError("record the events once before passing them")
     _check("jolt_set_sweep_events", lib().jolt_set_sweep_events(a, b))
+
+
+def jolt_model_candidates(cfg, n_units, ws, eps2_host: Sequence[float], dist, ws_bytes=None,
+                          stream=None):
+    """Modeled-error distortion table from the factor step's spectra."""
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    arr = (ctypes.c_double * max(1, len(eps2_host)))(*[float(e) for e in eps2_host])
+    _check("jolt_model_candidates", lib().jolt_model_candidates(
+        ctypes.byref(cfg), n_units, _ptr(ws), ws_bytes, arr, _ptr(dist), _stream(stream)))
+
+
+def jolt_calibrate_eps2(rows, bits: Sequence[int], scratch, eps2, stream=None):
+    """eps^2(b) of the codec's quantizer on Gaussian rows (n x D fp32, device)."""
+    arr = (ctypes.c_int32 * len(bits))(*[int(b) for b in bits])
+    _check("jolt_calibrate_eps2", lib().jolt_calibrate_eps2(
+        _ptr(rows), rows.shape[0], rows.shape[1], arr, len(bits), _ptr(scratch), _ptr(eps2),
+        _stream(stream)))
 
 
 def jolt_blob_bytes(cfg: JoltConfig, cand: int) -> int:

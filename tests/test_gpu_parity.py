@@ -318,3 +318,58 @@ def test_refine_and_uniform_allocators_bit_exact_on_gpu_tables(name):
             zref, sref = oj.allocate_uniform(r.dist, r.cost, bud, cand)
             assert list(out.cpu().numpy()) == list(zref)
             assert int(stt.item()) == (J.OK if sref == oj.ALLOC_OK else J.ERR_INFEASIBLE)
+
+
+def test_eps2_calibration_matches_oracle():
+    """eps^2(b) of the codec's quantizer on the same seeded Gaussian rows."""
+    import torch
+    from partial_tucker_rotated_st_b300 import jolt as J
+    rng = np.random.default_rng(20260101)
+    bits = [0, 2, 4, 8]
+    for D in (32, 128):
+        rows = rng.standard_normal((3000, D)).astype(np.float32)
+        ref = oj.eps2_calibrate(rows.astype(np.float64), bits)
+        scratch = torch.zeros(8, dtype=torch.float64, device="cuda")
+        eps2 = torch.zeros(len(bits), dtype=torch.float64, device="cuda")
+        J.jolt_calibrate_eps2(torch.from_numpy(rows).cuda(), bits, scratch, eps2)
+        torch.cuda.synchronize()
+        assert np.all(close(eps2.cpu().numpy(), ref, rel=1e-4, ab=0.0)), (D, eps2, ref)
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_model_table_matches_oracle_and_allocates(name):
+    """The modeled-error table from the GPU's spectra against the oracle's
+    from its own (f64) factorization, at the path's tolerance; the bisection
+    on the GPU's modeled table matches the oracle's bisection on it."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    w = SMALL[name]
+    xs, signs, sk = gh.host_inputs(w, range(w.n_units))
+    X, S, K = gh.to_device(w, xs, signs, sk)
+    cfg = codec.config_for(w)
+    U = w.n_units
+    enc = codec.Encoder(cfg, U)
+    enc.factor(X, K)
+    eps2 = [1.0, 0.59, 0.0138, 4.2e-5][: len(w.bits)] if list(w.bits) == [0, 2, 4, 8] else \
+        [1.0 if b == 0 else 4.0 ** (-b) for b in w.bits]
+    md = torch.zeros(U, enc.ncand, dtype=torch.float64, device="cuda")
+    J.jolt_model_candidates(cfg, U, enc.ws, eps2, md)
+    assert enc.status() == J.OK
+    md = md.cpu().numpy()
+    for i in range(U):
+        x64 = kvgen.unit_values_f64(w, xs[i])
+        s_ = None if sk is None else sk[i].astype(np.float64)
+        fac = oj.factorize(x64, w.rT, w.rd, w.token_mode, s_, w.power_iters)
+        ref = oj.model_dist_table(fac, float(np.sum(x64 * x64)), w.bits, eps2)
+        assert np.all(close(md[i], ref)), i
+    enc.sweep(X, S)   # the cost table
+    budget = int(w.budget_bytes * U // w.n_units)
+    ch = torch.zeros(U, dtype=torch.int32, device="cuda")
+    lam = torch.zeros(1, dtype=torch.float64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    J.jolt_allocate(U, enc.ncand, torch.from_numpy(md).cuda(), enc.cost, budget, cfg.align, ch,
+                    lam, st)
+    torch.cuda.synchronize()
+    zref, lref, sref = oj.allocate(md, enc.cost.cpu().numpy(), budget, cfg.align)
+    assert list(ch.cpu().numpy()) == list(zref) and float(lam.item()) == lref
