@@ -312,6 +312,8 @@ def run_ours(args):
            "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size() + Sh.numel()),
            "d2h_bytes_per_step": int(blob_h.numel())}
 
+    modeled = modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws)
+
     hbm, kind, pk = peaks()
     # dominant stage and its roofline
     dom = max(("factor", "sweep", "encode", "decode"), key=lambda s: per[s])
@@ -331,6 +333,7 @@ def run_ours(args):
             "wall_ms_per_step": 1e3 * wall / args.steps,
             "roofline": roof,
             "e2e": e2e,
+            "modeled_allocator": modeled,
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
     if rank == 0 and not args.no_cpu_baseline:
@@ -345,6 +348,59 @@ SWEEP_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tu
                          "csrc", "gram_tc.cu")
 SWEEP_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
                              "sweep_tc_kernel_mistral_t1024.md")
+
+
+def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):
+    """The modeled-error allocation path (no sweep): factor -> modeled table
+    from the spectra -> bisection -> serialize, timed like the main step; and
+    the measured distortion of its choice against the measured-table choice
+    (both from the last main step's tables, same budget)."""
+    rng = np.random.default_rng(20260101)
+    rows = torch.from_numpy(rng.standard_normal((8192, w.D)).astype(np.float32)).cuda()
+    scratch = torch.zeros(8, dtype=torch.float64, device="cuda")
+    eps2 = torch.zeros(len(w.bits), dtype=torch.float64, device="cuda")
+    J.jolt_calibrate_eps2(rows, list(w.bits), scratch, eps2)
+    eps2_h = eps2.cpu().tolist()
+    U = enc.U
+    md = torch.zeros(U, enc.ncand, dtype=torch.float64, device="cuda")
+    ch = torch.zeros(U, dtype=torch.int32, device="cuda")
+    lam = torch.zeros(1, dtype=torch.float64, device="cuda")
+    stt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dist_meas = enc.dist.clone()
+    cost = enc.cost.clone()
+    choice_meas = enc.choice.clone()
+
+    def step():
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        enc.factor(X, K)
+        J.jolt_model_candidates(enc.cfg, U, enc.ws, eps2_h, md)
+        J.jolt_allocate(U, enc.ncand, md, cost, budget, enc.cfg.align, ch, lam, stt)
+        ch_h = ch.cpu().tolist()
+        enc.serialize(X, S, ch_h)
+        e1.record(st)
+        return e0, e1
+
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1)
+    tot = 0.0
+    for _ in range(args.steps):
+        e0, e1 = step()
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) / 1e3
+        flush.fill_(1)
+    t = max_over_ranks(ws, tot / args.steps, "cuda")
+    dm, cm, zm = dist_meas.cpu().numpy(), cost.cpu().numpy(), choice_meas.cpu().numpy()
+    zmod = ch.cpu().numpy()
+    idx = np.arange(U)
+    return {"encode_gbs": ws * in_bytes / t / 1e9, "unit": "GB/s",
+            "eps2": eps2_h,
+            "measured_dist_sum_of_model_choice": float(dm[idx, zmod].sum()),
+            "measured_dist_sum_of_measured_choice": float(dm[idx, zm].sum()),
+            "bytes_model_choice": int(cm[idx, zmod].sum()),
+            "bytes_measured_choice": int(cm[idx, zm].sum())}
 
 
 def sweep_traffic(workload):

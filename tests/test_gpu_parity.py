@@ -362,7 +362,13 @@ def test_model_table_matches_oracle_and_allocates(name):
         s_ = None if sk is None else sk[i].astype(np.float64)
         fac = oj.factorize(x64, w.rT, w.rd, w.token_mode, s_, w.power_iters)
         ref = oj.model_dist_table(fac, float(np.sum(x64 * x64)), w.bits, eps2)
-        assert np.all(close(md[i], ref)), i
+        # for r_T < T the captured energy is a sum of r_T fp32 token
+        # eigenvalues, each off by a few units of roundoff of ||S_T|| <=
+        # ||X||^2 (Jacobi is backward stable), and tau = ||X||^2 - captured
+        # cancels: |dD| <= eps^2 * 4 r_T 2^-24 absolute
+        ok = close(md[i], ref, rel=REL, ab=4.0 * max(fac.rT_max, 1) * 2.0 ** -24)
+        j = int(np.argmax(np.abs(md[i] - ref)))
+        assert np.all(ok), (i, j, md[i][j], ref[j])
     enc.sweep(X, S)   # the cost table
     budget = int(w.budget_bytes * U // w.n_units)
     ch = torch.zeros(U, dtype=torch.int32, device="cuda")
