@@ -620,16 +620,15 @@ def sign_bits(signs: np.ndarray) -> bytes:
     return bytes(out)
 
 
-def encode_unit(X: np.ndarray, fac: Factors, signs: np.ndarray, rT: int, rd: int,
-                b: int, block: int, align: int = 256) -> bytes:
-    """Serialize candidate (rT, rd, b) of one unit (resolved ranks)."""
-    X = np.asarray(X, dtype=np.float64)
-    H, T, D = X.shape
-    if block != D:
-        raise ValueError("one quantization block is one row of D values")
+def pack_blob(H: int, T: int, D: int, rT: int, rd: int, b: int, block: int,
+              signs: np.ndarray, UT16: Optional[np.ndarray], G16: np.ndarray,
+              Ud16: Optional[np.ndarray], s: Optional[np.ndarray] = None,
+              codes: Optional[np.ndarray] = None, align: int = 256) -> bytes:
+    """Lay out given stored sections as one blob: the header fields, the sign
+    bits, then U_T, U_d, G, scales and packed codes at blob_layout's offsets
+    (U_T / U_d None for a whole mode; s, codes only for b > 0)."""
     lay = blob_layout(H, T, D, rT, rd, b, block, align)
     buf = bytearray(lay["bytes"])
-    UT16, G16, Ud16 = fac.stored(rT, rd)
     flags = (1 if UT16 is None else 0) | (2 if Ud16 is None else 0)
     struct.pack_into("<IIiiiiiiiI", buf, 0, MAGIC, VERSION, H, T, D, rT, rd, b, block, flags)
     struct.pack_into("<QQQQQQ", buf, 40, lay["UT"], lay["Ud"], lay["G"], lay["scale"],
@@ -642,12 +641,25 @@ def encode_unit(X: np.ndarray, fac: Factors, signs: np.ndarray, rT: int, rd: int
         buf[lay["Ud"]:lay["Ud"] + lay["Ud_bytes"]] = Ud16.astype(np.float16).tobytes()
     buf[lay["G"]:lay["G"] + lay["G_bytes"]] = G16.astype(np.float16).tobytes()
     if b > 0:
-        Xt = reconstruct(UT16, G16, Ud16)
-        Q = rotation_matrix(signs)
-        codes, s = quantize_blocks((X - Xt).reshape(H * T, D) @ Q.T, b)
         buf[lay["scale"]:lay["scale"] + lay["scale_bytes"]] = s.astype(np.float16).tobytes()
         buf[lay["codes"]:lay["codes"] + lay["codes_bytes"]] = pack_codes(codes, b)
     return bytes(buf)
+
+
+def encode_unit(X: np.ndarray, fac: Factors, signs: np.ndarray, rT: int, rd: int,
+                b: int, block: int, align: int = 256) -> bytes:
+    """Serialize candidate (rT, rd, b) of one unit (resolved ranks)."""
+    X = np.asarray(X, dtype=np.float64)
+    H, T, D = X.shape
+    if block != D:
+        raise ValueError("one quantization block is one row of D values")
+    UT16, G16, Ud16 = fac.stored(rT, rd)
+    s = codes = None
+    if b > 0:
+        Xt = reconstruct(UT16, G16, Ud16)
+        Q = rotation_matrix(signs)
+        codes, s = quantize_blocks((X - Xt).reshape(H * T, D) @ Q.T, b)
+    return pack_blob(H, T, D, rT, rd, b, block, signs, UT16, G16, Ud16, s, codes, align)
 
 
 def parse_header(blob: bytes) -> Dict[str, int]:
@@ -681,6 +693,51 @@ def decode_unit(blob: bytes) -> np.ndarray:
     s = arr(hd["scale"], n // hd["block"], (n // hd["block"],))
     codes = unpack_codes(blob[hd["codes"]:hd["codes"] + n * b // 8], n, b).reshape(H * T, D)
     return Xt + decode_residual(rotation_matrix(hd["signs"]), codes, s, (H, T, D))
+
+
+# --------------------------------------------------------------------------
+# attention over the rebuilt cache  [P1 Implementation notes: at inference the
+# low-rank part and the residual are rebuilt right before attention, ideally
+# in one fused kernel; P5 Results (deployment cost): a fused
+# reconstruction-and-attention kernel is the step that removes the per-step
+# rebuild]
+# --------------------------------------------------------------------------
+def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float) -> np.ndarray:
+    """Scaled dot-product attention of each head's queries over that head's
+    keys and values, float64:
+        O[h, i] = sum_t p[h, i, t] V[h, t],
+        p[h, i, :] = softmax_t(scale * q[h, i] . K[h, t])   (max subtracted).
+    q: [H, nq, D]; K, V: [H, T, D]; returns [H, nq, D]."""
+    q = np.asarray(q, dtype=np.float64)
+    S = scale * np.einsum("hid,htd->hit", q, np.asarray(K, dtype=np.float64))
+    S = S - S.max(axis=2, keepdims=True)
+    P = np.exp(S)
+    P = P / P.sum(axis=2, keepdims=True)
+    return np.einsum("hit,htd->hid", P, np.asarray(V, dtype=np.float64))
+
+
+def attend_group(q: np.ndarray, blob_K: bytes, blob_V: bytes, scale: float) -> np.ndarray:
+    """Attention of one group's queries over K^ and V^ rebuilt from the two
+    blobs (decode_unit of each, then attention())."""
+    return attention(q, decode_unit(blob_K), decode_unit(blob_V), scale)
+
+
+def random_blob(rng: np.random.Generator, H: int, T: int, D: int, rT: int, rd: int, b: int,
+                signs: np.ndarray, align: int = 256) -> bytes:
+    """A valid blob of candidate (rT, rd, b) whose sections are random draws
+    (no encoding): factor entries N(0, 1/r) for rank r, G entries N(0, 1) (so
+    that X~ has entries of unit variance), scales |N(0, 1)| / 2^(b-1) as
+    fp16, codes uniform on the b-bit range.  For attention tests at sizes the
+    oracle cannot factor."""
+    UT = None if rT == T else f16(rng.standard_normal((T, rT)) / np.sqrt(rT))
+    Ud = None if rd == D else f16(rng.standard_normal((D, rd)) / np.sqrt(rd))
+    G = f16(rng.standard_normal((H, rT, rd)))
+    s = codes = None
+    if b > 0:
+        n = H * T
+        s = f16(np.abs(rng.standard_normal(n)) / 2 ** (b - 1))
+        codes = rng.integers(-(2 ** (b - 1)), 2 ** (b - 1), size=(n, D))
+    return pack_blob(H, T, D, rT, rd, b, D, signs, UT, G, Ud, s, codes, align)
 
 
 # --------------------------------------------------------------------------

@@ -17,6 +17,12 @@ What pins which oracle function:
   cost_formula           hand arithmetic; fp16 footprint 268.4 MB [P5 Efficiency]
   blob_layout/codec      decode(encode) reproduces the scored candidate
   allocate               hand cases; brute force over all tiny allocations
+  attention              torch's scaled_dot_product_attention (CPU, float64);
+                         equal keys -> mean of V; T = 1 -> V; a dominant key;
+                         joint permutation of the tokens
+  pack_blob/random_blob  parse_header/decode_unit read back the drawn sections
+  attend_group           = attention on decode_unit of each blob; full ranks,
+                         b = 0 -> attention on the fp16-rounded tensors
 """
 import itertools
 import os
@@ -469,3 +475,71 @@ def test_model_dist_table_layout_and_scaling():
     assert np.allclose(t[0, 0, 1:], eps2[1:] * t[0, 0, 0], rtol=1e-15)
     assert abs(t[1, 0, 0] - fac.feat_eigvals[4:].sum() / nx) <= 1e-12
     assert np.all(jolt.model_dist_table(fac, 0.0, [0, 2, 4, 8], eps2) == 0.0)
+
+
+# ---------------------------------------------------------------- attention
+def test_attention_matches_library_sdpa():
+    import torch
+    rng = np.random.default_rng(11)
+    H, nq, T, D = 3, 5, 37, 16
+    q = rng.standard_normal((H, nq, D))
+    K = rng.standard_normal((H, T, D))
+    V = rng.standard_normal((H, T, D))
+    for scale in (1.0 / np.sqrt(D), 0.7):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q), torch.from_numpy(K), torch.from_numpy(V), scale=scale).numpy()
+        assert np.allclose(jolt.attention(q, K, V, scale), ref, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(12)
+    H, nq, T, D = 2, 3, 9, 8
+    q = rng.standard_normal((H, nq, D))
+    V = rng.standard_normal((H, T, D))
+    # every key equal: uniform weights, the mean value row
+    K = np.repeat(rng.standard_normal((H, 1, D)), T, axis=1)
+    assert np.allclose(jolt.attention(q, K, V, 0.5), np.repeat(V.mean(axis=1, keepdims=True),
+                                                               nq, axis=1), atol=1e-14)
+    # one token: its value row, whatever the score
+    assert np.allclose(jolt.attention(q, K[:, :1], V[:, :1], 3.0),
+                       np.repeat(V[:, :1], nq, axis=1), atol=1e-14)
+    # a key aligned with the query and a large scale: that token's value row
+    K = rng.standard_normal((H, T, D)) * 0.01
+    K[:, 4] = q[:, 0] * 10.0
+    out = jolt.attention(q[:, :1], K, V, 50.0)
+    assert np.allclose(out[:, 0], V[:, 4], atol=1e-12)
+    # tokens permuted jointly in K and V: the same output
+    K = rng.standard_normal((H, T, D))
+    perm = rng.permutation(T)
+    assert np.allclose(jolt.attention(q, K, V, 0.3), jolt.attention(q, K[:, perm], V[:, perm], 0.3),
+                       atol=1e-13)
+
+
+@pytest.mark.parametrize("rT,rd,b", [(5, 4, 4), (16, 32, 0), (16, 8, 8), (5, 32, 2)])
+def test_random_blob_sections_read_back(rT, rd, b):
+    rng = np.random.default_rng(rT * 100 + rd + b)
+    H, T, D = 3, 16, 32
+    signs = np.where(rng.random(D) < 0.5, -1, 1).astype(np.int8)
+    blob = jolt.random_blob(rng, H, T, D, rT, rd, b, signs)
+    hd = jolt.parse_header(blob)
+    assert (hd["H"], hd["T"], hd["D"], hd["rT"], hd["rd"], hd["b"]) == (H, T, D, rT, rd, b)
+    assert np.array_equal(hd["signs"], signs)
+    assert hd["bytes"] == len(blob) == jolt.blob_layout(H, T, D, rT, rd, b, D)["bytes"]
+    X = jolt.decode_unit(blob)
+    assert X.shape == (H, T, D) and np.all(np.isfinite(X))
+
+
+def test_attend_group_full_rank_no_residual_is_attention_on_fp16_tensors():
+    """Full ranks and b = 0 store G = X in fp16, so attention over the blobs
+    is attention over the fp16-rounded K and V."""
+    rng = np.random.default_rng(13)
+    Kx = rng.standard_normal((2, 16, 32))
+    Vx = rng.standard_normal((2, 16, 32))
+    signs = np.ones(32, dtype=np.int8)
+    blobs = []
+    for X in (Kx, Vx):
+        fac = jolt.factorize(X, (jolt.FULL,), (jolt.FULL,))
+        blobs.append(jolt.encode_unit(X, fac, signs, 16, 32, 0, 32))
+    q = rng.standard_normal((2, 3, 32))
+    ref = jolt.attention(q, jolt.f16(Kx), jolt.f16(Vx), 0.25)
+    assert np.allclose(jolt.attend_group(q, blobs[0], blobs[1], 0.25), ref, atol=1e-13)
