@@ -55,7 +55,10 @@ def peaks():
 
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 50 ms; the summary keeps the samples that
+    arrived between mark_start() and mark_end() (the timed region).  Entering
+    waits (up to 5 s) for the first sample, so the sampler is live before the
+    region starts."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -65,18 +68,28 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.span = (0, None)
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.perf_counter()
+            while not self.lines and self.proc.poll() is None and time.perf_counter() - t0 < 5.0:
+                time.sleep(0.01)
         except OSError:
             self.proc = None
         return self
+
+    def mark_start(self):
+        self.span = (len(self.lines), None)
+
+    def mark_end(self):
+        self.span = (self.span[0], len(self.lines))
 
     def _read(self):
         for line in self.proc.stdout:
@@ -93,7 +106,7 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in self.lines[self.span[0]:self.span[1]]:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -268,12 +281,14 @@ def run_ours(args):
     barrier(ws)
     n0 = J.jolt_launch_count()
     with ClockSampler(local) as clk:
+        clk.mark_start()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             desc = step(timers)
             flush.fill_(1)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
+        clk.mark_end()
     launches = (J.jolt_launch_count() - n0) // max(args.steps, 1)
     barrier(ws)
     per = {s: 0.0 for s in stages}
@@ -312,9 +327,10 @@ def run_ours(args):
            "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size() + Sh.numel()),
            "d2h_bytes_per_step": int(blob_h.numel())}
 
+    hbm, kind, pk = peaks()
+    attn = attention_bench(args, w, r.desc, enc, flush, st, hbm, kind)
     modeled = modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws)
 
-    hbm, kind, pk = peaks()
     # dominant stage and its roofline
     dom = max(("factor", "sweep", "encode", "decode"), key=lambda s: per[s])
     roof = roofline(w, sweep_kernel_s, hbm, kind, pk)
@@ -334,6 +350,7 @@ def run_ours(args):
             "roofline": roof,
             "e2e": e2e,
             "modeled_allocator": modeled,
+            "attention": attn,
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
     if rank == 0 and not args.no_cpu_baseline:
@@ -350,11 +367,77 @@ SWEEP_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profil
                              "sweep_tc_kernel_mistral_t1024.md")
 
 
+def attention_bench(args, w, desc, enc, flush, st, hbm, hbm_kind, nq=4):
+    """Attention of nq queries per head over every group's compressed K and V
+    (the blobs of the last encode), through jolt_attend, against
+    materializing the cache (jolt_decode to bf16) and running torch's
+    scaled_dot_product_attention on it.  L2 is flushed before every call.
+    Algorithmic bytes: the sections of every blob (U_T, U_d, G, scales,
+    codes) plus the queries and the outputs."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    G, H, T, D = len(desc) // 2, w.H, w.T, w.D
+    rng = np.random.default_rng(20260102)
+    q = torch.from_numpy(rng.standard_normal((G, H, nq, D)).astype(np.float32)).cuda()
+    scale = 1.0 / float(np.sqrt(D))
+    aws = torch.empty(J.jolt_attend_workspace_size(G, H, T, D, nq), dtype=torch.uint8,
+                      device="cuda")
+    out = torch.empty_like(q)
+    xhat = torch.empty(2 * G, H, T, D, dtype=torch.bfloat16, device="cuda")
+    qb = q.to(torch.bfloat16)
+
+    def fused():
+        codec.attend(desc, enc.blob, enc.stride, q, scale, out=out, ws=aws)
+
+    def materialize():
+        codec.decode(desc, enc.blob, enc.stride, J.BF16, out=xhat)
+        torch.nn.functional.scaled_dot_product_attention(qb, xhat[0::2], xhat[1::2], scale=scale)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+            flush.fill_(1)
+        tot = 0.0
+        for _ in range(args.steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1) / 1e3
+            flush.fill_(1)
+        return tot / args.steps
+
+    n0 = J.jolt_launch_count()
+    t = timed(fused)
+    launches = (J.jolt_launch_count() - n0) // (args.warmup + args.steps)
+    tm = timed(materialize)
+    sec = 0
+    for d in desc:
+        sec += (2 * T * d.rT if d.rT < T else 0) + (2 * D * d.rd if d.rd < D else 0)
+        sec += 2 * H * d.rT * d.rd
+        if d.b > 0:
+            sec += 2 * H * T + H * T * D * d.b // 8
+    alg = sec + 2 * q.numel() * 4
+    return {"ms": 1e3 * t, "queries_per_call": G * H * nq, "tokens": T, "nq_per_head": nq,
+            "launches_per_call": int(launches),
+            "roofline": {"kernel": "attend_chunk_kernel + attend_merge_kernel", "bound": "hbm",
+                         "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
+                         "frac": alg / t / 1e9 / hbm, "traffic": None,
+                         "bytes_algorithmic": int(alg), "peak_kind": hbm_kind},
+            "materialize_then_sdpa_ms": 1e3 * tm,
+            "speedup_vs_materialize": tm / t}
+
+
 def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):
     """The modeled-error allocation path (no sweep): factor -> modeled table
     from the spectra -> bisection -> serialize, timed like the main step; and
     the measured distortion of its choice against the measured-table choice
     (both from the last main step's tables, same budget)."""
+    import torch
+    from partial_tucker_rotated_st_b300 import jolt as J
     rng = np.random.default_rng(20260101)
     rows = torch.from_numpy(rng.standard_normal((8192, w.D)).astype(np.float32)).cuda()
     scratch = torch.zeros(8, dtype=torch.float64, device="cuda")
@@ -366,6 +449,7 @@ def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):
     ch = torch.zeros(U, dtype=torch.int32, device="cuda")
     lam = torch.zeros(1, dtype=torch.float64, device="cuda")
     stt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ch_host = torch.empty(U, dtype=torch.int32, pin_memory=True)
     dist_meas = enc.dist.clone()
     cost = enc.cost.clone()
     choice_meas = enc.choice.clone()
@@ -377,8 +461,9 @@ def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):
         enc.factor(X, K)
         J.jolt_model_candidates(enc.cfg, U, enc.ws, eps2_h, md)
         J.jolt_allocate(U, enc.ncand, md, cost, budget, enc.cfg.align, ch, lam, stt)
-        ch_h = ch.cpu().tolist()
-        enc.serialize(X, S, ch_h)
+        ch_host.copy_(ch, non_blocking=True)
+        st.synchronize()
+        enc.serialize(X, S, ch_host.tolist())
         e1.record(st)
         return e0, e1
 
@@ -454,7 +539,7 @@ def roofline(w, kernel_s, hbm, kind, pk):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--workload", default="mistral_t1024", choices=sorted(kvgen.WORKLOADS))

@@ -68,6 +68,8 @@ typedef enum {
 #define JOLT_MAX_GRID 8
 #define JOLT_MAX_CAND (JOLT_MAX_GRID * JOLT_MAX_GRID * 4)   /* largest candidate grid */
 #define JOLT_HEADER_BYTES 256
+#define JOLT_ATTN_MAX_Q 8          /* queries per head of one jolt_attend call */
+#define JOLT_ATTN_MAX_RANK 128     /* longest low-rank token row jolt_attend accepts */
 
 /*
  * Shape, candidate grid and options of one batch of units.
@@ -266,6 +268,37 @@ jolt_status jolt_encode(const jolt_config* cfg, int n_units, const void* X,
  */
 jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blob,
                         size_t blob_stride, void* xhat, jolt_dtype out_dtype, void* stream);
+
+/*
+ * Attention of each group's queries over its compressed K and V, with the
+ * rebuild fused in [P1 Implementation notes: rebuild the low-rank part and
+ * the residual right before attention, preferably in a fused kernel; P5
+ * Results (deployment cost): a fused reconstruction-and-attention kernel]:
+ *   O[g][h][i] = sum_t p_t V^[g][h][t],
+ *   p = softmax_t(scale * q[g][h][i] . K^[g][h][t]),
+ * with K^, V^ the decodes of blobs 2g and 2g+1 (jolt_decode's X^).  Neither
+ * is written to memory: the rotation moves onto the queries and the
+ * output, the low-rank part is scored through U_T / G rows, and the codes
+ * are read once per call.
+ *   n_groups     groups; blob slot 2g holds K, slot 2g+1 holds V of group g
+ *                (the unit order jolt_encode writes for K/V pairs)
+ *   desc         [2 * n_groups] blob descriptions (host); all with the same
+ *                H, T, D (D in {32, 64, 128}), block = D, truncated ranks
+ *                <= 64, sections aligned as jolt_encode lays them out
+ *   blob         [2 * n_groups] slots of blob_stride bytes (device)
+ *   q            [n_groups][H][nq][D] fp32 queries (device), 1 <= nq <=
+ *                JOLT_ATTN_MAX_Q (e.g. the query heads that share one KV head)
+ *   scale        softmax scale (1/sqrt(D) for standard attention)
+ *   ws, ws_bytes scratch of at least jolt_attend_workspace_size() bytes
+ *                (device; per-chunk partial results, no clearing needed)
+ *   out          [n_groups][H][nq][D] fp32 (device)
+ * Returns JOLT_ERR_INVALID for a bad shape, rank, alignment or pointer and
+ * JOLT_ERR_WORKSPACE for a short ws, before any launch.
+ */
+size_t jolt_attend_workspace_size(int n_groups, int H, int T, int D, int nq);
+jolt_status jolt_attend(int n_groups, const jolt_blob_desc* desc, const void* blob,
+                        size_t blob_stride, const float* q, int nq, float scale, void* ws,
+                        size_t ws_bytes, float* out, void* stream);
 
 /*
  * The same sweep as jolt_sweep_candidates, for callers that cannot allocate

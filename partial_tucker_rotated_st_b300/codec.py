@@ -105,3 +105,20 @@ def decode(desc: Sequence[J.JoltBlobDesc], blob: torch.Tensor, stride: int,
                           device=blob.device)
     J.jolt_decode(desc, blob, stride, out, out_dtype, stream=stream)
     return out
+
+
+def attend(desc: Sequence[J.JoltBlobDesc], blob: torch.Tensor, stride: int, q: torch.Tensor,
+           scale: float, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+           stream=None):
+    """Attention of q [groups][H][nq][D] (fp32) over the compressed K (even
+    blob slots) and V (odd slots) of each group; returns out (fp32, same
+    shape as q).  ws: scratch of jolt_attend_workspace_size bytes (allocated
+    here when None)."""
+    G, H, nq, D = q.shape
+    if ws is None:
+        ws = torch.empty(J.jolt_attend_workspace_size(G, H, desc[0].T, D, nq), dtype=torch.uint8,
+                         device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    J.jolt_attend(desc, blob, stride, q, nq, scale, ws, out, stream=stream)
+    return out

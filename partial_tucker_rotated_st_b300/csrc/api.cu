@@ -326,6 +326,44 @@ jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blo
   return decode_run(n_units, desc, (const char*)blob, blob_stride, xhat, out_dtype, S(stream));
 }
 
+size_t jolt_attend_workspace_size(int n_groups, int H, int T, int D, int nq) {
+  if (n_groups < 1 || H < 1 || T < 1 || D < 1 || nq < 1 || nq > JOLT_ATTN_MAX_Q) return 0;
+  return attend_ws_bytes(n_groups, H, T, D, nq);
+}
+
+jolt_status jolt_attend(int n_groups, const jolt_blob_desc* desc, const void* blob,
+                        size_t blob_stride, const float* q, int nq, float scale, void* ws,
+                        size_t ws_bytes, float* out, void* stream) {
+  if (n_groups < 1 || !desc || !blob || !q || !ws || !out) return JOLT_ERR_INVALID;
+  if (nq < 1 || nq > JOLT_ATTN_MAX_Q || !(scale == scale) || scale > 3.4e38f || scale < -3.4e38f)
+    return JOLT_ERR_INVALID;
+  if (((uintptr_t)blob % 256) || (blob_stride % 256) || ((uintptr_t)q % 16) ||
+      ((uintptr_t)out % 16) || ((uintptr_t)ws % 16))
+    return JOLT_ERR_INVALID;
+  const int H = desc[0].H, T = desc[0].T, D = desc[0].D;
+  if (H <= 0 || H > 65535 || T <= 0 || !(D == 32 || D == 64 || D == 128)) return JOLT_ERR_INVALID;
+  for (int u = 0; u < 2 * n_groups; ++u) {
+    const jolt_blob_desc& d = desc[u];
+    if (d.H != H || d.T != T || d.D != D || d.block != D) return JOLT_ERR_INVALID;
+    if (!(d.rT == T || (d.rT >= 1 && d.rT <= 64 && d.rT < T))) return JOLT_ERR_INVALID;
+    if (!(d.rd == D || (d.rd >= 1 && d.rd <= 64 && d.rd < D))) return JOLT_ERR_INVALID;
+    if (!(d.b == 0 || d.b == 2 || d.b == 4 || d.b == 8)) return JOLT_ERR_INVALID;
+    if (d.bytes > blob_stride) return JOLT_ERR_INVALID;
+    if (d.off_G + 2ull * H * d.rT * d.rd > d.bytes) return JOLT_ERR_INVALID;
+    if (d.rT < T && d.off_UT + 2ull * T * d.rT > d.bytes) return JOLT_ERR_INVALID;
+    if (d.rd < D && d.off_Ud + 2ull * D * d.rd > d.bytes) return JOLT_ERR_INVALID;
+    if ((d.off_UT % 4) || (d.off_Ud % 4) || (d.off_G % 4)) return JOLT_ERR_INVALID;
+    if (d.b > 0) {
+      if (d.off_scale + 2ull * H * T > d.bytes) return JOLT_ERR_INVALID;
+      if (d.off_codes + (unsigned long long)H * T * D * d.b / 8 > d.bytes) return JOLT_ERR_INVALID;
+      if ((d.off_scale % 2) || (d.off_codes % 16)) return JOLT_ERR_INVALID;
+    }
+  }
+  if (ws_bytes < attend_ws_bytes(n_groups, H, T, D, nq)) return JOLT_ERR_WORKSPACE;
+  return attend_run(n_groups, desc, (const char*)blob, blob_stride, q, nq, scale, (float*)ws, out,
+                    S(stream));
+}
+
 jolt_status jolt_read_status(const jolt_config* cfg, int n_units, void* ws, void* stream) {
   Layout L;
   jolt_status s = make_layout(cfg, &L);

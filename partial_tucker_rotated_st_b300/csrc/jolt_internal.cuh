@@ -201,6 +201,10 @@ jolt_status encode_run(const Layout& L, int n_units, const void* X, const int8_t
                        size_t blob_stride, jolt_blob_desc* desc, cudaStream_t st);
 jolt_status decode_run(int n_units, const jolt_blob_desc* desc, const char* blob,
                        size_t blob_stride, void* xhat, int out_dtype, cudaStream_t st);
+size_t attend_ws_bytes(int n_groups, int H, int T, int D, int nq);
+jolt_status attend_run(int n_groups, const jolt_blob_desc* desc, const char* blob,
+                       size_t stride, const float* q, int nq, float scale, float* part,
+                       float* out, cudaStream_t st);
 
 // ------------------------------------------------------------------ cost/blob
 // Candidate (iT, id, ib) <-> flat index, iT-major.

@@ -87,6 +87,11 @@ _SIG = {
                                    ctypes.POINTER(JoltBlobDesc), _P]),
     "jolt_decode": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(JoltBlobDesc), _P,
                                    ctypes.c_size_t, _P, ctypes.c_int, _P]),
+    "jolt_attend_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_int]),
+    "jolt_attend": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(JoltBlobDesc), _P,
+                                   ctypes.c_size_t, _P, ctypes.c_int, ctypes.c_float, _P,
+                                   ctypes.c_size_t, _P, _P]),
     "jolt_sweep_candidates_noalloc": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P,
                                                      _P, _P, ctypes.c_size_t, _P, _P, _P]),
     "jolt_noalloc_scratch_bytes": (ctypes.c_size_t, []),
@@ -277,6 +282,24 @@ def jolt_decode(desc: Sequence[JoltBlobDesc], blob, blob_stride, xhat, out_dtype
     arr = (JoltBlobDesc * n)(*desc)
     _check("jolt_decode", lib().jolt_decode(n, arr, _ptr(blob), blob_stride, _ptr(xhat),
                                             out_dtype, _stream(stream)))
+
+
+def jolt_attend_workspace_size(n_groups, H, T, D, nq) -> int:
+    return int(lib().jolt_attend_workspace_size(n_groups, H, T, D, nq))
+
+
+def jolt_attend(desc: Sequence[JoltBlobDesc], blob, blob_stride, q, nq, scale, ws, out,
+                ws_bytes=None, stream=None):
+    """Attention over the compressed K (even slots) and V (odd slots) of each
+    group; q and out are [groups][H][nq][D] fp32 device tensors."""
+    n = len(desc)
+    if n % 2:
+        raise ValueError("desc holds K, V pairs")
+    arr = (JoltBlobDesc * n)(*desc)
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("jolt_attend", lib().jolt_attend(n // 2, arr, _ptr(blob), blob_stride, _ptr(q), nq,
+                                            float(scale), _ptr(ws), ws_bytes, _ptr(out),
+                                            _stream(stream)))
 
 
 def jolt_read_status(cfg, n_units, ws, stream=None) -> int:

@@ -32,7 +32,7 @@ def header_functions():
 
 def test_library_exports_every_declared_symbol():
     names = header_functions()
-    assert len(names) == 18
+    assert len(names) == 20
     lib = ctypes.CDLL(J.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -116,3 +116,59 @@ def test_decode_rejects_inconsistent_descriptors():
 def test_status_strings():
     for s in range(8):
         assert J.jolt_status_string(s) and "unknown" not in J.jolt_status_string(s)
+
+
+def _attn_desc(H=4, T=300, D=128, rT=8, rd=16, b=4):
+    lay = oj.blob_layout(H, T, D, rT, rd, b, D)
+    d = J.JoltBlobDesc()
+    d.H, d.T, d.D, d.rT, d.rd, d.b, d.block = H, T, D, rT, rd, b, D
+    d.flags = (1 if rT == T else 0) | (2 if rd == D else 0)
+    d.off_UT, d.off_Ud, d.off_G = lay["UT"], lay["Ud"], lay["G"]
+    d.off_scale, d.off_codes, d.bytes = lay["scale"], lay["codes"], lay["bytes"]
+    return d
+
+
+def test_attend_workspace_size():
+    # per (group, head, chunk of 128 tokens): nq * (max, sum, z[D], cv[128]) floats
+    assert J.jolt_attend_workspace_size(3, 4, 300, 128, 4) == 3 * 4 * 3 * 4 * (2 + 128 + 128) * 4
+    assert J.jolt_attend_workspace_size(1, 1, 128, 32, 1) == 1 * (2 + 32 + 128) * 4
+    assert J.jolt_attend_workspace_size(1, 1, 128, 32, 9) == 0
+    assert J.jolt_attend_workspace_size(0, 1, 128, 32, 1) == 0
+
+
+@pytest.mark.parametrize("case", ["nq0", "nq9", "odd_blob", "stride", "mismatch", "rank",
+                                  "bits", "block", "codes_align", "ws", "null"])
+def test_attend_rejects_bad_arguments_before_launch(case):
+    good = [_attn_desc(), _attn_desc(rT=300, rd=32, b=2)]
+    desc = list(good)
+    dev = 1 << 40                       # never dereferenced: validation fails first
+    blob, stride, nq = dev, 1 << 20, 4
+    ws_bytes = J.jolt_attend_workspace_size(1, 4, 300, 128, 4)
+    q = out = ws = dev
+    want = J.ERR_INVALID
+    if case == "nq0":
+        nq = 0
+    elif case == "nq9":
+        nq = 9
+    elif case == "odd_blob":
+        blob = dev + 16
+    elif case == "stride":
+        stride = (1 << 20) + 16
+    elif case == "mismatch":
+        desc[1] = _attn_desc(T=256)
+    elif case == "rank":
+        desc[0] = _attn_desc(rT=80)
+    elif case == "bits":
+        desc[0] = _attn_desc(b=3)
+    elif case == "block":
+        desc[0].block = 64
+    elif case == "codes_align":
+        desc[0].off_codes += 8
+    elif case == "ws":
+        ws_bytes -= 4
+        want = J.ERR_WORKSPACE
+    elif case == "null":
+        q = None
+    arr = (J.JoltBlobDesc * 2)(*desc)
+    st = J.lib().jolt_attend(1, arr, blob, stride, q, nq, 0.125, ws, ws_bytes, out, None)
+    assert st == want

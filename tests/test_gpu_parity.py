@@ -379,3 +379,123 @@ def test_model_table_matches_oracle_and_allocates(name):
     torch.cuda.synchronize()
     zref, lref, sref = oj.allocate(md, enc.cost.cpu().numpy(), budget, cfg.align)
     assert list(ch.cpu().numpy()) == list(zref) and float(lam.item()) == lref
+
+
+# ------------------------------------------------ attention over the compressed cache
+def _desc_of(blob):
+    from partial_tucker_rotated_st_b300 import jolt as J
+    hd = oj.parse_header(blob)
+    d = J.JoltBlobDesc()
+    d.H, d.T, d.D, d.rT, d.rd, d.b = hd["H"], hd["T"], hd["D"], hd["rT"], hd["rd"], hd["b"]
+    d.block, d.flags = hd["block"], hd["flags"]
+    d.off_UT, d.off_Ud, d.off_G = hd["UT"], hd["Ud"], hd["G"]
+    d.off_scale, d.off_codes, d.bytes = hd["scale"], hd["codes"], hd["bytes"]
+    return d
+
+
+def _attend_gpu(blobs, q, scale):
+    """jolt_attend on blobs uploaded from the host (K in even, V in odd slots)."""
+    import torch
+    from partial_tucker_rotated_st_b300 import jolt as J
+    stride = -(-max(len(b) for b in blobs) // 256) * 256
+    host = np.zeros((len(blobs), stride), dtype=np.uint8)
+    for i, b in enumerate(blobs):
+        host[i, :len(b)] = np.frombuffer(b, dtype=np.uint8)
+    dev = torch.from_numpy(host).cuda()
+    G, H, nq, D = q.shape
+    T = oj.parse_header(blobs[0])["T"]
+    ws = torch.empty(J.jolt_attend_workspace_size(G, H, T, D, nq), dtype=torch.uint8, device="cuda")
+    qd = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32)).cuda()
+    out = torch.full((G, H, nq, D), float("nan"), dtype=torch.float32, device="cuda")
+    J.jolt_attend([_desc_of(b) for b in blobs], dev, stride, qd, nq, scale, ws, out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().astype(np.float64)
+
+
+def _check_attention(blobs, q, scale):
+    """Every output of the GPU against the oracle's attention over the two
+    decoded blobs of each group.  fp32 bound: a score sums at most
+    D + JOLT_ATTN_MAX_RANK products (the query-side coefficients as many
+    again), so |ds| <= 4 (D + 128) 2^-24 (1 + scale |q| |K^_t|); the output
+    moves by at most 2 max|ds| max|V^| through the softmax, plus the fp32
+    sums over T tokens and D + 128 back-projection terms, (T + D + 128)
+    2^-24 max|V^|.  Norm-wise the error must also stay below 1e-5."""
+    out = _attend_gpu(blobs, q, scale)
+    G, H, nq, D = q.shape
+    q64 = q.astype(np.float64)
+    for g in range(G):
+        Kh, Vh = oj.decode_unit(blobs[2 * g]), oj.decode_unit(blobs[2 * g + 1])
+        ref = oj.attention(q64[g], Kh, Vh, scale)
+        T = Kh.shape[1]
+        u = 2.0 ** -24
+        E = scale * np.max(np.linalg.norm(q64[g], axis=2)) * np.max(np.linalg.norm(Kh, axis=2))
+        vmax = np.max(np.abs(Vh))
+        tol = (2 * 4 * (D + 128) * u * (1 + E) + (T + D + 128) * u) * vmax
+        err = np.abs(out[g] - ref)
+        assert np.all(np.isfinite(out[g]))
+        j = np.unravel_index(np.argmax(err), err.shape)
+        assert err[j] <= tol, (g, j, out[g][j], ref[j], tol)
+        rel = np.linalg.norm(out[g] - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert rel <= 1e-5, (g, rel)
+
+
+# candidate (iT, id, ib) of K and V per round: every branch of the fused
+# rebuild (token rank truncated or whole, feature rank truncated or whole,
+# every bit width, b = 0)
+_ATT_CANDS = [(0, 0, 2), (-1, 0, 1), (1, -1, 3), (-1, -1, 0), (2, 1, 0), (0, -1, 2),
+              (-1, 1, 2), (1, 1, 1), (-1, -1, 3), (3, 2, 2), (-1, 2, 3), (2, 0, 1)]
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_attend_matches_oracle_on_oracle_blobs(name):
+    """The oracle serializes candidates of its own factors; the GPU attends
+    over those blobs; the oracle attends over their decodes."""
+    w, r = SMALL[name], gpu_run(name)
+    facs = oracle_tables(name)[1]
+    U = len(r.units)
+    rng = np.random.default_rng(31)
+    scale = 1.0 / np.sqrt(w.D)
+    for rnd, nq in enumerate((1, 3, 4, 8)):
+        blobs = []
+        for u in range(U):
+            iT, id_, ib = _ATT_CANDS[(rnd * U + u) % len(_ATT_CANDS)]
+            f = facs[u]
+            blobs.append(oj.encode_unit(r.X64[u], f, r.signs[u], f.rT_list[iT], f.rd_list[id_],
+                                        w.bits[ib], w.block))
+        q = rng.standard_normal((U // 2, w.H, nq, w.D)).astype(np.float32)
+        _check_attention(blobs, q, scale)
+
+
+def test_attend_full_size_random_blobs():
+    """mistral_t1024's shape and the bench's launch (8 groups of
+    [32, 1024, 128], 4 queries per head) on random blobs of mixed
+    candidates, every output against the oracle."""
+    w = kvgen.WORKLOADS["mistral_t1024"]
+    rng = np.random.default_rng(32)
+    rT = [oj.resolve(x, w.T) for x in w.rT]
+    rd = [oj.resolve(x, w.D) for x in w.rd]
+    blobs = []
+    for u in range(w.n_units):
+        signs = kvgen.make_signs(w, u)
+        blobs.append(oj.random_blob(rng, w.H, w.T, w.D, rT[rng.integers(len(rT))],
+                                    rd[rng.integers(len(rd))], w.bits[u % len(w.bits)], signs))
+    q = rng.standard_normal((w.n_groups, w.H, 4, w.D)).astype(np.float32)
+    _check_attention(blobs, q, 1.0 / np.sqrt(w.D))
+
+
+@pytest.mark.parametrize("T,D,nq,rT,rd,b", [(1, 64, 2, 1, 8, 4), (129, 32, 8, 5, 4, 2),
+                                            (257, 128, 5, 64, 128, 8), (200, 64, 1, 200, 64, 0)])
+def test_attend_edge_shapes(T, D, nq, rT, rd, b):
+    """One token; a last chunk of one token; an odd rank; whole modes."""
+    rng = np.random.default_rng(T + D)
+    H = 3
+    signs = np.where(rng.random(D) < 0.5, -1, 1).astype(np.int8)
+    blobs = [oj.random_blob(rng, H, T, D, rT, rd, b, signs),
+             oj.random_blob(rng, H, T, D, rT if rT < T else T, max(1, rd // 2) if rd < D else D,
+                            {0: 2, 2: 4, 4: 8, 8: 2}[b], signs[::-1].copy())]
+    q = rng.standard_normal((1, H, nq, D)).astype(np.float32)
+    _check_attention(blobs, q, 0.5 / np.sqrt(D))
+    # all-zero queries: uniform weights, the mean of V^ over the tokens
+    out = _attend_gpu(blobs, np.zeros_like(q), 1.0)
+    mean = oj.decode_unit(blobs[1]).mean(axis=1)
+    assert np.allclose(out[0], np.repeat(mean[:, None, :], nq, axis=1), rtol=1e-5, atol=1e-5)
