@@ -741,6 +741,106 @@ def random_blob(rng: np.random.Generator, H: int, T: int, D: int, rT: int, rd: i
 
 
 # --------------------------------------------------------------------------
+# admission of a new token block into an encoded unit  [P4 Implementation
+# notes: the Tucker factors are kept, X~ is rebuilt for each incoming token
+# block and only R = X - X~ is coded; P1 Implementation notes: integrate at
+# KV-cache admission time]
+# --------------------------------------------------------------------------
+PIVOT_DROP = 2.0 ** -40
+
+
+def cholesky_solve_drop(M: np.ndarray, rhs: np.ndarray) -> np.ndarray:
+    """Solve M u^T = rhs^T (M symmetric positive semidefinite, rhs rows are
+    right-hand sides) by the textbook Cholesky factorization M = L L^T.  A
+    pivot at most PIVOT_DROP * max diag(M) is dropped: its column of L is
+    zero and that coordinate of every solution is 0 (so a singular M gives
+    the solution restricted to the kept coordinates)."""
+    M = np.asarray(M, dtype=np.float64)
+    n = M.shape[0]
+    L = np.zeros((n, n))
+    keep = np.zeros(n, dtype=bool)
+    tol = PIVOT_DROP * (float(np.max(np.diag(M))) if n else 0.0)
+    for j in range(n):
+        d = M[j, j] - float(np.dot(L[j, :j], L[j, :j]))
+        if not d > tol:
+            continue
+        keep[j] = True
+        L[j, j] = np.sqrt(d)
+        for i in range(j + 1, n):
+            L[i, j] = (M[i, j] - float(np.dot(L[i, :j], L[j, :j]))) / L[j, j]
+    rhs = np.atleast_2d(np.asarray(rhs, dtype=np.float64))
+    out = np.zeros_like(rhs)
+    for r in range(rhs.shape[0]):
+        z = np.zeros(n)
+        for j in range(n):
+            if keep[j]:
+                z[j] = (rhs[r, j] - float(np.dot(L[j, :j], z[:j]))) / L[j, j]
+        u = np.zeros(n)
+        for j in range(n - 1, -1, -1):
+            if keep[j]:
+                u[j] = (z[j] - float(np.dot(L[j + 1:, j], u[j + 1:]))) / L[j, j]
+        out[r] = u
+    return out
+
+
+def fold_in(Y: np.ndarray, G: np.ndarray) -> np.ndarray:
+    """Token coordinates of new tokens under a fixed core: for each new token
+    t, u_t = argmin_u sum_h ||Y[h, t] - u G[h]||^2, i.e. the normal equations
+    u (sum_h G_h G_h^T) = sum_h Y[h, t] G_h^T.  For factors from an exact
+    ST-HOSVD this returns the token's own row of U_T (fold-in).
+    Y: [H, tau, r_d]; G: [H, r_T, r_d]; returns [tau, r_T]."""
+    Y = np.asarray(Y, dtype=np.float64)
+    G = np.asarray(G, dtype=np.float64)
+    M = np.einsum("hkj,hlj->kl", G, G)
+    rhs = np.einsum("htj,hkj->tk", Y, G)
+    return cholesky_solve_drop(M, rhs)
+
+
+def admit_unit(blob: bytes, X_new: np.ndarray, align: int = 256) -> bytes:
+    """The blob of the unit extended by tau new tokens X_new [H, tau, D],
+    with the unit's candidate, factors, signs and bit width kept:
+      Y = X_new U_d16 (X_new itself when r_d = D);
+      r_T < T: U_T gains the fp16 rows fold_in(Y, G16), G is unchanged;
+      r_T = T: G gains the rows fp16(Y) (the token mode stays whole);
+      the residual X_new - X~_new is rotated and quantized as in encode.
+    Every stored section of the old tokens is kept bit for bit."""
+    hd = parse_header(blob)
+    H, T, D, rT, rd, b = hd["H"], hd["T"], hd["D"], hd["rT"], hd["rd"], hd["b"]
+    X_new = np.asarray(X_new, dtype=np.float64)
+    tau = X_new.shape[1]
+    Tn = T + tau
+
+    def arr(off, n, shape):
+        return np.frombuffer(blob, dtype=np.float16, count=n, offset=off).astype(np.float64).reshape(shape)
+
+    UT16 = None if hd["flags"] & 1 else arr(hd["UT"], T * rT, (T, rT))
+    Ud16 = None if hd["flags"] & 2 else arr(hd["Ud"], D * rd, (D, rd))
+    G16 = arr(hd["G"], H * rT * rd, (H, rT, rd))
+    Y = X_new if Ud16 is None else np.einsum("htd,dj->htj", X_new, Ud16)
+    if UT16 is None:
+        G_new = f16(Y)
+        G_all = np.concatenate([G16, G_new], axis=1)
+        UT_all, rT_n = None, Tn
+        Xt_new = reconstruct(None, G_new, Ud16)
+    else:
+        u16 = f16(fold_in(Y, G16))
+        UT_all, G_all, rT_n = np.vstack([UT16, u16]), G16, rT
+        Xt_new = reconstruct(u16, G16, Ud16)
+    s_all = codes_all = None
+    if b > 0:
+        n_old = H * T * D
+        s_old = arr(hd["scale"], H * T, (H, T))
+        c_old = unpack_codes(blob[hd["codes"]:hd["codes"] + n_old * b // 8], n_old, b)
+        Q = rotation_matrix(hd["signs"])
+        c_new, s_new = quantize_blocks((X_new - Xt_new).reshape(H * tau, D) @ Q.T, b)
+        s_all = np.concatenate([s_old, s_new.reshape(H, tau)], axis=1).reshape(-1)
+        codes_all = np.concatenate([c_old.reshape(H, T, D), c_new.reshape(H, tau, D)],
+                                   axis=1).reshape(H * Tn, D)
+    return pack_blob(H, Tn, D, rT_n, rd, b, hd["block"], hd["signs"], UT_all, G_all, Ud16,
+                     s_all, codes_all, align)
+
+
+# --------------------------------------------------------------------------
 # whole encode pass over a set of units
 # --------------------------------------------------------------------------
 def candidate_list(rT_list, rd_list, bits=BITS):

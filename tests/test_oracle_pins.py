@@ -23,6 +23,15 @@ What pins which oracle function:
   pack_blob/random_blob  parse_header/decode_unit read back the drawn sections
   attend_group           = attention on decode_unit of each blob; full ranks,
                          b = 0 -> attention on the fp16-rounded tensors
+  cholesky_solve_drop    numpy.linalg.solve on SPD systems; hand case with
+                         zero pivots
+  fold_in                exact ST-HOSVD factors: a token's own U_T row
+  admit_unit             old tokens decode unchanged; tokens in the span of
+                         the stored factors give zero residual; two blocks
+                         admitted one after the other = one concatenated block;
+                         whole modes, b = 0: the new tokens decode to fp16(X);
+                         the rotated error of every new row is within half a
+                         quantization step
 """
 import itertools
 import os
@@ -543,3 +552,99 @@ def test_attend_group_full_rank_no_residual_is_attention_on_fp16_tensors():
     q = rng.standard_normal((2, 3, 32))
     ref = jolt.attention(q, jolt.f16(Kx), jolt.f16(Vx), 0.25)
     assert np.allclose(jolt.attend_group(q, blobs[0], blobs[1], 0.25), ref, atol=1e-13)
+
+
+# ---------------------------------------------------------------- admission
+def test_cholesky_solve_drop_matches_library_solve():
+    rng = np.random.default_rng(41)
+    for n in (1, 5, 17):
+        A = rng.standard_normal((n, n + 3))
+        M = A @ A.T
+        rhs = rng.standard_normal((4, n))
+        ref = np.linalg.solve(M, rhs.T).T
+        assert np.allclose(jolt.cholesky_solve_drop(M, rhs), ref, rtol=1e-10, atol=1e-12)
+
+
+def test_cholesky_solve_drop_zero_pivots():
+    M = np.diag([4.0, 0.0, 2.0, 0.0])
+    rhs = np.array([[8.0, 5.0, -2.0, 7.0]])
+    assert np.allclose(jolt.cholesky_solve_drop(M, rhs), np.array([[2.0, 0.0, -1.0, 0.0]]),
+                       rtol=0, atol=1e-15)
+    assert np.array_equal(jolt.cholesky_solve_drop(np.zeros((3, 3)), np.ones((1, 3))),
+                          np.zeros((1, 3)))
+
+
+def test_fold_in_returns_the_tokens_own_row():
+    """With the unrounded factors of an exact ST-HOSVD (U_T the leading
+    eigenvectors of the token Gram, G = U_T^T Y), the least-squares
+    coordinates of any existing token are its row of U_T."""
+    w = kvgen.custom_workload("tiny", H=4, T=40, D=32)
+    X = kvgen.make_unit_f64(w, 0)
+    fac = jolt.factorize(X, (8, jolt.FULL), (8, jolt.FULL))
+    for rd in fac.rd_list:
+        Y, UT, G = fac.Y[rd], fac.UT[rd][:, :8], fac.G[rd][:, :8, :]
+        u = jolt.fold_in(Y[:, 3:9, :], G)
+        assert np.allclose(u, UT[3:9], atol=1e-9), rd
+
+
+def _admit_case(rT, rd, b, T=24, tau=10, seed=0):
+    rng = np.random.default_rng(seed)
+    w = kvgen.custom_workload("tiny", H=3, T=T + tau, D=32)
+    X = kvgen.make_unit_f64(w, 1)
+    signs = kvgen.make_signs(w, 1)
+    fac = jolt.factorize(X[:, :T], (rT,), (rd,))
+    blob = jolt.encode_unit(X[:, :T], fac, signs, fac.rT_list[0], fac.rd_list[0], b, 32)
+    return blob, X[:, T:], rng
+
+
+@pytest.mark.parametrize("rT,rd,b", [(6, 8, 4), (jolt.FULL, 8, 2), (6, jolt.FULL, 8),
+                                     (jolt.FULL, jolt.FULL, 4), (4, 4, 0)])
+def test_admit_keeps_old_tokens_and_bounds_new_error(rT, rd, b):
+    blob, Xn, _ = _admit_case(rT, rd, b)
+    out = jolt.admit_unit(blob, Xn)
+    hd, ho = jolt.parse_header(blob), jolt.parse_header(out)
+    T, tau = hd["T"], Xn.shape[1]
+    assert ho["T"] == T + tau and ho["rd"] == hd["rd"] and ho["b"] == hd["b"]
+    assert ho["rT"] == (T + tau if hd["rT"] == T else hd["rT"])
+    assert np.array_equal(ho["signs"], hd["signs"])
+    old, new = jolt.decode_unit(blob), jolt.decode_unit(out)
+    assert np.array_equal(new[:, :T], old)
+    if b > 0:
+        # every new row's rotated error is within half its quantization step
+        Q = jolt.rotation_matrix(ho["signs"])
+        s = np.frombuffer(out, dtype=np.float16, count=3 * (T + tau),
+                          offset=ho["scale"]).astype(np.float64).reshape(3, T + tau)[:, T:]
+        err = np.abs((new[:, T:] - Xn).reshape(-1, 32) @ Q.T)
+        assert np.all(err <= 0.5 * s.reshape(-1, 1) * (1 + 1e-9) + 1e-12)
+
+
+def test_admit_whole_modes_no_residual_is_fp16_of_the_block():
+    blob, Xn, _ = _admit_case(jolt.FULL, jolt.FULL, 0)
+    out = jolt.admit_unit(blob, Xn)
+    assert np.array_equal(jolt.decode_unit(out)[:, 24:], jolt.f16(Xn))
+
+
+def test_admit_tokens_in_the_factor_span_have_zero_residual():
+    """r_d = D (Y = X): a block u* G16 in the span of the stored core gets
+    back u* as its U_T rows and a zero residual (zero scales)."""
+    blob, Xn, rng = _admit_case(6, jolt.FULL, 4)
+    hd = jolt.parse_header(blob)
+    G = np.frombuffer(blob, dtype=np.float16, count=3 * 6 * 32, offset=hd["G"]).astype(
+        np.float64).reshape(3, 6, 32)
+    u_star = jolt.f16(rng.standard_normal((5, 6)) * 0.1)
+    X_span = jolt.reconstruct(u_star, G, None)
+    out = jolt.admit_unit(blob, X_span)
+    ho = jolt.parse_header(out)
+    UT = np.frombuffer(out, dtype=np.float16, count=(24 + 5) * 6, offset=ho["UT"]).astype(
+        np.float64).reshape(29, 6)
+    assert np.array_equal(UT[24:], u_star)
+    s = np.frombuffer(out, dtype=np.float16, count=3 * 29, offset=ho["scale"]).reshape(3, 29)
+    assert np.all(s[:, 24:] == 0)
+
+
+@pytest.mark.parametrize("rT,rd,b", [(6, 8, 4), (jolt.FULL, 8, 2)])
+def test_admit_two_blocks_equals_one_block(rT, rd, b):
+    blob, Xn, _ = _admit_case(rT, rd, b)
+    one = jolt.admit_unit(blob, Xn)
+    two = jolt.admit_unit(jolt.admit_unit(blob, Xn[:, :4]), Xn[:, 4:])
+    assert one == two
