@@ -329,6 +329,7 @@ def run_ours(args):
 
     hbm, kind, pk = peaks()
     attn = attention_bench(args, w, r.desc, enc, flush, st, hbm, kind)
+    adm = admission_bench(args, w, r.desc, enc, flush, st)
     modeled = modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws)
 
     # dominant stage and its roofline
@@ -351,6 +352,7 @@ def run_ours(args):
             "e2e": e2e,
             "modeled_allocator": modeled,
             "attention": attn,
+            "admission": adm,
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
     if rank == 0 and not args.no_cpu_baseline:
@@ -429,6 +431,46 @@ def attention_bench(args, w, desc, enc, flush, st, hbm, hbm_kind, nq=4):
                          "bytes_algorithmic": int(alg), "peak_kind": hbm_kind},
             "materialize_then_sdpa_ms": 1e3 * tm,
             "speedup_vs_materialize": tm / t}
+
+
+def admission_bench(args, w, desc, enc, flush, st, tau=128):
+    """Admission of tau new tokens into every unit of the last encode
+    (jolt_admit: fold-in under the fixed factors, residual coded), timed
+    like the main step; GB/s of 16-bit-equivalent new-token input."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    U = len(desc)
+    rng = np.random.default_rng(20260103)
+    xn = kvgen.round_to_bf16(rng.standard_normal((U, w.H, tau, w.D)).astype(np.float32))
+    X = torch.from_numpy(xn.view(np.int16)).view(torch.bfloat16).cuda()
+    sout = codec.admit_stride(enc.stride, w.H, tau, w.D)
+    out = torch.empty(U, sout, dtype=torch.uint8, device="cuda")
+    aws = torch.empty(J.jolt_admit_workspace_size(U, w.H, tau, w.D), dtype=torch.uint8,
+                      device="cuda")
+
+    def call():
+        codec.admit(desc, enc.blob, enc.stride, X, out=out, ws=aws)
+
+    for _ in range(args.warmup):
+        call()
+        flush.fill_(1)
+    n0 = J.jolt_launch_count()
+    tot = 0.0
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        call()
+        e1.record(st)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) / 1e3
+        flush.fill_(1)
+    t = tot / args.steps
+    nbytes = U * w.H * tau * w.D * 2
+    return {"ms": 1e3 * t, "new_tokens": tau, "units": U, "unit": "GB/s",
+            "value": nbytes / t / 1e9,
+            "launches_per_call": int((J.jolt_launch_count() - n0) // max(args.steps, 1))}
 
 
 def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):

@@ -301,6 +301,35 @@ jolt_status jolt_attend(int n_groups, const jolt_blob_desc* desc, const void* bl
                         size_t ws_bytes, float* out, void* stream);
 
 /*
+ * Admission of a block of tau new tokens into encoded units [P4
+ * Implementation notes: the Tucker factors are kept, X~ is rebuilt for each
+ * incoming token block and only R = X - X~ is coded; P1 Implementation
+ * notes: at KV-cache admission time].  Each unit keeps its candidate
+ * (r_T, r_d, b), factors and signs:
+ *   Y = X_new U_d (X_new itself when r_d = D);
+ *   r_T < T: U_T gains the fp16 rows u_t solving (sum_h G_h G_h^T) u_t =
+ *            sum_h G_h Y[h][t]^T (the fold-in of the token under the fixed
+ *            core; Cholesky pivots at most 2^-40 max diag dropped, that
+ *            coordinate 0);
+ *   r_T = T: G gains the rows fp16(Y), and r_T becomes T + tau;
+ *   the residual of the new tokens is rotated and quantized as in
+ *   jolt_encode.  Every section of the old tokens is copied bit for bit.
+ *   desc_in, blob_in, stride_in   the units' blobs (as jolt_decode takes them)
+ *   X_new       [n_units][H][tau][D] in x_dtype (JOLT_F32 or JOLT_BF16), device
+ *   align       section alignment of the new blobs (cfg->align; power of two
+ *               >= 16)
+ *   ws          jolt_admit_workspace_size(n_units, H, tau, D) bytes, device
+ *   blob_out    [n_units] slots of stride_out bytes (device, not overlapping
+ *               blob_in); desc_out [n_units] filled on the host
+ * Returns JOLT_ERR_INVALID / JOLT_ERR_WORKSPACE before any launch.
+ */
+size_t jolt_admit_workspace_size(int n_units, int H, int tau, int D);
+jolt_status jolt_admit(int n_units, const jolt_blob_desc* desc_in, const void* blob_in,
+                       size_t stride_in, const void* X_new, jolt_dtype x_dtype, int tau,
+                       int align, void* ws, size_t ws_bytes, void* blob_out, size_t stride_out,
+                       jolt_blob_desc* desc_out, void* stream);
+
+/*
  * The same sweep as jolt_sweep_candidates, for callers that cannot allocate
  * device memory (code that runs where cudaMalloc is not allowed, or whose
  * memory belongs to an allocator it may not call at this point).  The pages

@@ -122,3 +122,28 @@ def attend(desc: Sequence[J.JoltBlobDesc], blob: torch.Tensor, stride: int, q: t
         out = torch.empty_like(q)
     J.jolt_attend(desc, blob, stride, q, nq, scale, ws, out, stream=stream)
     return out
+
+
+def admit_stride(stride_in: int, H: int, tau: int, D: int, align: int = 256) -> int:
+    """A blob slot size that holds any unit of slot size stride_in after tau
+    more tokens: the new U_T rows or core rows, scales and codes, plus a
+    section's alignment padding each."""
+    extra = H * tau * (2 * D + 2 + D) + 2 * 64 * tau + 6 * align
+    return -(-(stride_in + extra) // 256) * 256
+
+
+def admit(desc: Sequence[J.JoltBlobDesc], blob: torch.Tensor, stride: int, X_new: torch.Tensor,
+          align: int = 256, out: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None,
+          stream=None):
+    """Admit the new tokens X_new [units][H][tau][D] (bf16 or fp32) into the
+    encoded units; returns (blob_out, stride_out, desc_out)."""
+    U, H, tau, D = X_new.shape
+    dt = J.BF16 if X_new.dtype == torch.bfloat16 else J.F32
+    sout = admit_stride(stride, H, tau, D, align)
+    if out is None:
+        out = torch.empty(U, sout, dtype=torch.uint8, device=blob.device)
+    if ws is None:
+        ws = torch.empty(J.jolt_admit_workspace_size(U, H, tau, D), dtype=torch.uint8,
+                         device=blob.device)
+    d = J.jolt_admit(desc, blob, stride, X_new, dt, tau, align, ws, out, sout, stream=stream)
+    return out, sout, d

@@ -364,6 +364,51 @@ jolt_status jolt_attend(int n_groups, const jolt_blob_desc* desc, const void* bl
                     S(stream));
 }
 
+size_t jolt_admit_workspace_size(int n_units, int H, int tau, int D) {
+  if (n_units < 1 || H < 1 || tau < 1 || !(D == 32 || D == 64 || D == 128)) return 0;
+  return (size_t)n_units * admit_ws_unit_bytes(H, tau, D);
+}
+
+jolt_status jolt_admit(int n_units, const jolt_blob_desc* desc_in, const void* blob_in,
+                       size_t stride_in, const void* X_new, jolt_dtype x_dtype, int tau,
+                       int align, void* ws, size_t ws_bytes, void* blob_out, size_t stride_out,
+                       jolt_blob_desc* desc_out, void* stream) {
+  if (n_units < 1 || !desc_in || !blob_in || !X_new || !ws || !blob_out || !desc_out)
+    return JOLT_ERR_INVALID;
+  if (x_dtype != JOLT_F32 && x_dtype != JOLT_BF16) return JOLT_ERR_INVALID;
+  if (tau < 1 || align < 16 || align > 4096 || (align & (align - 1))) return JOLT_ERR_INVALID;
+  if (((uintptr_t)blob_in % 256) || (stride_in % 256) || ((uintptr_t)blob_out % 256) ||
+      (stride_out % 256) || ((uintptr_t)ws % 256) ||
+      ((uintptr_t)X_new % (x_dtype == JOLT_BF16 ? 2 : 4)))
+    return JOLT_ERR_INVALID;
+  const uintptr_t i0 = (uintptr_t)blob_in, i1 = i0 + (uintptr_t)n_units * stride_in;
+  const uintptr_t o0 = (uintptr_t)blob_out, o1 = o0 + (uintptr_t)n_units * stride_out;
+  if (i0 < o1 && o0 < i1) return JOLT_ERR_INVALID;
+  const int H = desc_in[0].H, T = desc_in[0].T, D = desc_in[0].D;
+  if (H <= 0 || H > 65535 || T <= 0 || !(D == 32 || D == 64 || D == 128)) return JOLT_ERR_INVALID;
+  if ((long long)T + tau > (1LL << 30)) return JOLT_ERR_INVALID;
+  for (int u = 0; u < n_units; ++u) {
+    const jolt_blob_desc& d = desc_in[u];
+    if (d.H != H || d.T != T || d.D != D || d.block != D) return JOLT_ERR_INVALID;
+    if (!(d.rT == T || (d.rT >= 1 && d.rT <= 64 && d.rT < T))) return JOLT_ERR_INVALID;
+    if (!(d.rd == D || (d.rd >= 1 && d.rd <= 64 && d.rd < D))) return JOLT_ERR_INVALID;
+    if (!(d.b == 0 || d.b == 2 || d.b == 4 || d.b == 8)) return JOLT_ERR_INVALID;
+    if (d.bytes > stride_in) return JOLT_ERR_INVALID;
+    if (d.off_G + 2ull * H * d.rT * d.rd > d.bytes) return JOLT_ERR_INVALID;
+    if (d.rT < T && d.off_UT + 2ull * T * d.rT > d.bytes) return JOLT_ERR_INVALID;
+    if (d.rd < D && d.off_Ud + 2ull * D * d.rd > d.bytes) return JOLT_ERR_INVALID;
+    if ((d.off_UT % 4) || (d.off_Ud % 4) || (d.off_G % 4)) return JOLT_ERR_INVALID;
+    if (d.b > 0) {
+      if (d.off_scale + 2ull * H * T > d.bytes) return JOLT_ERR_INVALID;
+      if (d.off_codes + (unsigned long long)H * T * D * d.b / 8 > d.bytes) return JOLT_ERR_INVALID;
+      if ((d.off_scale % 4) || (d.off_codes % 4)) return JOLT_ERR_INVALID;
+    }
+  }
+  if (ws_bytes < (size_t)n_units * admit_ws_unit_bytes(H, tau, D)) return JOLT_ERR_WORKSPACE;
+  return admit_run(n_units, desc_in, (const char*)blob_in, stride_in, X_new, x_dtype, tau, align,
+                   (char*)ws, (char*)blob_out, stride_out, desc_out, S(stream));
+}
+
 jolt_status jolt_read_status(const jolt_config* cfg, int n_units, void* ws, void* stream) {
   Layout L;
   jolt_status s = make_layout(cfg, &L);

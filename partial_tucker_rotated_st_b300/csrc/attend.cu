@@ -21,12 +21,18 @@
 // the back-projection being U_d G[h]^T cv (r_T < T) or U_d cv (r_T = T), with
 // an identity U_d when r_d = D.
 //
-// Tokens are split into chunks of ATT_CHUNK, one CTA per (chunk, head, group):
-// phase 1 scores the chunk's tokens (one thread per token), phase 2 turns them
-// into probabilities against the chunk's max, phase 3 accumulates cv and z
-// (a warp per 32 tokens, lanes over the feature / rank index), and the CTA
-// writes its max, sum, cv and z.  A second kernel merges the chunks
-// (flash-decoding) and applies the back-projection and the inverse rotation.
+// Three kernels.  attend_prep computes c and v~ once per (head, group).
+// attend_chunk takes ATT_CHUNK tokens per CTA: it first copies the chunk's
+// codes and low-rank rows of both blobs and the query coefficients into
+// shared memory with cp.async, so that the whole working set of the CTA is
+// in flight at once; then phase 1 scores the chunk's tokens (one thread per
+// token), phase 2 turns them into probabilities against the chunk's max,
+// phase 3 accumulates cv and z (a warp per 32 tokens, lanes over the feature
+// / rank index), and the CTA writes its max, sum, cv and z.  attend_merge
+// combines the chunks of each (head, group, query) (flash-decoding) and
+// applies the back-projection and the inverse rotation.
+#include <algorithm>
+
 #include "jolt_internal.cuh"
 
 namespace jolt {
@@ -36,6 +42,8 @@ namespace {
 constexpr int ATT_CHUNK = 128;     // tokens per CTA = threads per CTA
 constexpr int ATT_WARPS = ATT_CHUNK / 32;
 constexpr int ATT_MAX_G = 16;      // groups per launch
+constexpr int KM = JOLT_ATTN_MAX_RANK;
+constexpr int ATT_STAGE_RANK = 64; // low-rank rows up to this length go through shared memory
 
 struct AttUnit {
   int rT, rd, b, pad;
@@ -48,11 +56,17 @@ struct AttArgs {
   const char* blob;
   unsigned long long stride;
   const float* q;       // [groups][H][nq][D]
+  float* qc;            // [groups][H][KM + D][NQ]: c, then v~
   float* part;          // [groups][H][nch][rec]
   float* out;           // [groups][H][nq][D]
   int g0;               // first group of this launch
+  // attend_chunk's data region (bytes, 16-aligned offsets): K codes, K rows,
+  // V codes, V rows; `data` >= their end and >= the phase-3 partial sums
+  int o_kr, o_vc, o_vr, data;
   AttUnit k[ATT_MAX_G], v[ATT_MAX_G];
 };
+
+__host__ __device__ constexpr int nq_pad(int nq) { return nq <= 1 ? 1 : nq <= 2 ? 2 : nq <= 4 ? 4 : 8; }
 
 // b-bit code u as the float u - 2^(b-1), exactly: 2^23 + u has u in its low
 // mantissa bits.
@@ -60,12 +74,67 @@ __device__ __forceinline__ float code_f(unsigned u, float bias) {
   return __uint_as_float(0x4B000000u | u) - bias;
 }
 
-__device__ __forceinline__ size_t rec_floats(int nq, int D) {
-  return (size_t)nq * (2 + D + JOLT_ATTN_MAX_RANK);
+__host__ __device__ __forceinline__ size_t rec_floats(int nq, int D) {
+  return (size_t)nq * (2 + D + KM);
+}
+
+// Asynchronous copy of nbytes (even) from global to shared memory by nthr
+// threads, in 16-, 8- or 4-byte pieces as the source alignment allows (the
+// last piece reads only the bytes that remain); 2-byte aligned sources are
+// copied with plain loads.
+__device__ __forceinline__ void copy_async(void* dst, const void* src, int nbytes, int tid,
+                                           int nthr) {
+  char* d = (char*)dst;
+  const char* s = (const char*)src;
+  const uintptr_t al = (uintptr_t)src;
+  if ((al & 15) == 0) {
+    for (int p = tid; p * 16 < nbytes; p += nthr) {
+      const int rem = nbytes - p * 16;
+      const uint32_t sd = (uint32_t)__cvta_generic_to_shared(d + p * 16);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sd), "l"(s + p * 16),
+                   "r"(rem < 16 ? rem : 16) : "memory");
+    }
+  } else if ((al & 7) == 0) {
+    for (int p = tid; p * 8 < nbytes; p += nthr) {
+      const int rem = nbytes - p * 8;
+      const uint32_t sd = (uint32_t)__cvta_generic_to_shared(d + p * 8);
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(sd), "l"(s + p * 8),
+                   "r"(rem < 8 ? rem : 8) : "memory");
+    }
+  } else if ((al & 3) == 0) {
+    for (int p = tid; p * 4 < nbytes; p += nthr) {
+      const int rem = nbytes - p * 4;
+      const uint32_t sd = (uint32_t)__cvta_generic_to_shared(d + p * 4);
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(sd), "l"(s + p * 4),
+                   "r"(rem < 4 ? rem : 4) : "memory");
+    }
+  } else {
+    for (int p = tid; p * 2 < nbytes; p += nthr)
+      reinterpret_cast<__half*>(d)[p] = reinterpret_cast<const __half*>(s)[p];
+  }
+}
+
+// NQ consecutive floats of shared memory (16-byte aligned for NQ >= 4) into
+// registers with vector loads.
+template <int NQ>
+__device__ __forceinline__ void load_q(const float* p, float (&o)[NQ]) {
+  if constexpr (NQ >= 4) {
+#pragma unroll
+    for (int c = 0; c < NQ / 4; ++c) {
+      const float4 v = reinterpret_cast<const float4*>(p)[c];
+      o[4 * c] = v.x; o[4 * c + 1] = v.y; o[4 * c + 2] = v.z; o[4 * c + 3] = v.w;
+    }
+  } else if constexpr (NQ == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    o[0] = v.x; o[1] = v.y;
+  } else {
+    o[0] = p[0];
+  }
 }
 
 // One token's residual dot products sum_d v~_i[d] (u_d - 2^(b-1)) for every
-// query, the codes row read as 32-bit words (B bits per code).
+// query, the codes row read as 32-bit words (B bits per code), all loads
+// issued before the arithmetic.
 template <int D, int NQ, int B>
 __device__ __forceinline__ void res_dots(const uint32_t* __restrict__ row,
                                          const float* __restrict__ vt, float (&r)[NQ]) {
@@ -73,36 +142,30 @@ __device__ __forceinline__ void res_dots(const uint32_t* __restrict__ row,
   constexpr int NW = D * B / 32;           // words per row
   constexpr unsigned MASK = (1u << B) - 1u;
   const float bias = 8388608.0f + (float)(1 << (B - 1));
-#pragma unroll
-  for (int i = 0; i < NQ; ++i) r[i] = 0.f;
+  uint32_t wd[NW];
   if constexpr (NW % 4 == 0) {
-#pragma unroll 2
+#pragma unroll
     for (int w4 = 0; w4 < NW / 4; ++w4) {
-      const uint4 wv = reinterpret_cast<const uint4*>(row)[w4];
-      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-          const int d = (w4 * 4 + c) * PER + j;
-          const float f = code_f((ws[c] >> (j * B)) & MASK, bias);
-#pragma unroll
-          for (int i = 0; i < NQ; ++i) r[i] = fmaf(vt[d * NQ + i], f, r[i]);
-        }
+      const uint4 v = reinterpret_cast<const uint4*>(row)[w4];
+      wd[4 * w4] = v.x; wd[4 * w4 + 1] = v.y; wd[4 * w4 + 2] = v.z; wd[4 * w4 + 3] = v.w;
     }
   } else {
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const uint32_t wd = row[w];
-#pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const int d = w * PER + j;
-        const float f = code_f((wd >> (j * B)) & MASK, bias);
-#pragma unroll
-        for (int i = 0; i < NQ; ++i) r[i] = fmaf(vt[d * NQ + i], f, r[i]);
-      }
-    }
+    for (int w = 0; w < NW; ++w) wd[w] = row[w];
   }
+#pragma unroll
+  for (int i = 0; i < NQ; ++i) r[i] = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int d = w * PER + j;
+      const float f = code_f((wd[w] >> (j * B)) & MASK, bias);
+      float v[NQ];
+      load_q<NQ>(vt + d * NQ, v);
+#pragma unroll
+      for (int i = 0; i < NQ; ++i) r[i] = fmaf(v[i], f, r[i]);
+    }
 }
 
 // z[i][e] += ps[i] * (u - 2^(b-1)) for this lane's EPT codes of one row.
@@ -122,115 +185,163 @@ __device__ __forceinline__ void res_accum(const uint32_t* __restrict__ row, int 
   }
 }
 
+// n halves from global to shared memory, every load independent.
+__device__ __forceinline__ void stage_halves(__half* dst, const __half* __restrict__ src, int n,
+                                             int tid, int nthr) {
+#pragma unroll 8
+  for (int i = tid; i < n; i += nthr) dst[i] = src[i];
+}
+
+__device__ __forceinline__ float sign_of(const unsigned char* sb, int d) {
+  return ((sb[d >> 3] >> (d & 7)) & 1) ? -1.f : 1.f;
+}
+
+// Query coefficients of the K blob for one (head, group): c (score weights
+// of the low-rank row R[t]) and v~ (the rotated query).
+template <int EPT, int NQ>
+__global__ void __launch_bounds__(128) attend_prep_kernel(AttArgs a) {
+  constexpr int D = 32 * EPT;
+  __shared__ float vq[NQ][D], wq[NQ][KM];
+  __shared__ __half st_Ud[D * 64], st_G[64 * (KM > D ? KM : D)];
+  const int h = blockIdx.x, gl = blockIdx.y, g = a.g0 + gl;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int T = a.T, H = a.H, nq = a.nq;
+  const AttUnit ku = a.k[gl];
+  const char* kb = a.blob + (unsigned long long)(2 * g) * a.stride;
+  const bool kfT = (ku.rT == T), kfD = (ku.rd == D);
+  const int Kk = kfT ? ku.rd : ku.rT;
+  float* qc = a.qc + ((size_t)g * H + h) * (KM + D) * NQ;
+  const float* qg = a.q + ((size_t)g * H + h) * nq * D;
+  for (int x = tid; x < NQ * D; x += 128) vq[x / D][x % D] = (x / D) < nq ? qg[x] : 0.f;
+  if (!kfD) stage_halves(st_Ud, (const __half*)(kb + ku.off_Ud), D * ku.rd, tid, 128);
+  if (!kfT)
+    stage_halves(st_G, (const __half*)(kb + ku.off_G) + (size_t)h * ku.rT * ku.rd,
+                 ku.rT * ku.rd, tid, 128);
+  __syncthreads();
+  // w = U_d^T v (or v)
+  for (int x = tid; x < NQ * ku.rd; x += 128) {
+    const int i = x / ku.rd, j = x % ku.rd;
+    float s = 0.f;
+    if (kfD) {
+      s = vq[i][j];
+    } else {
+#pragma unroll 8
+      for (int d = 0; d < D; ++d) s = fmaf(__half2float(st_Ud[d * ku.rd + j]), vq[i][d], s);
+    }
+    wq[i][j] = s;
+  }
+  __syncthreads();
+  // c = G[h] w (r_T < T) or w (r_T = T)
+  for (int x = tid; x < NQ * Kk; x += 128) {
+    const int i = x / Kk, k = x % Kk;
+    float s;
+    if (kfT) {
+      s = wq[i][k];
+    } else {
+      s = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < ku.rd; ++j) s = fmaf(__half2float(st_G[k * ku.rd + j]), wq[i][j], s);
+    }
+    qc[k * NQ + i] = s;
+  }
+  // v~ = H_D diag(sigma) v / sqrt(D), a warp per query
+  if (ku.b > 0) {
+    const unsigned char* sb = (const unsigned char*)kb + 88;
+    const float rs = rsqrtf((float)D);
+    for (int i = w; i < NQ; i += 4) {
+      float v[EPT];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) v[e] = sign_of(sb, lane * EPT + e) * vq[i][lane * EPT + e];
+      fwht_row<EPT>(v, lane);
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) qc[(KM + lane * EPT + e) * NQ + i] = v[e] * rs;
+    }
+  }
+}
+
 template <int EPT, int NQ>
 __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
   constexpr int D = 32 * EPT;
-  constexpr int KM = JOLT_ATTN_MAX_RANK;
   extern __shared__ __align__(16) float asm_[];
-  float* vq = asm_;                       // [NQ][D]   queries
-  float* wq = vq + NQ * D;                // [NQ][KM]  U_d^T v
-  float* cq = wq + NQ * KM;               // [KM][NQ]  score coefficients of R[t]
-  float* vt = cq + KM * NQ;               // [D][NQ]   rotated queries v~
-  float* sc = vt + D * NQ;                // [CHUNK][NQ] scores, then p
-  float* red = sc + ATT_CHUNK * NQ;       // [WARPS][NQ][D + KM]
-  float* stat = red + ATT_WARPS * NQ * (D + KM);   // [2][NQ] max, sum
+  float* qcs = asm_;                      // [KM + D][NQ]  c, then v~
+  float* sc = qcs + (KM + D) * NQ;        // [CHUNK][NQ]   scores, then p
+  float* stat = sc + ATT_CHUNK * NQ;      // [2][8]        max, sum
+  float* sv = stat + 16;                  // [CHUNK]       V scales
+  char* data = reinterpret_cast<char*>(sv + ATT_CHUNK);   // codes and rows; later the partials
   const int chunk = blockIdx.x, h = blockIdx.y, gl = blockIdx.z;
   const int g = a.g0 + gl;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int T = a.T, H = a.H, nq = a.nq;
-  const int t0 = chunk * ATT_CHUNK;
+  const int t0 = chunk * ATT_CHUNK, t = t0 + tid;
+  const int n = min(ATT_CHUNK, T - t0);
   const AttUnit ku = a.k[gl], vu = a.v[gl];
   const char* kb = a.blob + (unsigned long long)(2 * g) * a.stride;
   const char* vb = a.blob + (unsigned long long)(2 * g + 1) * a.stride;
+  const bool kfT = (ku.rT == T), vfT = (vu.rT == T);
+  const int Kk = kfT ? ku.rd : ku.rT, Kv = vfT ? vu.rd : vu.rT;
+  const bool kst = Kk <= ATT_STAGE_RANK, vst = Kv <= ATT_STAGE_RANK;
+  const __half* kR = kfT ? (const __half*)(kb + ku.off_G) + ((size_t)h * T + t0) * ku.rd
+                         : (const __half*)(kb + ku.off_UT) + (size_t)t0 * ku.rT;
+  const __half* vR = vfT ? (const __half*)(vb + vu.off_G) + ((size_t)h * T + t0) * vu.rd
+                         : (const __half*)(vb + vu.off_UT) + (size_t)t0 * vu.rT;
+  const size_t kcb = (size_t)D * ku.b / 8, vcb = (size_t)D * vu.b / 8;   // code bytes per row
 
-  // ---- queries and their coefficients for the K blob
-  const float* qg = a.q + ((size_t)g * H + h) * nq * D;
-  for (int x = tid; x < NQ * D; x += ATT_CHUNK) {
-    const int i = x / D;
-    vq[x] = i < nq ? qg[x] : 0.f;
-  }
-  __syncthreads();
-  const bool kfT = (ku.rT == T), kfD = (ku.rd == D);
-  const int Kk = kfT ? ku.rd : ku.rT;
-  {
-    const __half* Ud = (const __half*)(kb + ku.off_Ud);
-    for (int x = tid; x < NQ * ku.rd; x += ATT_CHUNK) {
-      const int i = x / ku.rd, j = x % ku.rd;
-      float s = 0.f;
-      if (kfD) {
-        s = vq[i * D + j];
-      } else {
-        for (int d = 0; d < D; ++d) s = fmaf(__half2float(Ud[d * ku.rd + j]), vq[i * D + d], s);
-      }
-      wq[i * KM + j] = s;
-    }
-  }
-  __syncthreads();
-  if (kfT) {
-    for (int x = tid; x < NQ * Kk; x += ATT_CHUNK) {
-      const int i = x / Kk, k = x % Kk;
-      cq[k * NQ + i] = wq[i * KM + k];
-    }
-  } else {
-    const __half* Gh = (const __half*)(kb + ku.off_G) + (size_t)h * ku.rT * ku.rd;
-    for (int x = tid; x < NQ * Kk; x += ATT_CHUNK) {
-      const int i = x / Kk, k = x % Kk;
-      float s = 0.f;
-      for (int j = 0; j < ku.rd; ++j) s = fmaf(__half2float(Gh[k * ku.rd + j]), wq[i * KM + j], s);
-      cq[k * NQ + i] = s;
-    }
-  }
-  if (ku.b > 0) {
-    const unsigned char* sb = (const unsigned char*)kb + 88;
-    const float rs = rsqrtf((float)D);
-    for (int i = w; i < NQ; i += ATT_WARPS) {
-      float v[EPT];
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        const int d = lane * EPT + e;
-        v[e] = (((sb[d >> 3] >> (d & 7)) & 1) ? -1.f : 1.f) * vq[i * D + d];
-      }
-      fwht_row<EPT>(v, lane);
-#pragma unroll
-      for (int e = 0; e < EPT; ++e) vt[(lane * EPT + e) * NQ + i] = v[e] * rs;
-    }
-  }
+  // ---- everything the CTA reads, in flight at once
+  copy_async(qcs, a.qc + ((size_t)g * H + h) * (KM + D) * NQ, (KM + D) * NQ * 4, tid, ATT_CHUNK);
+  if (ku.b > 0)
+    copy_async(data, kb + ku.off_codes + ((size_t)h * T + t0) * kcb, (int)(n * kcb), tid,
+               ATT_CHUNK);
+  if (kst) copy_async(data + a.o_kr, kR, n * Kk * 2, tid, ATT_CHUNK);
+  if (vu.b > 0)
+    copy_async(data + a.o_vc, vb + vu.off_codes + ((size_t)h * T + t0) * vcb, (int)(n * vcb), tid,
+               ATT_CHUNK);
+  if (vst) copy_async(data + a.o_vr, vR, n * Kv * 2, tid, ATT_CHUNK);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const float ks = (ku.b > 0 && t < T)
+                       ? __half2float(((const __half*)(kb + ku.off_scale))[(size_t)h * T + t]) : 0.f;
+  sv[tid] = (vu.b > 0 && t < T)
+                ? __half2float(((const __half*)(vb + vu.off_scale))[(size_t)h * T + t]) : 0.f;
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
   // ---- phase 1: one thread per token, the scores of every query
   {
-    const int t = t0 + tid;
     float acc[NQ];
 #pragma unroll
     for (int i = 0; i < NQ; ++i) acc[i] = 0.f;
     if (t < T) {
-      const __half* R = kfT ? (const __half*)(kb + ku.off_G) + ((size_t)h * T + t) * ku.rd
-                            : (const __half*)(kb + ku.off_UT) + (size_t)t * ku.rT;
+      const __half* R = kst ? reinterpret_cast<const __half*>(data + a.o_kr) + (size_t)tid * Kk
+                            : kR + (size_t)tid * Kk;
       if ((Kk & 1) == 0) {
         const __half2* R2 = reinterpret_cast<const __half2*>(R);
+#pragma unroll 8
         for (int k2 = 0; k2 < Kk / 2; ++k2) {
           const float2 r = __half22float2(R2[k2]);
+          float c0[NQ], c1[NQ];
+          load_q<NQ>(qcs + 2 * k2 * NQ, c0);
+          load_q<NQ>(qcs + (2 * k2 + 1) * NQ, c1);
 #pragma unroll
-          for (int i = 0; i < NQ; ++i)
-            acc[i] = fmaf(r.y, cq[(2 * k2 + 1) * NQ + i], fmaf(r.x, cq[2 * k2 * NQ + i], acc[i]));
+          for (int i = 0; i < NQ; ++i) acc[i] = fmaf(r.y, c1[i], fmaf(r.x, c0[i], acc[i]));
         }
       } else {
+#pragma unroll 8
         for (int k = 0; k < Kk; ++k) {
           const float r = __half2float(R[k]);
+          float c0[NQ];
+          load_q<NQ>(qcs + k * NQ, c0);
 #pragma unroll
-          for (int i = 0; i < NQ; ++i) acc[i] = fmaf(r, cq[k * NQ + i], acc[i]);
+          for (int i = 0; i < NQ; ++i) acc[i] = fmaf(r, c0[i], acc[i]);
         }
       }
       if (ku.b > 0) {
-        const size_t row = (size_t)h * T + t;
-        const float s = __half2float(((const __half*)(kb + ku.off_scale))[row]);
         float r[NQ];
-        const uint32_t* cw = (const uint32_t*)(kb + ku.off_codes) + row * (size_t)(D * ku.b / 32);
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(data + tid * kcb);
+        const float* vt = qcs + KM * NQ;
         if (ku.b == 2) res_dots<D, NQ, 2>(cw, vt, r);
         else if (ku.b == 4) res_dots<D, NQ, 4>(cw, vt, r);
         else res_dots<D, NQ, 8>(cw, vt, r);
 #pragma unroll
-        for (int i = 0; i < NQ; ++i) acc[i] = fmaf(s, r[i], acc[i]);
+        for (int i = 0; i < NQ; ++i) acc[i] = fmaf(ks, r[i], acc[i]);
       }
     }
 #pragma unroll
@@ -250,13 +361,11 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
       l += p;
     }
     l = warp_sum(l);
-    if (lane == 0) { stat[i] = m; stat[NQ + i] = l; }
+    if (lane == 0) { stat[i] = m; stat[8 + i] = l; }
   }
   __syncthreads();
 
   // ---- phase 3: cv and z over this warp's 32 tokens
-  const bool vfT = (vu.rT == T);
-  const int Kv = vfT ? vu.rd : vu.rT;
   constexpr int KPL = KM / 32;
   float z[NQ][EPT], cv[NQ][KPL];
 #pragma unroll
@@ -267,17 +376,16 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
     for (int j = 0; j < KPL; ++j) cv[i][j] = 0.f;
   }
   {
-    const __half* sv = (const __half*)(vb + vu.off_scale);
-    const uint32_t* cvw = (const uint32_t*)(vb + vu.off_codes);
-    const size_t rw = (size_t)D * vu.b / 32;
-    for (int j = 0; j < 32; ++j) {
-      const int x = w * 32 + j, t = t0 + x;
-      if (t >= T) break;
+    const uint32_t* cvw = reinterpret_cast<const uint32_t*>(data + a.o_vc);
+    const int rw = D * vu.b / 32;
+    const __half* Rb = vst ? reinterpret_cast<const __half*>(data + a.o_vr) : vR;
+    const int ntok = min(32, n - w * 32);
+#pragma unroll 4
+    for (int j = 0; j < ntok; ++j) {
+      const int x = w * 32 + j;
       float p[NQ];
-#pragma unroll
-      for (int i = 0; i < NQ; ++i) p[i] = sc[x * NQ + i];
-      const __half* R = vfT ? (const __half*)(vb + vu.off_G) + ((size_t)h * T + t) * vu.rd
-                            : (const __half*)(vb + vu.off_UT) + (size_t)t * vu.rT;
+      load_q<NQ>(sc + x * NQ, p);
+      const __half* R = Rb + (size_t)x * Kv;
 #pragma unroll
       for (int jj = 0; jj < KPL; ++jj) {
         const int k = lane + 32 * jj;
@@ -288,17 +396,18 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
         }
       }
       if (vu.b > 0) {
-        const size_t row = (size_t)h * T + t;
-        const float s = __half2float(sv[row]);
+        const float s = sv[x];
         float ps[NQ];
 #pragma unroll
         for (int i = 0; i < NQ; ++i) ps[i] = p[i] * s;
-        if (vu.b == 2) res_accum<EPT, NQ, 2>(cvw + row * rw, lane, ps, z);
-        else if (vu.b == 4) res_accum<EPT, NQ, 4>(cvw + row * rw, lane, ps, z);
-        else res_accum<EPT, NQ, 8>(cvw + row * rw, lane, ps, z);
+        if (vu.b == 2) res_accum<EPT, NQ, 2>(cvw + x * rw, lane, ps, z);
+        else if (vu.b == 4) res_accum<EPT, NQ, 4>(cvw + x * rw, lane, ps, z);
+        else res_accum<EPT, NQ, 8>(cvw + x * rw, lane, ps, z);
       }
     }
   }
+  __syncthreads();   // the data region becomes the per-warp partial sums
+  float* red = reinterpret_cast<float*>(data);
   float* rw_ = red + (size_t)w * NQ * (D + KM);
 #pragma unroll
   for (int i = 0; i < NQ; ++i) {
@@ -311,9 +420,9 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
 
   // ---- the chunk's record: max, sum, z, cv (summed over the warps)
   float* rec = a.part + (((size_t)g * H + h) * a.nch + chunk) * rec_floats(nq, D);
-  for (int i = tid; i < nq; i += ATT_CHUNK) {
-    rec[i] = stat[i];
-    rec[nq + i] = stat[NQ + i];
+  if (tid < nq) {
+    rec[tid] = stat[tid];
+    rec[nq + tid] = stat[8 + tid];
   }
   for (int x = tid; x < nq * (D + KM); x += ATT_CHUNK) {
     const int i = x / (D + KM), c = x % (D + KM);
@@ -325,14 +434,13 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
   }
 }
 
-// Merge the chunks of one (head, group) and map back to feature space.
-template <int EPT, int NQ>
+// Merge the chunks of one (head, group, query) and map back to feature space.
+template <int EPT>
 __global__ void __launch_bounds__(128) attend_merge_kernel(AttArgs a) {
   constexpr int D = 32 * EPT;
-  constexpr int KM = JOLT_ATTN_MAX_RANK;
-  __shared__ float zf[NQ][D], cf[NQ][KM], ef[NQ][KM > D ? KM : D];
-  __shared__ float Mx[NQ], Lx[NQ];
-  const int h = blockIdx.x, gl = blockIdx.y, g = a.g0 + gl;
+  __shared__ float zf[D], cf[KM], ef[KM > D ? KM : D], red[2][4];
+  __shared__ __half st_Ud[D * 64], st_G[64 * (KM > D ? KM : D)];
+  const int h = blockIdx.x, gl = blockIdx.y, i = blockIdx.z, g = a.g0 + gl;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int T = a.T, H = a.H, nq = a.nq, nch = a.nch;
   const AttUnit vu = a.v[gl];
@@ -341,69 +449,73 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(AttArgs a) {
   const int Kv = vfT ? vu.rd : vu.rT;
   const size_t rf = rec_floats(nq, D);
   const float* base = a.part + ((size_t)g * H + h) * nch * rf;
-
-  // global max and sum of every query
-  for (int i = w; i < nq; i += 4) {
-    float m = -INFINITY;
-    for (int c = lane; c < nch; c += 32) m = fmaxf(m, base[c * rf + i]);
-    m = warp_max(m);
-    float l = 0.f;
-    for (int c = lane; c < nch; c += 32) l += expf(base[c * rf + i] - m) * base[c * rf + nq + i];
-    l = warp_sum(l);
-    if (lane == 0) { Mx[i] = m; Lx[i] = l; }
-  }
+  if (!vfD) stage_halves(st_Ud, (const __half*)(vb + vu.off_Ud), D * vu.rd, tid, 128);
+  if (!vfT)
+    stage_halves(st_G, (const __half*)(vb + vu.off_G) + (size_t)h * vu.rT * vu.rd,
+                 vu.rT * vu.rd, tid, 128);
+  // the global max M and sum L of this query
+  float m = -INFINITY;
+  for (int c = tid; c < nch; c += 128) m = fmaxf(m, base[c * rf + i]);
+  m = warp_max(m);
+  if (lane == 0) red[0][w] = m;
   __syncthreads();
-  // z and cv: chunk records weighted by exp(m_c - M)
-  for (int x = tid; x < nq * (D + KM); x += 128) {
-    const int i = x / (D + KM), c = x % (D + KM);
-    if (c >= D + Kv) continue;
-    float s = 0.f;
-    for (int ch = 0; ch < nch; ++ch) {
-      const float* r = base + ch * rf;
-      s = fmaf(expf(r[i] - Mx[i]), r[2 * nq + (size_t)i * (D + KM) + c], s);
-    }
-    if (c < D) zf[i][c] = s;
-    else cf[i][c - D] = s;
+  const float M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+  float l = 0.f;
+  for (int c = tid; c < nch; c += 128) l += expf(base[c * rf + i] - M) * base[c * rf + nq + i];
+  l = warp_sum(l);
+  if (lane == 0) red[1][w] = l;
+  // z and cv: the chunk records weighted by exp(m_c - M), two entries per thread
+  const int ne = D + Kv;
+  const int x0 = tid, x1 = tid + 128;
+  float s0 = 0.f, s1 = 0.f;
+  const size_t col = 2 * nq + (size_t)i * (D + KM);
+#pragma unroll 4
+  for (int c = 0; c < nch; ++c) {
+    const float* r = base + c * rf;
+    const float wc = expf(r[i] - M);
+    if (x0 < ne) s0 = fmaf(wc, r[col + x0], s0);
+    if (x1 < ne) s1 = fmaf(wc, r[col + x1], s1);
   }
+  if (x0 < ne) { if (x0 < D) zf[x0] = s0; else cf[x0 - D] = s0; }
+  if (x1 < ne) { if (x1 < D) zf[x1] = s1; else cf[x1 - D] = s1; }
   __syncthreads();
+  const float L = red[1][0] + red[1][1] + red[1][2] + red[1][3];
   // back-projection, stage 1: e = G[h]^T cv (r_T < T) or cv itself (r_T = T)
-  if (vfT) {
-    for (int x = tid; x < nq * vu.rd; x += 128) ef[x / vu.rd][x % vu.rd] = cf[x / vu.rd][x % vu.rd];
-  } else {
-    const __half* Gh = (const __half*)(vb + vu.off_G) + (size_t)h * vu.rT * vu.rd;
-    for (int x = tid; x < nq * vu.rd; x += 128) {
-      const int i = x / vu.rd, j = x % vu.rd;
-      float s = 0.f;
-      for (int k = 0; k < vu.rT; ++k) s = fmaf(__half2float(Gh[k * vu.rd + j]), cf[i][k], s);
-      ef[i][j] = s;
+  for (int j = tid; j < vu.rd; j += 128) {
+    float s;
+    if (vfT) {
+      s = cf[j];
+    } else {
+      s = 0.f;
+#pragma unroll 8
+      for (int k = 0; k < vu.rT; ++k) s = fmaf(__half2float(st_G[k * vu.rd + j]), cf[k], s);
     }
+    ef[j] = s;
   }
   __syncthreads();
-  // stage 2 (U_d e) plus the inverse rotation of z, a warp per query
-  const __half* Ud = (const __half*)(vb + vu.off_Ud);
-  const unsigned char* sb = (const unsigned char*)vb + 88;
-  const float rs = rsqrtf((float)D);
-  for (int i = w; i < nq; i += 4) {
+  // stage 2 (U_d e) plus the inverse rotation of z: warp 0 holds the row
+  if (w == 0) {
     float v[EPT];
     if (vu.b > 0) {
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) v[e] = zf[i][lane * EPT + e];
+      for (int e = 0; e < EPT; ++e) v[e] = zf[lane * EPT + e];
       fwht_row<EPT>(v, lane);
     }
-    const float inv = 1.f / Lx[i];
+    const unsigned char* sb = (const unsigned char*)vb + 88;
+    const float rs = rsqrtf((float)D), inv = 1.f / L;
     float* o = a.out + (((size_t)g * H + h) * nq + i) * D;
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
       const int d = lane * EPT + e;
       float lo;
       if (vfD) {
-        lo = ef[i][d];
+        lo = ef[d];
       } else {
         lo = 0.f;
-        for (int j = 0; j < vu.rd; ++j) lo = fmaf(__half2float(Ud[d * vu.rd + j]), ef[i][j], lo);
+#pragma unroll 8
+        for (int j = 0; j < vu.rd; ++j) lo = fmaf(__half2float(st_Ud[d * vu.rd + j]), ef[j], lo);
       }
-      float res = 0.f;
-      if (vu.b > 0) res = (((sb[d >> 3] >> (d & 7)) & 1) ? -1.f : 1.f) * v[e] * rs;
+      const float res = (vu.b > 0) ? sign_of(sb, d) * v[e] * rs : 0.f;
       o[d] = (lo + res) * inv;
     }
   }
@@ -412,28 +524,31 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(AttArgs a) {
 template <int EPT, int NQ>
 jolt_status launch_attend(const AttArgs& a, int ng, cudaStream_t st) {
   constexpr int D = 32 * EPT;
-  constexpr int KM = JOLT_ATTN_MAX_RANK;
-  const size_t smem = sizeof(float) * (NQ * D + NQ * KM + KM * NQ + D * NQ + ATT_CHUNK * NQ +
-                                       ATT_WARPS * NQ * (D + KM) + 2 * NQ);
-  static bool attr = false;
-  if (!attr) {
+  const size_t smem = sizeof(float) * ((KM + D) * NQ + ATT_CHUNK * NQ + 16 + ATT_CHUNK) + a.data;
+  if (smem > 227 * 1024) return JOLT_ERR_INVALID;
+  static int attr = 0;
+  if ((int)smem > attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(attend_chunk_kernel<EPT, NQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    attr = true;
+    attr = (int)smem;
   }
+  attend_prep_kernel<EPT, NQ><<<dim3(a.H, ng), 128, 0, st>>>(a);
+  JOLT_LAUNCH_CHECK();
   attend_chunk_kernel<EPT, NQ><<<dim3(a.nch, a.H, ng), ATT_CHUNK, smem, st>>>(a);
   JOLT_LAUNCH_CHECK();
-  attend_merge_kernel<EPT, NQ><<<dim3(a.H, ng), 128, 0, st>>>(a);
+  attend_merge_kernel<EPT><<<dim3(a.H, ng, a.nq), 128, 0, st>>>(a);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
 
 template <int EPT>
 jolt_status launch_attend_nq(const AttArgs& a, int ng, cudaStream_t st) {
-  if (a.nq <= 1) return launch_attend<EPT, 1>(a, ng, st);
-  if (a.nq <= 2) return launch_attend<EPT, 2>(a, ng, st);
-  if (a.nq <= 4) return launch_attend<EPT, 4>(a, ng, st);
-  return launch_attend<EPT, 8>(a, ng, st);
+  switch (nq_pad(a.nq)) {
+    case 1: return launch_attend<EPT, 1>(a, ng, st);
+    case 2: return launch_attend<EPT, 2>(a, ng, st);
+    case 4: return launch_attend<EPT, 4>(a, ng, st);
+    default: return launch_attend<EPT, 8>(a, ng, st);
+  }
 }
 
 AttUnit att_unit(const jolt_blob_desc& d) {
@@ -444,30 +559,52 @@ AttUnit att_unit(const jolt_blob_desc& d) {
   return u;
 }
 
+// Low-rank row length of a blob (r_T < T: U_T rows; r_T = T: G rows).
+int row_len(const jolt_blob_desc& d) { return d.rT == d.T ? d.rd : d.rT; }
+
+size_t part_bytes(int n_groups, int H, int T, int D, int nq) {
+  return align_up((size_t)n_groups * H * ((T + ATT_CHUNK - 1) / ATT_CHUNK) * rec_floats(nq, D) *
+                      sizeof(float), 256);
+}
+
 }  // namespace
 
-size_t attend_chunks(int T) { return (size_t)((T + ATT_CHUNK - 1) / ATT_CHUNK); }
-
 size_t attend_ws_bytes(int n_groups, int H, int T, int D, int nq) {
-  return (size_t)n_groups * H * attend_chunks(T) * nq * (2 + D + JOLT_ATTN_MAX_RANK) *
-         sizeof(float);
+  return part_bytes(n_groups, H, T, D, nq) +
+         (size_t)n_groups * H * (KM + D) * nq_pad(nq) * sizeof(float);
 }
 
 jolt_status attend_run(int n_groups, const jolt_blob_desc* desc, const char* blob,
-                       size_t stride, const float* q, int nq, float scale, float* part,
+                       size_t stride, const float* q, int nq, float scale, float* ws,
                        float* out, cudaStream_t st) {
   const int H = desc[0].H, T = desc[0].T, D = desc[0].D;
+  float* part = ws;
+  float* qc = (float*)((char*)ws + part_bytes(n_groups, H, T, D, nq));
   for (int g0 = 0; g0 < n_groups; g0 += ATT_MAX_G) {
     const int ng = (n_groups - g0) < ATT_MAX_G ? (n_groups - g0) : ATT_MAX_G;
     AttArgs a;
     memset(&a, 0, sizeof(a));
-    a.H = H; a.T = T; a.nq = nq; a.nch = (int)attend_chunks(T);
-    a.scale = scale; a.blob = blob; a.stride = stride; a.q = q; a.part = part; a.out = out;
-    a.g0 = g0;
+    a.H = H; a.T = T; a.nq = nq; a.nch = (T + ATT_CHUNK - 1) / ATT_CHUNK;
+    a.scale = scale; a.blob = blob; a.stride = stride; a.q = q; a.qc = qc; a.part = part;
+    a.out = out; a.g0 = g0;
+    // the data region holds the largest K codes, K rows, V codes, V rows of
+    // this launch's groups (rows only when short enough to stage)
+    size_t kc = 0, kr = 0, vc = 0, vr = 0;
     for (int i = 0; i < ng; ++i) {
-      a.k[i] = att_unit(desc[2 * (g0 + i)]);
-      a.v[i] = att_unit(desc[2 * (g0 + i) + 1]);
+      const jolt_blob_desc& kd = desc[2 * (g0 + i)];
+      const jolt_blob_desc& vd = desc[2 * (g0 + i) + 1];
+      a.k[i] = att_unit(kd);
+      a.v[i] = att_unit(vd);
+      kc = std::max(kc, (size_t)ATT_CHUNK * D * kd.b / 8);
+      vc = std::max(vc, (size_t)ATT_CHUNK * D * vd.b / 8);
+      if (row_len(kd) <= ATT_STAGE_RANK) kr = std::max(kr, (size_t)ATT_CHUNK * row_len(kd) * 2);
+      if (row_len(vd) <= ATT_STAGE_RANK) vr = std::max(vr, (size_t)ATT_CHUNK * row_len(vd) * 2);
     }
+    a.o_kr = (int)align_up(kc, 16);
+    a.o_vc = (int)align_up(a.o_kr + kr, 16);
+    a.o_vr = (int)align_up(a.o_vc + vc, 16);
+    const size_t red = sizeof(float) * ATT_WARPS * nq_pad(nq) * (D + KM);
+    a.data = (int)align_up(std::max((size_t)a.o_vr + vr, red), 16);
     jolt_status s;
     switch (D) {
       case 128: s = launch_attend_nq<4>(a, ng, st); break;

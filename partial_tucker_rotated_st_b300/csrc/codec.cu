@@ -48,6 +48,7 @@ struct EncArgs {
   float rs_hi, rs_lo;  // 1/sqrt(D) as a double-float
   char* blob;
   unsigned long long off_scale, off_codes;
+  long long row_ld, row_off;   // token t of head h is row h * row_ld + row_off + t of the blob
 };
 
 // Error-free transformations (Knuth TwoSum; TwoProduct through the fused
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
     }
     __syncwarp();
     if (t < a.T) {
-      const long long row = (long long)h * a.T + t;
+      const long long row = (long long)h * a.row_ld + a.row_off + t;
       unsigned char* cb = (unsigned char*)a.blob + a.off_codes + row * nbytes;
       const int per = 8 / b;
       for (int j = lane; j < nbytes; j += 32) {
@@ -550,6 +551,262 @@ jolt_status launch_dec(dim3 grid, const DecArgs& a, cudaStream_t st) {
 }
 
 
+
+// ------------------------------------------------------------------ admission
+// A block of tau new tokens joins an encoded unit whose candidate, factors,
+// signs and bit width stay fixed.  ["Rotated Tucker residual for
+// outlier-resistant KV quantization", Implementation notes: keep the Tucker
+// factors, rebuild X~ for each incoming token block and code R = X - X~.]
+// The stored rows of the new tokens are computed in double-float (fp16 x
+// fp16 and bf16 x fp16 products are exact in fp32, the rest through
+// TwoProduct) with the small normal-equation solve in f64, so that their
+// fp16 rounding is the correctly rounded one except at exact ties.
+constexpr int ADM_MAX_UNITS = 16;
+constexpr int ADM_MAX_JOBS = 6;
+constexpr int ADM_RT = 64;            // largest truncated token rank
+
+// fp16 rounding (to nearest, ties to even) of the signed double-float zh + zl.
+__device__ __forceinline__ __half round_f16_df_signed(float zh, float zl) {
+  const __half h = __float2half_rn(zh);
+  const float hf = __half2float(h);
+  const float d = zh - hf;
+  if (d == 0.f || zl == 0.f) return h;
+  const unsigned short hb = __half_as_ushort(h);
+  const bool neg = (hb & 0x8000u) != 0;
+  unsigned short nb;   // the fp16 neighbour of hf on the side of zh
+  if (d > 0.f) nb = neg ? (hb == 0x8000u ? 0x0001u : (unsigned short)(hb - 1)) : (unsigned short)(hb + 1);
+  else nb = neg ? (unsigned short)(hb + 1) : (hb == 0 ? 0x8001u : (unsigned short)(hb - 1));
+  const float nf = __half2float(__ushort_as_half(nb));
+  if (zh == 0.5f * (hf + nf) && (d > 0.f) == (zl > 0.f)) return __ushort_as_half(nb);
+  return h;
+}
+
+struct AdmJob {
+  unsigned long long src, dst;        // byte offsets in the old / new blob
+  long long nblk, blk, sstride, dstride;
+};
+struct AdmCopyUnit {
+  const char* in;
+  char* out;
+  unsigned char hdr[88];
+  int D, njobs;
+  int8_t* signs;                      // the sign vector as int8 (workspace)
+  AdmJob job[ADM_MAX_JOBS];
+};
+struct AdmCopyBatch {
+  AdmCopyUnit u[ADM_MAX_UNITS];
+};
+
+// New header, the sign bits carried over, and every section of the old
+// tokens moved to its place in the longer layout (grid y = unit).
+__global__ void adm_copy_kernel(const __grid_constant__ AdmCopyBatch cb) {
+  const AdmCopyUnit& u = cb.u[blockIdx.y];
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < 88; i += blockDim.x) u.out[i] = (char)u.hdr[i];
+    for (int i = threadIdx.x; i < (u.D + 7) / 8; i += blockDim.x) u.out[88 + i] = u.in[88 + i];
+    for (int d = threadIdx.x; d < u.D; d += blockDim.x)
+      u.signs[d] = ((((const unsigned char*)u.in)[88 + (d >> 3)] >> (d & 7)) & 1) ? -1 : 1;
+  }
+  for (int j = 0; j < u.njobs; ++j) {
+    const AdmJob& jb = u.job[j];
+    const bool w4 = ((jb.src | jb.dst | (unsigned long long)jb.blk | (unsigned long long)jb.sstride |
+                      (unsigned long long)jb.dstride) & 3) == 0;
+    if (w4) {
+      const long long per = jb.blk / 4, n = jb.nblk * per;
+      for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+           e += (long long)gridDim.x * blockDim.x) {
+        const long long bk = e / per, o = e % per;
+        reinterpret_cast<uint32_t*>(u.out + jb.dst + bk * jb.dstride)[o] =
+            reinterpret_cast<const uint32_t*>(u.in + jb.src + bk * jb.sstride)[o];
+      }
+    } else {
+      const long long per = jb.blk / 2, n = jb.nblk * per;
+      for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+           e += (long long)gridDim.x * blockDim.x) {
+        const long long bk = e / per, o = e % per;
+        reinterpret_cast<unsigned short*>(u.out + jb.dst + bk * jb.dstride)[o] =
+            reinterpret_cast<const unsigned short*>(u.in + jb.src + bk * jb.sstride)[o];
+      }
+    }
+  }
+}
+
+struct AdmUnit {
+  const void* X;          // [H][tau][D] new tokens
+  const __half* Ud;       // stored U_d [D][rd], or null for r_d = D
+  const __half* G;        // stored core [H][rT][rd] (r_T < T)
+  __half* Gout;           // r_T = T: new core rows at Gout + h * g_hs + t * rd
+  long long g_hs;
+  __half* UTout;          // r_T < T: new U_T rows [tau][rT]
+  float* Yh;              // r_T < T: Y = X U_d as double-float [H][tau][rd]
+  float* Yl;
+  double* M;              // sum_h G_h G_h^T [rT][rT]
+  int rT, rd, whole;      // whole: r_T = T (the core gains rows)
+};
+struct AdmBatch {
+  AdmUnit u[ADM_MAX_UNITS];
+  int H, tau, D, xdt;
+};
+
+// Y[h][t][j] = sum_d X[h][t][d] U_d[d][j] in double-float; for a whole
+// token mode the core rows fp16(Y) go straight to the new blob.  Grid:
+// (ceil(tau / 8), H, unit), 256 threads = 8 tokens x 32 lanes over j.
+__global__ void adm_proj_kernel(const __grid_constant__ AdmBatch ab) {
+  const AdmUnit& a = ab.u[blockIdx.z];
+  const int D = ab.D, tau = ab.tau, h = blockIdx.y;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + w;
+  __shared__ float xs[8][128];
+  if (t < tau)
+    for (int d = lane; d < D; d += 32) {
+      const long long o = ((long long)h * tau + t) * D + d;
+      xs[w][d] = ab.xdt == JOLT_BF16 ? __bfloat162float(((const __nv_bfloat16*)a.X)[o])
+                                     : ((const float*)a.X)[o];
+    }
+  __syncwarp();
+  if (t >= tau) return;
+  for (int j = lane; j < a.rd; j += 32) {
+    float sh, sl;
+    if (!a.Ud) {
+      sh = xs[w][j];
+      sl = 0.f;
+    } else {
+      sh = 0.f; sl = 0.f;
+      for (int d = 0; d < D; ++d) {
+        const float u = __half2float(a.Ud[(long long)d * a.rd + j]);
+        const float p = xs[w][d] * u;
+        const float pe = fmaf(xs[w][d], u, -p);
+        float s2, e;
+        two_sum(sh, p, s2, e);
+        sh = s2;
+        sl += e + pe;
+      }
+      const float hi = sh + sl;
+      sl = sl - (hi - sh);
+      sh = hi;
+    }
+    if (a.whole) {
+      a.Gout[(long long)h * a.g_hs + (long long)t * a.rd + j] = round_f16_df_signed(sh, sl);
+    } else {
+      const long long o = ((long long)h * tau + t) * a.rd + j;
+      a.Yh[o] = sh;
+      a.Yl[o] = sl;
+    }
+  }
+}
+
+// M[k][l] = sum_h sum_j G[h][k][j] G[h][l][j] (fp16 products exact in fp32,
+// TwoSum accumulation), as f64.  Grid: (rT, unit), 64 threads over l.
+__global__ void adm_gram_kernel(const __grid_constant__ AdmBatch ab) {
+  const AdmUnit& a = ab.u[blockIdx.y];
+  const int k = blockIdx.x, l = threadIdx.x;
+  if (a.whole || k >= a.rT || l >= a.rT) return;
+  float sh = 0.f, sl = 0.f;
+  for (int h = 0; h < ab.H; ++h) {
+    const __half* Gh = a.G + (long long)h * a.rT * a.rd;
+    for (int j = 0; j < a.rd; ++j) {
+      const float p = __half2float(Gh[k * a.rd + j]) * __half2float(Gh[l * a.rd + j]);
+      float s2, e;
+      two_sum(sh, p, s2, e);
+      sh = s2;
+      sl += e;
+    }
+  }
+  a.M[k * a.rT + l] = (double)sh + (double)sl;
+}
+
+// The fold-in: for each new token t, u_t solves (sum_h G_h G_h^T) u =
+// sum_h G_h Y[h][t]^T.  One CTA per (8 tokens, unit): the CTA factors M by
+// Cholesky in f64 (pivots at most 2^-40 max diag(M) dropped: that
+// coordinate is 0), a warp per token forms its right-hand side in
+// double-float and substitutes in f64; u is rounded to fp16 into the blob.
+__global__ void __launch_bounds__(256) adm_solve_kernel(const __grid_constant__ AdmBatch ab) {
+  const AdmUnit& a = ab.u[blockIdx.y];
+  if (a.whole) return;
+  const int rT = a.rT, rd = a.rd, H = ab.H, tau = ab.tau;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  __shared__ double L[ADM_RT][ADM_RT + 1];
+  __shared__ int keep[ADM_RT];
+  __shared__ double tol;
+  for (int e = tid; e < rT * rT; e += 256) L[e / rT][e % rT] = a.M[e];
+  __syncthreads();
+  if (tid == 0) {
+    double mx = 0.0;
+    for (int j = 0; j < rT; ++j) mx = fmax(mx, L[j][j]);
+    tol = 0x1p-40 * mx;
+  }
+  __syncthreads();
+  // right-looking Cholesky on the lower triangle
+  for (int j = 0; j < rT; ++j) {
+    const double d = L[j][j];
+    const bool kj = d > tol;
+    __syncthreads();
+    if (tid == 0) {
+      keep[j] = kj;
+      L[j][j] = kj ? sqrt(d) : 0.0;
+    }
+    __syncthreads();
+    for (int i = j + 1 + tid; i < rT; i += 256) L[i][j] = kj ? L[i][j] / L[j][j] : 0.0;
+    __syncthreads();
+    if (kj)
+      for (int e = tid; e < (rT - j - 1) * (rT - j - 1); e += 256) {
+        const int i = j + 1 + e / (rT - j - 1), c = j + 1 + e % (rT - j - 1);
+        if (c <= i) L[i][c] -= L[i][j] * L[c][j];
+      }
+    __syncthreads();
+  }
+  const int t = blockIdx.x * 8 + w;
+  if (t >= tau) return;
+  // right-hand side: lanes over k (k = lane, lane + 32)
+  double r[2];
+  for (int q = 0; q < 2; ++q) {
+    const int k = lane + 32 * q;
+    float sh = 0.f, sl = 0.f;
+    if (k < rT) {
+      for (int h = 0; h < H; ++h) {
+        const __half* Gk = a.G + ((long long)h * rT + k) * rd;
+        const float* yh = a.Yh + ((long long)h * tau + t) * rd;
+        const float* yl = a.Yl + ((long long)h * tau + t) * rd;
+        for (int j = 0; j < rd; ++j) {
+          const float g = __half2float(Gk[j]);
+          const float p = yh[j] * g;
+          const float pe = fmaf(yh[j], g, -p);
+          float s2, e;
+          two_sum(sh, p, s2, e);
+          sh = s2;
+          sl += e + fmaf(yl[j], g, pe);
+        }
+      }
+    }
+    r[q] = (double)sh + (double)sl;
+  }
+  // forward substitution L z = r, then back substitution L^T u = z
+  for (int j = 0; j < rT; ++j) {
+    const int owner = j & 31, q = j >> 5;
+    double zj = __shfl_sync(0xffffffffu, q ? r[1] : r[0], owner);
+    zj = keep[j] ? zj / L[j][j] : 0.0;
+    if (lane == owner) { if (q) r[1] = zj; else r[0] = zj; }
+    for (int qq = 0; qq < 2; ++qq) {
+      const int i = lane + 32 * qq;
+      if (i > j && i < rT) r[qq] -= L[i][j] * zj;
+    }
+  }
+  for (int j = rT - 1; j >= 0; --j) {
+    const int owner = j & 31, q = j >> 5;
+    double uj = __shfl_sync(0xffffffffu, q ? r[1] : r[0], owner);
+    uj = keep[j] ? uj / L[j][j] : 0.0;
+    if (lane == owner) { if (q) r[1] = uj; else r[0] = uj; }
+    for (int qq = 0; qq < 2; ++qq) {
+      const int i = lane + 32 * qq;
+      if (i < j) r[qq] -= L[j][i] * uj;
+    }
+  }
+  for (int q = 0; q < 2; ++q) {
+    const int k = lane + 32 * q;
+    if (k < rT) a.UTout[(long long)t * rT + k] = __double2half(r[q]);
+  }
+}
+
 }  // namespace
 
 void blob_layout(int H, int T, int D, int rT, int rd, int b, int block, int align,
@@ -656,6 +913,7 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
       ea.X = Xu; ea.signs = signs + (size_t)u * D;
       ea.H = H; ea.T = T; ea.D = D; ea.dtype = L.dtype; ea.b = b;
       ea.blob = bl; ea.off_scale = dsc.off_scale; ea.off_codes = dsc.off_codes;
+      ea.row_ld = T; ea.row_off = 0;
       {
         const double rs = 1.0 / sqrt((double)D);
         ea.rs_hi = (float)rs;
@@ -722,6 +980,149 @@ jolt_status decode_run(int U, const jolt_blob_desc* desc, const char* blob, size
       default: ls = launch_dec<1>(grid, a, st);
     }
     if (ls != JOLT_OK) return ls;
+  }
+  return JOLT_OK;
+}
+
+size_t admit_ws_unit_bytes(int H, int tau, int D) {
+  // signs, Y (double-float), M (f64), chain rows (double-float)
+  return align_up(256 + (size_t)H * tau * D * 8 + (size_t)ADM_RT * ADM_RT * 8 +
+                      (size_t)H * ADM_RT * D * 8, 256);
+}
+
+jolt_status admit_run(int U, const jolt_blob_desc* din, const char* bin, size_t sin,
+                      const void* Xn, int xdt, int tau, int align, char* ws, char* bout,
+                      size_t sout, jolt_blob_desc* dout, cudaStream_t st) {
+  const int H = din[0].H, T = din[0].T, D = din[0].D;
+  const int Tn = T + tau;
+  const size_t wub = admit_ws_unit_bytes(H, tau, D);
+  const size_t xes = xdt == JOLT_BF16 ? 2 : 4;
+  for (int u = 0; u < U; ++u) {
+    const jolt_blob_desc& d = din[u];
+    const int rTn = d.rT == T ? Tn : d.rT;
+    blob_layout(H, Tn, D, rTn, d.rd, d.b, D, align, &dout[u]);
+    if (dout[u].bytes > sout) return JOLT_ERR_INVALID;
+  }
+  JOLT_CUDA_TRY(cudaMemsetAsync(bout, 0, (size_t)U * sout, st));
+  for (int u0 = 0; u0 < U; u0 += ADM_MAX_UNITS) {
+    const int nu = (U - u0) < ADM_MAX_UNITS ? (U - u0) : ADM_MAX_UNITS;
+    AdmCopyBatch cb;
+    AdmBatch ab;
+    RowsBatch rows;
+    EncBatch eb;
+    memset(&cb, 0, sizeof(cb));
+    memset(&ab, 0, sizeof(ab));
+    memset(&rows, 0, sizeof(rows));
+    memset(&eb, 0, sizeof(eb));
+    ab.H = H; ab.tau = tau; ab.D = D; ab.xdt = xdt;
+    rows.D = D;
+    int nrows = 0, nenc = 0, nsolve = 0;
+    for (int i = 0; i < nu; ++i) {
+      const int u = u0 + i;
+      const jolt_blob_desc& di = din[u];
+      const jolt_blob_desc& dn = dout[u];
+      const char* bi = bin + (size_t)u * sin;
+      char* bo = bout + (size_t)u * sout;
+      char* wu = ws + (size_t)u * wub;
+      const int rT = di.rT, rd = di.rd, b = di.b;
+      const bool whole = (rT == T), fullD = (rd == D);
+      // header and the old tokens' sections
+      AdmCopyUnit& cu = cb.u[i];
+      cu.in = bi; cu.out = bo; cu.D = D; cu.signs = (int8_t*)wu;
+      const uint32_t hd32[10] = {MAGIC, VERSION, (uint32_t)H, (uint32_t)Tn, (uint32_t)D,
+                                 (uint32_t)dn.rT, (uint32_t)rd, (uint32_t)b, (uint32_t)D,
+                                 (uint32_t)dn.flags};
+      memcpy(cu.hdr, hd32, 40);
+      const uint64_t hd64[6] = {dn.off_UT, dn.off_Ud, dn.off_G, dn.off_scale, dn.off_codes,
+                                dn.bytes};
+      memcpy(cu.hdr + 40, hd64, 48);
+      auto job = [&](unsigned long long src, unsigned long long dst, long long nblk, long long blk,
+                     long long ss, long long ds) {
+        AdmJob& j = cu.job[cu.njobs++];
+        j.src = src; j.dst = dst; j.nblk = nblk; j.blk = blk; j.sstride = ss; j.dstride = ds;
+      };
+      if (!whole) job(di.off_UT, dn.off_UT, 1, 2LL * T * rT, 0, 0);
+      if (!fullD) job(di.off_Ud, dn.off_Ud, 1, 2LL * D * rd, 0, 0);
+      if (!whole) job(di.off_G, dn.off_G, 1, 2LL * H * rT * rd, 0, 0);
+      else job(di.off_G, dn.off_G, H, 2LL * T * rd, 2LL * T * rd, 2LL * Tn * rd);
+      if (b > 0) {
+        job(di.off_scale, dn.off_scale, H, 2LL * T, 2LL * T, 2LL * Tn);
+        const long long rb = (long long)T * D * b / 8, rbn = (long long)Tn * D * b / 8;
+        job(di.off_codes, dn.off_codes, H, rb, rb, rbn);
+      }
+      // the new tokens' stored rows
+      AdmUnit& au = ab.u[i];
+      au.X = (const char*)Xn + (size_t)u * H * tau * D * xes;
+      au.Ud = fullD ? nullptr : (const __half*)(bo + dn.off_Ud);
+      au.G = (const __half*)(bo + dn.off_G);
+      au.rT = whole ? 0 : rT; au.rd = rd; au.whole = whole;
+      float* Y = (float*)(wu + 256);
+      au.Yh = Y;
+      au.Yl = Y + (size_t)H * tau * rd;
+      au.M = (double*)(wu + 256 + (size_t)H * tau * D * 8);
+      float* Bh = (float*)(wu + 256 + (size_t)H * tau * D * 8 + (size_t)ADM_RT * ADM_RT * 8);
+      if (whole) {
+        au.Gout = (__half*)(bo + dn.off_G) + (size_t)T * rd;
+        au.g_hs = (long long)Tn * rd;
+      } else {
+        au.UTout = (__half*)(bo + dn.off_UT) + (size_t)T * rT;
+        ++nsolve;
+      }
+      // the new tokens' codes, from the stored rows as in encode
+      if (b > 0) {
+        EncArgs& ea = eb.u[nenc++];
+        ea.X = au.X; ea.signs = cu.signs;
+        ea.H = H; ea.T = tau; ea.D = D; ea.dtype = xdt; ea.b = b;
+        ea.blob = bo; ea.off_scale = dn.off_scale; ea.off_codes = dn.off_codes;
+        ea.row_ld = Tn; ea.row_off = T;
+        const double rs = 1.0 / sqrt((double)D);
+        ea.rs_hi = (float)rs;
+        ea.rs_lo = (float)(rs - (double)ea.rs_hi);
+        if (whole && fullD) {
+          ea.mode = 2;
+        } else if (whole) {
+          ea.mode = 1; ea.K = rd;
+          ea.Kg = au.Gout; ea.k_hs = (long long)Tn * rd; ea.k_ld = rd;
+          ea.B16 = au.Ud; ea.b_hs = 0; ea.b_ks = 1; ea.b_ds = rd;
+        } else {
+          ea.mode = 0; ea.K = rT;
+          ea.Kg = au.UTout; ea.k_hs = 0; ea.k_ld = rT;
+          if (fullD) {
+            ea.B16 = au.G; ea.b_hs = (long long)rT * D; ea.b_ks = D; ea.b_ds = 1;
+          } else {
+            RowsUnit& ru = rows.u[nrows++];
+            ru.G = au.G; ru.g_hs = (long long)rT * rd; ru.Ud = au.Ud; ru.ldu = rd;
+            ru.rT = rT; ru.rd = rd; ru.Bhi = Bh; ru.Blo = Bh + (size_t)H * rT * D;
+            ea.Bhi = ru.Bhi; ea.Blo = ru.Blo; ea.b_hs = (long long)rT * D;
+          }
+        }
+      }
+    }
+    adm_copy_kernel<<<dim3(128, nu), 256, 0, st>>>(cb);
+    JOLT_LAUNCH_CHECK();
+    adm_proj_kernel<<<dim3((tau + 7) / 8, H, nu), 256, 0, st>>>(ab);
+    JOLT_LAUNCH_CHECK();
+    if (nsolve > 0) {
+      adm_gram_kernel<<<dim3(ADM_RT, nu), 64, 0, st>>>(ab);
+      JOLT_LAUNCH_CHECK();
+      adm_solve_kernel<<<dim3((tau + 7) / 8, nu), 256, 0, st>>>(ab);
+      JOLT_LAUNCH_CHECK();
+    }
+    if (nrows > 0) {
+      enc_rows_batch_kernel<<<dim3((ADM_RT * D + 255) / 256, H, nrows), 256, 0, st>>>(rows);
+      JOLT_LAUNCH_CHECK();
+    }
+    if (nenc > 0) {
+      const dim3 grid((tau + CD_TILE - 1) / CD_TILE, H, nenc);
+      jolt_status ls;
+      const bool bf = (xdt == JOLT_BF16);
+      switch (D) {
+        case 128: ls = bf ? launch_enc<__nv_bfloat16, 4>(grid, eb, st) : launch_enc<float, 4>(grid, eb, st); break;
+        case 64: ls = bf ? launch_enc<__nv_bfloat16, 2>(grid, eb, st) : launch_enc<float, 2>(grid, eb, st); break;
+        default: ls = bf ? launch_enc<__nv_bfloat16, 1>(grid, eb, st) : launch_enc<float, 1>(grid, eb, st);
+      }
+      if (ls != JOLT_OK) return ls;
+    }
   }
   return JOLT_OK;
 }

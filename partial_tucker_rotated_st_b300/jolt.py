@@ -92,6 +92,12 @@ _SIG = {
     "jolt_attend": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(JoltBlobDesc), _P,
                                    ctypes.c_size_t, _P, ctypes.c_int, ctypes.c_float, _P,
                                    ctypes.c_size_t, _P, _P]),
+    "jolt_admit_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                    ctypes.c_int]),
+    "jolt_admit": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(JoltBlobDesc), _P, ctypes.c_size_t,
+                                  _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
+                                  ctypes.c_size_t, _P, ctypes.c_size_t,
+                                  ctypes.POINTER(JoltBlobDesc), _P]),
     "jolt_sweep_candidates_noalloc": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P,
                                                      _P, _P, ctypes.c_size_t, _P, _P, _P]),
     "jolt_noalloc_scratch_bytes": (ctypes.c_size_t, []),
@@ -300,6 +306,24 @@ def jolt_attend(desc: Sequence[JoltBlobDesc], blob, blob_stride, q, nq, scale, w
     _check("jolt_attend", lib().jolt_attend(n // 2, arr, _ptr(blob), blob_stride, _ptr(q), nq,
                                             float(scale), _ptr(ws), ws_bytes, _ptr(out),
                                             _stream(stream)))
+
+
+def jolt_admit_workspace_size(n_units, H, tau, D) -> int:
+    return int(lib().jolt_admit_workspace_size(n_units, H, tau, D))
+
+
+def jolt_admit(desc_in: Sequence[JoltBlobDesc], blob_in, stride_in, X_new, x_dtype, tau, align,
+               ws, blob_out, stride_out, ws_bytes=None, stream=None):
+    """Admit tau new tokens (X_new [units][H][tau][D]) into each unit; returns
+    the new blobs' descriptions."""
+    n = len(desc_in)
+    arr = (JoltBlobDesc * n)(*desc_in)
+    out = (JoltBlobDesc * n)()
+    ws_bytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("jolt_admit", lib().jolt_admit(n, arr, _ptr(blob_in), stride_in, _ptr(X_new), x_dtype,
+                                          tau, align, _ptr(ws), ws_bytes, _ptr(blob_out),
+                                          stride_out, out, _stream(stream)))
+    return list(out)
 
 
 def jolt_read_status(cfg, n_units, ws, stream=None) -> int:

@@ -32,7 +32,7 @@ def header_functions():
 
 def test_library_exports_every_declared_symbol():
     names = header_functions()
-    assert len(names) == 20
+    assert len(names) == 22
     lib = ctypes.CDLL(J.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -129,9 +129,15 @@ def _attn_desc(H=4, T=300, D=128, rT=8, rd=16, b=4):
 
 
 def test_attend_workspace_size():
-    # per (group, head, chunk of 128 tokens): nq * (max, sum, z[D], cv[128]) floats
-    assert J.jolt_attend_workspace_size(3, 4, 300, 128, 4) == 3 * 4 * 3 * 4 * (2 + 128 + 128) * 4
-    assert J.jolt_attend_workspace_size(1, 1, 128, 32, 1) == 1 * (2 + 32 + 128) * 4
+    # per (group, head, chunk of 128 tokens): nq * (max, sum, z[D], cv[128])
+    # floats, padded to 256 bytes; then per (group, head) the query
+    # coefficients, (128 + D) x nq' floats with nq' = nq rounded up to 1, 2, 4, 8
+    def want(G, H, T, D, nq):
+        part = G * H * (-(-T // 128)) * nq * (2 + D + 128) * 4
+        npad = 1 if nq <= 1 else 2 if nq <= 2 else 4 if nq <= 4 else 8
+        return -(-part // 256) * 256 + G * H * (128 + D) * npad * 4
+    for args in [(3, 4, 300, 128, 4), (1, 1, 128, 32, 1), (2, 5, 1000, 64, 3), (1, 2, 1, 32, 8)]:
+        assert J.jolt_attend_workspace_size(*args) == want(*args), args
     assert J.jolt_attend_workspace_size(1, 1, 128, 32, 9) == 0
     assert J.jolt_attend_workspace_size(0, 1, 128, 32, 1) == 0
 
@@ -171,4 +177,51 @@ def test_attend_rejects_bad_arguments_before_launch(case):
         q = None
     arr = (J.JoltBlobDesc * 2)(*desc)
     st = J.lib().jolt_attend(1, arr, blob, stride, q, nq, 0.125, ws, ws_bytes, out, None)
+    assert st == want
+
+
+def test_admit_workspace_size():
+    # per unit: 256 bytes (signs), Y as double-float (H tau D 8), M in f64
+    # (64 x 64 x 8), chain rows as double-float (H 64 D 8), padded to 256
+    def want(U, H, tau, D):
+        return U * (-(-(256 + H * tau * D * 8 + 64 * 64 * 8 + H * 64 * D * 8) // 256) * 256)
+    for args in [(2, 4, 10, 32), (16, 32, 128, 128), (1, 3, 1, 64)]:
+        assert J.jolt_admit_workspace_size(*args) == want(*args)
+    assert J.jolt_admit_workspace_size(1, 4, 0, 32) == 0
+    assert J.jolt_admit_workspace_size(1, 4, 8, 48) == 0
+
+
+@pytest.mark.parametrize("case", ["tau0", "dtype", "align", "overlap", "mismatch", "rank",
+                                  "ws", "null", "odd_out"])
+def test_admit_rejects_bad_arguments_before_launch(case):
+    desc = [_attn_desc(T=300, rT=8, rd=16, b=4), _attn_desc(T=300, rT=300, rd=32, b=2)]
+    dev = 1 << 40
+    blob_in, sin, blob_out, sout = dev, 1 << 20, dev + (4 << 20), 2 << 20
+    tau, align, dt = 16, 256, J.BF16
+    ws_bytes = J.jolt_admit_workspace_size(2, 4, 16, 128)
+    X = ws = dev + (64 << 20)
+    want = J.ERR_INVALID
+    if case == "tau0":
+        tau = 0
+    elif case == "dtype":
+        dt = J.F16
+    elif case == "align":
+        align = 96
+    elif case == "overlap":
+        blob_out = dev + (1 << 20)
+    elif case == "mismatch":
+        desc[1] = _attn_desc(T=256)
+    elif case == "rank":
+        desc[0] = _attn_desc(T=300, rT=80)
+    elif case == "ws":
+        ws_bytes -= 256
+        want = J.ERR_WORKSPACE
+    elif case == "null":
+        X = None
+    elif case == "odd_out":
+        blob_out += 128
+    arr = (J.JoltBlobDesc * 2)(*desc)
+    out = (J.JoltBlobDesc * 2)()
+    st = J.lib().jolt_admit(2, arr, blob_in, sin, X, dt, tau, align, ws, ws_bytes, blob_out, sout,
+                            out, None)
     assert st == want

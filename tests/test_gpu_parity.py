@@ -499,3 +499,143 @@ def test_attend_edge_shapes(T, D, nq, rT, rd, b):
     out = _attend_gpu(blobs, np.zeros_like(q), 1.0)
     mean = oj.decode_unit(blobs[1]).mean(axis=1)
     assert np.allclose(out[0], np.repeat(mean[:, None, :], nq, axis=1), rtol=1e-5, atol=1e-5)
+
+
+# ------------------------------------------------ admission of a new token block
+def _upload(blobs):
+    import torch
+    stride = -(-max(len(b) for b in blobs) // 256) * 256
+    host = np.zeros((len(blobs), stride), dtype=np.uint8)
+    for i, b in enumerate(blobs):
+        host[i, :len(b)] = np.frombuffer(b, dtype=np.uint8)
+    return torch.from_numpy(host).cuda(), stride
+
+
+def _admit_gpu(blobs, Xn_stored, dtype):
+    """jolt_admit on oracle blobs uploaded from the host; the new blobs back
+    as bytes."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    dev, stride = _upload(blobs)
+    arr = np.ascontiguousarray(np.stack(Xn_stored))
+    if dtype == "bf16":
+        X = torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16).cuda()
+    else:
+        X = torch.from_numpy(arr).cuda()
+    out, sout, desc = codec.admit([_desc_of(b) for b in blobs], dev, stride, X)
+    torch.cuda.synchronize()
+    host = out.cpu().numpy()
+    return [host[i, :desc[i].bytes].tobytes() for i in range(len(blobs))], desc
+
+
+def _compare_admitted(gpu, ref):
+    """Header and the old tokens' sections bit for bit; the new fp16 rows of
+    U_T or G: the GPU rounds a double-float value, the oracle an f64 one, so
+    they agree except where the value sits within ~2^-40 of an fp16 tie
+    (allowed: one fp16 step, at most 1e-3 of the rows' entries); new scales
+    by at most one fp16 step and codes by at most one, at most 1e-4 of them
+    (or 8), as for encode.  Returns (rows differing, codes differing, codes)."""
+    hg, hr = oj.parse_header(gpu), oj.parse_header(ref)
+    assert len(gpu) == len(ref) and gpu[:256] == ref[:256]
+    H, T, D, rT, rd, b = hr["H"], hr["T"], hr["D"], hr["rT"], hr["rd"], hr["b"]
+    f16 = lambda blob, off, n: np.frombuffer(blob, np.float16, n, off)
+    nrow = 0
+    if not hr["flags"] & 1:
+        a, r = f16(gpu, hr["UT"], T * rT), f16(ref, hr["UT"], T * rT)
+        nrow += _ulp_diffs(a, r)
+    else:
+        a, r = f16(gpu, hr["G"], H * T * rd), f16(ref, hr["G"], H * T * rd)
+        nrow += _ulp_diffs(a, r)
+    for k in ("Ud",):
+        if hr[k]:
+            assert gpu[hr[k]:hr[k] + 2 * D * rd] == ref[hr[k]:hr[k] + 2 * D * rd]
+    if not hr["flags"] & 1:
+        assert gpu[hr["G"]:hr["G"] + 2 * H * rT * rd] == ref[hr["G"]:hr["G"] + 2 * H * rT * rd]
+    nbad = ncode = 0
+    if b > 0:
+        n = H * T * D
+        sg, sr = f16(gpu, hr["scale"], H * T), f16(ref, hr["scale"], H * T)
+        assert _ulp_diffs(sg, sr) <= max(1e-4 * sg.size, 8)
+        qg = oj.unpack_codes(gpu[hr["codes"]:hr["codes"] + n * b // 8], n, b)
+        qr = oj.unpack_codes(ref[hr["codes"]:hr["codes"] + n * b // 8], n, b)
+        d = np.abs(qg - qr)
+        assert d.max(initial=0) <= 1
+        nbad, ncode = int(np.count_nonzero(d)), n
+    return nrow, nbad, ncode
+
+
+def _ulp_diffs(a, r):
+    """Entries of two fp16 arrays that differ; every difference one fp16 step."""
+    ai, ri = a.view(np.int16).astype(np.int64), r.view(np.int16).astype(np.int64)
+    diff = ai != ri
+    if diff.any():
+        step = np.abs(np.nextafter(r[diff], np.float16(np.inf)).astype(np.float64) -
+                      r[diff].astype(np.float64))
+        assert np.all(np.abs(a[diff].astype(np.float64) - r[diff].astype(np.float64)) <= step * 1.0001)
+    return int(np.count_nonzero(diff))
+
+
+# (rT index, rd index, b index) per unit, cycling: truncated and whole token
+# ranks, truncated and whole feature ranks, every bit width
+_ADM_CANDS = [(0, 0, 2), (-1, 0, 1), (1, -1, 3), (-1, -1, 0), (2, 1, 2), (-1, 1, 3), (0, -1, 1),
+              (-1, -1, 2)]
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_admit_matches_oracle(name):
+    """The oracle encodes each unit (its own factors, candidates cycling
+    through every branch); the GPU and the oracle admit tau new tokens of
+    the same distribution (the generator with the next seed) into those
+    blobs."""
+    import dataclasses
+    w, r = SMALL[name], gpu_run(name)
+    facs = oracle_tables(name)[1]
+    tau = 40
+    wn = dataclasses.replace(w, seed=w.seed + 1)
+    nrow = nbad = ncode = 0
+    for rnd in range(2):
+        blobs, refs, Xn = [], [], []
+        for u in range(len(r.units)):
+            iT, id_, ib = _ADM_CANDS[(rnd * len(r.units) + u) % len(_ADM_CANDS)]
+            f = facs[u]
+            blob = oj.encode_unit(r.X64[u], f, r.signs[u], f.rT_list[iT], f.rd_list[id_],
+                                  w.bits[ib], w.block)
+            xs = np.ascontiguousarray(kvgen.make_unit(wn, u)[:, :tau])
+            blobs.append(blob)
+            refs.append(oj.admit_unit(blob, kvgen.unit_values_f64(w, xs)))
+            Xn.append(xs)
+        outs, desc = _admit_gpu(blobs, Xn, w.dtype)
+        for g, ref, d in zip(outs, refs, desc):
+            assert d.bytes == len(ref)
+            a, c, n = _compare_admitted(g, ref)
+            nrow, nbad, ncode = nrow + a, nbad + c, ncode + n
+    assert nbad <= max(1e-4 * ncode, 8), (nbad, ncode)
+    assert nrow <= 8, nrow
+
+
+def test_admit_full_size_random_blobs():
+    """mistral_t1024's units ([32, 1024, 128]) as random blobs of mixed
+    candidates, 128 new tokens each, every admitted blob against the
+    oracle's."""
+    w = kvgen.WORKLOADS["mistral_t1024"]
+    rng = np.random.default_rng(51)
+    tau = 128
+    rT = [oj.resolve(x, w.T) for x in w.rT]
+    rd = [oj.resolve(x, w.D) for x in w.rd]
+    blobs, refs, Xn = [], [], []
+    for u in range(w.n_units):
+        blob = oj.random_blob(rng, w.H, w.T, w.D, rT[u % len(rT)], rd[(u // 2) % len(rd)],
+                              w.bits[(u // 5) % len(w.bits)], kvgen.make_signs(w, u))
+        x = rng.standard_normal((w.H, tau, w.D)).astype(np.float32)
+        xb = kvgen.round_to_bf16(x)
+        x64 = kvgen.bf16_to_f32(xb).astype(np.float64)
+        blobs.append(blob)
+        refs.append(oj.admit_unit(blob, x64))
+        Xn.append(xb)
+    outs, desc = _admit_gpu(blobs, Xn, "bf16")
+    nrow = nbad = ncode = 0
+    for g, r in zip(outs, refs):
+        a, c, n = _compare_admitted(g, r)
+        nrow, nbad, ncode = nrow + a, nbad + c, ncode + n
+    assert nbad <= max(1e-4 * ncode, 8), (nbad, ncode)
+    assert nrow <= 1e-3 * w.n_units * tau * 64, nrow
