@@ -203,6 +203,9 @@ __global__ void __launch_bounds__(128) attend_prep_kernel(AttArgs a) {
   constexpr int D = 32 * EPT;
   __shared__ float vq[NQ][D], wq[NQ][KM];
   __shared__ __half st_Ud[D * 64], st_G[64 * (KM > D ? KM : D)];
+  // attend_chunk may start now: it stages its own data first and waits for
+  // this grid before it reads c and v~
+  asm volatile("griddepcontrol.launch_dependents;");
   const int h = blockIdx.x, gl = blockIdx.y, g = a.g0 + gl;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int T = a.T, H = a.H, nq = a.nq;
@@ -286,8 +289,10 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
                          : (const __half*)(vb + vu.off_UT) + (size_t)t0 * vu.rT;
   const size_t kcb = (size_t)D * ku.b / 8, vcb = (size_t)D * vu.b / 8;   // code bytes per row
 
-  // ---- everything the CTA reads, in flight at once
-  copy_async(qcs, a.qc + ((size_t)g * H + h) * (KM + D) * NQ, (KM + D) * NQ * 4, tid, ATT_CHUNK);
+  // the merge grid may start staging its factors
+  asm volatile("griddepcontrol.launch_dependents;");
+  // ---- everything the CTA reads, in flight at once (c and v~ once the
+  // prep grid has finished)
   if (ku.b > 0)
     copy_async(data, kb + ku.off_codes + ((size_t)h * T + t0) * kcb, (int)(n * kcb), tid,
                ATT_CHUNK);
@@ -301,6 +306,9 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
                        ? __half2float(((const __half*)(kb + ku.off_scale))[(size_t)h * T + t]) : 0.f;
   sv[tid] = (vu.b > 0 && t < T)
                 ? __half2float(((const __half*)(vb + vu.off_scale))[(size_t)h * T + t]) : 0.f;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  copy_async(qcs, a.qc + ((size_t)g * H + h) * (KM + D) * NQ, (KM + D) * NQ * 4, tid, ATT_CHUNK);
+  asm volatile("cp.async.commit_group;" ::: "memory");
   asm volatile("cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
 
@@ -453,6 +461,7 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(AttArgs a) {
   if (!vfT)
     stage_halves(st_G, (const __half*)(vb + vu.off_G) + (size_t)h * vu.rT * vu.rd,
                  vu.rT * vu.rd, tid, 128);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the global max M and sum L of this query
   float m = -INFINITY;
   for (int c = tid; c < nch; c += 128) m = fmaxf(m, base[c * rf + i]);
@@ -534,9 +543,26 @@ jolt_status launch_attend(const AttArgs& a, int ng, cudaStream_t st) {
   }
   attend_prep_kernel<EPT, NQ><<<dim3(a.H, ng), 128, 0, st>>>(a);
   JOLT_LAUNCH_CHECK();
-  attend_chunk_kernel<EPT, NQ><<<dim3(a.nch, a.H, ng), ATT_CHUNK, smem, st>>>(a);
+  // the chunk and merge grids are programmatic dependents of the grid
+  // before them: their CTAs start staging data while it still runs and wait
+  // for it (griddepcontrol.wait) before reading its results
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.stream = st;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(a.nch, a.H, ng);
+  cfg.blockDim = dim3(ATT_CHUNK);
+  cfg.dynamicSmemBytes = smem;
+  JOLT_CUDA_TRY(cudaLaunchKernelEx(&cfg, attend_chunk_kernel<EPT, NQ>, a));
   JOLT_LAUNCH_CHECK();
-  attend_merge_kernel<EPT><<<dim3(a.H, ng, a.nq), 128, 0, st>>>(a);
+  cfg.gridDim = dim3(a.H, ng, a.nq);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  JOLT_CUDA_TRY(cudaLaunchKernelEx(&cfg, attend_merge_kernel<EPT>, a));
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
