@@ -147,3 +147,18 @@ def admit(desc: Sequence[J.JoltBlobDesc], blob: torch.Tensor, stride: int, X_new
                          device=blob.device)
     d = J.jolt_admit(desc, blob, stride, X_new, dt, tau, align, ws, out, sout, stream=stream)
     return out, sout, d
+
+
+def blob_desc(header: bytes) -> J.JoltBlobDesc:
+    """The description of a serialized unit read from its 256-byte header
+    (little-endian: magic, version, H, T, D, r_T, r_d, b, block, flags, then
+    the section offsets and the total size)."""
+    import struct
+    magic, ver, H, T, D, rT, rd, b, block, flags = struct.unpack_from("<IIiiiiiiiI", header, 0)
+    if magic != 0x544C4F4A:
+        raise ValueError("not a JoLT blob header")
+    offs = struct.unpack_from("<QQQQQQ", header, 40)
+    d = J.JoltBlobDesc()
+    d.H, d.T, d.D, d.rT, d.rd, d.b, d.block, d.flags = H, T, D, rT, rd, b, block, flags
+    d.off_UT, d.off_Ud, d.off_G, d.off_scale, d.off_codes, d.bytes = offs
+    return d

@@ -109,8 +109,9 @@ def test_allocation_total_distortion_vs_oracle(name):
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_blob_header_and_scored_distortion(name):
-    """The oracle decodes the GPU's blob; its distortion is the GPU's table
-    entry for the chosen candidate."""
+    """The GPU's blob has the layout of its candidate, and the distortion of
+    what the GPU's own decoder rebuilds from it is the GPU's table entry for
+    that candidate (the sweep scores what is stored)."""
     w, r = SMALL[name], gpu_run(name)
     for i in range(len(r.units)):
         hd = oj.parse_header(r.blobs[i])
@@ -121,7 +122,9 @@ def test_blob_header_and_scored_distortion(name):
             assert hd[k] == lay[k]
         assert np.array_equal(hd["signs"], r.signs[i])
         assert r.cost[i, c] >= hd["bytes"]
-        d = oj.distortion(r.X64[i], oj.decode_unit(r.blobs[i]))
+        x = r.X64[i]
+        e = x - r.xhat32[i].astype(np.float64)
+        d = float(np.sum(e * e) / max(np.sum(x * x), 1e-300))
         assert close(r.dist[i, c], d, 1e-4, 1e-7), (i, c, r.dist[i, c], d)
 
 
@@ -202,17 +205,35 @@ def test_codes_match_oracle_quantizer(name):
 
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_decode_matches_oracle_decode(name):
+    """The oracle serializes candidates of its own factors (cycling through
+    every branch of the rebuild); the GPU decodes those blobs."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
     w, r = SMALL[name], gpu_run(name)
-    for i in range(len(r.units)):
-        ref = oj.decode_unit(r.blobs[i])
-        err = np.linalg.norm(r.xhat32[i] - ref) / max(np.linalg.norm(ref), 1e-30)
-        assert err <= 1e-5
-        # bf16 output: within bf16 rounding of the oracle's value plus the
-        # fp32 arithmetic error of the reconstruction (absolute, at 1e-5 of
-        # the RMS value)
-        g16 = kvgen.bf16_to_f32(r.xhat16[i]).astype(np.float64)
-        rms = np.linalg.norm(ref) / np.sqrt(ref.size)
-        assert np.all(np.abs(g16 - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * rms)
+    facs = oracle_tables(name)[1]
+    U = len(r.units)
+    for rnd in range(3):
+        blobs = []
+        for u in range(U):
+            iT, id_, ib = _ATT_CANDS[(rnd * U + u) % len(_ATT_CANDS)]
+            f = facs[u]
+            blobs.append(oj.encode_unit(r.X64[u], f, r.signs[u], f.rT_list[iT], f.rd_list[id_],
+                                        w.bits[ib], w.block))
+        dev, stride = _upload(blobs)
+        desc = [_desc_of(b) for b in blobs]
+        x32 = codec.decode(desc, dev, stride, J.F32).cpu().numpy()
+        x16 = codec.decode(desc, dev, stride, J.BF16).view(torch.int16).cpu().numpy()
+        for i in range(U):
+            ref = oj.decode_unit(blobs[i])
+            err = np.linalg.norm(x32[i] - ref) / max(np.linalg.norm(ref), 1e-30)
+            assert err <= 1e-5
+            # bf16 output: within bf16 rounding of the oracle's value plus the
+            # fp32 arithmetic error of the reconstruction (absolute, at 1e-5
+            # of the RMS value)
+            g16 = kvgen.bf16_to_f32(x16[i].view(np.uint16)).astype(np.float64)
+            rms = np.linalg.norm(ref) / np.sqrt(ref.size)
+            assert np.all(np.abs(g16 - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * rms)
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
