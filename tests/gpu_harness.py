@@ -59,7 +59,8 @@ class GpuRun:
 
 
 def run(w, units: Optional[Sequence[int]] = None, budget: Optional[int] = None,
-        serialize: bool = True, decode: bool = True, choice_override=None) -> GpuRun:
+        serialize: bool = True, decode: bool = True, choice_override=None,
+        refine: bool = False) -> GpuRun:
     ensure_built()
     units = list(range(w.n_units)) if units is None else list(units)
     xs, signs, sk = host_inputs(w, units)
@@ -73,7 +74,7 @@ def run(w, units: Optional[Sequence[int]] = None, budget: Optional[int] = None,
                enc.dist.cpu().numpy(), enc.cost.cpu().numpy(), st)
     if budget is None:
         budget = int(w.budget_bytes * len(units) // w.n_units)
-    enc.allocate(budget)
+    enc.allocate(budget, refine=refine)
     torch.cuda.synchronize()
     r.choice = enc.choice.cpu().numpy().astype(np.int64)
     r.lam = float(enc.lam.cpu().item())
