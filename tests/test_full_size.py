@@ -1,19 +1,27 @@
-"""The main path at the bench's size and launch configuration: mistral_t1024,
-16 units of [32, 1024, 128] bf16 in one batch, exact token mode, the
-bisection then the greedy swaps.  The oracle cannot factor 1024-token units
-in seconds, so this file checks what it can compute exactly at this size:
+"""The main path at full size on the four large configurations, in the
+launch the bench uses (all units of a configuration in one batch, the
+bisection then the greedy swaps):
+
+  mistral_t1024  8 groups x {K,V} of [32, 1024, 128], exact, 2x budget
+  mistral_t2048  8 groups x {K,V} of [32, 2048, 128], exact, 3x budget
+  llama_t1024    10 groups x {K,V} of [160, 1024, 128], exact, 2x budget
+  flash_t4096    8 groups x {K,V} of [32, 4096, 128], randomized, 2x budget
+
+The oracle cannot run its exhaustive grid on 1024-4096-token units in
+seconds, so each configuration checks what it can compute exactly:
 
   * the cost table, bit for bit (oracle cost_table);
   * the allocation and the greedy swaps, bit for bit, on the GPU's tables
     (oracle allocate / refine_greedy);
-  * every b = 0 entry of two sampled units against the exact ST-HOSVD tail
-    ||X||^2 - sum_{j < r_T} mu_j(r_d) of that unit (oracle feature mode,
-    token-Gram eigenvalues by numpy's eigvalsh), at the path's tolerance
-    (fp16 storage of the factors moves these values by ~1e-7 relative);
+  * every b = 0 entry of one sampled unit against its ST-HOSVD tail
+    ||X||^2 - ||G(r_T, r_d)||^2, at the path's tolerance (fp16 storage of
+    the factors moves these values by ~1e-7 relative): exact modes take the
+    token-Gram eigenvalues (numpy eigvalsh), the randomized mode the
+    oracle's own FlashJoLT factors on the same sketch;
   * the chosen candidate's table entry against the distortion of what the
-    GPU's decoder rebuilds from the blob, for every unit;
-  * the codes of four units against the oracle's quantizer on the blob's
-    stored factors (the same bar as the small parity tests).
+    GPU's decoder rebuilds from the blob (fp32 and bf16 output), every unit;
+  * the codes of up to four units against the oracle's quantizer on the
+    blob's stored factors (the bar of the small parity tests).
 """
 import numpy as np
 import pytest
@@ -25,74 +33,78 @@ from tests import gpu_harness as gh
 pytestmark = pytest.mark.gpu
 
 REL, ABS = 1e-3, 1e-6
-W = kvgen.WORKLOADS["mistral_t1024"]
-_RUN = {}
+BIG = ["mistral_t1024", "mistral_t2048", "llama_t1024", "flash_t4096"]
 
 
-def full_run():
-    if "r" not in _RUN:
-        _RUN["r"] = gh.run(W, refine=True)
-    return _RUN["r"]
-
-
-def test_full_size_status_and_cost_table():
-    r = full_run()
-    assert r.status == 0
-    rT = [oj.resolve(x, W.T) for x in W.rT]
-    rd = [oj.resolve(x, W.D) for x in W.rd]
-    ref = oj.cost_table(W.H, W.T, W.D, rT, rd, W.bits, W.block).reshape(-1)
-    for u in range(W.n_units):
-        assert np.array_equal(r.cost[u], ref)
-
-
-def test_full_size_allocation_and_refinement_bit_exact():
-    r = full_run()
-    z, lam, st = oj.allocate(r.dist, r.cost, W.budget_bytes, 256)
-    assert st == oj.ALLOC_OK and lam == r.lam
-    zr, _ = oj.refine_greedy(r.dist, r.cost, W.budget_bytes, np.array(z))
-    assert list(zr) == list(r.choice)
-    assert sum(int(r.cost[u, zr[u]]) for u in range(W.n_units)) <= W.budget_bytes
-
-
-@pytest.mark.parametrize("u", [0, 5])
-def test_full_size_b0_distortions_are_the_hosvd_tails(u):
-    r = full_run()
-    x = r.X64[u]
+def _b0_reference(w, x, sk):
+    """[n_rT][n_rd] of ||X - X~||^2 / ||X||^2 for the unrounded factors."""
     xn = float(np.sum(x * x))
+    rT = [oj.resolve(v, w.T) for v in w.rT]
+    rd = [oj.resolve(v, w.D) for v in w.rd]
+    out = np.zeros((len(rT), len(rd)))
+    if w.token_mode == "randomized":
+        fac = oj.factorize(x, w.rT, w.rd, "randomized", sk, w.power_iters)
+        for j, r_d in enumerate(rd):
+            ny = float(np.sum(fac.Y[r_d] ** 2))
+            g2 = np.sum(fac.G[r_d] ** 2, axis=(0, 2))      # per token rank
+            for i, r_T in enumerate(rT):
+                cap = ny if r_T == w.T else float(np.sum(g2[:r_T]))
+                out[i, j] = max(xn - cap, 0.0) / xn
+        return out
     _, V = oj.feature_mode(x)
-    rT = [oj.resolve(v, W.T) for v in W.rT]
-    rd = [oj.resolve(v, W.D) for v in W.rd]
-    d = r.dist[u].reshape(len(rT), len(rd), len(W.bits))
     for j, r_d in enumerate(rd):
-        Y = x if r_d == W.D else np.einsum("htd,dj->htj", x, V[:, :r_d])
+        Y = x if r_d == w.D else np.einsum("htd,dj->htj", x, V[:, :r_d])
         A = oj.token_unfolding(Y)
         mu = np.linalg.eigvalsh(A @ A.T)[::-1]
         for i, r_T in enumerate(rT):
-            cap = float(np.sum(mu[:r_T])) if r_T < W.T else float(np.sum(Y * Y))
-            ref = max(xn - cap, 0.0) / xn
-            got = d[i, j, W.bits.index(0)]
-            assert abs(got - ref) <= max(REL * ref, ABS), (r_T, r_d, got, ref)
+            cap = float(np.sum(mu[:r_T])) if r_T < w.T else float(np.sum(Y * Y))
+            out[i, j] = max(xn - cap, 0.0) / xn
+    return out
 
 
-def test_full_size_chosen_candidate_is_what_decodes():
-    r = full_run()
-    for u in range(W.n_units):
+@pytest.mark.parametrize("name", BIG)
+def test_full_size_config(name):
+    from tests.test_gpu_parity import check_codes_against_oracle
+    w = kvgen.WORKLOADS[name]
+    r = gh.run(w, refine=True)
+    U = w.n_units
+    assert r.status == 0
+    # cost table
+    rT = [oj.resolve(x, w.T) for x in w.rT]
+    rd = [oj.resolve(x, w.D) for x in w.rd]
+    ref = oj.cost_table(w.H, w.T, w.D, rT, rd, w.bits, w.block).reshape(-1)
+    for u in range(U):
+        assert np.array_equal(r.cost[u], ref)
+    # bisection and greedy swaps on the GPU's tables
+    z, lam, st = oj.allocate(r.dist, r.cost, w.budget_bytes, 256)
+    assert st == oj.ALLOC_OK and lam == r.lam
+    zr, _ = oj.refine_greedy(r.dist, r.cost, w.budget_bytes, np.array(z))
+    assert list(zr) == list(r.choice)
+    assert sum(int(r.cost[u, zr[u]]) for u in range(U)) <= w.budget_bytes
+    # b = 0 entries of a sampled unit (a K unit with its outlier channels)
+    u = 2
+    sk = None if r.sketch is None else r.sketch[u].astype(np.float64)
+    b0 = _b0_reference(w, r.X64[u], sk)
+    d = r.dist[u].reshape(len(rT), len(rd), len(w.bits))[:, :, w.bits.index(0)]
+    bad = np.abs(d - b0) > np.maximum(REL * b0, ABS)
+    assert not bad.any(), [(rT[i], rd[j], d[i, j], b0[i, j]) for i, j in np.argwhere(bad)]
+    # the chosen candidates are what decodes (fp32 and bf16 output)
+    for u in range(U):
         x = r.X64[u]
+        xx = float(np.sum(x * x))
         e = x - r.xhat32[u]
-        got = float(np.sum(e * e) / np.sum(x * x))
+        got = float(np.sum(e * e)) / xx
         c = int(r.choice[u])
         assert abs(r.dist[u, c] - got) <= max(1e-4 * got, 1e-7), (u, r.dist[u, c], got)
-
-
-def test_full_size_codes_match_oracle_quantizer():
-    from tests.test_gpu_parity import check_codes_against_oracle
-    r = full_run()
-    bad = tot = 0
-    for u in range(W.n_units):
+        x16 = kvgen.bf16_to_f32(r.xhat16[u]).astype(np.float64)
+        assert np.all(np.abs(x16 - r.xhat32[u]) <= 2.0 ** -8 * np.abs(r.xhat32[u]) + 1e-30)
+    # codes of up to four units with b > 0
+    bad = tot = done = 0
+    for u in range(U):
+        if done == 4:
+            break
         if oj.parse_header(r.blobs[u])["b"] == 0:
             continue
-        nbad, n = check_codes_against_oracle(r.X64[u], r.blobs[u], W.D)
-        bad, tot = bad + nbad, tot + n
-        if tot > 4 * W.elems_per_unit:
-            break
-    assert tot > 0 and bad <= max(1e-4 * tot, 8), (bad, tot)
+        nbad, n = check_codes_against_oracle(r.X64[u], r.blobs[u], w.D)
+        bad, tot, done = bad + nbad, tot + n, done + 1
+    assert bad <= max(1e-4 * tot, 8), (bad, tot)
