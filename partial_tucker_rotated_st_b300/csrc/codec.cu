@@ -960,6 +960,13 @@ jolt_status encode_run(const Layout& L, int U, const void* X, const int8_t* sign
 jolt_status decode_run(int U, const jolt_blob_desc* desc, const char* blob, size_t stride,
                        void* xhat, int out_dtype, cudaStream_t st) {
   const int H = desc[0].H, T = desc[0].T, D = desc[0].D;
+  // D = 128: the tensor-core decoder (16-byte vector loads of codes and
+  // whole-mode cores, 16-byte stores)
+  bool tc_ok = decode_tc_supported(D) && ((uintptr_t)xhat % 16) == 0 &&
+               ((uintptr_t)blob % 16) == 0 && (stride % 16) == 0;
+  for (int u = 0; u < U && tc_ok; ++u)
+    tc_ok = (desc[u].off_codes % 16) == 0 && (desc[u].off_G % 16) == 0;
+  if (tc_ok) return decode_tc_run(U, desc, blob, stride, xhat, out_dtype, st);
   for (int u0 = 0; u0 < U; u0 += DEC_MAX_UNITS) {
     const int nu = (U - u0) < DEC_MAX_UNITS ? (U - u0) : DEC_MAX_UNITS;
     DecArgs a;

@@ -201,6 +201,9 @@ jolt_status encode_run(const Layout& L, int n_units, const void* X, const int8_t
                        size_t blob_stride, jolt_blob_desc* desc, cudaStream_t st);
 jolt_status decode_run(int n_units, const jolt_blob_desc* desc, const char* blob,
                        size_t blob_stride, void* xhat, int out_dtype, cudaStream_t st);
+bool decode_tc_supported(int D);
+jolt_status decode_tc_run(int n_units, const jolt_blob_desc* desc, const char* blob,
+                          size_t blob_stride, void* xhat, int out_dtype, cudaStream_t st);
 size_t admit_ws_unit_bytes(int H, int tau, int D);
 jolt_status admit_run(int n_units, const jolt_blob_desc* desc_in, const char* blob_in,
                       size_t stride_in, const void* X_new, int x_dtype, int tau, int align,
