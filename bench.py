@@ -344,7 +344,13 @@ def run_ours(args):
                        "budget_bytes": budget, "token_mode": w.token_mode,
                        "allocator": "lambda bisection + greedy swaps",
                        "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas{ws}"},
-            "decode": {"value": dec_gbs, "unit": "GB/s"},
+            "decode": {"value": dec_gbs, "unit": "GB/s",
+                       "roofline": {"kernel": "decode_tc_kernel", "bound": "hbm",
+                                    "achieved": (blob_bytes + 2 * w.elems_per_unit * U) / dec_t / 1e9,
+                                    "peak": hbm, "unit": "GB/s",
+                                    "frac": (blob_bytes + 2 * w.elems_per_unit * U) / dec_t / 1e9 / hbm,
+                                    "bytes_algorithmic": int(blob_bytes + 2 * w.elems_per_unit * U),
+                                    "traffic": None}},
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "dominant_stage": dom,
             "wall_ms_per_step": 1e3 * wall / args.steps,
