@@ -843,16 +843,13 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
       float cp[RPT], cq[RPT];
       ld_rows<RPT>(M + p * LDM, l16, cp);
       ld_rows<RPT>(M + q * LDM, l16, cq);
-      // the three dot products on packed pairs of rows (f32x2 FMAs)
-      float2 a2 = make_float2(0.f, 0.f), b2 = a2, g2 = a2;
+      float a = 0.f, b = 0.f, g = 0.f;
 #pragma unroll
-      for (int i = 0; i < RPT; i += 2) {
-        const float2 p2 = make_float2(cp[i], cp[i + 1]), q2 = make_float2(cq[i], cq[i + 1]);
-        a2 = __ffma2_rn(p2, p2, a2);
-        b2 = __ffma2_rn(q2, q2, b2);
-        g2 = __ffma2_rn(p2, q2, g2);
+      for (int i = 0; i < RPT; ++i) {
+        a = fmaf(cp[i], cp[i], a);
+        b = fmaf(cq[i], cq[i], b);
+        g = fmaf(cp[i], cq[i], g);
       }
-      float a = a2.x + a2.y, b = b2.x + b2.y, g = g2.x + g2.y;
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) {
         a += __shfl_xor_sync(0xffffffffu, a, o);
@@ -867,14 +864,10 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
         const float tt = __fdividef(copysignf(1.f, zeta), fabsf(zeta) + __fsqrt_rn(fmaf(zeta, zeta, 1.f)));
         const float c = rsqrtf(fmaf(tt, tt, 1.f)), s = tt * c;
         float np_[RPT], nq_[RPT];
-        const float2 c2 = make_float2(c, c), s2 = make_float2(s, s), ns2 = make_float2(-s, -s);
 #pragma unroll
-        for (int i = 0; i < RPT; i += 2) {
-          const float2 p2 = make_float2(cp[i], cp[i + 1]), q2 = make_float2(cq[i], cq[i + 1]);
-          const float2 n1 = __ffma2_rn(ns2, q2, __fmul2_rn(c2, p2));
-          const float2 n2 = __ffma2_rn(s2, p2, __fmul2_rn(c2, q2));
-          np_[i] = n1.x; np_[i + 1] = n1.y;
-          nq_[i] = n2.x; nq_[i + 1] = n2.y;
+        for (int i = 0; i < RPT; ++i) {
+          np_[i] = c * cp[i] - s * cq[i];
+          nq_[i] = s * cp[i] + c * cq[i];
         }
         st_rows<RPT>(M + p * LDM, l16, np_);
         st_rows<RPT>(M + q * LDM, l16, nq_);
