@@ -93,6 +93,19 @@ class Encoder:
         desc = self.serialize(X, signs, choice, stream)
         return EncodeResult(self.dist, self.cost, choice, float("nan"), -1, self.blob, desc)
 
+    def blobs_to_host(self, desc: Sequence[J.JoltBlobDesc], out: torch.Tensor, stream=None) -> int:
+        """Copy the serialized bytes of every unit (desc[u].bytes of slot u,
+        not the slot padding) back to back into the 1-D uint8 host tensor
+        `out` (pinned for an asynchronous copy); returns the byte count."""
+        off = 0
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            for u, d in enumerate(desc):
+                n = int(d.bytes)
+                out[off:off + n].copy_(self.blob[u, :n], non_blocking=True)
+                off += n
+        return off
+
     def status(self) -> int:
         return J.jolt_read_status(self.cfg, self.U, self.ws)
 
