@@ -102,14 +102,25 @@ __device__ __forceinline__ float* tf32_at(unsigned char* op, int row, int k) {
 // A row of KW values v[k] = src[k * step] (k < n, else 0), every load issued
 // before any is used; then stored as tf32 row `row` of an operand.
 template <int KW>
-__device__ __forceinline__ void gather_row(unsigned char* op, int row, const __half* src,
-                                           long long step, int n, bool valid) {
-  float v[KW];
+__device__ __forceinline__ void load_row(__half (&v)[KW], const __half* src, long long step, int n,
+                                         bool valid) {
 #pragma unroll
-  for (int k = 0; k < KW; ++k) v[k] = (valid && k < n) ? __half2float(src[k * step]) : 0.f;
+  for (int k = 0; k < KW; ++k) v[k] = (valid && k < n) ? src[k * step] : __float2half(0.f);
+}
+template <int KW>
+__device__ __forceinline__ void store_row(unsigned char* op, int row, const __half (&v)[KW]) {
 #pragma unroll
   for (int k = 0; k < KW; k += 4)
-    *reinterpret_cast<float4*>(tf32_at(op, row, k)) = make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+    *reinterpret_cast<float4*>(tf32_at(op, row, k)) =
+        make_float4(__half2float(v[k]), __half2float(v[k + 1]), __half2float(v[k + 2]),
+                    __half2float(v[k + 3]));
+}
+template <int KW>
+__device__ __forceinline__ void gather_row(unsigned char* op, int row, const __half* src,
+                                           long long step, int n, bool valid) {
+  __half v[KW];
+  load_row<KW>(v, src, step, n, valid);
+  store_row<KW>(op, row, v);
 }
 
 __host__ __device__ constexpr uint32_t idesc_f16h(int M, int N) {
@@ -127,9 +138,8 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 // table of four fp16 +-1 values for each 4-bit sign pattern.
 template <int B>
 __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char* sH, int r,
-                                               int half, const uint32_t* __restrict__ cw,
-                                               bool in, const unsigned char* sb,
-                                               const uint2* sgn) {
+                                               int half, const uint4 (&cq)[4], bool in,
+                                               const unsigned char* sb, const uint2* sgn) {
   constexpr int PER = 32 / B, M = 8 / B, NW = 64 * B / 32;   // words in 64 codes
   constexpr uint32_t MASK = B == 8 ? 0xFFFFFFFFu : (B == 4 ? 0x0F0F0F0Fu : 0x03030303u);
   constexpr uint32_t BIAS = 0x64006400u | (1u << (B - 1)) | (1u << (B - 1 + 16));
@@ -138,8 +148,7 @@ __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char*
   uint32_t w[NW];
 #pragma unroll
   for (int q = 0; q < NW / 4; ++q) {
-    const uint4 v = in ? reinterpret_cast<const uint4*>(cw + half * NW)[q] : make_uint4(0, 0, 0, 0);
-    w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    w[4 * q] = cq[q].x; w[4 * q + 1] = cq[q].y; w[4 * q + 2] = cq[q].z; w[4 * q + 3] = cq[q].w;
   }
 #pragma unroll
   for (int wi = 0; wi < NW; ++wi)
@@ -181,7 +190,7 @@ __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char*
 }
 
 template <int KW>
-__global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_constant__ DecTcArgs a) {
+__global__ void __launch_bounds__(DT_THREADS, KW == 32 ? 2 : 1) decode_tc_kernel(const __grid_constant__ DecTcArgs a) {
   constexpr int NCH = KW / 32;                 // swizzle atoms per tf32 row
   extern __shared__ __align__(1024) unsigned char dtc_raw[];
   unsigned char* base = (unsigned char*)(((uintptr_t)dtc_raw + 1023) & ~(uintptr_t)1023);
@@ -215,6 +224,35 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
   const int k8 = (kz + 7) & ~7;
   const int rT8 = (rT + 7) & ~7, rd8 = (rd + 7) & ~7, rd16 = (rd + 15) & ~15;
 
+  // ---- every global read of the CTA issued first: this thread's half row of
+  // codes, its scale, the rows it gathers for the low-rank operands
+  const __half* UT = reinterpret_cast<const __half*>(blob + du.off_UT);
+  const __half* Ud = reinterpret_cast<const __half*>(blob + du.off_Ud);
+  const __half* G = reinterpret_cast<const __half*>(blob + du.off_G);
+  const __half* Gh = G + (size_t)h * rT * rd;
+  uint4 cq[4];                                 // up to 64 bytes of codes
+  {
+    const uint4* cw = reinterpret_cast<const uint4*>(
+        blob + du.off_codes + ((unsigned long long)h * T + (in ? row : 0)) * (DT_D * b / 8) +
+        half * (8 * b));
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      cq[q] = (b > 0 && in && q < b / 2) ? cw[q] : make_uint4(0, 0, 0, 0);
+  }
+  const float s = (b > 0 && in) ? __half2float(reinterpret_cast<const __half*>(blob + du.off_scale)
+                                                   [(size_t)h * T + row]) * rsqrtf((float)DT_D)
+                                : 0.f;
+  __half g1[KW], g2[KW];   // first-product operand row; mode 0: the U_d row of the second
+  if (mode == 0 || mode == 1) {
+    if (half == 0) load_row<KW>(g1, UT + (size_t)(in ? row : 0) * rT, 1, rT, in);
+    else if (mode == 0) load_row<KW>(g1, Gh + (r < rd ? r : 0), rd, rT, r < rd);
+    else load_row<KW>(g1, Gh + r, DT_D, rT, true);
+  } else if (mode == 2) {
+    if (half == 0) load_row<KW>(g1, G + ((size_t)h * T + (in ? row : 0)) * rd, 1, rd, in);
+    else load_row<KW>(g1, Ud + (size_t)r * rd, 1, rd, true);
+  }
+  if (mode == 0 && half == 1) load_row<KW>(g2, Ud + (size_t)r * rd, 1, rd, true);
+
   if (t == 0) {
     tc::mbar_init(tc::smem_u32(&S->mma), 1);
     tc::fence_barrier_init();
@@ -243,34 +281,18 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
 
   // ---- residual operands: codes (A) and H diag(sigma) (B), fp16
   if (b > 0) {
-    const uint32_t* cw = reinterpret_cast<const uint32_t*>(
-        blob + du.off_codes + ((unsigned long long)h * T + (in ? row : 0)) * (DT_D * b / 8));
     const unsigned char* sb = reinterpret_cast<const unsigned char*>(blob) + 88;
-    if (b == 2) build_residual<2>(sC, sH, r, half, cw, in, sb, S->sgn);
-    else if (b == 4) build_residual<4>(sC, sH, r, half, cw, in, sb, S->sgn);
-    else build_residual<8>(sC, sH, r, half, cw, in, sb, S->sgn);
+    if (b == 2) build_residual<2>(sC, sH, r, half, cq, in, sb, S->sgn);
+    else if (b == 4) build_residual<4>(sC, sH, r, half, cq, in, sb, S->sgn);
+    else build_residual<8>(sC, sH, r, half, cq, in, sb, S->sgn);
   }
 
   // ---- low-rank operands of the first product: A = sA (half 0), B = sX (half 1)
-  const __half* UT = reinterpret_cast<const __half*>(blob + du.off_UT);
-  const __half* Ud = reinterpret_cast<const __half*>(blob + du.off_Ud);
-  const __half* G = reinterpret_cast<const __half*>(blob + du.off_G);
-  if (mode == 0 || mode == 1) {
-    const __half* Gh = G + (size_t)h * rT * rd;
-    if (half == 0) {
-      // A: this row of U_T (K = r_T)
-      gather_row<KW>(sA, r, UT + (size_t)(in ? row : 0) * rT, 1, rT, in);
-    } else if (mode == 0) {
-      // B rows j < rd16: G_h[k][j], k < r_T  (Z = U_T G_h)
-      if (r < rd16) gather_row<KW>(sX, r, Gh + (r < rd ? r : 0), rd, rT, r < rd);
-    } else {
-      // B rows d: G_h[k][d], k < r_T  (X~ = U_T G_h)
-      gather_row<KW>(sX, r, Gh + r, DT_D, rT, true);
-    }
-  } else if (mode == 2) {
-    // A: this row of G_h (K = r_d), B rows d: U_d[d][:]
-    if (half == 0) gather_row<KW>(sA, r, G + ((size_t)h * T + (in ? row : 0)) * rd, 1, rd, in);
-    else gather_row<KW>(sX, r, Ud + (size_t)r * rd, 1, rd, true);
+  if (mode == 0) {
+    if (half == 0) store_row<KW>(sA, r, g1);
+    else if (r < rd16) store_row<KW>(sX, r, g1);   // B rows j < rd16: G_h[k][j]
+  } else if (mode == 1 || mode == 2) {
+    store_row<KW>(half == 0 ? sA : sX, r, g1);
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc::tc_fence_before();
@@ -332,7 +354,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
         }
       }
     } else {
-      gather_row<KW>(sU, r, Ud + (size_t)r * rd, 1, rd, true);
+      store_row<KW>(sU, r, g2);
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc::tc_fence_before();
@@ -354,9 +376,6 @@ __global__ void __launch_bounds__(DT_THREADS, 1) decode_tc_kernel(const __grid_c
 
   // ---- epilogue: x^ = X~ + s R / sqrt(D) for columns [64 half, 64 half + 64)
   // of row r, staged row-major (padded rows)
-  const float s = (b > 0 && in) ? __half2float(reinterpret_cast<const __half*>(blob + du.off_scale)
-                                                   [(size_t)h * T + row]) * rsqrtf((float)DT_D)
-                                : 0.f;
   const bool f32 = (a.out_dtype == JOLT_F32);
   const int rowb = f32 ? DT_D * 4 + 16 : DT_D * 2 + 16;   // staging row stride (bytes)
   unsigned char* stg = sC;                                 // no operand is read any more
