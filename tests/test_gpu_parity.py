@@ -660,3 +660,30 @@ def test_admit_full_size_random_blobs():
         nrow, nbad, ncode = nrow + a, nbad + c, ncode + n
     assert nbad <= max(1e-4 * ncode, 8), (nbad, ncode)
     assert nrow <= 1e-3 * w.n_units * tau * 64, nrow
+
+
+@pytest.mark.parametrize("rT,rd,b", [(64, 48, 4), (48, 64, 8), (40, 128, 2), (200, 64, 4),
+                                     (64, 40, 0), (33, 17, 2)])
+def test_decode_wide_ranks_and_ragged_tiles(rT, rd, b):
+    """Truncated ranks above 32 (the decoder's 64-wide operand variant), odd
+    ranks, a ragged last tile (T = 200), fp32 and bf16 output, against the
+    oracle's decode of the same random blobs."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    rng = np.random.default_rng(rT * 7 + rd + b)
+    H, T, D = 3, 200, 128
+    blobs = [oj.random_blob(rng, H, T, D, rT, rd, b,
+                            np.where(rng.random(D) < 0.5, -1, 1).astype(np.int8))
+             for _ in range(2)]
+    dev, stride = _upload(blobs)
+    desc = [_desc_of(x) for x in blobs]
+    x32 = codec.decode(desc, dev, stride, J.F32).cpu().numpy()
+    x16 = codec.decode(desc, dev, stride, J.BF16).view(torch.int16).cpu().numpy()
+    for i in range(2):
+        ref = oj.decode_unit(blobs[i])
+        err = np.linalg.norm(x32[i] - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert err <= 1e-5, err
+        g16 = kvgen.bf16_to_f32(x16[i].view(np.uint16)).astype(np.float64)
+        rms = np.linalg.norm(ref) / np.sqrt(ref.size)
+        assert np.all(np.abs(g16 - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * rms)
