@@ -351,7 +351,7 @@ def run_ours(args):
                                     "peak": hbm, "unit": "GB/s",
                                     "frac": (blob_bytes + 2 * w.elems_per_unit * U) / dec_t / 1e9 / hbm,
                                     "bytes_algorithmic": int(blob_bytes + 2 * w.elems_per_unit * U),
-                                    "traffic": None}},
+                                    "traffic": decode_traffic(args.workload)}},
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "dominant_stage": dom,
             "wall_ms_per_step": 1e3 * wall / args.steps,
@@ -541,6 +541,29 @@ ATTEND_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profi
                               "attend_chunk_kernel_mistral_t1024.md")
 ATTEND_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tucker_rotated_st_b300",
                           "csrc", "attend.cu")
+
+
+DECODE_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
+                              "decode_tc_kernel_mistral_t1024.md")
+DECODE_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tucker_rotated_st_b300",
+                          "csrc", "decode_tc.cu")
+
+
+def decode_traffic(workload):
+    """DRAM bytes of one decoder launch from the committed ncu summary, while
+    decode_tc.cu is the source it was taken on."""
+    try:
+        txt = open(DECODE_PROFILE).read()
+        src = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    rec = {}
+    for line in txt.splitlines():
+        if line.startswith("traffic_record:"):
+            rec = json.loads(line.split(":", 1)[1])
+    if rec.get("decode_src_sha256") != src or rec.get("workload") != workload:
+        return None
+    return int(rec["dram_bytes_per_launch"])
 
 
 def attend_traffic(workload):
