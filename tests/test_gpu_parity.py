@@ -687,3 +687,31 @@ def test_decode_wide_ranks_and_ragged_tiles(rT, rd, b):
         g16 = kvgen.bf16_to_f32(x16[i].view(np.uint16)).astype(np.float64)
         rms = np.linalg.norm(ref) / np.sqrt(ref.size)
         assert np.all(np.abs(g16 - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5 * rms)
+
+
+@pytest.mark.parametrize("tau", [1, 3])
+def test_admit_single_tokens_and_zero_block(tau):
+    """The decode-time case, one (or a few) new tokens per unit, and a block
+    of zeros (zero residual, zero scales), against the oracle."""
+    w, r = SMALL["mistral_small"], gpu_run("mistral_small")
+    facs = oracle_tables("mistral_small")[1]
+    import dataclasses
+    wn = dataclasses.replace(w, seed=w.seed + 2)
+    for zero in (False, True):
+        blobs, refs, Xn = [], [], []
+        for u in range(len(r.units)):
+            iT, id_, ib = _ADM_CANDS[(u + 3 * tau) % len(_ADM_CANDS)]
+            f = facs[u]
+            blob = oj.encode_unit(r.X64[u], f, r.signs[u], f.rT_list[iT], f.rd_list[id_],
+                                  w.bits[ib], w.block)
+            xs = np.ascontiguousarray(kvgen.make_unit(wn, u)[:, :tau])
+            if zero:
+                xs = np.zeros_like(xs)
+            blobs.append(blob)
+            refs.append(oj.admit_unit(blob, kvgen.unit_values_f64(w, xs)))
+            Xn.append(xs)
+        outs, desc = _admit_gpu(blobs, Xn, w.dtype)
+        for g, ref, d in zip(outs, refs, desc):
+            assert d.bytes == len(ref)
+            nrow, nbad, _ = _compare_admitted(g, ref)
+            assert nrow == 0 and nbad == 0
