@@ -265,6 +265,10 @@ jolt_status jolt_encode(const jolt_config* cfg, int n_units, const void* X,
  * inverse transform, add X~].  The kernel reads each blob's header on the
  * device; desc gives the host the shapes for validation.
  *   xhat  [n_units][H][T][D] in out_dtype (JOLT_F32 or JOLT_BF16, RNE).
+ * D = 128 with 16-byte aligned xhat, blob, stride and code / core sections
+ * (as jolt_encode lays them out) runs on the tensor cores; other shapes run
+ * the same arithmetic on the SIMT decoder.  A tensor-core tile whose
+ * bounded wait gave up is written as NaN (no kernel traps).
  */
 jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blob,
                         size_t blob_stride, void* xhat, jolt_dtype out_dtype, void* stream);
