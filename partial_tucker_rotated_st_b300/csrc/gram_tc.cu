@@ -529,7 +529,9 @@ __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt
 // ---------------------------------------------------------------- sweep (TC)
 // The candidate sweep with the dense products on the tensor cores, for bf16
 // X with D = 128 and truncated ranks <= 32.  One CTA scores 128 tokens of one
-// head, one thread per token row:
+// head with two threads per token row, each owning one 64-column half (warps
+// w and w + 4 read the same TMEM lane quarter; the row maximum is exchanged
+// through shared memory between the pair):
 //   * QX = X (diag(sigma) H) by kind::f16 MMAs (bf16 X and the +-1 matrix are
 //     exact; fp32 accumulate) into TMEM columns [0, 128);
 //   * every reconstruction in the rotated domain, U_T W or Y16 (Q U_d)^T at a
@@ -537,13 +539,13 @@ __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt
 //     values, is exact in tf32; B split hi + lo) into TMEM columns [128, 256),
 //     recomputed from k = 0 for each checkpoint (columns r..8*ceil(r/8) of K
 //     zeroed meanwhile);
-//   * each thread then reads its row y = QX / sqrt(D) - P back in 32-column
-//     chunks and scores every b exactly as the SIMT sweep does (row max,
-//     fp16 scale, round-half-even by the magic constant, squared error).
+//   * each thread then reads its half row y = QX / sqrt(D) - P back in
+//     16-column chunks and scores every b exactly as the SIMT sweep does (row
+//     max, fp16 scale, round-half-even by the magic constant, squared error).
 // The K and B operands are written by the threads in the 128-byte swizzled
 // K-major layout (16-byte unit u of row r at u ^ (r % 8)), X and the sign
 // matrix arrive by TMA in the same layout.
-constexpr int STC_ROWS = 128, STC_THREADS = 128;
+constexpr int STC_ROWS = 128, STC_THREADS = 256;
 constexpr int STC_XBYTES = STC_ROWS * 256;       // 128 rows x 128 bf16
 constexpr int STC_KBYTES = STC_ROWS * 128;       // 128 rows x 32 fp32
 
@@ -572,6 +574,30 @@ __device__ __forceinline__ void tmem_ld16_issue(uint32_t addr, uint32_t (&r)[16]
         "=r"(r[14]), "=r"(r[15])
       : "r"(addr));
 }
+// 8 columns of this thread's TMEM lane into registers, without waiting.
+__device__ __forceinline__ void tmem_ld8_issue(uint32_t addr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(addr));
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[8], uint32_t (&q)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3]),
+                 "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_ld_issue(uint32_t addr, uint32_t (&r)[8]) { tmem_ld8_issue(addr, r); }
+__device__ __forceinline__ void tmem_ld_issue(uint32_t addr, uint32_t (&r)[16]) { tmem_ld16_issue(addr, r); }
 // Wait for this thread's TMEM loads, tied to the registers it makes valid
 // (so that no use of them can be scheduled before it).
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
@@ -594,20 +620,23 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16], uint32_t (&q)[16
                : "memory");
 }
 
-// One pass over this thread's row, 16 columns at a time, with the loads of
-// the next 16 columns in flight while the current ones are used:
+// One pass over this thread's 64-column half row (`trow` carries the half's
+// column offset), STC_CH columns at a time, with the loads of the next
+// STC_CH columns in flight while the current ones are used:
 // f(y0, y1) is called on consecutive pairs of y = QX rs - P (with_qx) or
 // y = P rs.
+constexpr int STC_CH = 16;
 template <typename F>
 __device__ __forceinline__ void stc_pass(uint32_t trow, bool with_qx, float rs, F&& f) {
   const float2 rs2 = make_float2(rs, rs);
-  uint32_t pa[16], qa[16], pb[16], qb[16];
-  tmem_ld16_issue(trow + 128, pa);
-  if (with_qx) tmem_ld16_issue(trow, qa);
+  uint32_t pa[STC_CH], qa[STC_CH], pb[STC_CH], qb[STC_CH];
+  auto issue = [&](uint32_t addr, uint32_t (&r)[STC_CH]) { tmem_ld_issue(addr, r); };
+  issue(trow + 128, pa);
+  if (with_qx) issue(trow, qa);
   if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);
-  auto use = [&](const uint32_t (&p)[16], const uint32_t (&q)[16]) {
+  auto use = [&](const uint32_t (&p)[STC_CH], const uint32_t (&q)[STC_CH]) {
 #pragma unroll
-    for (int j = 0; j < 16; j += 2) {
+    for (int j = 0; j < STC_CH; j += 2) {
       const float2 pp = make_float2(__uint_as_float(p[j]), __uint_as_float(p[j + 1]));
       const float2 y = with_qx
                            ? __ffma2_rn(make_float2(__uint_as_float(q[j]), __uint_as_float(q[j + 1])),
@@ -617,27 +646,33 @@ __device__ __forceinline__ void stc_pass(uint32_t trow, bool with_qx, float rs, 
     }
   };
 #pragma unroll
-  for (int c = 0; c < 128; c += 32) {
-    // columns c..c+15 are in (pa, qa); fetch c+16..c+31 into (pb, qb)
-    tmem_ld16_issue(trow + 128 + c + 16, pb);
-    if (with_qx) tmem_ld16_issue(trow + c + 16, qb);
+  for (int c = 0; c < 64; c += 2 * STC_CH) {
+    // columns c .. c + STC_CH - 1 are in (pa, qa); fetch the next STC_CH
+    // into (pb, qb)
+    issue(trow + 128 + c + STC_CH, pb);
+    if (with_qx) issue(trow + c + STC_CH, qb);
     use(pa, qa);
     if (with_qx) tmem_ld_wait(pb, qb); else tmem_ld_wait(pb);
-    if (c + 32 < 128) {
-      tmem_ld16_issue(trow + 128 + c + 32, pa);
-      if (with_qx) tmem_ld16_issue(trow + c + 32, qa);
+    if (c + 2 * STC_CH < 64) {
+      issue(trow + 128 + c + 2 * STC_CH, pa);
+      if (with_qx) issue(trow + c + 2 * STC_CH, qa);
     }
     use(pb, qb);
-    if (c + 32 < 128) {
+    if (c + 2 * STC_CH < 64) {
       if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);
     }
   }
 }
 
-// Score one candidate from TMEM: row `trow` (this thread's lane address);
-// y = QX rs - P (with_qx) or y = P rs (the whole-modes residual).
+// Score one candidate from TMEM: half row `trow` (this thread's lane
+// address and column offset); y = QX rs - P (with_qx) or y = P rs (the
+// whole-modes residual).  The two halves of a row meet on the row maximum
+// through rmax[half][lr] and a 64-thread named barrier of their warp pair;
+// the squared errors of the halves add in the cells.  The caller separates
+// consecutive calls by a CTA barrier (rmax is rewritten by the next call).
 __device__ __forceinline__ void stc_score(uint32_t trow, bool with_qx, float rs,
-                                          const SweepTcArgs& a, float* cells, int cell0) {
+                                          const SweepTcArgs& a, float* cells, int cell0,
+                                          float* rmax, int lr, int half, int pair) {
   float m0 = 0.f, m1 = 0.f;
   float2 e0 = make_float2(0.f, 0.f);
   stc_pass(trow, with_qx, rs, [&](float2 y) {
@@ -645,7 +680,10 @@ __device__ __forceinline__ void stc_score(uint32_t trow, bool with_qx, float rs,
     m1 = fmaxf(m1, fabsf(y.y));
     e0 = __ffma2_rn(y, y, e0);
   });
-  const float m = fmaxf(m0, m1);
+  float m = fmaxf(m0, m1);
+  rmax[half * STC_ROWS + lr] = m;
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+  m = fmaxf(m, rmax[(half ^ 1) * STC_ROWS + lr]);
   float s[4], inv[4];
 #pragma unroll
   for (int ib = 0; ib < 4; ++ib) {
@@ -692,9 +730,11 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
   float* cells = (float*)(base + 2 * STC_XBYTES); // [ncand + 1]
   struct Bars { uint64_t tma, mma; uint32_t tmem; int nz; };
   Bars* S = (Bars*)(cells + 260);
+  float* rmax = cells + 260 + 16;                 // [2][128] half-row maxima
   const int t = threadIdx.x, warp = t >> 5;
+  const int lr = t & (STC_ROWS - 1), half = t >> 7;  // token row, column half
   const int tt = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
-  const int t0 = tt * STC_ROWS, row = t0 + t;
+  const int t0 = tt * STC_ROWS, row = t0 + lr;
   const bool in = row < a.T;
   char* ub = a.ws + (size_t)u * a.ub;
   for (int i = t; i <= a.ncand; i += STC_THREADS) cells[i] = 0.f;
@@ -708,7 +748,7 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = S->tmem;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 64 * half;
   bool ok = true;
   uint32_t mma_phase = 0;
   auto mma_wait = [&]() {
@@ -752,8 +792,8 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
     float xn = 0.f;
     int nz = 0;
 #pragma unroll 4
-    for (int c = 0; c < 128; c += 8) {
-      unsigned char* p = sX + (c >> 6) * (STC_XBYTES / 2) + sw128(t, (c & 63) * 2);
+    for (int c = 0; c < 64; c += 8) {
+      unsigned char* p = sX + half * (STC_XBYTES / 2) + sw128(lr, c * 2);
       uint4 v = *reinterpret_cast<uint4*>(p);
       __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&v);
 #pragma unroll
@@ -775,7 +815,8 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
       __syncthreads();
       mma_x(128);
       mma_wait();
-      stc_score(trow, false, rs, a, cells, ((a.nT - 1) * a.nd + (a.nd - 1)) * a.nb);
+      stc_score(trow, false, rs, a, cells, ((a.nT - 1) * a.nd + (a.nd - 1)) * a.nb, rmax, lr,
+                half, warp & 3);
     }
   }
   // ---- rank chains: P = K[:, :r] B[:r, :] for each checkpoint r
@@ -786,57 +827,60 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
                        const int* ranks, int cellbase, int cellstride) {
     tc::tc_fence_before();
     __syncthreads();   // previous MMAs and TMEM reads done, operands free
-    // K rows (this thread's token row), fp16 -> fp32, zero past kn / T
+    // K rows (this thread's token row, columns 16 half .. 16 half + 15),
+    // fp16 -> fp32, zero past kn / T
+    const int k0 = 16 * half;
     if (kn == 32 && (k_ld & 7) == 0) {
-      uint4 raw[4];
+      uint4 raw[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        raw[i] = in ? reinterpret_cast<const uint4*>(Kg + (long long)row * k_ld)[i] : make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < 2; ++i)
+        raw[i] = in ? reinterpret_cast<const uint4*>(Kg + (long long)row * k_ld + k0)[i] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         const __half* hv = reinterpret_cast<const __half*>(&raw[i]);
         float4 v0, v1;
         v0.x = __half2float(hv[0]); v0.y = __half2float(hv[1]); v0.z = __half2float(hv[2]); v0.w = __half2float(hv[3]);
         v1.x = __half2float(hv[4]); v1.y = __half2float(hv[5]); v1.z = __half2float(hv[6]); v1.w = __half2float(hv[7]);
-        *reinterpret_cast<float4*>(sK + sw128(t, (8 * i) * 4)) = v0;
-        *reinterpret_cast<float4*>(sK + sw128(t, (8 * i + 4) * 4)) = v1;
+        *reinterpret_cast<float4*>(sK + sw128(lr, (k0 + 8 * i) * 4)) = v0;
+        *reinterpret_cast<float4*>(sK + sw128(lr, (k0 + 8 * i + 4) * 4)) = v1;
       }
     } else {
-      for (int k = 0; k < 32; k += 4) {
+      for (int k = k0; k < k0 + 16; k += 4) {
         float4 v;
         float* pv = reinterpret_cast<float*>(&v);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           pv[i] = (in && k + i < kn) ? __half2float(Kg[(long long)row * k_ld + k + i]) : 0.f;
-        *reinterpret_cast<float4*>(sK + sw128(t, k * 4)) = v;
+        *reinterpret_cast<float4*>(sK + sw128(lr, k * 4)) = v;
       }
     }
-    // B^T rows: n = t, B^T[n][k] = B[k][n], split hi + lo
-    for (int k = 0; k < 32; k += 4) {
+    // B^T rows: n = lr, B^T[n][k] = B[k][n] for this half's k, split hi + lo
+    for (int k = k0; k < k0 + 16; k += 4) {
       float4 hi, lo;
       float* ph = reinterpret_cast<float*>(&hi);
       float* pl = reinterpret_cast<float*>(&lo);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float b = (k + i < kn) ? Bg[(long long)(k + i) * 128 + t] : 0.f;
+        const float b = (k + i < kn) ? Bg[(long long)(k + i) * 128 + lr] : 0.f;
         const float bh = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
         ph[i] = bh;
         pl[i] = b - bh;
       }
-      *reinterpret_cast<float4*>(sBh + sw128(t, k * 4)) = hi;
-      *reinterpret_cast<float4*>(sBl + sw128(t, k * 4)) = lo;
+      *reinterpret_cast<float4*>(sBh + sw128(lr, k * 4)) = hi;
+      *reinterpret_cast<float4*>(sBl + sw128(lr, k * 4)) = lo;
     }
     for (int ci = 0; ci < nck; ++ci) {
       const int r = ranks[ci];
       const int ks = (r + 7) >> 3;
-      // zero K columns r .. 8 ks - 1 of this row for this checkpoint
+      // zero K columns r .. 8 ks - 1 of this row for this checkpoint (each
+      // half its own columns)
       float saved[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = r + i;
         saved[i] = 0.f;
-        if (k < 8 * ks) {
-          float* p = reinterpret_cast<float*>(sK + sw128(t, k * 4));
+        if (k < 8 * ks && (k >> 4) == half) {
+          float* p = reinterpret_cast<float*>(sK + sw128(lr, k * 4));
           saved[i] = *p;
           *p = 0.f;
         }
@@ -856,12 +900,12 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
         tc::mma_commit(tc::smem_u32(&S->mma));
       }
       mma_wait();
-      stc_score(trow, true, rs, a, cells, cellbase + ci * cellstride);
+      stc_score(trow, true, rs, a, cells, cellbase + ci * cellstride, rmax, lr, half, warp & 3);
       // restore the zeroed columns for the next checkpoint
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int k = r + i;
-        if (k < 8 * ks) *reinterpret_cast<float*>(sK + sw128(t, k * 4)) = saved[i];
+        if (k < 8 * ks && (k >> 4) == half) *reinterpret_cast<float*>(sK + sw128(lr, k * 4)) = saved[i];
       }
       tc::tc_fence_before();
       __syncthreads();
@@ -1121,7 +1165,9 @@ jolt_status sweep_tc_run(const Layout& L, int U, const void* X, char* ws, float*
   a.ws = ws; a.ub = L.unit_bytes;
   a.o_UT16 = L.o_UT16; a.o_W = L.o_W; a.o_Y16 = L.o_Y16; a.o_QUd = L.o_QUd; a.o_status = L.o_status;
   a.part = part; a.part_us = part_us;
-  const size_t smem = 2 * STC_XBYTES + 260 * 4 + 64 + 1024;
+  // cells (260 floats), barriers (64 bytes), row maxima (256 floats), and
+  // the 1024-byte alignment slack; 2 CTAs per SM by TMEM (256 columns each)
+  const size_t smem = 2 * STC_XBYTES + 260 * 4 + 64 + 2 * STC_ROWS * 4 + 1024;
   static bool attr = false;
   if (!attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
