@@ -50,22 +50,35 @@ __device__ __forceinline__ bool less_key(const Key& a, const Key& b) {
   return a.i < b.i;
 }
 
+// The tables as the best responses read them: dist, cost, and the cost
+// converted to double once (exact for |cost| < 2^53; null when the tables
+// stay in global memory, then converted on the fly).
+struct Tabs {
+  const double* dist;
+  const int64_t* cost;
+  const double* costd;
+};
+
 // mode 0: z(lambda), key (dist + lambda*cost, cost, index)
 // mode 1: cheapest allocation, key (cost, dist, index)
-// Writes out[u] and, through *tot, the total cost (all threads see it).
-__device__ void best_response(int U, int nc, const double* dist, const int64_t* cost, double lam,
-                              int mode, int* out, long long* tot) {
+// Writes out[u] and returns the total cost (the same in every thread).  One
+// barrier per call: the warps' totals go to one of two buffers in turn
+// (`parity`), and every warp sums them itself.
+__device__ long long best_response(int U, int nc, const Tabs& tb, double lam, int mode, int* out,
+                                   int& parity) {
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32, nw = blockDim.x / 32;
-  __shared__ long long part[AL_THREADS / 32];
+  __shared__ long long part[2][AL_THREADS / 32];
   long long mine = 0;
   for (int u = w; u < U; u += nw) {
     Key b{~0ull, ~0ull, INT_MAX};
     for (int c = lane; c < nc; c += 32) {
-      const double d = dist[(long long)u * nc + c];
-      const long long k = cost[(long long)u * nc + c];
+      const long long i = (long long)u * nc + c;
+      const double d = tb.dist[i];
+      const long long k = tb.cost[i];
       Key x;
       if (mode == 0) {
-        x.k1 = dkey(__dadd_rn(d, __dmul_rn(lam, (double)k)));
+        const double kd = tb.costd ? tb.costd[i] : (double)k;
+        x.k1 = dkey(__dadd_rn(d, __dmul_rn(lam, kd)));
         x.k2 = ikey(k);
       } else {
         x.k1 = ikey(k);
@@ -84,17 +97,16 @@ __device__ void best_response(int U, int nc, const double* dist, const int64_t* 
     }
     if (lane == 0) {
       out[u] = b.i;
-      mine += cost[(long long)u * nc + b.i];
+      mine += tb.cost[(long long)u * nc + b.i];
     }
   }
-  if (lane == 0) part[w] = mine;
+  if (lane == 0) part[parity][w] = mine;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    long long s = 0;
-    for (int i = 0; i < nw; ++i) s += part[i];
-    *tot = s;
-  }
-  __syncthreads();
+  long long s = lane < nw ? part[parity][lane] : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  parity ^= 1;
+  return s;
 }
 
 __global__ void __launch_bounds__(AL_THREADS)
@@ -102,57 +114,59 @@ alloc_kernel(int U, int nc, const double* __restrict__ gdist, const int64_t* __r
              long long budget, int align, int32_t* choice, double* lambda, int32_t* status,
              int cached) {
   extern __shared__ __align__(16) unsigned char asm_raw[];
-  __shared__ long long tot;
   // tables copied into shared memory once when they fit (the bisection
   // evaluates best responses up to a few hundred times)
-  const double* dist = gdist;
-  const int64_t* cost = gcost;
+  Tabs tb{gdist, gcost, nullptr};
   int* zs;
   if (cached) {
     double* sd = (double*)asm_raw;
-    int64_t* sc = (int64_t*)(sd + (size_t)U * nc);
-    for (int i = threadIdx.x; i < U * nc; i += blockDim.x) { sd[i] = gdist[i]; sc[i] = gcost[i]; }
-    dist = sd;
-    cost = sc;
+    double* scd = sd + (size_t)U * nc;
+    int64_t* sc = (int64_t*)(scd + (size_t)U * nc);
+    for (int i = threadIdx.x; i < U * nc; i += blockDim.x) {
+      sd[i] = gdist[i];
+      sc[i] = gcost[i];
+      scd[i] = (double)gcost[i];
+    }
+    tb = Tabs{sd, sc, scd};
     zs = (int*)(sc + (size_t)U * nc);
   } else {
     zs = (int*)asm_raw;
   }
   __syncthreads();
-  int* zhi = zs;            // [U]
-  int* zmid = zs + U;       // [U]
-  best_response(U, nc, dist, cost, 0.0, 0, zhi, &tot);
+  int* zhi = zs;            // [U], the last feasible best response
+  int* zmid = zs + U;       // [U], the one being evaluated (the two swap roles)
+  int parity = 0;
+  long long tot = best_response(U, nc, tb, 0.0, 0, zhi, parity);
   if (tot <= budget) {
     for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = zhi[u];
     if (threadIdx.x == 0) { *lambda = 0.0; *status = JOLT_OK; }
     return;
   }
-  best_response(U, nc, dist, cost, 0.0, 1, zhi, &tot);
+  tot = best_response(U, nc, tb, 0.0, 1, zhi, parity);
   if (tot > budget) {
     for (int u = threadIdx.x; u < U; u += blockDim.x) choice[u] = zhi[u];
     if (threadIdx.x == 0) { *lambda = INFINITY; *status = JOLT_ERR_INFEASIBLE; }
     return;
   }
   double lo = 0.0, hi = 1.0;
-  best_response(U, nc, dist, cost, hi, 0, zhi, &tot);
-  long long chi = tot;
+  long long chi = best_response(U, nc, tb, hi, 0, zhi, parity);
   // z(lambda) reaches the cheapest allocation, which fits, as lambda grows;
   // the cap only guards non-finite tables
   while (chi > budget && hi < 1e300) {
     lo = hi;
     hi = hi * 2.0;
-    best_response(U, nc, dist, cost, hi, 0, zhi, &tot);
-    chi = tot;
+    chi = best_response(U, nc, tb, hi, 0, zhi, parity);
   }
   for (int it = 0; it < AL_MAX_ITER; ++it) {
     if ((budget - align < chi && chi <= budget) || hi - lo <= 0x1.0p-52 * hi) break;
     const double mid = 0.5 * (lo + hi);
-    best_response(U, nc, dist, cost, mid, 0, zmid, &tot);
+    tot = best_response(U, nc, tb, mid, 0, zmid, parity);
     if (tot <= budget) {
       hi = mid;
       chi = tot;
-      for (int u = threadIdx.x; u < U; u += blockDim.x) zhi[u] = zmid[u];
-      __syncthreads();
+      int* z = zhi;
+      zhi = zmid;
+      zmid = z;
     } else {
       lo = mid;
     }
@@ -297,7 +311,7 @@ jolt_status alloc_run(int U, int nc, const double* dist, const int64_t* cost, in
                       int align, int32_t* choice, double* lambda, int32_t* status,
                       cudaStream_t st) {
   const size_t ztab = (size_t)2 * U * sizeof(int);
-  const size_t tabs = (size_t)U * nc * (sizeof(double) + sizeof(int64_t));
+  const size_t tabs = (size_t)U * nc * (2 * sizeof(double) + sizeof(int64_t));
   const int cached = (tabs + ztab <= 150 * 1024) ? 1 : 0;
   const size_t smem = cached ? tabs + ztab : ztab;
   if (smem > 160 * 1024) return JOLT_ERR_INVALID;

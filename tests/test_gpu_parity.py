@@ -107,6 +107,36 @@ def test_allocation_total_distortion_vs_oracle(name):
     assert abs(d_gpu - d_ora) <= 1e-3 * abs(d_ora) + 1e-9
 
 
+@pytest.mark.parametrize("U,nc", [(16, 100), (3, 7), (40, 33), (300, 100)])
+def test_allocate_synthetic_tables_bit_exact(U, nc):
+    """The bisection allocator on seeded synthetic tables against the oracle's
+    on the same tables: choice, lambda and status bit for bit, for a budget
+    that z(0) meets, binding budgets, and one below the cheapest allocation.
+    Dyadic distortions on a coarse grid make equal keys frequent (the tie
+    rules decide); the (300, 100) tables do not fit in shared memory and are
+    read from global memory."""
+    import torch
+    from partial_tucker_rotated_st_b300 import jolt as J
+    rng = np.random.default_rng(7000 + U * 131 + nc)
+    cost = rng.integers(1, 1 << 18, size=(U, nc)).astype(np.int64) * 256
+    dist = rng.integers(0, 64, size=(U, nc)).astype(np.float64) / 64.0
+    cmin = int(cost.min(axis=1).sum())
+    z0, _, _ = oj.allocate(dist, cost, 1 << 62, 256)
+    c0 = int(oj.total_cost(cost, z0))
+    budgets = [c0 + 4096, cmin + (c0 - cmin) // 3, cmin + (c0 - cmin) // 50, cmin, cmin - 1]
+    dd, cc = torch.from_numpy(dist).cuda(), torch.from_numpy(cost).cuda()
+    ch = torch.zeros(U, dtype=torch.int32, device="cuda")
+    lam = torch.zeros(1, dtype=torch.float64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for budget in budgets:
+        J.jolt_allocate(U, nc, dd, cc, budget, 256, ch, lam, st)
+        torch.cuda.synchronize()
+        zref, lref, sref = oj.allocate(dist, cost, budget, 256)
+        assert list(ch.cpu().numpy()) == list(zref), budget
+        assert float(lam.item()) == lref, (budget, float(lam.item()), lref)
+        assert int(st.item()) == (J.OK if sref == oj.ALLOC_OK else J.ERR_INFEASIBLE)
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
 def test_blob_header_and_scored_distortion(name):
     """The GPU's blob has the layout of its candidate, and the distortion of
