@@ -107,19 +107,26 @@ def test_allocation_total_distortion_vs_oracle(name):
     assert abs(d_gpu - d_ora) <= 1e-3 * abs(d_ora) + 1e-9
 
 
-@pytest.mark.parametrize("U,nc", [(16, 100), (3, 7), (40, 33), (300, 100)])
-def test_allocate_synthetic_tables_bit_exact(U, nc):
+@pytest.mark.parametrize("U,nc,coarse", [(16, 100, False), (16, 100, True), (3, 7, False),
+                                         (40, 33, True), (300, 100, False)])
+def test_allocate_synthetic_tables_bit_exact(U, nc, coarse):
     """The bisection allocator on seeded synthetic tables against the oracle's
     on the same tables: choice, lambda and status bit for bit, for a budget
     that z(0) meets, binding budgets, and one below the cheapest allocation.
     Dyadic distortions on a coarse grid make equal keys frequent (the tie
-    rules decide); the (300, 100) tables do not fit in shared memory and are
+    rules decide); the coarse tables also repeat costs and whole (cost,
+    distortion) pairs, so that candidates dominated only through the index
+    tie-break occur; the (300, 100) tables do not fit in shared memory and are
     read from global memory."""
     import torch
     from partial_tucker_rotated_st_b300 import jolt as J
-    rng = np.random.default_rng(7000 + U * 131 + nc)
-    cost = rng.integers(1, 1 << 18, size=(U, nc)).astype(np.int64) * 256
-    dist = rng.integers(0, 64, size=(U, nc)).astype(np.float64) / 64.0
+    rng = np.random.default_rng(7000 + U * 131 + nc + 17 * coarse)
+    if coarse:
+        cost = rng.integers(1, 12, size=(U, nc)).astype(np.int64) * 4096
+        dist = rng.integers(0, 8, size=(U, nc)).astype(np.float64) / 8.0
+    else:
+        cost = rng.integers(1, 1 << 18, size=(U, nc)).astype(np.int64) * 256
+        dist = rng.integers(0, 64, size=(U, nc)).astype(np.float64) / 64.0
     cmin = int(cost.min(axis=1).sum())
     z0, _, _ = oj.allocate(dist, cost, 1 << 62, 256)
     c0 = int(oj.total_cost(cost, z0))
