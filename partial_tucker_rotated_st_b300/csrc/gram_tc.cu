@@ -574,30 +574,6 @@ __device__ __forceinline__ void tmem_ld16_issue(uint32_t addr, uint32_t (&r)[16]
         "=r"(r[14]), "=r"(r[15])
       : "r"(addr));
 }
-// 8 columns of this thread's TMEM lane into registers, without waiting.
-__device__ __forceinline__ void tmem_ld8_issue(uint32_t addr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(addr));
-}
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[8]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7])
-               :
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[8], uint32_t (&q)[8]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(q[0]), "+r"(q[1]), "+r"(q[2]), "+r"(q[3]),
-                 "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7])
-               :
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld_issue(uint32_t addr, uint32_t (&r)[8]) { tmem_ld8_issue(addr, r); }
-__device__ __forceinline__ void tmem_ld_issue(uint32_t addr, uint32_t (&r)[16]) { tmem_ld16_issue(addr, r); }
 // Wait for this thread's TMEM loads, tied to the registers it makes valid
 // (so that no use of them can be scheduled before it).
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
@@ -630,7 +606,7 @@ template <typename F>
 __device__ __forceinline__ void stc_pass(uint32_t trow, bool with_qx, float rs, F&& f) {
   const float2 rs2 = make_float2(rs, rs);
   uint32_t pa[STC_CH], qa[STC_CH], pb[STC_CH], qb[STC_CH];
-  auto issue = [&](uint32_t addr, uint32_t (&r)[STC_CH]) { tmem_ld_issue(addr, r); };
+  auto issue = [&](uint32_t addr, uint32_t (&r)[STC_CH]) { tmem_ld16_issue(addr, r); };
   issue(trow + 128, pa);
   if (with_qx) issue(trow, qa);
   if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);

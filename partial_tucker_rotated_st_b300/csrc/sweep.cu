@@ -344,11 +344,16 @@ __global__ void sign_hadamard_kernel(char* ws, size_t ub, const int8_t* signs, s
 
 // W[id][h][k][:] = sum_j G16[id][h][k][j] QUd[j][:]  (r_d < D), or
 //                = Q G16[id][h][k][:]                  (r_d = D).
+// One launch for every feature rank: block (id, h, u).
+struct RdList {
+  int rd[JOLT_MAX_GRID];
+};
 template <int EPT>
 __global__ void build_w_kernel(char* ws, size_t ub, const int8_t* signs, size_t o_G16,
-                               size_t o_QUd, size_t o_W, int H, int RT, int id, int rdv) {
+                               size_t o_QUd, size_t o_W, int H, int RT, RdList rl) {
   constexpr int D = 32 * EPT;
-  const int u = blockIdx.z, h = blockIdx.y;
+  const int id = blockIdx.x, u = blockIdx.z, h = blockIdx.y;
+  const int rdv = rl.rd[id];
   const int lane = threadIdx.x % 32, w = threadIdx.x / 32, nw = blockDim.x / 32;
   char* base = ws + u * ub;
   const __half* G = (const __half*)(base + o_G16) + ((long long)id * H * RT * D) +
@@ -382,22 +387,36 @@ __global__ void build_w_kernel(char* ws, size_t ub, const int8_t* signs, size_t 
 }
 
 // dist[u][c] = sum_tiles e / sum_tiles ||x||^2 (f64), 0 for an all-zero unit.
-__global__ void sweep_reduce_kernel(char* ws, size_t ub, const float* part_base, long long part_us,
-                                    size_t o_status, int ntiles, int ncand, double* dist) {
+// Block (u, group of 32 candidates), 256 threads: warp w sums tiles w, w + 8,
+// ... of its lane's candidate, the eight partial sums are then added in warp
+// order; every block reduces the ||x||^2 column (slot ncand) in the same
+// fixed order.
+constexpr int SR_THREADS = 256, SR_WARPS = SR_THREADS / 32;
+__global__ void __launch_bounds__(SR_THREADS)
+sweep_reduce_kernel(char* ws, size_t ub, const float* part_base, long long part_us,
+                    size_t o_status, int ntiles, int ncand, double* dist) {
   const int u = blockIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.y * 32 + lane;
   const float* part = part_base + u * part_us;
-  __shared__ double xn;
-  if (threadIdx.x < 32) {
-    double s = 0.0;
-    for (int i = threadIdx.x; i < ntiles; i += 32) s += (double)part[(long long)i * (ncand + 1) + ncand];
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (threadIdx.x == 0) xn = s;
-  }
+  const long long ld = ncand + 1;
+  __shared__ double px[SR_WARPS], pc[SR_WARPS][32];
+  double sx = 0.0;
+  for (int i = threadIdx.x; i < ntiles; i += SR_THREADS) sx += (double)part[(long long)i * ld + ncand];
+  for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+  if (lane == 0) px[w] = sx;
+  double s = 0.0;
+  if (c < ncand)
+    for (int i = w; i < ntiles; i += SR_WARPS) s += (double)part[(long long)i * ld + c];
+  pc[w][lane] = s;
   __syncthreads();
-  for (int c = threadIdx.x; c < ncand; c += blockDim.x) {
-    double s = 0.0;
-    for (int i = 0; i < ntiles; ++i) s += (double)part[(long long)i * (ncand + 1) + c];
-    double d = (xn > 0.0) ? s / xn : 0.0;
+  if (w == 0 && c < ncand) {
+    double xn = 0.0, e = 0.0;
+    for (int k = 0; k < SR_WARPS; ++k) {
+      xn += px[k];
+      e += pc[k][lane];
+    }
+    const double d = (xn > 0.0) ? e / xn : 0.0;
     if (!isfinite(d) || !isfinite(xn)) atomicOr((int*)(ws + u * ub + o_status), ST_NONFINITE);
     dist[(long long)u * ncand + c] = d;
   }
@@ -480,13 +499,13 @@ jolt_status sweep_prep(const Layout& L, int U, const int8_t* signs, char* ws, cu
     JOLT_LAUNCH_CHECK();
   }
   if (L.RT > 0) {
-    for (int id = 0; id < L.nd; ++id) {
-      dim3 g(1, L.H, U);
-      if (EPT == 4) build_w_kernel<4><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, id, L.rd[id]);
-      else if (EPT == 2) build_w_kernel<2><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, id, L.rd[id]);
-      else build_w_kernel<1><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, id, L.rd[id]);
-      JOLT_LAUNCH_CHECK();
-    }
+    RdList rl;
+    for (int id = 0; id < JOLT_MAX_GRID; ++id) rl.rd[id] = id < L.nd ? L.rd[id] : 0;
+    dim3 g(L.nd, L.H, U);
+    if (EPT == 4) build_w_kernel<4><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl);
+    else if (EPT == 2) build_w_kernel<2><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl);
+    else build_w_kernel<1><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl);
+    JOLT_LAUNCH_CHECK();
   }
   return JOLT_OK;
 }
@@ -537,8 +556,8 @@ jolt_status sweep_run(const Layout& L, int U, const void* X, const int8_t* signs
   }
   if (g_sweep_ev[1]) JOLT_CUDA_TRY(cudaEventRecord((cudaEvent_t)g_sweep_ev[1], st));
   if (s != JOLT_OK) return s;
-  sweep_reduce_kernel<<<U, 128, 0, st>>>(ws, ub, a.part, a.part_us, L.o_status, ntiles, L.ncand,
-                                        dist);
+  sweep_reduce_kernel<<<dim3(U, (L.ncand + 31) / 32), SR_THREADS, 0, st>>>(
+      ws, ub, a.part, a.part_us, L.o_status, ntiles, L.ncand, dist);
   JOLT_LAUNCH_CHECK();
   CostArgs ca;
   ca.H = L.H; ca.T = L.T; ca.D = D; ca.nT = L.nT; ca.nd = L.nd; ca.nb = L.nb;
