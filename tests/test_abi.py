@@ -225,3 +225,100 @@ def test_admit_rejects_bad_arguments_before_launch(case):
     st = J.lib().jolt_admit(2, arr, blob_in, sin, X, dt, tau, align, ws, ws_bytes, blob_out, sout,
                             out, None)
     assert st == want
+
+
+MAX_CAND = 8 * 8 * 4   # JOLT_MAX_CAND of include/jolt.h
+
+
+def _bad_call(case):
+    """One call that the library must reject before any CUDA call, and the
+    status it must return.  Device pointers are fake and never dereferenced."""
+    cfg = _cfg()
+    L = J.lib()
+    dev = 1 << 40
+    wsz = J.jolt_workspace_size(cfg)
+    ncand = J.jolt_num_candidates(cfg)
+    i32 = lambda *v: (ctypes.c_int32 * max(len(v), 1))(*v)
+    f64 = lambda *v: (ctypes.c_double * len(v))(*v)
+    sweep_args = dict(n=1, X=dev, signs=dev, ws=dev, wsb=wsz, dist=dev, cost=dev)
+
+    def sweep(fn, **kw):
+        a = dict(sweep_args, **kw)
+        return fn(ctypes.byref(cfg), a["n"], a["X"], a["signs"], a["ws"], a["wsb"], a["dist"],
+                  a["cost"], None)
+
+    def encode(n=1, choice=(0,), blob=dev, stride=1 << 26, ws=dev, wsb=wsz):
+        desc = (J.JoltBlobDesc * max(n, 1))()
+        return L.jolt_encode(ctypes.byref(cfg), n, dev, dev, ws, wsb,
+                             i32(*choice) if choice is not None else None, blob, stride, desc,
+                             None)
+
+    cases = {
+        "sweep_units0": (lambda: sweep(L.jolt_sweep_candidates, n=0), J.ERR_INVALID),
+        "sweep_signs": (lambda: sweep(L.jolt_sweep_candidates, signs=None), J.ERR_INVALID),
+        "sweep_dist": (lambda: sweep(L.jolt_sweep_candidates, dist=None), J.ERR_INVALID),
+        "sweep_ws_small": (lambda: sweep(L.jolt_sweep_candidates, wsb=wsz - 256), J.ERR_WORKSPACE),
+        "sweep_ws_align": (lambda: sweep(L.jolt_sweep_candidates, ws=dev + 8), J.ERR_WORKSPACE),
+        "noalloc_cost": (lambda: sweep(L.jolt_sweep_candidates_noalloc, cost=None), J.ERR_INVALID),
+        "noalloc_ws_small": (lambda: sweep(L.jolt_sweep_candidates_noalloc, wsb=wsz - 256),
+                             J.ERR_WORKSPACE),
+        "noalloc_too_large": (lambda: sweep(L.jolt_sweep_candidates_noalloc, n=65535,
+                                            wsb=65535 * wsz), J.ERR_TOO_LARGE),
+        "encode_units0": (lambda: encode(n=0), J.ERR_INVALID),
+        "encode_choice_null": (lambda: encode(choice=None), J.ERR_INVALID),
+        "encode_blob_align": (lambda: encode(blob=dev + 16), J.ERR_INVALID),
+        "encode_stride_align": (lambda: encode(stride=(1 << 26) + 16), J.ERR_INVALID),
+        "encode_stride_small": (lambda: encode(stride=256), J.ERR_INVALID),
+        "encode_choice_range": (lambda: encode(choice=(ncand,)), J.ERR_INVALID),
+        "encode_choice_negative": (lambda: encode(choice=(-1,)), J.ERR_INVALID),
+        "encode_ws_small": (lambda: encode(wsb=wsz - 256), J.ERR_WORKSPACE),
+        "refine_ncand": (lambda: L.jolt_refine(4, MAX_CAND + 1, dev, dev, 1 << 20, dev, dev, None),
+                         J.ERR_INVALID),
+        "refine_dist": (lambda: L.jolt_refine(4, 10, None, dev, 1 << 20, dev, dev, None),
+                        J.ERR_INVALID),
+        "uniform_cand_range": (lambda: L.jolt_allocate_uniform(4, 10, dev, dev, 1 << 20, i32(3, 10),
+                                                               2, dev, dev, None), J.ERR_INVALID),
+        "uniform_empty_list": (lambda: L.jolt_allocate_uniform(4, 10, dev, dev, 1 << 20, i32(3), 0,
+                                                               dev, dev, None), J.ERR_INVALID),
+        "allocate_align": (lambda: L.jolt_allocate(4, 10, dev, dev, 1 << 20, 0, dev, dev, dev, None),
+                           J.ERR_INVALID),
+        "model_eps2_negative": (lambda: L.jolt_model_candidates(ctypes.byref(cfg), 1, dev, wsz,
+                                                                f64(1.0, -0.5, 0.01, 1e-4), dev,
+                                                                None), J.ERR_INVALID),
+        "model_eps2_nan": (lambda: L.jolt_model_candidates(ctypes.byref(cfg), 1, dev, wsz,
+                                                           f64(1.0, 0.5, float("nan"), 1e-4), dev,
+                                                           None), J.ERR_INVALID),
+        "model_ws_small": (lambda: L.jolt_model_candidates(ctypes.byref(cfg), 1, dev, wsz - 256,
+                                                           f64(1.0, 0.5, 0.01, 1e-4), dev, None),
+                           J.ERR_WORKSPACE),
+        "eps2_D": (lambda: L.jolt_calibrate_eps2(dev, 64, 96, i32(2, 4), 2, dev, dev, None),
+                   J.ERR_INVALID),
+        "eps2_bits": (lambda: L.jolt_calibrate_eps2(dev, 64, 128, i32(2, 3), 2, dev, dev, None),
+                      J.ERR_INVALID),
+        "eps2_nb": (lambda: L.jolt_calibrate_eps2(dev, 64, 128, i32(0, 2, 4, 8, 8), 5, dev, dev,
+                                                  None), J.ERR_INVALID),
+        "events_half": (lambda: L.jolt_set_sweep_events(dev, None), J.ERR_INVALID),
+        "status_units0": (lambda: L.jolt_read_status(ctypes.byref(cfg), 0, dev, None),
+                          J.ERR_INVALID),
+        "status_ws_null": (lambda: L.jolt_read_status(ctypes.byref(cfg), 1, None, None),
+                           J.ERR_INVALID),
+    }
+    return cases[case]
+
+
+_BAD_CASES = ["sweep_units0", "sweep_signs", "sweep_dist", "sweep_ws_small", "sweep_ws_align",
+              "noalloc_cost", "noalloc_ws_small", "noalloc_too_large", "encode_units0",
+              "encode_choice_null", "encode_blob_align", "encode_stride_align",
+              "encode_stride_small", "encode_choice_range", "encode_choice_negative",
+              "encode_ws_small", "refine_ncand", "refine_dist", "uniform_cand_range",
+              "uniform_empty_list", "allocate_align", "model_eps2_negative", "model_eps2_nan",
+              "model_ws_small", "eps2_D", "eps2_bits", "eps2_nb", "events_half",
+              "status_units0", "status_ws_null"]
+
+
+@pytest.mark.parametrize("case", _BAD_CASES)
+def test_entry_points_reject_bad_arguments_before_launch(case):
+    call, want = _bad_call(case)
+    n0 = J.jolt_launch_count()
+    assert call() == want
+    assert J.jolt_launch_count() == n0
