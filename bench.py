@@ -549,56 +549,41 @@ DECODE_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_t
                           "csrc", "decode_tc.cu")
 
 
-def decode_traffic(workload):
-    """DRAM bytes of one decoder launch from the committed ncu summary, while
-    decode_tc.cu is the source it was taken on."""
+def traffic_record(profile, src_path, hash_key, bytes_key, workload):
+    """The DRAM bytes recorded on the `traffic_record:` line of a committed ncu
+    summary, only while the kernel source still hashes to the sha256 prefix
+    recorded beside them and the workload matches; else None (the counters
+    belong to another kernel or workload)."""
     try:
-        txt = open(DECODE_PROFILE).read()
-        src = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+        txt = open(profile).read()
+        src = hashlib.sha256(open(src_path, "rb").read()).hexdigest()[:16]
     except OSError:
         return None
     rec = {}
     for line in txt.splitlines():
         if line.startswith("traffic_record:"):
             rec = json.loads(line.split(":", 1)[1])
-    if rec.get("decode_src_sha256") != src or rec.get("workload") != workload:
+    if rec.get(hash_key) != src or rec.get("workload") != workload:
         return None
-    return int(rec["dram_bytes_per_launch"])
+    return int(rec[bytes_key])
+
+
+def decode_traffic(workload):
+    """DRAM bytes of one decoder launch."""
+    return traffic_record(DECODE_PROFILE, DECODE_SRC, "decode_src_sha256",
+                          "dram_bytes_per_launch", workload)
 
 
 def attend_traffic(workload):
-    """DRAM bytes of one jolt_attend call (its three kernels) from the
-    committed ncu summary, while attend.cu is the source it was taken on."""
-    try:
-        txt = open(ATTEND_PROFILE).read()
-        src = hashlib.sha256(open(ATTEND_SRC, "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
-    rec = {}
-    for line in txt.splitlines():
-        if line.startswith("traffic_record:"):
-            rec = json.loads(line.split(":", 1)[1])
-    if rec.get("attend_src_sha256") != src or rec.get("workload") != workload:
-        return None
-    return int(rec["dram_bytes_per_call"])
+    """DRAM bytes of one jolt_attend call (its three kernels)."""
+    return traffic_record(ATTEND_PROFILE, ATTEND_SRC, "attend_src_sha256",
+                          "dram_bytes_per_call", workload)
 
 
 def sweep_traffic(workload):
-    """DRAM bytes of one sweep-kernel launch from the committed ncu summary,
-    only while the kernel source is the one that summary was taken on (its
-    sha256 prefix is recorded there); else None."""
-    try:
-        txt = open(SWEEP_PROFILE).read()
-        src = hashlib.sha256(open(SWEEP_SRC, "rb").read()).hexdigest()[:16]
-    except OSError:
-        return None
-    rec = {}
-    for line in txt.splitlines():
-        if line.startswith("traffic_record:"):
-            rec = json.loads(line.split(":", 1)[1])
-    if rec.get("sweep_src_sha256") != src or rec.get("workload") != workload:
-        return None
-    return int(rec["dram_bytes_per_launch"])
+    """DRAM bytes of one sweep-kernel launch."""
+    return traffic_record(SWEEP_PROFILE, SWEEP_SRC, "sweep_src_sha256",
+                          "dram_bytes_per_launch", workload)
 
 
 def roofline(w, kernel_s, hbm, kind, pk):
