@@ -2,7 +2,7 @@
 """Benchmark of the JoLT KV-cache encode/decode path on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME]
+                    [--workload NAME] [--configs A,B,...|none]
 
 One step = the whole hot path over one batch of synthetic units: factor
 (ST-HOSVD) -> sweep of the full (r_T, r_d, b) grid -> Lagrangian allocation ->
@@ -14,8 +14,15 @@ outside the timed events.  `e2e` repeats the encode through the same public
 calls from pinned host memory: host-to-device copy of X and signs, encode,
 device-to-host copy of the blobs, all inside the timed region.
 
+The line's workload is the largest single-GPU configuration, the LLaMA-2-13B
+shaped cache (20 units of [160, 1024, 128] bf16).  `configs` adds one record
+per other large configuration (Mistral-7B shaped at 1024 and 2048 tokens, and
+the 4096-token FlashJoLT case with its decode of all 16 units back to bf16),
+each timed the same way.
+
 --impl reference times the float64 CPU oracle (oracle/) on a bounded sample
-of the same workload (a token window of one unit) on the host cores.
+of the same workload: one token window of each of P units, P = min(units,
+host cores), one single-threaded process per unit.
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload (no data-path collective); the timed region is bracketed by
@@ -26,6 +33,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import multiprocessing as mp
 import os
 import statistics
 import subprocess
@@ -42,6 +50,9 @@ import kvgen  # noqa: E402
 
 METRIC = "KV encode GB/s (full (r_T,r_d,b) sweep+alloc) and decode GB/s, 1×B300"
 L2_BYTES = 126 * 2 ** 20
+MAIN_WORKLOAD = "llama_t1024"
+EXTRA_CONFIGS = ("mistral_t1024", "mistral_t2048", "flash_t4096")
+THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
 
 
 def peaks():
@@ -51,6 +62,17 @@ def peaks():
             d = json.load(f)
         return d.get("hbm_gbs", 6400.0), "measured", d
     return 6400.0, "fallback", {}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # ----------------------------------------------------------------- clocks
@@ -157,223 +179,401 @@ def max_over_ranks(ws, v: float, device=None) -> float:
     return float(t.item())
 
 
+# ----------------------------------------------------------------- process pools
+class single_threaded_children:
+    """Environment for spawned children: one BLAS/OpenMP thread each (the
+    variables are read when a child imports numpy)."""
+
+    def __enter__(self):
+        self.saved = {k: os.environ.get(k) for k in THREAD_VARS}
+        for k in THREAD_VARS:
+            os.environ[k] = "1"
+        return self
+
+    def __exit__(self, *a):
+        for k, v in self.saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def _gen_unit(task):
+    name, u = task
+    w = kvgen.WORKLOADS[name]
+    x = kvgen.make_unit(w, u)
+    s = kvgen.make_signs(w, u)
+    sk = kvgen.make_sketch(w, u) if w.token_mode == "randomized" else None
+    return name, u, x, s, sk
+
+
+def gen_inputs(names, procs=None):
+    """Host inputs of every unit of each named workload, generated by a pool
+    of spawned processes (before any CUDA call of this process):
+    {name: (list of stored unit arrays, signs [U][D], sketch [U][H][D][ell] or None)}."""
+    tasks = [(n, u) for n in names for u in range(kvgen.WORKLOADS[n].n_units)]
+    procs = max(1, min(procs or (os.cpu_count() or 1), len(tasks)))
+    out = {n: ([None] * kvgen.WORKLOADS[n].n_units, [None] * kvgen.WORKLOADS[n].n_units,
+               [None] * kvgen.WORKLOADS[n].n_units) for n in names}
+    if procs == 1:
+        results = map(_gen_unit, tasks)
+    else:
+        with single_threaded_children():
+            pool = mp.get_context("spawn").Pool(procs)
+        results = pool.imap_unordered(_gen_unit, tasks)
+    for name, u, x, s, sk in results:
+        out[name][0][u] = x
+        out[name][1][u] = s
+        out[name][2][u] = sk
+    if procs > 1:
+        pool.close()
+        pool.join()
+    res = {}
+    for n, (xs, ss, sks) in out.items():
+        res[n] = (xs, np.stack(ss), None if sks[0] is None else np.stack(sks))
+    return res
+
+
 # ----------------------------------------------------------------- CPU oracle
-def oracle_sample(w, T_win=128):
-    """The float64 oracle, as it stands, on a token window of unit 1 of the
-    workload (all heads and features, the first T_win tokens)."""
+def oracle_window(w) -> int:
+    """Tokens of the oracle's sample window: the whole unit up to 128 tokens,
+    else 48 (above every truncated token rank of the grid)."""
+    return w.T if w.T <= 128 else 48
+
+
+def _oracle_unit(task):
+    """One process of the CPU baseline: the float64 oracle, as it stands, on
+    a token window of one unit (all heads and features).  Returns (input
+    bytes, seconds, BLAS threads of this process)."""
+    name, u = task
     from oracle import run as orun
-    x = kvgen.unit_values_f64(w, kvgen.make_unit(w, 1))[:, :T_win, :].copy()
-    s = kvgen.make_signs(w, 1)
+    w = kvgen.WORKLOADS[name]
+    tw = oracle_window(w)
+    x = kvgen.unit_values_f64(w, kvgen.make_unit(w, u))[:, :tw, :].copy()
+    s = kvgen.make_signs(w, u)
     sk = None
     if w.token_mode == "randomized":
-        sk = [kvgen.make_sketch(w, 1).astype(np.float64)]
+        sk = [kvgen.make_sketch(w, u).astype(np.float64)]
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = 1
     t = time.perf_counter()
     orun.encode_units([x], [s], w.rT, w.rd, w.bits, w.block, 10 ** 12, token_mode=w.token_mode,
                       sketches=sk, power_iters=w.power_iters, serialize=True)
-    dt = time.perf_counter() - t
-    return x.size * 2, dt, f"oracle encode of unit g0V tokens [0,{T_win}) ({x.shape}, f64)"
+    return x.size * 2, time.perf_counter() - t, int(threads)
 
 
-def oracle_threads():
+class OraclePool:
+    """P = min(units, host cores) spawned single-threaded processes; a sample
+    runs the oracle on one token window of each of units 0 .. P-1 at once."""
+
+    def __init__(self, name):
+        self.name = name
+        w = kvgen.WORKLOADS[name]
+        self.P = max(1, min(w.n_units, os.cpu_count() or 1))
+        with single_threaded_children():
+            self.pool = mp.get_context("spawn").Pool(self.P)
+        self.pool.map(int, range(self.P))      # the workers are up before timing
+
+    def sample(self):
+        t = time.perf_counter()
+        res = self.pool.map(_oracle_unit, [(self.name, u) for u in range(self.P)], chunksize=1)
+        wall = time.perf_counter() - t
+        nbytes = sum(r[0] for r in res)
+        threads = sum(r[2] for r in res)
+        w = kvgen.WORKLOADS[self.name]
+        desc = (f"oracle encode (factor, full grid, allocation, serialization) of a "
+                f"{oracle_window(w)}-token window of units 0..{self.P - 1} "
+                f"({w.H}x{oracle_window(w)}x{w.D} each, f64), one single-threaded process "
+                f"per unit")
+        return nbytes, wall, threads, desc
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline_record(name, samples=1):
+    pool = OraclePool(name)
     try:
-        from threadpoolctl import threadpool_info
-        n = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
-        return int(n)
-    except Exception:
-        return 1
+        tb, tt = 0, 0.0
+        for _ in range(samples):
+            b, dt, threads, desc = pool.sample()
+            tb += b
+            tt += dt
+    finally:
+        pool.close()
+    return {"value": tb / tt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "host_cpu_count": os.cpu_count(), "cpu_model": cpu_model(),
+            "processes": pool.P, "wall_s_per_sample": tt / samples}
 
 
 def run_reference(args):
     ws, rank, _ = init_dist("gloo")
     if rank != 0:
         return
-    w = kvgen.WORKLOADS[args.workload]
-    for _ in range(args.warmup):
-        oracle_sample(w)
-    tot_b, tot_t = 0, 0.0
-    sample = ""
-    for _ in range(args.steps):
-        b, dt, sample = oracle_sample(w)
-        tot_b += b
-        tot_t += dt
+    pool = OraclePool(args.workload)
+    try:
+        for _ in range(args.warmup):
+            pool.sample()
+        tot_b, tot_t = 0, 0.0
+        threads, sample = 1, ""
+        for _ in range(args.steps):
+            b, dt, threads, sample = pool.sample()
+            tot_b += b
+            tot_t += dt
+    finally:
+        pool.close()
     gbs = tot_b / tot_t / 1e9
-    cores = oracle_threads()
     line = {"metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+            "ms_per_step": 1e3 * tot_t / max(args.steps, 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": args.workload, "sample": sample},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample, "host_cpu_count": os.cpu_count(),
+                             "cpu_model": cpu_model()},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------- GPU path
-def run_ours(args):
+STAGES = ("factor", "sweep", "allocate", "encode", "decode")
+
+
+class Run:
+    """The device state of one workload: inputs, encoder, output buffer."""
+
+    def __init__(self, w, host):
+        import torch
+        from partial_tucker_rotated_st_b300 import codec
+        self.w = w
+        xs, signs, sk = host
+        arr = np.ascontiguousarray(np.stack(xs))
+        Xh = torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16) if w.dtype == "bf16" \
+            else torch.from_numpy(arr)
+        self.Xh = Xh.pin_memory()
+        self.Sh = torch.from_numpy(signs).pin_memory()
+        self.X = self.Xh.cuda()
+        self.S = self.Sh.cuda()
+        self.K = None if sk is None else torch.from_numpy(sk).cuda()
+        self.cfg = codec.config_for(w)
+        self.enc = codec.Encoder(self.cfg, w.n_units)
+        self.xhat = torch.empty(w.n_units, w.H, w.T, w.D, dtype=torch.bfloat16, device="cuda")
+        self.in_bytes = 2 * w.elems_per_unit * w.n_units      # 16-bit-equivalent bytes
+
+
+def timed_steps(run, steps, warmup, flush, st, clk=None):
+    """Warm-up, then `steps` timed steps; per-stage device time (CUDA events
+    on the launching stream), the fused sweep kernel's own time (events the
+    library records around its launch), the decoder's time, host wall time
+    and library launches per step."""
     import torch
-    ws, rank, local = init_dist("nccl")
-    torch.cuda.set_device(local)
-    from partial_tucker_rotated_st_b300 import build as jbuild
-    jbuild.build()
     from partial_tucker_rotated_st_b300 import codec
     from partial_tucker_rotated_st_b300 import jolt as J
-
-    w = kvgen.WORKLOADS[args.workload]
-    U = w.n_units
-    xs = kvgen.make_all(w)
-    signs = np.stack([kvgen.make_signs(w, u) for u in range(U)])
-    sk = None
-    if w.token_mode == "randomized":
-        sk = np.stack([kvgen.make_sketch(w, u) for u in range(U)])
-    arr = np.ascontiguousarray(np.stack(xs))
-    Xh = torch.from_numpy(arr.view(np.int16)).view(torch.bfloat16) if w.dtype == "bf16" \
-        else torch.from_numpy(arr)
-    Xh = Xh.pin_memory()
-    Sh = torch.from_numpy(signs).pin_memory()
-    X = Xh.cuda()
-    S = Sh.cuda()
-    K = None if sk is None else torch.from_numpy(sk).cuda()
-    cfg = codec.config_for(w)
-    enc = codec.Encoder(cfg, U)
-    budget = w.budget_bytes
-    in_bytes = 2 * w.elems_per_unit * U          # 16-bit-equivalent bytes
-    xhat = torch.empty(U, w.H, w.T, w.D, dtype=torch.bfloat16, device="cuda")
-    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
-    st = torch.cuda.current_stream()
-    stages = ("factor", "sweep", "allocate", "encode", "decode")
+    enc, w = run.enc, run.w
 
     def step(timers=None):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-        # the fused sweep kernel alone, between two events the library records
         kev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         for e in kev:
             e.record(st)   # creates the CUDA event; the library records it again
         ev[0].record(st)
-        enc.factor(X, K)
+        enc.factor(run.X, run.K)
         ev[1].record(st)
         J.jolt_set_sweep_events(*kev)
-        enc.sweep(X, S)
+        enc.sweep(run.X, run.S)
         J.jolt_set_sweep_events()
         ev[2].record(st)
-        enc.allocate(budget, refine=True)
+        enc.allocate(w.budget_bytes, refine=True)
         ev[3].record(st)
         enc.choice_host.copy_(enc.choice, non_blocking=True)
         st.synchronize()
-        desc = enc.serialize(X, S, enc.choice_host.tolist())
+        desc = enc.serialize(run.X, run.S, enc.choice_host.tolist())
         ev[4].record(st)
-        codec.decode(desc, enc.blob, enc.stride, J.BF16, out=xhat)
+        codec.decode(desc, enc.blob, enc.stride, J.BF16, out=run.xhat)
         ev[5].record(st)
         if timers is not None:
             timers.append((ev, kev))
         return desc
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
         flush.fill_(1)
     st0 = enc.status()
     if st0 != J.OK:
-        raise SystemExit(f"device status {J.jolt_status_string(st0)}")
+        raise SystemExit(f"{w.name}: device status {J.jolt_status_string(st0)}")
     timers = []
     torch.cuda.synchronize()
-    barrier(ws)
     n0 = J.jolt_launch_count()
-    with ClockSampler(local) as clk:
+    if clk is not None:
         clk.mark_start()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            desc = step(timers)
-            flush.fill_(1)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    desc = None
+    for _ in range(steps):
+        desc = step(timers)
+        flush.fill_(1)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if clk is not None:
         clk.mark_end()
-    launches = (J.jolt_launch_count() - n0) // max(args.steps, 1)
-    barrier(ws)
-    per = {s: 0.0 for s in stages}
-    sweep_kernel_s = 0.0
+    launches = (J.jolt_launch_count() - n0) // max(steps, 1)
+    per = {s: 0.0 for s in STAGES}
+    sweep_k = 0.0
     for ev, kev in timers:
-        for i, s in enumerate(stages):
+        for i, s in enumerate(STAGES):
             per[s] += ev[i].elapsed_time(ev[i + 1]) / 1e3
-        sweep_kernel_s += kev[0].elapsed_time(kev[1]) / 1e3
-    per = {s: v / args.steps for s, v in per.items()}
-    sweep_kernel_s /= args.steps
+        sweep_k += kev[0].elapsed_time(kev[1]) / 1e3
+    per = {s: v / steps for s, v in per.items()}
+    st1 = enc.status()
+    if st1 != J.OK:
+        raise SystemExit(f"{w.name}: device status {J.jolt_status_string(st1)}")
+    return {"per": per, "sweep_kernel_s": sweep_k / steps, "wall_s": wall / steps,
+            "launches": int(launches), "desc": desc}
+
+
+def blob_bytes_of(desc):
+    return sum(int(d.bytes) for d in desc)
+
+
+def decode_roofline(w, desc, dec_t, hbm, name_for_traffic):
+    alg = blob_bytes_of(desc) + 2 * w.elems_per_unit * w.n_units
+    return {"kernel": "decode_tc_kernel", "bound": "hbm", "achieved": alg / dec_t / 1e9,
+            "peak": hbm, "unit": "GB/s", "frac": alg / dec_t / 1e9 / hbm,
+            "bytes_algorithmic": int(alg), "traffic": decode_traffic(name_for_traffic)}
+
+
+def config_record(run, res, hbm, kind, pk, sms):
+    """Per-configuration record: encode and decode GB/s, stage times, the
+    fused sweep's and the decoder's rooflines."""
+    w = run.w
+    per = res["per"]
+    enc_t = per["factor"] + per["sweep"] + per["allocate"] + per["encode"]
+    return {"workload": w.name, "units": w.n_units, "unit_shape": [w.H, w.T, w.D],
+            "token_mode": w.token_mode, "budget_bytes": w.budget_bytes,
+            "encode_gbs": run.in_bytes / enc_t / 1e9,
+            "decode_gbs": run.in_bytes / per["decode"] / 1e9,
+            "decode_output": f"bf16 [{w.n_units}][{w.H}][{w.T}][{w.D}]",
+            "stages_ms": {s: 1e3 * v for s, v in per.items()},
+            "sweep_roofline": roofline(w, res["sweep_kernel_s"], hbm, kind, pk, sms),
+            "decode_roofline": decode_roofline(w, res["desc"], per["decode"], hbm, w.name),
+            "gpu_launches": res["launches"]}
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    names = [args.workload] + [c for c in args.configs if c != args.workload]
+    host = gen_inputs(names, max(1, (os.cpu_count() or 1) // ws))   # before any CUDA call
+    ws, rank, local = init_dist("nccl")
+    torch.cuda.set_device(local)
+    from partial_tucker_rotated_st_b300 import build as jbuild
+    jbuild.build()
+    from partial_tucker_rotated_st_b300 import jolt as J
+
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
+    hbm, kind, pk = peaks()
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+
+    # ---- the line's workload
+    w = kvgen.WORKLOADS[args.workload]
+    run = Run(w, host.pop(args.workload))
+    torch.cuda.synchronize()
+    barrier(ws)
+    with ClockSampler(local) as clk:
+        res = timed_steps(run, args.steps, args.warmup, flush, st, clk)
+    barrier(ws)
+    per = res["per"]
     enc_t = per["factor"] + per["sweep"] + per["allocate"] + per["encode"]
     enc_t = max_over_ranks(ws, enc_t, "cuda")
     dec_t = max_over_ranks(ws, per["decode"], "cuda")
-    value = ws * in_bytes / enc_t / 1e9
-    dec_gbs = ws * in_bytes / dec_t / 1e9
-    blob_bytes = sum(int(d.bytes) for d in desc)
+    value = ws * run.in_bytes / enc_t / 1e9
+    dec_gbs = ws * run.in_bytes / dec_t / 1e9
+    desc = res["desc"]
 
     # end to end through the public calls, from pinned host memory
-    blob_h = torch.empty(U * enc.stride, dtype=torch.uint8, pin_memory=True)
+    enc = run.enc
+    blob_h = torch.empty(w.n_units * enc.stride, dtype=torch.uint8, pin_memory=True)
     d2h = 0
     e2e_t = 0.0
+    r = None
     for i in range(args.warmup + args.steps):
         flush.fill_(1)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        X.copy_(Xh, non_blocking=True)
-        S.copy_(Sh, non_blocking=True)
-        r = enc.encode(X, S, budget, K)
+        run.X.copy_(run.Xh, non_blocking=True)
+        run.S.copy_(run.Sh, non_blocking=True)
+        r = enc.encode(run.X, run.S, w.budget_bytes, run.K)
         d2h = enc.blobs_to_host(r.desc, blob_h)   # the serialized bytes, not the slot padding
         e1.record(st)
         e1.synchronize()
         if i >= args.warmup:
             e2e_t += e0.elapsed_time(e1) / 1e3
     e2e_t = max_over_ranks(ws, e2e_t / args.steps, "cuda")
-    e2e = {"value": ws * in_bytes / e2e_t / 1e9, "unit": "GB/s",
-           "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size() + Sh.numel()),
+    e2e = {"value": ws * run.in_bytes / e2e_t / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": int(run.Xh.numel() * run.Xh.element_size() + run.Sh.numel()),
            "d2h_bytes_per_step": int(d2h)}
 
-    hbm, kind, pk = peaks()
     attn = attention_bench(args, w, r.desc, enc, flush, st, hbm, kind)
     adm = admission_bench(args, w, r.desc, enc, flush, st)
-    modeled = modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws)
-
-    # dominant stage and its roofline
+    modeled = modeled_allocator(args, w, enc, run.X, run.K, run.S, w.budget_bytes, run.in_bytes,
+                                flush, st, ws)
     dom = max(("factor", "sweep", "encode", "decode"), key=lambda s: per[s])
-    roof = roofline(w, sweep_kernel_s, hbm, kind, pk)
+    roof = roofline(w, res["sweep_kernel_s"], hbm, kind, pk, sms)
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * (enc_t + dec_t),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": args.workload, "units": U,
-                       "unit_shape": [w.H, w.T, w.D], "input": "bf16" if w.dtype == "bf16" else "f32",
-                       "budget_bytes": budget, "token_mode": w.token_mode,
+            "config": {"workload": args.workload, "units": w.n_units,
+                       "unit_shape": [w.H, w.T, w.D],
+                       "input": "bf16" if w.dtype == "bf16" else "f32",
+                       "budget_bytes": w.budget_bytes, "token_mode": w.token_mode,
                        "allocator": "lambda bisection + greedy swaps",
-                       "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas{ws}"},
+                       "l2": "flushed between steps (256 MiB write)",
+                       "parallelism": f"replicas{ws}"},
             "decode": {"value": dec_gbs, "unit": "GB/s",
-                       "roofline": {"kernel": "decode_tc_kernel", "bound": "hbm",
-                                    "achieved": (blob_bytes + 2 * w.elems_per_unit * U) / dec_t / 1e9,
-                                    "peak": hbm, "unit": "GB/s",
-                                    "frac": (blob_bytes + 2 * w.elems_per_unit * U) / dec_t / 1e9 / hbm,
-                                    "bytes_algorithmic": int(blob_bytes + 2 * w.elems_per_unit * U),
-                                    "traffic": decode_traffic(args.workload)}},
+                       "roofline": decode_roofline(w, desc, dec_t, hbm, args.workload)},
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "dominant_stage": dom,
-            "wall_ms_per_step": 1e3 * wall / args.steps,
+            "wall_ms_per_step": 1e3 * res["wall_s"],
             "roofline": roof,
             "e2e": e2e,
             "modeled_allocator": modeled,
             "attention": attn,
             "admission": adm,
-            "gpu_launches": int(launches),
+            "gpu_launches": res["launches"],
+            "sm_count": sms,
             "clocks": clk.summary()}
+    del run, r, enc
+    torch.cuda.empty_cache()
+
+    # ---- one record per other configuration, timed the same way
+    recs = {}
+    for name in args.configs:
+        if name == args.workload:
+            continue
+        wx = kvgen.WORKLOADS[name]
+        rx = Run(wx, host.pop(name))
+        resx = timed_steps(rx, args.steps, args.warmup, flush, st)
+        recs[name] = config_record(rx, resx, hbm, kind, pk, sms)
+        del rx
+        torch.cuda.empty_cache()
+    line["configs"] = recs
+
     if rank == 0 and not args.no_cpu_baseline:
-        b, dt, sample = oracle_sample(w)
-        line["cpu_baseline"] = {"value": b / dt / 1e9, "unit": "GB/s", "cores": oracle_threads(),
-                                "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = cpu_baseline_record(args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
-SWEEP_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tucker_rotated_st_b300",
-                         "csrc", "gram_tc.cu")
-SWEEP_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
-                             "sweep_tc_kernel_mistral_t1024.md")
+SWEEP_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "gram_tc.cu")
+SWEEP_PROFILE = os.path.join(ROOT, "profiles", "sweep_tc_kernel_mistral_t1024.md")
 
 
 def attention_bench(args, w, desc, enc, flush, st, hbm, hbm_kind, nq=4):
@@ -434,7 +634,7 @@ def attention_bench(args, w, desc, enc, flush, st, hbm, hbm_kind, nq=4):
             "launches_per_call": int(launches),
             "roofline": {"kernel": "attend_prep + attend_chunk + attend_merge (one call)",
                          "bound": "hbm", "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
-                         "frac": alg / t / 1e9 / hbm, "traffic": attend_traffic(args.workload),
+                         "frac": alg / t / 1e9 / hbm, "traffic": attend_traffic(w.name),
                          "bytes_algorithmic": int(alg), "peak_kind": hbm_kind},
             "materialize_then_sdpa_ms": 1e3 * tm,
             "speedup_vs_materialize": tm / t}
@@ -537,35 +737,29 @@ def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):
             "bytes_measured_choice": int(cm[idx, zm].sum())}
 
 
-ATTEND_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
-                              "attend_chunk_kernel_mistral_t1024.md")
-ATTEND_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tucker_rotated_st_b300",
-                          "csrc", "attend.cu")
-
-
-DECODE_PROFILE = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
-                              "decode_tc_kernel_mistral_t1024.md")
-DECODE_SRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "partial_tucker_rotated_st_b300",
-                          "csrc", "decode_tc.cu")
+ATTEND_PROFILE = os.path.join(ROOT, "profiles", "attend_chunk_kernel_mistral_t1024.md")
+ATTEND_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "attend.cu")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_tc_kernel_mistral_t1024.md")
+DECODE_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "decode_tc.cu")
 
 
 def traffic_record(profile, src_path, hash_key, bytes_key, workload):
-    """The DRAM bytes recorded on the `traffic_record:` line of a committed ncu
-    summary, only while the kernel source still hashes to the sha256 prefix
-    recorded beside them and the workload matches; else None (the counters
-    belong to another kernel or workload)."""
+    """The DRAM bytes recorded on a `traffic_record:` line of a committed ncu
+    summary for this workload, only while the kernel source still hashes to
+    the sha256 prefix recorded beside them; else None (the counters belong to
+    another kernel source or workload)."""
     try:
         txt = open(profile).read()
         src = hashlib.sha256(open(src_path, "rb").read()).hexdigest()[:16]
     except OSError:
         return None
-    rec = {}
     for line in txt.splitlines():
-        if line.startswith("traffic_record:"):
-            rec = json.loads(line.split(":", 1)[1])
-    if rec.get(hash_key) != src or rec.get("workload") != workload:
-        return None
-    return int(rec[bytes_key])
+        if not line.startswith("traffic_record:"):
+            continue
+        rec = json.loads(line.split(":", 1)[1])
+        if rec.get(hash_key) == src and rec.get("workload") == workload:
+            return int(rec[bytes_key])
+    return None
 
 
 def decode_traffic(workload):
@@ -586,15 +780,17 @@ def sweep_traffic(workload):
                           "dram_bytes_per_launch", workload)
 
 
-def roofline(w, kernel_s, hbm, kind, pk):
-    """Roofline of the fused sweep kernel (the dominant kernel of the step).
-    Its dense products (the rotation of X and every rank checkpoint's
-    reconstruction) run on the tensor cores; what bounds it is the FP32
-    scoring of every candidate, counted per element and rank pair as: the
-    residual y (1 FMA), |y| max (1), y^2 for b = 0 (1 FMA), and per b > 0 the
-    scaled rounding (1 FMA + 1 add), the residual (1 FMA) and its square
-    (1 FMA), FMA = 2 flops: 26 flops per pair per element.  `kernel_s` is the
-    kernel's own average duration (CUDA events around its launch)."""
+def roofline(w, kernel_s, hbm, kind, pk, sms=148):
+    """Roofline of the fused sweep kernel.  Its dense products (the rotation
+    of X and every rank checkpoint's reconstruction) run on the tensor cores;
+    what bounds it is the FP32 scoring of every candidate, counted per element
+    and rank pair as: the residual y (1 FMA), |y| max (1), y^2 for b = 0
+    (1 FMA), and per b > 0 the scaled rounding (1 FMA + 1 add), the residual
+    (1 FMA) and its square (1 FMA), FMA = 2 flops: 26 flops per pair per
+    element.  `kernel_s` is the kernel's own average duration (CUDA events
+    around its launch); `sms` the device's multiprocessor count.  The HBM
+    fraction of the same launch (X read once, 2 bytes per element) is
+    reported beside it."""
     U, N = w.n_units, w.elems_per_unit
     RT = max(r for r in w.rT if r != kvgen.FULL)
     RD = max(r for r in w.rd if r != kvgen.FULL)
@@ -605,26 +801,42 @@ def roofline(w, kernel_s, hbm, kind, pk):
     tensor_el = 2 * w.D + 2 * 2 * (nd * RT + RD)   # rotation; chains with the hi/lo split
     flops = flops_el * N * U
     sm_max = pk.get("sm_max_mhz", 2032.0)
-    peak = 148 * 128 * 2 * sm_max * 1e6 / 1e12
+    peak = sms * 128 * 2 * sm_max * 1e6 / 1e12
     ach = flops / kernel_s / 1e12
+    hbm_ach = 2.0 * N * U / kernel_s / 1e9
     return {"kernel": "sweep_tc_kernel", "bound": "alu", "achieved": ach, "peak": peak,
             "unit": "TFLOP/s", "frac": ach / peak, "traffic": sweep_traffic(w.name),
             "kernel_ms": 1e3 * kernel_s,
-            "peak_source": "derived: FP32 pipe, 148 SMs x 128 lanes x 2 flop x max SM clock",
+            "peak_source": f"derived: FP32 pipe, {sms} SMs (device) x 128 lanes x 2 flop x "
+                           f"max SM clock",
             "flops_per_element": flops_el, "tensor_flops_per_element": tensor_el,
             "bytes_per_element_algorithmic": 2,
+            "hbm_achieved_gbs": hbm_ach, "hbm_frac": hbm_ach / hbm,
             "hbm_peak_gbs": hbm, "hbm_peak_kind": kind}
+
+
+def parse_configs(s):
+    if s in ("", "none"):
+        return []
+    out = [c.strip() for c in s.split(",") if c.strip()]
+    for c in out:
+        if c not in kvgen.WORKLOADS:
+            raise SystemExit(f"unknown workload {c}")
+    return out
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
-    ap.add_argument("--workload", default="mistral_t1024", choices=sorted(kvgen.WORKLOADS))
+    ap.add_argument("--workload", default=MAIN_WORKLOAD, choices=sorted(kvgen.WORKLOADS))
+    ap.add_argument("--configs", default=",".join(EXTRA_CONFIGS),
+                    help="comma-separated workloads with a record of their own, or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    args.configs = parse_configs(args.configs)
     if args.impl == "reference":
         run_reference(args)
     else:

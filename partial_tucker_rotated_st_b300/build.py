@@ -1,12 +1,14 @@
 """Build libjolt.so in place with nvcc for sm_103a (B300).
 
-    python -m partial_tucker_rotated_st_b300.build [--debug]
+    python -m partial_tucker_rotated_st_b300.build [-v]
 
-Every .cu file under csrc/ is compiled into one shared library next to this
+Every .cu file under csrc/ is compiled to an object (in parallel, one nvcc
+per file) and the objects are linked into one shared library next to this
 file.  nvcc cross-compiles, so no GPU is needed to build.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import glob
 import os
 import subprocess
@@ -15,6 +17,7 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libjolt.so")
+OBJ_DIR = os.path.join(HERE, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,13 +41,28 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
     if not force and up_to_date():
         return LIB
     nvcc = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
-    cmd = [nvcc, "-O3", "-std=c++17", "-lineinfo", *ARCH, "-shared", "-Xcompiler", "-fPIC",
-           "-I", os.path.join(ROOT, "include"), "-o", LIB + ".tmp", *sources(), "-lcudart"]
-    if extra:
-        cmd[1:1] = list(extra)
+    flags = ["-O3", "-std=c++17", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC",
+             "-I", os.path.join(ROOT, "include")] + list(extra or [])
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    objs = [os.path.join(OBJ_DIR, os.path.basename(s)[:-3] + ".o") for s in sources()]
+    cmds = [[nvcc, *flags, "-c", s, "-o", o] for s, o in zip(sources(), objs)]
+
+    def compile_one(cmd):
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        return subprocess.run(cmd, capture_output=not verbose, text=True)
+
+    workers = max(1, min(len(cmds), os.cpu_count() or 1))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        results = list(ex.map(compile_one, cmds))
+    for cmd, r in zip(cmds, results):
+        if r.returncode != 0:
+            sys.stderr.write((r.stderr or "") + (r.stdout or ""))
+            raise subprocess.CalledProcessError(r.returncode, cmd)
+    link = [nvcc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-lcudart"]
     if verbose:
-        print(" ".join(cmd), flush=True)
-    subprocess.run(cmd, check=True)
+        print(" ".join(link), flush=True)
+    subprocess.run(link, check=True)
     os.replace(LIB + ".tmp", LIB)
     return LIB
 
