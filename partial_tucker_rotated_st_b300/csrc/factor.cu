@@ -668,7 +668,13 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     TRY(launch_jacobi(c.f(L.o_Sd), ub4, D, D, 1, 0, U, c.f(L.o_evd), ub4, c.f(L.o_Vd), ub4, D, D,
                       status, ub4, done, ub4, JAC_ABS_EXACT, fs));
   }
-  if (RD > 0) {
+  // projection Y = X U_d[:, :RD]: on the tensor cores for bf16 X (which also
+  // writes U_d16, Y16 and the token-Gram relayout Yt), else the SIMT product
+  bool yt_done = false;
+  if (RD > 0 && proj_tc_supported(L)) {
+    TRY(proj_tc(L, U, X, ws, true, fs));
+    yt_done = L.o_Yt != 0;
+  } else if (RD > 0) {
     round_f16_kernel<<<dim3(blocks_for(D * RD), 1, U), 256, 0, fs>>>(ws, ub, L.o_Vd, D, L.o_Ud16,
                                                                      RD, D, RD, 0, 0, 1);
     JOLT_LAUNCH_CHECK();
@@ -686,7 +692,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     char* preg0 = ws + (size_t)U * ub;
     const size_t pb0 = L.prob_bytes;
     if (ygram_tc_supported(L)) {
-      TRY(ytrans(L, U, ws, fs));
+      if (!yt_done) TRY(ytrans(L, U, ws, fs));
       TRY(ygram_tc(L, U, ws, preg0, pb0, fs));
     } else {
       for (int id = 0; id < L.ndt; ++id) {
@@ -740,7 +746,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       // when T > 128), then one batched solve for all of them
       if (early_tr) {
       } else if (T > 128 && ygram_tc_supported(L)) {
-        TRY(ytrans(L, U, ws, st));
+        if (!yt_done) TRY(ytrans(L, U, ws, st));
         TRY(ygram_tc(L, U, ws, preg, pb, st));
       } else {
         for (int id = 0; id < ndt; ++id) {

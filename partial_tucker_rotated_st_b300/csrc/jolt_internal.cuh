@@ -71,6 +71,7 @@ struct Layout {
   size_t o_UT32, o_UT16, o_tokev, o_G32, o_G16, o_W, o_part, o_P;
   size_t o_Yt;           // Y relaid [T][RD*H] and its tf32 low part (token Gram)
   size_t o_Hs;           // diag(sigma) H_D as bf16 [D][D] (tensor-core sweep), or 0
+  size_t o_Vs3;          // U_d in three bf16 parts [3 * 32][D] (tensor-core projection), or 0
   size_t unit_bytes;
   // Token-mode problems, one per (unit, feature rank), in a region after the
   // n unit regions of a call: truncated rank id of unit u is problem
@@ -161,6 +162,12 @@ jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride,
 jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, size_t o_Z,
                   cudaStream_t st);
 bool ygram_tc_supported(const Layout& L);
+// Y = X U_d[:, :RD] (bf16 X, D = 128, RD <= 32) on the tensor cores: U_d16,
+// Y16, Yt and its tf32 low part (when the layout has Yt), and Y in fp32 when
+// write_y.
+bool proj_tc_supported(const Layout& L);
+jolt_status proj_tc(const Layout& L, int n_units, const void* X, char* ws, bool write_y,
+                    cudaStream_t st);
 // Yt (unit region) = Y relaid [T][RD * H] and its tf32 low part.
 jolt_status ytrans(const Layout& L, int n_units, char* ws, cudaStream_t st);
 // p_ST of truncated problem p = u * ndt + id: the Gram of feature ranks

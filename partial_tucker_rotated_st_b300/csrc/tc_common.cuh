@@ -6,12 +6,21 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 namespace jolt {
 namespace tc {
 
 constexpr int WAIT_LIMIT = 1 << 24;
+
+// Host: the driver's cuTensorMapEncodeTiled (null when unavailable), and a
+// tiled tensor map with the 128-byte swizzle over a rank-2 or rank-3 tensor
+// (dims innermost first, strides in bytes of the outer dims).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
