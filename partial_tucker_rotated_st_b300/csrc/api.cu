@@ -133,6 +133,9 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   L.o_Hs = (L.dtype == JOLT_BF16 && D == 128) ? sect((size_t)D * D * 2) : 0;
   L.o_Vs3 = (L.dtype == JOLT_BF16 && D == 128 && RD > 0 && RD <= 32) ? sect((size_t)3 * 32 * D * 2)
                                                                       : 0;
+  L.o_Ub3 = (L.dtype == JOLT_BF16 && D == 128 && RT > 0 && RT <= 32 && L.nd * 96 <= 512)
+                ? sect((size_t)T * 512 * 2)
+                : 0;
   L.o_UT32 = sect((size_t)L.nd * T * RT * 4);
   L.o_UT16 = sect((size_t)L.nd * T * RT * 2);
   L.o_tokev = sect((size_t)L.nd * RT * 4);

@@ -787,8 +787,11 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       ws, ub, L.o_UT32, L.o_tokev, L.o_status, preg, pb, L.p_UT, L.p_ev, 1, L.p_status, U, ndt, T,
       RT);
   JOLT_LAUNCH_CHECK();
-  // cores G(r_d)[h] = U_T^T A_h  (RT x rdv): the truncated ranks share one
-  // pass over Y, the whole-feature rank reads X
+  // cores G(r_d)[h] = U_T^T A_h  (RT x rdv): on the tensor cores for bf16 X
+  // (one pass over X for every rank, fp16 cores and U_T written directly)
+  if (cores_tc_supported(L)) return cores_tc(L, U, X, ws, st);
+  // else the truncated ranks share one pass over Y, the whole-feature rank
+  // reads X
   for (int pass = 0; pass < 2; ++pass) {
     CoreArgs ca;
     memset(&ca, 0, sizeof(ca));

@@ -72,6 +72,7 @@ struct Layout {
   size_t o_Yt;           // Y relaid [T][RD*H] and its tf32 low part (token Gram)
   size_t o_Hs;           // diag(sigma) H_D as bf16 [D][D] (tensor-core sweep), or 0
   size_t o_Vs3;          // U_d in three bf16 parts [3 * 32][D] (tensor-core projection), or 0
+  size_t o_Ub3;          // every rank's U_T in three bf16 parts [T][512] (tensor-core cores), or 0
   size_t unit_bytes;
   // Token-mode problems, one per (unit, feature rank), in a region after the
   // n unit regions of a call: truncated rank id of unit u is problem
@@ -168,6 +169,10 @@ bool ygram_tc_supported(const Layout& L);
 bool proj_tc_supported(const Layout& L);
 jolt_status proj_tc(const Layout& L, int n_units, const void* X, char* ws, bool write_y,
                     cudaStream_t st);
+// The cores of every feature rank from X and U_T (bf16 X, D = 128, r_T <= 32):
+// G16 of every rank and U_T16.
+bool cores_tc_supported(const Layout& L);
+jolt_status cores_tc(const Layout& L, int n_units, const void* X, char* ws, cudaStream_t st);
 // Yt (unit region) = Y relaid [T][RD * H] and its tf32 low part.
 jolt_status ytrans(const Layout& L, int n_units, char* ws, cudaStream_t st);
 // p_ST of truncated problem p = u * ndt + id: the Gram of feature ranks

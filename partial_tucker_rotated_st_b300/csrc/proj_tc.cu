@@ -1,5 +1,5 @@
-// Feature-mode projection Y = X U_d[:, :RD] on the 5th-generation tensor
-// cores, for bf16 X with D = 128.
+// Feature-mode projection Y = X U_d[:, :RD] and the Tucker cores on the
+// 5th-generation tensor cores, for bf16 X with D = 128.
 //
 // ["Technical Summary: A JOLT for the KV Cache", Methodology 1: sequential
 //  truncation, the token mode is taken on the tensor already projected onto
@@ -17,8 +17,19 @@
 // token row) writes, per head, Y16 = fp16(Y) [H][T][RD] and, when asked, Y in
 // fp32 [H][T][RD]; and the token-Gram relayout Yt[t][j H + h] with its tf32
 // low part, HB consecutive heads per store, staged through shared memory.
+//
+// Cores (after the token mode):
+//   G(r_d)[h] = U_T(r_d)^T X_h U_d[:, :r_d]   (U_d = I for the whole feature rank)
+// as Z = X_h^T [U_T(r_d) of every feature rank], one MN-major kind::f16
+// product per head over K = T: X_h (bf16, exact) and each U_T split into three
+// bf16 parts (N = 96 per rank, up to 480 TMEM columns).  The whole-feature
+// core is Z itself; a truncated core is the small product U_d[:, :r_d]^T Z in
+// fp32 on the CUDA cores from shared memory.  Cores and U_T are written in
+// fp16 (the storage type) directly.
 #include "jolt_internal.cuh"
 #include "tc_common.cuh"
+
+#include <string.h>
 
 namespace jolt {
 
@@ -200,6 +211,210 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ C
   if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
 }
 
+
+// ---------------------------------------------------------------- cores
+constexpr int CT_THREADS = 192;             // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int CT_KT = 64;                   // tokens per stage
+constexpr int CT_XST = CT_KT * 256;         // X stage: 64 tokens x 128 features (two atoms)
+constexpr int CT_NATOM = CT_KT * 128;       // one 64-column atom of the U_T parts
+constexpr int CT_NMAX = 512;                // columns of the U_T part rows
+constexpr int CT_STAGES = 2;
+constexpr int CT_ZROW = 36;                 // padded row (floats) of the staged Z and U_d
+
+struct CoresArgs {
+  int H, T, RT, nd, ntot, natoms;
+  int rd[JOLT_MAX_GRID];
+  int full_id;                  // index of the whole feature rank, or -1
+  char* ws;
+  size_t ub, o_Vd, o_G16, o_status;
+};
+
+// Ub3[u][t][96 id + 32 p + j] = bf16 part p of U_T(id)[t][j] (zero for
+// j >= RT and for the columns past nd * 96); U_T16[id][t][j] = fp16(U_T).
+__global__ void split_ut_kernel(char* ws, size_t ub, size_t o_UT32, size_t o_UT16, size_t o_Ub3,
+                                int T, int RT, int nd) {
+  const int u = blockIdx.y;
+  const float* U32 = (const float*)(ws + (size_t)u * ub + o_UT32);
+  __half* U16 = (__half*)(ws + (size_t)u * ub + o_UT16);
+  __nv_bfloat16* Ub = (__nv_bfloat16*)(ws + (size_t)u * ub + o_Ub3);
+  const long long n = (long long)T * CT_NMAX;
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(e / CT_NMAX), c = (int)(e % CT_NMAX);
+    const int id = c / 96, p = (c % 96) / 32, j = c % 32;
+    float v = 0.f;
+    if (id < nd && j < RT) v = U32[((size_t)id * T + t) * RT + j];
+    const float r1 = v - __bfloat162float(__float2bfloat16_rn(v));
+    const float r2 = r1 - __bfloat162float(__float2bfloat16_rn(r1));
+    const float part = p == 0 ? v : (p == 1 ? r1 : r2);
+    Ub[e] = __float2bfloat16_rn(part);
+    if (p == 0 && id < nd && j < RT) U16[((size_t)id * T + t) * RT + j] = __float2half_rn(v);
+  }
+}
+
+__global__ void __launch_bounds__(CT_THREADS, 1)
+cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tU,
+                CoresArgs a) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const int stage_bytes = CT_XST + a.natoms * CT_NATOM;
+  // the stages, later the epilogue's Z and U_d staging; the barriers after both
+  const int epi_bytes = (a.nd + 1) * 128 * CT_ZROW * 4;
+  const int region = CT_STAGES * stage_bytes > epi_bytes ? CT_STAGES * stage_bytes : epi_bytes;
+  struct Bars { uint64_t full[CT_STAGES], empty[CT_STAGES], accum; uint32_t tmem; };
+  Bars* S = (Bars*)(base + region);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int h = blockIdx.x, u = blockIdx.y;
+  const int nk = (a.T + CT_KT - 1) / CT_KT;
+  char* wu = a.ws + (size_t)u * a.ub;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < CT_STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&S->accum), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % CT_STAGES, r = kk / CT_STAGES;
+      if (r > 0 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), (r - 1) & 1)) { ok = false; break; }
+      const uint32_t fb = tc::smem_u32(&S->full[s]);
+      tc::mbar_expect_tx(fb, stage_bytes);
+      const uint32_t sa = tc::smem_u32(base + s * stage_bytes);
+      const int xr = u * a.H + h;
+      tc::tma_load_3d(sa, &tX, 0, kk * CT_KT, xr, fb);
+      tc::tma_load_3d(sa + CT_XST / 2, &tX, 64, kk * CT_KT, xr, fb);
+      for (int at = 0; at < a.natoms; ++at)
+        tc::tma_load_3d(sa + CT_XST + at * CT_NATOM, &tU, 64 * at, kk * CT_KT, u, fb);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const int n1 = a.ntot < 256 ? a.ntot : 256, n2 = a.ntot - n1;
+    const uint32_t id1 = tc::idesc_bf16(128, n1, 1, 1);
+    const uint32_t id2 = tc::idesc_bf16(128, n2 > 0 ? n2 : 16, 1, 1);
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % CT_STAGES, r = kk / CT_STAGES;
+      if (!tc::mbar_wait(tc::smem_u32(&S->full[s]), r & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(base + s * stage_bytes);
+      const uint32_t sb = sa + CT_XST;
+#pragma unroll
+      for (int k4 = 0; k4 < CT_KT / 16; ++k4) {
+        const uint64_t ad = tc::sdesc_sw128(sa + 2048 * k4, CT_XST / 2, 1024);
+        const uint64_t b1 = tc::sdesc_sw128(sb + 2048 * k4, CT_NATOM, 1024);
+        tc::mma_f16(tmem, ad, b1, id1, (kk | k4) != 0);
+        if (n2 > 0) {
+          const uint64_t b2 = tc::sdesc_sw128(sb + 4 * CT_NATOM + 2048 * k4, CT_NATOM, 1024);
+          tc::mma_f16(tmem + 256, ad, b2, id2, (kk | k4) != 0);
+        }
+      }
+      tc::mma_commit(tc::smem_u32(&S->empty[s]));
+    }
+    tc::mma_commit(tc::smem_u32(&S->accum));
+  }
+  // ---- epilogue: thread e (warps 2-5) owns feature row d = TMEM lane
+  const int e = threadIdx.x - 64;
+  float* Zs = reinterpret_cast<float*>(base);                      // [truncated id][d][36]
+  float* Vs = Zs + (size_t)a.nd * 128 * CT_ZROW;                    // [d][36]
+  const int RT = a.RT;
+  if (warp >= 2) {
+    if (!tc::mbar_wait(tc::smem_u32(&S->accum), 0)) ok = false;
+    tc::tc_fence_after();
+    const int q = warp & 3, d = 32 * q + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+    int it = 0;
+    for (int id = 0; id < a.nd; ++id) {
+      float c0[32], c1[32], c2[32];
+      tc::tmem_ld32(tl + (uint32_t)(96 * id), c0);
+      tc::tmem_ld32(tl + (uint32_t)(96 * id + 32), c1);
+      tc::tmem_ld32(tl + (uint32_t)(96 * id + 64), c2);
+      float z[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) z[j] = ok ? (c2[j] + c1[j]) + c0[j] : __int_as_float(0x7fc00000);
+      if (id == a.full_id) {
+        // G(D)[h][j][d] = Z[d][j]
+        __half* G = (__half*)(wu + a.o_G16) + (size_t)id * a.H * RT * 128 + (size_t)h * RT * 128;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < RT) G[(size_t)j * 128 + d] = __float2half_rn(z[j]);
+      } else {
+        float* zr = Zs + ((size_t)it * 128 + d) * CT_ZROW;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(zr + j) = make_float4(z[j], z[j + 1], z[j + 2], z[j + 3]);
+        ++it;
+      }
+    }
+    // U_d[d][:32] (unrounded, fp32)
+    const float* Vd = (const float*)(wu + a.o_Vd) + (size_t)d * 128;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      *reinterpret_cast<float4*>(Vs + (size_t)d * CT_ZROW + j) = *reinterpret_cast<const float4*>(Vd + j);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+  // ---- truncated cores G(r_d)[h][jt][jd] = sum_d Z[d][jt] U_d[d][jd], one
+  // 4 x 4 block per thread and step
+  if (warp >= 2) {
+    int tot = 0;
+    for (int id = 0; id < a.nd; ++id)
+      if (id != a.full_id) tot += (RT / 4) * (a.rd[id] / 4);
+    for (int tile = e; tile < tot; tile += 128) {
+      int rem = tile, it = 0, id = 0;
+      for (id = 0; id < a.nd; ++id) {
+        if (id == a.full_id) continue;
+        const int n = (RT / 4) * (a.rd[id] / 4);
+        if (rem < n) break;
+        rem -= n;
+        ++it;
+      }
+      const int rd = a.rd[id];
+      const int jt0 = (rem / (rd / 4)) * 4, jd0 = (rem % (rd / 4)) * 4;
+      float acc[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+      const float* zb = Zs + (size_t)it * 128 * CT_ZROW + jt0;
+      const float* vb = Vs + jd0;
+#pragma unroll 4
+      for (int d = 0; d < 128; ++d) {
+        const float4 zv = *reinterpret_cast<const float4*>(zb + (size_t)d * CT_ZROW);
+        const float4 vv = *reinterpret_cast<const float4*>(vb + (size_t)d * CT_ZROW);
+        const float zz[4] = {zv.x, zv.y, zv.z, zv.w}, ww[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(zz[i], ww[j], acc[i][j]);
+      }
+      __half* G = (__half*)(wu + a.o_G16) + (size_t)id * a.H * RT * 128 + (size_t)h * RT * rd;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __half2 p0 = __floats2half2_rn(acc[i][0], acc[i][1]);
+        __half2 p1 = __floats2half2_rn(acc[i][2], acc[i][3]);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t*>(&p0);
+        v.y = *reinterpret_cast<uint32_t*>(&p1);
+        *reinterpret_cast<uint2*>(G + (size_t)(jt0 + i) * rd + jd0) = v;
+      }
+    }
+  }
+  if (!ok) atomicOr((int*)(wu + a.o_status), ST_TIMEOUT);
+}
+
+size_t cores_smem(int natoms, int nd) {
+  const size_t stages = (size_t)CT_STAGES * (CT_XST + natoms * CT_NATOM);
+  const size_t epi = (size_t)(nd + 1) * 128 * CT_ZROW * 4;
+  return 1024 + (stages > epi ? stages : epi) + 128;
+}
+
 template <int HB>
 size_t proj_smem() {
   return 1024 + (size_t)HB * PJ_XBYTES + 2 * PJ_N * 128 + 64;
@@ -251,6 +466,53 @@ jolt_status proj_tc(const Layout& L, int U, const void* X, char* ws, bool write_
   if (L.H % 4 == 0) return launch_proj<4>(dim3(tiles, L.H / 4, U), tX, tB, a, st);
   if (L.H % 2 == 0) return launch_proj<2>(dim3(tiles, L.H / 2, U), tX, tB, a, st);
   return launch_proj<1>(dim3(tiles, L.H, U), tX, tB, a, st);
+}
+
+
+bool cores_tc_supported(const Layout& L) {
+  if (!(L.dtype == JOLT_BF16 && L.D == 128 && L.RT > 0 && L.RT <= 32 && L.RT % 4 == 0 &&
+        L.nd * 96 <= CT_NMAX && L.o_Ub3 != 0 && tc::encode_fn() != nullptr))
+    return false;
+  for (int i = 0; i < L.nd; ++i)
+    if (L.rd[i] != L.D && (L.rd[i] % 4 || L.rd[i] > 32)) return false;
+  return true;
+}
+
+jolt_status cores_tc(const Layout& L, int U, const void* X, char* ws, cudaStream_t st) {
+  if (!cores_tc_supported(L)) return JOLT_ERR_INVALID;
+  split_ut_kernel<<<dim3(256, U), 256, 0, st>>>(ws, L.unit_bytes, L.o_UT32, L.o_UT16, L.o_Ub3,
+                                                L.T, L.RT, L.nd);
+  JOLT_LAUNCH_CHECK();
+  CoresArgs a;
+  memset(&a, 0, sizeof(a));
+  a.H = L.H; a.T = L.T; a.RT = L.RT; a.nd = L.nd;
+  a.ntot = 96 * L.nd;
+  a.natoms = (a.ntot + 63) / 64;
+  a.full_id = -1;
+  for (int i = 0; i < L.nd; ++i) {
+    a.rd[i] = L.rd[i];
+    if (L.rd[i] == L.D) a.full_id = i;
+  }
+  a.ws = ws; a.ub = L.unit_bytes; a.o_Vd = L.o_Vd; a.o_G16 = L.o_G16; a.o_status = L.o_status;
+  CUtensorMap tX, tU;
+  const cuuint64_t dX[3] = {128, (cuuint64_t)L.T, (cuuint64_t)U * L.H};
+  const cuuint64_t sX[2] = {256, (cuuint64_t)L.T * 256};
+  const cuuint32_t bX[3] = {64, CT_KT, 1};
+  if (!tc::make_map(&tX, X, 3, dX, sX, bX)) return JOLT_ERR_CUDA;
+  const cuuint64_t dU[3] = {CT_NMAX, (cuuint64_t)L.T, (cuuint64_t)U};
+  const cuuint64_t sU[2] = {CT_NMAX * 2, (cuuint64_t)L.unit_bytes};
+  const cuuint32_t bU[3] = {64, CT_KT, 1};
+  if (!tc::make_map(&tU, ws + L.o_Ub3, 3, dU, sU, bU)) return JOLT_ERR_CUDA;
+  const size_t smem = cores_smem(a.natoms, a.nd);
+  static bool attr = false;
+  if (!attr) {
+    JOLT_CUDA_TRY(cudaFuncSetAttribute(cores_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)cores_smem(CT_NMAX / 64, CT_NMAX / 96)));
+    attr = true;
+  }
+  cores_tc_kernel<<<dim3(L.H, U), CT_THREADS, smem, st>>>(tX, tU, a);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
 }
 
 }  // namespace jolt
