@@ -555,387 +555,6 @@ __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt
   }
 }
 
-// ---------------------------------------------------------------- sweep (TC)
-// The candidate sweep with the dense products on the tensor cores, for bf16
-// X with D = 128 and truncated ranks <= 32.  One CTA scores 128 tokens of one
-// head with two threads per token row, each owning one 64-column half (warps
-// w and w + 4 read the same TMEM lane quarter; the row maximum is exchanged
-// through shared memory between the pair):
-//   * QX = X (diag(sigma) H) by kind::f16 MMAs (bf16 X and the +-1 matrix are
-//     exact; fp32 accumulate) into TMEM columns [0, 128);
-//   * every reconstruction in the rotated domain, U_T W or Y16 (Q U_d)^T at a
-//     rank checkpoint r, as K[:, :r] B[:r, :] by kind::tf32 MMAs (K, fp16
-//     values, is exact in tf32; B split hi + lo) into TMEM columns [128, 256),
-//     recomputed from k = 0 for each checkpoint (columns r..8*ceil(r/8) of K
-//     zeroed meanwhile);
-//   * each thread then reads its half row y = QX / sqrt(D) - P back in
-//     16-column chunks and scores every b exactly as the SIMT sweep does (row
-//     max, fp16 scale, round-half-even by the magic constant, squared error).
-// The K and B operands are written by the threads in the 128-byte swizzled
-// K-major layout (16-byte unit u of row r at u ^ (r % 8)), X and the sign
-// matrix arrive by TMA in the same layout.
-constexpr int STC_ROWS = 128, STC_THREADS = 256;
-constexpr int STC_XBYTES = STC_ROWS * 256;       // 128 rows x 128 bf16
-constexpr int STC_KBYTES = STC_ROWS * 128;       // 128 rows x 32 fp32
-
-struct SweepTcArgs {
-  int H, T, nT, nd, nb, nTt, ndt, RT, RD, hasFullT, hasFullD;
-  int rT[JOLT_MAX_GRID], rd[JOLT_MAX_GRID], b[4];
-  float rq[4];
-  int ncand, tiles_t;
-  char* ws;
-  size_t ub, o_UT16, o_W, o_Y16, o_QUd, o_status;
-  float* part;
-  long long part_us;
-};
-
-__device__ __forceinline__ uint32_t sw128(int r, int byte) {
-  return (uint32_t)(r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
-}
-
-// 16 columns of this thread's TMEM lane into registers, without waiting.
-__device__ __forceinline__ void tmem_ld16_issue(uint32_t addr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(addr));
-}
-// Wait for this thread's TMEM loads, tied to the registers it makes valid
-// (so that no use of them can be scheduled before it).
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-               :
-               : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16], uint32_t (&q)[16]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(q[0]), "+r"(q[1]),
-                 "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7]),
-                 "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]), "+r"(q[12]), "+r"(q[13]),
-                 "+r"(q[14]), "+r"(q[15])
-               :
-               : "memory");
-}
-
-// One pass over this thread's 64-column half row (`trow` carries the half's
-// column offset), STC_CH columns at a time, with the loads of the next
-// STC_CH columns in flight while the current ones are used:
-// f(y0, y1) is called on consecutive pairs of y = QX rs - P (with_qx) or
-// y = P rs.
-constexpr int STC_CH = 16;
-template <typename F>
-__device__ __forceinline__ void stc_pass(uint32_t trow, bool with_qx, float rs, F&& f) {
-  const float2 rs2 = make_float2(rs, rs);
-  uint32_t pa[STC_CH], qa[STC_CH], pb[STC_CH], qb[STC_CH];
-  auto issue = [&](uint32_t addr, uint32_t (&r)[STC_CH]) { tmem_ld16_issue(addr, r); };
-  issue(trow + 128, pa);
-  if (with_qx) issue(trow, qa);
-  if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);
-  auto use = [&](const uint32_t (&p)[STC_CH], const uint32_t (&q)[STC_CH]) {
-#pragma unroll
-    for (int j = 0; j < STC_CH; j += 2) {
-      const float2 pp = make_float2(__uint_as_float(p[j]), __uint_as_float(p[j + 1]));
-      const float2 y = with_qx
-                           ? __ffma2_rn(make_float2(__uint_as_float(q[j]), __uint_as_float(q[j + 1])),
-                                        rs2, make_float2(-pp.x, -pp.y))
-                           : __fmul2_rn(pp, rs2);
-      f(y);
-    }
-  };
-#pragma unroll
-  for (int c = 0; c < 64; c += 2 * STC_CH) {
-    // columns c .. c + STC_CH - 1 are in (pa, qa); fetch the next STC_CH
-    // into (pb, qb)
-    issue(trow + 128 + c + STC_CH, pb);
-    if (with_qx) issue(trow + c + STC_CH, qb);
-    use(pa, qa);
-    if (with_qx) tmem_ld_wait(pb, qb); else tmem_ld_wait(pb);
-    if (c + 2 * STC_CH < 64) {
-      issue(trow + 128 + c + 2 * STC_CH, pa);
-      if (with_qx) issue(trow + c + 2 * STC_CH, qa);
-    }
-    use(pb, qb);
-    if (c + 2 * STC_CH < 64) {
-      if (with_qx) tmem_ld_wait(pa, qa); else tmem_ld_wait(pa);
-    }
-  }
-}
-
-// Score one candidate from TMEM: half row `trow` (this thread's lane
-// address and column offset); y = QX rs - P (with_qx) or y = P rs (the
-// whole-modes residual).  The two halves of a row meet on the row maximum
-// through rmax[half][lr] and a 64-thread named barrier of their warp pair;
-// the squared errors of the halves add in the cells.  The caller separates
-// consecutive calls by a CTA barrier (rmax is rewritten by the next call).
-__device__ __forceinline__ void stc_score(uint32_t trow, bool with_qx, float rs,
-                                          const SweepTcArgs& a, float* cells, int cell0,
-                                          float* rmax, int lr, int half, int pair) {
-  float m0 = 0.f, m1 = 0.f;
-  float2 e0 = make_float2(0.f, 0.f);
-  stc_pass(trow, with_qx, rs, [&](float2 y) {
-    m0 = fmaxf(m0, fabsf(y.x));
-    m1 = fmaxf(m1, fabsf(y.y));
-    e0 = __ffma2_rn(y, y, e0);
-  });
-  float m = fmaxf(m0, m1);
-  rmax[half * STC_ROWS + lr] = m;
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-  m = fmaxf(m, rmax[(half ^ 1) * STC_ROWS + lr]);
-  float s[4], inv[4];
-#pragma unroll
-  for (int ib = 0; ib < 4; ++ib) {
-    s[ib] = 0.f; inv[ib] = 0.f;
-    if (ib < a.nb && a.b[ib] > 0) {
-      s[ib] = round_f16(m * a.rq[ib]);
-      float r;
-      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s[ib]));
-      inv[ib] = s[ib] > 0.f ? r : 0.f;
-    }
-  }
-  const float2 M2 = make_float2(12582912.0f, 12582912.0f), nM2 = make_float2(-12582912.0f, -12582912.0f);
-  float2 eb[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  stc_pass(trow, with_qx, rs, [&](float2 y) {
-#pragma unroll
-    for (int ib = 0; ib < 4; ++ib) {
-      if (ib >= a.nb || a.b[ib] == 0) continue;
-      const float2 i2 = make_float2(inv[ib], inv[ib]), ns2 = make_float2(-s[ib], -s[ib]);
-      const float2 qq = __fadd2_rn(__ffma2_rn(y, i2, M2), nM2);
-      const float2 d = __ffma2_rn(ns2, qq, y);
-      eb[ib] = __ffma2_rn(d, d, eb[ib]);
-    }
-  });
-  float v[4];
-#pragma unroll
-  for (int ib = 0; ib < 4; ++ib) v[ib] = (ib < a.nb && a.b[ib] == 0) ? e0.x + e0.y : eb[ib].x + eb[ib].y;
-#pragma unroll
-  for (int ib = 0; ib < 4; ++ib)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v[ib] += __shfl_xor_sync(0xffffffffu, v[ib], o);
-  if ((threadIdx.x & 31) == 0)
-#pragma unroll
-    for (int ib = 0; ib < 4; ++ib)
-      if (ib < a.nb) atomicAdd(&cells[cell0 + ib], v[ib]);
-}
-
-__global__ void __launch_bounds__(STC_THREADS, 2)
-sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tHs,
-                SweepTcArgs a) {
-  extern __shared__ __align__(1024) unsigned char smraw[];
-  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-  unsigned char* sX = base;                       // X tile (2 chunks), later K operand
-  unsigned char* sH = base + STC_XBYTES;          // sign matrix (2 chunks), later B hi / lo
-  float* cells = (float*)(base + 2 * STC_XBYTES); // [ncand + 1]
-  struct Bars { uint64_t tma, mma; uint32_t tmem; int nz; };
-  Bars* S = (Bars*)(cells + 260);
-  float* rmax = cells + 260 + 16;                 // [2][128] half-row maxima
-  const int t = threadIdx.x, warp = t >> 5;
-  const int lr = t & (STC_ROWS - 1), half = t >> 7;  // token row, column half
-  const int tt = blockIdx.x, h = blockIdx.y, u = blockIdx.z;
-  const int t0 = tt * STC_ROWS, row = t0 + lr;
-  const bool in = row < a.T;
-  char* ub = a.ws + (size_t)u * a.ub;
-  for (int i = t; i <= a.ncand; i += STC_THREADS) cells[i] = 0.f;
-  if (t == 0) {
-    tc::mbar_init(tc::smem_u32(&S->tma), 1);
-    tc::mbar_init(tc::smem_u32(&S->mma), 1);
-    tc::fence_barrier_init();
-  }
-  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&S->tmem), 256);
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = S->tmem;
-  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 64 * half;
-  bool ok = true;
-  uint32_t mma_phase = 0;
-  auto mma_wait = [&]() {
-    if (!tc::mbar_wait(tc::smem_u32(&S->mma), mma_phase & 1)) ok = false;
-    ++mma_phase;
-    tc::tc_fence_after();
-  };
-  // ---- X and the sign matrix by TMA; QX = X Hs into TMEM [0, 128)
-  if (t == 0) {
-    const uint32_t fb = tc::smem_u32(&S->tma);
-    tc::mbar_expect_tx(fb, 2 * STC_XBYTES);
-    const int xr = u * a.H + h;
-    tc::tma_load_3d(tc::smem_u32(sX), &tX, 0, t0, xr, fb);
-    tc::tma_load_3d(tc::smem_u32(sX + STC_XBYTES / 2), &tX, 64, t0, xr, fb);
-    tc::tma_load_3d(tc::smem_u32(sH), &tHs, 0, 0, u, fb);
-    tc::tma_load_3d(tc::smem_u32(sH + STC_XBYTES / 2), &tHs, 64, 0, u, fb);
-  }
-  if (!tc::mbar_wait(tc::smem_u32(&S->tma), 0)) ok = false;
-  constexpr uint32_t idesc16 = tc::idesc_bf16(128, 128, 0, 0);
-  constexpr uint32_t idesc32 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(128 >> 3) << 17) |
-                               ((uint32_t)(128 >> 4) << 24);
-  auto mma_x = [&](uint32_t dcol) {   // D[dcol..] = sX sH^T over K = 128 (bf16)
-    if (t == 0) {
-      tc::tc_fence_after();
-#pragma unroll
-      for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sX + kc * (STC_XBYTES / 2)) + 32 * k, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sH + kc * (STC_XBYTES / 2)) + 32 * k, 16, 1024);
-          tc::mma_f16(tmem + dcol, ad, bd, idesc16, (kc | k) != 0);
-        }
-      tc::mma_commit(tc::smem_u32(&S->mma));
-    }
-  };
-  mma_x(0);
-  mma_wait();
-  // ---- ||x||^2 and the whole-modes residual x - fp16(x) (in place, bf16-exact)
-  const float rs = rsqrtf(128.f);
-  {
-    float xn = 0.f;
-    int nz = 0;
-#pragma unroll 4
-    for (int c = 0; c < 64; c += 8) {
-      unsigned char* p = sX + half * (STC_XBYTES / 2) + sw128(lr, c * 2);
-      uint4 v = *reinterpret_cast<uint4*>(p);
-      __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&v);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float x = __bfloat162float(e[i]);
-        xn = fmaf(x, x, xn);
-        const float r = x - round_f16(x);
-        nz |= (r != 0.f);
-        e[i] = __float2bfloat16_rn(r);
-      }
-      *reinterpret_cast<uint4*>(p) = v;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) xn += __shfl_xor_sync(0xffffffffu, xn, o);
-    if ((t & 31) == 0) atomicAdd(&cells[a.ncand], xn);
-    nz = __syncthreads_or(nz);
-    if (a.hasFullT && a.hasFullD && nz) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncthreads();
-      mma_x(128);
-      mma_wait();
-      stc_score(trow, false, rs, a, cells, ((a.nT - 1) * a.nd + (a.nd - 1)) * a.nb, rmax, lr,
-                half, warp & 3);
-    }
-  }
-  // ---- rank chains: P = K[:, :r] B[:r, :] for each checkpoint r
-  unsigned char* sK = sX;                 // 128 x 32 fp32
-  unsigned char* sBh = sH;                // 128 (n) x 32 fp32
-  unsigned char* sBl = sH + STC_KBYTES;
-  auto run_chain = [&](const __half* Kg, long long k_ld, int kn, const float* Bg, int nck,
-                       const int* ranks, int cellbase, int cellstride) {
-    tc::tc_fence_before();
-    __syncthreads();   // previous MMAs and TMEM reads done, operands free
-    // K rows (this thread's token row, columns 16 half .. 16 half + 15),
-    // fp16 -> fp32, zero past kn / T
-    const int k0 = 16 * half;
-    if (kn == 32 && (k_ld & 7) == 0) {
-      uint4 raw[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i)
-        raw[i] = in ? reinterpret_cast<const uint4*>(Kg + (long long)row * k_ld + k0)[i] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const __half* hv = reinterpret_cast<const __half*>(&raw[i]);
-        float4 v0, v1;
-        v0.x = __half2float(hv[0]); v0.y = __half2float(hv[1]); v0.z = __half2float(hv[2]); v0.w = __half2float(hv[3]);
-        v1.x = __half2float(hv[4]); v1.y = __half2float(hv[5]); v1.z = __half2float(hv[6]); v1.w = __half2float(hv[7]);
-        *reinterpret_cast<float4*>(sK + sw128(lr, (k0 + 8 * i) * 4)) = v0;
-        *reinterpret_cast<float4*>(sK + sw128(lr, (k0 + 8 * i + 4) * 4)) = v1;
-      }
-    } else {
-      for (int k = k0; k < k0 + 16; k += 4) {
-        float4 v;
-        float* pv = reinterpret_cast<float*>(&v);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          pv[i] = (in && k + i < kn) ? __half2float(Kg[(long long)row * k_ld + k + i]) : 0.f;
-        *reinterpret_cast<float4*>(sK + sw128(lr, k * 4)) = v;
-      }
-    }
-    // B^T rows: n = lr, B^T[n][k] = B[k][n] for this half's k, split hi + lo
-    for (int k = k0; k < k0 + 16; k += 4) {
-      float4 hi, lo;
-      float* ph = reinterpret_cast<float*>(&hi);
-      float* pl = reinterpret_cast<float*>(&lo);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float b = (k + i < kn) ? Bg[(long long)(k + i) * 128 + lr] : 0.f;
-        const float bh = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
-        ph[i] = bh;
-        pl[i] = b - bh;
-      }
-      *reinterpret_cast<float4*>(sBh + sw128(lr, k * 4)) = hi;
-      *reinterpret_cast<float4*>(sBl + sw128(lr, k * 4)) = lo;
-    }
-    for (int ci = 0; ci < nck; ++ci) {
-      const int r = ranks[ci];
-      const int ks = (r + 7) >> 3;
-      // zero K columns r .. 8 ks - 1 of this row for this checkpoint (each
-      // half its own columns)
-      float saved[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = r + i;
-        saved[i] = 0.f;
-        if (k < 8 * ks && (k >> 4) == half) {
-          float* p = reinterpret_cast<float*>(sK + sw128(lr, k * 4));
-          saved[i] = *p;
-          *p = 0.f;
-        }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tc::tc_fence_before();
-      __syncthreads();
-      if (t == 0) {
-        tc::tc_fence_after();
-        for (int k = 0; k < ks; ++k) {
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sK) + 32 * k, 16, 1024);
-          const uint64_t bh = tc::sdesc_sw128(tc::smem_u32(sBh) + 32 * k, 16, 1024);
-          const uint64_t bl = tc::sdesc_sw128(tc::smem_u32(sBl) + 32 * k, 16, 1024);
-          tc::mma_tf32(tmem + 128, ad, bh, idesc32, k != 0);
-          tc::mma_tf32(tmem + 128, ad, bl, idesc32, 1);
-        }
-        tc::mma_commit(tc::smem_u32(&S->mma));
-      }
-      mma_wait();
-      stc_score(trow, true, rs, a, cells, cellbase + ci * cellstride, rmax, lr, half, warp & 3);
-      // restore the zeroed columns for the next checkpoint
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int k = r + i;
-        if (k < 8 * ks && (k >> 4) == half) *reinterpret_cast<float*>(sK + sw128(lr, k * 4)) = saved[i];
-      }
-      tc::tc_fence_before();
-      __syncthreads();
-    }
-  };
-  if (a.hasFullT && a.ndt > 0) {
-    const __half* Yh = (const __half*)(ub + a.o_Y16) + (long long)h * a.T * a.RD;
-    run_chain(Yh, a.RD, a.RD, (const float*)(ub + a.o_QUd), a.ndt, a.rd,
-              ((a.nT - 1) * a.nd) * a.nb, a.nb);
-  }
-  if (a.nTt > 0) {
-    for (int id = 0; id < a.nd; ++id) {
-      const __half* Ug = (const __half*)(ub + a.o_UT16) + (long long)id * a.T * a.RT;
-      const float* Wg = (const float*)(ub + a.o_W) + ((long long)id * a.H + h) * a.RT * 128;
-      run_chain(Ug, a.RT, a.RT, Wg, a.nTt, a.rT, id * a.nb, a.nd * a.nb);
-    }
-  }
-  if (!ok) atomicOr((int*)(ub + a.o_status), ST_TIMEOUT);
-  tc::tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
-  float* part = a.part + u * a.part_us + ((long long)h * a.tiles_t + tt) * (a.ncand + 1);
-  for (int i = t; i <= a.ncand; i += STC_THREADS) part[i] = cells[i];
-}
-
 size_t tc_smem(int stage_bytes) { return (size_t)STAGES * stage_bytes + 1024 + sizeof(Smem) + 64; }
 
 }  // namespace
@@ -1108,58 +727,5 @@ jolt_status ygram_tc(const Layout& L, int U, const char* ws, char* pbase, size_t
   return JOLT_OK;
 }
 
-// ---- tensor-core sweep
-bool sweep_tc_supported(const Layout& L) {
-  if (!(L.dtype == JOLT_BF16 && L.D == 128 && L.RT <= 32 && L.RD <= 32 && L.o_Hs != 0 &&
-        encode_fn() != nullptr && L.ncand + 1 <= 260 && L.nb <= 4))
-    return false;
-  return true;
-}
-
-jolt_status sweep_tc_run(const Layout& L, int U, const void* X, char* ws, float* part,
-                         long long part_us, int* tiles_t_out, cudaStream_t st) {
-  CUtensorMap tX;
-  const cuuint64_t dX[3] = {128, (cuuint64_t)L.T, (cuuint64_t)U * L.H};
-  const cuuint64_t sX[2] = {256, (cuuint64_t)L.T * 256};
-  const cuuint32_t bX[3] = {64, 128, 1};
-  if (!make_map(&tX, X, 3, dX, sX, bX)) return JOLT_ERR_CUDA;
-  // the sign matrices sit one per unit region: a 3-D map (128 cols, 128 rows, unit)
-  CUtensorMap tH3;
-  const cuuint64_t dH3[3] = {128, 128, (cuuint64_t)U};
-  const cuuint64_t sH3[2] = {256, (cuuint64_t)L.unit_bytes};
-  const cuuint32_t bH3[3] = {64, 128, 1};
-  if (!make_map(&tH3, ws + L.o_Hs, 3, dH3, sH3, bH3)) return JOLT_ERR_CUDA;
-  SweepTcArgs a;
-  memset(&a, 0, sizeof(a));
-  a.H = L.H; a.T = L.T; a.nT = L.nT; a.nd = L.nd; a.nb = L.nb; a.nTt = L.nTt; a.ndt = L.ndt;
-  a.RT = L.RT; a.RD = L.RD; a.hasFullT = L.hasFullT; a.hasFullD = L.hasFullD;
-  for (int i = 0; i < JOLT_MAX_GRID; ++i) {
-    a.rT[i] = i < L.nTt ? L.rT[i] : -1;
-    a.rd[i] = i < L.ndt ? L.rd[i] : -1;
-  }
-  for (int i = 0; i < 4; ++i) {
-    a.b[i] = L.b[i];
-    a.rq[i] = L.b[i] > 0 ? 1.f / (float)((1 << (L.b[i] - 1)) - 1) : 0.f;
-  }
-  a.ncand = L.ncand;
-  a.tiles_t = (L.T + STC_ROWS - 1) / STC_ROWS;
-  a.ws = ws; a.ub = L.unit_bytes;
-  a.o_UT16 = L.o_UT16; a.o_W = L.o_W; a.o_Y16 = L.o_Y16; a.o_QUd = L.o_QUd; a.o_status = L.o_status;
-  a.part = part; a.part_us = part_us;
-  // cells (260 floats), barriers (64 bytes), row maxima (256 floats), and
-  // the 1024-byte alignment slack; 2 CTAs per SM by TMEM (256 columns each)
-  const size_t smem = 2 * STC_XBYTES + 260 * 4 + 64 + 2 * STC_ROWS * 4 + 1024;
-  static bool attr = false;
-  if (!attr) {
-    JOLT_CUDA_TRY(cudaFuncSetAttribute(sweep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem));
-    attr = true;
-  }
-  dim3 grid(a.tiles_t, L.H, U);
-  sweep_tc_kernel<<<grid, STC_THREADS, smem, st>>>(tX, tH3, a);
-  JOLT_LAUNCH_CHECK();
-  *tiles_t_out = a.tiles_t;
-  return JOLT_OK;
-}
 
 }  // namespace jolt
