@@ -121,10 +121,104 @@ struct EncBatch {
   EncArgs u[ENC_MAX_UNITS];
 };
 
+// The block scale and codes of one rotated residual row from its exact
+// value: the residual of the row in double-float (the chain products are
+// exact or TwoProduct-split), rotated by a double-float Walsh-Hadamard
+// transform, and every decision taken on the double-float y, so that it
+// agrees with a correctly rounded evaluation except within ~2^-44 |y| of a
+// boundary.  x: this lane's EPT inputs of the row (x - fp16(x) for the
+// whole modes); the chain coefficients of the row are Ks[k * CD_TILE + rr].
+template <int EPT>
+__device__ __forceinline__ void exact_row(const EncArgs& a, const float (&x)[EPT], const float* Ks,
+                                          int rr, const float* Bsh, const float* Bsl,
+                                          const float (&sg)[EPT], float qmax, int lane,
+                                          float (&q)[EPT], float& s_out) {
+  constexpr int D = 32 * EPT;
+  float yh[EPT], yl[EPT];
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    yh[e] = x[e];
+    yl[e] = 0.f;
+  }
+  if (a.mode != 2) {
+    for (int k = 0; k < a.K; ++k) {
+      const float c = Ks[k * CD_TILE + rr];
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const float bh = Bsh[k * D + lane * EPT + e], bl = Bsl[k * D + lane * EPT + e];
+        const float p = c * bh;
+        const float pe = fmaf(c, bh, -p);  // c bh = p + pe exactly
+        float sm, es;
+        two_sum(yh[e], -p, sm, es);
+        yh[e] = sm;
+        yl[e] = fmaf(-c, bl, yl[e] + (es - pe));
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    yh[e] *= sg[e];
+    yl[e] *= sg[e];
+  }
+  fwht_row_df<EPT>(yh, yl, lane);
+  // times 1/sqrt(D), renormalised so that yh is the fp32 rounding of y
+  float mh = 0.f, ml = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    const float p = yh[e] * a.rs_hi;
+    const float l = fmaf(yh[e], a.rs_hi, -p) + fmaf(yh[e], a.rs_lo, yl[e] * a.rs_hi);
+    yh[e] = p + l;
+    yl[e] = l - (yh[e] - p);
+    const float ay = fabsf(yh[e]), aly = yh[e] < 0.f ? -yl[e] : yl[e];
+    if (ay > mh || (ay == mh && aly > ml)) { mh = ay; ml = aly; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, mh, o);
+    const float ol = __shfl_xor_sync(0xffffffffu, ml, o);
+    if (oh > mh || (oh == mh && ol > ml)) { mh = oh; ml = ol; }
+  }
+  // s = fp16(max|y| / qmax) from the double-float max
+  const float z0 = __fdiv_rn(mh, qmax);
+  const float z1 = __fdiv_rn(fmaf(-z0, qmax, mh) + ml, qmax);
+  const float zh = z0 + z1;  // renormalised: zh is the fp32 rounding of the quotient
+  const float s = round_f16_df(zh, z1 - (zh - z0));
+#pragma unroll
+  for (int e = 0; e < EPT; ++e) {
+    float qq = 0.f;
+    if (s > 0.f) {
+      qq = rintf(__fdiv_rn(yh[e], s));
+      // the boundaries (q +- 1/2) s are exact in fp32; their side is the
+      // sign of y - (q +- 1/2) s, taken on the double-float y
+      const float up = fmaf(-(qq + 0.5f), s, yh[e]) + yl[e];
+      const float dn = fmaf(-(qq - 0.5f), s, yh[e]) + yl[e];
+      if (up > 0.f || (up == 0.f && fmodf(qq, 2.f) != 0.f)) qq += 1.f;
+      else if (dn < 0.f || (dn == 0.f && fmodf(qq, 2.f) != 0.f)) qq -= 1.f;
+    }
+    q[e] = qq;
+  }
+  s_out = s;
+}
+
+// Codes of one tile of rows (64 tokens of one head; a warp holds 8 rows, a
+// lane EPT elements of each).
+// ["Rotated Tucker residual for outlier-resistant KV quantization",
+//  Formulas: Y = Q R, s = max|y| / (2^(b-1) - 1) in fp16, codes = round(y / s)
+//  clipped to the b-bit range.]
+// Each row is first formed in fp32 with an a-posteriori bound on its
+// rounding error: the chain R = X - K B by fused multiply-adds (each rounding
+// at most u |partial residual|, u = 2^-24, the partials' magnitudes summed
+// per element), the Walsh-Hadamard transform (at most 8 u ||v||_1 / sqrt(D)
+// for its seven levels and the scaling).  Where the bound proves that the
+// fp32 row decides the fp16 scale and every code the same way as the exact
+// value, those decisions are taken; any other row (a value within the bound
+// of a rounding boundary) is recomputed by exact_row.  The codes are
+// therefore those of the exact evaluation.
 template <typename TX, int EPT>
 __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __grid_constant__ EncBatch eb) {
   const EncArgs& a = eb.u[blockIdx.z];
   constexpr int D = 32 * EPT;
+  constexpr float U = 5.9604645e-08f;          // 2^-24
   extern __shared__ __align__(16) float dsm[];
   float* Ks = dsm;                       // [64][CD_TILE]
   float* Bsh = Ks + 64 * CD_TILE;        // [64][D]
@@ -133,17 +227,18 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
   const int h = blockIdx.y, t0 = blockIdx.x * CD_TILE;
   const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
   const TX* Xh = (const TX*)a.X + (long long)h * a.T * D;
-  float ah[CD_ROWS][EPT], al[CD_ROWS][EPT];
+  float rv[CD_ROWS][EPT], sv[CD_ROWS][EPT];   // fp32 residuals, sums of |partial residuals|
 #pragma unroll
   for (int r = 0; r < CD_ROWS; ++r) {
     const int t = t0 + w * CD_ROWS + r;
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
       const float x = (t < a.T) ? to_f32(Xh[(long long)t * D + lane * EPT + e]) : 0.f;
-      ah[r][e] = a.mode == 2 ? x - round_f16(x) : x;  // exact
-      al[r][e] = 0.f;
+      rv[r][e] = a.mode == 2 ? x - round_f16(x) : x;  // exact
+      sv[r][e] = 0.f;
     }
   }
+  const bool lo_part = (a.mode != 2 && a.K > 0 && a.B16 == nullptr);
   if (a.mode != 2 && a.K > 0) {
     for (int i = threadIdx.x; i < CD_TILE * a.K; i += CD_THREADS) {
       const int row = i / a.K, k = i % a.K;
@@ -179,12 +274,13 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
         const float c = kk[r];
 #pragma unroll
         for (int e = 0; e < EPT; ++e) {
-          const float p = c * bh[e];
-          const float pe = fmaf(c, bh[e], -p);  // c bh = p + pe exactly
-          float s, es;
-          two_sum(ah[r][e], -p, s, es);
-          ah[r][e] = s;
-          al[r][e] = fmaf(-c, bl[e], al[r][e] + (es - pe));
+          float v = fmaf(-c, bh[e], rv[r][e]);
+          if (lo_part) {
+            sv[r][e] += fabsf(v);
+            v = fmaf(-c, bl[e], v);
+          }
+          rv[r][e] = v;
+          sv[r][e] += fabsf(v);
         }
       }
     }
@@ -196,58 +292,87 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
   const float qmax = (float)((1 << (b - 1)) - 1);
   const int qoff = 1 << (b - 1);
   const int nbytes = D * b / 8;
+  const float rs = a.rs_hi;
   // one row at a time, not unrolled (the row's values are picked out of the
   // register arrays by static selects, which keeps the code small)
 #pragma unroll 1
   for (int r = 0; r < CD_ROWS; ++r) {
     const int t = t0 + w * CD_ROWS + r;
-    float yh[EPT], yl[EPT];
+    float y[EPT], l1s = 0.f, l1v = 0.f;
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
-      float vh = ah[0][e], vl = al[0][e];
+      float vh = rv[0][e], vs = sv[0][e];
 #pragma unroll
       for (int rr = 1; rr < CD_ROWS; ++rr)
-        if (rr == r) { vh = ah[rr][e]; vl = al[rr][e]; }
-      yh[e] = vh * sg[e];
-      yl[e] = vl * sg[e];
+        if (rr == r) { vh = rv[rr][e]; vs = sv[rr][e]; }
+      y[e] = vh * sg[e];
+      l1v += fabsf(vh);
+      l1s += vs;
     }
-    fwht_row_df<EPT>(yh, yl, lane);
-    // times 1/sqrt(D), renormalised so that yh is the fp32 rounding of y
-    float mh = 0.f, ml = 0.f;
+    fwht_row<EPT>(y, lane);
+    float m = 0.f;
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
-      const float p = yh[e] * a.rs_hi;
-      const float l = fmaf(yh[e], a.rs_hi, -p) + fmaf(yh[e], a.rs_lo, yl[e] * a.rs_hi);
-      yh[e] = p + l;
-      yl[e] = l - (yh[e] - p);
-      const float ay = fabsf(yh[e]), aly = yh[e] < 0.f ? -yl[e] : yl[e];
-      if (ay > mh || (ay == mh && aly > ml)) { mh = ay; ml = aly; }
+      y[e] *= rs;
+      m = fmaxf(m, fabsf(y[e]));
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float oh = __shfl_xor_sync(0xffffffffu, mh, o);
-      const float ol = __shfl_xor_sync(0xffffffffu, ml, o);
-      if (oh > mh || (oh == mh && ol > ml)) { mh = oh; ml = ol; }
+    m = warp_max(m);
+    l1s = warp_sum(l1s);
+    l1v = warp_sum(l1v);
+    // bound on |y - exact y| for every element of the row: the chain's
+    // roundings (l1s u), the transform's seven levels and the scaling
+    // (8 u l1v), over sqrt(D); each element adds 2 u |y| (the product by the
+    // fp32 1/sqrt(D) and its rounding).  The sums themselves are rounded:
+    // 1% of slack covers them.
+    const float E = 1.01f * U * (l1s + 8.f * l1v) * rs;
+    const float Em = E + 2.f * U * m;
+    // the scale: certain when no fp16 rounding boundary lies within the
+    // bound of max|y| / qmax
+    bool sure = true;
+    float s = 0.f;
+    {
+      const float z = __fdiv_rn(m, qmax);
+      const float dz = 1.01f * (Em / qmax + U * z);
+      const __half hz = __float2half_rn(z);
+      const float hf = __half2float(hz);
+      const unsigned short hb = __half_as_ushort(hz);
+      // neighbours of hz among the fp16 values (z >= 0)
+      const float up = __half2float(__ushort_as_half((unsigned short)(hb + 1)));
+      const float dn = hb > 0 ? __half2float(__ushort_as_half((unsigned short)(hb - 1))) : -hf;
+      const float mid_hi = 0.5f * (hf + up), mid_lo = 0.5f * (hf + dn);
+      if (!(z - dz > mid_lo && z + dz < mid_hi)) sure = false;
+      if (m == 0.f && E > 0.f) sure = false;
+      s = hf;
     }
-    // s = fp16(max|y| / qmax) from the double-float max
-    const float z0 = __fdiv_rn(mh, qmax);
-    const float z1 = __fdiv_rn(fmaf(-z0, qmax, mh) + ml, qmax);
-    const float zh = z0 + z1;  // renormalised: zh is the fp32 rounding of the quotient
-    const float s = round_f16_df(zh, z1 - (zh - z0));
+    float q[EPT];
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
-      float q = 0.f;
+      float qq = 0.f;
       if (s > 0.f) {
-        q = rintf(__fdiv_rn(yh[e], s));
-        // the boundaries (q +- 1/2) s are exact in fp32; their side is the
-        // sign of y - (q +- 1/2) s, taken on the double-float y
-        const float up = fmaf(-(q + 0.5f), s, yh[e]) + yl[e];
-        const float dn = fmaf(-(q - 0.5f), s, yh[e]) + yl[e];
-        if (up > 0.f || (up == 0.f && fmodf(q, 2.f) != 0.f)) q += 1.f;
-        else if (dn < 0.f || (dn == 0.f && fmodf(q, 2.f) != 0.f)) q -= 1.f;
+        qq = rintf(__fdiv_rn(y[e], s));
+        // the exact y must lie strictly between (q - 1/2) s and (q + 1/2) s
+        const float Ee = 1.01f * (E + 2.f * U * fabsf(y[e]));
+        const float up = fmaf(-(qq + 0.5f), s, y[e]);
+        const float dn = fmaf(-(qq - 0.5f), s, y[e]);
+        if (!(up + Ee + U * fabsf(up) < 0.f && dn - Ee - U * fabsf(dn) > 0.f)) sure = false;
       }
-      q = fminf(fmaxf(q, -(float)qoff), (float)(qoff - 1));
-      codes[w][lane * EPT + e] = (unsigned char)((int)q + qoff);
+      q[e] = qq;
+    }
+    if (__any_sync(0xffffffffu, !sure)) {
+      // recompute the row from its exact value
+      float xr[EPT];
+      const bool okr = t < a.T;
+#pragma unroll
+      for (int e = 0; e < EPT; ++e) {
+        const float x = okr ? to_f32(Xh[(long long)t * D + lane * EPT + e]) : 0.f;
+        xr[e] = a.mode == 2 ? x - round_f16(x) : x;
+      }
+      exact_row<EPT>(a, xr, Ks, w * CD_ROWS + r, Bsh, Bsl, sg, qmax, lane, q, s);
+    }
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+      const float qq = fminf(fmaxf(q[e], -(float)qoff), (float)(qoff - 1));
+      codes[w][lane * EPT + e] = (unsigned char)((int)qq + qoff);
     }
     __syncwarp();
     if (t < a.T) {

@@ -75,7 +75,7 @@ struct Job {
 };
 
 struct Smem {
-  uint64_t hs, tma[2], mma[2][2];
+  uint64_t hs, tma[2], mma[2][2], ops[2];
   uint32_t tmem;
   int njobs;
   Job job[STC_MAX_JOBS];
@@ -84,19 +84,6 @@ struct Smem {
 // Byte offset of (row r, byte b) in a K-major operand with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw128(int r, int byte) {
   return (uint32_t)(r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
-}
-
-// Barrier of one group's 256 threads (named barrier `id`); returns whether
-// any of them passed v = true.
-__device__ __forceinline__ bool group_sync_or(int id, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 256, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id)
-      : "memory");
-  return r != 0;
 }
 
 // 16 fp32 columns of this thread's TMEM lane into registers, not waited for.
@@ -262,6 +249,7 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
       tc::mbar_init(tc::smem_u32(&S->tma[i]), 1);
       tc::mbar_init(tc::smem_u32(&S->mma[i][0]), 1);
       tc::mbar_init(tc::smem_u32(&S->mma[i][1]), 1);
+      tc::mbar_init(tc::smem_u32(&S->ops[i]), 8);
     }
     tc::fence_barrier_init();
   }
@@ -302,6 +290,7 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
   // jobs of this group issued / waited for, counted over the whole kernel:
   // job n uses accumulator n & 1, and is phase n >> 1 of that buffer's barrier
   uint32_t jobs_issued = 0, jobs_waited = 0;
+  uint32_t ops_phase = 0;
   int loaded_unit = -1, fail_unit = 0;
   // this group's tile of pair p (unit, head, token tile), or false
   auto tile_of = [&](int p, int& u, int& h, int& tt) {
@@ -491,11 +480,25 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
     };
     auto wait_mma = [&]() {
       const int buf = (int)(jobs_waited & 1);
-      if (!tc::mbar_wait(tc::smem_u32(&S->mma[g][buf]), (jobs_waited >> 1) & 1)) ok = false;
+      if (!tc::mbar_wait(tc::smem_u32(&S->mma[g][buf]), (jobs_waited >> 1) & 1,
+                         ok ? tc::WAIT_LIMIT : 1024))
+        ok = false;
       ++jobs_waited;
       tc::tc_fence_after();
     };
 
+    // every warp of the group has written its share of the next job's
+    // operands (and is done with the accumulator that job overwrites): one
+    // arrival per warp; the leader, which issues the job, waits for all eight
+    auto ops_ready = [&]() {
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&S->ops[g]))
+                     : "memory");
+      if (leader && !tc::mbar_wait(tc::smem_u32(&S->ops[g]), ops_phase & 1, ok ? tc::WAIT_LIMIT : 1024))
+        ok = false;
+      ++ops_phase;
+    };
     // ---- job 0
     Pre pre;
     {
@@ -509,7 +512,7 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc::tc_fence_before();
-      if (group_sync_or(gbar, !ok)) { stop = true; continue; }
+      ops_ready();
       issue_mma(j0);
     }
     for (int j = 0; j < J; ++j) {
@@ -531,7 +534,7 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc::tc_fence_before();
-        if (group_sync_or(gbar, !ok)) { stop = true; break; }
+        ops_ready();
         issue_mma(jn);
       } else if (p + (int)gridDim.x < a.npairs) {
         // every product of this tile is done: the next X may land
@@ -557,7 +560,6 @@ sweep_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
         if (iq1 >= 0) atomicAdd(&cells[jb.cell + iq1], vq[1]);
       }
     }
-    if (stop) continue;
     // ---- the tile's partials
     asm volatile("bar.sync %0, 256;" ::"r"(gbar) : "memory");
     float* part = a.part + u * a.part_us + ((long long)h * a.tiles_t + tt) * (a.ncand + 1);

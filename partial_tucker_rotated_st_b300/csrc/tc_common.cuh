@@ -40,9 +40,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < WAIT_LIMIT; ++i) {
+// Bounded wait for the phase with the given parity to complete (at most
+// `limit` polls).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit = WAIT_LIMIT) {
+  for (int i = 0; i < limit; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
