@@ -436,6 +436,54 @@ def timed_steps(run, steps, warmup, flush, st, clk=None):
             "launches": int(launches), "desc": desc}
 
 
+def factor_record(run, steps, flush, st, pk):
+    """The factor step alone with its stage-boundary events: the feature
+    stage (side stream), the whole-feature token solve (caller's stream),
+    the truncated token solves after the join, the cores; its dense
+    contractions' algorithmic flops against the sustained bf16 tensor peak
+    (the step is a chain of small latency-bound solves, so the fraction is
+    small by construction)."""
+    import torch
+    from partial_tucker_rotated_st_b300 import jolt as J
+    w, enc = run.w, run.enc
+    acc = {k: 0.0 for k in ("feature", "full_token_solve", "truncated_solves", "cores", "total")}
+    for i in range(steps + 2):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for e in ev:
+            e.record(st)
+        J.jolt_set_factor_events(ev)
+        enc.factor(run.X, run.K)
+        J.jolt_set_factor_events()
+        torch.cuda.synchronize()
+        flush.fill_(1)
+        if i < 2:
+            continue
+        acc["feature"] += ev[0].elapsed_time(ev[1])
+        acc["full_token_solve"] += ev[0].elapsed_time(ev[2])
+        acc["truncated_solves"] += min(ev[1].elapsed_time(ev[3]), ev[2].elapsed_time(ev[3]))
+        acc["cores"] += ev[3].elapsed_time(ev[4])
+        acc["total"] += ev[0].elapsed_time(ev[4])
+    ms = {k: v / steps for k, v in acc.items()}
+    H, T, D, U = w.H, w.T, w.D, w.n_units
+    RT = max(r for r in w.rT if r != kvgen.FULL)
+    RD = max(r for r in w.rd if r != kvgen.FULL)
+    N = H * T * D
+    flops_unit = (2 * N * D                       # feature Gram
+                  + 2 * N * RD                    # projection Y = X U_d
+                  + 2 * T * T * H * RD            # truncated token Grams (prefix slabs)
+                  + 2 * N * RT * len(w.rd))       # cores Z = X_h^T U_T of every rank
+    if w.token_mode == "exact":
+        flops_unit += 2 * T * T * H * D           # whole-feature token Gram
+    flops = flops_unit * U
+    peak = pk.get("bf16_tflops_sustained", 1400.0)
+    crit = "feature" if ms["feature"] >= ms["full_token_solve"] else "full_token_solve"
+    return {"stages_ms": ms, "critical_path": [crit, "truncated_solves", "cores"],
+            "dense_flops": int(flops),
+            "dense_tflops_achieved": flops / (ms["total"] / 1e3) / 1e12,
+            "peak_tflops": peak, "peak_kind": "measured bf16 sustained",
+            "frac": flops / (ms["total"] / 1e3) / 1e12 / peak}
+
+
 def blob_bytes_of(desc):
     return sum(int(d.bytes) for d in desc)
 
@@ -520,6 +568,7 @@ def run_ours(args):
            "h2d_bytes_per_step": int(run.Xh.numel() * run.Xh.element_size() + run.Sh.numel()),
            "d2h_bytes_per_step": int(d2h)}
 
+    fac = factor_record(run, args.steps, flush, st, pk)
     attn = attention_bench(args, w, r.desc, enc, flush, st, hbm, kind)
     adm = admission_bench(args, w, r.desc, enc, flush, st)
     modeled = modeled_allocator(args, w, enc, run.X, run.K, run.S, w.budget_bytes, run.in_bytes,
@@ -541,6 +590,7 @@ def run_ours(args):
                        "roofline": decode_roofline(w, desc, dec_t, hbm, args.workload)},
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "dominant_stage": dom,
+            "factor": fac,
             "wall_ms_per_step": 1e3 * res["wall_s"],
             "roofline": roof,
             "e2e": e2e,

@@ -213,6 +213,23 @@ jolt_status jolt_allocate_uniform(int n_units, int n_cand, const double* dist,
 jolt_status jolt_set_sweep_events(void* start, void* stop);
 
 /*
+ * Measurement hook for the factor step: when `events` is non-NULL it points
+ * to five CUDA events (cudaEvent_t created with timing enabled, owned by the
+ * caller) that every later jolt_factor_group call records at its stage
+ * boundaries:
+ *   [0] the start of the call (caller's stream);
+ *   [1] the feature stage done: feature Gram, eigen-solve, projection Y and
+ *       the truncated ranks' token Grams (the library's side stream);
+ *   [2] the whole-feature token-mode solve done (caller's stream; recorded
+ *       as [0] when there is no such solve);
+ *   [3] every token-mode solve done, after the two streams joined;
+ *   [4] the cores and fp16 factors done (the end of the call's work).
+ * The critical path is max([1], [2]) - [0], then [3], then [4].  NULL turns it
+ * off.  Process-wide setting, not thread-safe.
+ */
+jolt_status jolt_set_factor_events(void* const* events);
+
+/*
  * Modeled-error distortion table, an alternative to jolt_sweep_candidates
  * that needs no pass over X ["A JoLT for the KV cache" verdict page, referee
  * report on Section 4, Eq. (2): e ~ eps^2(b) tau; P5 Methodology 4: tail-mass

@@ -243,6 +243,11 @@ jolt_status jolt_set_sweep_events(void* start, void* stop) {
   return JOLT_OK;
 }
 
+jolt_status jolt_set_factor_events(void* const* events) {
+  for (int i = 0; i < 5; ++i) g_factor_ev[i] = events ? events[i] : nullptr;
+  return JOLT_OK;
+}
+
 jolt_status jolt_model_candidates(const jolt_config* cfg, int n_units, const void* ws,
                                   size_t ws_bytes, const double* eps2_host, double* dist,
                                   void* stream) {

@@ -30,6 +30,8 @@
 
 namespace jolt {
 
+void* g_factor_ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+
 namespace {
 
 constexpr int SUB_STEPS = 5;        // power steps between Rayleigh-Ritz checks
@@ -438,33 +440,44 @@ unsigned blocks_for(long long n, int tpb = 256) { return (unsigned)((n + tpb - 1
 // alongside the whole-feature token problem (it needs only X).  Callers that
 // share it serialise their feature stages on it; each joins through its own
 // events.
-jolt_status aux_stream(cudaStream_t* out) {
+//
+// The whole-feature token solve, a chain of small latency-bound launches, runs
+// on a second side stream of the highest priority, so that its blocks are
+// scheduled ahead of the feature stage's wide launches.
+jolt_status aux_stream(cudaStream_t* out, bool high = false) {
   static std::mutex mu;
-  static cudaStream_t streams[64] = {};
+  static cudaStream_t streams[2][64] = {};
   int dev = 0;
   JOLT_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return JOLT_ERR_CUDA;
   std::lock_guard<std::mutex> lk(mu);
-  if (!streams[dev]) JOLT_CUDA_TRY(cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking));
-  *out = streams[dev];
+  cudaStream_t& s = streams[high ? 1 : 0][dev];
+  if (!s) {
+    int least = 0, greatest = 0;
+    JOLT_CUDA_TRY(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+    JOLT_CUDA_TRY(cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, high ? greatest : least));
+  }
+  *out = s;
   return JOLT_OK;
 }
 
 struct EventPair {
-  cudaEvent_t a = nullptr, b = nullptr;
+  cudaEvent_t a = nullptr, b = nullptr, c = nullptr;
   ~EventPair() {
     if (a) cudaEventDestroy(a);
     if (b) cudaEventDestroy(b);
+    if (c) cudaEventDestroy(c);
   }
 };
 
 // On every exit (errors included) the caller's stream waits for all the
-// side-stream work, so that the workspace is never released under it.
+// side streams' work, so that the workspace is never released under it.
 struct JoinGuard {
-  cudaStream_t st = nullptr, fs = nullptr;
-  cudaEvent_t ev = nullptr;
+  cudaStream_t st = nullptr, fs = nullptr, ps = nullptr;
+  cudaEvent_t ev = nullptr, ev2 = nullptr;
   ~JoinGuard() {
     if (ev && fs && fs != st && cudaEventRecord(ev, fs) == cudaSuccess) cudaStreamWaitEvent(st, ev, 0);
+    if (ev2 && ps && ps != st && cudaEventRecord(ev2, ps) == cudaSuccess) cudaStreamWaitEvent(st, ev2, 0);
   }
 };
 
@@ -626,24 +639,41 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   const long long xu = (long long)H * T * D;
   int* status = (int*)(ws + L.o_status);
 
+  // measurement hook: stage-boundary events (see jolt_set_factor_events)
+  auto mark = [&](int i, cudaStream_t s) -> jolt_status {
+    if (g_factor_ev[i]) JOLT_CUDA_TRY(cudaEventRecord((cudaEvent_t)g_factor_ev[i], s));
+    return JOLT_OK;
+  };
+  TRY(mark(0, st));
   set_int_kernel<<<U, 32, 0, st>>>(ws, ub, L.o_status, 0);
   JOLT_LAUNCH_CHECK();
+  if (RT > 0) {
+    // the token problems' status words, before any stream forks off
+    set_int_kernel<<<U * L.nprob, 32, 0, st>>>(ws + (size_t)U * ub, L.prob_bytes, L.p_status, 0);
+    JOLT_LAUNCH_CHECK();
+  }
 
   const bool tc = gram_tc_supported(L);
   // The whole-feature token problem (r_d = D) reads only X: the feature
   // stage runs beside it on a side stream and the truncated ranks join it.
   const bool overlap = RT > 0 && L.hasFullD && RD > 0;
-  cudaStream_t fs = st;
+  cudaStream_t fs = st, ps = st;
   EventPair ev;
   if (overlap) {
     TRY(aux_stream(&fs));
+    TRY(aux_stream(&ps, true));
     JOLT_CUDA_TRY(cudaEventCreateWithFlags(&ev.a, cudaEventDisableTiming));
     JOLT_CUDA_TRY(cudaEventCreateWithFlags(&ev.b, cudaEventDisableTiming));
+    JOLT_CUDA_TRY(cudaEventCreateWithFlags(&ev.c, cudaEventDisableTiming));
     JOLT_CUDA_TRY(cudaEventRecord(ev.a, st));
     JOLT_CUDA_TRY(cudaStreamWaitEvent(fs, ev.a, 0));
+    JOLT_CUDA_TRY(cudaStreamWaitEvent(ps, ev.a, 0));
   }
   JoinGuard join_guard;
-  if (overlap) { join_guard.st = st; join_guard.fs = fs; join_guard.ev = ev.a; }
+  if (overlap) {
+    join_guard.st = st; join_guard.fs = fs; join_guard.ev = ev.a;
+    join_guard.ps = ps; join_guard.ev2 = ev.b;
+  }
   // ---- feature mode: S_d, split over groups of hg heads, f64 reduction
   {
     const int hg = H / L.nsplit;
@@ -672,7 +702,12 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   // writes U_d16, Y16 and the token-Gram relayout Yt), else the SIMT product
   bool yt_done = false;
   if (RD > 0 && proj_tc_supported(L)) {
-    TRY(proj_tc(L, U, X, ws, true, fs));
+    // Y in fp32 only for the consumers that read it: the randomized token
+    // mode, the SIMT token Grams (T <= 128 or no tensor-core path) and the
+    // SIMT cores
+    const bool y_needed = L.token_mode == JOLT_TOKEN_RANDOMIZED || L.T <= 128 ||
+                          !ygram_tc_supported(L) || !cores_tc_supported(L);
+    TRY(proj_tc(L, U, X, ws, y_needed, fs));
     yt_done = L.o_Yt != 0;
   } else if (RD > 0) {
     round_f16_kernel<<<dim3(blocks_for(D * RD), 1, U), 256, 0, fs>>>(ws, ub, L.o_Vd, D, L.o_Ud16,
@@ -707,8 +742,13 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     }
     if (sv_tc_supported(L)) TRY(split_tok_gram(L, U * L.ndt, preg0, pb0, fs));
   }
+  TRY(mark(1, fs));
   if (overlap) JOLT_CUDA_TRY(cudaEventRecord(ev.b, fs));
-  if (RT == 0) return JOLT_OK;
+  if (RT == 0) {
+    TRY(mark(2, st));
+    TRY(mark(3, st));
+    return mark(4, st);
+  }
 
   // ---- token mode: one problem per (unit, feature rank)
   const bool exact = (L.token_mode == JOLT_TOKEN_EXACT);
@@ -718,11 +758,15 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   const PS all_tr{preg, pb, U * ndt};
   const PS full_ps{preg + (size_t)U * ndt * pb, pb, U};
   auto tr_id = [&](int id) { return PS{preg + (size_t)id * pb, (size_t)ndt * pb, U}; };
-  set_int_kernel<<<U * L.nprob, 32, 0, st>>>(preg, pb, L.p_status, 0);
-  JOLT_LAUNCH_CHECK();
   bool joined = !overlap;
+  // the caller's stream waits for the feature stage (event b) and for the
+  // whole-feature solve on the high-priority stream (event c)
   auto join = [&]() -> jolt_status {
-    if (!joined) JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
+    if (!joined) {
+      JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.b, 0));
+      JOLT_CUDA_TRY(cudaEventRecord(ev.c, ps));
+      JOLT_CUDA_TRY(cudaStreamWaitEvent(st, ev.c, 0));
+    }
     joined = true;
     return JOLT_OK;
   };
@@ -731,15 +775,16 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
     // beside the feature stage
     if (L.hasFullD) {
       if (tc) {
-        TRY(gram_tok_tc(L, U, X, full_ps.base, pb, st));
+        TRY(gram_tok_tc(L, U, X, full_ps.base, pb, ps));
       } else {
         TRY(launch_gemm(gd(T, T, D, H, U, 1, opnd(X, xdt, D, 1, (long long)T * D, xu),
                            opnd(X, xdt, 1, D, (long long)T * D, xu), full_ps.f(L.p_ST), T, 1,
                            full_ps.s4(), 0),
-                        st));
+                        ps));
       }
-      TRY(token_exact(L, full_ps, false, st));
+      TRY(token_exact(L, full_ps, false, ps));
     }
+    TRY(mark(2, ps));
     TRY(join());
     if (ndt > 0) {
       // every truncated rank's Gram (already queued after the feature stage
@@ -767,13 +812,18 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       TRY(token_exact(L, all_tr, warm, st, early_tr));
     }
   } else {
+    bool marked = false;
     // randomized: the whole-feature rank first (beside the feature stage),
     // then the truncated ranks one at a time (their sketches differ in size)
     for (int oi = L.nd - 1; oi >= 0; --oi) {
       const int id = oi;
       const int rdv = L.rd[id];
       const bool full = (rdv == D);
-      if (!full) TRY(join());
+      if (!full) {
+        if (!marked) TRY(mark(2, st));
+        marked = true;
+        TRY(join());
+      }
       if (full) {
         TRY(token_randomized(c, full_ps, X, xdt, D, (long long)T * D, xu, rdv, sketch));
       } else {
@@ -781,15 +831,20 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
                              sketch));
       }
     }
+    if (!marked) TRY(mark(2, st));
   }
   TRY(join());
+  TRY(mark(3, st));
   scatter_problems_kernel<<<dim3(64, L.nd, U), 256, 0, st>>>(
       ws, ub, L.o_UT32, L.o_tokev, L.o_status, preg, pb, L.p_UT, L.p_ev, 1, L.p_status, U, ndt, T,
       RT);
   JOLT_LAUNCH_CHECK();
   // cores G(r_d)[h] = U_T^T A_h  (RT x rdv): on the tensor cores for bf16 X
   // (one pass over X for every rank, fp16 cores and U_T written directly)
-  if (cores_tc_supported(L)) return cores_tc(L, U, X, ws, st);
+  if (cores_tc_supported(L)) {
+    TRY(cores_tc(L, U, X, ws, st));
+    return mark(4, st);
+  }
   // else the truncated ranks share one pass over Y, the whole-feature rank
   // reads X
   for (int pass = 0; pass < 2; ++pass) {
@@ -858,7 +913,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   round_f16_kernel<<<dim3(blocks_for((long long)L.nd * T * RT), 1, U), 256, 0, st>>>(
       ws, ub, L.o_UT32, RT, L.o_UT16, RT, L.nd * T, RT, 0, 0, 1);
   JOLT_LAUNCH_CHECK();
-  return JOLT_OK;
+  return mark(4, st);
 }
 
 }  // namespace jolt

@@ -538,6 +538,128 @@ ygram_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constant__ 
   if (warp == 1) tc::tmem_dealloc(tmem, TILE);
 }
 
+// The same Grams for every truncated feature rank of a unit from one pass
+// over its Yt columns: the slab of feature ranks [rd[i-1], rd[i]) (columns
+// [H rd[i-1], H rd[i])) is accumulated into TMEM accumulator i (up to four,
+// 128 columns each), and the epilogue writes S(rd[i]) = sum over i' <= i of
+// slab i' (nested feature ranks: each Gram is a prefix sum of the slabs).
+// One CTA per upper-triangular 128 x 128 tile and unit; half the tensor work
+// of one product per rank.
+__global__ void __launch_bounds__(TC_THREADS, 1)
+ygram_pre_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constant__ CUtensorMap tL,
+                    YgArgs a) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* base = (unsigned char*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  struct Bars { uint64_t full[YG_STAGES], empty[YG_STAGES], accum; uint32_t tmem; };
+  Bars* S = (Bars*)(base + YG_STAGES * YG_STAGE);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int u = blockIdx.y;
+  int mi = 0, idx = blockIdx.x;
+  while (idx >= a.nt - mi) { idx -= a.nt - mi; ++mi; }
+  const int ni = mi + idx;
+  const bool diag = (mi == ni);
+  const int klen = a.k1s[a.ndt - 1];
+  const int nk = (klen + 31) / 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < YG_STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+    }
+    tc::mbar_init(tc::smem_u32(&S->accum), 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = S->tmem;
+  bool ok = true;
+  if (warp == 0 && lane == 0) {
+    const uint32_t bytes = diag ? 2 * YG_A : 4 * YG_A;
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % YG_STAGES, r = kk / YG_STAGES;
+      if (r > 0 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), (r - 1) & 1)) { ok = false; break; }
+      const uint32_t fb = tc::smem_u32(&S->full[s]);
+      tc::mbar_expect_tx(fb, bytes);
+      const uint32_t sa = tc::smem_u32(base + s * YG_STAGE);
+      const int kc = kk * 32;
+      tc::tma_load_3d(sa, &tH, kc, mi * TILE, u, fb);
+      tc::tma_load_3d(sa + YG_A, &tL, kc, mi * TILE, u, fb);
+      if (!diag) {
+        tc::tma_load_3d(sa + 2 * YG_A, &tH, kc, ni * TILE, u, fb);
+        tc::tma_load_3d(sa + 3 * YG_A, &tL, kc, ni * TILE, u, fb);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = (1u << 4) | (2u << 7) | (2u << 10) |
+                               ((uint32_t)(TILE >> 3) << 17) | ((uint32_t)(TILE >> 4) << 24);
+    int slab = 0;
+    bool first = true;
+    for (int kk = 0; kk < nk && ok; ++kk) {
+      const int s = kk % YG_STAGES, r = kk / YG_STAGES;
+      if (!tc::mbar_wait(tc::smem_u32(&S->full[s]), r & 1)) { ok = false; break; }
+      tc::tc_fence_after();
+      const uint32_t sa = tc::smem_u32(base + s * YG_STAGE);
+      const uint32_t sb = diag ? sa : sa + 2 * YG_A;
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int col = kk * 32 + 8 * k4;     // slab boundaries are multiples of 8
+        if (col >= klen) break;
+        if (col >= a.k1s[slab]) { ++slab; first = true; }
+        const uint32_t d = tmem + 128u * (uint32_t)slab;
+        const uint64_t ah = tc::sdesc_sw128(sa + 32 * k4, 16, 1024);
+        const uint64_t al = tc::sdesc_sw128(sa + YG_A + 32 * k4, 16, 1024);
+        const uint64_t bh = tc::sdesc_sw128(sb + 32 * k4, 16, 1024);
+        const uint64_t bl = tc::sdesc_sw128(sb + YG_A + 32 * k4, 16, 1024);
+        tc::mma_tf32(d, ah, bh, idesc, first ? 0u : 1u);
+        tc::mma_tf32(d, ah, bl, idesc, 1);
+        tc::mma_tf32(d, al, bh, idesc, 1);
+        first = false;
+      }
+      tc::mma_commit(tc::smem_u32(&S->empty[s]));
+    }
+    tc::mma_commit(tc::smem_u32(&S->accum));
+  } else if (warp >= 2) {
+    const int q = warp & 3;
+    if (!tc::mbar_wait(tc::smem_u32(&S->accum), 0)) {
+      ok = false;
+    } else {
+      tc::tc_fence_after();
+      const int T = a.T;
+      const int rt = 32 * q + lane, row = mi * TILE + rt;
+#pragma unroll 1
+      for (int c = 0; c < TILE / 32; ++c) {
+        float sum[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum[j] = 0.f;
+        for (int i = 0; i < a.ndt; ++i) {
+          float v[32];
+          tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 128u * (uint32_t)i + (uint32_t)(c * 32), v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum[j] += v[j];
+          float* C = a.S + (long long)(u * a.ndt + i) * a.s_us;
+          if (row < T) {
+            float* cr = C + (long long)row * T + ni * TILE + c * 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (ni * TILE + c * 32 + j < T) cr[j] = sum[j];
+          }
+          if (!diag) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = ni * TILE + c * 32 + j;
+              if (col < T && row < T) C[(long long)col * T + row] = sum[j];
+            }
+          }
+        }
+      }
+    }
+  }
+  if (!ok) atomicOr((int*)(a.ws + (size_t)(u * a.ndt) * a.ub + a.o_status), ST_TIMEOUT);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tc::tmem_dealloc(tmem, 512);
+}
+
 // Yt[u][t][j*H + h] = Y[u][h][t][j] and its tf32 low part.
 __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt, int H, int T,
                               int RD) {
@@ -715,6 +837,19 @@ jolt_status ygram_tc(const Layout& L, int U, const char* ws, char* pbase, size_t
   a.s_us = (long long)pstride / 4;
   a.ws = pbase; a.ub = pstride; a.o_status = L.p_status;
   const size_t smem = (size_t)YG_STAGES * YG_STAGE + 1024 + 256;
+  if (L.ndt <= 4) {
+    // one pass per unit: the ranks' Grams as prefix sums of slabs
+    static bool attr_pre = false;
+    if (!attr_pre) {
+      JOLT_CUDA_TRY(cudaFuncSetAttribute(ygram_pre_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      attr_pre = true;
+    }
+    dim3 grid(a.nt * (a.nt + 1) / 2, U);
+    ygram_pre_tc_kernel<<<grid, TC_THREADS, smem, st>>>(tH, tL, a);
+    JOLT_LAUNCH_CHECK();
+    return JOLT_OK;
+  }
   static bool attr = false;
   if (!attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(ygram_tc_kernel,

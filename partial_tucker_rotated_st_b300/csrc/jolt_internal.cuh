@@ -24,6 +24,7 @@ enum : int {
 
 extern unsigned long long g_launches;
 extern void* g_sweep_ev[2];   // cudaEvent_t pair recorded around the fused sweep kernel, or null
+extern void* g_factor_ev[5];  // cudaEvent_t recorded at the factor's stage boundaries, or null
 inline void count_launch(int n = 1) { g_launches += (unsigned long long)n; }
 
 #define JOLT_CUDA_TRY(expr)                                   \

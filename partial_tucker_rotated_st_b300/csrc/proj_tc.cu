@@ -12,8 +12,8 @@
 // one kind::f16 product per 128-token tile and head:
 //   D[t][32 p + j] = sum_d X[t][d] u_p[d][j]      (exact products, fp32 sums)
 //   Y[t][j] = (D[t][64 + j] + D[t][32 + j]) + D[t][j].
-// One CTA covers one 128-token tile of HB heads of one unit; X tiles and the
-// split factor arrive by TMA (128-byte swizzle).  The epilogue (one thread per
+// One CTA covers one 128-token tile of HB heads of one unit (HB = 2: two CTAs
+// per SM); X tiles and the split factor arrive by TMA (128-byte swizzle).  The epilogue (one thread per
 // token row) writes, per head, Y16 = fp16(Y) [H][T][RD] and, when asked, Y in
 // fp32 [H][T][RD]; and the token-Gram relayout Yt[t][j H + h] with its tf32
 // low part, HB consecutive heads per store, staged through shared memory.
@@ -70,7 +70,7 @@ __global__ void split_ud_kernel(char* ws, size_t ub, size_t o_Vd, size_t o_Vs3, 
 }
 
 template <int HB>
-__global__ void __launch_bounds__(PJ_THREADS, 1)
+__global__ void __launch_bounds__(PJ_THREADS, HB >= 4 ? 1 : 2)
 proj_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ CUtensorMap tB,
                ProjArgs a) {
   constexpr int BCHUNK = PJ_N * 128;                  // one 64-column chunk of the B rows
@@ -462,8 +462,9 @@ jolt_status proj_tc(const Layout& L, int U, const void* X, char* ws, bool write_
   a.ws = ws; a.ub = L.unit_bytes;
   a.o_Y = L.o_Y; a.o_Y16 = L.o_Y16; a.o_Yt = L.o_Yt; a.o_status = L.o_status;
   a.write_y = write_y ? 1 : 0;
+  // two heads per CTA: two CTAs per SM (TMEM 256 columns, 88 KB of shared
+  // memory each) overlap one CTA's loads with the other's epilogue
   const int tiles = (L.T + PJ_ROWS - 1) / PJ_ROWS;
-  if (L.H % 4 == 0) return launch_proj<4>(dim3(tiles, L.H / 4, U), tX, tB, a, st);
   if (L.H % 2 == 0) return launch_proj<2>(dim3(tiles, L.H / 2, U), tX, tB, a, st);
   return launch_proj<1>(dim3(tiles, L.H, U), tX, tB, a, st);
 }

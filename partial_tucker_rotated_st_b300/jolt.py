@@ -75,6 +75,7 @@ _SIG = {
                                              ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _P,
                                              _P, _P]),
     "jolt_set_sweep_events": (ctypes.c_int, [_P, _P]),
+    "jolt_set_factor_events": (ctypes.c_int, [ctypes.POINTER(_P)]),
     "jolt_model_candidates": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P,
                                              ctypes.c_size_t, ctypes.POINTER(ctypes.c_double),
                                              _P, _P]),
@@ -248,6 +249,19 @@ def jolt_set_sweep_events(start=None, stop=None):
     if (start is not None and not a) or (stop is not None and not b):
         raise ValueError("record the events once before passing them")
     _check("jolt_set_sweep_events", lib().jolt_set_sweep_events(a, b))
+
+
+def jolt_set_factor_events(events=None):
+    """Record five torch.cuda.Event (timing enabled, already recorded once) at
+    the factor step's stage boundaries of later jolt_factor_group calls (see
+    include/jolt.h); no argument turns it off."""
+    if events is None:
+        _check("jolt_set_factor_events", lib().jolt_set_factor_events(None))
+        return
+    if len(events) != 5 or any(not e.cuda_event for e in events):
+        raise ValueError("five events, each recorded once before")
+    arr = (_P * 5)(*[e.cuda_event for e in events])
+    _check("jolt_set_factor_events", lib().jolt_set_factor_events(arr))
 
 
 def jolt_model_candidates(cfg, n_units, ws, eps2_host: Sequence[float], dist, ws_bytes=None,
