@@ -285,10 +285,19 @@ jolt_status jolt_encode(const jolt_config* cfg, int n_units, const void* X,
  * D = 128 with 16-byte aligned xhat, blob, stride and code / core sections
  * (as jolt_encode lays them out) runs on the tensor cores; other shapes run
  * the same arithmetic on the SIMT decoder.  A tensor-core tile whose
- * bounded wait gave up is written as NaN (no kernel traps).
+ * bounded wait gave up is written as NaN (no kernel traps) and is reported
+ * by jolt_decode_status.
  */
 jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blob,
                         size_t blob_stride, void* xhat, jolt_dtype out_dtype, void* stream);
+
+/*
+ * The decoder's device-side status since the last call: synchronises `stream`,
+ * then returns JOLT_ERR_CUDA when a bounded wait of a tensor-core decode gave
+ * up (those tiles were written as NaN), else JOLT_OK, and clears it.  The
+ * status is one word per device, shared by every decode on that device.
+ */
+jolt_status jolt_decode_status(void* stream);
 
 /*
  * Attention of each group's queries over its compressed K and V, with the

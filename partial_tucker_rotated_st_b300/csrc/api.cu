@@ -336,6 +336,13 @@ jolt_status jolt_decode(int n_units, const jolt_blob_desc* desc, const void* blo
   return decode_run(n_units, desc, (const char*)blob, blob_stride, xhat, out_dtype, S(stream));
 }
 
+jolt_status jolt_decode_status(void* stream) {
+  int v = 0;
+  const jolt_status s = decode_tc_status(&v, S(stream));
+  if (s != JOLT_OK) return s;
+  return (v & ST_TIMEOUT) ? JOLT_ERR_CUDA : JOLT_OK;
+}
+
 size_t jolt_attend_workspace_size(int n_groups, int H, int T, int D, int nq) {
   if (n_groups < 1 || H < 1 || T < 1 || D < 1 || nq < 1 || nq > JOLT_ATTN_MAX_Q) return 0;
   return attend_ws_bytes(n_groups, H, T, D, nq);

@@ -1,5 +1,5 @@
-// Decoder on the tensor cores (D = 128): X^ = X~ + Q^T (s * codes) for one
-// 128-token tile of one head per CTA.
+// Decoder on the tensor cores (D = 128): X^ = X~ + Q^T (s * codes), every
+// 128-token tile of every head of a batch of units.
 //
 // ["Rotated Tucker residual for outlier-resistant KV quantization",
 //  Implementation notes: decode by multiplying the codes by s, applying the
@@ -10,18 +10,16 @@
 //   residual   R = codes (128 x 128, fp16, exact small integers)
 //                  x (H diag(sigma))^T (fp16, exact +-1)      kind::f16
 //              -> exact integer sums in fp32; x^ gets s_t R / sqrt(D);
-//   low rank   r_T < T, r_d < D:  Z = U_T G_h (tf32, fp16 values exact),
-//                                 X~ = (Z_hi + Z_lo) U_d^T (tf32 split)
-//              r_T < T, r_d = D:  X~ = U_T G_h
+//   low rank   r_T < T, r_d < D:  X~ = U_T W_h, W_h = G_h U_d^T (fp32 sums
+//                                 of exact fp16 products, split tf32 hi + lo)
+//              r_T < T, r_d = D:  X~ = U_T G_h (fp16 values, exact in tf32)
 //              r_T = T, r_d < D:  X~ = G_h[t] U_d^T
 //              r_T = T, r_d = D:  X~ = G_h[t] (fp16(X)), no product.
 // The codes are unpacked by placing each b-bit code in the mantissa of the
 // fp16 1024 (0x6400 | u = 1024 + u) and subtracting 1024 + 2^(b-1) in
 // half2 arithmetic; a 32-bit word of codes is split into its byte lanes, so
 // within a word the codes reach the K index in an order that depends on b,
-// and the rows of H diag(sigma) are built in the same order.  The epilogue
-// (one thread per token row) reads both accumulators from TMEM, adds them
-// and stages the tile in shared memory for coalesced stores.
+// and the rows of H diag(sigma) are built in the same order.
 #include "jolt_internal.cuh"
 #include "tc_common.cuh"
 
@@ -31,7 +29,7 @@ namespace jolt {
 
 namespace {
 
-constexpr int DT_ROWS = 128, DT_THREADS = 256, DT_D = 128;
+constexpr int DT_ROWS = 128, DT_D = 128;
 constexpr int DT_ATOM = 128 * 128;          // 128 rows x 128 bytes, one swizzle block
 constexpr int DT_MAX_UNITS = 32;
 
@@ -40,7 +38,7 @@ struct DecTcUnit {
   unsigned long long off_UT, off_Ud, off_G, off_scale, off_codes;
 };
 struct DecTcArgs {
-  int H, T, out_dtype, u0;
+  int H, T, out_dtype, u0, nu;
   const char* blob;
   unsigned long long stride;
   void* xhat;
@@ -49,26 +47,6 @@ struct DecTcArgs {
 
 __device__ __forceinline__ uint32_t sw128(int r, int byte) {
   return (uint32_t)(r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
-}
-
-// 16 fp32 TMEM columns of this thread's lane, waited for.
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(addr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
-               :
-               : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // 16 columns of this thread's TMEM lane, issued without waiting.
@@ -139,7 +117,8 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 template <int B>
 __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char* sH, int r,
                                                int half, const uint4 (&cq)[4], bool in,
-                                               const unsigned char* sb, const uint2* sgn) {
+                                               const unsigned char* sb, const uint2* sgn,
+                                               bool codes = true, bool signs = true) {
   constexpr int PER = 32 / B, M = 8 / B, NW = 64 * B / 32;   // words in 64 codes
   constexpr uint32_t MASK = B == 8 ? 0xFFFFFFFFu : (B == 4 ? 0x0F0F0F0Fu : 0x03030303u);
   constexpr uint32_t BIAS = 0x64006400u | (1u << (B - 1)) | (1u << (B - 1 + 16));
@@ -150,6 +129,7 @@ __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char*
   for (int q = 0; q < NW / 4; ++q) {
     w[4 * q] = cq[q].x; w[4 * q + 1] = cq[q].y; w[4 * q + 2] = cq[q].z; w[4 * q + 3] = cq[q].w;
   }
+  if (codes)
 #pragma unroll
   for (int wi = 0; wi < NW; ++wi)
 #pragma unroll
@@ -165,6 +145,7 @@ __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char*
       v.y = in ? *reinterpret_cast<const uint32_t*>(&h2) : 0u;
       *reinterpret_cast<uint2*>(sC + (k >> 6) * DT_ATOM + sw128(r, (k & 63) * 2)) = v;
     }
+  if (!signs) return;
   // H diag(sigma), row d = r: neg(k) = parity(d & c(k)) ^ sigma_d; c(k) =
   // word base + local code, and the parity splits over the two
   const int d = r;
@@ -189,72 +170,77 @@ __device__ __forceinline__ void build_residual(unsigned char* sC, unsigned char*
   }
 }
 
+
+// ------------------------------------------------------------------ kernel
+// One persistent CTA per SM walks a contiguous range of 128-token tiles
+// (unit-major, then head, then token tile), two tiles in flight:
+//   warps 0-7  (two threads per tile row) stage tile n's operands in shared
+//              memory stage n % 2: the row's codes unpacked to fp16, its
+//              low-rank row (a U_T row, or a G row for r_T = T) as tf32; and,
+//              when the unit or head changes, the B operands: H diag(sigma)
+//              (per unit and bit width) and the low-rank factor (per head:
+//              W_h = G_h U_d^T split tf32 hi + lo; G_h; or U_d);
+//   warp 8     issues tile n's products into TMEM buffer n % 2 (residual,
+//              256 columns per buffer: [0, 128) the codes times H diag(sigma),
+//              [128, 256) the low-rank rebuild);
+//   warps 9-16 read buffer n % 2 (two threads per row, 64 columns each), form
+//              x^ = X~ + (s_t / sqrt(D)) R and write the row.
+// Hand-offs by mbarriers: full (stage written), empty (the stage's products
+// done), tfull (buffer written), tempty (buffer read).  Every wait is
+// bounded; a wait that gives up sets the decoder's status word and the
+// tile's output reads NaN.
+constexpr int DP_THREADS = 544;
+
+__device__ int g_decode_status;   // ST_* bits of decoder waits that gave up
+
+struct DpBars {
+  uint64_t full[2], empty[2], tfull[2], tempty[2];
+  uint32_t tmem;
+  uint2 sgn[16];
+};
+
 template <int KW>
-__global__ void __launch_bounds__(DT_THREADS, KW == 32 ? 2 : 1) decode_tc_kernel(const __grid_constant__ DecTcArgs a) {
-  constexpr int NCH = KW / 32;                 // swizzle atoms per tf32 row
+struct DpLayout {
+  static constexpr int NCH = KW / 32;                     // swizzle atoms per tf32 row
+  static constexpr int STAGE = 2 * DT_ATOM + NCH * DT_ATOM;   // codes fp16, low-rank A
+  static constexpr int O_HS = 2 * STAGE;                   // H diag(sigma), 2 atoms
+  static constexpr int O_LBH = O_HS + 2 * DT_ATOM;         // low-rank B hi
+  static constexpr int O_LBL = O_LBH + NCH * DT_ATOM;      // low-rank B lo
+  static constexpr int O_BARS = O_LBL + NCH * DT_ATOM;
+  // bf16 output staging for the TMA stores, two tiles (KW = 32 only: the
+  // 64-wide operands leave no room, and that variant stores directly)
+  static constexpr bool STAGED = KW == 32;
+  static constexpr int O_OUT = O_BARS + 1024;
+  static constexpr int BYTES = O_OUT + (STAGED ? 2 * 2 * DT_ATOM : 0) + 1024;
+};
+
+__device__ __forceinline__ int dp_mode(int rT, int rd, int T) {
+  // 0: U_T W_h (both truncated); 1: U_T G_h (r_d = D); 2: G rows U_d^T
+  // (r_T = T); 3: G rows themselves
+  return rT == T ? (rd == DT_D ? 3 : 2) : (rd == DT_D ? 1 : 0);
+}
+
+template <int KW>
+__global__ void __launch_bounds__(DP_THREADS, 1)
+decode_tc_kernel(const __grid_constant__ DecTcArgs a, const __grid_constant__ CUtensorMap tO) {
+  using LY = DpLayout<KW>;
   extern __shared__ __align__(1024) unsigned char dtc_raw[];
-  unsigned char* base = (unsigned char*)(((uintptr_t)dtc_raw + 1023) & ~(uintptr_t)1023);
-  // region R: the residual operands (codes, H diag(sigma)); once the
-  // residual product is done, Z hi / Z lo / U_d of the second stage (mode 0)
-  // and at the end the output staging
-  unsigned char* sC = base;                    // codes, fp16 [128 rows][128], 2 atoms
-  unsigned char* sH = sC + 2 * DT_ATOM;        // H diag(sigma), fp16 [128 d][128], 2 atoms
-  unsigned char* sA = sH + 2 * DT_ATOM;        // tf32 A of the first product [128 rows][KW]
-  unsigned char* sX = sA + NCH * DT_ATOM;      // tf32 B of the first product
-  unsigned char* sZh = sC;                     // mode 0, second stage: Z hi, Z lo, U_d rows
-  unsigned char* sZl = sC + NCH * DT_ATOM;
-  unsigned char* sU = sC + 2 * NCH * DT_ATOM;
-  struct Bars { uint64_t mma; uint32_t tmem; uint2 sgn[16]; };
-  Bars* S = reinterpret_cast<Bars*>(sX + NCH * DT_ATOM);
-  const int tile = blockIdx.x, h = blockIdx.y, uz = blockIdx.z;
-  const int u = a.u0 + uz;
-  const DecTcUnit du = a.un[uz];
-  // two threads per token row: r = the row (and the TMEM lane), half = which
-  // half of the K range / the output columns
-  const int t = threadIdx.x, warp = t >> 5, r = t & (DT_ROWS - 1), half = t >> 7;
+  unsigned char* base = dtc_raw + ((1024u - (tc::smem_u32(dtc_raw) & 1023u)) & 1023u);
+  DpBars* S = reinterpret_cast<DpBars*>(base + LY::O_BARS);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int T = a.T, H = a.H;
-  const int t0 = tile * DT_ROWS, row = t0 + r;
-  const bool in = row < T;
-  const char* blob = a.blob + (unsigned long long)u * a.stride;
-  const int rT = du.rT, rd = du.rd, b = du.b;
-  const bool fullT = (rT == T), fullD = (rd == DT_D);
-  // 0: Z = U_T G_h then Z U_d^T; 1: U_T G_h; 2: G rows U_d^T; 3: G rows as X~
-  const int mode = fullT ? (fullD ? 3 : 2) : (fullD ? 1 : 0);
-  const int kz = fullT ? rd : rT;              // K of the product into X~ (modes 1, 2)
-  const int k8 = (kz + 7) & ~7;
-  const int rT8 = (rT + 7) & ~7, rd8 = (rd + 7) & ~7, rd16 = (rd + 15) & ~15;
-
-  // ---- every global read of the CTA issued first: this thread's half row of
-  // codes, its scale, the rows it gathers for the low-rank operands
-  const __half* UT = reinterpret_cast<const __half*>(blob + du.off_UT);
-  const __half* Ud = reinterpret_cast<const __half*>(blob + du.off_Ud);
-  const __half* G = reinterpret_cast<const __half*>(blob + du.off_G);
-  const __half* Gh = G + (size_t)h * rT * rd;
-  uint4 cq[4];                                 // up to 64 bytes of codes
-  {
-    const uint4* cw = reinterpret_cast<const uint4*>(
-        blob + du.off_codes + ((unsigned long long)h * T + (in ? row : 0)) * (DT_D * b / 8) +
-        half * (8 * b));
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      cq[q] = (b > 0 && in && q < b / 2) ? cw[q] : make_uint4(0, 0, 0, 0);
-  }
-  const float s = (b > 0 && in) ? __half2float(reinterpret_cast<const __half*>(blob + du.off_scale)
-                                                   [(size_t)h * T + row]) * rsqrtf((float)DT_D)
-                                : 0.f;
-  __half g1[KW], g2[KW];   // first-product operand row; mode 0: the U_d row of the second
-  if (mode == 0 || mode == 1) {
-    if (half == 0) load_row<KW>(g1, UT + (size_t)(in ? row : 0) * rT, 1, rT, in);
-    else if (mode == 0) load_row<KW>(g1, Gh + (r < rd ? r : 0), rd, rT, r < rd);
-    else load_row<KW>(g1, Gh + r, DT_D, rT, true);
-  } else if (mode == 2) {
-    if (half == 0) load_row<KW>(g1, G + ((size_t)h * T + (in ? row : 0)) * rd, 1, rd, in);
-    else load_row<KW>(g1, Ud + (size_t)r * rd, 1, rd, true);
-  }
-  if (mode == 0 && half == 1) load_row<KW>(g2, Ud + (size_t)r * rd, 1, rd, true);
-
+  const int tiles_t = (T + DT_ROWS - 1) / DT_ROWS;
+  const int ntot = a.nu * H * tiles_t;
+  const int chunk = (ntot + gridDim.x - 1) / gridDim.x;
+  const int i0 = blockIdx.x * chunk, i1 = min(ntot, i0 + chunk);
+  const int nt = i1 > i0 ? i1 - i0 : 0;
   if (t == 0) {
-    tc::mbar_init(tc::smem_u32(&S->mma), 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(tc::smem_u32(&S->full[s]), 8);
+      tc::mbar_init(tc::smem_u32(&S->empty[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->tfull[s]), 1);
+      tc::mbar_init(tc::smem_u32(&S->tempty[s]), 8);
+    }
     tc::fence_barrier_init();
   }
   if (t < 16) {
@@ -265,190 +251,374 @@ __global__ void __launch_bounds__(DT_THREADS, KW == 32 ? 2 : 1) decode_tc_kernel
              ((0x3C00u | (((uint32_t)t >> (2 * j + 1)) & 1u) << 15) << 16);
     S->sgn[t] = make_uint2(v[0], v[1]);
   }
-  if (warp == 0) tc::tmem_alloc(tc::smem_u32(&S->tmem), 256);
+  if (warp == 8) tc::tmem_alloc(tc::smem_u32(&S->tmem), 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = S->tmem;
-  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   bool ok = true;
-  uint32_t phase = 0;
-  auto mma_wait = [&]() {
-    if (!tc::mbar_wait(tc::smem_u32(&S->mma), phase & 1)) ok = false;
-    ++phase;
-    tc::tc_fence_after();
+  const float rsD = rsqrtf((float)DT_D);
+  auto tile_at = [&](int n, int& u, int& h, int& tt) {
+    const int i = i0 + n;
+    u = i / (H * tiles_t);
+    h = (i / tiles_t) % H;
+    tt = i % tiles_t;
   };
 
-  // ---- residual operands: codes (A) and H diag(sigma) (B), fp16
-  if (b > 0) {
-    const unsigned char* sb = reinterpret_cast<const unsigned char*>(blob) + 88;
-    if (b == 2) build_residual<2>(sC, sH, r, half, cq, in, sb, S->sgn);
-    else if (b == 4) build_residual<4>(sC, sH, r, half, cq, in, sb, S->sgn);
-    else build_residual<8>(sC, sH, r, half, cq, in, sb, S->sgn);
-  }
-
-  // ---- low-rank operands of the first product: A = sA (half 0), B = sX (half 1)
-  if (mode == 0) {
-    if (half == 0) store_row<KW>(sA, r, g1);
-    else if (r < rd16) store_row<KW>(sX, r, g1);   // B rows j < rd16: G_h[k][j]
-  } else if (mode == 1 || mode == 2) {
-    store_row<KW>(half == 0 ? sA : sX, r, g1);
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  tc::tc_fence_before();
-  __syncthreads();
-
-  // ---- residual into TMEM [0, 128); the first low-rank product into
-  // [128, ...): X~ itself (modes 1, 2) or Z = U_T G_h (mode 0)
-  const bool any = (b > 0) || mode != 3;
-  if (t == 0 && any) {
-    tc::tc_fence_after();
-    if (b > 0) {
+  if (warp < 8) {
+    // ---------------- operand staging: two threads per tile row, thread
+    // (r, hf) owns half hf of the row's K range; the next tile's global
+    // reads are issued before the current tile's operands are written
+    const int r = t & (DT_ROWS - 1), hf = t >> 7;
+    int hs_key = -1, lb_key = -1;          // what the B operands hold
+    // this thread's reads of tile n: its half of the codes, its half of the
+    // low-rank A row (raw fp16)
+    uint4 pc[4], pa[KW / 16];
+    auto fetch = [&](int n) {
+      int u, h, tt;
+      tile_at(n, u, h, tt);
+      const DecTcUnit du = a.un[u];
+      const int mode = dp_mode(du.rT, du.rd, T), b = du.b;
+      const char* blob = a.blob + (unsigned long long)(a.u0 + u) * a.stride;
+      const int row = tt * DT_ROWS + r;
+      const bool in = row < T;
+      const uint4* cw = reinterpret_cast<const uint4*>(
+          blob + du.off_codes + ((unsigned long long)h * T + (in ? row : 0)) * (DT_D * b / 8));
 #pragma unroll
-      for (int kc = 0; kc < 2; ++kc)
+      for (int qq = 0; qq < 4; ++qq)
+        pc[qq] = (b > 0 && in && qq < b / 2) ? cw[hf * (b / 2) + qq] : make_uint4(0, 0, 0, 0);
+      const int K = mode == 2 ? du.rd : du.rT;
+      const __half* src = mode == 2 ? reinterpret_cast<const __half*>(blob + du.off_G) +
+                                          ((size_t)h * T + (in ? row : 0)) * du.rd
+                                    : reinterpret_cast<const __half*>(blob + du.off_UT) +
+                                          (size_t)(in ? row : 0) * du.rT;
+      const int k0 = hf * (KW / 2);
+      const bool vec = (K % 8) == 0;          // rows start on 16-byte boundaries
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sC + kc * DT_ATOM) + 32 * k, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sH + kc * DT_ATOM) + 32 * k, 16, 1024);
-          tc::mma_f16(tmem, ad, bd, idesc_f16h(128, 128), (kc | k) != 0);
-        }
-    }
-    if (mode != 3) {
-      const int kk_n = (mode == 0 ? rT8 : k8) / 8;
-      const uint32_t id = idesc_tf32(128, mode == 0 ? rd16 : 128);
-      for (int kk = 0; kk < kk_n; ++kk) {
-        const uint32_t off = (kk >> 2) * DT_ATOM;
-        const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sA + off) + 32 * (kk & 3), 16, 1024);
-        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sX + off) + 32 * (kk & 3), 16, 1024);
-        tc::mma_tf32(tmem + 128, ad, bd, id, kk != 0);
-      }
-    }
-    tc::mma_commit(tc::smem_u32(&S->mma));
-  }
-  if (any) mma_wait();
-
-  // ---- mode 0, second stage: X~ = (Z hi + Z lo) U_d^T into [128, 256)
-  if (mode == 0) {
-    // half 0: the Z row -> tf32 hi and lo (K = r_d); half 1: U_d row d = r;
-    // both over the residual's operands (its product is done)
-    if (half == 0) {
-      for (int c = 0; c < rd16; c += 16) {
-        float z[16];
-        tmem_ld16(trow + 128 + c, z);
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-          float4 hi, lo;
-          float* ph = reinterpret_cast<float*>(&hi);
-          float* pl = reinterpret_cast<float*>(&lo);
+      for (int i = 0; i < KW / 16; ++i) {
+        const int k = k0 + 8 * i;
+        if (mode == 3 || !in || k >= K) {
+          pa[i] = make_uint4(0, 0, 0, 0);
+        } else if (vec) {
+          pa[i] = *reinterpret_cast<const uint4*>(src + k);
+        } else {
+          uint32_t hw[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float v = (c + i + e < rd) ? z[i + e] : 0.f;
-            const float vh = __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
-            ph[e] = vh;
-            pl[e] = v - vh;
+            const unsigned short lo = k + 2 * e < K ? __half_as_ushort(src[k + 2 * e]) : 0;
+            const unsigned short hi = k + 2 * e + 1 < K ? __half_as_ushort(src[k + 2 * e + 1]) : 0;
+            hw[e] = (uint32_t)lo | ((uint32_t)hi << 16);
           }
-          if (c + i < rd8) {
-            *reinterpret_cast<float4*>(tf32_at(sZh, r, c + i)) = hi;
-            *reinterpret_cast<float4*>(tf32_at(sZl, r, c + i)) = lo;
+          pa[i] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+      }
+    };
+    if (nt > 0) fetch(0);
+    for (int n = 0; n < nt; ++n) {
+      int u, h, tt;
+      tile_at(n, u, h, tt);
+      const DecTcUnit du = a.un[u];
+      const int rT = du.rT, rd = du.rd, b = du.b;
+      const int mode = dp_mode(rT, rd, T);
+      const char* blob = a.blob + (unsigned long long)(a.u0 + u) * a.stride;
+      const int s = n & 1;
+      unsigned char* sC = base + s * LY::STAGE;
+      unsigned char* sA = sC + 2 * DT_ATOM;
+      const int hk = b > 0 ? u * 16 + b : -1;
+      const int lk = mode == 0 || mode == 1 ? u * H + h : (mode == 2 ? (1 << 30) + u : -1);
+      const bool need_hs = b > 0 && hk != hs_key;
+      const bool need_lb = lk >= 0 && lk != lb_key;
+      // the B operands are rewritten only once every product of earlier
+      // tiles is done; the stage once tile n - 2's products are
+      if (n >= 1 && (need_hs || need_lb)) {
+        if (!tc::mbar_wait(tc::smem_u32(&S->empty[(n - 1) & 1]), ((n - 1) >> 1) & 1)) ok = false;
+      }
+      if (n >= 2 && !tc::mbar_wait(tc::smem_u32(&S->empty[s]), ((n - 2) >> 1) & 1)) ok = false;
+      const int row = tt * DT_ROWS + r;
+      const bool in = row < T;
+      const __half* Ud = reinterpret_cast<const __half*>(blob + du.off_Ud);
+      const __half* G = reinterpret_cast<const __half*>(blob + du.off_G);
+      const __half* Gh = G + (size_t)h * rT * rd;
+      if (need_lb) {
+        // low-rank B^T, K-major [n = d][k], column d = r, this thread's half
+        // of k; zero past K
+        unsigned char* sBh = base + LY::O_LBH;
+        unsigned char* sBl = base + LY::O_LBL;
+        const int d = r, kb = hf * (KW / 2);
+        if (mode == 0) {
+          // W_h[k][d] = sum_j G_h[k][j] U_d[d][j], split tf32 hi + lo; G_h
+          // (r_T x r_d) and U_d (D x r_d) are first staged, in fp32, in this
+          // stage's operand area (free: its codes and A rows come after)
+          float* gs = reinterpret_cast<float*>(sC);
+          for (int e = t; e < rT * rd; e += 256) gs[e] = __half2float(Gh[e]);
+          // the U_d row, staged beside G_h (fp32), read back as a broadcast
+          float* us = gs + rT * rd;
+          for (int e = t; e < DT_D * rd; e += 256) us[e] = __half2float(Ud[e]);
+          asm volatile("bar.sync 1, 256;" ::: "memory");
+          const float* udr = us + (size_t)d * rd;
+          for (int k = kb; k < kb + KW / 2; k += 4) {
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int j = 0; j < rd; ++j) {
+              const float uj = udr[j];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (k + e < rT) v[e] = fmaf(gs[(k + e) * rd + j], uj, v[e]);
+            }
+            float hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              hi[e] = __uint_as_float(__float_as_uint(v[e]) & 0xFFFFE000u);
+              lo[e] = v[e] - hi[e];
+            }
+            *reinterpret_cast<float4*>(tf32_at(sBh, d, k)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<float4*>(tf32_at(sBl, d, k)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
+          }
+          asm volatile("bar.sync 1, 256;" ::: "memory");   // the area is overwritten next
+        } else {
+          // exact fp16 values: G_h[k][d] (mode 1) or U_d[d][k] (mode 2)
+          const int K = mode == 1 ? rT : rd;
+          for (int k = kb; k < kb + KW / 2; k += 4) {
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int kk = k + e;
+              v[e] = kk >= K ? 0.f
+                             : __half2float(mode == 1 ? Gh[(size_t)kk * DT_D + d] : Ud[(size_t)d * rd + kk]);
+            }
+            *reinterpret_cast<float4*>(tf32_at(sBh, d, k)) = make_float4(v[0], v[1], v[2], v[3]);
+          }
+        }
+        lb_key = lk;
+      }
+      // this thread's half of the row's codes and, when the unit or bit
+      // width changed, of row d = r of H diag(sigma)
+      if (b > 0) {
+        const unsigned char* sb = reinterpret_cast<const unsigned char*>(blob) + 88;
+        unsigned char* sH = base + LY::O_HS;
+        if (b == 2) build_residual<2>(sC, sH, r, hf, pc, in, sb, S->sgn, true, need_hs);
+        else if (b == 4) build_residual<4>(sC, sH, r, hf, pc, in, sb, S->sgn, true, need_hs);
+        else build_residual<8>(sC, sH, r, hf, pc, in, sb, S->sgn, true, need_hs);
+        if (need_hs) hs_key = hk;
+      }
+      // this thread's half of the low-rank A row, fp16 -> tf32
+      if (mode != 3) {
+#pragma unroll
+        for (int i = 0; i < KW / 16; ++i) {
+          const __half2* hv = reinterpret_cast<const __half2*>(&pa[i]);
+          const int k = hf * (KW / 2) + 8 * i;
+          const float2 f0 = __half22float2(hv[0]), f1 = __half22float2(hv[1]);
+          const float2 f2 = __half22float2(hv[2]), f3 = __half22float2(hv[3]);
+          *reinterpret_cast<float4*>(tf32_at(sA, r, k)) = make_float4(f0.x, f0.y, f1.x, f1.y);
+          *reinterpret_cast<float4*>(tf32_at(sA, r, k + 4)) = make_float4(f2.x, f2.y, f3.x, f3.y);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&S->full[s]))
+                     : "memory");
+      if (n + 1 < nt) fetch(n + 1);
+    }
+  } else if (warp == 8) {
+    // ---------------- products
+    for (int n = 0; n < nt; ++n) {
+      int u, h, tt;
+      tile_at(n, u, h, tt);
+      const DecTcUnit du = a.un[u];
+      const int mode = dp_mode(du.rT, du.rd, T), b = du.b;
+      const int s = n & 1;
+      bool okw = tc::mbar_wait(tc::smem_u32(&S->full[s]), (n >> 1) & 1);
+      if (n >= 2) okw = tc::mbar_wait(tc::smem_u32(&S->tempty[s]), ((n - 2) >> 1) & 1) && okw;
+      if (!okw) ok = false;
+      tc::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t d0 = tmem + 256u * (uint32_t)s;
+        const uint32_t sC = tc::smem_u32(base + s * LY::STAGE), sA = sC + 2 * DT_ATOM;
+        const uint32_t sH = tc::smem_u32(base + LY::O_HS);
+        const uint32_t sBh = tc::smem_u32(base + LY::O_LBH), sBl = tc::smem_u32(base + LY::O_LBL);
+        if (b > 0) {
+#pragma unroll
+          for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = tc::sdesc_sw128(sC + kc * DT_ATOM + 32 * k, 16, 1024);
+              const uint64_t bd = tc::sdesc_sw128(sH + kc * DT_ATOM + 32 * k, 16, 1024);
+              tc::mma_f16(d0, ad, bd, idesc_f16h(128, 128), (kc | k) != 0);
+            }
+        }
+        if (mode != 3) {
+          const int K = (mode == 2) ? du.rd : du.rT;
+          const int ks = (K + 7) >> 3;
+          for (int kk = 0; kk < ks; ++kk) {
+            const uint32_t off = (kk >> 2) * DT_ATOM + 32 * (kk & 3);
+            const uint64_t ad = tc::sdesc_sw128(sA + off, 16, 1024);
+            const uint64_t bh = tc::sdesc_sw128(sBh + off, 16, 1024);
+            tc::mma_tf32(d0 + 128, ad, bh, idesc_tf32(128, 128), kk != 0);
+            if (mode == 0) {
+              const uint64_t bl = tc::sdesc_sw128(sBl + off, 16, 1024);
+              tc::mma_tf32(d0 + 128, ad, bl, idesc_tf32(128, 128), 1);
+            }
+          }
+        }
+        tc::mma_commit(tc::smem_u32(&S->tfull[s]));
+        tc::mma_commit(tc::smem_u32(&S->empty[s]));
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---------------- epilogue, thread = row 32 q + lane (TMEM lane quarter
+    // q), columns [64 hf, 64 hf + 64)
+    const int q = warp & 3, r = 32 * q + lane, hf = (warp - 9) >> 2;
+    const bool f32 = (a.out_dtype == JOLT_F32);
+    // bf16 tiles go out through shared memory by TMA stores (the 128-byte
+    // swizzled layout: conflict-free row writes), fp32 ones directly
+    const bool staged = LY::STAGED && !f32;
+    const bool lead = (warp == 9 && lane == 0);
+    // this row's scale of tile n (raw fp16), read one tile ahead
+    auto scale_of = [&](int n) -> unsigned short {
+      int u, h, tt;
+      tile_at(n, u, h, tt);
+      const DecTcUnit du = a.un[u];
+      const int row = tt * DT_ROWS + r;
+      if (du.b == 0 || row >= T) return 0;
+      const char* blob = a.blob + (unsigned long long)(a.u0 + u) * a.stride;
+      return reinterpret_cast<const unsigned short*>(blob + du.off_scale)[(size_t)h * T + row];
+    };
+    unsigned short sc_next = nt > 0 ? scale_of(0) : 0;
+    for (int n = 0; n < nt; ++n) {
+      int u, h, tt;
+      tile_at(n, u, h, tt);
+      const DecTcUnit du = a.un[u];
+      const int mode = dp_mode(du.rT, du.rd, T), b = du.b;
+      const int s = n & 1;
+      const float sc = __half2float(__ushort_as_half(sc_next)) * rsD;
+      if (n + 1 < nt) sc_next = scale_of(n + 1);
+      const bool okw = tc::mbar_wait(tc::smem_u32(&S->tfull[s]), (n >> 1) & 1);
+      if (!okw) ok = false;
+      tc::tc_fence_after();
+      const int row = tt * DT_ROWS + r;
+      const bool in = row < T;
+      const char* blob = a.blob + (unsigned long long)(a.u0 + u) * a.stride;
+      const __half* Grow = reinterpret_cast<const __half*>(blob + du.off_G) +
+                           ((size_t)h * T + (in ? row : 0)) * DT_D;
+      const uint32_t tl = tmem + 256u * (uint32_t)s + ((uint32_t)(32 * q) << 16);
+      const size_t obase = (((size_t)(a.u0 + u) * H + h) * T + (in ? row : 0)) * DT_D;
+      unsigned char* stg = base + LY::O_OUT + (n & 1) * 2 * DT_ATOM;
+      if (staged) {
+        // the TMA store that last read this buffer (tile n - 2) is done
+        if (lead && n >= 2) tc::bulk_wait_read1();
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+      }
+      const int cb = 64 * hf;
+      uint32_t rr[16], rl[16];
+      if (b > 0) tmem_ld16_issue(tl + cb, rr);
+      if (mode != 3) tmem_ld16_issue(tl + 128 + cb, rl);
+#pragma unroll 1
+      for (int c = cb; c < cb + 64; c += 16) {
+        tmem_ld_wait2(rr, rl);
+        float xr[16], xl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          xr[i] = __uint_as_float(rr[i]);
+          xl[i] = __uint_as_float(rl[i]);
+        }
+        // the next 16 columns are loaded while these are written
+        if (c + 16 < cb + 64) {
+          if (b > 0) tmem_ld16_issue(tl + c + 16, rr);
+          if (mode != 3) tmem_ld16_issue(tl + 128 + c + 16, rl);
+        }
+        if (mode == 3) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 8) {
+            const uint4 raw = in ? *reinterpret_cast<const uint4*>(Grow + c + i) : make_uint4(0, 0, 0, 0);
+            const __half2* hv = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = __half22float2(hv[e]);
+              xl[i + 2 * e] = f.x;
+              xl[i + 2 * e + 1] = f.y;
+            }
+          }
+        }
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          x[i] = b > 0 ? fmaf(sc, xr[i], xl[i]) : xl[i];
+          if (!okw) x[i] = __int_as_float(0x7fc00000);   // a tile whose wait gave up reads NaN
+        }
+        if (f32) {
+          if (in) {
+            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.xhat) + obase + c);
+#pragma unroll
+            for (int i = 0; i < 16; i += 4) o[i / 4] = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+          }
+        } else {
+          uint32_t pk[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const __nv_bfloat162 pv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+            pk[e] = *reinterpret_cast<const uint32_t*>(&pv);
+          }
+          if (staged) {
+            unsigned char* at = stg + (c >> 6) * DT_ATOM;
+            *reinterpret_cast<uint4*>(at + sw128(r, (c & 63) * 2)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4*>(at + sw128(r, (c & 63) * 2 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          } else if (in) {
+            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.xhat) + obase + c);
+            o[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            o[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
       }
-    } else {
-      store_row<KW>(sU, r, g2);
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tc::tc_fence_before();
-    __syncthreads();
-    if (t == 0) {
-      tc::tc_fence_after();
-      for (int kk = 0; kk < rd8 / 8; ++kk) {
-        const uint32_t off = (kk >> 2) * DT_ATOM;
-        const uint64_t ah = tc::sdesc_sw128(tc::smem_u32(sZh + off) + 32 * (kk & 3), 16, 1024);
-        const uint64_t al = tc::sdesc_sw128(tc::smem_u32(sZl + off) + 32 * (kk & 3), 16, 1024);
-        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sU + off) + 32 * (kk & 3), 16, 1024);
-        tc::mma_tf32(tmem + 128, ah, bd, idesc_tf32(128, 128), kk != 0);
-        tc::mma_tf32(tmem + 128, al, bd, idesc_tf32(128, 128), 1);
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(&S->tempty[s]))
+                     : "memory");
+      if (staged) {
+        // the tile's rows below T go out in two 64-column boxes
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        if (lead) {
+          const int rb = (a.u0 + u) * H + h;
+          tc::tma_store_3d(&tO, tc::smem_u32(stg), 0, tt * DT_ROWS, rb);
+          tc::tma_store_3d(&tO, tc::smem_u32(stg + DT_ATOM), 64, tt * DT_ROWS, rb);
+          tc::bulk_commit();
+        }
       }
-      tc::mma_commit(tc::smem_u32(&S->mma));
     }
-    mma_wait();
+    if (lead) tc::bulk_wait_all();
   }
-
-  // ---- epilogue: x^ = X~ + s R / sqrt(D) for columns [64 half, 64 half + 64)
-  // of row r, staged row-major (padded rows)
-  const bool f32 = (a.out_dtype == JOLT_F32);
-  const int rowb = f32 ? DT_D * 4 + 16 : DT_D * 2 + 16;   // staging row stride (bytes)
-  unsigned char* stg = sC;                                 // no operand is read any more
-  const __half* Grow = G + ((size_t)h * T + (in ? row : 0)) * DT_D;
-  for (int c = 64 * half; c < 64 * half + 64; c += 16) {
-    uint32_t lu[16], ru[16];
-    if (mode != 3) tmem_ld16_issue(trow + 128 + c, lu);
-    if (b > 0) tmem_ld16_issue(trow + c, ru);
-    if (mode != 3 || b > 0) tmem_ld_wait2(lu, ru);
-    float lr[16], rr[16];
-    if (mode != 3) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) lr[i] = __uint_as_float(lu[i]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; i += 8) {
-        const uint4 raw = in ? *reinterpret_cast<const uint4*>(Grow + c + i) : make_uint4(0, 0, 0, 0);
-        const __half* hv = reinterpret_cast<const __half*>(&raw);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) lr[i + e] = __half2float(hv[e]);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) rr[i] = __uint_as_float(ru[i]);
-    float x[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (b > 0) ? fmaf(s, rr[i], lr[i]) : lr[i];
-    if (!ok) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = __int_as_float(0x7fc00000);   // a timed-out tile reads NaN
-    }
-    if (f32) {
-#pragma unroll
-      for (int i = 0; i < 16; i += 4)
-        *reinterpret_cast<float4*>(stg + r * rowb + (c + i) * 4) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
-    } else {
-      uint32_t pk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-        pk[i] = *reinterpret_cast<const uint32_t*>(&p);
-      }
-      *reinterpret_cast<uint4*>(stg + r * rowb + c * 2) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(stg + r * rowb + c * 2 + 16) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    }
-  }
+  if (!ok) atomicOr(&g_decode_status, ST_TIMEOUT);
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
-  // coalesced copy-out of the tile's rows < T
-  const int rowbytes = f32 ? DT_D * 4 : DT_D * 2;
-  const int per_row = rowbytes / 16;
-  const int nrows = min(DT_ROWS, T - t0);
-  char* out = reinterpret_cast<char*>(a.xhat) +
-              (((size_t)u * H + h) * T + t0) * (size_t)rowbytes;
-  for (int i = t; i < nrows * per_row; i += DT_THREADS) {
-    const int rr = i / per_row, c16 = i % per_row;
-    *reinterpret_cast<uint4*>(out + (size_t)rr * rowbytes + c16 * 16) =
-        *reinterpret_cast<const uint4*>(stg + rr * rowb + c16 * 16);
+  if (warp == 8) tc::tmem_dealloc(tmem, 512);
+}
+
+int dp_sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    n[dev] = v;
   }
+  return n[dev];
 }
 
 template <int KW>
-jolt_status launch_dtc(dim3 grid, const DecTcArgs& a, cudaStream_t st) {
-  constexpr int NCH = KW / 32;
-  const size_t smem = 1024 + 4 * DT_ATOM + 2 * NCH * DT_ATOM + 256;
+jolt_status launch_dtc(int ntiles, const DecTcArgs& a, const CUtensorMap& tO, cudaStream_t st) {
+  const size_t smem = DpLayout<KW>::BYTES;
   static bool attr = false;
   if (!attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(decode_tc_kernel<KW>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     attr = true;
   }
-  decode_tc_kernel<KW><<<grid, DT_THREADS, smem, st>>>(a);
+  const int grid = ntiles < dp_sm_count() ? ntiles : dp_sm_count();
+  decode_tc_kernel<KW><<<grid, DP_THREADS, smem, st>>>(a, tO);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
@@ -465,7 +635,7 @@ jolt_status decode_tc_run(int U, const jolt_blob_desc* desc, const char* blob, s
     DecTcArgs a;
     memset(&a, 0, sizeof(a));
     a.H = H; a.T = T; a.out_dtype = out_dtype; a.u0 = u0; a.blob = blob; a.stride = stride;
-    a.xhat = xhat;
+    a.xhat = xhat; a.nu = nu;
     int kmax = 0;
     for (int i = 0; i < nu; ++i) {
       const jolt_blob_desc& d = desc[u0 + i];
@@ -475,10 +645,34 @@ jolt_status decode_tc_run(int U, const jolt_blob_desc* desc, const char* blob, s
       if (d.rT < T) kmax = kmax > d.rT ? kmax : d.rT;
       if (d.rd < DT_D) kmax = kmax > d.rd ? kmax : d.rd;
     }
-    const dim3 grid((T + DT_ROWS - 1) / DT_ROWS, H, nu);
-    const jolt_status s = kmax <= 32 ? launch_dtc<32>(grid, a, st) : launch_dtc<64>(grid, a, st);
+    const int ntiles = nu * H * ((T + DT_ROWS - 1) / DT_ROWS);
+    // bf16 output by TMA stores: a map over every unit's rows
+    CUtensorMap tO;
+    memset(&tO, 0, sizeof(tO));
+    if (out_dtype == JOLT_BF16 && kmax <= 32) {
+      const cuuint64_t dO[3] = {DT_D, (cuuint64_t)T, (cuuint64_t)U * H};
+      const cuuint64_t sO[2] = {DT_D * 2, (cuuint64_t)T * DT_D * 2};
+      const cuuint32_t bO[3] = {64, DT_ROWS, 1};
+      if (!tc::make_map(&tO, xhat, 3, dO, sO, bO)) return JOLT_ERR_CUDA;
+    }
+    const jolt_status s =
+        kmax <= 32 ? launch_dtc<32>(ntiles, a, tO, st) : launch_dtc<64>(ntiles, a, tO, st);
     if (s != JOLT_OK) return s;
   }
+  return JOLT_OK;
+}
+
+// The decoder's status word: ST_* bits of bounded waits that gave up since
+// the last read (which clears it).
+jolt_status decode_tc_status(int* out, cudaStream_t st) {
+  JOLT_CUDA_TRY(cudaStreamSynchronize(st));
+  int v = 0;
+  JOLT_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(int)));
+  if (v) {
+    const int zero = 0;
+    JOLT_CUDA_TRY(cudaMemcpyToSymbol(g_decode_status, &zero, sizeof(int)));
+  }
+  *out = v;
   return JOLT_OK;
 }
 

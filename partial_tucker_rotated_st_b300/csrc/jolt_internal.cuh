@@ -215,6 +215,7 @@ jolt_status encode_run(const Layout& L, int n_units, const void* X, const int8_t
 jolt_status decode_run(int n_units, const jolt_blob_desc* desc, const char* blob,
                        size_t blob_stride, void* xhat, int out_dtype, cudaStream_t st);
 bool decode_tc_supported(int D);
+jolt_status decode_tc_status(int* out, cudaStream_t st);
 jolt_status decode_tc_run(int n_units, const jolt_blob_desc* desc, const char* blob,
                           size_t blob_stride, void* xhat, int out_dtype, cudaStream_t st);
 size_t admit_ws_unit_bytes(int H, int tau, int D);

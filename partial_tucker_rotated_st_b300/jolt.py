@@ -103,6 +103,7 @@ _SIG = {
                                                      _P, _P, ctypes.c_size_t, _P, _P, _P]),
     "jolt_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "jolt_read_status": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P, _P]),
+    "jolt_decode_status": (ctypes.c_int, [_P]),
     "jolt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "jolt_launch_count": (ctypes.c_uint64, []),
 }
@@ -302,6 +303,12 @@ def jolt_decode(desc: Sequence[JoltBlobDesc], blob, blob_stride, xhat, out_dtype
     arr = (JoltBlobDesc * n)(*desc)
     _check("jolt_decode", lib().jolt_decode(n, arr, _ptr(blob), blob_stride, _ptr(xhat),
                                             out_dtype, _stream(stream)))
+
+
+def jolt_decode_status(stream=None) -> int:
+    """Synchronises and returns the decoder's device status code (not
+    raised): ERR_CUDA when a bounded wait of a decode gave up."""
+    return lib().jolt_decode_status(_stream(stream))
 
 
 def jolt_attend_workspace_size(n_groups, H, T, D, nq) -> int:
