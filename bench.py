@@ -31,6 +31,7 @@ barriers and the slowest rank's time is reported.
 from __future__ import annotations
 
 import argparse
+import glob
 import hashlib
 import json
 import multiprocessing as mp
@@ -198,23 +199,32 @@ class single_threaded_children:
                 os.environ[k] = v
 
 
+def workload(name, groups=0):
+    """The named workload, or the same shapes and generator with only its
+    first `groups` layer groups (a smaller batch of identical units, for
+    profiling runs)."""
+    if groups:
+        return kvgen.custom_workload(name, n_groups=groups)
+    return kvgen.WORKLOADS[name]
+
+
 def _gen_unit(task):
-    name, u = task
-    w = kvgen.WORKLOADS[name]
+    name, groups, u = task
+    w = workload(name, groups)
     x = kvgen.make_unit(w, u)
     s = kvgen.make_signs(w, u)
     sk = kvgen.make_sketch(w, u) if w.token_mode == "randomized" else None
     return name, u, x, s, sk
 
 
-def gen_inputs(names, procs=None):
+def gen_inputs(names, procs=None, groups=0):
     """Host inputs of every unit of each named workload, generated by a pool
     of spawned processes (before any CUDA call of this process):
     {name: (list of stored unit arrays, signs [U][D], sketch [U][H][D][ell] or None)}."""
-    tasks = [(n, u) for n in names for u in range(kvgen.WORKLOADS[n].n_units)]
+    nu = {n: workload(n, groups).n_units for n in names}
+    tasks = [(n, groups, u) for n in names for u in range(nu[n])]
     procs = max(1, min(procs or (os.cpu_count() or 1), len(tasks)))
-    out = {n: ([None] * kvgen.WORKLOADS[n].n_units, [None] * kvgen.WORKLOADS[n].n_units,
-               [None] * kvgen.WORKLOADS[n].n_units) for n in names}
+    out = {n: ([None] * nu[n], [None] * nu[n], [None] * nu[n]) for n in names}
     if procs == 1:
         results = map(_gen_unit, tasks)
     else:
@@ -488,11 +498,11 @@ def blob_bytes_of(desc):
     return sum(int(d.bytes) for d in desc)
 
 
-def decode_roofline(w, desc, dec_t, hbm, name_for_traffic):
+def decode_roofline(w, desc, dec_t, hbm):
     alg = blob_bytes_of(desc) + 2 * w.elems_per_unit * w.n_units
     return {"kernel": "decode_tc_kernel", "bound": "hbm", "achieved": alg / dec_t / 1e9,
             "peak": hbm, "unit": "GB/s", "frac": alg / dec_t / 1e9 / hbm,
-            "bytes_algorithmic": int(alg), "traffic": decode_traffic(name_for_traffic)}
+            "bytes_algorithmic": int(alg), "traffic": decode_traffic(w)}
 
 
 def config_record(run, res, hbm, kind, pk, sms):
@@ -508,7 +518,7 @@ def config_record(run, res, hbm, kind, pk, sms):
             "decode_output": f"bf16 [{w.n_units}][{w.H}][{w.T}][{w.D}]",
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "sweep_roofline": roofline(w, res["sweep_kernel_s"], hbm, kind, pk, sms),
-            "decode_roofline": decode_roofline(w, res["desc"], per["decode"], hbm, w.name),
+            "decode_roofline": decode_roofline(w, res["desc"], per["decode"], hbm),
             "gpu_launches": res["launches"]}
 
 
@@ -516,7 +526,7 @@ def run_ours(args):
     import torch
     ws, rank, local = dist_env()
     names = [args.workload] + [c for c in args.configs if c != args.workload]
-    host = gen_inputs(names, max(1, (os.cpu_count() or 1) // ws))   # before any CUDA call
+    host = gen_inputs(names, max(1, (os.cpu_count() or 1) // ws), args.groups)   # before any CUDA call
     ws, rank, local = init_dist("nccl")
     torch.cuda.set_device(local)
     from partial_tucker_rotated_st_b300 import build as jbuild
@@ -529,7 +539,7 @@ def run_ours(args):
     st = torch.cuda.current_stream()
 
     # ---- the line's workload
-    w = kvgen.WORKLOADS[args.workload]
+    w = workload(args.workload, args.groups)
     run = Run(w, host.pop(args.workload))
     torch.cuda.synchronize()
     barrier(ws)
@@ -585,12 +595,14 @@ def run_ours(args):
                        "budget_bytes": w.budget_bytes, "token_mode": w.token_mode,
                        "allocator": "lambda bisection + greedy swaps",
                        "l2": "flushed between steps (256 MiB write)",
-                       "parallelism": f"replicas{ws}"},
+                       "parallelism": f"replicas{ws}",
+                       **({"groups": args.groups} if args.groups else {})},
             "decode": {"value": dec_gbs, "unit": "GB/s",
-                       "roofline": decode_roofline(w, desc, dec_t, hbm, args.workload)},
+                       "roofline": decode_roofline(w, desc, dec_t, hbm)},
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "dominant_stage": dom,
             "factor": fac,
+            "gram_tensor": gram_tensor_record(w),
             "wall_ms_per_step": 1e3 * res["wall_s"],
             "roofline": roof,
             "e2e": e2e,
@@ -608,7 +620,7 @@ def run_ours(args):
     for name in args.configs:
         if name == args.workload:
             continue
-        wx = kvgen.WORKLOADS[name]
+        wx = workload(name, args.groups)
         rx = Run(wx, host.pop(name))
         resx = timed_steps(rx, args.steps, args.warmup, flush, st)
         recs[name] = config_record(rx, resx, hbm, kind, pk, sms)
@@ -622,8 +634,7 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-SWEEP_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "gram_tc.cu")
-SWEEP_PROFILE = os.path.join(ROOT, "profiles", "sweep_tc_kernel_mistral_t1024.md")
+SWEEP_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "sweep_tc.cu")
 
 
 def attention_bench(args, w, desc, enc, flush, st, hbm, hbm_kind, nq=4):
@@ -684,7 +695,7 @@ def attention_bench(args, w, desc, enc, flush, st, hbm, hbm_kind, nq=4):
             "launches_per_call": int(launches),
             "roofline": {"kernel": "attend_prep + attend_chunk + attend_merge (one call)",
                          "bound": "hbm", "achieved": alg / t / 1e9, "peak": hbm, "unit": "GB/s",
-                         "frac": alg / t / 1e9 / hbm, "traffic": attend_traffic(w.name),
+                         "frac": alg / t / 1e9 / hbm, "traffic": attend_traffic(w),
                          "bytes_algorithmic": int(alg), "peak_kind": hbm_kind},
             "materialize_then_sdpa_ms": 1e3 * tm,
             "speedup_vs_materialize": tm / t}
@@ -787,47 +798,78 @@ def modeled_allocator(args, w, enc, X, K, S, budget, in_bytes, flush, st, ws):
             "bytes_measured_choice": int(cm[idx, zm].sum())}
 
 
-ATTEND_PROFILE = os.path.join(ROOT, "profiles", "attend_chunk_kernel_mistral_t1024.md")
 ATTEND_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "attend.cu")
-DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_tc_kernel_mistral_t1024.md")
 DECODE_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "decode_tc.cu")
+GRAM_SRC = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc", "gram_tc.cu")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
-def traffic_record(profile, src_path, hash_key, bytes_key, workload):
-    """The DRAM bytes recorded on a `traffic_record:` line of a committed ncu
-    summary for this workload, only while the kernel source still hashes to
-    the sha256 prefix recorded beside them; else None (the counters belong to
-    another kernel source or workload)."""
+def _sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def profile_records(kind, src_path, workload, profiles_dir=PROFILES):
+    """The `<kind>:` JSON lines of the committed ncu summaries under profiles/
+    for this workload whose `src_sha256` still matches the kernel source
+    (counters of another source or workload are not this kernel's)."""
     try:
-        txt = open(profile).read()
-        src = hashlib.sha256(open(src_path, "rb").read()).hexdigest()[:16]
+        src = _sha(src_path)
+        files = sorted(glob.glob(os.path.join(profiles_dir, "*.md")))
     except OSError:
-        return None
-    for line in txt.splitlines():
-        if not line.startswith("traffic_record:"):
+        return []
+    out = []
+    for f in files:
+        for line in open(f).read().splitlines():
+            if not line.startswith(kind + ":"):
+                continue
+            rec = json.loads(line.split(":", 1)[1])
+            if rec.get("src_sha256") == src and rec.get("workload") == workload:
+                rec["source"] = os.path.relpath(f, os.path.dirname(profiles_dir))
+                out.append(rec)
+    return out
+
+
+def traffic_record(kernel, src_path, bytes_key, w, profiles_dir=PROFILES):
+    """DRAM bytes per launch of `kernel` on workload w from a committed ncu
+    capture: the figure as recorded when the capture ran all w.n_units units,
+    else scaled by the units processed (the kernels read each unit's data a
+    fixed number of times, so traffic grows in proportion); None if no
+    capture of the current source exists."""
+    for rec in profile_records("traffic_record", src_path, w.name, profiles_dir):
+        if rec.get("kernel") != kernel:
             continue
-        rec = json.loads(line.split(":", 1)[1])
-        if rec.get(hash_key) == src and rec.get("workload") == workload:
-            return int(rec[bytes_key])
+        units = int(rec.get("units", w.n_units))
+        return int(round(int(rec[bytes_key]) * w.n_units / units))
     return None
 
 
-def decode_traffic(workload):
+def decode_traffic(w):
     """DRAM bytes of one decoder launch."""
-    return traffic_record(DECODE_PROFILE, DECODE_SRC, "decode_src_sha256",
-                          "dram_bytes_per_launch", workload)
+    return traffic_record("decode_tc_kernel", DECODE_SRC, "dram_bytes_per_launch", w)
 
 
-def attend_traffic(workload):
+def attend_traffic(w):
     """DRAM bytes of one jolt_attend call (its three kernels)."""
-    return traffic_record(ATTEND_PROFILE, ATTEND_SRC, "attend_src_sha256",
-                          "dram_bytes_per_call", workload)
+    return traffic_record("attend", ATTEND_SRC, "dram_bytes_per_call", w)
 
 
-def sweep_traffic(workload):
+def sweep_traffic(w):
     """DRAM bytes of one sweep-kernel launch."""
-    return traffic_record(SWEEP_PROFILE, SWEEP_SRC, "sweep_src_sha256",
-                          "dram_bytes_per_launch", workload)
+    return traffic_record("sweep_tc_kernel", SWEEP_SRC, "dram_bytes_per_launch", w)
+
+
+def gram_tensor_record(w):
+    """Tensor-pipe activity of the factor step's tcgen05 products (the feature
+    and token Grams, the subspace-iteration product, the projection and the
+    cores) from a committed ncu capture of the current sources, keyed by
+    kernel; {} when none matches."""
+    out = {}
+    for src in (GRAM_SRC, os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc",
+                                       "proj_tc.cu")):
+        for rec in profile_records("tensor_record", src, w.name):
+            out[rec["kernel"]] = {k: v for k, v in rec.items()
+                                  if k not in ("kernel", "workload", "src_sha256")}
+    return out
 
 
 def roofline(w, kernel_s, hbm, kind, pk, sms=148):
@@ -855,7 +897,7 @@ def roofline(w, kernel_s, hbm, kind, pk, sms=148):
     ach = flops / kernel_s / 1e12
     hbm_ach = 2.0 * N * U / kernel_s / 1e9
     return {"kernel": "sweep_tc_kernel", "bound": "alu", "achieved": ach, "peak": peak,
-            "unit": "TFLOP/s", "frac": ach / peak, "traffic": sweep_traffic(w.name),
+            "unit": "TFLOP/s", "frac": ach / peak, "traffic": sweep_traffic(w),
             "kernel_ms": 1e3 * kernel_s,
             "peak_source": f"derived: FP32 pipe, {sms} SMs (device) x 128 lanes x 2 flop x "
                            f"max SM clock",
@@ -885,6 +927,8 @@ def main():
     ap.add_argument("--configs", default=",".join(EXTRA_CONFIGS),
                     help="comma-separated workloads with a record of their own, or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="run only the first N layer groups of each workload (profiling runs)")
     args = ap.parse_args()
     args.configs = parse_configs(args.configs)
     if args.impl == "reference":

@@ -29,6 +29,12 @@
  *     No kernel traps or asserts.
  *   - Random draws of the method (the rotation's sign vector and the
  *     FlashJoLT Gaussian sketch) are inputs, never generated inside.
+ *   - One GPU per process: kernels that need more than 48 KB of dynamic
+ *     shared memory have their limit raised (cudaFuncSetAttribute) once per
+ *     process, on the device current at the first call, and the attribute
+ *     holds for that device only.  Drive the library from one device per
+ *     process (the usual one-rank-per-GPU launch); a call on a second device
+ *     of the same process may fail with JOLT_ERR_CUDA.
  */
 #ifndef JOLT_H
 #define JOLT_H
@@ -230,6 +236,18 @@ jolt_status jolt_set_sweep_events(void* start, void* stop);
 jolt_status jolt_set_factor_events(void* const* events);
 
 /*
+ * Iteration caps of the factor step's eigensolvers, for exercising the
+ * non-convergence path: `max_sweeps` bounds the sweeps of every Jacobi solve
+ * (feature Gram, token Gram, Rayleigh-Ritz blocks; default 40) and
+ * `max_subspace_blocks` the blocks of the exact token mode's subspace
+ * iteration (default 25).  0 restores a default; negative values return
+ * JOLT_ERR_INVALID and change nothing.  A solve that reaches its cap sets the
+ * unit's status, and jolt_read_status then returns JOLT_ERR_NOCONVERGE.
+ * Process-wide setting read at launch time, not thread-safe.
+ */
+jolt_status jolt_set_solver_limits(int max_sweeps, int max_subspace_blocks);
+
+/*
  * Modeled-error distortion table, an alternative to jolt_sweep_candidates
  * that needs no pass over X ["A JoLT for the KV cache" verdict page, referee
  * report on Section 4, Eq. (2): e ~ eps^2(b) tau; P5 Methodology 4: tail-mass
@@ -371,9 +389,16 @@ jolt_status jolt_admit(int n_units, const jolt_blob_desc* desc_in, const void* b
  *     allocated.  A batch needs n_units * ceil(T / (8192 / D)) * H *
  *     (n_cand + 1) * 4 bytes of it; a larger batch returns
  *     JOLT_ERR_TOO_LARGE before any launch (split it into smaller batches).
+ *     The bound counts the SIMT kernel's 8192 / D-row tiles for every path;
+ *     the tensor-core sweep (bf16, D = 128) writes 128-row tiles at the same
+ *     stride, so there the bound is conservative by a factor of two.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
+ *   - One device per process: the kernels' shared-memory limits are raised
+ *     once per process (see the note at the top of this file), so although
+ *     the array address is kept per device, use this call from one GPU per
+ *     process.
  *   - Sharing: every call on a device uses the same array.  Calls that
  *     overlap on the GPU (different streams, no ordering between them) race
  *     on it; order them on one stream or with events.  Every entry a call

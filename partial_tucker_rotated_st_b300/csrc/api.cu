@@ -139,6 +139,14 @@ jolt_status make_layout(const jolt_config* cfg, Layout* Lp) {
   L.o_UT32 = sect((size_t)L.nd * T * RT * 4);
   L.o_UT16 = sect((size_t)L.nd * T * RT * 2);
   L.o_tokev = sect((size_t)L.nd * RT * 4);
+  L.o_cap = sect((size_t)L.nd * RT * 8);
+  {
+    const bool fl = RT > 0 && L.token_mode == JOLT_TOKEN_RANDOMIZED && L.dtype == JOLT_BF16 &&
+                    D == 128;
+    L.o_Bx = fl ? sect((size_t)H * 512 * D * 2) : 0;
+    L.o_Qs = fl ? sect((size_t)T * 512 * 2) : 0;
+    L.o_C = fl ? sect((size_t)H * D * 160 * 4) : 0;
+  }
   L.o_G32 = sect((size_t)L.nd * H * RT * D * 4);
   L.o_G16 = sect((size_t)L.nd * H * RT * D * 2);
   // rotated chain rows of the sweep; the encoder reuses the first two slots
@@ -245,6 +253,13 @@ jolt_status jolt_set_sweep_events(void* start, void* stop) {
 
 jolt_status jolt_set_factor_events(void* const* events) {
   for (int i = 0; i < 5; ++i) g_factor_ev[i] = events ? events[i] : nullptr;
+  return JOLT_OK;
+}
+
+jolt_status jolt_set_solver_limits(int max_sweeps, int max_subspace_blocks) {
+  if (max_sweeps < 0 || max_subspace_blocks < 0) return JOLT_ERR_INVALID;
+  set_max_sweeps(max_sweeps);
+  set_subspace_blocks(max_subspace_blocks);
   return JOLT_OK;
 }
 

@@ -9,6 +9,7 @@
 // ends the solve.  The matrix and the accumulated rotations live in shared
 // memory (fp32).
 #include "jolt_internal.cuh"
+#include "chol_smem.cuh"
 
 namespace jolt {
 
@@ -16,6 +17,7 @@ namespace {
 
 constexpr int JAC_THREADS = 1024;   // viewed as 32 x 32 (ty, tx)
 constexpr int JAC_MAX_SWEEPS = 40;
+int g_max_sweeps = JAC_MAX_SWEEPS;   // sweep cap of every Jacobi solve (host-settable)
 constexpr float JAC_TOL = 1e-6f;    // relative: |a_pq| vs sqrt(|a_pp a_qq|)
 constexpr float FEAT_TOL = 4e-6f;   // one-sided: |b_p . b_q| vs |b_p| |b_q| (fp32 dot products)
 // absolute floors vs ||A||_F: JAC_ABS_EXACT for solves whose small
@@ -26,7 +28,7 @@ __global__ void __launch_bounds__(JAC_THREADS, 1)
 jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int nparts,
               long long part_s, float* __restrict__ evals, long long e_bs,
               float* __restrict__ evecs, long long v_bs, int ldv, int ncols_out, int* status,
-              long long s_bs, const int* skip, long long sk_s, float abs_tol) {
+              long long s_bs, const int* skip, long long sk_s, float abs_tol, int max_sweeps) {
   const int bidx = blockIdx.x;
   if (skip && skip[bidx * sk_s]) return;
   extern __shared__ float sm[];
@@ -65,7 +67,7 @@ jacobi_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int
 
   bool converged = false;
   int sweep = 0;
-  for (; sweep < JAC_MAX_SWEEPS; ++sweep) {
+  for (; sweep < max_sweeps; ++sweep) {
     int rotated = 0;
     for (int r = 0; r < m - 1; ++r) {
       if (t < half) {
@@ -186,7 +188,8 @@ __global__ void __launch_bounds__(1024, 1)
 jacobi_bl_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, int nparts,
                  long long part_s, float* __restrict__ evals, long long e_bs,
                  float* __restrict__ evecs, long long v_bs, int ldv, int ncols_out, int* status,
-                 long long s_bs, const int* skip, long long sk_s, float abs_tol) {
+                 long long s_bs, const int* skip, long long sk_s, float abs_tol,
+                 int max_sweeps) {
   const int bidx = blockIdx.x;
   if (skip && skip[bidx * sk_s]) return;
   const int m = n + (n & 1);      // even size; a padded index stays zero
@@ -256,7 +259,7 @@ jacobi_bl_kernel(const float* __restrict__ Ain, long long a_bs, int lda, int n, 
 
   bool converged = false;
   int sweep = 0;
-  for (; sweep < JAC_MAX_SWEEPS; ++sweep) {
+  for (; sweep < max_sweeps; ++sweep) {
     int rotated = 0;
     for (int r = 0; r < m - 1; ++r) {
       // 1. rotations of the pairs, from the diagonal blocks
@@ -458,9 +461,8 @@ __global__ void __launch_bounds__(256)
 chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long long part_s,
                 float* __restrict__ Rinv, long long r_bs, int* status, long long s_bs,
                 const int* skip, long long sk_s, float shift) {
-  constexpr int NB = 8, NBLK = N / NB, NT = 256;
+  constexpr int NT = 256;
   constexpr int LD = N + 1;
-  static_assert(N % NB == 0 && N <= 64, "block size");
   const int u = blockIdx.x;
   if (skip && skip[u * sk_s]) return;
   __shared__ float S[N * LD];    // the Gram, then L' (lower)
@@ -468,7 +470,7 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
   __shared__ float rds[N];
   __shared__ float rpiv[N];      // 1 / L'_jj
   __shared__ int bad;
-  const int t = threadIdx.x, lane = t & 31, tx = t & 31, ty = t >> 5;
+  const int t = threadIdx.x;
   const float* Gg = G + u * g_bs;
   if (t == 0) bad = 0;
   {
@@ -488,126 +490,7 @@ chol_inv_kernel(const float* __restrict__ G, long long g_bs, int nparts, long lo
       if (e < N * N) X[(e / N) * LD + e % N] = (g[0][i] + g[1][i]) + (g[2][i] + g[3][i]);  // raw Gram, staged in X
     }
   }
-  __syncthreads();
-  if (t < N) {
-    const float d = X[t * LD + t];
-    rds[t] = d > 0.f ? rsqrtf(d) : 0.f;
-  }
-  __syncthreads();
-  // S' = D^-1 sym(G) D^-1 (+ shift on the diagonal), lower triangle
-  for (int e = t; e < N * N; e += NT) {
-    const int i = e / N, k = e % N;
-    if (k <= i) {
-      float v = 0.5f * (X[i * LD + k] + X[k * LD + i]) * rds[i] * rds[k];
-      if (k == i && rds[i] > 0.f) v += shift;
-      S[i * LD + k] = v;
-    }
-  }
-  __syncthreads();
-  for (int kb = 0; kb < NBLK; ++kb) {
-    const int c0 = kb * NB, c1 = c0 + NB;
-    // (a) diagonal block, warp 0: lane r < 8 holds row c0 + r
-    if (t < 32) {
-      float a[NB];
-#pragma unroll
-      for (int m = 0; m < NB; ++m) a[m] = (lane < NB && m <= lane) ? S[(c0 + lane) * LD + c0 + m] : 0.f;
-#pragma unroll
-      for (int j = 0; j < NB; ++j) {
-        float d = __shfl_sync(0xffffffffu, a[j], j);
-        if (!(d >= 0.f)) { if (lane == 0) bad = 1; d = 0.f; }
-        const float rp = d > 0.f ? rsqrtf(d) : 0.f;
-        if (lane == j) { a[j] = d * rp; rpiv[c0 + j] = rp; }
-        else if (lane > j) a[j] *= rp;
-#pragma unroll
-        for (int m = j + 1; m < NB; ++m) {
-          const float lm = __shfl_sync(0xffffffffu, a[j], m);
-          if (lane >= m && lane < NB) a[m] = fmaf(-a[j], lm, a[m]);
-        }
-      }
-      if (lane < NB)
-#pragma unroll
-        for (int m = 0; m < NB; ++m)
-          if (m <= lane) S[(c0 + lane) * LD + c0 + m] = a[m];
-    }
-    __syncthreads();
-    if (c1 >= N) break;
-    // (b) panel: row i solves x L11^T = a, x_m = (a_m - sum_{q<m} x_q L11[m][q]) / L11[m][m]
-    for (int i = c1 + t; i < N; i += NT) {
-      float x[NB];
-#pragma unroll
-      for (int m = 0; m < NB; ++m) {
-        float v = S[i * LD + c0 + m];
-#pragma unroll
-        for (int q = 0; q < m; ++q) v = fmaf(-x[q], S[(c0 + m) * LD + c0 + q], v);
-        x[m] = v * rpiv[c0 + m];
-      }
-#pragma unroll
-      for (int m = 0; m < NB; ++m) S[i * LD + c0 + m] = x[m];
-    }
-    __syncthreads();
-    // (c) trailing update of the lower triangle: a_ik -= sum_m L[i][c0+m] L[k][c0+m]
-    for (int i = c1 + ty; i < N; i += NT / 32) {
-      float li[NB];
-#pragma unroll
-      for (int m = 0; m < NB; ++m) li[m] = S[i * LD + c0 + m];
-      for (int k = c1 + tx; k <= i; k += 32) {
-        float v = S[i * LD + k];
-#pragma unroll
-        for (int m = 0; m < NB; ++m) v = fmaf(-li[m], S[k * LD + c0 + m], v);
-        S[i * LD + k] = v;
-      }
-    }
-    __syncthreads();
-  }
-  // X = L'^{-1}: diagonal blocks first, row r of block kb by substitution
-  // (x L_kk = e_r: x_r = 1 / L_rr, x_j = -(sum_{m=j+1}^{r} x_m L_mj) / L_jj)
-  if (t < N) {
-    const int kb = t / NB, r = t % NB, c0 = kb * NB;
-    float x[NB];
-#pragma unroll
-    for (int j = NB - 1; j >= 0; --j) {
-      float v = 0.f;
-      if (j == r) v = rpiv[c0 + r];
-      else if (j < r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int m = j + 1; m < NB; ++m)
-          if (m <= r) acc = fmaf(x[m], S[(c0 + m) * LD + c0 + j], acc);
-        v = -acc * rpiv[c0 + j];
-      }
-      x[j] = v;
-    }
-#pragma unroll
-    for (int j = 0; j < NB; ++j) X[(c0 + r) * LD + c0 + j] = x[j];
-  }
-  __syncthreads();
-  // off-diagonal blocks, one block diagonal d = i - k at a time:
-  // P_ik = sum_{m=k}^{i-1} L_im X_mk (into the upper triangle of X as scratch),
-  // then X_ik = -X_ii P_ik
-  for (int d = 1; d < NBLK; ++d) {
-    const int nblk = NBLK - d;
-    for (int e = t; e < nblk * NB * NB; e += NT) {
-      const int k = e / (NB * NB), rc = e % (NB * NB), r = rc / NB, c = rc % NB;
-      const int i = k + d;
-      const int row = i * NB + r, col = k * NB + c;
-      float acc = 0.f;
-      for (int m = k * NB + c; m < i * NB; ++m)   // X_mk is zero above its diagonal
-        acc = fmaf(S[row * LD + m], X[m * LD + col], acc);
-      X[col * LD + row] = acc;                     // P^T, upper triangle
-    }
-    __syncthreads();
-    for (int e = t; e < nblk * NB * NB; e += NT) {
-      const int k = e / (NB * NB), rc = e % (NB * NB), r = rc / NB, c = rc % NB;
-      const int i = k + d;
-      const int row = i * NB + r, col = k * NB + c;
-      float acc = 0.f;
-#pragma unroll
-      for (int q = 0; q < NB; ++q)
-        if (q <= r) acc = fmaf(X[row * LD + i * NB + q], X[col * LD + i * NB + q], acc);
-      X[row * LD + col] = -acc;
-    }
-    __syncthreads();
-  }
+  chol_inv_smem<N>(S, X, rds, rpiv, &bad, shift);
   // R^{-1}[k][r] = X[r][k] / s_k
   float* Rg = Rinv + u * r_bs;
   for (int e = t; e < N * N; e += NT) {
@@ -713,7 +596,8 @@ __global__ void __launch_bounds__(8 * N, 1)
 sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, long long part_s,
                float* __restrict__ evals, long long e_bs, float* __restrict__ evecs,
                long long v_bs, int ldv, int ncols_out, int* status, long long st_bs, int* done,
-               long long d_bs, const int* skip, long long sk_s, float tol, float abs_tol) {
+               long long d_bs, const int* skip, long long sk_s, float tol, float abs_tol,
+               int max_sweeps) {
   constexpr int NT = 8 * N;
   constexpr int TY = NT / 32;   // thread rows of the Cholesky update
   constexpr int RPT = N / 16;   // Jacobi rows per thread
@@ -831,7 +715,23 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
   const int k = t >> 4, l16 = t & 15;
   bool converged = false;
   int sweep = 0;
-  for (; sweep < 40; ++sweep) {
+  for (; sweep < max_sweeps; ++sweep) {
+    // exact squared column norms at the start of every sweep (group k: columns
+    // 2k and 2k + 1); each rotation then updates the pair's norms by
+    // |b_p'|^2 = |b_p|^2 - t g, |b_q'|^2 = |b_q|^2 + t g (t = tan of the
+    // angle), so a round computes only the cross product g
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      float v[RPT];
+      ld_rows<RPT>(M + (2 * k + cc) * LDM, l16, v);
+      float s2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) s2 = fmaf(v[i], v[i], s2);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      if (l16 == 0) lam[2 * k + cc] = s2;
+    }
+    __syncthreads();
     int rot = 0;
     for (int r = 0; r < N - 1; ++r) {
       int p, q;
@@ -843,19 +743,16 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
       float cp[RPT], cq[RPT];
       ld_rows<RPT>(M + p * LDM, l16, cp);
       ld_rows<RPT>(M + q * LDM, l16, cq);
-      float a = 0.f, b = 0.f, g = 0.f;
+      float g0 = 0.f, g1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < RPT; ++i) {
-        a = fmaf(cp[i], cp[i], a);
-        b = fmaf(cq[i], cq[i], b);
-        g = fmaf(cp[i], cq[i], g);
+      for (int i = 0; i < RPT; i += 2) {
+        g0 = fmaf(cp[i], cq[i], g0);
+        if (i + 1 < RPT) g1 = fmaf(cp[i + 1], cq[i + 1], g1);
       }
+      float g = g0 + g1;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
-        g += __shfl_xor_sync(0xffffffffu, g, o);
-      }
+      for (int o = 8; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+      const float a = lam[p], b = lam[q];
       if (fabsf(g) > tol * sqrtf(a * b) && fabsf(g) > floor_abs) {
         // rotation parameters with the approximate (few-ulp) intrinsics: an
         // angle off by an ulp only leaves a residue for the next sweep, and
@@ -871,6 +768,10 @@ sym_eig_kernel(const TIn* __restrict__ G, long long g_bs, int lda, int nparts, l
         }
         st_rows<RPT>(M + p * LDM, l16, np_);
         st_rows<RPT>(M + q * LDM, l16, nq_);
+        if (l16 == 0) {
+          lam[p] = fmaf(-tt, g, a);
+          lam[q] = fmaf(tt, g, b);
+        }
         rot = 1;
       }
       __syncthreads();
@@ -973,7 +874,8 @@ jolt_status launch_jacobi(const float* A, long long a_bs, int lda, int n, int np
     }
     jacobi_bl_kernel<1><<<batch, 1024, smem, st>>>(A, a_bs, lda, n, nparts < 1 ? 1 : nparts,
                                                    part_s, evals, e_bs, evecs, v_bs, ldv,
-                                                   ncols_out, status, s_bs, skip, sk_s, abs_tol);
+                                                   ncols_out, status, s_bs, skip, sk_s, abs_tol,
+                                                   g_max_sweeps);
     JOLT_LAUNCH_CHECK();
     return JOLT_OK;
   }
@@ -988,7 +890,7 @@ jolt_status launch_jacobi(const float* A, long long a_bs, int lda, int n, int np
   }
   jacobi_kernel<<<batch, JAC_THREADS, smem, st>>>(A, a_bs, lda, n, nparts < 1 ? 1 : nparts, part_s,
                                                   evals, e_bs, evecs, v_bs, ldv, ncols_out, status,
-                                                  s_bs, skip, sk_s, abs_tol);
+                                                  s_bs, skip, sk_s, abs_tol, g_max_sweeps);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
@@ -1053,7 +955,7 @@ jolt_status launch_sym_eig(const void* G, bool f64_in, long long g_bs, int lda, 
     JOLT_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     kern<<<batch, 8 * N, smem, st>>>(gp, g_bs, lda, nparts, part_s, evals, e_bs, evecs, v_bs, ldv,
                                      ncols_out, status, st_bs, done, d_bs, skip, sk_s, FEAT_TOL,
-                                     abs_tol);
+                                     abs_tol, g_max_sweeps);
     JOLT_LAUNCH_CHECK();
     return JOLT_OK;
   };
@@ -1083,5 +985,7 @@ jolt_status launch_trsm_rows(const float* In, float* Out, long long blk_bs, cons
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }
+
+void set_max_sweeps(int n) { g_max_sweeps = n > 0 ? n : JAC_MAX_SWEEPS; }
 
 }  // namespace jolt

@@ -37,6 +37,7 @@ namespace {
 constexpr int SUB_STEPS = 5;        // power steps between Rayleigh-Ritz checks
 constexpr float SUB_SHIFT = 1e-5f;  // shift of the equilibrated first CholeskyQR pass (f32)
 constexpr int SUB_MAX_BLOCKS = 25;
+int g_sub_blocks = SUB_MAX_BLOCKS;   // subspace-iteration block cap (host-settable)
 constexpr float RITZ_TOL_REL = 1e-4f;
 constexpr float RITZ_TOL_ABS = 1e-5f;
 
@@ -194,7 +195,7 @@ __global__ void warm_copy_kernel(char* pbase, size_t pb, size_t o_V, int ndt, co
 __global__ void scatter_problems_kernel(char* ws, size_t ub, size_t o_UT, size_t o_ev,
                                         size_t o_status, const char* pbase, size_t pb,
                                         size_t p_UT, size_t p_ev, int ev_ld, size_t p_status,
-                                        int U, int ndt, int T, int RT) {
+                                        int U, int ndt, int T, int RT, size_t o_cap) {
   const int id = blockIdx.y, u = blockIdx.z;
   const int p = id < ndt ? u * ndt + id : U * ndt + u;
   const char* pr = pbase + (size_t)p * pb;
@@ -206,13 +207,38 @@ __global__ void scatter_problems_kernel(char* ws, size_t ub, size_t o_UT, size_t
        e += (long long)gridDim.x * blockDim.x)
     dst[e] = src[e];
   if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < RT; i += blockDim.x)
+    for (int i = threadIdx.x; i < RT; i += blockDim.x) {
       ((float*)(un + o_ev))[id * RT + i] = ((const float*)(pr + p_ev))[i * ev_ld];
+      ((double*)(un + o_cap))[id * RT + i] = 0.0;   // the cores stage adds into it
+    }
     if (threadIdx.x == 0) {
       const int sv = *(const int*)(pr + p_status);
       if (sv) atomicOr((int*)(un + o_status), sv);
     }
   }
+}
+
+// Captured energy of the unrounded cores, cap[id][j] = sum over h and i < r_d
+// of G(r_d)[h][j][i]^2 in f64 (one warp per (rank, j)), from the fp32 cores
+// G32[id][h][j][i] (row stride r_d).
+struct RdList { int rd[JOLT_MAX_GRID]; };
+__global__ void cap_g32_kernel(char* ws, size_t ub, size_t o_G32, size_t o_cap, int H, int RT,
+                               int D, int nd, RdList rl) {
+  const int u = blockIdx.y;
+  char* un = ws + (size_t)u * ub;
+  const int lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (w >= nd * RT) return;
+  const int id = w / RT, j = w % RT, rd = rl.rd[id];
+  const float* G = (const float*)(un + o_G32) + (size_t)id * H * RT * D;
+  double s = 0.0;
+  for (int e = lane; e < H * rd; e += 32) {
+    const int h = e / rd, i = e % rd;
+    const double g = G[((size_t)h * RT + j) * rd + i];
+    s += g * g;
+  }
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) ((double*)(un + o_cap))[id * RT + j] = s;
 }
 
 // Cores G(r_d)[h] = U_T(r_d)^T B_h[:, :n] for a set of feature ranks that
@@ -390,6 +416,9 @@ jolt_status cholqr(const Layout& L, const PS& P, int T, int Lw, size_t src, size
   const int ks = L.ks, kc = T / L.ks;
   const int* skip = use_flags ? (const int*)P.c(L.p_flag) : nullptr;
   int* status = (int*)P.c(L.p_status);
+  if (!f64 && cholqr_fused_supported(T, Lw, P.np))
+    return cholqr_fused(P.base, P.stride, P.np, src, dst, L.p_status, skip, s4, T, passes, shift,
+                        st);
   const size_t ins[2] = {src, mid}, outs[2] = {passes == 1 ? dst : mid, dst};
   for (int pass = 0; pass < passes; ++pass) {
     GemmDesc g = gd(Lw, Lw, kc, 1, P.np, ks,
@@ -422,6 +451,15 @@ jolt_status cholqr2(const Layout& L, const PS& P, int T, int Lw, size_t src, siz
                     size_t dst, bool use_flags, bool f64, cudaStream_t st) {
   return cholqr(L, P, T, Lw, src, mid, dst, use_flags, f64, 2, f64 ? 0.f : SUB_SHIFT, st);
 }
+
+}  // namespace
+
+jolt_status cholqr2_set(const Layout& L, char* base, size_t stride, int np, cudaStream_t st) {
+  const PS P{base, stride, np};
+  return cholqr2(L, P, L.T, L.ell, L.p_Z, L.p_V2, L.p_V, false, true, st);
+}
+
+namespace {
 
 jolt_status read_flags_all(const Layout& L, const PS& P, cudaStream_t st, bool* all) {
   std::vector<int> h(P.np);
@@ -523,7 +561,7 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
   };
   // blocks of SUB_STEPS power steps V <- orth(S V), then Rayleigh-Ritz and
   // the residual test; converged problems are skipped from then on
-  for (int blk = 0; blk < SUB_MAX_BLOCKS; ++blk) {
+  for (int blk = 0; blk < g_sub_blocks; ++blk) {
     // one shifted CholeskyQR pass per power step; the last step of a block
     // takes two so that Rayleigh-Ritz sees an orthonormal basis
     for (int q = 0; q < SUB_STEPS; ++q) {
@@ -562,7 +600,7 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
            opnd(P.c(L.p_Wm), JOLT_F32, Lw, 1, 0, s4), P.f(zn), Lw, 1, s4, 0, 0.f, flags);
     g.skip_stride = s4;
     TRY(launch_gemm(g, st));
-    const int last = (blk == SUB_MAX_BLOCKS - 1);
+    const int last = (blk == g_sub_blocks - 1);
     ritz_check_kernel<<<P.np, 512, 0, st>>>(P.base, P.stride, L.p_V2, zn, L.p_theta, L.p_UT,
                                             L.p_ev, L.p_flag, L.p_status, L.p_V, T, Lw, RT, last);
     JOLT_LAUNCH_CHECK();
@@ -622,6 +660,24 @@ jolt_status token_randomized(const F& c, const PS& P, const void* Ab, int adt, l
                      opnd(P.c(L.p_Wm), JOLT_F32, ell, 1, 0, s4), P.f(L.p_UT), RT, 1, s4, 0),
                   st));
   copy_cols_kernel<<<dim3(blocks_for(RT), c.U), 256, 0, st>>>(P.base, P.stride, L.p_theta, ell,
+                                                              L.p_ev, 1, RT);
+  JOLT_LAUNCH_CHECK();
+  return JOLT_OK;
+}
+
+// The end of a randomized solve for a set of problems whose p_Hm (the
+// Rayleigh-Ritz matrix, one part) and p_V (the orthonormal Q) are final:
+// eigenpairs of p_Hm, U_T = Q W, eigenvalues to p_ev.
+jolt_status rand_finish(const Layout& L, const PS& P, cudaStream_t st) {
+  const int T = L.T, RT = L.RT, ell = L.ell;
+  const long long s4 = P.s4();
+  int* status = (int*)P.c(L.p_status);
+  TRY(launch_jacobi(P.f(L.p_Hm), s4, ell, ell, 1, (long long)ell * ell, P.np, P.f(L.p_theta), s4,
+                    P.f(L.p_Wm), s4, ell, RT, status, s4, nullptr, 0, JAC_ABS_EXACT, st));
+  TRY(launch_gemm(gd(T, RT, ell, 1, P.np, 1, opnd(P.c(L.p_V), JOLT_F32, ell, 1, 0, s4),
+                     opnd(P.c(L.p_Wm), JOLT_F32, ell, 1, 0, s4), P.f(L.p_UT), RT, 1, s4, 0),
+                  st));
+  copy_cols_kernel<<<dim3(blocks_for(RT), P.np), 256, 0, st>>>(P.base, P.stride, L.p_theta, ell,
                                                               L.p_ev, 1, RT);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
@@ -811,6 +867,23 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       }
       TRY(token_exact(L, all_tr, warm, st, early_tr));
     }
+  } else if (flash_tc_supported(L) && ndt <= 4 && ndt * L.ell <= 160) {
+    // randomized on the tensor cores: the whole-feature rank first (beside
+    // the feature stage: it needs only X), then every truncated rank in
+    // lockstep (they need U_d)
+    if (L.hasFullD) {
+      const int rid[1] = {L.nd - 1}, pidx0[1] = {U * ndt};
+      TRY(flash_tc_solve(L, U, X, sketch, ws, preg, 1, pidx0, rid, 1, st));
+      TRY(rand_finish(L, full_ps, st));
+    }
+    TRY(mark(2, st));
+    TRY(join());
+    if (ndt > 0) {
+      int rid[4], pidx0[4];
+      for (int r = 0; r < ndt; ++r) rid[r] = pidx0[r] = r;
+      TRY(flash_tc_solve(L, U, X, sketch, ws, preg, ndt, pidx0, rid, ndt, st));
+      TRY(rand_finish(L, all_tr, st));
+    }
   } else {
     bool marked = false;
     // randomized: the whole-feature rank first (beside the feature stage),
@@ -837,7 +910,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   TRY(mark(3, st));
   scatter_problems_kernel<<<dim3(64, L.nd, U), 256, 0, st>>>(
       ws, ub, L.o_UT32, L.o_tokev, L.o_status, preg, pb, L.p_UT, L.p_ev, 1, L.p_status, U, ndt, T,
-      RT);
+      RT, L.o_cap);
   JOLT_LAUNCH_CHECK();
   // cores G(r_d)[h] = U_T^T A_h  (RT x rdv): on the tensor cores for bf16 X
   // (one pass over X for every rank, fp16 cores and U_T written directly)
@@ -903,6 +976,13 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
       }
     }
   }
+  {
+    RdList rl;
+    for (int i = 0; i < JOLT_MAX_GRID; ++i) rl.rd[i] = L.rd[i];
+    cap_g32_kernel<<<dim3((L.nd * RT + 7) / 8, U), 256, 0, st>>>(ws, ub, L.o_G32, L.o_cap, H, RT,
+                                                                D, L.nd, rl);
+    JOLT_LAUNCH_CHECK();
+  }
   for (int id = 0; id < L.nd; ++id) {
     const int rdv = L.rd[id];
     const size_t oG = L.o_G32 + (size_t)id * H * RT * D * 4;
@@ -915,5 +995,7 @@ jolt_status factor_run(const Layout& L, int U, const void* X, const float* sketc
   JOLT_LAUNCH_CHECK();
   return mark(4, st);
 }
+
+void set_subspace_blocks(int n) { g_sub_blocks = n > 0 ? n : SUB_MAX_BLOCKS; }
 
 }  // namespace jolt

@@ -45,7 +45,8 @@ bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
               const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapDataType dt) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  if (rank < 1 || rank > 5) return false;
   return fn(m, dt, rank, const_cast<void*>(ptr), dims, strides, box,
             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -660,9 +661,13 @@ ygram_pre_tc_kernel(const __grid_constant__ CUtensorMap tH, const __grid_constan
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
-// Yt[u][t][j*H + h] = Y[u][h][t][j] and its tf32 low part.
+// Yt[u][t][k] = Y[u][h][t][j] and its tf32 low part, the columns k over the
+// feature-rank slabs [jb[s], jb[s + 1]) of the truncated ranks, each slab
+// head-major: k = H jb[s] + h w_s + (j - jb[s]), w_s = jb[s + 1] - jb[s]
+// (every truncated rank's Gram is then the prefix k < H rd).
+struct Slabs { int n; int jb[JOLT_MAX_GRID + 1]; };
 __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt, int H, int T,
-                              int RD) {
+                              int RD, Slabs sl) {
   const int u = blockIdx.y;
   const float* Y = (const float*)(ws + (size_t)u * ub + o_Y);
   float* Yt = (float*)((char*)ws + (size_t)u * ub + o_Yt);
@@ -670,7 +675,11 @@ __global__ void ytrans_kernel(const char* ws, size_t ub, size_t o_Y, size_t o_Yt
   const int K = RD * H;
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < (long long)T * K;
        e += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(e / K), c = (int)(e % K), j = c / H, h = c % H;
+    const int t = (int)(e / K), c = (int)(e % K);
+    int s = 0;
+    while (s + 1 < sl.n && c >= H * sl.jb[s + 1]) ++s;
+    const int j0 = sl.jb[s], w = sl.jb[s + 1] - j0, off = c - H * j0;
+    const int h = off / w, j = j0 + off % w;
     const float v = Y[((long long)h * T + t) * RD + j];
     Yt[e] = v;
     Ytl[e] = v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
@@ -806,8 +815,12 @@ bool ygram_tc_supported(const Layout& L) {
 
 // Yt = relayout of Y (once per factor call).
 jolt_status ytrans(const Layout& L, int U, char* ws, cudaStream_t st) {
+  Slabs sl;
+  sl.n = L.ndt;
+  sl.jb[0] = 0;
+  for (int s = 0; s < L.ndt; ++s) sl.jb[s + 1] = L.rd[s];
   dim3 grid(512, U);
-  ytrans_kernel<<<grid, 256, 0, st>>>(ws, L.unit_bytes, L.o_Y, L.o_Yt, L.H, L.T, L.RD);
+  ytrans_kernel<<<grid, 256, 0, st>>>(ws, L.unit_bytes, L.o_Y, L.o_Yt, L.H, L.T, L.RD, sl);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

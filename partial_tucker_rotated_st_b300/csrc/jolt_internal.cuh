@@ -74,6 +74,10 @@ struct Layout {
   size_t o_Hs;           // diag(sigma) H_D as bf16 [D][D] (tensor-core sweep), or 0
   size_t o_Vs3;          // U_d in three bf16 parts [3 * 32][D] (tensor-core projection), or 0
   size_t o_Ub3;          // every rank's U_T in three bf16 parts [T][512] (tensor-core cores), or 0
+  size_t o_cap;          // f64 [nd][RT]: sum over h, i < r_d of G(r_d)[h][j][i]^2, unrounded cores
+  size_t o_Bx, o_Qs, o_C; // randomized token mode on the tensor cores: per-head B blocks
+                          // [H][512][D] bf16, Q parts [T][512] bf16, C = X_h^T Q [H][D][160]
+                          // fp32 (0 when that path is not taken)
   size_t unit_bytes;
   // Token-mode problems, one per (unit, feature rank), in a region after the
   // n unit regions of a call: truncated rank id of unit u is problem
@@ -88,6 +92,29 @@ struct Layout {
 };
 
 jolt_status make_layout(const jolt_config* cfg, Layout* L);
+
+// CholeskyQR (passes 1 or 2) of np T x 64 blocks (problem i at base + i *
+// stride, offsets src / dst / o_status), one cluster launch; supported when
+// every problem's cluster fits on the device at once
+bool cholqr_fused_supported(int T, int Lw, int np);
+jolt_status cholqr_fused(char* base, size_t stride, int np, size_t src, size_t dst,
+                         size_t o_status, const int* skip, long long sk_s, int T, int passes,
+                         float shift, cudaStream_t st);
+
+// FlashJoLT's range finder with its products over X on the tensor cores: the
+// ranks rid[0..nr) of every unit in lockstep, problem (u, r) at pbase +
+// (u * pmul + pidx0[r]) * prob_bytes; leaves Q in p_V and the Rayleigh-Ritz
+// matrix in p_Hm of every problem.
+bool flash_tc_supported(const Layout& L);
+jolt_status flash_tc_solve(const Layout& L, int U, const void* X, const float* sketch, char* ws,
+                           char* pbase, int pmul, const int* pidx0, const int* rid, int nr,
+                           cudaStream_t st);
+// CholeskyQR2 (f64 Cholesky) of the T x ell blocks p_Z -> p_V of np problems
+jolt_status cholqr2_set(const Layout& L, char* base, size_t stride, int np, cudaStream_t st);
+
+// iteration caps of the eigensolvers (0 -> default)
+void set_max_sweeps(int n);
+void set_subspace_blocks(int n);
 
 // ------------------------------------------------------------------ GEMM
 // C[b1,b2] = alpha * sum_s A[b1,b2,s] (M x K) * B[b1,b2,s] (K x N) + beta * C

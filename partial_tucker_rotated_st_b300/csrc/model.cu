@@ -7,12 +7,21 @@
 //  accounting, the omitted spectral tail counted as residual energy.]
 //
 // tau(r_T, r_d) = ||X - X~||^2 of the unrounded ST-HOSVD factors follows
-// from the spectra of the factor step alone:
+// from the factor step alone:
 //   r_T = T:  sum_{i >= r_d} lambda_i            (feature tail)
 //   r_T < T:  ||X||^2 - sum_{j < r_T} mu_j(r_d)   (all energy minus the token
-//             energy captured), ||X||^2 = sum_i lambda_i = trace S_d,
+//             energy captured), ||X||^2 = trace S_d (the f64 feature Gram),
 // so the table needs no pass over X.  D_model = eps^2(b) tau / ||X||^2 with
 // eps^2(0) = 1; 0 for an all-zero unit.
+//
+// The captured energy is not summed from the fp32 token eigenvalues: each of
+// those is only good to a few roundoffs of ||S_T|| ~ ||X||^2, and tau then
+// cancels them against ||X||^2.  It is taken as the Rayleigh quotients
+// mu_j = ||G_j||^2 / ||u_j||^2 of the unrounded cores G = Y x_2 U_T^T, summed
+// in f64 by the cores stage (rows of G are u_j^T Y, so ||G_j||^2 = u_j^T S_T u_j).
+// A Rayleigh quotient is off from the eigenvalue by the square of the
+// eigenvector's error, and dividing by ||u_j||^2 removes the first-order
+// error of a not quite unit u_j.
 #include "jolt_internal.cuh"
 
 namespace jolt {
@@ -24,7 +33,7 @@ struct ModelArgs {
   int rT[JOLT_MAX_GRID], rd[JOLT_MAX_GRID];
   double eps2[4];
   char* ws;
-  size_t ub, o_evd, o_tokev;
+  size_t ub, o_evd, o_Sd64, o_cap, o_UT32;
   int ncand;
 };
 
@@ -32,12 +41,36 @@ __global__ void model_table_kernel(ModelArgs a, double* dist) {
   const int u = blockIdx.x;
   const char* base = a.ws + (size_t)u * a.ub;
   const float* lam = (const float*)(base + a.o_evd);
-  const float* mu = (const float*)(base + a.o_tokev);
   __shared__ double xn;
+  __shared__ double capsum[JOLT_MAX_GRID][JOLT_MAX_GRID];   // [id][iT]
   if (threadIdx.x == 0) {
+    const double* Sd = (const double*)(base + a.o_Sd64);
     double s = 0.0;
-    for (int i = 0; i < a.D; ++i) s += (double)lam[i];
+    for (int i = 0; i < a.D; ++i) s += Sd[(size_t)i * a.D + i];
     xn = s;
+  }
+  for (int i = threadIdx.x; i < JOLT_MAX_GRID * JOLT_MAX_GRID; i += blockDim.x)
+    capsum[i / JOLT_MAX_GRID][i % JOLT_MAX_GRID] = 0.0;
+  __syncthreads();
+  if (a.RT > 0) {
+    const double* cap = (const double*)(base + a.o_cap);
+    const float* UT = (const float*)(base + a.o_UT32);
+    const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    for (int k = threadIdx.x >> 5; k < a.nd * a.RT; k += nw) {
+      const int id = k / a.RT, j = k % a.RT;
+      const float* col = UT + (size_t)id * a.T * a.RT + j;
+      double nrm = 0.0;
+      for (int t = lane; t < a.T; t += 32) {
+        const double x = col[(size_t)t * a.RT];
+        nrm += x * x;
+      }
+      for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
+      if (lane == 0) {
+        const double mu = nrm > 0.0 ? cap[k] / nrm : 0.0;
+        for (int iT = 0; iT < a.nT; ++iT)
+          if (a.rT[iT] < a.T && j < a.rT[iT]) atomicAdd(&capsum[id][iT], mu);
+      }
+    }
   }
   __syncthreads();
   for (int c = threadIdx.x; c < a.ncand; c += blockDim.x) {
@@ -47,9 +80,7 @@ __global__ void model_table_kernel(ModelArgs a, double* dist) {
     if (rT == a.T) {
       for (int i = rd; i < a.D; ++i) tau += (double)lam[i];
     } else {
-      double cap = 0.0;
-      for (int j = 0; j < rT; ++j) cap += (double)mu[id * a.RT + j];
-      tau = xn - cap;
+      tau = xn - capsum[id][iT];
     }
     if (tau < 0.0) tau = 0.0;   // the captured energy may round above the total
     dist[(long long)u * a.ncand + c] = (xn > 0.0) ? a.eps2[ib] * tau / xn : 0.0;
@@ -115,9 +146,9 @@ jolt_status model_table_run(const Layout& L, int U, const char* ws, const double
   a.nT = L.nT; a.nd = L.nd; a.nb = L.nb; a.T = L.T; a.D = L.D; a.RT = L.RT;
   for (int i = 0; i < JOLT_MAX_GRID; ++i) { a.rT[i] = L.rT[i]; a.rd[i] = L.rd[i]; }
   for (int i = 0; i < 4; ++i) a.eps2[i] = i < L.nb ? (L.b[i] == 0 ? 1.0 : eps2_host[i]) : 0.0;
-  a.ws = (char*)ws; a.ub = L.unit_bytes; a.o_evd = L.o_evd; a.o_tokev = L.o_tokev;
+  a.ws = (char*)ws; a.ub = L.unit_bytes; a.o_evd = L.o_evd; a.o_Sd64 = L.o_Sd64; a.o_cap = L.o_cap; a.o_UT32 = L.o_UT32;
   a.ncand = L.ncand;
-  model_table_kernel<<<U, 128, 0, st>>>(a, dist);
+  model_table_kernel<<<U, 256, 0, st>>>(a, dist);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

@@ -15,8 +15,13 @@
 // One CTA covers one 128-token tile of HB heads of one unit (HB = 2: two CTAs
 // per SM); X tiles and the split factor arrive by TMA (128-byte swizzle).  The epilogue (one thread per
 // token row) writes, per head, Y16 = fp16(Y) [H][T][RD] and, when asked, Y in
-// fp32 [H][T][RD]; and the token-Gram relayout Yt[t][j H + h] with its tf32
-// low part, HB consecutive heads per store, staged through shared memory.
+// fp32 [H][T][RD]; and the token-Gram relayout Yt[t][k] with its tf32 low
+// part.  Yt's columns k run over the feature-rank slabs [rd_{s-1}, rd_s) of
+// the truncated ranks, each slab head-major: k = H rd_{s-1} + h w_s + (j - rd_{s-1})
+// with w_s = rd_s - rd_{s-1}, so that every truncated rank's Gram is a prefix
+// k < H rd_s and a CTA's HB heads own one contiguous run per slab.  The rows
+// are staged in shared memory and each warp writes its 32 rows' runs with
+// consecutive lanes on consecutive columns.
 //
 // Cores (after the token mode):
 //   G(r_d)[h] = U_T(r_d)^T X_h U_d[:, :r_d]   (U_d = I for the whole feature rank)
@@ -45,6 +50,8 @@ struct ProjArgs {
   char* ws;
   size_t ub, o_Y, o_Y16, o_Yt, o_status;
   int write_y;
+  int nsl;                        // slabs of Yt: feature ranks [jb[s], jb[s + 1])
+  int jb[JOLT_MAX_GRID + 1];
 };
 
 // Vs3[u][p * 32 + j][d] = bf16 part p of V_d[d][j] (zero for j >= RD), K-major
@@ -180,28 +187,43 @@ proj_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ C
 #pragma unroll
     for (int j = 0; j < 32; ++j) stg[j * HB + i] = y[j];
   }
-  // ---- Yt[t][j H + h0 .. h0 + HB - 1] and its tf32 low part
-  if (a.o_Yt && in) {
+  // ---- Yt and its tf32 low part: this CTA's HB heads own, per slab s, the
+  // run of HB w_s columns at H jb[s] + h0 w_s of each row; element e of the
+  // concatenated runs is (head h0 + i, rank j).  Lane l writes elements l,
+  // l + 32, ... of each of its warp's rows (staged by that warp's threads).
+  if (a.o_Yt) {
+    __syncwarp();
     const size_t K = (size_t)RD * a.H;
-    float* yt = (float*)(wu + a.o_Yt) + (size_t)row * K + h0;
-    float* ytl = yt + (size_t)a.T * K;
-#pragma unroll 4
-    for (int j = 0; j < RD; ++j) {
-      float v[HB], l[HB];
+    float* ytb = (float*)(wu + a.o_Yt);
+    const int lane = t & 31;
+    constexpr int EMAX = (HB * PJ_RDP + 31) / 32;
+    int col[EMAX], src[EMAX];
 #pragma unroll
-      for (int i = 0; i < HB; ++i) {
-        v[i] = stg[j * HB + i];
-        l[i] = v[i] - __uint_as_float(__float_as_uint(v[i]) & 0xFFFFE000u);
+    for (int c = 0; c < EMAX; ++c) {
+      const int e = lane + 32 * c;
+      col[c] = -1;
+      src[c] = 0;
+      int s = 0;
+      while (s < a.nsl && e >= HB * a.jb[s + 1]) ++s;
+      if (s < a.nsl) {
+        const int j0 = a.jb[s], w = a.jb[s + 1] - j0, off = e - HB * j0;
+        const int i = off / w, j = j0 + off % w;
+        col[c] = a.H * j0 + (h0 + i) * w + (j - j0);
+        src[c] = j * HB + i;
       }
-      if (HB == 4) {
-        *reinterpret_cast<float4*>(yt + (size_t)j * a.H) = make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4*>(ytl + (size_t)j * a.H) = make_float4(l[0], l[1], l[2], l[3]);
-      } else if (HB == 2) {
-        *reinterpret_cast<float2*>(yt + (size_t)j * a.H) = make_float2(v[0], v[1]);
-        *reinterpret_cast<float2*>(ytl + (size_t)j * a.H) = make_float2(l[0], l[1]);
-      } else {
-        yt[(size_t)j * a.H] = v[0];
-        ytl[(size_t)j * a.H] = l[0];
+    }
+#pragma unroll 2
+    for (int r = 0; r < 32; ++r) {
+      const int rr = warp * 32 + r, grow = t0 + rr;
+      if (grow >= a.T) break;
+      const float* sr = reinterpret_cast<const float*>(sX) + (size_t)rr * SROW;
+      float* yt = ytb + (size_t)grow * K;
+#pragma unroll
+      for (int c = 0; c < EMAX; ++c) {
+        if (col[c] < 0) continue;
+        const float v = sr[src[c]];
+        yt[col[c]] = v;
+        yt[(size_t)a.T * K + col[c]] = v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
       }
     }
   }
@@ -226,8 +248,24 @@ struct CoresArgs {
   int rd[JOLT_MAX_GRID];
   int full_id;                  // index of the whole feature rank, or -1
   char* ws;
-  size_t ub, o_Vd, o_G16, o_status;
+  size_t ub, o_Vd, o_G16, o_status, o_cap;
 };
+
+// Sum over the warp's lanes of v[j] for each j, lane j receiving the sum of
+// index j (recursive halving: 31 exchanges instead of 32 x 5).
+__device__ __forceinline__ double warp_reduce_scatter32(double (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const double send = up ? v[k] : v[k + o];
+      const double keep = up ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
 
 // Ub3[u][t][96 id + 32 p + j] = bf16 part p of U_T(id)[t][j] (zero for
 // j >= RT and for the columns past nd * 96); U_T16[id][t][j] = fp16(U_T).
@@ -261,7 +299,11 @@ cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
   // the stages, later the epilogue's Z and U_d staging; the barriers after both
   const int epi_bytes = (a.nd + 1) * 128 * CT_ZROW * 4;
   const int region = CT_STAGES * stage_bytes > epi_bytes ? CT_STAGES * stage_bytes : epi_bytes;
-  struct Bars { uint64_t full[CT_STAGES], empty[CT_STAGES], accum; uint32_t tmem; };
+  struct Bars {
+    uint64_t full[CT_STAGES], empty[CT_STAGES], accum;
+    double cap[(CT_NMAX / 96) * 32];   // per-block captured energy of the truncated ranks
+    uint32_t tmem;
+  };
   Bars* S = (Bars*)(base + region);
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int h = blockIdx.x, u = blockIdx.y;
@@ -275,6 +317,7 @@ cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
     tc::mbar_init(tc::smem_u32(&S->accum), 1);
     tc::fence_barrier_init();
   }
+  for (int i = threadIdx.x; i < (CT_NMAX / 96) * 32; i += CT_THREADS) S->cap[i] = 0.0;
   if (warp == 1) tc::tmem_alloc(tc::smem_u32(&S->tmem), 512);
   tc::tc_fence_before();
   __syncthreads();
@@ -343,6 +386,11 @@ cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j < RT) G[(size_t)j * 128 + d] = __float2half_rn(z[j]);
+        double sq[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sq[j] = (double)z[j] * (double)z[j];
+        const double cj = warp_reduce_scatter32(sq, lane);
+        if (lane < RT) atomicAdd((double*)(wu + a.o_cap) + id * RT + lane, cj);
       } else {
         float* zr = Zs + ((size_t)it * 128 + d) * CT_ZROW;
 #pragma unroll
@@ -397,6 +445,10 @@ cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
       __half* G = (__half*)(wu + a.o_G16) + (size_t)id * a.H * RT * 128 + (size_t)h * RT * rd;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
+        double c = 0.0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c += (double)acc[i][j] * (double)acc[i][j];
+        atomicAdd(&S->cap[id * 32 + jt0 + i], c);
         __half2 p0 = __floats2half2_rn(acc[i][0], acc[i][1]);
         __half2 p1 = __floats2half2_rn(acc[i][2], acc[i][3]);
         uint2 v;
@@ -405,6 +457,12 @@ cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
         *reinterpret_cast<uint2*>(G + (size_t)(jt0 + i) * rd + jd0) = v;
       }
     }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int k = e; k < a.nd * 32; k += 128) {
+      const int id = k / 32, j = k % 32;
+      if (id != a.full_id && j < RT)
+        atomicAdd((double*)(wu + a.o_cap) + id * RT + j, S->cap[k]);
+    }
   }
   if (!ok) atomicOr((int*)(wu + a.o_status), ST_TIMEOUT);
 }
@@ -412,7 +470,7 @@ cores_tc_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ 
 size_t cores_smem(int natoms, int nd) {
   const size_t stages = (size_t)CT_STAGES * (CT_XST + natoms * CT_NATOM);
   const size_t epi = (size_t)(nd + 1) * 128 * CT_ZROW * 4;
-  return 1024 + (stages > epi ? stages : epi) + 128;
+  return 1024 + (stages > epi ? stages : epi) + 64 + (CT_NMAX / 96) * 32 * 8 + 64;
 }
 
 template <int HB>
@@ -462,6 +520,9 @@ jolt_status proj_tc(const Layout& L, int U, const void* X, char* ws, bool write_
   a.ws = ws; a.ub = L.unit_bytes;
   a.o_Y = L.o_Y; a.o_Y16 = L.o_Y16; a.o_Yt = L.o_Yt; a.o_status = L.o_status;
   a.write_y = write_y ? 1 : 0;
+  a.nsl = L.ndt;
+  a.jb[0] = 0;
+  for (int s = 0; s < L.ndt; ++s) a.jb[s + 1] = L.rd[s];
   // two heads per CTA: two CTAs per SM (TMEM 256 columns, 88 KB of shared
   // memory each) overlap one CTA's loads with the other's epilogue
   const int tiles = (L.T + PJ_ROWS - 1) / PJ_ROWS;
@@ -495,6 +556,7 @@ jolt_status cores_tc(const Layout& L, int U, const void* X, char* ws, cudaStream
     if (L.rd[i] == L.D) a.full_id = i;
   }
   a.ws = ws; a.ub = L.unit_bytes; a.o_Vd = L.o_Vd; a.o_G16 = L.o_G16; a.o_status = L.o_status;
+  a.o_cap = L.o_cap;
   CUtensorMap tX, tU;
   const cuuint64_t dX[3] = {128, (cuuint64_t)L.T, (cuuint64_t)U * L.H};
   const cuuint64_t sX[2] = {256, (cuuint64_t)L.T * 256};

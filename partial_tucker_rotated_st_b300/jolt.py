@@ -76,6 +76,7 @@ _SIG = {
                                              _P, _P]),
     "jolt_set_sweep_events": (ctypes.c_int, [_P, _P]),
     "jolt_set_factor_events": (ctypes.c_int, [ctypes.POINTER(_P)]),
+    "jolt_set_solver_limits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "jolt_model_candidates": (ctypes.c_int, [ctypes.POINTER(JoltConfig), ctypes.c_int, _P,
                                              ctypes.c_size_t, ctypes.POINTER(ctypes.c_double),
                                              _P, _P]),
@@ -303,6 +304,12 @@ def jolt_decode(desc: Sequence[JoltBlobDesc], blob, blob_stride, xhat, out_dtype
     arr = (JoltBlobDesc * n)(*desc)
     _check("jolt_decode", lib().jolt_decode(n, arr, _ptr(blob), blob_stride, _ptr(xhat),
                                             out_dtype, _stream(stream)))
+
+
+def jolt_set_solver_limits(max_sweeps: int = 0, max_subspace_blocks: int = 0):
+    """Iteration caps of the eigensolvers (0 restores a default)."""
+    _check("jolt_set_solver_limits", lib().jolt_set_solver_limits(int(max_sweeps),
+                                                                  int(max_subspace_blocks)))
 
 
 def jolt_decode_status(stream=None) -> int:

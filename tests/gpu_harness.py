@@ -56,11 +56,12 @@ class GpuRun:
     desc: Optional[list] = None
     xhat32: Optional[np.ndarray] = None
     xhat16: Optional[np.ndarray] = None   # bf16 bit patterns
+    dev: Optional[tuple] = None           # (encoder, X, signs, sketch) on the device, if kept
 
 
 def run(w, units: Optional[Sequence[int]] = None, budget: Optional[int] = None,
         serialize: bool = True, decode: bool = True, choice_override=None,
-        refine: bool = False) -> GpuRun:
+        refine: bool = False, keep: bool = False) -> GpuRun:
     ensure_built()
     units = list(range(w.n_units)) if units is None else list(units)
     xs, signs, sk = host_inputs(w, units)
@@ -72,6 +73,8 @@ def run(w, units: Optional[Sequence[int]] = None, budget: Optional[int] = None,
     st = enc.status()
     r = GpuRun(w, units, [kvgen.unit_values_f64(w, x) for x in xs], signs, sk,
                enc.dist.cpu().numpy(), enc.cost.cpu().numpy(), st)
+    if keep:
+        r.dev = (enc, X, S, K)
     if budget is None:
         budget = int(w.budget_bytes * len(units) // w.n_units)
     enc.allocate(budget, refine=refine)

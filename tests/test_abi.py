@@ -32,7 +32,7 @@ def header_functions():
 
 def test_library_exports_every_declared_symbol():
     names = header_functions()
-    assert len(names) == 24
+    assert len(names) == 25
     lib = ctypes.CDLL(J.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
@@ -322,3 +322,13 @@ def test_entry_points_reject_bad_arguments_before_launch(case):
     n0 = J.jolt_launch_count()
     assert call() == want
     assert J.jolt_launch_count() == n0
+
+
+def test_solver_limits_setter_is_host_only():
+    """The eigensolver caps are plain host state: set, rejected, restored."""
+    from partial_tucker_rotated_st_b300 import jolt as J
+    lib = J.lib()
+    assert lib.jolt_set_solver_limits(1, 1) == J.OK
+    assert lib.jolt_set_solver_limits(-1, 0) == J.ERR_INVALID
+    assert lib.jolt_set_solver_limits(0, -3) == J.ERR_INVALID
+    assert lib.jolt_set_solver_limits(0, 0) == J.OK

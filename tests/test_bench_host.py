@@ -15,54 +15,82 @@ import bench   # noqa: E402
 import kvgen   # noqa: E402
 
 
-def _write_record(tmp_path, src_text, workload, nbytes, key="k_src_sha256"):
+def _write_record(tmp_path, src_text, workload, nbytes, kernel="k", units=None,
+                  kind="traffic_record"):
     src = tmp_path / "kernel.cu"
     src.write_text(src_text)
     h = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    prof = tmp_path / "profile.md"
-    rec = {"workload": workload, "dram_bytes_per_launch": nbytes, key: h}
-    prof.write_text("# summary\n\n| a | b |\n\ntraffic_record: " + json.dumps(rec) + "\n")
+    prof = tmp_path / "profiles"
+    prof.mkdir(exist_ok=True)
+    rec = {"kernel": kernel, "workload": workload, "dram_bytes_per_launch": nbytes,
+           "src_sha256": h}
+    if units is not None:
+        rec["units"] = units
+    (prof / "k_profile.md").write_text("# summary\n\n| a | b |\n\n" + kind + ": " +
+                                       json.dumps(rec) + "\n")
     return str(prof), str(src)
 
 
-def test_traffic_record_matches_source_and_workload(tmp_path):
+def _get(prof, src, wl, kernel="k"):
+    return bench.traffic_record(kernel, src, "dram_bytes_per_launch", wl, prof)
+
+
+def test_traffic_record_matches_source_kernel_and_workload(tmp_path):
     prof, src = _write_record(tmp_path, "__global__ void k() {}\n", "mistral_t1024", 123456789)
-    get = lambda wl: bench.traffic_record(prof, src, "k_src_sha256", "dram_bytes_per_launch", wl)
-    assert get("mistral_t1024") == 123456789
-    assert get("llama_t1024") is None                    # counters of another workload
+    assert _get(prof, src, kvgen.WORKLOADS["mistral_t1024"]) == 123456789
+    assert _get(prof, src, kvgen.WORKLOADS["llama_t1024"]) is None    # another workload
+    assert _get(prof, src, kvgen.WORKLOADS["mistral_t1024"], "other") is None
+
+
+def test_traffic_record_scales_a_smaller_capture_by_units(tmp_path):
+    prof, src = _write_record(tmp_path, "x", "llama_t1024", 1000, units=4)
+    w = kvgen.WORKLOADS["llama_t1024"]
+    assert _get(prof, src, w) == 1000 * w.n_units // 4
+    assert _get(prof, src, kvgen.custom_workload("llama_t1024", n_groups=2)) == 1000
 
 
 def test_traffic_record_is_dropped_when_the_source_changes(tmp_path):
     prof, src = _write_record(tmp_path, "__global__ void k() {}\n", "mistral_t1024", 5)
     with open(src, "a") as f:
         f.write("// edited\n")
-    assert bench.traffic_record(prof, src, "k_src_sha256", "dram_bytes_per_launch",
-                                "mistral_t1024") is None
+    assert _get(prof, src, kvgen.WORKLOADS["mistral_t1024"]) is None
 
 
-def test_traffic_record_missing_files_or_keys(tmp_path):
+def test_traffic_record_missing_files(tmp_path):
     prof, src = _write_record(tmp_path, "x", "mistral_t1024", 5)
-    assert bench.traffic_record(str(tmp_path / "none.md"), src, "k_src_sha256",
-                                "dram_bytes_per_launch", "mistral_t1024") is None
-    assert bench.traffic_record(prof, str(tmp_path / "none.cu"), "k_src_sha256",
-                                "dram_bytes_per_launch", "mistral_t1024") is None
-    # a record keyed for another kernel's source never matches
-    assert bench.traffic_record(prof, src, "other_src_sha256", "dram_bytes_per_launch",
-                                "mistral_t1024") is None
+    w = kvgen.WORKLOADS["mistral_t1024"]
+    assert _get(str(tmp_path / "none"), src, w) is None
+    assert _get(prof, str(tmp_path / "none.cu"), w) is None
 
 
-@pytest.mark.parametrize("path,key,bkey", [
-    (bench.DECODE_PROFILE, "decode_src_sha256", "dram_bytes_per_launch"),
-    (bench.ATTEND_PROFILE, "attend_src_sha256", "dram_bytes_per_call"),
-    (bench.SWEEP_PROFILE, "sweep_src_sha256", "dram_bytes_per_launch"),
-])
-def test_committed_profiles_carry_one_well_formed_record(path, key, bkey):
-    lines = [l for l in open(path).read().splitlines() if l.startswith("traffic_record:")]
-    assert len(lines) == 1
-    rec = json.loads(lines[0].split(":", 1)[1])
-    assert rec["workload"] in kvgen.WORKLOADS
-    assert len(rec[key]) == 16 and int(rec[key], 16) >= 0
-    assert int(rec[bkey]) > 0
+def test_tensor_records_are_read_by_kind(tmp_path):
+    prof, src = _write_record(tmp_path, "x", "llama_t1024", 5, kernel="gram_tok_tc_kernel",
+                              kind="tensor_record")
+    recs = bench.profile_records("tensor_record", src, "llama_t1024", prof)
+    assert [r["kernel"] for r in recs] == ["gram_tok_tc_kernel"]
+    assert bench.profile_records("traffic_record", src, "llama_t1024", prof) == []
+
+
+def test_committed_profile_records_are_well_formed():
+    import glob
+    n = 0
+    for f in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        for line in open(f).read().splitlines():
+            kind = line.split(":", 1)[0]
+            if kind not in ("traffic_record", "tensor_record"):
+                continue
+            rec = json.loads(line.split(":", 1)[1])
+            assert rec["workload"] in kvgen.WORKLOADS, f
+            assert isinstance(rec["kernel"], str) and rec["kernel"], f
+            assert len(rec["src_sha256"]) == 16 and int(rec["src_sha256"], 16) >= 0, f
+            if kind == "traffic_record":
+                key = "dram_bytes_per_call" if "dram_bytes_per_call" in rec else \
+                    "dram_bytes_per_launch"
+                assert int(rec[key]) > 0, f
+            else:
+                assert 0.0 <= float(rec["tensor_pipe_active_pct"]) <= 100.0, f
+            n += 1
+    assert n >= 1
 
 
 def test_sweep_roofline_counts_650_flops_per_element_on_the_5x5x4_grid():

@@ -21,13 +21,26 @@ seconds, so each configuration checks what it can compute exactly:
   * the chosen candidate's table entry against the distortion of what the
     GPU's decoder rebuilds from the blob (fp32 and bf16 output), every unit;
   * the codes of up to four units against the oracle's quantizer on the
-    blob's stored factors (the bar of the small parity tests).
+    blob's stored factors (the bar of the small parity tests);
+  * b > 0 and b = 0 table entries of two units (one K, one V) on five rank
+    pairs spread over the grid, every bit width, against the oracle's
+    distortion of the same candidate: each candidate is serialized in
+    turn, and the oracle rebuilds X~ from the blob's fp16 factors, quantizes
+    the rotated residual with its own quantizer and measures D in f64
+    (the fused sweep's scoring against the definition, at full size);
+  * the modeled table (unrounded factors) of the sampled unit against the
+    same tails.
+
+The oracle's own Jacobi does not finish a 1024 x 1024 token Gram in ten
+minutes, so the exact token spectra at full size come from LAPACK
+(numpy eigvalsh); the Jacobi is pinned against it at small sizes.
 """
 import numpy as np
 import pytest
 
 import kvgen
 from oracle import jolt as oj
+from partial_tucker_rotated_st_b300.codec import config_for as codec_cfg
 from tests import gpu_harness as gh
 
 pytestmark = pytest.mark.gpu
@@ -62,11 +75,61 @@ def _b0_reference(w, x, sk):
     return out
 
 
+def _rank_pairs(nT, nd):
+    """Five (iT, id) cells spread over the grid: the corners and the middle."""
+    out = []
+    for c in [(0, 0), (nT - 1, nd - 1), (nT // 2, nd // 2), (0, nd - 1), (nT - 1, 0),
+              (1, nd - 2), (nT - 2, 1)]:
+        if c not in out and 0 <= c[0] < nT and 0 <= c[1] < nd:
+            out.append(c)
+    return out[:5]
+
+
+def _check_candidates(w, r, units=(2, 3)):
+    """Table entries of every bit width on five rank pairs against the
+    oracle's distortion of the candidate's own stored factors (the factors of
+    a rank pair are the same for every b, so one blob per pair serves all)."""
+    import torch
+    enc, X, S, _ = r.dev
+    nT, nd, nb = len(w.rT), len(w.rd), len(w.bits)
+    ib_top = int(np.argmax(w.bits))
+    for iT, id_ in _rank_pairs(nT, nd):
+        c_top = (iT * nd + id_) * nb + ib_top
+        desc = enc.serialize(X, S, [c_top] * len(r.units))
+        torch.cuda.synchronize()
+        for u in units:
+            blob = enc.blob[u, :desc[u].bytes].cpu().numpy().tobytes()
+            hd = oj.parse_header(blob)
+            Xt = _stored_xtilde(blob, hd)
+            Q = oj.rotation_matrix(hd["signs"])
+            x = r.X64[u]
+            for ib, b in enumerate(w.bits):
+                c = (iT * nd + id_) * nb + ib
+                ref = oj.distortion(x, oj.candidate_xhat(x, Xt, Q, b))
+                got = float(r.dist[u, c])
+                assert abs(got - ref) <= max(REL * ref, ABS), \
+                    (u, c, (hd["rT"], hd["rd"], b), got, ref)
+
+
+def _stored_xtilde(blob, hd):
+    H, T, D, rT, rd = hd["H"], hd["T"], hd["D"], hd["rT"], hd["rd"]
+
+    def arr(off, n, shape):
+        return np.frombuffer(blob, np.float16, n, off).astype(np.float64).reshape(shape)
+
+    UT = None if hd["flags"] & 1 else arr(hd["UT"], T * rT, (T, rT))
+    Ud = None if hd["flags"] & 2 else arr(hd["Ud"], D * rd, (D, rd))
+    G = arr(hd["G"], H * rT * rd, (H, rT, rd))
+    return oj.reconstruct(UT, G, Ud)
+
+
 @pytest.mark.parametrize("name", BIG)
 def test_full_size_config(name):
+    import torch
+    from partial_tucker_rotated_st_b300 import jolt as J
     from tests.test_gpu_parity import check_codes_against_oracle
     w = kvgen.WORKLOADS[name]
-    r = gh.run(w, refine=True)
+    r = gh.run(w, refine=True, keep=True)
     U = w.n_units
     assert r.status == 0
     # cost table
@@ -88,6 +151,20 @@ def test_full_size_config(name):
     d = r.dist[u].reshape(len(rT), len(rd), len(w.bits))[:, :, w.bits.index(0)]
     bad = np.abs(d - b0) > np.maximum(REL * b0, ABS)
     assert not bad.any(), [(rT[i], rd[j], d[i, j], b0[i, j]) for i, j in np.argwhere(bad)]
+    # the modeled table of the same unit: eps^2(b) times the same tails
+    enc = r.dev[0]
+    eps2 = [1.0 if b == 0 else 4.0 ** (-b) for b in w.bits]
+    md = torch.zeros(U, enc.ncand, dtype=torch.float64, device="cuda")
+    J.jolt_model_candidates(codec_cfg(w), U, enc.ws, eps2, md)
+    torch.cuda.synchronize()
+    md = md[u].cpu().numpy().reshape(len(rT), len(rd), len(w.bits))
+    for ib in range(len(w.bits)):
+        ref_m = eps2[ib] * b0
+        bad = np.abs(md[:, :, ib] - ref_m) > np.maximum(REL * ref_m, ABS)
+        assert not bad.any(), [(rT[i], rd[j], w.bits[ib], md[i, j, ib], ref_m[i, j])
+                               for i, j in np.argwhere(bad)]
+    # b > 0 (and b = 0) cells of two units against the oracle's distortion
+    _check_candidates(w, r)
     # the chosen candidates are what decodes (fp32 and bf16 output)
     for u in range(U):
         x = r.X64[u]

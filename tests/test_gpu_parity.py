@@ -307,6 +307,41 @@ def test_zero_unit_and_nonfinite_input():
     assert enc.status() == J.ERR_NONFINITE
 
 
+@pytest.mark.parametrize("name", ["tiny", "mistral_small"])
+def test_eigensolver_cap_reports_noconverge(name):
+    """Every Jacobi solve capped at one sweep and the subspace iteration at
+    one block: the factor step finishes (the loops are bounded compute) and
+    reports JOLT_ERR_NOCONVERGE through the unit status; with the default caps
+    restored the same input factors cleanly."""
+    import torch
+    from partial_tucker_rotated_st_b300 import codec
+    from partial_tucker_rotated_st_b300 import jolt as J
+    w = SMALL[name]
+    xs, signs, sk = gh.host_inputs(w, range(w.n_units))
+    X, S, K = gh.to_device(w, xs, signs, sk)
+    cfg = codec.config_for(w)
+    enc = codec.Encoder(cfg, w.n_units)
+    try:
+        J.jolt_set_solver_limits(1, 1)
+        enc.factor(X, K)
+        torch.cuda.synchronize()
+        assert enc.status() == J.ERR_NOCONVERGE
+    finally:
+        J.jolt_set_solver_limits(0, 0)
+    enc.factor(X, K)
+    assert enc.status() == J.OK
+
+
+def test_decode_status_clear_after_clean_decode():
+    """jolt_decode_status reports no gave-up wait after ordinary decodes on the
+    tensor-core decoder (bf16, D = 128), and reading it clears it."""
+    from partial_tucker_rotated_st_b300 import jolt as J
+    r = gpu_run("mistral_small")
+    assert r.xhat16 is not None
+    assert J.jolt_decode_status() == J.OK
+    assert J.jolt_decode_status() == J.OK
+
+
 def test_rank_deficient_feature_gram_matches_oracle():
     """A feature that is identically zero makes S_d singular: the Cholesky of
     the one-sided eigensolver meets a zero pivot, and that unit is solved by
@@ -420,11 +455,7 @@ def test_model_table_matches_oracle_and_allocates(name):
         s_ = None if sk is None else sk[i].astype(np.float64)
         fac = oj.factorize(x64, w.rT, w.rd, w.token_mode, s_, w.power_iters)
         ref = oj.model_dist_table(fac, float(np.sum(x64 * x64)), w.bits, eps2)
-        # for r_T < T the captured energy is a sum of r_T fp32 token
-        # eigenvalues, each off by a few units of roundoff of ||S_T|| <=
-        # ||X||^2 (Jacobi is backward stable), and tau = ||X||^2 - captured
-        # cancels: |dD| <= eps^2 * 4 r_T 2^-24 absolute
-        ok = close(md[i], ref, rel=REL, ab=4.0 * max(fac.rT_max, 1) * 2.0 ** -24)
+        ok = close(md[i], ref)
         j = int(np.argmax(np.abs(md[i] - ref)))
         assert np.all(ok), (i, j, md[i][j], ref[j])
     enc.sweep(X, S)   # the cost table

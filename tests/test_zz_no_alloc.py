@@ -20,12 +20,18 @@ pytestmark = pytest.mark.gpu
 REL, ABS = 1e-3, 1e-6
 
 
-def test_noalloc_sweep_matches_regular_sweep_twice():
+@pytest.mark.parametrize("case", ["tensor_core", "simt_f32_d32"])
+def test_noalloc_sweep_matches_regular_sweep_twice(case):
+    """bf16 D = 128 takes the tensor-core sweep; the fp32 D = 32 workload the
+    SIMT sweep kernel with its per-tile partials in the static array."""
     import torch
     from partial_tucker_rotated_st_b300 import codec
     from partial_tucker_rotated_st_b300 import jolt as J
     gh.ensure_built()
-    w = kvgen.custom_workload("mistral_t1024", n_groups=2, H=8, T=160)
+    if case == "tensor_core":
+        w = kvgen.custom_workload("mistral_t1024", n_groups=2, H=8, T=160)
+    else:
+        w = kvgen.WORKLOADS["tiny"]
     xs, signs, sk = gh.host_inputs(w, range(w.n_units))
     X, S, K = gh.to_device(w, xs, signs, sk)
     cfg = codec.config_for(w)
