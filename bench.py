@@ -484,6 +484,12 @@ def factor_record(run, steps, flush, st, pk):
                   + 2 * N * RT * len(w.rd))       # cores Z = X_h^T U_T of every rank
     if w.token_mode == "exact":
         flops_unit += 2 * T * T * H * D           # whole-feature token Gram
+    else:
+        # FlashJoLT: Z = A Omega, then q times A^T Q and A (A^T Q), and the
+        # final A^T Q, each 2 H T r_d ell for every feature rank
+        ell = RT + w.oversample
+        rds = sum(w.D if r == kvgen.FULL else r for r in w.rd)
+        flops_unit += (2 + 2 * w.power_iters) * 2 * H * T * rds * ell
     flops = flops_unit * U
     peak = pk.get("bf16_tflops_sustained", 1400.0)
     crit = "feature" if ms["feature"] >= ms["full_token_solve"] else "full_token_solve"
@@ -505,9 +511,10 @@ def decode_roofline(w, desc, dec_t, hbm):
             "bytes_algorithmic": int(alg), "traffic": decode_traffic(w)}
 
 
-def config_record(run, res, hbm, kind, pk, sms):
+def config_record(run, res, hbm, kind, pk, sms, fac=None):
     """Per-configuration record: encode and decode GB/s, stage times, the
-    fused sweep's and the decoder's rooflines."""
+    factor step's stage breakdown, the fused sweep's and the decoder's
+    rooflines."""
     w = run.w
     per = res["per"]
     enc_t = per["factor"] + per["sweep"] + per["allocate"] + per["encode"]
@@ -519,6 +526,7 @@ def config_record(run, res, hbm, kind, pk, sms):
             "stages_ms": {s: 1e3 * v for s, v in per.items()},
             "sweep_roofline": roofline(w, res["sweep_kernel_s"], hbm, kind, pk, sms),
             "decode_roofline": decode_roofline(w, res["desc"], per["decode"], hbm),
+            "factor": fac,
             "gpu_launches": res["launches"]}
 
 
@@ -623,7 +631,8 @@ def run_ours(args):
         wx = workload(name, args.groups)
         rx = Run(wx, host.pop(name))
         resx = timed_steps(rx, args.steps, args.warmup, flush, st)
-        recs[name] = config_record(rx, resx, hbm, kind, pk, sms)
+        facx = factor_record(rx, args.steps, flush, st, pk)
+        recs[name] = config_record(rx, resx, hbm, kind, pk, sms, facx)
         del rx
         torch.cuda.empty_cache()
     line["configs"] = recs

@@ -666,14 +666,14 @@ jolt_status token_randomized(const F& c, const PS& P, const void* Ab, int adt, l
 }
 
 // The end of a randomized solve for a set of problems whose p_Hm (the
-// Rayleigh-Ritz matrix, one part) and p_V (the orthonormal Q) are final:
+// Rayleigh-Ritz matrix in L.hs partials) and p_V (the orthonormal Q) are final:
 // eigenpairs of p_Hm, U_T = Q W, eigenvalues to p_ev.
 jolt_status rand_finish(const Layout& L, const PS& P, cudaStream_t st) {
   const int T = L.T, RT = L.RT, ell = L.ell;
   const long long s4 = P.s4();
   int* status = (int*)P.c(L.p_status);
-  TRY(launch_jacobi(P.f(L.p_Hm), s4, ell, ell, 1, (long long)ell * ell, P.np, P.f(L.p_theta), s4,
-                    P.f(L.p_Wm), s4, ell, RT, status, s4, nullptr, 0, JAC_ABS_EXACT, st));
+  TRY(launch_jacobi(P.f(L.p_Hm), s4, ell, ell, L.hs, (long long)ell * ell, P.np, P.f(L.p_theta),
+                    s4, P.f(L.p_Wm), s4, ell, RT, status, s4, nullptr, 0, JAC_ABS_EXACT, st));
   TRY(launch_gemm(gd(T, RT, ell, 1, P.np, 1, opnd(P.c(L.p_V), JOLT_F32, ell, 1, 0, s4),
                      opnd(P.c(L.p_Wm), JOLT_F32, ell, 1, 0, s4), P.f(L.p_UT), RT, 1, s4, 0),
                   st));

@@ -52,6 +52,7 @@ struct FlashSet {
   int rdv[4];                  // feature rank (D = the whole feature rank: V = I)
   int pidx0[4], pmul;          // problem of (unit u, rank r) = u * pmul + pidx0[r]
   int H, T, D;
+  int hs;                      // head groups of the Rayleigh-Ritz partial Grams (divides H)
   char* ws;                    // units
   size_t ub, o_Vd, o_Bx, o_Qs, o_C, o_status;
   char* pbase;                 // problems
@@ -82,10 +83,10 @@ flash_b_kernel(FlashSet s, const float* __restrict__ sketch, int mode) {
   extern __shared__ float fb_sm[];
   float* In = fb_sm;                    // [D][NC]: Omega_h (every rank) or C_h
   float* Pm = In + D * NC;              // [32][NC]: V_r^T C_h,r of the truncated ranks
-  float* Vs = Pm + 32 * NC;             // [D][32]: U_d[:, :32]
+  float* Vs = Pm + 32 * NC;             // [32][D]: U_d[:, :32] transposed
   const char* wu = s.ws + (size_t)u * s.ub;
   const float* Vg = (const float*)(wu + s.o_Vd);
-  for (int e = t; e < D * 32; e += 256) Vs[e] = Vg[(size_t)(e >> 5) * D + (e & 31)];
+  for (int e = t; e < D * 32; e += 256) Vs[(e & 31) * D + (e >> 5)] = Vg[(size_t)(e >> 5) * D + (e & 31)];
   for (int e = t; e < D * NC; e += 256) {
     const int d = e / NC, c = e % NC;
     In[e] = mode == 0 ? sketch[(((size_t)u * s.H + h) * D + d) * ell + c % ell]
@@ -98,7 +99,7 @@ flash_b_kernel(FlashSet s, const float* __restrict__ sketch, int mode) {
       const int j = e / NC, c = e % NC, r = c / ell;
       float a = 0.f;
       if (s.rdv[r] < D && j < s.rdv[r])
-        for (int d = 0; d < D; ++d) a = fmaf(Vs[d * 32 + j], In[d * NC + c], a);
+        for (int d = 0; d < D; ++d) a = fmaf(Vs[j * D + d], In[d * NC + c], a);
       Pm[e] = a;
     }
     __syncthreads();
@@ -112,9 +113,9 @@ flash_b_kernel(FlashSet s, const float* __restrict__ sketch, int mode) {
       if (rd >= D) {
         v = In[d * NC + c];                   // V = I
       } else if (mode == 0) {
-        for (int j = 0; j < rd; ++j) v = fmaf(Vs[d * 32 + j], In[j * NC + c], v);
+        for (int j = 0; j < rd; ++j) v = fmaf(Vs[j * D + d], In[j * NC + c], v);
       } else {
-        for (int j = 0; j < rd; ++j) v = fmaf(Vs[d * 32 + j], Pm[j * NC + r * ell + k], v);
+        for (int j = 0; j < rd; ++j) v = fmaf(Vs[j * D + d], Pm[j * NC + r * ell + k], v);
       }
     }
     __nv_bfloat16 p[3];
@@ -338,23 +339,29 @@ flash_c_kernel(const __grid_constant__ CUtensorMap tX, const __grid_constant__ C
 }
 
 // Rayleigh-Ritz matrix of problem (u, r): Hm = sum_h P_h^T P_h with P_h =
-// V_r^T C_h,r (rdv x ell; C_h,r itself for the whole feature rank), into the
-// problem's p_Hm (ell x ell).  One CTA per (rank, unit).
+// V_r^T C_h,r (rdv x ell; C_h,r itself for the whole feature rank), one
+// partial per group of H / hs heads into the problem's p_Hm + g ell^2 (the
+// eigen-solve sums the partials).  One CTA per (head group, rank, unit).
 __global__ void __launch_bounds__(256)
 flash_rr_kernel(FlashSet s) {
-  const int r = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
+  const int g = blockIdx.x, r = blockIdx.y, u = blockIdx.z, t = threadIdx.x;
   const int D = s.D, ell = s.ell, NC = s.nr * ell, rd = s.rdv[r];
   const int rows = rd < D ? rd : D;
+  const int hper = s.H / s.hs;
   extern __shared__ float fr_sm[];
   float* Ch = fr_sm;                 // [D][ell]
-  float* Ph = Ch + D * ell;          // [rows][ell]
+  float* Ph = Ch + D * ell;          // [32][ell]
+  float* Vs = Ph + 32 * ell;         // [32][D]: U_d[:, :32] transposed
   const char* wu = s.ws + (size_t)u * s.ub;
-  const float* Vd = (const float*)(wu + s.o_Vd);
   const float* Cg = (const float*)(wu + s.o_C);
+  if (rd < D) {
+    const float* Vg = (const float*)(wu + s.o_Vd);
+    for (int e = t; e < D * 32; e += 256) Vs[(e & 31) * D + (e >> 5)] = Vg[(size_t)(e >> 5) * D + (e & 31)];
+  }
   float acc[16];                     // entries t + 256 i of the ell x ell matrix (ell <= 64)
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  for (int h = 0; h < s.H; ++h) {
+  for (int h = g * hper; h < (g + 1) * hper; ++h) {
     __syncthreads();
     for (int e = t; e < D * ell; e += 256) {
       const int d = e / ell, k = e % ell;
@@ -365,7 +372,7 @@ flash_rr_kernel(FlashSet s) {
       for (int e = t; e < rows * ell; e += 256) {
         const int j = e / ell, k = e % ell;
         float a = 0.f;
-        for (int d = 0; d < D; ++d) a = fmaf(Vd[(size_t)d * D + j], Ch[d * ell + k], a);
+        for (int d = 0; d < D; ++d) a = fmaf(Vs[j * D + d], Ch[d * ell + k], a);
         Ph[e] = a;
       }
       __syncthreads();
@@ -382,7 +389,7 @@ flash_rr_kernel(FlashSet s) {
       }
     }
   }
-  float* Hm = (float*)(prob(s, u, r) + s.p_Hm);
+  float* Hm = (float*)(prob(s, u, r) + s.p_Hm) + (size_t)g * ell * ell;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int e = t + 256 * i;
@@ -413,7 +420,7 @@ jolt_status flash_tc_solve(const Layout& L, int U, const void* X, const float* s
     s.pidx0[r] = pidx0[r];
   }
   s.pmul = pmul;
-  s.H = L.H; s.T = L.T; s.D = L.D;
+  s.H = L.H; s.T = L.T; s.D = L.D; s.hs = L.hs;
   s.ws = ws; s.ub = L.unit_bytes; s.o_Vd = L.o_Vd; s.o_Bx = L.o_Bx; s.o_Qs = L.o_Qs;
   s.o_C = L.o_C; s.o_status = L.o_status;
   s.pbase = pbase; s.pb = L.prob_bytes; s.p_Z = L.p_Z; s.p_V = L.p_V; s.p_Hm = L.p_Hm;
@@ -446,7 +453,7 @@ jolt_status flash_tc_solve(const Layout& L, int U, const void* X, const float* s
   const size_t zsm = 1024 + (size_t)FL_STAGES * FZ_STAGE + 128;
   const size_t csm = 1024 + (size_t)FL_STAGES * (FC_XST + 8 * FC_NATOM) + 128;
   const size_t bsm = ((size_t)L.D * NC + 32 * NC + (size_t)L.D * 32) * 4;
-  const size_t rsm = ((size_t)L.D * L.ell * 2) * 4;
+  const size_t rsm = ((size_t)L.D * L.ell + 32 * L.ell + (size_t)L.D * 32) * 4;
   static bool attr = false;
   if (!attr) {
     JOLT_CUDA_TRY(cudaFuncSetAttribute(flash_z_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)zsm));
@@ -454,7 +461,7 @@ jolt_status flash_tc_solve(const Layout& L, int U, const void* X, const float* s
     JOLT_CUDA_TRY(cudaFuncSetAttribute(flash_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)(((size_t)128 * FL_WMAX + 32 * FL_WMAX + 128 * 32) * 4)));
     JOLT_CUDA_TRY(cudaFuncSetAttribute(flash_rr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(((size_t)128 * 64 * 2) * 4)));
+                                       (int)(((size_t)128 * 64 + 32 * 64 + 128 * 32) * 4)));
     attr = true;
   }
   const dim3 gh(L.H, U), gz((L.T + 127) / 128, U);
@@ -495,7 +502,7 @@ jolt_status flash_tc_solve(const Layout& L, int U, const void* X, const float* s
     if (jolt_status e = zpass()) return e;        // Z = A (A^T Q)
     if (jolt_status e = orth_all()) return e;
   }
-  flash_rr_kernel<<<dim3(nr, U), 256, rsm, st>>>(s);
+  flash_rr_kernel<<<dim3(L.hs, nr, U), 256, rsm, st>>>(s);
   JOLT_LAUNCH_CHECK();
   return JOLT_OK;
 }

@@ -104,7 +104,7 @@ jolt_status cholqr_fused(char* base, size_t stride, int np, size_t src, size_t d
 // FlashJoLT's range finder with its products over X on the tensor cores: the
 // ranks rid[0..nr) of every unit in lockstep, problem (u, r) at pbase +
 // (u * pmul + pidx0[r]) * prob_bytes; leaves Q in p_V and the Rayleigh-Ritz
-// matrix in p_Hm of every problem.
+// matrix, as L.hs partials of ell x ell, in p_Hm of every problem.
 bool flash_tc_supported(const Layout& L);
 jolt_status flash_tc_solve(const Layout& L, int U, const void* X, const float* sketch, char* ws,
                            char* pbase, int pmul, const int* pidx0, const int* rid, int nr,
