@@ -238,6 +238,8 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
       sv[r][e] = 0.f;
     }
   }
+  // double-float chain rows (B = hi + lo): the fp32 chain takes hi only, its
+  // error |c lo| <= 2^-24 |c hi| per term added to the bound with |c hi|
   const bool lo_part = (a.mode != 2 && a.K > 0 && a.B16 == nullptr);
   if (a.mode != 2 && a.K > 0) {
     for (int i = threadIdx.x; i < CD_TILE * a.K; i += CD_THREADS) {
@@ -263,24 +265,18 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
     __syncthreads();
     for (int k = 0; k < a.K; ++k) {
       const float* kk = Ks + k * CD_TILE + w * CD_ROWS;
-      float bh[EPT], bl[EPT];
+      float bh[EPT];
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) {
-        bh[e] = Bsh[k * D + lane * EPT + e];
-        bl[e] = Bsl[k * D + lane * EPT + e];
-      }
+      for (int e = 0; e < EPT; ++e) bh[e] = Bsh[k * D + lane * EPT + e];
 #pragma unroll
       for (int r = 0; r < CD_ROWS; ++r) {
         const float c = kk[r];
 #pragma unroll
         for (int e = 0; e < EPT; ++e) {
-          float v = fmaf(-c, bh[e], rv[r][e]);
-          if (lo_part) {
-            sv[r][e] += fabsf(v);
-            v = fmaf(-c, bl[e], v);
-          }
+          const float v = fmaf(-c, bh[e], rv[r][e]);
           rv[r][e] = v;
           sv[r][e] += fabsf(v);
+          if (lo_part) sv[r][e] = fmaf(fabsf(c), fabsf(bh[e]), sv[r][e]);
         }
       }
     }
@@ -320,7 +316,7 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
     l1s = warp_sum(l1s);
     l1v = warp_sum(l1v);
     // bound on |y - exact y| for every element of the row: the chain's
-    // roundings (l1s u), the transform's seven levels and the scaling
+    // roundings and dropped low parts (l1s u), the transform's seven levels and the scaling
     // (8 u l1v), over sqrt(D); each element adds 2 u |y| (the product by the
     // fp32 1/sqrt(D) and its rounding).  The sums themselves are rounded:
     // 1% of slack covers them.
@@ -345,11 +341,14 @@ __global__ void __launch_bounds__(CD_THREADS, 2) encode_codes_kernel(const __gri
       s = hf;
     }
     float q[EPT];
+    // the quotient by the reciprocal: a code it rounds the wrong way lies
+    // within a few ulps of a tie, where the check below fails anyway
+    const float inv_s = s > 0.f ? __fdiv_rn(1.f, s) : 0.f;
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
       float qq = 0.f;
       if (s > 0.f) {
-        qq = rintf(__fdiv_rn(y[e], s));
+        qq = rintf(y[e] * inv_s);
         // the exact y must lie strictly between (q - 1/2) s and (q + 1/2) s
         const float Ee = 1.01f * (E + 2.f * U * fabsf(y[e]));
         const float up = fmaf(-(qq + 0.5f), s, y[e]);
