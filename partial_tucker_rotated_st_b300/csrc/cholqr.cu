@@ -9,8 +9,8 @@
 // The unfused path takes three launches per pass (the Gram, the Cholesky
 // factor and its inverse, the product Z R^{-1}), each a few tens of
 // microseconds of latency for a T x 64 block.  Here a cluster of CQ_NC CTAs
-// (8, or 4 when 8 per problem would not all be resident at once: a problem
-// holds its SMs for the whole call) owns one problem: each CTA keeps
+// (8, or 4 or 2 when 8 per problem would not all be resident at once: a
+// problem holds its SMs for the whole call) owns one problem: each CTA keeps
 // T / CQ_NC rows of the block in shared
 // memory for every pass, forms their partial 64 x 64 Gram, and the partials
 // are summed through distributed shared memory into CTA 0, which factors and
@@ -235,6 +235,7 @@ int cq_width(int T, int np) {
   const int sms = sm_count_cq();
   if ((T + 7) / 8 <= CQ_MAXROWS && np * 8 <= sms) return 8;
   if ((T + 3) / 4 <= CQ_MAXROWS && np * 4 <= sms) return 4;
+  if ((T + 1) / 2 <= CQ_MAXROWS && np * 2 <= sms) return 2;
   return 0;
 }
 
@@ -253,7 +254,9 @@ jolt_status cholqr_fused(char* base, size_t stride, int np, size_t src, size_t d
   CqArgs a;
   a.base = base; a.stride = stride; a.src = src; a.dst = dst; a.o_status = o_status;
   a.skip = skip; a.sk_s = sk_s; a.T = T; a.passes = passes; a.shift = shift;
-  return nc == 8 ? launch_cq<8>(a, np, st) : launch_cq<4>(a, np, st);
+  if (nc == 8) return launch_cq<8>(a, np, st);
+  if (nc == 4) return launch_cq<4>(a, np, st);
+  return launch_cq<2>(a, np, st);
 }
 
 }  // namespace jolt
