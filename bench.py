@@ -527,6 +527,7 @@ def config_record(run, res, hbm, kind, pk, sms, fac=None):
             "sweep_roofline": roofline(w, res["sweep_kernel_s"], hbm, kind, pk, sms),
             "decode_roofline": decode_roofline(w, res["desc"], per["decode"], hbm),
             "factor": fac,
+            "gram_tensor": gram_tensor_record(w),
             "gpu_launches": res["launches"]}
 
 
@@ -873,8 +874,8 @@ def gram_tensor_record(w):
     cores) from a committed ncu capture of the current sources, keyed by
     kernel; {} when none matches."""
     out = {}
-    for src in (GRAM_SRC, os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc",
-                                       "proj_tc.cu")):
+    csrc = os.path.join(ROOT, "partial_tucker_rotated_st_b300", "csrc")
+    for src in (GRAM_SRC, os.path.join(csrc, "proj_tc.cu"), os.path.join(csrc, "flash_tc.cu")):
         for rec in profile_records("tensor_record", src, w.name):
             out[rec["kernel"]] = {k: v for k, v in rec.items()
                                   if k not in ("kernel", "workload", "src_sha256")}
