@@ -892,7 +892,10 @@ def roofline(w, kernel_s, hbm, kind, pk, sms=148):
     element.  `kernel_s` is the kernel's own average duration (CUDA events
     around its launch); `sms` the device's multiprocessor count.  The HBM
     fraction of the same launch (X read once, 2 bytes per element) is
-    reported beside it."""
+    reported beside it, and so are the launch's algorithmic bytes: X, and the
+    chains' operands each read once (the fp16 token coefficients Y16 and U_T16,
+    the fp32 rotated factor rows W of every feature rank, Q U_d and the sign
+    matrix), against which the measured DRAM traffic is compared."""
     U, N = w.n_units, w.elems_per_unit
     RT = max(r for r in w.rT if r != kvgen.FULL)
     RD = max(r for r in w.rd if r != kvgen.FULL)
@@ -906,8 +909,17 @@ def roofline(w, kernel_s, hbm, kind, pk, sms=148):
     peak = sms * 128 * 2 * sm_max * 1e6 / 1e12
     ach = flops / kernel_s / 1e12
     hbm_ach = 2.0 * N * U / kernel_s / 1e9
+    has_full_t = kvgen.FULL in w.rT
+    alg = U * (2 * N                                        # X
+               + (2 * w.H * w.T * RD if has_full_t else 0)  # Y16 (the r_T = T chains)
+               + 2 * nd * w.T * RT                          # U_T16 of every feature rank
+               + 4 * nd * w.H * RT * w.D                    # W rows of every feature rank
+               + 4 * RD * w.D + 2 * w.D * w.D)              # Q U_d, diag(sigma) H
+    traffic = sweep_traffic(w)
     return {"kernel": "sweep_tc_kernel", "bound": "alu", "achieved": ach, "peak": peak,
-            "unit": "TFLOP/s", "frac": ach / peak, "traffic": sweep_traffic(w),
+            "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic,
+            "bytes_algorithmic": int(alg),
+            "traffic_over_algorithmic": None if traffic is None else traffic / alg,
             "kernel_ms": 1e3 * kernel_s,
             "peak_source": f"derived: FP32 pipe, {sms} SMs (device) x 128 lanes x 2 flop x "
                            f"max SM clock",
