@@ -607,6 +607,9 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
     if (last) break;
     // the next block starts from Z2 (equilibrated by the check)
     const size_t tmp = zc; zc = zn; zn = tmp;
+    // a cold start takes two blocks at least: no host round trip before the
+    // second (problems that converge earlier are skipped by their flags)
+    if (!warm && blk == 0) continue;
     bool all = false;
     TRY(read_flags_all(L, P, st, &all));
     if (all) break;
