@@ -38,6 +38,7 @@ struct CqArgs {
   char* base;
   size_t stride;        // problem p at base + p * stride
   size_t src, dst;      // T x 64 input and output blocks (may coincide)
+  size_t vt;            // 64 x T transpose of the output and its tf32 low part (0: none)
   size_t o_status;
   const int* skip;      // optional per-problem flag (ints, stride sk_s): set -> skipped
   long long sk_s;
@@ -183,6 +184,17 @@ cholqr_cluster_kernel(CqArgs a) {
     *reinterpret_cast<float4*>(dst + (size_t)(r0 + r) * CQ_N + 4 * c4) =
         *reinterpret_cast<const float4*>(Z + r * CQ_ZLD + 4 * c4);
   }
+  // the power step's operand: V^T (64 x T) and its tf32 low part
+  if (a.vt) {
+    float* vh = reinterpret_cast<float*>(pb + a.vt);
+    float* vl = vh + (size_t)a.T * CQ_N;
+    for (int e = t; e < CQ_N * nr; e += CQ_THREADS) {
+      const int n = e / nr, r = e % nr;
+      const float v = Z[r * CQ_ZLD + n];
+      vh[(size_t)n * a.T + r0 + r] = v;
+      vl[(size_t)n * a.T + r0 + r] = v - __uint_as_float(__float_as_uint(v) & 0xFFFFE000u);
+    }
+  }
   if (rank == 0 && t == 0 && *bad) atomicOr(reinterpret_cast<int*>(pb + a.o_status), ST_NOTPD);
 }
 
@@ -247,12 +259,12 @@ bool cholqr_fused_supported(int T, int Lw, int np) {
 
 jolt_status cholqr_fused(char* base, size_t stride, int np, size_t src, size_t dst,
                          size_t o_status, const int* skip, long long sk_s, int T, int passes,
-                         float shift, cudaStream_t st) {
+                         float shift, cudaStream_t st, size_t vt) {
   if (np <= 0) return JOLT_OK;
   const int nc = cq_width(T, np);
   if (nc == 0 || passes < 1 || np > 65535) return JOLT_ERR_INVALID;
   CqArgs a;
-  a.base = base; a.stride = stride; a.src = src; a.dst = dst; a.o_status = o_status;
+  a.base = base; a.stride = stride; a.src = src; a.dst = dst; a.vt = vt; a.o_status = o_status;
   a.skip = skip; a.sk_s = sk_s; a.T = T; a.passes = passes; a.shift = shift;
   if (nc == 8) return launch_cq<8>(a, np, st);
   if (nc == 4) return launch_cq<4>(a, np, st);

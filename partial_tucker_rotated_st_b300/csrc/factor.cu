@@ -411,14 +411,20 @@ GemmDesc gd(int M, int N, int K, int nseg, int nb1, int nb2, Opnd A, Opnd B, flo
 // result goes straight to dst.  Problems whose flag is set are skipped when
 // `use_flags`.
 jolt_status cholqr(const Layout& L, const PS& P, int T, int Lw, size_t src, size_t mid, size_t dst,
-                   bool use_flags, bool f64, int passes, float shift, cudaStream_t st) {
+                   bool use_flags, bool f64, int passes, float shift, cudaStream_t st,
+                   bool* vs_written = nullptr) {
   const long long s4 = P.s4();
   const int ks = L.ks, kc = T / L.ks;
   const int* skip = use_flags ? (const int*)P.c(L.p_flag) : nullptr;
   int* status = (int*)P.c(L.p_status);
-  if (!f64 && cholqr_fused_supported(T, Lw, P.np))
+  if (vs_written) *vs_written = false;
+  if (!f64 && cholqr_fused_supported(T, Lw, P.np)) {
+    // the fused kernel also writes the power step's transposed operand
+    const size_t vt = (dst == L.p_V && L.p_Vs != 0) ? L.p_Vs : 0;
+    if (vs_written) *vs_written = vt != 0;
     return cholqr_fused(P.base, P.stride, P.np, src, dst, L.p_status, skip, s4, T, passes, shift,
-                        st);
+                        st, vt);
+  }
   const size_t ins[2] = {src, mid}, outs[2] = {passes == 1 ? dst : mid, dst};
   for (int pass = 0; pass < passes; ++pass) {
     GemmDesc g = gd(Lw, Lw, kc, 1, P.np, ks,
@@ -448,8 +454,10 @@ jolt_status cholqr(const Layout& L, const PS& P, int T, int Lw, size_t src, size
 }
 
 jolt_status cholqr2(const Layout& L, const PS& P, int T, int Lw, size_t src, size_t mid,
-                    size_t dst, bool use_flags, bool f64, cudaStream_t st) {
-  return cholqr(L, P, T, Lw, src, mid, dst, use_flags, f64, 2, f64 ? 0.f : SUB_SHIFT, st);
+                    size_t dst, bool use_flags, bool f64, cudaStream_t st,
+                    bool* vs_written = nullptr) {
+  return cholqr(L, P, T, Lw, src, mid, dst, use_flags, f64, 2, f64 ? 0.f : SUB_SHIFT, st,
+                vs_written);
 }
 
 }  // namespace
@@ -536,11 +544,12 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
     JOLT_LAUNCH_CHECK();
     return JOLT_OK;
   }
+  bool vs_ready = false;   // p_Vs holds the current p_V's transpose and low part
   if (!warm) {
     init_block_kernel<<<dim3(blocks_for((long long)T * Lw), P.np), 256, 0, st>>>(
         P.base, P.stride, L.p_V, T * Lw);
     JOLT_LAUNCH_CHECK();
-    TRY(cholqr2(L, P, T, Lw, L.p_V, L.p_V2, L.p_V, false, false, st));
+    TRY(cholqr2(L, P, T, Lw, L.p_V, L.p_V2, L.p_V, false, false, st, &vs_ready));
   }
   set_int_kernel<<<P.np, 32, 0, st>>>(P.base, P.stride, L.p_flag, 0);
   JOLT_LAUNCH_CHECK();
@@ -552,7 +561,7 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
   // already done), so the roles swap every block
   size_t zc = L.p_Z, zn = L.p_Z2;
   auto apply_S = [&]() -> jolt_status {  // Z = S V
-    if (svtc) return sv_tc(L, P.np, P.base, P.stride, zc, st);
+    if (svtc) return sv_tc(L, P.np, P.base, P.stride, zc, st, vs_ready);
     GemmDesc gg = gd(T, Lw, T, 1, P.np, 1, opnd(P.c(L.p_ST), JOLT_F32, T, 1, 0, s4),
                      opnd(P.c(L.p_V), JOLT_F32, Lw, 1, 0, s4), P.f(zc), Lw, 1, s4, 0, 0.f,
                      flags);
@@ -567,7 +576,7 @@ jolt_status token_exact(const Layout& L, const PS& P, bool warm, cudaStream_t st
     for (int q = 0; q < SUB_STEPS; ++q) {
       if (q > 0 || blk == 0) TRY(apply_S());
       TRY(cholqr(L, P, T, Lw, zc, L.p_V2, L.p_V, true, false, q == SUB_STEPS - 1 ? 2 : 1,
-                 SUB_SHIFT, st));
+                 SUB_SHIFT, st, &vs_ready));
     }
     TRY(apply_S());
     // H = V^T Z, split over row chunks; the eigensolver sums the partials

@@ -766,13 +766,15 @@ jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride,
 
 // Z = S V for every problem not flagged (T x 64 blocks at p_V / o_Z).
 jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, size_t o_Z,
-                  cudaStream_t st) {
+                  cudaStream_t st, bool vs_ready) {
   const int* flags = (const int*)(pbase + L.p_flag);
   const long long f_us = (long long)pstride / 4;
-  dim3 g2((L.T + 31) / 32, 2, np);
-  split_v_kernel<<<g2, dim3(32, 8), 0, st>>>(pbase, pstride, L.p_V, L.p_Vs,
-                                             L.p_Vs + (size_t)L.T * 64 * 4, L.T, flags, f_us);
-  JOLT_LAUNCH_CHECK();
+  if (!vs_ready) {
+    dim3 g2((L.T + 31) / 32, 2, np);
+    split_v_kernel<<<g2, dim3(32, 8), 0, st>>>(pbase, pstride, L.p_V, L.p_Vs,
+                                               L.p_Vs + (size_t)L.T * 64 * 4, L.T, flags, f_us);
+    JOLT_LAUNCH_CHECK();
+  }
   CUtensorMap tS, tSl, tV, tVl;
   const cuuint64_t dS[3] = {(cuuint64_t)L.T, (cuuint64_t)L.T, (cuuint64_t)np};
   const cuuint64_t sS[2] = {(cuuint64_t)L.T * 4, (cuuint64_t)pstride};

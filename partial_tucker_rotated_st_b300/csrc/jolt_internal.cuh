@@ -99,7 +99,7 @@ jolt_status make_layout(const jolt_config* cfg, Layout* L);
 bool cholqr_fused_supported(int T, int Lw, int np);
 jolt_status cholqr_fused(char* base, size_t stride, int np, size_t src, size_t dst,
                          size_t o_status, const int* skip, long long sk_s, int T, int passes,
-                         float shift, cudaStream_t st);
+                         float shift, cudaStream_t st, size_t vt = 0);
 
 // FlashJoLT's range finder with its products over X on the tensor cores: the
 // ranks rid[0..nr) of every unit in lockstep, problem (u, r) at pbase +
@@ -187,9 +187,10 @@ jolt_status gram_feat_tc(const Layout& L, int n_units, const void* X, char* ws, 
 bool sv_tc_supported(const Layout& L);
 // p_STs = tf32 low part of p_ST for np problems.
 jolt_status split_tok_gram(const Layout& L, int np, char* pbase, size_t pstride, cudaStream_t st);
-// (o_Z) = p_ST p_V for every problem whose p_flag is zero.
+// (o_Z) = p_ST p_V for every problem whose p_flag is zero; vs_ready: p_Vs
+// already holds p_V^T and its low part.
 jolt_status sv_tc(const Layout& L, int np, char* pbase, size_t pstride, size_t o_Z,
-                  cudaStream_t st);
+                  cudaStream_t st, bool vs_ready = false);
 bool ygram_tc_supported(const Layout& L);
 // Y = X U_d[:, :RD] (bf16 X, D = 128, RD <= 32) on the tensor cores: U_d16,
 // Y16, Yt and its tf32 low part (when the layout has Yt), and Y in fp32 when

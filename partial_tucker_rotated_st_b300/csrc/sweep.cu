@@ -350,7 +350,8 @@ struct RdList {
 };
 template <int EPT>
 __global__ void build_w_kernel(char* ws, size_t ub, const int8_t* signs, size_t o_G16,
-                               size_t o_QUd, size_t o_W, int H, int RT, RdList rl) {
+                               size_t o_QUd, size_t o_W, int H, int RT, RdList rl, int RD,
+                               int staged) {
   constexpr int D = 32 * EPT;
   const int id = blockIdx.x, u = blockIdx.z, h = blockIdx.y;
   const int rdv = rl.rd[id];
@@ -360,6 +361,17 @@ __global__ void build_w_kernel(char* ws, size_t ub, const int8_t* signs, size_t 
                     (long long)h * RT * rdv;
   float* W = (float*)(base + o_W) + ((long long)id * H + h) * RT * D;
   const float rs = rsqrtf((float)D);
+  // a truncated rank's rows W[k] = G[k] (Q U_d)^T: Q U_d (r_d x D) and this
+  // head's core (RT x r_d) staged in shared memory first
+  extern __shared__ float bw_sm[];
+  float* qsm = bw_sm;                  // [r_d][D]
+  float* gsm = bw_sm + RD * D;         // [RT][r_d]
+  const float* QUg = (const float*)(base + o_QUd);
+  if (staged && rdv < D) {
+    for (int e = threadIdx.x; e < rdv * D; e += blockDim.x) qsm[e] = QUg[e];
+    for (int e = threadIdx.x; e < RT * rdv; e += blockDim.x) gsm[e] = __half2float(G[e]);
+    __syncthreads();
+  }
   for (int k = w; k < RT; k += nw) {
     float v[EPT];
     if (rdv == D) {
@@ -372,13 +384,20 @@ __global__ void build_w_kernel(char* ws, size_t ub, const int8_t* signs, size_t 
 #pragma unroll
       for (int e = 0; e < EPT; ++e) v[e] *= rs;
     } else {
-      const float* QU = (const float*)(base + o_QUd);
 #pragma unroll
       for (int e = 0; e < EPT; ++e) v[e] = 0.f;
-      for (int j = 0; j < rdv; ++j) {
-        const float g = __half2float(G[(long long)k * rdv + j]);
+      if (staged) {
+        for (int j = 0; j < rdv; ++j) {
+          const float g = gsm[k * rdv + j];
 #pragma unroll
-        for (int e = 0; e < EPT; ++e) v[e] = fmaf(g, QU[(long long)j * D + lane * EPT + e], v[e]);
+          for (int e = 0; e < EPT; ++e) v[e] = fmaf(g, qsm[j * D + lane * EPT + e], v[e]);
+        }
+      } else {
+        for (int j = 0; j < rdv; ++j) {
+          const float g = __half2float(G[(long long)k * rdv + j]);
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) v[e] = fmaf(g, QUg[(long long)j * D + lane * EPT + e], v[e]);
+        }
       }
     }
 #pragma unroll
@@ -502,9 +521,14 @@ jolt_status sweep_prep(const Layout& L, int U, const int8_t* signs, char* ws, cu
     RdList rl;
     for (int id = 0; id < JOLT_MAX_GRID; ++id) rl.rd[id] = id < L.nd ? L.rd[id] : 0;
     dim3 g(L.nd, L.H, U);
-    if (EPT == 4) build_w_kernel<4><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl);
-    else if (EPT == 2) build_w_kernel<2><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl);
-    else build_w_kernel<1><<<g, 256, 0, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl);
+    // Q U_d (RD x D) and one head's core (RT x RD) in shared memory when
+    // they fit the default 48 KB, else read from global memory
+    const size_t need = ((size_t)L.RD * L.D + (size_t)L.RT * L.RD) * 4;
+    const int staged = need <= 48 * 1024 ? 1 : 0;
+    const size_t smem = staged ? need : 0;
+    if (EPT == 4) build_w_kernel<4><<<g, 256, smem, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl, L.RD, staged);
+    else if (EPT == 2) build_w_kernel<2><<<g, 256, smem, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl, L.RD, staged);
+    else build_w_kernel<1><<<g, 256, smem, st>>>(ws, ub, signs, L.o_G16, L.o_QUd, L.o_W, L.H, L.RT, rl, L.RD, staged);
     JOLT_LAUNCH_CHECK();
   }
   return JOLT_OK;
