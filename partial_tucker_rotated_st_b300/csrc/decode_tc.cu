@@ -293,14 +293,24 @@ decode_tc_kernel(const __grid_constant__ DecTcArgs a, const __grid_constant__ CU
                                     : reinterpret_cast<const __half*>(blob + du.off_UT) +
                                           (size_t)(in ? row : 0) * du.rT;
       const int k0 = hf * (KW / 2);
-      const bool vec = (K % 8) == 0;          // rows start on 16-byte boundaries
+      // rows start on 16-, 8- or 4-byte boundaries as K is a multiple of 8,
+      // 4 or 2; the widest aligned loads land in pa without being combined,
+      // so nothing waits for them until the next tile is staged
 #pragma unroll
       for (int i = 0; i < KW / 16; ++i) {
         const int k = k0 + 8 * i;
         if (mode == 3 || !in || k >= K) {
           pa[i] = make_uint4(0, 0, 0, 0);
-        } else if (vec) {
+        } else if ((K & 7) == 0) {
           pa[i] = *reinterpret_cast<const uint4*>(src + k);
+        } else if ((K & 3) == 0) {
+          const uint2 lo = *reinterpret_cast<const uint2*>(src + k);
+          const uint2 hi = k + 4 < K ? *reinterpret_cast<const uint2*>(src + k + 4) : make_uint2(0, 0);
+          pa[i] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        } else if ((K & 1) == 0) {
+          const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src + k);
+          pa[i] = make_uint4(s32[0], k + 2 < K ? s32[1] : 0u, k + 4 < K ? s32[2] : 0u,
+                             k + 6 < K ? s32[3] : 0u);
         } else {
           uint32_t hw[4];
 #pragma unroll
@@ -349,11 +359,34 @@ decode_tc_kernel(const __grid_constant__ DecTcArgs a, const __grid_constant__ CU
           // W_h[k][d] = sum_j G_h[k][j] U_d[d][j], split tf32 hi + lo; G_h
           // (r_T x r_d) and U_d (D x r_d) are first staged, in fp32, in this
           // stage's operand area (free: its codes and A rows come after)
+          // (every global read issued before the first is used)
+          constexpr int UQ = DT_D * KW / 512, GQ = KW * KW / 256;   // per-thread bounds
+          __half2 ur[UQ];
+          __half gr[GQ];
+          const __half2* Ud2 = reinterpret_cast<const __half2*>(Ud);
+#pragma unroll
+          for (int i = 0; i < UQ; ++i) {
+            const int e = t + 256 * i;
+            ur[i] = e < DT_D * rd / 2 ? Ud2[e] : __floats2half2_rn(0.f, 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < GQ; ++i) {
+            const int e = t + 256 * i;
+            gr[i] = e < rT * rd ? Gh[e] : __float2half(0.f);
+          }
           float* gs = reinterpret_cast<float*>(sC);
-          for (int e = t; e < rT * rd; e += 256) gs[e] = __half2float(Gh[e]);
-          // the U_d row, staged beside G_h (fp32), read back as a broadcast
+          // U_d, staged beside G_h (fp32); row d is read back as a broadcast
           float* us = gs + rT * rd;
-          for (int e = t; e < DT_D * rd; e += 256) us[e] = __half2float(Ud[e]);
+#pragma unroll
+          for (int i = 0; i < GQ; ++i)
+            if (t + 256 * i < rT * rd) gs[t + 256 * i] = __half2float(gr[i]);
+#pragma unroll
+          for (int i = 0; i < UQ; ++i)
+            if (t + 256 * i < DT_D * rd / 2) {
+              const float2 f = __half22float2(ur[i]);
+              us[2 * (t + 256 * i)] = f.x;
+              us[2 * (t + 256 * i) + 1] = f.y;
+            }
           asm volatile("bar.sync 1, 256;" ::: "memory");
           const float* udr = us + (size_t)d * rd;
           for (int k = kb; k < kb + KW / 2; k += 4) {
