@@ -262,6 +262,119 @@ __global__ void __launch_bounds__(128) attend_prep_kernel(AttArgs a) {
   }
 }
 
+// One chunk CTA's view of its (chunk, head, group): the two blobs, the
+// low-rank row length of each (U_T rows, or G rows when r_T = T), whether
+// the rows are short enough to stage, and the chunk's first rows.
+struct ChunkView {
+  int chunk, h, g, t0, n, Kk, Kv, kcb, vcb;   // kcb, vcb: code bytes per row
+  bool kst, vst;
+  AttUnit ku, vu;
+  const char* kb;
+  const char* vb;
+  const __half* kR;
+  const __half* vR;
+};
+
+template <int D>
+__device__ __forceinline__ ChunkView chunk_view(const AttArgs& a) {
+  ChunkView c;
+  c.chunk = blockIdx.x;
+  c.h = blockIdx.y;
+  const int gl = blockIdx.z, T = a.T;
+  c.g = a.g0 + gl;
+  c.t0 = c.chunk * ATT_CHUNK;
+  c.n = min(ATT_CHUNK, T - c.t0);
+  c.ku = a.k[gl];
+  c.vu = a.v[gl];
+  c.kb = a.blob + (unsigned long long)(2 * c.g) * a.stride;
+  c.vb = a.blob + (unsigned long long)(2 * c.g + 1) * a.stride;
+  const bool kfT = (c.ku.rT == T), vfT = (c.vu.rT == T);
+  c.Kk = kfT ? c.ku.rd : c.ku.rT;
+  c.Kv = vfT ? c.vu.rd : c.vu.rT;
+  c.kst = c.Kk <= ATT_STAGE_RANK;
+  c.vst = c.Kv <= ATT_STAGE_RANK;
+  c.kR = kfT ? (const __half*)(c.kb + c.ku.off_G) + ((size_t)c.h * T + c.t0) * c.ku.rd
+             : (const __half*)(c.kb + c.ku.off_UT) + (size_t)c.t0 * c.ku.rT;
+  c.vR = vfT ? (const __half*)(c.vb + c.vu.off_G) + ((size_t)c.h * T + c.t0) * c.vu.rd
+             : (const __half*)(c.vb + c.vu.off_UT) + (size_t)c.t0 * c.vu.rT;
+  c.kcb = D * c.ku.b / 8;
+  c.vcb = D * c.vu.b / 8;
+  return c;
+}
+
+// Everything the CTA reads, in flight at once: the chunk's codes and short
+// low-rank rows of both blobs and the V scales (into sv), then, once the
+// prep grid has finished, c and v~ (into qcs).  Returns this thread's token's
+// K scale.
+template <int D, int NQ>
+__device__ __forceinline__ float chunk_stage(const AttArgs& a, const ChunkView& c, float* qcs,
+                                             float* sv, char* data, int tid) {
+  const int T = a.T, t = c.t0 + tid;
+  // the merge grid may start staging its factors
+  asm volatile("griddepcontrol.launch_dependents;");
+  if (c.ku.b > 0)
+    copy_async(data, c.kb + c.ku.off_codes + ((size_t)c.h * T + c.t0) * c.kcb, c.n * c.kcb, tid,
+               ATT_CHUNK);
+  if (c.kst) copy_async(data + a.o_kr, c.kR, c.n * c.Kk * 2, tid, ATT_CHUNK);
+  if (c.vu.b > 0)
+    copy_async(data + a.o_vc, c.vb + c.vu.off_codes + ((size_t)c.h * T + c.t0) * c.vcb,
+               c.n * c.vcb, tid, ATT_CHUNK);
+  if (c.vst) copy_async(data + a.o_vr, c.vR, c.n * c.Kv * 2, tid, ATT_CHUNK);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  const float ks =
+      (c.ku.b > 0 && t < T)
+          ? __half2float(((const __half*)(c.kb + c.ku.off_scale))[(size_t)c.h * T + t]) : 0.f;
+  sv[tid] = (c.vu.b > 0 && t < T)
+                ? __half2float(((const __half*)(c.vb + c.vu.off_scale))[(size_t)c.h * T + t]) : 0.f;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  copy_async(qcs, a.qc + ((size_t)c.g * a.H + c.h) * (KM + D) * NQ, (KM + D) * NQ * 4, tid,
+             ATT_CHUNK);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  return ks;
+}
+
+// Phase 2: the chunk's scores sc[x][i] become probabilities against the
+// chunk's max (a warp per query); stat gets the max and the sum.
+template <int NQ>
+__device__ __forceinline__ void chunk_softmax(float* sc, float* stat, int w, int lane) {
+  for (int i = w; i < NQ; i += ATT_WARPS) {
+    float m = -INFINITY;
+    for (int x = lane; x < ATT_CHUNK; x += 32) m = fmaxf(m, sc[x * NQ + i]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int x = lane; x < ATT_CHUNK; x += 32) {
+      const float p = expf(sc[x * NQ + i] - m);
+      sc[x * NQ + i] = p;
+      l += p;
+    }
+    l = warp_sum(l);
+    if (lane == 0) { stat[i] = m; stat[8 + i] = l; }
+  }
+}
+
+// The chunk's record: max, sum, then z and cv of each query, summed over
+// the warps' partials red[warp][query][D + KM].
+template <int D, int NQ>
+__device__ __forceinline__ void chunk_record(const AttArgs& a, const ChunkView& c,
+                                             const float* stat, const float* red, int tid) {
+  const int nq = a.nq;
+  float* rec = a.part + (((size_t)c.g * a.H + c.h) * a.nch + c.chunk) * rec_floats(nq, D);
+  if (tid < nq) {
+    rec[tid] = stat[tid];
+    rec[nq + tid] = stat[8 + tid];
+  }
+  for (int x = tid; x < nq * (D + KM); x += ATT_CHUNK) {
+    const int i = x / (D + KM), col = x % (D + KM);
+    if (col >= D + c.Kv) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < ATT_WARPS; ++ww) s += red[(size_t)ww * NQ * (D + KM) + i * (D + KM) + col];
+    rec[2 * nq + (size_t)i * (D + KM) + col] = s;
+  }
+}
+
 template <int EPT, int NQ>
 __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
   constexpr int D = 32 * EPT;
@@ -271,46 +384,11 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
   float* stat = sc + ATT_CHUNK * NQ;      // [2][8]        max, sum
   float* sv = stat + 16;                  // [CHUNK]       V scales
   char* data = reinterpret_cast<char*>(sv + ATT_CHUNK);   // codes and rows; later the partials
-  const int chunk = blockIdx.x, h = blockIdx.y, gl = blockIdx.z;
-  const int g = a.g0 + gl;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int T = a.T, H = a.H, nq = a.nq;
-  const int t0 = chunk * ATT_CHUNK, t = t0 + tid;
-  const int n = min(ATT_CHUNK, T - t0);
-  const AttUnit ku = a.k[gl], vu = a.v[gl];
-  const char* kb = a.blob + (unsigned long long)(2 * g) * a.stride;
-  const char* vb = a.blob + (unsigned long long)(2 * g + 1) * a.stride;
-  const bool kfT = (ku.rT == T), vfT = (vu.rT == T);
-  const int Kk = kfT ? ku.rd : ku.rT, Kv = vfT ? vu.rd : vu.rT;
-  const bool kst = Kk <= ATT_STAGE_RANK, vst = Kv <= ATT_STAGE_RANK;
-  const __half* kR = kfT ? (const __half*)(kb + ku.off_G) + ((size_t)h * T + t0) * ku.rd
-                         : (const __half*)(kb + ku.off_UT) + (size_t)t0 * ku.rT;
-  const __half* vR = vfT ? (const __half*)(vb + vu.off_G) + ((size_t)h * T + t0) * vu.rd
-                         : (const __half*)(vb + vu.off_UT) + (size_t)t0 * vu.rT;
-  const size_t kcb = (size_t)D * ku.b / 8, vcb = (size_t)D * vu.b / 8;   // code bytes per row
-
-  // the merge grid may start staging its factors
-  asm volatile("griddepcontrol.launch_dependents;");
-  // ---- everything the CTA reads, in flight at once (c and v~ once the
-  // prep grid has finished)
-  if (ku.b > 0)
-    copy_async(data, kb + ku.off_codes + ((size_t)h * T + t0) * kcb, (int)(n * kcb), tid,
-               ATT_CHUNK);
-  if (kst) copy_async(data + a.o_kr, kR, n * Kk * 2, tid, ATT_CHUNK);
-  if (vu.b > 0)
-    copy_async(data + a.o_vc, vb + vu.off_codes + ((size_t)h * T + t0) * vcb, (int)(n * vcb), tid,
-               ATT_CHUNK);
-  if (vst) copy_async(data + a.o_vr, vR, n * Kv * 2, tid, ATT_CHUNK);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  const float ks = (ku.b > 0 && t < T)
-                       ? __half2float(((const __half*)(kb + ku.off_scale))[(size_t)h * T + t]) : 0.f;
-  sv[tid] = (vu.b > 0 && t < T)
-                ? __half2float(((const __half*)(vb + vu.off_scale))[(size_t)h * T + t]) : 0.f;
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  copy_async(qcs, a.qc + ((size_t)g * H + h) * (KM + D) * NQ, (KM + D) * NQ * 4, tid, ATT_CHUNK);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
+  const ChunkView c = chunk_view<D>(a);
+  const AttUnit ku = c.ku, vu = c.vu;
+  const int T = a.T, t = c.t0 + tid, n = c.n, Kk = c.Kk, Kv = c.Kv;
+  const float ks = chunk_stage<D, NQ>(a, c, qcs, sv, data, tid);
 
   // ---- phase 1: one thread per token, the scores of every query
   {
@@ -318,8 +396,8 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
 #pragma unroll
     for (int i = 0; i < NQ; ++i) acc[i] = 0.f;
     if (t < T) {
-      const __half* R = kst ? reinterpret_cast<const __half*>(data + a.o_kr) + (size_t)tid * Kk
-                            : kR + (size_t)tid * Kk;
+      const __half* R = c.kst ? reinterpret_cast<const __half*>(data + a.o_kr) + (size_t)tid * Kk
+                              : c.kR + (size_t)tid * Kk;
       if ((Kk & 1) == 0) {
         const __half2* R2 = reinterpret_cast<const __half2*>(R);
 #pragma unroll 8
@@ -343,7 +421,7 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
       }
       if (ku.b > 0) {
         float r[NQ];
-        const uint32_t* cw = reinterpret_cast<const uint32_t*>(data + tid * kcb);
+        const uint32_t* cw = reinterpret_cast<const uint32_t*>(data + tid * c.kcb);
         const float* vt = qcs + KM * NQ;
         if (ku.b == 2) res_dots<D, NQ, 2>(cw, vt, r);
         else if (ku.b == 4) res_dots<D, NQ, 4>(cw, vt, r);
@@ -356,21 +434,7 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
     for (int i = 0; i < NQ; ++i) sc[tid * NQ + i] = (t < T) ? a.scale * acc[i] : -INFINITY;
   }
   __syncthreads();
-
-  // ---- phase 2: probabilities against the chunk's max (a warp per query)
-  for (int i = w; i < NQ; i += ATT_WARPS) {
-    float m = -INFINITY;
-    for (int x = lane; x < ATT_CHUNK; x += 32) m = fmaxf(m, sc[x * NQ + i]);
-    m = warp_max(m);
-    float l = 0.f;
-    for (int x = lane; x < ATT_CHUNK; x += 32) {
-      const float p = expf(sc[x * NQ + i] - m);
-      sc[x * NQ + i] = p;
-      l += p;
-    }
-    l = warp_sum(l);
-    if (lane == 0) { stat[i] = m; stat[8 + i] = l; }
-  }
+  chunk_softmax<NQ>(sc, stat, w, lane);
   __syncthreads();
 
   // ---- phase 3: cv and z over this warp's 32 tokens
@@ -386,7 +450,7 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
   {
     const uint32_t* cvw = reinterpret_cast<const uint32_t*>(data + a.o_vc);
     const int rw = D * vu.b / 32;
-    const __half* Rb = vst ? reinterpret_cast<const __half*>(data + a.o_vr) : vR;
+    const __half* Rb = c.vst ? reinterpret_cast<const __half*>(data + a.o_vr) : c.vR;
     const int ntok = min(32, n - w * 32);
 #pragma unroll 4
     for (int j = 0; j < ntok; ++j) {
@@ -425,21 +489,362 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_kernel(AttArgs a) {
     for (int jj = 0; jj < KPL; ++jj) rw_[i * (D + KM) + D + lane + 32 * jj] = cv[i][jj];
   }
   __syncthreads();
+  chunk_record<D, NQ>(a, c, stat, red, tid);
+}
 
-  // ---- the chunk's record: max, sum, z, cv (summed over the warps)
-  float* rec = a.part + (((size_t)g * H + h) * a.nch + chunk) * rec_floats(nq, D);
-  if (tid < nq) {
-    rec[tid] = stat[tid];
-    rec[nq + tid] = stat[8 + tid];
-  }
-  for (int x = tid; x < nq * (D + KM); x += ATT_CHUNK) {
-    const int i = x / (D + KM), c = x % (D + KM);
-    if (c >= D + Kv) continue;
-    float s = 0.f;
+// ------------------------------------------------ tensor-core chunk, D = 128
+// The same three phases for D = 128 with the per-token contractions on
+// mma.sync m16n8k16 (fp16 operands, fp32 accumulators; a warp's 32 tokens
+// are two 16-row tiles, the queries the 8 columns):
+//   phase 1   scores = R_K[t] . c  +  s_t (u_t - 2^(b-1)) . v~   (K = k, d)
+//   phase 3   cv^T = R_V^T p,  z^T = (u - 2^(b-1))^T (p s)       (K = tokens)
+// The integer codes and the fp16 rows are exact fp16 operands.  The fp32
+// side of each product (c, v~, p, p s) is scaled by a power of two that
+// brings its largest magnitude just below 2^14, then split into fp16 hi +
+// lo (hi = fp16(x), lo = fp16(x - hi)): two MMAs carry 22 bits of each
+// value, against the 24 of the fp32 FMAs, and the scale comes off exactly.
+// The codes are unpacked as in the decoder (0x6400 | u = 1024 + u, less
+// 1024 + 2^(b-1) in half2), sixteen codes of one row at a time, in the
+// order unpack16 gives; the K (or M) index of each product follows that
+// order, and the other operand is built in the same order.
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 u2h(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+// The power of two that brings a largest magnitude m just below 2^14 (1
+// for m = 0), built from m's exponent field and clamped to the normal range.
+__device__ __forceinline__ float fp16_scale(float m) {
+  if (!(m > 0.f)) return 1.f;
+  const int e = ((__float_as_int(m) >> 23) & 0xFF) - 126;   // m < 2^e
+  const int k = max(-126, min(127, 14 - e));
+  return __int_as_float((127 + k) << 23);
+}
+
+// hi and lo fp16 parts of two values, packed as half2 (first value low).
+__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+  hi = h2u(__halves2half2(h0, h1));
+  lo = h2u(__floats2half2_rn(x0 - __half2float(h0), x1 - __half2float(h1)));
+}
+
+// Position, within a group of sixteen codes, of the p-th value unpack16
+// gives (value pair m holds positions (lpos(2m), lpos(2m + 1))).
+template <int B>
+__device__ __forceinline__ int lpos(int p) {
+  const int m = p >> 1, e = p & 1;
+  if constexpr (B == 2) return 8 * (m & 1) + 4 * e + (m >> 1);
+  else if constexpr (B == 4) return 8 * (m >> 2) + 4 * (m & 1) + ((m & 3) >> 1) + 2 * e;
+  else return p;
+}
+
+// Sixteen b-bit codes (b / 2 words, code i at bits b i) as eight half2 of
+// u - 2^(b-1), in lpos order.
+template <int B>
+__device__ __forceinline__ void unpack16(const uint32_t* w, uint32_t (&hv)[8]) {
+  if constexpr (B == 2) {
 #pragma unroll
-    for (int ww = 0; ww < ATT_WARPS; ++ww) s += red[(size_t)ww * NQ * (D + KM) + i * (D + KM) + c];
-    rec[2 * nq + (size_t)i * (D + KM) + c] = s;
+    for (int s = 0; s < 4; ++s) {
+      const uint32_t x = (w[0] >> (2 * s)) & 0x03030303u;
+      hv[2 * s] = __byte_perm(x, 0x64646464u, 0x5140);
+      hv[2 * s + 1] = __byte_perm(x, 0x64646464u, 0x7362);
+    }
+  } else if constexpr (B == 4) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint32_t ev = w[j] & 0x0F0F0F0Fu, od = (w[j] >> 4) & 0x0F0F0F0Fu;
+      hv[4 * j] = __byte_perm(ev, 0x64646464u, 0x5140);
+      hv[4 * j + 1] = __byte_perm(ev, 0x64646464u, 0x7362);
+      hv[4 * j + 2] = __byte_perm(od, 0x64646464u, 0x5140);
+      hv[4 * j + 3] = __byte_perm(od, 0x64646464u, 0x7362);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hv[2 * j] = __byte_perm(w[j], 0x64646464u, 0x5140);
+      hv[2 * j + 1] = __byte_perm(w[j], 0x64646464u, 0x7362);
+    }
   }
+  const __half2 off = u2h(0x64006400u | (1u << (B - 1)) | (1u << (B + 15)));
+#pragma unroll
+  for (int m = 0; m < 8; ++m) hv[m] = h2u(__hsub2(u2h(hv[m]), off));
+}
+
+// n consecutive 32-bit words of shared memory (n = 1, 2, 4 or 8, 16-byte
+// aligned for n >= 4).
+template <int N>
+__device__ __forceinline__ void lds_words(const uint32_t* p, uint32_t (&o)[N]) {
+  if constexpr (N == 1) {
+    o[0] = p[0];
+  } else if constexpr (N == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    o[0] = v.x; o[1] = v.y;
+  } else {
+#pragma unroll
+    for (int q = 0; q < N / 4; ++q) {
+      const uint4 v = reinterpret_cast<const uint4*>(p)[q];
+      o[4 * q] = v.x; o[4 * q + 1] = v.y; o[4 * q + 2] = v.z; o[4 * q + 3] = v.w;
+    }
+  }
+}
+
+// Phase 1, residual: acc[mt] += (scaled) v~ . (u - 2^(b-1)) for the warp's
+// two 16-token tiles.  Thread (g, q) of the MMA layout takes the 32 codes
+// d in [32 q, 32 q + 32) of its rows, sixteen per k-block group: k-block kb
+// (0..7) uses group kb / 4, value pairs 2 (kb % 4) and 2 (kb % 4) + 1.
+template <int B, int NQ>
+__device__ __forceinline__ float res_scores_tc(const char* codes, int kcb, const float* vt,
+                                               int w, int lane, float (&acc)[2][4]) {
+  const int mg = lane >> 2, mq = lane & 3;
+  uint32_t bh[8][2], bl[8][2];
+  float vmax = 0.f;
+  {
+    float vv[8][4];
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int d = 32 * mq + 16 * (kb >> 2) + lpos<B>(4 * (kb & 3) + e);
+        vv[kb][e] = mg < NQ ? vt[d * NQ + mg] : 0.f;
+        vmax = fmaxf(vmax, fabsf(vv[kb][e]));
+      }
+    const float sig = fp16_scale(warp_max(vmax));
+    vmax = sig;
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      split_h2(vv[kb][0] * sig, vv[kb][1] * sig, bh[kb][0], bl[kb][0]);
+      split_h2(vv[kb][2] * sig, vv[kb][3] * sig, bh[kb][1], bl[kb][1]);
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int x0 = 32 * w + 16 * mt + mg;
+    uint32_t w0[B], w1[B];
+    lds_words<B>(reinterpret_cast<const uint32_t*>(codes + x0 * kcb) + mq * B, w0);
+    lds_words<B>(reinterpret_cast<const uint32_t*>(codes + (x0 + 8) * kcb) + mq * B, w1);
+    uint32_t h0[2][8], h1[2][8];
+    unpack16<B>(w0, h0[0]);
+    unpack16<B>(w0 + B / 2, h0[1]);
+    unpack16<B>(w1, h1[0]);
+    unpack16<B>(w1 + B / 2, h1[1]);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+      const int gq = kb >> 2, m2 = 2 * (kb & 3);
+      mma16816(acc[mt], h0[gq][m2], h1[gq][m2], h0[gq][m2 + 1], h1[gq][m2 + 1], bh[kb][0], bh[kb][1]);
+      mma16816(acc[mt], h0[gq][m2], h1[gq][m2], h0[gq][m2 + 1], h1[gq][m2 + 1], bl[kb][0], bl[kb][1]);
+    }
+  }
+  return 1.f / vmax;   // the inverse scale (a power of two)
+}
+
+// Two fp16 values of low-rank rows as one half2: row x0 at k and row x1 at
+// k (pair = false), or row x0 at k and k + 1 (pair = true); zero past the
+// row length K or the chunk's n rows.
+__device__ __forceinline__ uint32_t row_pair(const __half* R, int K, int n, int x0, int x1, int k,
+                                             bool pair) {
+  const unsigned short z = 0;
+  unsigned short v0, v1;
+  if (pair) {
+    v0 = (x0 < n && k < K) ? __half_as_ushort(R[(size_t)x0 * K + k]) : z;
+    v1 = (x0 < n && k + 1 < K) ? __half_as_ushort(R[(size_t)x0 * K + k + 1]) : z;
+  } else {
+    v0 = (x0 < n && k < K) ? __half_as_ushort(R[(size_t)x0 * K + k]) : z;
+    v1 = (x1 < n && k < K) ? __half_as_ushort(R[(size_t)x1 * K + k]) : z;
+  }
+  return (uint32_t)v0 | ((uint32_t)v1 << 16);
+}
+
+template <int NQ>
+__global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
+  constexpr int D = 128;
+  extern __shared__ __align__(16) float asm_[];
+  float* qcs = asm_;                      // [KM + D][NQ]  c, then v~
+  float* sc = qcs + (KM + D) * NQ;        // [CHUNK][NQ]   scores, then p
+  float* stat = sc + ATT_CHUNK * NQ;      // [2][8]        max, sum
+  float* sv = stat + 16;                  // [CHUNK]       V scales
+  char* data = reinterpret_cast<char*>(sv + ATT_CHUNK);   // codes and rows; later the partials
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int mg = lane >> 2, mq = lane & 3;   // MMA fragment row group, column pair
+  const ChunkView c = chunk_view<D>(a);
+  const int n = c.n, Kk = c.Kk, Kv = c.Kv;
+  const float ks = chunk_stage<D, NQ>(a, c, qcs, sv, data, tid);
+
+  // ---- phase 1: scores of the warp's 32 tokens (rows 16 mt + mg, + 8)
+  {
+    float accr[2][4] = {}, accl[2][4] = {};
+    float ir = 0.f;
+    if (c.ku.b == 2) ir = res_scores_tc<2, NQ>(data, c.kcb, qcs + KM * NQ, w, lane, accr);
+    else if (c.ku.b == 4) ir = res_scores_tc<4, NQ>(data, c.kcb, qcs + KM * NQ, w, lane, accr);
+    else if (c.ku.b == 8) ir = res_scores_tc<8, NQ>(data, c.kcb, qcs + KM * NQ, w, lane, accr);
+    // low rank: R_K[t] . c, k-blocks of 16 (thread pairs 2 mq, 2 mq + 8)
+    const int nkb = (Kk + 15) >> 4;
+    float cmax = 0.f;
+    for (int kb = 0; kb < nkb; ++kb)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 16 * kb + 2 * mq + (e & 1) + 8 * (e >> 1);
+        if (k < Kk && mg < NQ) cmax = fmaxf(cmax, fabsf(qcs[k * NQ + mg]));
+      }
+    const float sl = fp16_scale(warp_max(cmax));
+    const __half* R = c.kst ? reinterpret_cast<const __half*>(data + a.o_kr) : c.kR;
+    for (int kb = 0; kb < nkb; ++kb) {
+      float cv4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int k = 16 * kb + 2 * mq + (e & 1) + 8 * (e >> 1);
+        cv4[e] = (k < Kk && mg < NQ) ? qcs[k * NQ + mg] * sl : 0.f;
+      }
+      uint32_t bh0, bl0, bh1, bl1;
+      split_h2(cv4[0], cv4[1], bh0, bl0);
+      split_h2(cv4[2], cv4[3], bh1, bl1);
+      const int k0 = 16 * kb + 2 * mq;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int x0 = 32 * w + 16 * mt + mg, x1 = x0 + 8;
+        const uint32_t a0 = row_pair(R, Kk, n, x0, x0, k0, true);
+        const uint32_t a1 = row_pair(R, Kk, n, x1, x1, k0, true);
+        const uint32_t a2 = row_pair(R, Kk, n, x0, x0, k0 + 8, true);
+        const uint32_t a3 = row_pair(R, Kk, n, x1, x1, k0 + 8, true);
+        mma16816(accl[mt], a0, a1, a2, a3, bh0, bh1);
+        mma16816(accl[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+    }
+    const float il = 1.f / sl;
+    // score = scale (lr + s_t res); c0, c1: row mg, queries 2 mq, 2 mq + 1;
+    // c2, c3: row mg + 8; the K scale of token x sits in lane x % 32
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int xr = 16 * mt + mg + 8 * hr, x = 32 * w + xr;
+        const float kx = __shfl_sync(0xffffffffu, ks, xr);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int i = 2 * mq + j;
+          const float s = a.scale * fmaf(kx, accr[mt][2 * hr + j] * ir, accl[mt][2 * hr + j] * il);
+          if (i < NQ) sc[x * NQ + i] = x < n ? s : -INFINITY;
+        }
+      }
+  }
+  __syncthreads();
+  chunk_softmax<NQ>(sc, stat, w, lane);
+  __syncthreads();
+
+  // ---- phase 3: z^T (d x queries) and cv^T (k x queries) over the warp's
+  // 32 tokens, two k-blocks of 16 (thread tokens 2 mq, 2 mq + 1, + 8, + 9)
+  float zacc[8][4] = {}, cacc[8][4] = {};
+  const int vb = c.vu.b;
+  float pmax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; j += 8) pmax = fmaxf(pmax, sv[32 * w + j + (lane & 7)]);
+  const float sz = fp16_scale(warp_max(pmax));   // p s <= max s: p <= 1
+  const float sp = 16384.f;                       // p <= 1
+  const int nmk = (Kv + 15) >> 4;
+  const __half* RV = c.vst ? reinterpret_cast<const __half*>(data + a.o_vr) : c.vR;
+  const char* vcodes = data + a.o_vc;
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    const int xb = 32 * w + 16 * kb + 2 * mq;
+    const int xs[4] = {xb, xb + 1, xb + 8, xb + 9};
+    float p[4], ps[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      p[e] = mg < NQ ? sc[xs[e] * NQ + mg] : 0.f;
+      ps[e] = p[e] * sv[xs[e]] * sz;
+      p[e] *= sp;
+    }
+    uint32_t bzh0, bzl0, bzh1, bzl1, bch0, bcl0, bch1, bcl1;
+    split_h2(ps[0], ps[1], bzh0, bzl0);
+    split_h2(ps[2], ps[3], bzh1, bzl1);
+    split_h2(p[0], p[1], bch0, bcl0);
+    split_h2(p[2], p[3], bch1, bcl1);
+    if (vb > 0) {
+      uint32_t hv[4][8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(vcodes + xs[e] * c.vcb);
+        if (vb == 2) {
+          uint32_t wd[1];
+          lds_words<1>(row + mg, wd);
+          unpack16<2>(wd, hv[e]);
+        } else if (vb == 4) {
+          uint32_t wd[2];
+          lds_words<2>(row + 2 * mg, wd);
+          unpack16<4>(wd, hv[e]);
+        } else {
+          uint32_t wd[4];
+          lds_words<4>(row + 4 * mg, wd);
+          unpack16<8>(wd, hv[e]);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint32_t a0 = __byte_perm(hv[0][m], hv[1][m], 0x5410);
+        const uint32_t a1 = __byte_perm(hv[0][m], hv[1][m], 0x7632);
+        const uint32_t a2 = __byte_perm(hv[2][m], hv[3][m], 0x5410);
+        const uint32_t a3 = __byte_perm(hv[2][m], hv[3][m], 0x7632);
+        mma16816(zacc[m], a0, a1, a2, a3, bzh0, bzh1);
+        mma16816(zacc[m], a0, a1, a2, a3, bzl0, bzl1);
+      }
+    }
+#pragma unroll
+    for (int mk = 0; mk < 8; ++mk) {
+      if (mk < nmk) {
+        const int k0 = 16 * mk + mg;
+        const uint32_t a0 = row_pair(RV, Kv, n, xs[0], xs[1], k0, false);
+        const uint32_t a1 = row_pair(RV, Kv, n, xs[0], xs[1], k0 + 8, false);
+        const uint32_t a2 = row_pair(RV, Kv, n, xs[2], xs[3], k0, false);
+        const uint32_t a3 = row_pair(RV, Kv, n, xs[2], xs[3], k0 + 8, false);
+        mma16816(cacc[mk], a0, a1, a2, a3, bch0, bch1);
+        mma16816(cacc[mk], a0, a1, a2, a3, bcl0, bcl1);
+      }
+    }
+  }
+  __syncthreads();   // the data region becomes the per-warp partial sums
+  float* red = reinterpret_cast<float*>(data);
+  float* rw_ = red + (size_t)w * NQ * (D + KM);
+  const float iz = 1.f / sz, ip = 1.f / sp;
+  // z^T rows of tile m: mg <-> d = 16 mg + lpos(2 m), mg + 8 <-> lpos(2 m + 1)
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    int d0, d1;
+    if (vb == 2) { d0 = lpos<2>(2 * m); d1 = lpos<2>(2 * m + 1); }
+    else if (vb == 4) { d0 = lpos<4>(2 * m); d1 = lpos<4>(2 * m + 1); }
+    else { d0 = 2 * m; d1 = 2 * m + 1; }
+    d0 += 16 * mg;
+    d1 += 16 * mg;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int i = 2 * mq + j;
+      if (i < NQ) {
+        rw_[i * (D + KM) + d0] = zacc[m][j] * iz;
+        rw_[i * (D + KM) + d1] = zacc[m][2 + j] * iz;
+      }
+    }
+  }
+#pragma unroll
+  for (int mk = 0; mk < 8; ++mk) {
+    if (mk < nmk) {
+      const int k0 = 16 * mk + mg;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int i = 2 * mq + j;
+        if (i < NQ) {
+          rw_[i * (D + KM) + D + k0] = cacc[mk][j] * ip;
+          rw_[i * (D + KM) + D + k0 + 8] = cacc[mk][2 + j] * ip;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  chunk_record<D, NQ>(a, c, stat, red, tid);
 }
 
 // Merge the chunks of one (head, group, query) and map back to feature space.
@@ -535,10 +940,12 @@ jolt_status launch_attend(const AttArgs& a, int ng, cudaStream_t st) {
   constexpr int D = 32 * EPT;
   const size_t smem = sizeof(float) * ((KM + D) * NQ + ATT_CHUNK * NQ + 16 + ATT_CHUNK) + a.data;
   if (smem > 227 * 1024) return JOLT_ERR_INVALID;
+  // D = 128 takes the tensor-core chunk kernel
+  auto chunk = EPT == 4 ? attend_chunk_tc_kernel<NQ> : attend_chunk_kernel<EPT, NQ>;
   static int attr = 0;
   if ((int)smem > attr) {
-    JOLT_CUDA_TRY(cudaFuncSetAttribute(attend_chunk_kernel<EPT, NQ>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    JOLT_CUDA_TRY(
+        cudaFuncSetAttribute(chunk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     attr = (int)smem;
   }
   attend_prep_kernel<EPT, NQ><<<dim3(a.H, ng), 128, 0, st>>>(a);
@@ -557,7 +964,7 @@ jolt_status launch_attend(const AttArgs& a, int ng, cudaStream_t st) {
   cfg.gridDim = dim3(a.nch, a.H, ng);
   cfg.blockDim = dim3(ATT_CHUNK);
   cfg.dynamicSmemBytes = smem;
-  JOLT_CUDA_TRY(cudaLaunchKernelEx(&cfg, attend_chunk_kernel<EPT, NQ>, a));
+  JOLT_CUDA_TRY(cudaLaunchKernelEx(&cfg, chunk, a));
   JOLT_LAUNCH_CHECK();
   cfg.gridDim = dim3(a.H, ng, a.nq);
   cfg.blockDim = dim3(128);
