@@ -302,11 +302,25 @@ __device__ __forceinline__ ChunkView chunk_view(const AttArgs& a) {
   return c;
 }
 
+// n rows of row_bytes (a multiple of 16; 16-byte aligned source) from
+// global to shared memory at a pitch of row_bytes + 16, 16 bytes per copy.
+__device__ __forceinline__ void copy_rows_async(char* dst, const char* src, int n, int row_bytes,
+                                                int tid, int nthr) {
+  const int per = row_bytes >> 4;
+  for (int p = tid; p < n * per; p += nthr) {
+    const int r = p / per, q = p - r * per;
+    const uint32_t sd = (uint32_t)__cvta_generic_to_shared(dst + r * (row_bytes + 16) + 16 * q);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sd), "l"(src + 16 * p)
+                 : "memory");
+  }
+}
+
 // Everything the CTA reads, in flight at once: the chunk's codes and short
 // low-rank rows of both blobs and the V scales (into sv), then, once the
-// prep grid has finished, c and v~ (into qcs).  Returns this thread's token's
-// K scale.
-template <int D, int NQ>
+// prep grid has finished, c and v~ (into qcs).  PADV: the V code rows land
+// at a pitch of 16 bytes more than their length.  Returns this thread's
+// token's K scale.
+template <int D, int NQ, bool PADV = false>
 __device__ __forceinline__ float chunk_stage(const AttArgs& a, const ChunkView& c, float* qcs,
                                              float* sv, char* data, int tid) {
   const int T = a.T, t = c.t0 + tid;
@@ -316,9 +330,11 @@ __device__ __forceinline__ float chunk_stage(const AttArgs& a, const ChunkView& 
     copy_async(data, c.kb + c.ku.off_codes + ((size_t)c.h * T + c.t0) * c.kcb, c.n * c.kcb, tid,
                ATT_CHUNK);
   if (c.kst) copy_async(data + a.o_kr, c.kR, c.n * c.Kk * 2, tid, ATT_CHUNK);
-  if (c.vu.b > 0)
-    copy_async(data + a.o_vc, c.vb + c.vu.off_codes + ((size_t)c.h * T + c.t0) * c.vcb,
-               c.n * c.vcb, tid, ATT_CHUNK);
+  if (c.vu.b > 0) {
+    const char* src = c.vb + c.vu.off_codes + ((size_t)c.h * T + c.t0) * c.vcb;
+    if (PADV) copy_rows_async(data + a.o_vc, src, c.n, c.vcb, tid, ATT_CHUNK);
+    else copy_async(data + a.o_vc, src, c.n * c.vcb, tid, ATT_CHUNK);
+  }
   if (c.vst) copy_async(data + a.o_vr, c.vR, c.n * c.Kv * 2, tid, ATT_CHUNK);
   asm volatile("cp.async.commit_group;" ::: "memory");
   const float ks =
@@ -661,6 +677,13 @@ __device__ __forceinline__ uint32_t row_pair(const __half* R, int K, int n, int 
   return (uint32_t)v0 | ((uint32_t)v1 << 16);
 }
 
+// Per-warp partial sums of the tensor-core chunk: a row of NQ floats per
+// entry (z at d, then cv at D + k), each 16 entries followed by one unused
+// row, so that the 8-byte stores of a fragment (8 row groups x 4 query
+// pairs) fall in different banks.
+constexpr int TC_RED_ROWS = (128 + KM) + (128 + KM) / 16;
+__device__ __forceinline__ int tc_red_row(int e) { return e + (e >> 4); }
+
 template <int NQ>
 __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
   constexpr int D = 128;
@@ -674,7 +697,7 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
   const int mg = lane >> 2, mq = lane & 3;   // MMA fragment row group, column pair
   const ChunkView c = chunk_view<D>(a);
   const int n = c.n, Kk = c.Kk, Kv = c.Kv;
-  const float ks = chunk_stage<D, NQ>(a, c, qcs, sv, data, tid);
+  const float ks = chunk_stage<D, NQ, true>(a, c, qcs, sv, data, tid);
 
   // ---- phase 1: scores of the warp's 32 tokens (rows 16 mt + mg, + 8)
   {
@@ -694,6 +717,10 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
       }
     const float sl = fp16_scale(warp_max(cmax));
     const __half* R = c.kst ? reinterpret_cast<const __half*>(data + a.o_kr) : c.kR;
+    // staged rows of even length: one 32-bit load per pair (rows past the
+    // chunk's n only feed their own scores, which are dropped)
+    const bool fastk = c.kst && (Kk & 1) == 0;
+    const uint32_t* R32 = reinterpret_cast<const uint32_t*>(data + a.o_kr);
     for (int kb = 0; kb < nkb; ++kb) {
       float cv4[4];
 #pragma unroll
@@ -708,10 +735,18 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         const int x0 = 32 * w + 16 * mt + mg, x1 = x0 + 8;
-        const uint32_t a0 = row_pair(R, Kk, n, x0, x0, k0, true);
-        const uint32_t a1 = row_pair(R, Kk, n, x1, x1, k0, true);
-        const uint32_t a2 = row_pair(R, Kk, n, x0, x0, k0 + 8, true);
-        const uint32_t a3 = row_pair(R, Kk, n, x1, x1, k0 + 8, true);
+        uint32_t a0, a1, a2, a3;
+        if (fastk) {
+          a0 = k0 < Kk ? R32[(x0 * Kk + k0) >> 1] : 0u;
+          a1 = k0 < Kk ? R32[(x1 * Kk + k0) >> 1] : 0u;
+          a2 = k0 + 8 < Kk ? R32[(x0 * Kk + k0 + 8) >> 1] : 0u;
+          a3 = k0 + 8 < Kk ? R32[(x1 * Kk + k0 + 8) >> 1] : 0u;
+        } else {
+          a0 = row_pair(R, Kk, n, x0, x0, k0, true);
+          a1 = row_pair(R, Kk, n, x1, x1, k0, true);
+          a2 = row_pair(R, Kk, n, x0, x0, k0 + 8, true);
+          a3 = row_pair(R, Kk, n, x1, x1, k0 + 8, true);
+        }
         mma16816(accl[mt], a0, a1, a2, a3, bh0, bh1);
         mma16816(accl[mt], a0, a1, a2, a3, bl0, bl1);
       }
@@ -748,7 +783,9 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
   const float sp = 16384.f;                       // p <= 1
   const int nmk = (Kv + 15) >> 4;
   const __half* RV = c.vst ? reinterpret_cast<const __half*>(data + a.o_vr) : c.vR;
+  const unsigned short* RV16 = reinterpret_cast<const unsigned short*>(data + a.o_vr);
   const char* vcodes = data + a.o_vc;
+  const int vpitch = c.vcb + 16;   // padded rows: lanes 2 mq apart hit different banks
 #pragma unroll
   for (int kb = 0; kb < 2; ++kb) {
     const int xb = 32 * w + 16 * kb + 2 * mq;
@@ -769,7 +806,7 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
       uint32_t hv[4][8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(vcodes + xs[e] * c.vcb);
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(vcodes + xs[e] * vpitch);
         if (vb == 2) {
           uint32_t wd[1];
           lds_words<1>(row + mg, wd);
@@ -794,14 +831,33 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
         mma16816(zacc[m], a0, a1, a2, a3, bzl0, bzl1);
       }
     }
+    // the rows of tokens past the chunk's n are zero here: they multiply
+    // every query's weights
+    bool xv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) xv[e] = xs[e] < n;
 #pragma unroll
     for (int mk = 0; mk < 8; ++mk) {
       if (mk < nmk) {
         const int k0 = 16 * mk + mg;
-        const uint32_t a0 = row_pair(RV, Kv, n, xs[0], xs[1], k0, false);
-        const uint32_t a1 = row_pair(RV, Kv, n, xs[0], xs[1], k0 + 8, false);
-        const uint32_t a2 = row_pair(RV, Kv, n, xs[2], xs[3], k0, false);
-        const uint32_t a3 = row_pair(RV, Kv, n, xs[2], xs[3], k0 + 8, false);
+        uint32_t a0, a1, a2, a3;
+        if (c.vst) {
+          uint32_t v[4][2];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[e][0] = (xv[e] && k0 < Kv) ? RV16[xs[e] * Kv + k0] : 0u;
+            v[e][1] = (xv[e] && k0 + 8 < Kv) ? RV16[xs[e] * Kv + k0 + 8] : 0u;
+          }
+          a0 = v[0][0] | (v[1][0] << 16);
+          a1 = v[0][1] | (v[1][1] << 16);
+          a2 = v[2][0] | (v[3][0] << 16);
+          a3 = v[2][1] | (v[3][1] << 16);
+        } else {
+          a0 = row_pair(RV, Kv, n, xs[0], xs[1], k0, false);
+          a1 = row_pair(RV, Kv, n, xs[0], xs[1], k0 + 8, false);
+          a2 = row_pair(RV, Kv, n, xs[2], xs[3], k0, false);
+          a3 = row_pair(RV, Kv, n, xs[2], xs[3], k0 + 8, false);
+        }
         mma16816(cacc[mk], a0, a1, a2, a3, bch0, bch1);
         mma16816(cacc[mk], a0, a1, a2, a3, bcl0, bcl1);
       }
@@ -809,8 +865,16 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
   }
   __syncthreads();   // the data region becomes the per-warp partial sums
   float* red = reinterpret_cast<float*>(data);
-  float* rw_ = red + (size_t)w * NQ * (D + KM);
+  float* rw_ = red + (size_t)w * TC_RED_ROWS * NQ;
   const float iz = 1.f / sz, ip = 1.f / sp;
+  // a query pair (2 mq, 2 mq + 1) of one row, as one 8-byte store
+  auto put = [&](int row, float v0, float v1) {
+    if constexpr (NQ == 1) {
+      if (mq == 0) rw_[row] = v0;
+    } else {
+      if (2 * mq < NQ) *reinterpret_cast<float2*>(rw_ + row * NQ + 2 * mq) = make_float2(v0, v1);
+    }
+  };
   // z^T rows of tile m: mg <-> d = 16 mg + lpos(2 m), mg + 8 <-> lpos(2 m + 1)
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
@@ -820,40 +884,44 @@ __global__ void __launch_bounds__(ATT_CHUNK) attend_chunk_tc_kernel(AttArgs a) {
     else { d0 = 2 * m; d1 = 2 * m + 1; }
     d0 += 16 * mg;
     d1 += 16 * mg;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int i = 2 * mq + j;
-      if (i < NQ) {
-        rw_[i * (D + KM) + d0] = zacc[m][j] * iz;
-        rw_[i * (D + KM) + d1] = zacc[m][2 + j] * iz;
-      }
-    }
+    put(tc_red_row(d0), zacc[m][0] * iz, zacc[m][1] * iz);
+    put(tc_red_row(d1), zacc[m][2] * iz, zacc[m][3] * iz);
   }
 #pragma unroll
   for (int mk = 0; mk < 8; ++mk) {
     if (mk < nmk) {
       const int k0 = 16 * mk + mg;
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int i = 2 * mq + j;
-        if (i < NQ) {
-          rw_[i * (D + KM) + D + k0] = cacc[mk][j] * ip;
-          rw_[i * (D + KM) + D + k0 + 8] = cacc[mk][2 + j] * ip;
-        }
-      }
+      put(tc_red_row(D + k0), cacc[mk][0] * ip, cacc[mk][1] * ip);
+      put(tc_red_row(D + k0 + 8), cacc[mk][2] * ip, cacc[mk][3] * ip);
     }
   }
   __syncthreads();
-  chunk_record<D, NQ>(a, c, stat, red, tid);
+  // the chunk's record: max, sum, z, cv, each entry summed over the warps
+  const int nq = a.nq;
+  float* rec = a.part + (((size_t)c.g * a.H + c.h) * a.nch + c.chunk) * rec_floats(nq, D);
+  if (tid < nq) {
+    rec[tid] = stat[tid];
+    rec[nq + tid] = stat[8 + tid];
+  }
+  for (int x = tid; x < (D + Kv) * NQ; x += ATT_CHUNK) {
+    const int col = x / NQ, i = x % NQ;
+    if (i >= nq) continue;
+    const int row = tc_red_row(col);
+    float s = 0.f;
+#pragma unroll
+    for (int ww = 0; ww < ATT_WARPS; ++ww) s += red[(ww * TC_RED_ROWS + row) * NQ + i];
+    rec[2 * nq + (size_t)i * (D + KM) + col] = s;
+  }
 }
 
-// Merge the chunks of one (head, group, query) and map back to feature space.
+// Merge the chunks of one (head, group) for each of its queries and map
+// back to feature space: U_d and G[h] are staged once for all the queries.
 template <int EPT>
 __global__ void __launch_bounds__(128) attend_merge_kernel(AttArgs a) {
-  constexpr int D = 32 * EPT;
-  __shared__ float zf[D], cf[KM], ef[KM > D ? KM : D], red[2][4];
+  constexpr int D = 32 * EPT, QM = JOLT_ATTN_MAX_Q;
+  __shared__ float zf[QM][D], cf[QM][KM], ef[QM][KM > D ? KM : D], sM[QM], sL[QM];
   __shared__ __half st_Ud[D * 64], st_G[64 * (KM > D ? KM : D)];
-  const int h = blockIdx.x, gl = blockIdx.y, i = blockIdx.z, g = a.g0 + gl;
+  const int h = blockIdx.x, gl = blockIdx.y, g = a.g0 + gl;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int T = a.T, H = a.H, nq = a.nq, nch = a.nch;
   const AttUnit vu = a.v[gl];
@@ -867,67 +935,68 @@ __global__ void __launch_bounds__(128) attend_merge_kernel(AttArgs a) {
     stage_halves(st_G, (const __half*)(vb + vu.off_G) + (size_t)h * vu.rT * vu.rd,
                  vu.rT * vu.rd, tid, 128);
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the global max M and sum L of this query
-  float m = -INFINITY;
-  for (int c = tid; c < nch; c += 128) m = fmaxf(m, base[c * rf + i]);
-  m = warp_max(m);
-  if (lane == 0) red[0][w] = m;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-  float l = 0.f;
-  for (int c = tid; c < nch; c += 128) l += expf(base[c * rf + i] - M) * base[c * rf + nq + i];
-  l = warp_sum(l);
-  if (lane == 0) red[1][w] = l;
-  // z and cv: the chunk records weighted by exp(m_c - M), two entries per thread
-  const int ne = D + Kv;
-  const int x0 = tid, x1 = tid + 128;
-  float s0 = 0.f, s1 = 0.f;
-  const size_t col = 2 * nq + (size_t)i * (D + KM);
-#pragma unroll 4
-  for (int c = 0; c < nch; ++c) {
-    const float* r = base + c * rf;
-    const float wc = expf(r[i] - M);
-    if (x0 < ne) s0 = fmaf(wc, r[col + x0], s0);
-    if (x1 < ne) s1 = fmaf(wc, r[col + x1], s1);
+  // the global max M and sum L of each query (a warp per query)
+  for (int i = w; i < nq; i += 4) {
+    float m = -INFINITY;
+    for (int c = lane; c < nch; c += 32) m = fmaxf(m, base[c * rf + i]);
+    m = warp_max(m);
+    float l = 0.f;
+    for (int c = lane; c < nch; c += 32) l += expf(base[c * rf + i] - m) * base[c * rf + nq + i];
+    l = warp_sum(l);
+    if (lane == 0) { sM[i] = m; sL[i] = l; }
   }
-  if (x0 < ne) { if (x0 < D) zf[x0] = s0; else cf[x0 - D] = s0; }
-  if (x1 < ne) { if (x1 < D) zf[x1] = s1; else cf[x1 - D] = s1; }
   __syncthreads();
-  const float L = red[1][0] + red[1][1] + red[1][2] + red[1][3];
+  // z and cv of every query: the chunk records weighted by exp(m_c - M)
+  const int ne = D + Kv;
+  for (int x = tid; x < nq * ne; x += 128) {
+    const int i = x / ne, col = x - i * ne;
+    const float M = sM[i];
+    const size_t at = 2 * nq + (size_t)i * (D + KM) + col;
+    float s = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < nch; ++c) {
+      const float* r = base + c * rf;
+      s = fmaf(expf(r[i] - M), r[at], s);
+    }
+    if (col < D) zf[i][col] = s; else cf[i][col - D] = s;
+  }
+  __syncthreads();
   // back-projection, stage 1: e = G[h]^T cv (r_T < T) or cv itself (r_T = T)
-  for (int j = tid; j < vu.rd; j += 128) {
+  for (int x = tid; x < nq * vu.rd; x += 128) {
+    const int i = x / vu.rd, j = x - i * vu.rd;
     float s;
     if (vfT) {
-      s = cf[j];
+      s = cf[i][j];
     } else {
       s = 0.f;
 #pragma unroll 8
-      for (int k = 0; k < vu.rT; ++k) s = fmaf(__half2float(st_G[k * vu.rd + j]), cf[k], s);
+      for (int k = 0; k < vu.rT; ++k) s = fmaf(__half2float(st_G[k * vu.rd + j]), cf[i][k], s);
     }
-    ef[j] = s;
+    ef[i][j] = s;
   }
   __syncthreads();
-  // stage 2 (U_d e) plus the inverse rotation of z: warp 0 holds the row
-  if (w == 0) {
+  // stage 2 (U_d e) plus the inverse rotation of z: a warp per query
+  const unsigned char* sb = (const unsigned char*)vb + 88;
+  const float rs = rsqrtf((float)D);
+  for (int i = w; i < nq; i += 4) {
     float v[EPT];
     if (vu.b > 0) {
 #pragma unroll
-      for (int e = 0; e < EPT; ++e) v[e] = zf[lane * EPT + e];
+      for (int e = 0; e < EPT; ++e) v[e] = zf[i][lane * EPT + e];
       fwht_row<EPT>(v, lane);
     }
-    const unsigned char* sb = (const unsigned char*)vb + 88;
-    const float rs = rsqrtf((float)D), inv = 1.f / L;
+    const float inv = 1.f / sL[i];
     float* o = a.out + (((size_t)g * H + h) * nq + i) * D;
 #pragma unroll
     for (int e = 0; e < EPT; ++e) {
       const int d = lane * EPT + e;
       float lo;
       if (vfD) {
-        lo = ef[d];
+        lo = ef[i][d];
       } else {
         lo = 0.f;
 #pragma unroll 8
-        for (int j = 0; j < vu.rd; ++j) lo = fmaf(__half2float(st_Ud[d * vu.rd + j]), ef[j], lo);
+        for (int j = 0; j < vu.rd; ++j) lo = fmaf(__half2float(st_Ud[d * vu.rd + j]), ef[i][j], lo);
       }
       const float res = (vu.b > 0) ? sign_of(sb, d) * v[e] * rs : 0.f;
       o[d] = (lo + res) * inv;
@@ -966,7 +1035,7 @@ jolt_status launch_attend(const AttArgs& a, int ng, cudaStream_t st) {
   cfg.dynamicSmemBytes = smem;
   JOLT_CUDA_TRY(cudaLaunchKernelEx(&cfg, chunk, a));
   JOLT_LAUNCH_CHECK();
-  cfg.gridDim = dim3(a.H, ng, a.nq);
+  cfg.gridDim = dim3(a.H, ng);
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = 0;
   JOLT_CUDA_TRY(cudaLaunchKernelEx(&cfg, attend_merge_kernel<EPT>, a));
@@ -1029,14 +1098,16 @@ jolt_status attend_run(int n_groups, const jolt_blob_desc* desc, const char* blo
       a.k[i] = att_unit(kd);
       a.v[i] = att_unit(vd);
       kc = std::max(kc, (size_t)ATT_CHUNK * D * kd.b / 8);
-      vc = std::max(vc, (size_t)ATT_CHUNK * D * vd.b / 8);
+      // D = 128: V code rows at a pitch of 16 bytes more than their length
+      vc = std::max(vc, (size_t)ATT_CHUNK * (D * vd.b / 8 + (D == 128 && vd.b > 0 ? 16 : 0)));
       if (row_len(kd) <= ATT_STAGE_RANK) kr = std::max(kr, (size_t)ATT_CHUNK * row_len(kd) * 2);
       if (row_len(vd) <= ATT_STAGE_RANK) vr = std::max(vr, (size_t)ATT_CHUNK * row_len(vd) * 2);
     }
     a.o_kr = (int)align_up(kc, 16);
     a.o_vc = (int)align_up(a.o_kr + kr, 16);
     a.o_vr = (int)align_up(a.o_vc + vc, 16);
-    const size_t red = sizeof(float) * ATT_WARPS * nq_pad(nq) * (D + KM);
+    const size_t red = sizeof(float) * ATT_WARPS * nq_pad(nq) *
+                       (D == 128 ? (size_t)TC_RED_ROWS : (size_t)(D + KM));
     a.data = (int)align_up(std::max((size_t)a.o_vr + vr, red), 16);
     jolt_status s;
     switch (D) {
