@@ -573,9 +573,11 @@ def test_attend_full_size_random_blobs():
 
 
 @pytest.mark.parametrize("T,D,nq,rT,rd,b", [(1, 64, 2, 1, 8, 4), (129, 32, 8, 5, 4, 2),
-                                            (257, 128, 5, 64, 128, 8), (200, 64, 1, 200, 64, 0)])
+                                            (257, 128, 5, 64, 128, 8), (200, 64, 1, 200, 64, 0),
+                                            (129, 128, 3, 5, 8, 4), (130, 128, 2, 130, 7, 2)])
 def test_attend_edge_shapes(T, D, nq, rT, rd, b):
-    """One token; a last chunk of one token; an odd rank; whole modes."""
+    """One token; a last chunk of one or two tokens; odd ranks (the
+    tensor-core chunk's unpaired row loads at D = 128); whole modes."""
     rng = np.random.default_rng(T + D)
     H = 3
     signs = np.where(rng.random(D) < 0.5, -1, 1).astype(np.int8)
