@@ -49,25 +49,28 @@ __device__ __forceinline__ uint32_t sw128(int r, int byte) {
   return (uint32_t)(r * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15)));
 }
 
-// 16 columns of this thread's TMEM lane, issued without waiting.
-__device__ __forceinline__ void tmem_ld16_issue(uint32_t addr, uint32_t (&r)[16]) {
+// 32 columns of this thread's TMEM lane, issued without waiting.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t addr, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15}, [%16];"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(addr));
 }
-// Wait for this thread's TMEM loads, tied to the registers they fill.
-__device__ __forceinline__ void tmem_ld_wait2(uint32_t (&r)[16], uint32_t (&q)[16]) {
+// Wait for this thread's TMEM loads, tied to the 32 registers of one load.
+__device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                  "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(q[0]), "+r"(q[1]),
-                 "+r"(q[2]), "+r"(q[3]), "+r"(q[4]), "+r"(q[5]), "+r"(q[6]), "+r"(q[7]),
-                 "+r"(q[8]), "+r"(q[9]), "+r"(q[10]), "+r"(q[11]), "+r"(q[12]), "+r"(q[13]),
-                 "+r"(q[14]), "+r"(q[15])
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
 }
@@ -543,63 +546,61 @@ decode_tc_kernel(const __grid_constant__ DecTcArgs a, const __grid_constant__ CU
         asm volatile("bar.sync 2, 256;" ::: "memory");
       }
       const int cb = 64 * hf;
-      uint32_t rr[16], rl[16];
-      if (b > 0) tmem_ld16_issue(tl + cb, rr);
-      if (mode != 3) tmem_ld16_issue(tl + 128 + cb, rl);
+      // 32 columns of both accumulators per TMEM load (two waits a tile)
 #pragma unroll 1
-      for (int c = cb; c < cb + 64; c += 16) {
-        tmem_ld_wait2(rr, rl);
-        float xr[16], xl[16];
+      for (int c0 = cb; c0 < cb + 64; c0 += 32) {
+        uint32_t rr[32], rl[32];
+        if (b > 0) tmem_ld32_issue(tl + c0, rr);
+        if (mode != 3) {
+          tmem_ld32_issue(tl + 128 + c0, rl);
+        } else {
+          // r_T = T, r_d = D: the row of G itself, read while the residual loads
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          xr[i] = __uint_as_float(rr[i]);
-          xl[i] = __uint_as_float(rl[i]);
-        }
-        // the next 16 columns are loaded while these are written
-        if (c + 16 < cb + 64) {
-          if (b > 0) tmem_ld16_issue(tl + c + 16, rr);
-          if (mode != 3) tmem_ld16_issue(tl + 128 + c + 16, rl);
-        }
-        if (mode == 3) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 8) {
-            const uint4 raw = in ? *reinterpret_cast<const uint4*>(Grow + c + i) : make_uint4(0, 0, 0, 0);
+          for (int i = 0; i < 32; i += 8) {
+            const uint4 raw = in ? *reinterpret_cast<const uint4*>(Grow + c0 + i) : make_uint4(0, 0, 0, 0);
             const __half2* hv = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f = __half22float2(hv[e]);
-              xl[i + 2 * e] = f.x;
-              xl[i + 2 * e + 1] = f.y;
+              rl[i + 2 * e] = __float_as_uint(f.x);
+              rl[i + 2 * e + 1] = __float_as_uint(f.y);
             }
           }
         }
-        float x[16];
+        if (b > 0) tmem_ld_wait32(rr);
+        if (mode != 3) tmem_ld_wait32(rl);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          x[i] = b > 0 ? fmaf(sc, xr[i], xl[i]) : xl[i];
-          if (!okw) x[i] = __int_as_float(0x7fc00000);   // a tile whose wait gave up reads NaN
-        }
-        if (f32) {
-          if (in) {
-            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.xhat) + obase + c);
+        for (int c = c0; c < c0 + 32; c += 16) {
+          const int o16 = c - c0;
+          float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) o[i / 4] = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+          for (int i = 0; i < 16; ++i) {
+            const float xl = __uint_as_float(rl[o16 + i]);
+            x[i] = b > 0 ? fmaf(sc, __uint_as_float(rr[o16 + i]), xl) : xl;
+            if (!okw) x[i] = __int_as_float(0x7fc00000);   // a tile whose wait gave up reads NaN
           }
-        } else {
-          uint32_t pk[8];
+          if (f32) {
+            if (in) {
+              float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.xhat) + obase + c);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const __nv_bfloat162 pv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
-            pk[e] = *reinterpret_cast<const uint32_t*>(&pv);
-          }
-          if (staged) {
-            unsigned char* at = stg + (c >> 6) * DT_ATOM;
-            *reinterpret_cast<uint4*>(at + sw128(r, (c & 63) * 2)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4*>(at + sw128(r, (c & 63) * 2 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          } else if (in) {
-            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.xhat) + obase + c);
-            o[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            o[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              for (int i = 0; i < 16; i += 4) o[i / 4] = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+            }
+          } else {
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const __nv_bfloat162 pv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+              pk[e] = *reinterpret_cast<const uint32_t*>(&pv);
+            }
+            if (staged) {
+              unsigned char* at = stg + (c >> 6) * DT_ATOM;
+              *reinterpret_cast<uint4*>(at + sw128(r, (c & 63) * 2)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              *reinterpret_cast<uint4*>(at + sw128(r, (c & 63) * 2 + 16)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            } else if (in) {
+              uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.xhat) + obase + c);
+              o[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              o[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
           }
         }
       }
