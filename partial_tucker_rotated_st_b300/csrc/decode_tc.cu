@@ -392,13 +392,37 @@ decode_tc_kernel(const __grid_constant__ DecTcArgs a, const __grid_constant__ CU
             }
           asm volatile("bar.sync 1, 256;" ::: "memory");
           const float* udr = us + (size_t)d * rd;
-          for (int k = kb; k < kb + KW / 2; k += 4) {
+          // the 4-row groups of column d alternate between the row's two
+          // threads; groups past r_T are zero.  With r_d a multiple of 4 the
+          // rows of G_h and U_d start on 16-byte boundaries: 4 values a load
+          const bool v4 = (rd & 3) == 0;
+          for (int k = 4 * hf; k < KW; k += 8) {
             float v[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int j = 0; j < rd; ++j) {
-              const float uj = udr[j];
+            if (k < rT && v4) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (k + e < rT) v[e] = fmaf(gs[(k + e) * rd + j], uj, v[e]);
+              for (int e = 0; e < 4; ++e) {
+                if (k + e < rT) {
+                  const float* gr = gs + (k + e) * rd;
+                  float acc = 0.f;
+#pragma unroll 1
+                  for (int j = 0; j < rd; j += 4) {
+                    const float4 u4 = *reinterpret_cast<const float4*>(udr + j);
+                    const float4 g4 = *reinterpret_cast<const float4*>(gr + j);
+                    acc = fmaf(g4.x, u4.x, acc);
+                    acc = fmaf(g4.y, u4.y, acc);
+                    acc = fmaf(g4.z, u4.z, acc);
+                    acc = fmaf(g4.w, u4.w, acc);
+                  }
+                  v[e] = acc;
+                }
+              }
+            } else if (k < rT) {
+              for (int j = 0; j < rd; ++j) {
+                const float uj = udr[j];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  if (k + e < rT) v[e] = fmaf(gs[(k + e) * rd + j], uj, v[e]);
+              }
             }
             float hi[4], lo[4];
 #pragma unroll
